@@ -1,0 +1,156 @@
+/*
+ * kvoracle.h -- CPU oracle for the DeepSeek-V4 two-pool (Classical + State)
+ * KV cache decode step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is a plain, slow, single-threaded model of
+ * what the GPU path computes, written from the design pages and used to
+ * check it.  Only the tests, the smoke check and the benchmark's CPU
+ * baseline leg may load it; the product library never links or calls it,
+ * and it shares no code with the CUDA path (the seeded input generator,
+ * which holds none of the method's arithmetic, is the one module both use,
+ * and only in the test harness).
+ *
+ * Sources (page title, section):
+ *   [P1] "Why does V4 split pools? How do block alignment and the tail
+ *        buffer work together": s1.1 pool table, s1.2 CSA m=4 / HCA m'=128,
+ *        s2.2 lcm block alignment and L = 128q + r, s2.3 the L = 130
+ *        example, s3.1 tail lengths, s3.3 tail vs SWA, s4 one decode step.
+ *   [P2] "V4 KV Layout: Classical + State dual pool": Classical KV cache
+ *        table (lcm alignment, immutable, CSA top-k sparse read, HCA dense
+ *        read of ~L/128 entries), State cache table (SWA, tail, indexer).
+ *   [P3] "Ch 12 Inference framework: heterogeneous KV scheduling": glossary
+ *        (State / Block cache, lcm blocks, 32 CSA + 1 HCA per block), s2.1
+ *        State cache per request, s2.2 Block cache with refcounted sharing,
+ *        Figure 12-1 (one block id spans all layers).
+ *   [P4] "V4 disk prefix cache": Zero SWA caching (recompute the window on a
+ *        prefix hit).
+ *
+ * Where the pages are silent the oracle takes these readings:
+ *   - compressor: entry = fp32 chain acc = fmaf(alpha_i, x_i, acc), i = 0..m-1
+ *     from acc = +0, alpha = softmax of seeded per-(layer, head, position)
+ *     gate logits computed in double and rounded to fp32; K and V share alpha;
+ *     the indexer key has its own gates per indexer head;
+ *   - CSA / indexer entries are formed at every completed 4-group and staged
+ *     in the request's State until their 128-token block seals;
+ *   - indexer score = fp32 chain over the flat (head, dim) order of
+ *     fmaf(q_idx, key, acc) from +0, times the entry's scale for fp8;
+ *   - top-k: k = min(top_k, #CSA entries), order (score desc, index asc),
+ *     returned as ascending indices padded with -1;
+ *   - attention: one softmax (scale 1/sqrt(d)) over [selected CSA entries,
+ *     all HCA entries, the SWA window] concatenated with no masking; the
+ *     window includes the token just appended; computed here in double;
+ *   - fp8 e4m3 cache: one bf16 scale per K half, per V half and per indexer
+ *     entry: scale = bf16_rn(amax / 448) (1 when that is 0), code =
+ *     e4m3_rn_satfinite(x / scale);
+ *   - block ids: smallest free id, drawn when a block seals, requests in
+ *     batch order then tokens in order; one id spans every layer;
+ *   - share_prefix shares whole sealed blocks only and takes the caller's
+ *     recomputed window (the Zero SWA policy).
+ */
+#ifndef KVORACLE_H
+#define KVORACLE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { KVO_F32 = 0, KVO_BF16 = 1, KVO_FP8 = 2 };
+enum { KVO_SWA_ONLY = 0, KVO_CSA = 1, KVO_HCA = 2, KVO_CSA_HCA = 3 };
+enum {
+  KVO_OK = 0,
+  KVO_ERR_INVALID_ARG = -1,
+  KVO_ERR_OUT_OF_BLOCKS = -2,
+  KVO_ERR_OUT_OF_REQUESTS = -3,
+  KVO_ERR_BAD_REQUEST = -4,
+  KVO_ERR_NOT_SHAREABLE = -5,
+  KVO_ERR_CAPACITY = -8, /* a request would exceed max_blocks_per_request */
+};
+
+typedef struct kvo_config {
+  int32_t m, m_prime, n_win;
+  int32_t heads, head_dim, idx_heads, idx_dim;
+  int32_t in_dtype, cache_dtype;
+  int32_t n_layers;
+  const int32_t* layer_kinds;
+  int32_t max_requests, max_blocks, max_blocks_per_request;
+  const float* gate_csa; /* logits [n_layers][heads][m]       */
+  const float* gate_hca; /* logits [n_layers][heads][m_prime] */
+  const float* gate_idx; /* logits [n_layers][idx_heads][m]   */
+} kvo_config;
+
+typedef struct kvo kvo_t;
+
+/* ---- scalar codecs (pinned against library casts in the tests) ---- */
+uint16_t kvo_bf16_from_f32(float x);
+float kvo_f32_from_bf16(uint16_t b);
+uint8_t kvo_e4m3_from_f32(float x); /* round to nearest even, saturate to +-448 */
+float kvo_f32_from_e4m3(uint8_t c);
+
+/* softmax of n logits, computed in double, rounded to fp32 */
+void kvo_softmax_f32(const float* logits, int n, float* alpha);
+
+/* Encode n fp32 values into the cache dtype: codes are 4/2/1 bytes per value
+ * (f32 bits, bf16 bits, e4m3); fp8 writes one bf16 scale to *scale. */
+void kvo_encode(int dtype, const float* x, int n, uint8_t* code, uint16_t* scale);
+/* Exact value of element i of an encoded vector (fp8 multiplies its scale). */
+double kvo_decode(int dtype, const uint8_t* code, const uint16_t* scale, int i);
+
+/* ---- the method's steps as pure functions ---- */
+/* entry (K half then V half, [2][heads][head_dim]) from cnt tokens laid out
+ * [cnt][2][heads][head_dim] (fp32 values of the inputs), gates of `layer`,
+ * kind 1 = CSA (cnt = m), 2 = HCA (cnt = m_prime).  code: 2*H*d*vsize bytes,
+ * scale: 2 bf16. */
+int kvo_compress_kv(const kvo_t* o, int layer, int kind, const float* tokens, uint8_t* code, uint16_t* scale);
+/* indexer entry ([idx_heads][idx_dim]) from m tokens' indexer keys */
+int kvo_compress_idx(const kvo_t* o, int layer, const float* keys, uint8_t* code, uint16_t* scale);
+/* indexer score of one encoded indexer entry */
+float kvo_score(const kvo_t* o, const uint8_t* code, const uint16_t* scale, const float* q_idx);
+/* top-k over n scores: writes k = min(top_k, n) ascending indices, then -1 up to top_k */
+int kvo_topk(const float* scores, int64_t n, int top_k, int32_t* out);
+/* attention of q ([heads][head_dim]) over n_src encoded entries laid out
+ * contiguously (codes [n_src][2*H*d*vsize], scales [n_src][2]); out [H][d] */
+int kvo_attend_sources(const kvo_t* o, int64_t n_src, const uint8_t* codes, const uint16_t* scales,
+                       const float* q, double* out);
+
+/* ---- the stateful two-pool cache ---- */
+int kvo_create(const kvo_config* cfg, kvo_t** out);
+void kvo_destroy(kvo_t* o);
+int kvo_alloc_request(kvo_t* o, int32_t* req);
+int kvo_free_request(kvo_t* o, int32_t req);
+/* k, v: [n_layers][T][heads][head_dim]; idx_k: [n_layers][T][idx_heads][idx_dim];
+ * T = sum(n_new); rows in batch order then position order (fp32 values). */
+int kvo_append(kvo_t* o, int n, const int32_t* req_ids, const int32_t* n_new, const float* k, const float* v,
+               const float* idx_k);
+/* win_k, win_v: [n_layers][w][heads][head_dim], w = min(n_tokens, n_win): the
+ * keys/values of positions n_tokens-w .. n_tokens-1 */
+int kvo_share_prefix(kvo_t* o, int32_t dst, int32_t src, int64_t n_tokens, const float* win_k, const float* win_v);
+/* q: [n][heads][head_dim]; q_idx: [n][idx_heads][idx_dim]; out: [n][heads][head_dim];
+ * topk: [n][top_k] or NULL */
+int kvo_decode_attend(kvo_t* o, int layer, int n, const int32_t* req_ids, const float* q, const float* q_idx,
+                      int top_k, double* out, int32_t* topk);
+
+/* ---- inspection ---- */
+typedef struct kvo_info {
+  int64_t length, n_csa, n_hca;
+  int32_t csa_tail, hca_tail, n_blocks, window;
+} kvo_info;
+int kvo_request_info(const kvo_t* o, int32_t req, kvo_info* info, int32_t* block_ids, int32_t cap);
+int kvo_block_refcount(const kvo_t* o, int32_t block_id);
+int kvo_free_block_count(const kvo_t* o);
+/* kind: 1 CSA entry, 2 HCA entry, 3 indexer entry; slot within the block */
+int kvo_block_entry(const kvo_t* o, int layer, int32_t block_id, int kind, int slot, uint8_t* code, uint16_t* scale);
+/* CSA / indexer entry e of a request (sealed or staged) */
+int kvo_request_entry(const kvo_t* o, int layer, int32_t req, int kind, int64_t e, uint8_t* code, uint16_t* scale);
+/* window token at absolute position pos (must be in the window) */
+int kvo_window_token(const kvo_t* o, int layer, int32_t req, int64_t pos, uint8_t* code, uint16_t* scale);
+/* all indexer scores of a request: out[n_csa] */
+int kvo_request_scores(const kvo_t* o, int layer, int32_t req, const float* q_idx, float* out);
+int kvo_value_bytes(int dtype);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVORACLE_H */
