@@ -1,0 +1,414 @@
+// kvpool_append.cu -- fused append / compress / seal kernel and the
+// share-prefix window fill.
+//
+// One CTA handles one (request, block segment, slice of the 2*H*d K/V
+// values, layer) of an append call ("Why does V4 split pools? ..." s4: a new
+// token enters the tail; when a 4-group or a 128-group completes it is
+// compressed into a CSA or HCA entry; the SWA window slides).
+//
+// The compressor is an fp32 chain acc = fma(alpha_i, x_i, acc) over a group's
+// tokens in position order.  Instead of keeping the tail's raw tokens and
+// re-reading them when a group completes, the kernel carries the chain's
+// running value: inside one call in registers, across calls in a per-request
+// fp32 accumulator in the State region.  The chain order is unchanged, so the
+// entry is bit-identical to compressing the stored tail at the end; the tail's
+// raw tokens themselves remain visible to attention through the SWA window
+// (the window is a whole number of blocks, so it always covers the tail).
+#include <cuda_runtime.h>
+
+#include "device_util.cuh"
+#include "kvpool_internal.h"
+
+namespace kvp {
+namespace {
+
+constexpr int kVpt = 8;  // consecutive values per thread
+
+template <int IN>
+struct InTraits;
+template <>
+struct InTraits<KVPOOL_F32> {
+  static constexpr int kBytes = 4;
+  struct Raw {
+    uint4 a, b;
+  };
+  __device__ static Raw load(const uint8_t* p) { return Raw{ld_nc16(p), ld_nc16(p + 16)}; }
+  __device__ static void unpack(const Raw& r, float* x) {
+    x[0] = __uint_as_float(r.a.x); x[1] = __uint_as_float(r.a.y); x[2] = __uint_as_float(r.a.z);
+    x[3] = __uint_as_float(r.a.w); x[4] = __uint_as_float(r.b.x); x[5] = __uint_as_float(r.b.y);
+    x[6] = __uint_as_float(r.b.z); x[7] = __uint_as_float(r.b.w);
+  }
+  __device__ static void load8(const uint8_t* p, float* x) { unpack(load(p), x); }
+};
+template <>
+struct InTraits<KVPOOL_BF16> {
+  static constexpr int kBytes = 2;
+  using Raw = uint4;
+  __device__ static Raw load(const uint8_t* p) { return ld_nc16(p); }
+  __device__ static void unpack(const Raw& a, float* x) {
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+      x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+    }
+  }
+  __device__ static void load8(const uint8_t* p, float* x) { unpack(load(p), x); }
+};
+
+// Store 8 fp32 values (already scaled for fp8) as cache codes at dst.
+template <int CACHE>
+__device__ __forceinline__ void store8(uint8_t* dst, const float* x, float inv_unused);
+
+template <>
+__device__ __forceinline__ void store8<KVPOOL_F32>(uint8_t* dst, const float* x, float) {
+  uint4 a = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]), __float_as_uint(x[3]));
+  uint4 b = make_uint4(__float_as_uint(x[4]), __float_as_uint(x[5]), __float_as_uint(x[6]), __float_as_uint(x[7]));
+  *reinterpret_cast<uint4*>(dst) = a;
+  *reinterpret_cast<uint4*>(dst + 16) = b;
+}
+template <>
+__device__ __forceinline__ void store8<KVPOOL_BF16>(uint8_t* dst, const float* x, float) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = (uint32_t)f32_to_bf16_bits(x[2 * i]) | ((uint32_t)f32_to_bf16_bits(x[2 * i + 1]) << 16);
+  *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+template <>
+__device__ __forceinline__ void store8<KVPOOL_FP8_E4M3>(uint8_t* dst, const float* x, float s) {
+  // code = e4m3_rn_satfinite(x / s), s the bf16 scale widened to fp32
+  uint32_t w[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(x[4 * i], s), __fdiv_rn(x[4 * i + 1], s));
+    const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(x[4 * i + 2], s), __fdiv_rn(x[4 * i + 3], s));
+    w[i] = lo | (hi << 16);
+  }
+  *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+}
+
+__device__ __forceinline__ float amax8(const float* x) {
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kVpt; ++i) a = fmaxf(a, fabsf(x[i]));
+  return a;
+}
+
+// Block-wide maxima of three per-thread values (K half, V half, indexer).
+__device__ __forceinline__ float3 block_max3(float a, float b, float c, float* sh) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+    c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, o));
+  }
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31, nw = blockDim.x >> 5;
+  __syncthreads();
+  if (l == 0) {
+    sh[3 * w] = a;
+    sh[3 * w + 1] = b;
+    sh[3 * w + 2] = c;
+  }
+  __syncthreads();
+  float3 r = make_float3(0.f, 0.f, 0.f);
+  for (int i = 0; i < nw; ++i) {
+    r.x = fmaxf(r.x, sh[3 * i]);
+    r.y = fmaxf(r.y, sh[3 * i + 1]);
+    r.z = fmaxf(r.z, sh[3 * i + 2]);
+  }
+  return r;
+}
+
+// Write one K/V entry (CSA entry, HCA entry or window token) of which this
+// thread holds 8 consecutive fp32 values starting at v0 of [K | V]; all
+// threads of the CTA call it together.  For fp8, K and V get one scale each
+// (amax over the half / 448, rounded to bf16).
+template <int CACHE>
+__device__ __forceinline__ void write_entry(uint8_t* entry, const PoolDesc& pd, int v0, int half, int hv,
+                                            const float* x, float* sh) {
+  if constexpr (CACHE == KVPOOL_FP8_E4M3) {
+    const float a = amax8(x);
+    const float3 r = block_max3(half == 0 ? a : 0.f, half == 1 ? a : 0.f, 0.f, sh);
+    const uint16_t sb = fp8_scale_bits(half == 0 ? r.x : r.y);
+    store8<CACHE>(entry + v0, x, bf16_bits_to_f32(sb));
+    if (hv == 0) *reinterpret_cast<uint16_t*>(entry + 2 * pd.HD + 2 * half) = sb;
+    if (v0 == 0) {
+      uint32_t* pad = reinterpret_cast<uint32_t*>(entry + 2 * pd.HD + 4);
+      pad[0] = 0u;
+      pad[1] = 0u;
+      pad[2] = 0u;
+    }
+  } else {
+    store8<CACHE>(entry + (int64_t)v0 * pd.vs, x, 1.0f);
+  }
+}
+
+// Indexer entry: 8 values at xv0 of the [Ih][Id] key, stored chunk-major.
+template <int CACHE>
+__device__ __forceinline__ void write_idx(uint8_t* sec, const PoolDesc& pd, const LayerDesc& L, int slot, int xv0,
+                                          const float* x, float s) {
+  const int CB = pd.csa_per_block;
+  uint8_t* base = sec + L.idx_off;
+  if constexpr (CACHE == KVPOOL_FP8_E4M3) {
+    const int c = xv0 / 16, within = xv0 % 16;
+    store8<CACHE>(base + ((int64_t)c * CB + slot) * 16 + within, x, s);
+  } else if constexpr (CACHE == KVPOOL_BF16) {
+    const int c = xv0 / 8;
+    store8<CACHE>(base + ((int64_t)c * CB + slot) * 16, x, 1.0f);
+  } else {
+    const int c = xv0 / 4;  // two chunks
+    uint4 a = make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]), __float_as_uint(x[3]));
+    uint4 b = make_uint4(__float_as_uint(x[4]), __float_as_uint(x[5]), __float_as_uint(x[6]), __float_as_uint(x[7]));
+    *reinterpret_cast<uint4*>(base + ((int64_t)c * CB + slot) * 16) = a;
+    *reinterpret_cast<uint4*>(base + ((int64_t)(c + 1) * CB + slot) * 16) = b;
+  }
+}
+
+constexpr int kTokGroup = 8;  // tokens whose loads are issued together
+
+template <int IN, int CACHE>
+__global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ AppendParams P) {
+  __shared__ float sh[3 * 16];
+  const PoolDesc& pd = P.pool;
+  const AppendUnit u = P.units[blockIdx.x];
+  const int slice = blockIdx.y;
+  const int layer = blockIdx.z;
+  const LayerDesc& L = P.layers[layer];
+  const int tid = threadIdx.x;
+  const int HD = pd.HD, XD = pd.XD, m = pd.m, mp = pd.m_prime;
+  constexpr int isz = InTraits<IN>::kBytes;
+
+  if (u.slot < 0 || u.slot >= pd.max_requests || u.seg < 0 || u.seg >= pd.max_bpr + 1 ||
+      u.block_id >= pd.max_blocks || u.t0 < 0 || u.t1 > mp || u.t0 > u.t1) {
+    if (tid == 0) flag_error(pd, kErrBadIndex);
+    return;
+  }
+
+  const int v0 = (slice * blockDim.x + tid) * kVpt;  // my values in [K | V]
+  const int half = v0 >= HD ? 1 : 0;
+  const int hv = v0 - half * HD;
+  const int h = hv / pd.head_dim;
+  const bool idx_thread = L.has_csa && slice == 0 && tid * kVpt < XD;
+  const int xv0 = tid * kVpt;
+  const int g = idx_thread ? xv0 / pd.idx_dim : 0;
+
+  const uint8_t* in_kv = reinterpret_cast<const uint8_t*>(half ? P.v : P.k) +
+                         ((int64_t)layer * P.rows + u.in_row) * HD * isz + (int64_t)hv * isz;
+  const uint8_t* in_x = idx_thread ? reinterpret_cast<const uint8_t*>(P.idx_k) +
+                                         ((int64_t)layer * P.rows + u.in_row) * XD * isz + (int64_t)xv0 * isz
+                                   : nullptr;
+
+  float* acc_base = reinterpret_cast<float*>(pd.arena + L.acc + (int64_t)u.slot * L.acc_req_bytes);
+  float* acc_c_ptr = acc_base + v0;
+  float* acc_x_ptr = acc_base + 2 * HD + xv0;
+  float* acc_h_ptr = acc_base + 2 * HD + XD + v0;
+  const float* a_csa = reinterpret_cast<const float*>(pd.arena + L.alpha_csa) + h * m;
+  const float* a_hca = reinterpret_cast<const float*>(pd.arena + L.alpha_hca) + h * mp;
+  const float* a_idx = reinterpret_cast<const float*>(pd.arena + L.alpha_idx) + g * m;
+
+  float acc_c[kVpt], acc_h[kVpt], acc_x[kVpt];
+#pragma unroll
+  for (int j = 0; j < kVpt; ++j) acc_c[j] = acc_h[j] = acc_x[j] = 0.0f;
+  if (L.has_hca && u.t0 > 0) {
+#pragma unroll
+    for (int j = 0; j < kVpt; ++j) acc_h[j] = acc_h_ptr[j];
+  }
+  if (L.has_csa && (u.t0 % m) != 0) {
+#pragma unroll
+    for (int j = 0; j < kVpt; ++j) acc_c[j] = acc_c_ptr[j];
+    if (idx_thread) {
+#pragma unroll
+      for (int j = 0; j < kVpt; ++j) acc_x[j] = acc_x_ptr[j];
+    }
+  }
+
+  const int32_t dst_block = u.block_id >= 0 ? u.block_id : pd.staging_base + u.slot;
+  uint8_t* blk = pd.arena + L.block_pool + (int64_t)dst_block * L.block_bytes;
+  uint8_t* ring = pd.arena + L.ring + (int64_t)u.slot * L.ring_req_bytes;
+  const int64_t seg_pos0 = (int64_t)u.seg * mp;
+
+  using Raw = typename InTraits<IN>::Raw;
+  for (int tb = u.t0; tb < u.t1; tb += kTokGroup) {
+    const int n = min(kTokGroup, u.t1 - tb);
+    Raw xr[kTokGroup], yr[kTokGroup];
+#pragma unroll
+    for (int gi = 0; gi < kTokGroup; ++gi) {
+      if (gi < n) {
+        xr[gi] = InTraits<IN>::load(in_kv + (int64_t)(tb - u.t0 + gi) * HD * isz);
+        if (idx_thread) yr[gi] = InTraits<IN>::load(in_x + (int64_t)(tb - u.t0 + gi) * XD * isz);
+      }
+    }
+#pragma unroll
+    for (int gi = 0; gi < kTokGroup; ++gi) {
+      if (gi >= n) break;
+      const int t = tb + gi;
+      float x[kVpt];
+      InTraits<IN>::unpack(xr[gi], x);
+      if (L.has_hca) {
+        const float a = a_hca[t];
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) acc_h[j] = __fmaf_rn(a, x[j], acc_h[j]);
+      }
+      if (L.has_csa) {
+        const float a = a_csa[t % m];
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) acc_c[j] = __fmaf_rn(a, x[j], acc_c[j]);
+        if (idx_thread) {
+          float y[kVpt];
+          InTraits<IN>::unpack(yr[gi], y);
+          const float b = a_idx[t % m];
+#pragma unroll
+          for (int j = 0; j < kVpt; ++j) acc_x[j] = __fmaf_rn(b, y[j], acc_x[j]);
+        }
+        if ((t + 1) % m == 0) {  // a CSA group completes: entry slot (t+1)/m - 1 of the block
+          const int slot = (t + 1) / m - 1;
+          write_entry<CACHE>(blk + L.csa_off + (int64_t)slot * pd.entry_bytes, pd, v0, half, hv, acc_c, sh);
+          float s = 1.0f;
+          if constexpr (CACHE == KVPOOL_FP8_E4M3) {
+            const float3 r = block_max3(0.f, 0.f, idx_thread ? amax8(acc_x) : 0.f, sh);
+            const uint16_t sb = fp8_scale_bits(r.z);
+            s = bf16_bits_to_f32(sb);
+            if (idx_thread && xv0 == 0) *reinterpret_cast<uint16_t*>(blk + L.idx_scale_off + 2 * slot) = sb;
+          }
+          if (idx_thread) write_idx<CACHE>(blk, pd, L, slot, xv0, acc_x, s);
+#pragma unroll
+          for (int j = 0; j < kVpt; ++j) acc_c[j] = acc_x[j] = 0.0f;
+        }
+      }
+      if (t >= u.ring_from) {  // the token enters the SWA window
+        const int64_t pos = seg_pos0 + t;
+        write_entry<CACHE>(ring + (pos % pd.n_win) * pd.entry_bytes, pd, v0, half, hv, x, sh);
+      }
+    }
+  }
+
+  if (L.has_hca && u.t1 == mp) {  // the HCA group completes with the block
+    if (u.block_id < 0) {
+      if (tid == 0) flag_error(pd, kErrBadBlock);
+    } else {
+      write_entry<CACHE>(blk + L.hca_off, pd, v0, half, hv, acc_h, sh);
+    }
+  }
+  if (L.has_hca && u.t1 < mp) {
+#pragma unroll
+    for (int j = 0; j < kVpt; ++j) acc_h_ptr[j] = acc_h[j];
+  }
+  if (L.has_csa && (u.t1 % m) != 0) {
+#pragma unroll
+    for (int j = 0; j < kVpt; ++j) acc_c_ptr[j] = acc_c[j];
+    if (idx_thread) {
+#pragma unroll
+      for (int j = 0; j < kVpt; ++j) acc_x_ptr[j] = acc_x[j];
+    }
+  }
+
+  // Seal: CSA / indexer entries staged by earlier calls move into the block.
+  if (u.block_id >= 0 && L.has_csa && u.t0 >= m) {
+    const int n_copy = u.t0 / m;
+    const uint8_t* stg = pd.arena + L.block_pool + (int64_t)(pd.staging_base + u.slot) * L.block_bytes;
+    const int64_t bytes = (int64_t)n_copy * pd.entry_bytes;  // CSA entries, multiple of 16
+    const int64_t per = ((bytes / 16 + P.n_slices - 1) / P.n_slices) * 16;
+    const int64_t b0 = per * slice, b1 = min(bytes, b0 + per);
+    for (int64_t o = b0 + tid * 16; o < b1; o += (int64_t)blockDim.x * 16)
+      *reinterpret_cast<uint4*>(blk + L.csa_off + o) = *reinterpret_cast<const uint4*>(stg + L.csa_off + o);
+    if (slice == 0) {
+      const int CB = pd.csa_per_block;
+      for (int i = tid; i < pd.idx_chunks * n_copy; i += blockDim.x) {
+        const int c = i / n_copy, e = i % n_copy;
+        const int64_t o = L.idx_off + ((int64_t)c * CB + e) * 16;
+        *reinterpret_cast<uint4*>(blk + o) = *reinterpret_cast<const uint4*>(stg + o);
+      }
+      if (CACHE == KVPOOL_FP8_E4M3) {
+        for (int e = tid; e < n_copy; e += blockDim.x)
+          *reinterpret_cast<uint16_t*>(blk + L.idx_scale_off + 2 * e) =
+              *reinterpret_cast<const uint16_t*>(stg + L.idx_scale_off + 2 * e);
+      }
+    }
+  }
+  if (u.block_id >= 0 && slice == 0 && layer == 0 && tid == 0)
+    reinterpret_cast<int32_t*>(pd.arena + pd.table)[(int64_t)u.slot * pd.max_bpr + u.seg] = u.block_id;
+}
+
+// share_prefix: blockIdx.x = window token, blockIdx.y = slice, blockIdx.z = layer;
+// the CTA (0, 0, 0) also copies the shared block ids into dst's table row.
+template <int IN, int CACHE>
+__global__ void __launch_bounds__(512) share_kernel(const __grid_constant__ ShareParams P) {
+  __shared__ float sh[3 * 16];
+  const PoolDesc& pd = P.pool;
+  const int tok = blockIdx.x, slice = blockIdx.y, layer = blockIdx.z;
+  const LayerDesc& L = P.layers[layer];
+  const int HD = pd.HD;
+  constexpr int isz = InTraits<IN>::kBytes;
+  const int v0 = (slice * blockDim.x + threadIdx.x) * kVpt;
+  const int half = v0 >= HD ? 1 : 0;
+  const int hv = v0 - half * HD;
+  if (blockIdx.x == 0 && slice == 0 && layer == 0) {
+    int32_t* table = reinterpret_cast<int32_t*>(pd.arena + pd.table);
+    for (int b = threadIdx.x; b < P.n_blocks; b += blockDim.x)
+      table[(int64_t)P.dst * pd.max_bpr + b] = table[(int64_t)P.src * pd.max_bpr + b];
+  }
+  float x[kVpt];
+  const uint8_t* src = reinterpret_cast<const uint8_t*>(half ? P.win_v : P.win_k) +
+                       ((int64_t)layer * P.w + tok) * HD * isz + (int64_t)hv * isz;
+  InTraits<IN>::load8(src, x);
+  const int64_t pos = P.n_tokens - P.w + tok;
+  uint8_t* ring = pd.arena + L.ring + (int64_t)P.dst * L.ring_req_bytes;
+  write_entry<CACHE>(ring + (pos % pd.n_win) * pd.entry_bytes, pd, v0, half, hv, x, sh);
+}
+
+
+int append_threads(const PoolDesc& pd, int n_slices) { return 2 * pd.HD / kVpt / n_slices; }
+
+}  // namespace
+
+// CTAs that split one unit's 2*H*d values (8 per thread): one CTA up to 256
+// threads; fp8 needs each half (K, V) inside one CTA for its scale.
+int append_slices(const PoolDesc& pd) {
+  const int chunks = 2 * pd.HD / kVpt;
+  if (chunks <= 256) return 1;
+  if (pd.cache_dtype == KVPOOL_FP8_E4M3) return 2;
+  return chunks / 256;
+}
+
+int launch_append(const AppendParams& p, int n_layers, void* stream) {
+  if (p.n_units <= 0) return 0;
+  if (p.n_slices != append_slices(p.pool)) return (int)cudaErrorInvalidValue;
+  const int threads = append_threads(p.pool, p.n_slices);
+  dim3 grid(p.n_units, p.n_slices, n_layers);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int key = p.pool.in_dtype * 3 + p.pool.cache_dtype;
+  switch (key) {
+    case KVPOOL_F32 * 3 + KVPOOL_F32: append_kernel<KVPOOL_F32, KVPOOL_F32><<<grid, threads, 0, s>>>(p); break;
+    case KVPOOL_F32 * 3 + KVPOOL_BF16: append_kernel<KVPOOL_F32, KVPOOL_BF16><<<grid, threads, 0, s>>>(p); break;
+    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3: append_kernel<KVPOOL_F32, KVPOOL_FP8_E4M3><<<grid, threads, 0, s>>>(p); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_F32: append_kernel<KVPOOL_BF16, KVPOOL_F32><<<grid, threads, 0, s>>>(p); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_BF16: append_kernel<KVPOOL_BF16, KVPOOL_BF16><<<grid, threads, 0, s>>>(p); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3:
+      append_kernel<KVPOOL_BF16, KVPOOL_FP8_E4M3><<<grid, threads, 0, s>>>(p);
+      break;
+    default: return (int)cudaErrorInvalidValue;
+  }
+  return (int)cudaGetLastError();
+}
+
+int launch_share(const ShareParams& p, int n_layers, void* stream) {
+  if (p.w <= 0) return 0;
+  const int n_slices = append_slices(p.pool);
+  const int threads = append_threads(p.pool, n_slices);
+  dim3 grid(p.w, n_slices, n_layers);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int key = p.pool.in_dtype * 3 + p.pool.cache_dtype;
+  switch (key) {
+    case KVPOOL_F32 * 3 + KVPOOL_F32: share_kernel<KVPOOL_F32, KVPOOL_F32><<<grid, threads, 0, s>>>(p); break;
+    case KVPOOL_F32 * 3 + KVPOOL_BF16: share_kernel<KVPOOL_F32, KVPOOL_BF16><<<grid, threads, 0, s>>>(p); break;
+    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3: share_kernel<KVPOOL_F32, KVPOOL_FP8_E4M3><<<grid, threads, 0, s>>>(p); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_F32: share_kernel<KVPOOL_BF16, KVPOOL_F32><<<grid, threads, 0, s>>>(p); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_BF16: share_kernel<KVPOOL_BF16, KVPOOL_BF16><<<grid, threads, 0, s>>>(p); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3: share_kernel<KVPOOL_BF16, KVPOOL_FP8_E4M3><<<grid, threads, 0, s>>>(p); break;
+    default: return (int)cudaErrorInvalidValue;
+  }
+  return (int)cudaGetLastError();
+}
+
+}  // namespace kvp

@@ -1,0 +1,718 @@
+// kvpool_host.cpp -- host runtime of the two-pool KV cache: configuration,
+// arena layout, block allocator with refcounts, request lifecycle, and the
+// launch plans of append / share_prefix / decode_attend.
+//
+// Bookkeeping follows "Why does V4 split pools? ..." (s2.2: blocks of
+// lcm(m, m') tokens; s3.1: tails; s4: one decode step) and "Ch 12 Inference
+// framework: heterogeneous KV scheduling" (s2.1: one State block per request,
+// freed whole; s2.2: Block cache shared by refcount).  The host never reads
+// device memory: every launch carries the per-request lengths, block ids and
+// work split it needs in its kernel parameters.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <set>
+#include <string>
+#include <vector>
+
+#include "kvpool.h"
+#include "kvpool_internal.h"
+
+namespace kvp {
+int append_slices(const PoolDesc& pd);
+int attend_stage_entries(const PoolDesc& pd);
+size_t attend_smem_bytes(const PoolDesc& pd);
+int attend_max_split_len();
+}  // namespace kvp
+
+using namespace kvp;
+
+namespace {
+
+constexpr int kMaxSplits = 4096;
+constexpr int kTargetSplits = 4 * 152;  // CTAs of the attention kernel per launch (2 per SM, 2 waves)
+
+int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+int value_bytes(int dtype) { return dtype == KVPOOL_F32 ? 4 : dtype == KVPOOL_BF16 ? 2 : 1; }
+bool kind_has_csa(int k) { return k == KVPOOL_CSA || k == KVPOOL_CSA_HCA; }
+bool kind_has_hca(int k) { return k == KVPOOL_HCA || k == KVPOOL_CSA_HCA; }
+
+struct Layout {
+  PoolDesc pd;
+  LayerDesc layers[kMaxLayers];
+  int64_t hist, keys, counts, sel, part_o, part_ml;
+  int64_t key_stride;
+  int32_t max_key_ctas, sel_stride, n_attend_rows;
+  int64_t total;
+};
+
+// Validate a configuration and compute the arena layout.  Returns "" on
+// success or the reason it is refused.
+std::string plan_layout(const kvpool_config* c, Layout* out) {
+  if (!c) return "config is NULL";
+  if (c->m < 1 || c->m_prime < c->m || c->m_prime % c->m != 0)
+    return "m must divide m_prime (block = lcm(m, m') = m')";
+  if (c->m_prime > 32767) return "m_prime too large";
+  if (c->m_prime / c->m > 32) return "at most 32 CSA entries per block";
+  if (c->n_win < c->m_prime || c->n_win % c->m_prime != 0) return "n_win must be a positive multiple of m_prime";
+  if (c->heads < 1 || (c->head_dim != 64 && c->head_dim != 128)) return "head_dim must be 64 or 128";
+  if (c->idx_heads < 1 || c->idx_dim < 1) return "indexer dims must be positive";
+  if (c->in_dtype != KVPOOL_F32 && c->in_dtype != KVPOOL_BF16) return "in_dtype must be F32 or BF16";
+  if (c->cache_dtype < KVPOOL_F32 || c->cache_dtype > KVPOOL_FP8_E4M3) return "bad cache_dtype";
+  if (c->n_layers < 1 || c->n_layers > kMaxLayers || !c->layer_kinds) return "n_layers must be 1..16";
+  if (c->max_requests < 1 || c->max_blocks < 1 || c->max_blocks_per_request < 1 || c->max_batch < 1 ||
+      c->max_top_k < 0)
+    return "capacities must be positive";
+  const int HD = c->heads * c->head_dim, XD = c->idx_heads * c->idx_dim;
+  if (HD % 256 != 0 || HD > 4096) return "heads * head_dim must be a multiple of 256, at most 4096";
+  if (XD % 16 != 0 || XD > 8 * 256) return "idx_heads * idx_dim must be a multiple of 16, at most 2048";
+  const int vs = value_bytes(c->cache_dtype);
+  bool any_csa = false;
+  for (int l = 0; l < c->n_layers; ++l) {
+    const int k = c->layer_kinds[l];
+    if (k < KVPOOL_SWA_ONLY || k > KVPOOL_CSA_HCA) return "bad layer kind";
+    any_csa |= kind_has_csa(k);
+    if (kind_has_csa(k) && (!c->gate_csa || !c->gate_idx)) return "gate_csa and gate_idx are required";
+    if (kind_has_hca(k) && !c->gate_hca) return "gate_hca is required";
+  }
+  (void)any_csa;
+
+  Layout L{};
+  PoolDesc& pd = L.pd;
+  pd.m = c->m;
+  pd.m_prime = c->m_prime;
+  pd.n_win = c->n_win;
+  pd.heads = c->heads;
+  pd.head_dim = c->head_dim;
+  pd.idx_heads = c->idx_heads;
+  pd.idx_dim = c->idx_dim;
+  pd.HD = HD;
+  pd.XD = XD;
+  pd.in_dtype = c->in_dtype;
+  pd.cache_dtype = c->cache_dtype;
+  pd.vs = vs;
+  pd.isz = value_bytes(c->in_dtype);
+  pd.csa_per_block = c->m_prime / c->m;
+  pd.idx_entry_bytes = (int64_t)XD * vs;
+  pd.idx_chunks = (int32_t)(pd.idx_entry_bytes / 16);
+  pd.entry_bytes = 2LL * HD * vs + (c->cache_dtype == KVPOOL_FP8_E4M3 ? 16 : 0);
+  pd.max_blocks = c->max_blocks;
+  pd.max_requests = c->max_requests;
+  pd.max_bpr = c->max_blocks_per_request;
+  pd.staging_base = c->max_blocks;
+
+  int64_t cur = 0;
+  pd.err = cur;
+  cur += 256;
+  pd.table = cur;
+  cur = round_up(cur + 4LL * c->max_requests * c->max_blocks_per_request, 256);
+  const int CB = pd.csa_per_block;
+  for (int l = 0; l < c->n_layers; ++l) {
+    LayerDesc& d = L.layers[l];
+    d.kind = c->layer_kinds[l];
+    d.has_csa = kind_has_csa(d.kind);
+    d.has_hca = kind_has_hca(d.kind);
+    d.alpha_csa = cur;
+    cur = round_up(cur + 4LL * c->heads * c->m, 256);
+    d.alpha_hca = cur;
+    cur = round_up(cur + 4LL * c->heads * c->m_prime, 256);
+    d.alpha_idx = cur;
+    cur = round_up(cur + 4LL * c->idx_heads * c->m, 256);
+    int64_t off = 0;
+    d.csa_off = d.idx_off = d.idx_scale_off = d.hca_off = -1;
+    if (d.has_csa) {
+      d.csa_off = off;
+      off += CB * pd.entry_bytes;
+      d.idx_off = off;
+      off += CB * pd.idx_entry_bytes;
+      if (c->cache_dtype == KVPOOL_FP8_E4M3) {
+        d.idx_scale_off = off;
+        off += round_up(2LL * CB, 16);
+      }
+    }
+    if (d.has_hca) {
+      d.hca_off = off;
+      off += pd.entry_bytes;
+    }
+    d.block_bytes = round_up(off, 256);
+    d.block_pool = cur;
+    cur = round_up(cur + d.block_bytes * ((int64_t)c->max_blocks + c->max_requests), 256);
+    d.ring_req_bytes = round_up((int64_t)c->n_win * pd.entry_bytes, 256);
+    d.ring = cur;
+    cur += d.ring_req_bytes * c->max_requests;
+    d.acc_req_bytes = (d.has_csa || d.has_hca) ? round_up(4LL * (4LL * HD + XD), 256) : 0;
+    d.acc = cur;
+    cur += d.acc_req_bytes * c->max_requests;
+  }
+  // decode-attention scratch
+  L.n_attend_rows = std::min(c->max_batch, kMaxAttendReqs);
+  L.key_stride = (int64_t)(c->max_blocks_per_request + 1) * CB;
+  L.max_key_ctas = (int32_t)((L.key_stride + kSelectKeysPerCta - 1) / kSelectKeysPerCta);
+  L.sel_stride = std::max(1, c->max_top_k);
+  L.hist = cur;
+  cur = round_up(cur + 4LL * L.n_attend_rows * 3 * kHistBins, 256);
+  L.keys = cur;
+  cur = round_up(cur + 4LL * L.n_attend_rows * L.key_stride, 256);
+  L.counts = cur;
+  cur = round_up(cur + 8LL * L.n_attend_rows * L.max_key_ctas, 256);
+  L.sel = cur;
+  cur = round_up(cur + 4LL * L.n_attend_rows * L.sel_stride, 256);
+  L.part_o = cur;
+  cur = round_up(cur + 4LL * kMaxSplits * HD, 256);
+  L.part_ml = cur;
+  cur = round_up(cur + 8LL * kMaxSplits * c->heads, 256);
+  L.total = cur;
+  *out = L;
+  return "";
+}
+
+// alpha = softmax(logits) over n positions, in double, rounded to fp32
+void softmax_rows(const float* g, int rows, int n, std::vector<float>* out) {
+  out->resize((size_t)rows * n);
+  std::vector<double> e(n);
+  for (int r = 0; r < rows; ++r) {
+    const float* x = g + (size_t)r * n;
+    double mx = x[0];
+    for (int i = 1; i < n; ++i) mx = x[i] > mx ? x[i] : mx;
+    double sum = 0.0;
+    for (int i = 0; i < n; ++i) {
+      e[i] = std::exp((double)x[i] - mx);
+      sum += e[i];
+    }
+    for (int i = 0; i < n; ++i) (*out)[(size_t)r * n + i] = (float)(e[i] / sum);
+  }
+}
+
+struct Request {
+  bool active = false;
+  int64_t length = 0;
+  std::vector<int32_t> table;
+};
+
+struct ProfileSlot {
+  cudaEvent_t a, b;
+  int kernel;
+  int64_t bytes;
+};
+
+}  // namespace
+
+struct kvpool {
+  kvpool_config cfg{};
+  std::vector<int32_t> kinds;
+  uint32_t flags = 0;
+  Layout lay{};
+  uint8_t* arena = nullptr;
+  std::vector<int32_t> refcount;
+  std::set<int32_t> free_blocks;
+  std::set<int32_t> free_slots;
+  std::vector<Request> reqs;
+  std::string err;
+  // profiling
+  bool profiling = false;
+  std::vector<ProfileSlot> prof;
+  std::vector<cudaEvent_t> event_pool;
+  double prof_ms[KVPOOL_KERNEL_COUNT] = {};
+  int64_t prof_launches[KVPOOL_KERNEL_COUNT] = {};
+  int64_t prof_bytes[KVPOOL_KERNEL_COUNT] = {};
+
+  bool device() const { return !(flags & KVPOOL_FLAG_NO_DEVICE); }
+  int fail(int code, const std::string& msg) {
+    err = msg;
+    return code;
+  }
+  int cuda_fail(cudaError_t e, const char* where) {
+    err = std::string(where) + ": " + cudaGetErrorString(e);
+    return KVPOOL_ERR_CUDA;
+  }
+  bool req_ok(int32_t r) const { return r >= 0 && r < cfg.max_requests && reqs[r].active; }
+
+  // ---- profiling helpers ----
+  cudaEvent_t take_event() {
+    if (!event_pool.empty()) {
+      cudaEvent_t e = event_pool.back();
+      event_pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e;
+    cudaEventCreate(&e);
+    return e;
+  }
+  template <class F>
+  int launch(int kernel, int64_t bytes, void* stream, F&& f) {
+    ProfileSlot s{};
+    if (profiling) {
+      s.a = take_event();
+      s.b = take_event();
+      s.kernel = kernel;
+      s.bytes = bytes;
+      cudaEventRecord(s.a, (cudaStream_t)stream);
+    }
+    const int rc = f();
+    if (profiling) {
+      cudaEventRecord(s.b, (cudaStream_t)stream);
+      prof.push_back(s);
+    }
+    return rc;
+  }
+  void settle_profile() {
+    for (auto& s : prof) {
+      cudaEventSynchronize(s.b);
+      float ms = 0.f;
+      cudaEventElapsedTime(&ms, s.a, s.b);
+      prof_ms[s.kernel] += ms;
+      prof_launches[s.kernel] += 1;
+      prof_bytes[s.kernel] += s.bytes;
+      event_pool.push_back(s.a);
+      event_pool.push_back(s.b);
+    }
+    prof.clear();
+  }
+};
+
+extern "C" {
+
+size_t kvpool_required_bytes(const kvpool_config* cfg) {
+  Layout L;
+  if (!plan_layout(cfg, &L).empty()) return 0;
+  return (size_t)L.total;
+}
+
+int kvpool_create(const kvpool_config* cfg, void* d_arena, size_t arena_bytes, void* stream, kvpool_t** out) {
+  if (!out) return KVPOOL_ERR_INVALID_ARG;
+  *out = nullptr;
+  Layout L;
+  if (!plan_layout(cfg, &L).empty()) return KVPOOL_ERR_INVALID_ARG;
+  const bool no_dev = (cfg->flags & KVPOOL_FLAG_NO_DEVICE) != 0;
+  if (no_dev ? d_arena != nullptr : (!d_arena || arena_bytes < (size_t)L.total)) return KVPOOL_ERR_INVALID_ARG;
+  if (!no_dev && (reinterpret_cast<uintptr_t>(d_arena) % 256) != 0) return KVPOOL_ERR_INVALID_ARG;
+
+  kvpool* p = new (std::nothrow) kvpool();
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  p->cfg = *cfg;
+  p->kinds.assign(cfg->layer_kinds, cfg->layer_kinds + cfg->n_layers);
+  p->cfg.layer_kinds = p->kinds.data();
+  p->cfg.gate_csa = p->cfg.gate_hca = p->cfg.gate_idx = nullptr;
+  p->flags = cfg->flags;
+  p->lay = L;
+  p->arena = static_cast<uint8_t*>(d_arena);
+  p->lay.pd.arena = p->arena;
+  p->refcount.assign(cfg->max_blocks, 0);
+  for (int32_t b = 0; b < cfg->max_blocks; ++b) p->free_blocks.insert(p->free_blocks.end(), b);
+  for (int32_t r = 0; r < cfg->max_requests; ++r) p->free_slots.insert(p->free_slots.end(), r);
+  p->reqs.resize(cfg->max_requests);
+
+  if (!no_dev) {
+    cudaStream_t s = (cudaStream_t)stream;
+    // gates: softmax on the host, one upload per layer and kind
+    std::vector<float> a;
+    for (int l = 0; l < cfg->n_layers; ++l) {
+      const LayerDesc& d = L.layers[l];
+      if (d.has_csa) {
+        softmax_rows(cfg->gate_csa + (size_t)l * cfg->heads * cfg->m, cfg->heads, cfg->m, &a);
+        cudaError_t e = cudaMemcpy(p->arena + d.alpha_csa, a.data(), a.size() * 4, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) { int rc = p->cuda_fail(e, "gate upload"); delete p; return rc; }
+        softmax_rows(cfg->gate_idx + (size_t)l * cfg->idx_heads * cfg->m, cfg->idx_heads, cfg->m, &a);
+        e = cudaMemcpy(p->arena + d.alpha_idx, a.data(), a.size() * 4, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) { int rc = p->cuda_fail(e, "gate upload"); delete p; return rc; }
+      }
+      if (d.has_hca) {
+        softmax_rows(cfg->gate_hca + (size_t)l * cfg->heads * cfg->m_prime, cfg->heads, cfg->m_prime, &a);
+        cudaError_t e = cudaMemcpy(p->arena + d.alpha_hca, a.data(), a.size() * 4, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) { int rc = p->cuda_fail(e, "gate upload"); delete p; return rc; }
+      }
+    }
+    // error word and select histograms start at zero
+    cudaError_t e = cudaMemsetAsync(p->arena + L.pd.err, 0, 256, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->arena + L.hist, 0, (size_t)(L.keys - L.hist), s);
+    if (e != cudaSuccess) { int rc = p->cuda_fail(e, "arena init"); delete p; return rc; }
+  }
+  *out = p;
+  return KVPOOL_OK;
+}
+
+int kvpool_destroy(kvpool_t* p) {
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  for (auto& s : p->prof) {
+    cudaEventDestroy(s.a);
+    cudaEventDestroy(s.b);
+  }
+  for (auto e : p->event_pool) cudaEventDestroy(e);
+  delete p;
+  return KVPOOL_OK;
+}
+
+int kvpool_alloc_request(kvpool_t* p, int32_t* req_out) {
+  if (!p || !req_out) return KVPOOL_ERR_INVALID_ARG;
+  if (p->free_slots.empty()) return p->fail(KVPOOL_ERR_OUT_OF_REQUESTS, "no free request slot");
+  const int32_t r = *p->free_slots.begin();
+  p->free_slots.erase(p->free_slots.begin());
+  Request& q = p->reqs[r];
+  q.active = true;
+  q.length = 0;
+  q.table.clear();
+  *req_out = r;
+  return KVPOOL_OK;
+}
+
+static void release_block(kvpool_t* p, int32_t b) {
+  if (--p->refcount[b] == 0) p->free_blocks.insert(b);
+}
+
+int kvpool_free_request(kvpool_t* p, int32_t r) {
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  if (!p->req_ok(r)) return p->fail(KVPOOL_ERR_BAD_REQUEST, "free_request: bad request id");
+  Request& q = p->reqs[r];
+  for (int32_t b : q.table) release_block(p, b);
+  q.table.clear();
+  q.active = false;
+  q.length = 0;
+  p->free_slots.insert(r);
+  return KVPOOL_OK;
+}
+
+int kvpool_share_prefix(kvpool_t* p, int32_t dst, int32_t src, int64_t n_tokens, const void* d_win_k,
+                        const void* d_win_v, void* stream) {
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  if (!p->req_ok(dst) || !p->req_ok(src) || dst == src) return p->fail(KVPOOL_ERR_BAD_REQUEST, "share_prefix: bad ids");
+  if (n_tokens <= 0) return p->fail(KVPOOL_ERR_INVALID_ARG, "share_prefix: n_tokens <= 0");
+  const int mp = p->cfg.m_prime;
+  Request& s = p->reqs[src];
+  Request& d = p->reqs[dst];
+  if (n_tokens % mp != 0 || n_tokens / mp > (int64_t)s.table.size())
+    return p->fail(KVPOOL_ERR_NOT_SHAREABLE, "share_prefix: prefix is not whole sealed blocks of src");
+  if (d.length != 0) return p->fail(KVPOOL_ERR_NOT_SHAREABLE, "share_prefix: dst is not fresh");
+  if (!d_win_k || !d_win_v) {
+    if (p->device()) return p->fail(KVPOOL_ERR_INVALID_ARG, "share_prefix: NULL window");
+  }
+  const int nb = (int)(n_tokens / mp);
+  const int w = (int)std::min<int64_t>(n_tokens, p->cfg.n_win);
+  if (p->device()) {
+    if ((reinterpret_cast<uintptr_t>(d_win_k) | reinterpret_cast<uintptr_t>(d_win_v)) % 16 != 0)
+      return p->fail(KVPOOL_ERR_INVALID_ARG, "share_prefix: window not 16-byte aligned");
+    ShareParams sp{};
+    sp.pool = p->lay.pd;
+    std::memcpy(sp.layers, p->lay.layers, sizeof(sp.layers));
+    sp.win_k = d_win_k;
+    sp.win_v = d_win_v;
+    sp.dst = dst;
+    sp.src = src;
+    sp.n_blocks = nb;
+    sp.w = w;
+    sp.n_tokens = n_tokens;
+    const int rc = p->launch(KVPOOL_KERNEL_APPEND, 0, stream, [&] { return launch_share(sp, p->cfg.n_layers, stream); });
+    if (rc != 0) return p->cuda_fail((cudaError_t)rc, "share_prefix launch");
+  }
+  d.table.assign(s.table.begin(), s.table.begin() + nb);
+  for (int32_t b : d.table) p->refcount[b] += 1;
+  d.length = n_tokens;
+  return KVPOOL_OK;
+}
+
+int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_t* h_n_new, const void* d_k,
+                  const void* d_v, const void* d_idx_k, void* stream) {
+  if (!p || n < 0 || (n > 0 && (!h_req_ids || !h_n_new))) return KVPOOL_ERR_INVALID_ARG;
+  if (n > p->cfg.max_batch) return p->fail(KVPOOL_ERR_INVALID_ARG, "append: n > max_batch");
+  const int mp = p->cfg.m_prime, W = p->cfg.n_win;
+  int64_t T = 0, seals = 0;
+  for (int i = 0; i < n; ++i) {
+    if (!p->req_ok(h_req_ids[i])) return p->fail(KVPOOL_ERR_BAD_REQUEST, "append: bad request id");
+    if (h_n_new[i] < 0) return p->fail(KVPOOL_ERR_INVALID_ARG, "append: negative count");
+    for (int j = 0; j < i; ++j)
+      if (h_req_ids[j] == h_req_ids[i]) return p->fail(KVPOOL_ERR_INVALID_ARG, "append: duplicate request id");
+    const int64_t L0 = p->reqs[h_req_ids[i]].length, L1 = L0 + h_n_new[i];
+    if (L1 / mp > p->cfg.max_blocks_per_request) return p->fail(KVPOOL_ERR_CAPACITY, "append: request too long");
+    T += h_n_new[i];
+    seals += L1 / mp - L0 / mp;
+  }
+  bool any_csa = false;
+  for (int k : p->kinds) any_csa |= kind_has_csa(k);
+  if (T > 0 && p->device() && (!d_k || !d_v || (any_csa && !d_idx_k)))
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "append: NULL input");
+  if (T > INT32_MAX / 2) return p->fail(KVPOOL_ERR_INVALID_ARG, "append: too many tokens in one call");
+  if (p->device() && ((reinterpret_cast<uintptr_t>(d_k) | reinterpret_cast<uintptr_t>(d_v) |
+                       reinterpret_cast<uintptr_t>(d_idx_k)) % 16) != 0)
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "append: inputs must be 16-byte aligned");
+  if (seals > (int64_t)p->free_blocks.size()) return p->fail(KVPOOL_ERR_OUT_OF_BLOCKS, "append: out of blocks");
+
+  // reserve block ids: smallest free, requests in batch order, then positions
+  std::vector<std::vector<int32_t>> new_ids(n);
+  for (int i = 0; i < n; ++i) {
+    const int64_t L0 = p->reqs[h_req_ids[i]].length, L1 = L0 + h_n_new[i];
+    for (int64_t s = L0 / mp; s < L1 / mp; ++s) {
+      const int32_t id = *p->free_blocks.begin();
+      p->free_blocks.erase(p->free_blocks.begin());
+      new_ids[i].push_back(id);
+    }
+  }
+
+  int rc = 0;
+  if (p->device() && T > 0) {
+    // build the units: one per (request, block segment touched)
+    std::vector<AppendUnit> phase1, phase2;
+    int64_t row = 0;
+    for (int i = 0; i < n; ++i) {
+      const int32_t slot = h_req_ids[i];
+      const int64_t L0 = p->reqs[slot].length, L1 = L0 + h_n_new[i];
+      if (L1 == L0) continue;
+      const int64_t s_first = L0 / mp, s_last = (L1 - 1) / mp;
+      const int64_t ring_from_abs = std::max(L0, L1 - W);
+      const bool split = s_last > s_first && (L0 % mp) != 0 && (L1 % mp) != 0;
+      for (int64_t s = s_first; s <= s_last; ++s) {
+        AppendUnit u{};
+        u.slot = slot;
+        u.seg = (int32_t)s;
+        const int64_t a = std::max(L0, s * mp), b = std::min(L1, (s + 1) * mp);
+        u.t0 = (int16_t)(a - s * mp);
+        u.t1 = (int16_t)(b - s * mp);
+        u.ring_from = (int16_t)(std::min<int64_t>(std::max(ring_from_abs, a), b) - s * mp);
+        u.in_row = (int32_t)(row + (a - L0));
+        u.block_id = (s < L1 / mp) ? new_ids[i][(size_t)(s - L0 / mp)] : -1;
+        (split && s == s_first ? phase1 : phase2).push_back(u);
+      }
+      row += h_n_new[i];
+    }
+    AppendParams* ap = new AppendParams();
+    ap->pool = p->lay.pd;
+    std::memcpy(ap->layers, p->lay.layers, sizeof(ap->layers));
+    ap->k = d_k;
+    ap->v = d_v;
+    ap->idx_k = d_idx_k;
+    ap->rows = T;
+    ap->n_slices = append_slices(p->lay.pd);
+    // algorithmic bytes: inputs read + window / entries written
+    const int64_t in_row_bytes = (2LL * p->lay.pd.HD + (any_csa ? p->lay.pd.XD : 0)) * p->lay.pd.isz;
+    int64_t bytes = T * in_row_bytes * p->cfg.n_layers;
+    for (auto* list : {&phase1, &phase2}) {
+      for (size_t o = 0; o < list->size() && rc == 0; o += kMaxAppendUnits) {
+        ap->n_units = (int32_t)std::min<size_t>(kMaxAppendUnits, list->size() - o);
+        std::memcpy(ap->units, list->data() + o, sizeof(AppendUnit) * ap->n_units);
+        rc = p->launch(KVPOOL_KERNEL_APPEND, bytes, stream, [&] { return launch_append(*ap, p->cfg.n_layers, stream); });
+        bytes = 0;
+      }
+    }
+    delete ap;
+  }
+  if (rc != 0) {  // undo the reservation: nothing changes on error
+    for (auto& v : new_ids)
+      for (int32_t id : v) p->free_blocks.insert(id);
+    return p->cuda_fail((cudaError_t)rc, "append launch");
+  }
+  for (int i = 0; i < n; ++i) {
+    Request& q = p->reqs[h_req_ids[i]];
+    for (int32_t id : new_ids[i]) {
+      p->refcount[id] = 1;
+      q.table.push_back(id);
+    }
+    q.length += h_n_new[i];
+  }
+  return KVPOOL_OK;
+}
+
+int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h_req_ids, const void* d_q,
+                         const void* d_q_idx, int32_t top_k, float* d_out, int32_t* d_topk_out, void* stream) {
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= p->cfg.n_layers || n < 0 || top_k < 0)
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "decode_attend: bad layer, n or top_k");
+  if (n > p->cfg.max_batch) return p->fail(KVPOOL_ERR_INVALID_ARG, "decode_attend: n > max_batch");
+  if (top_k > p->cfg.max_top_k) return p->fail(KVPOOL_ERR_INVALID_ARG, "decode_attend: top_k > max_top_k");
+  const LayerDesc& Ld = p->lay.layers[layer];
+  if (n > 0 && (!h_req_ids || !d_q || !d_out || (Ld.has_csa && !d_q_idx)))
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "decode_attend: NULL pointer");
+  for (int i = 0; i < n; ++i) {
+    if (!p->req_ok(h_req_ids[i])) return p->fail(KVPOOL_ERR_BAD_REQUEST, "decode_attend: bad request id");
+    if (p->reqs[h_req_ids[i]].length == 0) return p->fail(KVPOOL_ERR_INVALID_ARG, "decode_attend: empty request");
+  }
+  if (!p->device()) return p->fail(KVPOOL_ERR_INVALID_ARG, "decode_attend: pool has no device");
+  if (n == 0) return KVPOOL_OK;
+  if (reinterpret_cast<uintptr_t>(d_q) % 16 != 0) return p->fail(KVPOOL_ERR_INVALID_ARG, "decode_attend: q not 16-byte aligned");
+
+  const PoolDesc& pd = p->lay.pd;
+  const int CB = pd.csa_per_block;
+  const int max_split_len = attend_max_split_len();
+  AttendParams* ap = new AttendParams();
+  int rc = 0;
+  for (int g0 = 0; g0 < n && rc == 0; g0 += kMaxAttendReqs) {
+    const int gn = std::min(kMaxAttendReqs, n - g0);
+    AttendParams& P = *ap;
+    P.pool = pd;
+    P.layer = Ld;
+    P.q = d_q;
+    P.q_idx = d_q_idx;
+    P.out = d_out;
+    P.topk_out = d_topk_out;
+    P.top_k = top_k;
+    P.n = gn;
+    P.row0 = g0;
+    P.keys = reinterpret_cast<uint32_t*>(p->arena + p->lay.keys);
+    P.key_stride = p->lay.key_stride;
+    P.hist = reinterpret_cast<uint32_t*>(p->arena + p->lay.hist);
+    P.counts = reinterpret_cast<uint32_t*>(p->arena + p->lay.counts);
+    P.max_key_ctas = p->lay.max_key_ctas;
+    P.sel = reinterpret_cast<int32_t*>(p->arena + p->lay.sel);
+    P.sel_stride = p->lay.sel_stride;
+    P.part_o = reinterpret_cast<float*>(p->arena + p->lay.part_o);
+    P.part_ml = reinterpret_cast<float*>(p->arena + p->lay.part_ml);
+    int64_t total_src = 0;
+    int score_ctas = 0, key_ctas = 0;
+    int64_t score_bytes = 0, attend_bytes = 0, out_bytes = 0;
+    for (int i = 0; i < gn; ++i) {
+      const Request& q = p->reqs[h_req_ids[g0 + i]];
+      AttendReq& R = P.reqs[i];
+      R = AttendReq{};
+      R.slot = h_req_ids[g0 + i];
+      R.length = q.length;
+      R.n_sealed = (int32_t)q.table.size();
+      R.n_cand = Ld.has_csa ? (int32_t)(q.length / p->cfg.m) : 0;
+      R.k = std::min(top_k, R.n_cand);
+      R.select_all = (R.k == R.n_cand) ? 1 : 0;
+      R.n_hca = Ld.has_hca ? (int32_t)(q.length / p->cfg.m_prime) : 0;
+      R.w = (int32_t)std::min<int64_t>(q.length, p->cfg.n_win);
+      R.score_base = score_ctas;
+      const int nseg = (R.n_cand + CB - 1) / CB;
+      if (!R.select_all && R.k > 0) {
+        score_ctas += (nseg + kScoreSegsPerCta - 1) / kScoreSegsPerCta;
+        score_bytes += (int64_t)R.n_cand * (pd.idx_entry_bytes + (pd.cache_dtype == KVPOOL_FP8_E4M3 ? 2 : 0));
+      }
+      R.key_base = key_ctas;
+      if (Ld.has_csa) key_ctas += std::max(1, (int)((R.n_cand + kSelectKeysPerCta - 1) / kSelectKeysPerCta));
+      total_src += (int64_t)R.k + R.n_hca + R.w;
+      attend_bytes += ((int64_t)R.k + R.n_hca + R.w) * pd.entry_bytes + (int64_t)R.n_hca * 4;
+    }
+    out_bytes = (int64_t)gn * pd.HD * 4;
+    int64_t split_len = std::max<int64_t>(16, (total_src + kTargetSplits - 1) / kTargetSplits);
+    split_len = std::min<int64_t>(split_len, max_split_len);
+    int splits = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+      splits = 0;
+      for (int i = 0; i < gn; ++i) {
+        AttendReq& R = P.reqs[i];
+        const int64_t ns = (int64_t)R.k + R.n_hca + R.w;
+        R.split_len = (int32_t)split_len;
+        R.n_split = (int32_t)((ns + split_len - 1) / split_len);
+        R.split_base = splits;
+        splits += R.n_split;
+      }
+      if (splits <= kMaxSplits) break;
+      split_len = max_split_len;
+    }
+    if (splits > kMaxSplits) {
+      rc = -1;
+      p->fail(KVPOOL_ERR_INVALID_ARG, "decode_attend: too many attention splits");
+      break;
+    }
+    P.total_score_ctas = score_ctas;
+    P.total_key_ctas = key_ctas;
+    P.total_splits = splits;
+    if (Ld.has_csa) {
+      rc = p->launch(KVPOOL_KERNEL_SCORE, score_bytes, stream, [&] { return launch_score(P, stream); });
+      if (rc == 0) rc = p->launch(KVPOOL_KERNEL_SELECT, 0, stream, [&] { return launch_select(P, stream); });
+    }
+    if (rc == 0) rc = p->launch(KVPOOL_KERNEL_ATTEND, attend_bytes, stream, [&] { return launch_attend(P, stream); });
+    if (rc == 0) rc = p->launch(KVPOOL_KERNEL_COMBINE, out_bytes, stream, [&] { return launch_combine(P, stream); });
+  }
+  delete ap;
+  if (rc == -1) return KVPOOL_ERR_INVALID_ARG;
+  if (rc != 0) return p->cuda_fail((cudaError_t)rc, "decode_attend launch");
+  return KVPOOL_OK;
+}
+
+int kvpool_request_info(const kvpool_t* p, int32_t r, kvpool_info* info, int32_t* ids, int32_t cap) {
+  if (!p || !info) return KVPOOL_ERR_INVALID_ARG;
+  if (!p->req_ok(r)) return KVPOOL_ERR_BAD_REQUEST;
+  const Request& q = p->reqs[r];
+  info->length = q.length;
+  info->n_csa = q.length / p->cfg.m;
+  info->n_hca = q.length / p->cfg.m_prime;
+  info->csa_tail = (int32_t)(q.length % p->cfg.m);
+  info->hca_tail = (int32_t)(q.length % p->cfg.m_prime);
+  info->n_blocks = (int32_t)q.table.size();
+  info->window = (int32_t)std::min<int64_t>(q.length, p->cfg.n_win);
+  if (ids)
+    for (int32_t s = 0; s < (int32_t)q.table.size() && s < cap; ++s) ids[s] = q.table[s];
+  return KVPOOL_OK;
+}
+
+int kvpool_block_refcount(const kvpool_t* p, int32_t b) {
+  if (!p || b < 0 || b >= p->cfg.max_blocks) return KVPOOL_ERR_INVALID_ARG;
+  return p->refcount[b];
+}
+
+int kvpool_free_block_count(const kvpool_t* p) { return p ? (int)p->free_blocks.size() : KVPOOL_ERR_INVALID_ARG; }
+
+int kvpool_get_layout(const kvpool_t* p, kvpool_layout* out, int32_t layer, kvpool_layer_layout* lo) {
+  if (!p || !out) return KVPOOL_ERR_INVALID_ARG;
+  const Layout& L = p->lay;
+  out->entry_bytes = L.pd.entry_bytes;
+  out->idx_entry_bytes = L.pd.idx_entry_bytes;
+  out->csa_per_block = L.pd.csa_per_block;
+  out->staging_base = L.pd.staging_base;
+  out->table_offset = L.pd.table;
+  out->error_offset = L.pd.err;
+  out->total_bytes = L.total;
+  if (lo) {
+    if (layer < 0 || layer >= p->cfg.n_layers) return KVPOOL_ERR_INVALID_ARG;
+    const LayerDesc& d = L.layers[layer];
+    lo->kind = d.kind;
+    lo->pad = 0;
+    lo->block_pool_offset = d.block_pool;
+    lo->block_bytes = d.block_bytes;
+    lo->csa_offset = d.csa_off;
+    lo->idx_offset = d.idx_off;
+    lo->idx_scale_offset = d.idx_scale_off;
+    lo->hca_offset = d.hca_off;
+    lo->ring_offset = d.ring;
+    lo->ring_request_bytes = d.ring_req_bytes;
+    lo->acc_offset = d.acc;
+    lo->acc_request_bytes = d.acc_req_bytes;
+  }
+  return KVPOOL_OK;
+}
+
+int kvpool_check_device(kvpool_t* p, void* stream, uint32_t* word_out) {
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  if (!p->device()) {
+    if (word_out) *word_out = 0;
+    return KVPOOL_OK;
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t w = 0;
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess) e = cudaMemcpy(&w, p->arena + p->lay.pd.err, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && w != 0) e = cudaMemset(p->arena + p->lay.pd.err, 0, 4);
+  if (e != cudaSuccess) return p->cuda_fail(e, "check_device");
+  if (word_out) *word_out = w;
+  if (w != 0) return p->fail(KVPOOL_ERR_DEVICE_CHECK, "a kernel flagged an out-of-range index or a wait limit");
+  return KVPOOL_OK;
+}
+
+int kvpool_profile_enable(kvpool_t* p, int enable) {
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  if (enable) {
+    p->settle_profile();
+    for (int k = 0; k < KVPOOL_KERNEL_COUNT; ++k) {
+      p->prof_ms[k] = 0;
+      p->prof_launches[k] = 0;
+      p->prof_bytes[k] = 0;
+    }
+  }
+  p->profiling = enable != 0 && p->device();
+  return KVPOOL_OK;
+}
+
+int kvpool_profile_read(kvpool_t* p, int32_t kernel, double* ms_total, int64_t* launches, int64_t* bytes) {
+  if (!p || kernel < 0 || kernel >= KVPOOL_KERNEL_COUNT) return KVPOOL_ERR_INVALID_ARG;
+  p->settle_profile();
+  if (ms_total) *ms_total = p->prof_ms[kernel];
+  if (launches) *launches = p->prof_launches[kernel];
+  if (bytes) *bytes = p->prof_bytes[kernel];
+  return KVPOOL_OK;
+}
+
+const char* kvpool_last_error(const kvpool_t* p) { return p ? p->err.c_str() : "NULL pool"; }
+
+}  // extern "C"

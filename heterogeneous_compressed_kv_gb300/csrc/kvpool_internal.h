@@ -1,0 +1,136 @@
+// kvpool_internal.h -- shared definitions of the kvpool host runtime and its
+// CUDA kernels (not part of the public ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "kvpool.h"
+
+namespace kvp {
+
+constexpr int kMaxLayers = 16;
+constexpr int kHistBins = 2048;          // radix digit of the top-k select (11 bits)
+constexpr int kScoreSegsPerCta = 64;     // block segments scored by one CTA
+constexpr int kSelectKeysPerCta = 4096;  // keys handled by one select CTA
+constexpr int kMaxAppendUnits = 512;     // units per append launch
+constexpr int kMaxAttendReqs = 256;      // requests per attend-side launch
+constexpr int kAttendThreadsMax = 544;   // 16 consumer warps + 1 producer warp
+
+// device error word flags
+enum : uint32_t {
+  kErrWaitTimeout = 1u << 0,  // an mbarrier wait passed its time limit
+  kErrBadBlock = 1u << 1,     // block id out of range
+  kErrBadIndex = 1u << 2,     // entry / slot index out of range
+  kErrBadShape = 1u << 3,     // launch shape inconsistent with the pool
+};
+
+// Byte offsets of one layer inside the arena (see kvpool.h for the layout).
+struct LayerDesc {
+  int32_t kind;
+  int32_t has_csa, has_hca;
+  int64_t block_pool, block_bytes;
+  int64_t csa_off, idx_off, idx_scale_off, hca_off;
+  int64_t ring, ring_req_bytes;
+  int64_t acc, acc_req_bytes;  // acc: CSA [2HD] f32, idx [XD] f32, HCA [2HD] f32
+  int64_t alpha_csa, alpha_hca, alpha_idx;  // f32 [H][m], [H][m'], [Ih][m]
+};
+
+// Everything a kernel needs to know about the pool (passed by value).
+struct PoolDesc {
+  uint8_t* arena;
+  int32_t m, m_prime, n_win;
+  int32_t heads, head_dim, idx_heads, idx_dim, HD, XD;
+  int32_t in_dtype, cache_dtype, vs, isz;  // cache value bytes, input value bytes
+  int32_t csa_per_block, idx_chunks;       // idx_chunks: 16-B chunks per indexer key
+  int64_t entry_bytes, idx_entry_bytes;
+  int32_t max_blocks, max_requests, max_bpr, staging_base;
+  int64_t table;  // int32 [max_requests][max_bpr]
+  int64_t err;    // uint32
+};
+
+// ---- append ---------------------------------------------------------------
+// One (request, block segment) touched by an append call: positions
+// seg*m' + t for t in [t0, t1).
+struct AppendUnit {
+  int32_t slot;      // request slot
+  int32_t seg;       // block index within the request
+  int16_t t0, t1;    // token range inside the segment
+  int16_t ring_from; // first t written to the window (t1 if none)
+  int16_t pad;
+  int32_t in_row;    // input row of the token at t0
+  int32_t block_id;  // id the segment seals into in this call, or -1
+};
+
+struct AppendParams {
+  PoolDesc pool;
+  LayerDesc layers[kMaxLayers];
+  const void* k;
+  const void* v;
+  const void* idx_k;
+  int64_t rows;  // T: rows per layer in the inputs
+  int32_t n_units;
+  int32_t n_slices;  // CTAs that split one unit's 2*H*d values
+  AppendUnit units[kMaxAppendUnits];
+};
+
+// share_prefix: window fill of dst + table row copy
+struct ShareParams {
+  PoolDesc pool;
+  LayerDesc layers[kMaxLayers];
+  const void* win_k;
+  const void* win_v;
+  int32_t dst, src, n_blocks, w;
+  int64_t n_tokens;
+};
+
+// ---- decode attention -----------------------------------------------------
+struct AttendReq {
+  int32_t slot;
+  int32_t n_sealed;   // sealed blocks of the request
+  int32_t n_cand;     // CSA entries N_c (0 for layers without CSA)
+  int32_t k;          // min(top_k, N_c)
+  int32_t n_hca;      // HCA entries attended (0 for layers without HCA)
+  int32_t w;          // window tokens
+  int64_t length;     // L
+  int32_t select_all; // k == N_c: every CSA entry is selected
+  int32_t score_base; // first score CTA of this request
+  int32_t key_base;   // first select CTA of this request
+  int32_t split_base; // first attention split of this request
+  int32_t n_split;
+  int32_t split_len;  // virtual entries per split
+};
+
+struct AttendParams {
+  PoolDesc pool;
+  LayerDesc layer;
+  const void* q;
+  const void* q_idx;
+  float* out;
+  int32_t* topk_out;
+  int32_t top_k;
+  int32_t n;                 // requests in this launch
+  int32_t row0;              // first row of q / out for this launch
+  int32_t total_score_ctas, total_key_ctas, total_splits;
+  // scratch (device pointers)
+  uint32_t* keys;            // [kMaxAttendReqs][max_cand]
+  int64_t key_stride;        // max_cand
+  uint32_t* hist;            // [kMaxAttendReqs][3][kHistBins]
+  uint32_t* counts;          // [kMaxAttendReqs][max_key_ctas][2]
+  int32_t max_key_ctas;
+  int32_t* sel;              // [kMaxAttendReqs][max_top_k]
+  int32_t sel_stride;
+  float* part_o;             // [max_splits][HD]
+  float* part_ml;            // [max_splits][H][2]
+  AttendReq reqs[kMaxAttendReqs];
+};
+
+// ---- launchers (implemented in the .cu files; return cudaError_t as int) --
+int launch_append(const AppendParams& p, int n_layers, void* stream);
+int launch_share(const ShareParams& p, int n_layers, void* stream);
+int launch_score(const AttendParams& p, void* stream);
+int launch_select(const AttendParams& p, void* stream);
+int launch_attend(const AttendParams& p, void* stream);
+int launch_combine(const AttendParams& p, void* stream);
+
+}  // namespace kvp

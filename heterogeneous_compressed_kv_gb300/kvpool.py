@@ -1,0 +1,264 @@
+"""Thin Python binding of the kvpool C ABI (``include/kvpool.h``).
+
+Argument marshalling only: torch tensors are passed as raw device pointers,
+the current (or given) torch CUDA stream as a ``cudaStream_t``.  Every step of
+the path runs in the CUDA kernels of ``libkvpool.so``; there is no CPU or
+PyTorch fallback -- if the library cannot be built or loaded this module
+raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass, field
+from typing import Optional, Sequence
+
+import numpy as np
+
+F32, BF16, FP8_E4M3 = 0, 1, 2
+SWA_ONLY, CSA, HCA, CSA_HCA = 0, 1, 2, 3
+FLAG_NO_DEVICE = 1
+OK, ERR_INVALID_ARG, ERR_OUT_OF_BLOCKS, ERR_OUT_OF_REQUESTS, ERR_BAD_REQUEST = 0, -1, -2, -3, -4
+ERR_NOT_SHAREABLE, ERR_CUDA, ERR_DEVICE_CHECK, ERR_CAPACITY = -5, -6, -7, -8
+KERNEL_APPEND, KERNEL_SCORE, KERNEL_SELECT, KERNEL_ATTEND, KERNEL_COMBINE = range(5)
+KERNEL_NAMES = ["append", "score", "select", "attend", "combine"]
+
+EXPORTS = ["kvpool_required_bytes", "kvpool_create", "kvpool_destroy", "kvpool_alloc_request",
+           "kvpool_free_request", "kvpool_share_prefix", "kvpool_append", "kvpool_decode_attend",
+           "kvpool_request_info", "kvpool_block_refcount", "kvpool_free_block_count", "kvpool_get_layout",
+           "kvpool_check_device", "kvpool_profile_enable", "kvpool_profile_read", "kvpool_last_error"]
+
+
+class KvpoolError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"kvpool error {code}: {msg}")
+        self.code = code
+
+
+class _Config(C.Structure):
+    _fields_ = [("m", C.c_int32), ("m_prime", C.c_int32), ("n_win", C.c_int32), ("heads", C.c_int32),
+                ("head_dim", C.c_int32), ("idx_heads", C.c_int32), ("idx_dim", C.c_int32),
+                ("in_dtype", C.c_int32), ("cache_dtype", C.c_int32), ("n_layers", C.c_int32),
+                ("layer_kinds", C.POINTER(C.c_int32)), ("max_requests", C.c_int32), ("max_blocks", C.c_int32),
+                ("max_blocks_per_request", C.c_int32), ("max_batch", C.c_int32), ("max_top_k", C.c_int32),
+                ("gate_csa", C.POINTER(C.c_float)), ("gate_hca", C.POINTER(C.c_float)),
+                ("gate_idx", C.POINTER(C.c_float)), ("flags", C.c_uint32)]
+
+
+class _Info(C.Structure):
+    _fields_ = [("length", C.c_int64), ("n_csa", C.c_int64), ("n_hca", C.c_int64), ("csa_tail", C.c_int32),
+                ("hca_tail", C.c_int32), ("n_blocks", C.c_int32), ("window", C.c_int32)]
+
+
+class _Layout(C.Structure):
+    _fields_ = [("entry_bytes", C.c_int64), ("idx_entry_bytes", C.c_int64), ("csa_per_block", C.c_int32),
+                ("staging_base", C.c_int32), ("table_offset", C.c_int64), ("error_offset", C.c_int64),
+                ("total_bytes", C.c_int64)]
+
+
+class _LayerLayout(C.Structure):
+    _fields_ = [("kind", C.c_int32), ("pad", C.c_int32), ("block_pool_offset", C.c_int64),
+                ("block_bytes", C.c_int64), ("csa_offset", C.c_int64), ("idx_offset", C.c_int64),
+                ("idx_scale_offset", C.c_int64), ("hca_offset", C.c_int64), ("ring_offset", C.c_int64),
+                ("ring_request_bytes", C.c_int64), ("acc_offset", C.c_int64), ("acc_request_bytes", C.c_int64)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libkvpool.so (building it in-tree first if it is missing or stale)."""
+    global _lib
+    if _lib is None:
+        from ._build import build_lib
+        path = build_lib("kvpool")
+        L = C.CDLL(path)
+        vp, i32, i64 = C.c_void_p, C.c_int32, C.c_int64
+        L.kvpool_required_bytes.restype = C.c_size_t
+        L.kvpool_required_bytes.argtypes = [C.POINTER(_Config)]
+        L.kvpool_create.argtypes = [C.POINTER(_Config), vp, C.c_size_t, vp, C.POINTER(vp)]
+        L.kvpool_destroy.argtypes = [vp]
+        L.kvpool_alloc_request.argtypes = [vp, C.POINTER(i32)]
+        L.kvpool_free_request.argtypes = [vp, i32]
+        L.kvpool_share_prefix.argtypes = [vp, i32, i32, i64, vp, vp, vp]
+        L.kvpool_append.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
+        L.kvpool_decode_attend.argtypes = [vp, i32, i32, vp, vp, vp, i32, vp, vp, vp]
+        L.kvpool_request_info.argtypes = [vp, i32, C.POINTER(_Info), vp, i32]
+        L.kvpool_block_refcount.argtypes = [vp, i32]
+        L.kvpool_free_block_count.argtypes = [vp]
+        L.kvpool_get_layout.argtypes = [vp, C.POINTER(_Layout), i32, C.POINTER(_LayerLayout)]
+        L.kvpool_check_device.argtypes = [vp, vp, C.POINTER(C.c_uint32)]
+        L.kvpool_profile_enable.argtypes = [vp, C.c_int]
+        L.kvpool_profile_read.argtypes = [vp, i32, C.POINTER(C.c_double), C.POINTER(i64), C.POINTER(i64)]
+        L.kvpool_last_error.restype = C.c_char_p
+        L.kvpool_last_error.argtypes = [vp]
+        _lib = L
+    return _lib
+
+
+def library_path() -> str:
+    return lib()._name
+
+
+@dataclass
+class PoolConfig:
+    m: int
+    m_prime: int
+    n_win: int
+    heads: int
+    head_dim: int
+    idx_heads: int
+    idx_dim: int
+    in_dtype: int
+    cache_dtype: int
+    layer_kinds: Sequence[int]
+    max_requests: int
+    max_blocks: int
+    max_blocks_per_request: int
+    max_batch: int
+    max_top_k: int
+    gate_csa: np.ndarray  # [n_layers][heads][m] logits
+    gate_hca: np.ndarray  # [n_layers][heads][m_prime]
+    gate_idx: np.ndarray  # [n_layers][idx_heads][m]
+    flags: int = 0
+    _keep: list = field(default_factory=list, repr=False)
+
+    def to_c(self) -> _Config:
+        kinds = np.ascontiguousarray(self.layer_kinds, dtype=np.int32)
+        g = [np.ascontiguousarray(x, dtype=np.float32).reshape(-1) for x in (self.gate_csa, self.gate_hca,
+                                                                             self.gate_idx)]
+        self._keep = [kinds] + g
+        fp = C.POINTER(C.c_float)
+        return _Config(self.m, self.m_prime, self.n_win, self.heads, self.head_dim, self.idx_heads, self.idx_dim,
+                       self.in_dtype, self.cache_dtype, kinds.size, kinds.ctypes.data_as(C.POINTER(C.c_int32)),
+                       self.max_requests, self.max_blocks, self.max_blocks_per_request, self.max_batch,
+                       self.max_top_k, g[0].ctypes.data_as(fp), g[1].ctypes.data_as(fp), g[2].ctypes.data_as(fp),
+                       self.flags)
+
+
+def required_bytes(cfg: PoolConfig) -> int:
+    c = cfg.to_c()
+    return int(lib().kvpool_required_bytes(C.byref(c)))
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+class Pool:
+    """A two-pool KV cache living in a caller-owned device arena."""
+
+    def __init__(self, cfg: PoolConfig, arena=None, stream=None):
+        self.L = lib()
+        self.cfg = cfg
+        self._c = cfg.to_c()
+        self.arena = arena
+        h = C.c_void_p()
+        if cfg.flags & FLAG_NO_DEVICE:
+            rc = self.L.kvpool_create(C.byref(self._c), None, 0, None, C.byref(h))
+        else:
+            nbytes = arena.numel() * arena.element_size()
+            rc = self.L.kvpool_create(C.byref(self._c), arena.data_ptr(), nbytes, _stream(stream), C.byref(h))
+        if rc != OK:
+            raise KvpoolError(rc, "kvpool_create refused the configuration")
+        self.h = h
+        self.n_layers = len(cfg.layer_kinds)
+        self.HD = cfg.heads * cfg.head_dim
+        self.XD = cfg.idx_heads * cfg.idx_dim
+
+    def __del__(self):
+        if getattr(self, "h", None):
+            self.L.kvpool_destroy(self.h)
+            self.h = None
+
+    def last_error(self) -> str:
+        return self.L.kvpool_last_error(self.h).decode()
+
+    def _check(self, rc: int, what: str) -> int:
+        if rc != OK:
+            raise KvpoolError(rc, f"{what}: {self.last_error()}")
+        return rc
+
+    # ---- lifecycle ----
+    def alloc_request(self) -> int:
+        r = C.c_int32()
+        self._check(self.L.kvpool_alloc_request(self.h, C.byref(r)), "alloc_request")
+        return r.value
+
+    def free_request(self, req: int) -> None:
+        self._check(self.L.kvpool_free_request(self.h, req), "free_request")
+
+    def share_prefix(self, dst, src, n_tokens, win_k, win_v, stream=None, check=True) -> int:
+        rc = self.L.kvpool_share_prefix(self.h, dst, src, n_tokens, _ptr(win_k), _ptr(win_v), _stream(stream))
+        return self._check(rc, "share_prefix") if check else rc
+
+    def append(self, req_ids, n_new, k, v, idx_k, stream=None, check=True) -> int:
+        req, nn = _i32(req_ids), _i32(n_new)
+        rc = self.L.kvpool_append(self.h, req.size, req.ctypes.data_as(C.c_void_p), nn.ctypes.data_as(C.c_void_p),
+                                  _ptr(k), _ptr(v), _ptr(idx_k), _stream(stream))
+        return self._check(rc, "append") if check else rc
+
+    def decode_attend(self, layer, req_ids, q, q_idx, top_k, out, topk_out=None, stream=None, check=True) -> int:
+        req = _i32(req_ids)
+        rc = self.L.kvpool_decode_attend(self.h, layer, req.size, req.ctypes.data_as(C.c_void_p), _ptr(q),
+                                         _ptr(q_idx), top_k, _ptr(out), _ptr(topk_out), _stream(stream))
+        return self._check(rc, "decode_attend") if check else rc
+
+    # ---- queries ----
+    def request_info(self, req: int, cap: int = 1 << 16):
+        info = _Info()
+        ids = np.zeros(max(cap, 1), np.int32)
+        rc = self.L.kvpool_request_info(self.h, req, C.byref(info), ids.ctypes.data_as(C.c_void_p), cap)
+        if rc != OK:
+            return rc, None, None
+        d = {f: getattr(info, f) for f, _ in _Info._fields_}
+        return rc, d, ids[:info.n_blocks].copy()
+
+    def block_refcount(self, b: int) -> int:
+        return self.L.kvpool_block_refcount(self.h, b)
+
+    def free_block_count(self) -> int:
+        return self.L.kvpool_free_block_count(self.h)
+
+    def layout(self, layer: Optional[int] = None):
+        lo = _Layout()
+        ll = _LayerLayout()
+        rc = self.L.kvpool_get_layout(self.h, C.byref(lo), -1 if layer is None else layer,
+                                      None if layer is None else C.byref(ll))
+        self._check(rc, "get_layout")
+        d = {f: getattr(lo, f) for f, _ in _Layout._fields_}
+        if layer is not None:
+            d.update({f: getattr(ll, f) for f, _ in _LayerLayout._fields_})
+        return d
+
+    def check_device(self, stream=None) -> int:
+        w = C.c_uint32()
+        rc = self.L.kvpool_check_device(self.h, _stream(stream), C.byref(w))
+        if rc != OK:
+            raise KvpoolError(rc, f"check_device: {self.last_error()} (flags {w.value:#x})")
+        return w.value
+
+    def profile_enable(self, on: bool = True) -> None:
+        self._check(self.L.kvpool_profile_enable(self.h, 1 if on else 0), "profile_enable")
+
+    def profile_read(self, kernel: int):
+        ms, n, b = C.c_double(), C.c_int64(), C.c_int64()
+        self._check(self.L.kvpool_profile_read(self.h, kernel, C.byref(ms), C.byref(n), C.byref(b)), "profile_read")
+        return ms.value, n.value, b.value

@@ -1,0 +1,264 @@
+/*
+ * kvpool.h -- C ABI of a GPU-resident two-pool KV cache (DeepSeek-V4 style:
+ * a Classical/Block pool of immutable, lcm-aligned compressed blocks plus a
+ * per-request State pool), built for one GB300 (sm_103a).
+ *
+ * What the library computes, per decode step and attention layer, follows
+ * these design pages (cited by title and section):
+ *   [P1] "Why does V4 split pools? How do block alignment and the tail buffer
+ *        work together" -- s1.1 (Classical holds only full, immutable
+ *        compressed entries; State holds the tail and the SWA window), s1.2
+ *        (CSA: every m = 4 tokens -> 1 entry, read top-k sparse; HCA: every
+ *        m' = 128 tokens -> 1 entry, read densely), s2.2 (block = lcm(m, m')
+ *        = 128 tokens = 32 CSA + 1 HCA entries; L = 128q + r), s3.1 (tails of
+ *        at most 3 / 127 tokens), s4 (one decode step: token into the tail,
+ *        compress when a group fills, SWA slides, attention reads Classical
+ *        entries sparsely/densely plus the exact local window).
+ *   [P2] "V4 KV Layout: Classical + State dual pool" -- Classical KV cache
+ *        and State cache tables; the lightning indexer's light K vectors.
+ *   [P3] "Ch 12 Inference framework: heterogeneous KV scheduling" -- s2.1
+ *        (one State block per request, freed whole), s2.2 (Block cache shared
+ *        across requests by refcount), Figure 12-1 (a block id spans all
+ *        layers; each block holds CSA indexer KV, CSA main KV and HCA KV).
+ *   [P4] "V4 disk prefix cache" -- Zero SWA caching: on a prefix hit only
+ *        the compressed blocks are reused and the window is recomputed.
+ * The pages give no compressor, score or attention formula.  This library
+ * fixes them as follows (the same definitions as the CPU oracle):
+ *   compressor   entry[h][j] = fp32 chain acc = fma(alpha[h][i], x_i[h][j], acc)
+ *                over the group's tokens i = 0..m-1 (m' for HCA) from +0,
+ *                alpha = softmax of the caller's gate logits (double, rounded
+ *                to fp32); K and V share alpha; indexer entries use their own
+ *                gates per indexer head;
+ *   score        s_e = fp32 chain fma(q_idx[v], key_e[v], acc) over the flat
+ *                indexer (head, dim) order from +0, times the entry scale
+ *                (fp8 cache);
+ *   top-k        k = min(top_k, number of CSA entries), by (score desc,
+ *                index asc), -0 == +0;
+ *   attention    one softmax with scale 1/sqrt(head_dim) over [selected CSA
+ *                entries, every HCA entry, the SWA window] (no masking; the
+ *                window includes the token appended in this step), fp32.
+ *
+ * Conventions (all entry points):
+ *   - Device pointers ("d_") are read/written in stream order on `stream`
+ *     (a cudaStream_t; NULL = the legacy default stream).  Host pointers
+ *     ("h_") are read before the call returns.
+ *   - The caller owns the device arena (kvpool_required_bytes bytes, 256-B
+ *     aligned), every input and every output.  The library owns the layout
+ *     inside the arena and all host metadata.
+ *   - Every call validates its whole batch and reserves blocks on the host
+ *     before launching anything; a call that returns an error has changed
+ *     nothing.  No call synchronizes with the device except
+ *     kvpool_check_device and kvpool_profile_read.
+ *   - A pool is not thread safe; drive it from one host thread and one
+ *     stream.  No exception crosses this ABI.
+ */
+#ifndef KVPOOL_H
+#define KVPOOL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ---- */
+enum {
+  KVPOOL_OK = 0,
+  KVPOOL_ERR_INVALID_ARG = -1,     /* bad size, pointer, dtype or combination */
+  KVPOOL_ERR_OUT_OF_BLOCKS = -2,   /* the Classical pool has too few free blocks */
+  KVPOOL_ERR_OUT_OF_REQUESTS = -3, /* every request slot is in use */
+  KVPOOL_ERR_BAD_REQUEST = -4,     /* request id out of range or not allocated */
+  KVPOOL_ERR_NOT_SHAREABLE = -5,   /* prefix not whole sealed blocks, or dst not fresh */
+  KVPOOL_ERR_CUDA = -6,            /* a CUDA runtime call failed (see kvpool_last_error) */
+  KVPOOL_ERR_DEVICE_CHECK = -7,    /* a kernel flagged a bounds or wait-limit violation */
+  KVPOOL_ERR_CAPACITY = -8,        /* a request would exceed max_blocks_per_request */
+};
+
+/* ---- element types ---- */
+enum {
+  KVPOOL_F32 = 0,
+  KVPOOL_BF16 = 1,
+  KVPOOL_FP8_E4M3 = 2, /* cache only: e4m3 codes + one bf16 scale per K half, V half, indexer entry */
+};
+
+/* ---- layer kinds (Figure 12-1 lists SWA, CSA and HCA layers) ---- */
+enum {
+  KVPOOL_SWA_ONLY = 0, /* window only */
+  KVPOOL_CSA = 1,      /* CSA top-k + window */
+  KVPOOL_HCA = 2,      /* HCA dense + window */
+  KVPOOL_CSA_HCA = 3,  /* all three sources */
+};
+
+enum { KVPOOL_FLAG_NO_DEVICE = 1u }; /* bookkeeping only: no arena, no launches (host tests) */
+
+typedef struct kvpool_config {
+  int32_t m;          /* CSA group (4); must divide m_prime so lcm(m, m') = m' */
+  int32_t m_prime;    /* HCA group (128) = block length in tokens */
+  int32_t n_win;      /* SWA window in tokens; a positive multiple of m_prime */
+  int32_t heads;      /* attention heads (queries and cache alike) */
+  int32_t head_dim;   /* 64 or 128 */
+  int32_t idx_heads;  /* lightning-indexer heads */
+  int32_t idx_dim;    /* lightning-indexer head dim */
+  int32_t in_dtype;   /* KVPOOL_F32 or KVPOOL_BF16: new K/V/indexer keys and queries */
+  int32_t cache_dtype;/* KVPOOL_F32, KVPOOL_BF16 or KVPOOL_FP8_E4M3 */
+  int32_t n_layers;
+  const int32_t* layer_kinds;     /* [n_layers] */
+  int32_t max_requests;           /* request slots (State blocks) */
+  int32_t max_blocks;             /* Classical blocks (ids 0 .. max_blocks-1) */
+  int32_t max_blocks_per_request; /* block-table row length */
+  int32_t max_batch;              /* most requests in one append or decode_attend call */
+  int32_t max_top_k;              /* largest top_k a decode_attend call may ask for */
+  const float* gate_csa;          /* [n_layers][heads][m] gate logits (read at create) */
+  const float* gate_hca;          /* [n_layers][heads][m_prime] */
+  const float* gate_idx;          /* [n_layers][idx_heads][m] */
+  uint32_t flags;                 /* KVPOOL_FLAG_* */
+} kvpool_config;
+
+typedef struct kvpool kvpool_t;
+
+/* Arena bytes a config needs (0 if the config is invalid). */
+size_t kvpool_required_bytes(const kvpool_config* cfg);
+
+/* Create a pool in the caller's device arena.  Validates cfg ([P1] s2.2:
+ * m | m'; [P3] s2.2: the window is a whole number of blocks), computes the
+ * gates' softmax on the host and uploads them, and clears the device error
+ * word, in stream order on `stream`.  d_arena must stay allocated until
+ * kvpool_destroy.  With KVPOOL_FLAG_NO_DEVICE, d_arena must be NULL and the
+ * pool only keeps bookkeeping.  Errors: INVALID_ARG, CUDA. */
+int kvpool_create(const kvpool_config* cfg, void* d_arena, size_t arena_bytes, void* stream, kvpool_t** out);
+int kvpool_destroy(kvpool_t* pool);
+
+/* Take the smallest free request slot; its State block is empty (length 0).
+ * [P3] s2.1.  Errors: OUT_OF_REQUESTS. */
+int kvpool_alloc_request(kvpool_t* pool, int32_t* req_out);
+
+/* Release a request: its State block whole, and one reference on each of its
+ * sealed blocks (a block id returns to the free set at refcount 0).  [P3]
+ * s2.1, s2.2.  Errors: BAD_REQUEST. */
+int kvpool_free_request(kvpool_t* pool, int32_t req);
+
+/* Zero SWA prefix reuse ([P4], [P3] s2.2): the fresh request dst references
+ * (refcount + 1) the first n_tokens / m' sealed blocks of src and takes
+ * length n_tokens.  d_win_k, d_win_v: [n_layers][w][heads][head_dim] in
+ * in_dtype, w = min(n_tokens, n_win): the caller's recomputed K/V of
+ * positions n_tokens-w .. n_tokens-1, written into dst's window.  Errors:
+ * BAD_REQUEST (dst/src invalid or equal), INVALID_ARG (n_tokens <= 0 or a
+ * NULL window), NOT_SHAREABLE (n_tokens not a multiple of m', beyond src's
+ * sealed blocks, or dst not fresh), CUDA. */
+int kvpool_share_prefix(kvpool_t* pool, int32_t dst, int32_t src, int64_t n_tokens, const void* d_win_k,
+                        const void* d_win_v, void* stream);
+
+/* Append new tokens ([P1] s3, s4): for request h_req_ids[i], h_n_new[i]
+ * tokens.  d_k, d_v: [n_layers][T][heads][head_dim], d_idx_k:
+ * [n_layers][T][idx_heads][idx_dim] (may be NULL when no layer has CSA), all
+ * in_dtype, T = sum(h_n_new), rows in batch order then position order.  Each
+ * token enters its request's SWA window (rounded to the cache dtype) and
+ * tail; every completed m-group forms a CSA entry and an indexer entry, every
+ * completed m'-group forms an HCA entry and seals the block, which gets the
+ * smallest free block id (requests in batch order, then positions) and is
+ * immutable from then on.  Errors: INVALID_ARG (n < 0, n > max_batch,
+ * negative counts, duplicate ids, NULL inputs with T > 0), BAD_REQUEST,
+ * CAPACITY, OUT_OF_BLOCKS, CUDA. */
+int kvpool_append(kvpool_t* pool, int32_t n, const int32_t* h_req_ids, const int32_t* h_n_new, const void* d_k,
+                  const void* d_v, const void* d_idx_k, void* stream);
+
+/* Decode attention of one layer for n requests ([P1] s4, [P2] Classical KV
+ * cache table): score every CSA entry with the indexer, keep the top_k, and
+ * attend over [selected CSA entries | all HCA entries | SWA window] in one
+ * softmax.  d_q: [n][heads][head_dim], d_q_idx: [n][idx_heads][idx_dim] (may
+ * be NULL for layers without CSA), both in_dtype.  d_out: [n][heads][head_dim]
+ * fp32.  d_topk_out: [n][top_k] int32 or NULL: the selected CSA entry indices
+ * in ascending order, padded with -1.  Errors: INVALID_ARG (layer, n > max_batch,
+ * top_k < 0 or > max_top_k, NULL pointers, an empty request), BAD_REQUEST,
+ * CUDA. */
+int kvpool_decode_attend(kvpool_t* pool, int32_t layer, int32_t n, const int32_t* h_req_ids, const void* d_q,
+                         const void* d_q_idx, int32_t top_k, float* d_out, int32_t* d_topk_out, void* stream);
+
+/* ---- host-side queries (no device access) ---- */
+typedef struct kvpool_info {
+  int64_t length;   /* tokens appended (or shared) so far */
+  int64_t n_csa;    /* floor(length / m)  CSA entries (sealed + staged) */
+  int64_t n_hca;    /* floor(length / m') HCA entries (all sealed) */
+  int32_t csa_tail; /* length mod m  (<= m-1)  */
+  int32_t hca_tail; /* length mod m' (<= m'-1) */
+  int32_t n_blocks; /* sealed blocks in the block table */
+  int32_t window;   /* tokens in the SWA window: min(length, n_win) */
+} kvpool_info;
+
+/* Fill *info and up to cap block ids (table order).  Errors: BAD_REQUEST. */
+int kvpool_request_info(const kvpool_t* pool, int32_t req, kvpool_info* info, int32_t* h_block_ids,
+                        int32_t cap);
+/* Refcount of a block id (0 = free), or INVALID_ARG. */
+int kvpool_block_refcount(const kvpool_t* pool, int32_t block_id);
+/* Number of free Classical blocks. */
+int kvpool_free_block_count(const kvpool_t* pool);
+
+/* ---- arena layout (byte offsets from d_arena) ----
+ * Entry (CSA entry, HCA entry, window token), entry_bytes long:
+ *   K codes [heads][head_dim], V codes [heads][head_dim] in the cache dtype,
+ *   then for fp8 a bf16 K scale, a bf16 V scale and 12 zero bytes.
+ * Indexer keys of a block: 16-byte chunk c of entry e at (c * csa_per_block
+ *   + e) * 16 from idx_offset (chunk-major, so a warp reading chunk c of 32
+ *   consecutive entries reads 512 contiguous bytes); fp8 scales [csa_per_block]
+ *   bf16 at idx_scale_offset.
+ * Block section of a layer: csa entries [csa_per_block], indexer keys and
+ *   scales, HCA entry; absent parts have offset -1.  Section of block id b at
+ *   block_pool_offset + b * block_bytes; ids staging_base + r (r a request
+ *   slot) are request r's private staging sections (its open block).
+ * Window of request r: ring_offset + r * ring_request_bytes, token at
+ *   position p in slot p mod n_win.
+ * Compressor accumulators of request r (fp32): acc_offset + r * acc_request_bytes:
+ *   CSA [2][heads][head_dim], indexer [idx_heads][idx_dim], HCA [2][heads][head_dim].
+ * Block table: int32 [max_requests][max_blocks_per_request] at table_offset. */
+typedef struct kvpool_layer_layout {
+  int32_t kind;
+  int32_t pad;
+  int64_t block_pool_offset, block_bytes;
+  int64_t csa_offset, idx_offset, idx_scale_offset, hca_offset;
+  int64_t ring_offset, ring_request_bytes;
+  int64_t acc_offset, acc_request_bytes;
+} kvpool_layer_layout;
+
+typedef struct kvpool_layout {
+  int64_t entry_bytes;     /* bytes of one K/V entry or window token */
+  int64_t idx_entry_bytes; /* bytes of one indexer key (without scale) */
+  int32_t csa_per_block;   /* m' / m */
+  int32_t staging_base;    /* = max_blocks */
+  int64_t table_offset;
+  int64_t error_offset;    /* uint32 device error word */
+  int64_t total_bytes;
+} kvpool_layout;
+
+/* Layout of the pool and (if layer_out != NULL) of one layer. */
+int kvpool_get_layout(const kvpool_t* pool, kvpool_layout* out, int32_t layer, kvpool_layer_layout* layer_out);
+
+/* Synchronize `stream`, read and clear the device error word.  Returns OK,
+ * DEVICE_CHECK (a kernel met an out-of-range index or a wait limit; *word_out
+ * gets the flags), or CUDA. */
+int kvpool_check_device(kvpool_t* pool, void* stream, uint32_t* word_out);
+
+/* ---- profiling: CUDA events around each launch, on the launch stream ---- */
+enum {
+  KVPOOL_KERNEL_APPEND = 0,  /* fused append / compress / seal */
+  KVPOOL_KERNEL_SCORE = 1,   /* indexer scores + first radix histogram */
+  KVPOOL_KERNEL_SELECT = 2,  /* top-k radix select passes and emit */
+  KVPOOL_KERNEL_ATTEND = 3,  /* split-K attention over the three sources */
+  KVPOOL_KERNEL_COMBINE = 4, /* split-K merge */
+  KVPOOL_KERNEL_COUNT = 5
+};
+/* Enable (1) or disable (0) event recording; enabling resets the totals. */
+int kvpool_profile_enable(kvpool_t* pool, int enable);
+/* Synchronize and report, for one kernel kind, the summed device time of its
+ * launches since profiling was enabled, the launch count and the algorithmic
+ * bytes those launches had to move (inputs read + outputs written, scratch
+ * excluded). */
+int kvpool_profile_read(kvpool_t* pool, int32_t kernel, double* ms_total, int64_t* launches, int64_t* bytes);
+
+/* Last error message of this pool (never NULL). */
+const char* kvpool_last_error(const kvpool_t* pool);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVPOOL_H */

@@ -1,0 +1,192 @@
+"""CPU tests of the C-ABI library: it loads, exports every declared symbol,
+validates configurations, lays out the arena sanely, and its host bookkeeping
+(block ids, refcounts, tails, errors) matches the oracle bit for bit.  No
+kernel runs here (pools are created with KVPOOL_FLAG_NO_DEVICE)."""
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle as O
+from heterogeneous_compressed_kv_gb300 import kvpool as K
+from tests import harness as H
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "kvpool.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvpool_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert set(names) == set(K.EXPORTS)
+    L = K.lib()
+    for n in names:
+        assert hasattr(L, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", K.library_path()], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (kvpool_\w+)", out))
+    assert set(names) <= exported
+
+
+def cfg_of(w, **kw):
+    g = H.gates(w)
+    d = dict(m=w["m"], m_prime=w["m_prime"], n_win=w["n_win"], heads=w["heads"], head_dim=w["head_dim"],
+             idx_heads=w["idx_heads"], idx_dim=w["idx_dim"], in_dtype=w["in_dtype"], cache_dtype=w["cache_dtype"],
+             layer_kinds=w["layer_kinds"], max_requests=8, max_blocks=64, max_blocks_per_request=32, max_batch=8,
+             max_top_k=64, gate_csa=g[0], gate_hca=g[1], gate_idx=g[2], flags=K.FLAG_NO_DEVICE)
+    d.update(kw)
+    return K.PoolConfig(**d)
+
+
+def base_workload(**kw):
+    w = dict(m=4, m_prime=128, n_win=128, heads=4, head_dim=64, idx_heads=1, idx_dim=32, in_dtype=K.F32,
+             cache_dtype=K.F32, n_layers=1, layer_kinds=[K.CSA_HCA], seed=5)
+    w.update(kw)
+    return w
+
+
+@pytest.mark.parametrize("bad", [dict(m=3), dict(m=5, m_prime=128), dict(n_win=100), dict(n_win=64),
+                                 dict(head_dim=96), dict(cache_dtype=7), dict(in_dtype=2), dict(max_batch=0),
+                                 dict(heads=1), dict(idx_dim=3), dict(layer_kinds=[9])])
+def test_invalid_configs_are_refused(bad):
+    w = base_workload()
+    wk = {k: v for k, v in bad.items() if k in w}
+    ck = {k: v for k, v in bad.items() if k not in w}
+    if "layer_kinds" in bad:
+        wk.pop("layer_kinds", None)
+        ck["layer_kinds"] = bad["layer_kinds"]
+    cfg = cfg_of(base_workload(**wk), **ck)
+    assert K.required_bytes(cfg) == 0
+    with pytest.raises(K.KvpoolError):
+        K.Pool(cfg)
+
+
+@pytest.mark.parametrize("cache", [K.F32, K.BF16, K.FP8_E4M3])
+def test_layout_is_aligned_and_disjoint(cache):
+    w = base_workload(cache_dtype=cache, in_dtype=K.BF16 if cache != K.F32 else K.F32, heads=16, head_dim=128,
+                      idx_heads=4, idx_dim=64, n_layers=4, layer_kinds=[K.SWA_ONLY, K.CSA, K.HCA, K.CSA_HCA])
+    cfg = cfg_of(w)
+    total = K.required_bytes(cfg)
+    p = K.Pool(cfg)
+    lo = p.layout()
+    assert lo["total_bytes"] == total and lo["csa_per_block"] == 32
+    vs = {K.F32: 4, K.BF16: 2, K.FP8_E4M3: 1}[cache]
+    assert lo["entry_bytes"] == 2 * 2048 * vs + (16 if cache == K.FP8_E4M3 else 0)
+    assert lo["entry_bytes"] % 16 == 0 and lo["idx_entry_bytes"] % 16 == 0
+    spans = [(lo["table_offset"], lo["table_offset"] + 4 * 8 * 32), (lo["error_offset"], lo["error_offset"] + 4)]
+    for l in range(4):
+        d = p.layout(l)
+        nb = cfg.max_blocks + cfg.max_requests
+        for key in ("block_pool_offset", "ring_offset", "acc_offset"):
+            assert d[key] % 256 == 0
+        assert d["block_bytes"] % 256 == 0 and d["ring_request_bytes"] % 256 == 0
+        spans.append((d["block_pool_offset"], d["block_pool_offset"] + nb * d["block_bytes"]))
+        spans.append((d["ring_offset"], d["ring_offset"] + 8 * d["ring_request_bytes"]))
+        spans.append((d["acc_offset"], d["acc_offset"] + 8 * d["acc_request_bytes"]))
+        kind = d["kind"]
+        assert (d["csa_offset"] >= 0) == (kind in (K.CSA, K.CSA_HCA))
+        assert (d["hca_offset"] >= 0) == (kind in (K.HCA, K.CSA_HCA))
+        for key in ("csa_offset", "idx_offset", "idx_scale_offset", "hca_offset"):
+            assert d[key] == -1 or d[key] % 16 == 0
+        if kind == K.SWA_ONLY:
+            assert d["block_bytes"] == 0
+    spans = sorted(s for s in spans if s[1] > s[0])
+    for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+        assert a1 <= b0
+    assert spans[-1][1] <= total
+
+
+def both(w, max_requests=6, max_blocks=24, mbpr=6):
+    o = H.make_oracle(w, max_requests, max_blocks, mbpr)
+    p = K.Pool(cfg_of(w, max_requests=max_requests, max_blocks=max_blocks, max_blocks_per_request=mbpr,
+                      max_batch=max_requests))
+    return o, p
+
+
+def same_state(o, p, reqs):
+    for r in reqs:
+        rc1, i1, ids1 = o.request_info(r)
+        rc2, i2, ids2 = p.request_info(r)
+        assert rc1 == rc2
+        if rc1 == 0:
+            assert i1 == i2 and ids1.tolist() == ids2.tolist()
+    for b in range(24):
+        assert o.block_refcount(b) == p.block_refcount(b)
+    assert o.free_block_count() == p.free_block_count()
+
+
+def test_host_bookkeeping_matches_oracle_under_random_traffic():
+    w = base_workload(heads=4, head_dim=64, idx_heads=1, idx_dim=16, m_prime=16, n_win=32)
+    o, p = both(w)
+    rng = np.random.default_rng(12)
+    live = []
+    HD, XD = 256, 16
+    for step in range(300):
+        op = rng.integers(0, 10)
+        if op < 2:
+            rc1, r1 = o.alloc_request()
+            try:
+                r2 = p.alloc_request()
+                rc2 = 0
+            except K.KvpoolError as e:
+                rc2, r2 = e.code, None
+            assert rc1 == rc2
+            if rc1 == 0:
+                assert r1 == r2
+                live.append(r1)
+        elif op < 3 and live:
+            r = live.pop(rng.integers(0, len(live)))
+            assert o.free_request(r) == 0
+            p.free_request(r)
+        elif op < 4 and len(live) >= 2:
+            src, dst = rng.choice(live, 2, replace=False)
+            n_tok = int(rng.integers(0, 4)) * 16
+            win = np.zeros((1, min(max(n_tok, 1), 32), HD), np.float32)
+            rc1 = o.share_prefix(int(dst), int(src), n_tok, win, win)
+            rc2 = p.share_prefix(int(dst), int(src), n_tok, None, None, stream=0, check=False)
+            assert rc1 == rc2
+        elif live:
+            k = int(rng.integers(1, min(4, len(live)) + 1))
+            reqs = [int(x) for x in rng.choice(live, k, replace=False)]
+            if rng.random() < 0.1:
+                reqs.append(reqs[0])  # duplicate -> refused by both
+            counts = [int(x) for x in rng.integers(0, 40, len(reqs))]
+            T = sum(counts)
+            z = np.zeros((1, T, HD), np.float32)
+            rc1 = o.append(reqs, counts, z, z, np.zeros((1, T, XD), np.float32))
+            rc2 = p.append(reqs, counts, None, None, None, stream=0, check=False)
+            assert rc1 == rc2
+        same_state(o, p, range(6))
+
+
+def test_error_codes_match_oracle():
+    w = base_workload(m_prime=16, n_win=16, heads=4, head_dim=64, idx_dim=16)
+    o, p = both(w, max_requests=3, max_blocks=3, mbpr=2)
+    r = [p.alloc_request() for _ in range(3)]
+    assert [o.alloc_request()[1] for _ in range(3)] == r
+    with pytest.raises(K.KvpoolError) as e:
+        p.alloc_request()
+    assert e.value.code == o.alloc_request()[0] == K.ERR_OUT_OF_REQUESTS
+    z = lambda T: np.zeros((1, T, 256), np.float32)
+    zi = lambda T: np.zeros((1, T, 16), np.float32)
+    for reqs, counts in [([0, 1], [16, 16]), ([0, 1, 2], [16, 16, 16]), ([0], [40]), ([0, 0], [1, 1]),
+                         ([5], [1]), ([0], [-1]), ([2], [32])]:
+        T = sum(max(c, 0) for c in counts)
+        rc1 = o.append(reqs, counts, z(T), z(T), zi(T))
+        rc2 = p.append(reqs, counts, None, None, None, stream=0, check=False)
+        assert rc1 == rc2, (reqs, counts, rc1, rc2)
+        same_state(o, p, range(3))
+    win = np.zeros((1, 16, 256), np.float32)
+    for dst, src, n in [(1, 0, 16), (2, 0, 8), (2, 0, 48), (2, 2, 16), (2, 7, 16), (2, 0, 0)]:
+        assert o.share_prefix(dst, src, n, win, win) == p.share_prefix(dst, src, n, None, None, stream=0,
+                                                                       check=False)
+        same_state(o, p, range(3))
+    for r_ in (0, 1, 2):
+        assert o.free_request(r_) == p.L.kvpool_free_request(p.h, r_)
+    assert o.free_request(1) == p.L.kvpool_free_request(p.h, 1) == K.ERR_BAD_REQUEST
+    same_state(o, p, range(3))
