@@ -1,0 +1,472 @@
+"""Benchmark of the decode-step hot path of the two-pool KV cache on GB300.
+
+A step = append one new token to every request (window write, CSA / indexer
+/ HCA compression, block seals) + decode attention of the layer (indexer
+scores, top-k select, three-source split-K attention, merge), through the
+kvpool C ABI.  Default workload: the long-context configuration (8 requests
+at 1,048,576 tokens: 262,144 CSA and 8,192 HCA entries each, fp8 e4m3 cache
+with bf16 scales, 16 heads x 128, indexer 4 x 64, window 128, top_k 2048).
+
+Prints one JSON line (rank 0).  With torchrun (N > 1) every rank serves its
+own 8 requests on its own GPU (weak scaling, no data-path collective; the
+process group only carries the timing barrier and the max over ranks).
+
+  python bench.py [--steps K] [--warmup W] [--config long_context|decode_batch]
+  python bench.py --impl reference   # the CPU oracle on the same workload
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode steps/sec (tokens/s) and achieved HBM GB/s vs 8 TB/s per config"
+NOMINAL_HBM_GBS = 8000.0
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+def workload(name):
+    from heterogeneous_compressed_kv_gb300.gen import workloads as W
+    if name == "long_context":
+        w = dict(W.LONG_CONTEXT)
+        w["lengths"] = [w["length"]] * w["n_requests"]
+        return w
+    if name == "decode_batch":
+        w = dict(W.DECODE_BATCH)
+        w["lengths"] = W.uniform_lengths(w["seed"], w["n_requests"], w["len_lo"], w["len_hi"]).tolist()
+        w["chunk"] = 2048
+        return w
+    raise SystemExit(f"unknown config {name}")
+
+
+def gates(w):
+    from heterogeneous_compressed_kv_gb300 import gen
+    nl = w["n_layers"]
+    return (gen.gate_logits(w["seed"], gen.GATE_CSA, nl, w["heads"], w["m"]),
+            gen.gate_logits(w["seed"], gen.GATE_HCA, nl, w["heads"], w["m_prime"]),
+            gen.gate_logits(w["seed"], gen.GATE_IDX, nl, w["idx_heads"], w["m"]))
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (cpu_baseline and --impl reference); no CUDA in here
+# ---------------------------------------------------------------------------
+def _oracle_worker(args):
+    """Prefill one workload request into the oracle (untimed), then time
+    `steps` decode steps (append 1 token + decode_attend) of it."""
+    name, wid, steps, warm = args
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import oracle as O
+    from heterogeneous_compressed_kv_gb300 import gen
+    w = workload(name)
+    L0 = int(w["lengths"][wid])
+    total = L0 + warm + steps + 1
+    g = gates(w)
+    o = O.Oracle(m=w["m"], m_prime=w["m_prime"], n_win=w["n_win"], heads=w["heads"], head_dim=w["head_dim"],
+                 idx_heads=w["idx_heads"], idx_dim=w["idx_dim"], in_dtype=w["in_dtype"],
+                 cache_dtype=w["cache_dtype"], layer_kinds=w["layer_kinds"], max_requests=1,
+                 max_blocks=total // w["m_prime"] + 1, max_blocks_per_request=total // w["m_prime"] + 1,
+                 gate_csa=g[0], gate_hca=g[1], gate_idx=g[2])
+    _, r = o.alloc_request()
+    HD, XD = w["heads"] * w["head_dim"], w["idx_heads"] * w["idx_dim"]
+    dt = gen.OUT_F32 if w["in_dtype"] == 0 else gen.OUT_BF16
+
+    def vals(n, runs):
+        x = gen.fill_host(n, dt, w["seed"], runs)
+        return x if dt == gen.OUT_F32 else gen.bf16_bits_to_f32(x)
+
+    def toks(p0, n):
+        k = vals(n * HD, gen.token_runs(gen.K, 0, [wid], [p0], [n], HD)).reshape(1, n, HD)
+        v = vals(n * HD, gen.token_runs(gen.V, 0, [wid], [p0], [n], HD)).reshape(1, n, HD)
+        x = vals(n * XD, gen.token_runs(gen.IDXK, 0, [wid], [p0], [n], XD)).reshape(1, n, XD)
+        return k, v, x
+
+    t_setup = time.perf_counter()
+    p = 0
+    while p < L0:
+        n = min(16384, L0 - p)
+        assert o.append([r], [n], *toks(p, n)) == 0
+        p += n
+    t_setup = time.perf_counter() - t_setup
+
+    def step(s):
+        assert o.append([r], [1], *toks(L0 + s, 1)) == 0
+        q = vals(HD, gen.token_runs(gen.Q, 0, [wid], [s], [1], HD))
+        qi = vals(XD, gen.token_runs(gen.QIDX, 0, [wid], [s], [1], XD))
+        rc, out, tk = o.decode_attend(0, [r], q.reshape(1, HD), qi.reshape(1, XD), w["top_k"])
+        assert rc == 0
+
+    for s in range(warm):
+        step(s)
+    t0 = time.perf_counter()
+    for s in range(warm, warm + steps):
+        step(s)
+    return time.perf_counter() - t0, t_setup
+
+
+def start_oracle(name, n_workers, steps, warm):
+    """Spawned before any CUDA call: one oracle process per sampled request."""
+    ctx = mp.get_context("spawn")
+    pool = ctx.Pool(n_workers)
+    res = pool.map_async(_oracle_worker, [(name, i, steps, warm) for i in range(n_workers)])
+    return pool, res
+
+
+def oracle_workers(w):
+    cores = os.cpu_count() or 1
+    return max(1, min(w["n_requests"], cores - 1 if cores > 2 else 1))
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle, as it stands, on this workload.  One
+    step = one decode step (append 1 token + attend) of each sampled request,
+    the requests running in parallel processes on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = workload(args.config)
+    n = oracle_workers(w)
+    pool, res = start_oracle(args.config, n, args.steps, args.warmup)
+    out = res.get()
+    pool.close()
+    t = max(o[0] for o in out)
+    tokens = n * args.steps
+    value = tokens / t
+    line = dict(impl="reference", metric=METRIC, value=value, unit="tokens/s", n_gpus=args.gpus,
+                steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * t / args.steps, higher_is_better=True,
+                scaling="weak", vs_baseline=None, dtype="f64 attention / f32 compressor and scores",
+                data="synthetic", config=config_block(w, args),
+                cpu_baseline=dict(value=value, unit="tokens/s", cores=n, kind="oracle",
+                                  sample=f"{n} of {w['n_requests']} requests (one process each) at their full "
+                                         f"context; setup (oracle prefill) {max(o[1] for o in out):.0f} s untimed"),
+                e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line))
+
+
+def config_block(w, args):
+    c = dict(workload=w["name"], requests=w["n_requests"], heads=w["heads"], head_dim=w["head_dim"],
+             indexer=f"{w['idx_heads']}x{w['idx_dim']}", m=w["m"], m_prime=w["m_prime"], n_win=w["n_win"],
+             top_k=w["top_k"], in_dtype={0: "f32", 1: "bf16"}[w["in_dtype"]],
+             cache_dtype={0: "f32", 1: "bf16", 2: "fp8_e4m3+bf16_scale"}[w["cache_dtype"]])
+    if w["name"] == "long_context":
+        c["context"] = w["length"]
+    else:
+        c["lengths"] = f"uniform[{w['len_lo']},{w['len_hi']}] seed {w['seed']}"
+    return c
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class Clocks:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "20"], stdout=subprocess.PIPE,
+                                      stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if not self.p:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=mx, reasons=sorted(reasons), samples=len(sm))
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def traffic_record(kernel, source):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary, only if
+    the kernel source is unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except OSError:
+        return None
+    r = rec.get(kernel)
+    if not r:
+        return None
+    sha = hashlib.sha256(open(os.path.join(ROOT, source), "rb").read()).hexdigest()[:16]
+    return r["bytes_per_launch"] if r.get("source_sha") == sha else None
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="long_context", choices=["long_context", "decode_batch"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-steps", type=int, default=3)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = workload(args.config)
+
+    # the oracle baseline is spawned before the first CUDA call
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = (oracle_workers(w),) + start_oracle(args.config, oracle_workers(w), args.cpu_steps, 1)
+
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    from heterogeneous_compressed_kv_gb300 import gen
+    from heterogeneous_compressed_kv_gb300 import kvpool as K
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    B, K_, W_ = w["n_requests"], args.steps, args.warmup
+    lengths = [int(x) for x in w["lengths"]]
+    mp_ = w["m_prime"]
+    extra = 2 * (K_ + W_) + 2
+    mbpr = (max(lengths) + extra) // mp_ + 2
+    g = gates(w)
+    cfg = K.PoolConfig(m=w["m"], m_prime=mp_, n_win=w["n_win"], heads=w["heads"], head_dim=w["head_dim"],
+                       idx_heads=w["idx_heads"], idx_dim=w["idx_dim"], in_dtype=w["in_dtype"],
+                       cache_dtype=w["cache_dtype"], layer_kinds=w["layer_kinds"], max_requests=B,
+                       max_blocks=sum((L + extra) // mp_ + 1 for L in lengths), max_blocks_per_request=mbpr,
+                       max_batch=B, max_top_k=w["top_k"], gate_csa=g[0], gate_hca=g[1], gate_idx=g[2])
+    arena = torch.empty(K.required_bytes(cfg), dtype=torch.uint8, device=dev)
+    pool = K.Pool(cfg, arena, stream)
+    slots = [pool.alloc_request() for _ in range(B)]
+    wids = [rank * B + i for i in range(B)]
+    HD, XD = w["heads"] * w["head_dim"], w["idx_heads"] * w["idx_dim"]
+    tdt = torch.float32 if w["in_dtype"] == 0 else torch.bfloat16
+    gdt = gen.OUT_F32 if w["in_dtype"] == 0 else gen.OUT_BF16
+    seed = w["seed"]
+
+    # ---- untimed prefill, in chunks, inputs generated on the device ----
+    t_setup = time.perf_counter()
+    chunk = w["chunk"]
+    kbuf = torch.empty((1, B * chunk, HD), dtype=tdt, device=dev)
+    vbuf, xbuf = torch.empty_like(kbuf), torch.empty((1, B * chunk, XD), dtype=tdt, device=dev)
+    pos = [0] * B
+    while True:
+        cnt = [min(chunk, L - p) for L, p in zip(lengths, pos)]
+        if sum(cnt) == 0:
+            break
+        gen.fill_device(kbuf.data_ptr(), gdt, seed, gen.token_runs(gen.K, 0, wids, pos, cnt, HD), sp)
+        gen.fill_device(vbuf.data_ptr(), gdt, seed, gen.token_runs(gen.V, 0, wids, pos, cnt, HD), sp)
+        gen.fill_device(xbuf.data_ptr(), gdt, seed, gen.token_runs(gen.IDXK, 0, wids, pos, cnt, XD), sp)
+        pool.append(slots, cnt, kbuf, vbuf, xbuf, stream=sp)
+        pos = [p + c for p, c in zip(pos, cnt)]
+    del kbuf, vbuf, xbuf
+    torch.cuda.synchronize()
+    pool.check_device(sp)
+    t_setup = time.perf_counter() - t_setup
+
+    # ---- step inputs, resident in HBM before timing ----
+    S = 2 * (W_ + K_)  # device-timed steps then the end-to-end steps
+
+    def step_inputs(s0, n):
+        k = torch.empty((n, 1, B, HD), dtype=tdt, device=dev)
+        v, x = torch.empty_like(k), torch.empty((n, 1, B, XD), dtype=tdt, device=dev)
+        q, qi = torch.empty((n, B, HD), dtype=tdt, device=dev), torch.empty((n, B, XD), dtype=tdt, device=dev)
+        for t in range(n):
+            p = [L + s0 + t for L in lengths]
+            one = [1] * B
+            gen.fill_device(k[t].data_ptr(), gdt, seed, gen.token_runs(gen.K, 0, wids, p, one, HD), sp)
+            gen.fill_device(v[t].data_ptr(), gdt, seed, gen.token_runs(gen.V, 0, wids, p, one, HD), sp)
+            gen.fill_device(x[t].data_ptr(), gdt, seed, gen.token_runs(gen.IDXK, 0, wids, p, one, XD), sp)
+            st = [s0 + t] * B
+            gen.fill_device(q[t].data_ptr(), gdt, seed, gen.token_runs(gen.Q, 0, wids, st, one, HD), sp)
+            gen.fill_device(qi[t].data_ptr(), gdt, seed, gen.token_runs(gen.QIDX, 0, wids, st, one, XD), sp)
+        return k, v, x, q, qi
+
+    sk, sv, sx, sq, sqi = step_inputs(0, W_ + K_)
+    out = torch.empty((B, HD), dtype=torch.float32, device=dev)
+    one = [1] * B
+    top_k = w["top_k"]
+
+    def step(t, k, v, x, q, qi):
+        pool.append(slots, one, k[t], v[t], x[t], stream=sp)
+        pool.decode_attend(0, slots, q[t], qi[t], top_k, out, None, stream=sp)
+
+    for t in range(W_):
+        step(t, sk, sv, sx, sq, sqi)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    clocks = Clocks(local)
+    pool.profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.05)
+    ev0.record(stream)
+    for t in range(W_, W_ + K_):
+        step(t, sk, sv, sx, sq, sqi)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    prof = {n: pool.profile_read(i) for i, n in enumerate(K.KERNEL_NAMES)}
+    pool.profile_enable(False)
+    pool.check_device(sp)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end: pinned host inputs in, result out, every step ----
+    ek, ev_, ex, eq, eqi = step_inputs(W_ + K_, W_ + K_)
+    hk, hv, hx = ek.cpu().pin_memory(), ev_.cpu().pin_memory(), ex.cpu().pin_memory()
+    hq, hqi = eq.cpu().pin_memory(), eqi.cpu().pin_memory()
+    del ek, ev_, ex, eq, eqi
+    dk, dv, dx = (torch.empty((1, 1, B, HD), dtype=tdt, device=dev), torch.empty((1, 1, B, HD), dtype=tdt, device=dev),
+                  torch.empty((1, 1, B, XD), dtype=tdt, device=dev))
+    dq, dqi = torch.empty((1, B, HD), dtype=tdt, device=dev), torch.empty((1, B, XD), dtype=tdt, device=dev)
+    hout = torch.empty((W_ + K_, B, HD), dtype=torch.float32).pin_memory()
+
+    def e2e_step(t):
+        dk[0].copy_(hk[t], non_blocking=True)
+        dv[0].copy_(hv[t], non_blocking=True)
+        dx[0].copy_(hx[t], non_blocking=True)
+        dq[0].copy_(hq[t], non_blocking=True)
+        dqi[0].copy_(hqi[t], non_blocking=True)
+        step(0, dk, dv, dx, dq, dqi)
+        hout[t].copy_(out, non_blocking=True)
+
+    for t in range(W_):
+        e2e_step(t)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for t in range(W_, W_ + K_):
+        e2e_step(t)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = (hk[0].numel() + hv[0].numel() + hx[0].numel() + hq[0].numel() + hqi[0].numel()) * hk.element_size()
+    d2h = hout[0].numel() * 4
+
+    tokens = B * K_ * world
+    value = tokens / (ms / 1e3)
+    e2e_value = tokens / (e2e_ms / 1e3)
+    step_bytes = sum(b for (_, _, b) in prof.values()) / K_
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    # dominant kernel: the one with the most algorithmic bytes
+    dom = max(("score", "attend", "append"), key=lambda n: prof[n][2])
+    d_ms, d_n, d_b = prof[dom]
+    src = {"score": "heterogeneous_compressed_kv_gb300/csrc/kvpool_index.cu",
+           "attend": "heterogeneous_compressed_kv_gb300/csrc/kvpool_attend.cu",
+           "append": "heterogeneous_compressed_kv_gb300/csrc/kvpool_append.cu"}[dom]
+    launches_dom = d_n
+    achieved = (d_b / launches_dom) / (d_ms / launches_dom / 1e3) / 1e9 if d_ms > 0 else None
+    launches = sum(n for (_, n, _) in prof.values())
+
+    if rank != 0:
+        return
+    line = dict(metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=K_, warmup=W_,
+                ms_per_step=ms / K_, higher_is_better=True, scaling="weak", vs_baseline=None,
+                dtype="f32", data="synthetic (seeded counter generator; no dataset)",
+                config=dict(config_block(w, args), parallelism=f"replicas x{world} (requests per GPU fixed)",
+                            l2=f"inputs larger than L2: {step_bytes / 1e6:.0f} MB algorithmic per step"),
+                steps_per_s=K_ / (ms / 1e3),
+                hbm_gbs=step_bytes / (ms / K_ / 1e3) / 1e9,
+                hbm_frac_of_8tbs=step_bytes / (ms / K_ / 1e3) / 1e9 / NOMINAL_HBM_GBS,
+                hbm_frac_of_measured=step_bytes / (ms / K_ / 1e3) / 1e9 / hbm_peak,
+                kernels={n: dict(ms_per_step=pm / K_, launches=pn, gb_per_step=pb / K_ / 1e9,
+                                 gbs=(pb / (pm / 1e3) / 1e9) if pm > 0 else None)
+                         for n, (pm, pn, pb) in prof.items()},
+                roofline=dict(kernel=dom, bound="hbm", achieved=achieved, peak=hbm_peak, unit="GB/s",
+                              frac=(achieved / hbm_peak) if achieved else None,
+                              traffic=traffic_record(dom, src), peak_source=peak_kind,
+                              bytes_per_launch=d_b / launches_dom, ms_per_launch=d_ms / launches_dom),
+                e2e=dict(value=e2e_value, unit="tokens/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
+                gpu_launches=launches, setup_s=t_setup, clocks=clk)
+    if cpu is not None:
+        n_w, cpool, cres = cpu
+        try:
+            res = cres.get(timeout=900)
+            t = max(r[0] for r in res)
+            line["cpu_baseline"] = dict(value=n_w * args.cpu_steps / t, unit="tokens/s", cores=n_w, kind="oracle",
+                                        sample=f"{n_w} of {B} requests at full context, {args.cpu_steps} decode "
+                                               f"steps each, one process per request; oracle prefill "
+                                               f"{max(r[1] for r in res):.0f} s untimed")
+        except Exception as e:  # noqa: BLE001
+            line["cpu_baseline"] = dict(value=None, unit="tokens/s", cores=n_w, kind="oracle",
+                                        sample=f"not completed: {type(e).__name__}")
+        cpool.terminate()
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

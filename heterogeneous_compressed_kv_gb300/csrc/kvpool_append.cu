@@ -371,7 +371,7 @@ int append_slices(const PoolDesc& pd) {
   return chunks / 256;
 }
 
-int launch_append(const AppendParams& p, int n_layers, void* stream) {
+int launch_append(const AppendParams& p, int n_layers, void* stream, int* n_kernels) {
   if (p.n_units <= 0) return 0;
   if (p.n_slices != append_slices(p.pool)) return (int)cudaErrorInvalidValue;
   const int threads = append_threads(p.pool, p.n_slices);
@@ -389,10 +389,11 @@ int launch_append(const AppendParams& p, int n_layers, void* stream) {
       break;
     default: return (int)cudaErrorInvalidValue;
   }
+  *n_kernels += 1;
   return (int)cudaGetLastError();
 }
 
-int launch_share(const ShareParams& p, int n_layers, void* stream) {
+int launch_share(const ShareParams& p, int n_layers, void* stream, int* n_kernels) {
   if (p.w <= 0) return 0;
   const int n_slices = append_slices(p.pool);
   const int threads = append_threads(p.pool, n_slices);
@@ -408,6 +409,7 @@ int launch_share(const ShareParams& p, int n_layers, void* stream) {
     case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3: share_kernel<KVPOOL_BF16, KVPOOL_FP8_E4M3><<<grid, threads, 0, s>>>(p); break;
     default: return (int)cudaErrorInvalidValue;
   }
+  *n_kernels += 1;
   return (int)cudaGetLastError();
 }
 

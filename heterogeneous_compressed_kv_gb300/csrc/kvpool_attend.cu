@@ -281,11 +281,19 @@ int launch_attend_t(const AttendParams& p, cudaStream_t s, int e_stage, size_t s
   const int threads = p.pool.HD / 8 + 32;
   if (p.pool.head_dim == 128) {
     auto k = attend_kernel<IN, CACHE, 16>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static size_t set16 = 0;
+    if (set16 < smem) {
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      set16 = smem;
+    }
     k<<<p.total_splits, threads, smem, s>>>(p, e_stage);
   } else if (p.pool.head_dim == 64) {
     auto k = attend_kernel<IN, CACHE, 8>;
-    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static size_t set8 = 0;
+    if (set8 < smem) {
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      set8 = smem;
+    }
     k<<<p.total_splits, threads, smem, s>>>(p, e_stage);
   } else {
     return (int)cudaErrorInvalidValue;
@@ -307,11 +315,12 @@ size_t attend_smem_bytes(const PoolDesc& pd) {
 
 int attend_max_split_len() { return kMaxSplitLen; }
 
-int launch_attend(const AttendParams& p, void* stream) {
+int launch_attend(const AttendParams& p, void* stream, int* n_kernels) {
   if (p.total_splits <= 0) return 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int e_stage = attend_stage_entries(p.pool);
   const size_t smem = attend_smem_bytes(p.pool);
+  *n_kernels += 1;
   const int key = p.pool.in_dtype * 3 + p.pool.cache_dtype;
   switch (key) {
     case KVPOOL_F32 * 3 + KVPOOL_F32: return launch_attend_t<KVPOOL_F32, KVPOOL_F32>(p, s, e_stage, smem);
@@ -324,11 +333,12 @@ int launch_attend(const AttendParams& p, void* stream) {
   }
 }
 
-int launch_combine(const AttendParams& p, void* stream) {
+int launch_combine(const AttendParams& p, void* stream, int* n_kernels) {
   if (p.n <= 0) return 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   dim3 grid(p.n, p.pool.heads);
   combine_kernel<<<grid, p.pool.head_dim, 0, s>>>(p);
+  *n_kernels += 1;
   return (int)cudaGetLastError();
 }
 

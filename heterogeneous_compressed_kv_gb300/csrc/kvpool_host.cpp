@@ -196,6 +196,7 @@ struct Request {
 struct ProfileSlot {
   cudaEvent_t a, b;
   int kernel;
+  int n_kernels;
   int64_t bytes;
 };
 
@@ -242,6 +243,7 @@ struct kvpool {
     cudaEventCreate(&e);
     return e;
   }
+  // run f(&n_kernels), recording events around it when profiling
   template <class F>
   int launch(int kernel, int64_t bytes, void* stream, F&& f) {
     ProfileSlot s{};
@@ -252,9 +254,11 @@ struct kvpool {
       s.bytes = bytes;
       cudaEventRecord(s.a, (cudaStream_t)stream);
     }
-    const int rc = f();
+    int nk = 0;
+    const int rc = f(&nk);
     if (profiling) {
       cudaEventRecord(s.b, (cudaStream_t)stream);
+      s.n_kernels = nk;
       prof.push_back(s);
     }
     return rc;
@@ -265,7 +269,7 @@ struct kvpool {
       float ms = 0.f;
       cudaEventElapsedTime(&ms, s.a, s.b);
       prof_ms[s.kernel] += ms;
-      prof_launches[s.kernel] += 1;
+      prof_launches[s.kernel] += s.n_kernels;
       prof_bytes[s.kernel] += s.bytes;
       event_pool.push_back(s.a);
       event_pool.push_back(s.b);
@@ -404,7 +408,7 @@ int kvpool_share_prefix(kvpool_t* p, int32_t dst, int32_t src, int64_t n_tokens,
     sp.n_blocks = nb;
     sp.w = w;
     sp.n_tokens = n_tokens;
-    const int rc = p->launch(KVPOOL_KERNEL_APPEND, 0, stream, [&] { return launch_share(sp, p->cfg.n_layers, stream); });
+    const int rc = p->launch(KVPOOL_KERNEL_APPEND, 0, stream, [&](int* nk) { return launch_share(sp, p->cfg.n_layers, stream, nk); });
     if (rc != 0) return p->cuda_fail((cudaError_t)rc, "share_prefix launch");
   }
   d.table.assign(s.table.begin(), s.table.begin() + nb);
@@ -484,14 +488,26 @@ int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_
     ap->idx_k = d_idx_k;
     ap->rows = T;
     ap->n_slices = append_slices(p->lay.pd);
-    // algorithmic bytes: inputs read + window / entries written
-    const int64_t in_row_bytes = (2LL * p->lay.pd.HD + (any_csa ? p->lay.pd.XD : 0)) * p->lay.pd.isz;
-    int64_t bytes = T * in_row_bytes * p->cfg.n_layers;
+    // algorithmic bytes: inputs read + window tokens and new entries written
+    const PoolDesc& pd = p->lay.pd;
+    const int64_t fp8 = pd.cache_dtype == KVPOOL_FP8_E4M3 ? 1 : 0;
+    const int64_t entry_algo = 2LL * pd.HD * pd.vs + 4 * fp8, idx_algo = (int64_t)pd.XD * pd.vs + 2 * fp8;
+    int64_t bytes = 0;
+    for (int l = 0; l < p->cfg.n_layers; ++l) {
+      const LayerDesc& d = p->lay.layers[l];
+      bytes += T * 2LL * pd.HD * pd.isz + (d.has_csa ? T * (int64_t)pd.XD * pd.isz : 0);
+      for (int i = 0; i < n; ++i) {
+        const int64_t L0 = p->reqs[h_req_ids[i]].length, L1 = L0 + h_n_new[i];
+        bytes += std::min<int64_t>(h_n_new[i], W) * entry_algo;
+        if (d.has_csa) bytes += (L1 / p->cfg.m - L0 / p->cfg.m) * (entry_algo + idx_algo);
+        if (d.has_hca) bytes += (L1 / mp - L0 / mp) * entry_algo;
+      }
+    }
     for (auto* list : {&phase1, &phase2}) {
       for (size_t o = 0; o < list->size() && rc == 0; o += kMaxAppendUnits) {
         ap->n_units = (int32_t)std::min<size_t>(kMaxAppendUnits, list->size() - o);
         std::memcpy(ap->units, list->data() + o, sizeof(AppendUnit) * ap->n_units);
-        rc = p->launch(KVPOOL_KERNEL_APPEND, bytes, stream, [&] { return launch_append(*ap, p->cfg.n_layers, stream); });
+        rc = p->launch(KVPOOL_KERNEL_APPEND, bytes, stream, [&](int* nk) { return launch_append(*ap, p->cfg.n_layers, stream, nk); });
         bytes = 0;
       }
     }
@@ -557,6 +573,10 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
     P.sel_stride = p->lay.sel_stride;
     P.part_o = reinterpret_cast<float*>(p->arena + p->lay.part_o);
     P.part_ml = reinterpret_cast<float*>(p->arena + p->lay.part_ml);
+    // algorithmic bytes: codes + scales actually needed (layout padding excluded)
+    const int64_t fp8 = pd.cache_dtype == KVPOOL_FP8_E4M3 ? 1 : 0;
+    const int64_t entry_algo = 2LL * pd.HD * pd.vs + 4 * fp8;
+    const int64_t idx_algo = (int64_t)pd.XD * pd.vs + 2 * fp8;
     int64_t total_src = 0;
     int score_ctas = 0, key_ctas = 0;
     int64_t score_bytes = 0, attend_bytes = 0, out_bytes = 0;
@@ -576,12 +596,15 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
       const int nseg = (R.n_cand + CB - 1) / CB;
       if (!R.select_all && R.k > 0) {
         score_ctas += (nseg + kScoreSegsPerCta - 1) / kScoreSegsPerCta;
-        score_bytes += (int64_t)R.n_cand * (pd.idx_entry_bytes + (pd.cache_dtype == KVPOOL_FP8_E4M3 ? 2 : 0));
+        score_bytes += (int64_t)R.n_cand * idx_algo + (int64_t)nseg * 4 + (int64_t)pd.XD * pd.isz;
       }
       R.key_base = key_ctas;
-      if (Ld.has_csa) key_ctas += std::max(1, (int)((R.n_cand + kSelectKeysPerCta - 1) / kSelectKeysPerCta));
+      // emit CTAs: one per 4096 candidates; at least one when topk_out needs its -1 padding
+      if (Ld.has_csa || d_topk_out)
+        key_ctas += std::max(1, (int)((R.n_cand + kSelectKeysPerCta - 1) / kSelectKeysPerCta));
       total_src += (int64_t)R.k + R.n_hca + R.w;
-      attend_bytes += ((int64_t)R.k + R.n_hca + R.w) * pd.entry_bytes + (int64_t)R.n_hca * 4;
+      attend_bytes += ((int64_t)R.k + R.n_hca + R.w) * entry_algo + ((int64_t)R.k + R.n_hca) * 4 +
+                      (int64_t)pd.HD * pd.isz;
     }
     out_bytes = (int64_t)gn * pd.HD * 4;
     int64_t split_len = std::max<int64_t>(16, (total_src + kTargetSplits - 1) / kTargetSplits);
@@ -608,12 +631,11 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
     P.total_score_ctas = score_ctas;
     P.total_key_ctas = key_ctas;
     P.total_splits = splits;
-    if (Ld.has_csa) {
-      rc = p->launch(KVPOOL_KERNEL_SCORE, score_bytes, stream, [&] { return launch_score(P, stream); });
-      if (rc == 0) rc = p->launch(KVPOOL_KERNEL_SELECT, 0, stream, [&] { return launch_select(P, stream); });
-    }
-    if (rc == 0) rc = p->launch(KVPOOL_KERNEL_ATTEND, attend_bytes, stream, [&] { return launch_attend(P, stream); });
-    if (rc == 0) rc = p->launch(KVPOOL_KERNEL_COMBINE, out_bytes, stream, [&] { return launch_combine(P, stream); });
+    if (Ld.has_csa) rc = p->launch(KVPOOL_KERNEL_SCORE, score_bytes, stream, [&](int* nk) { return launch_score(P, stream, nk); });
+    if (rc == 0 && key_ctas > 0)
+      rc = p->launch(KVPOOL_KERNEL_SELECT, 0, stream, [&](int* nk) { return launch_select(P, stream, nk); });
+    if (rc == 0) rc = p->launch(KVPOOL_KERNEL_ATTEND, attend_bytes, stream, [&](int* nk) { return launch_attend(P, stream, nk); });
+    if (rc == 0) rc = p->launch(KVPOOL_KERNEL_COMBINE, out_bytes, stream, [&](int* nk) { return launch_combine(P, stream, nk); });
   }
   delete ap;
   if (rc == -1) return KVPOOL_ERR_INVALID_ARG;

@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(kSelThreads) select_emit_kernel(const __grid_c
 
 }  // namespace
 
-int launch_score(const AttendParams& p, void* stream) {
+int launch_score(const AttendParams& p, void* stream, int* n_kernels) {
   if (p.total_score_ctas <= 0) return 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t smem = sizeof(float) * p.pool.XD;
@@ -381,10 +381,11 @@ int launch_score(const AttendParams& p, void* stream) {
     case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3: score_kernel<KVPOOL_BF16, KVPOOL_FP8_E4M3><<<p.total_score_ctas, kScoreThreads, smem, s>>>(p); break;
     default: return (int)cudaErrorInvalidValue;
   }
+  *n_kernels += 1;
   return (int)cudaGetLastError();
 }
 
-int launch_select(const AttendParams& p, void* stream) {
+int launch_select(const AttendParams& p, void* stream, int* n_kernels) {
   if (p.total_key_ctas <= 0) return 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   bool any_radix = false;
@@ -393,8 +394,10 @@ int launch_select(const AttendParams& p, void* stream) {
     select_hist_kernel<<<p.total_key_ctas, kSelThreads, 0, s>>>(p, 2);
     select_hist_kernel<<<p.total_key_ctas, kSelThreads, 0, s>>>(p, 3);
     select_count_kernel<<<p.total_key_ctas, kSelThreads, 0, s>>>(p);
+    *n_kernels += 3;
   }
   select_emit_kernel<<<p.total_key_ctas, kSelThreads, 0, s>>>(p);
+  *n_kernels += 1;
   return (int)cudaGetLastError();
 }
 

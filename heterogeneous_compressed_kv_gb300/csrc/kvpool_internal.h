@@ -126,11 +126,12 @@ struct AttendParams {
 };
 
 // ---- launchers (implemented in the .cu files; return cudaError_t as int) --
-int launch_append(const AppendParams& p, int n_layers, void* stream);
-int launch_share(const ShareParams& p, int n_layers, void* stream);
-int launch_score(const AttendParams& p, void* stream);
-int launch_select(const AttendParams& p, void* stream);
-int launch_attend(const AttendParams& p, void* stream);
-int launch_combine(const AttendParams& p, void* stream);
+// Each launcher adds the number of kernels it launched to *n_kernels.
+int launch_append(const AppendParams& p, int n_layers, void* stream, int* n_kernels);
+int launch_share(const ShareParams& p, int n_layers, void* stream, int* n_kernels);
+int launch_score(const AttendParams& p, void* stream, int* n_kernels);
+int launch_select(const AttendParams& p, void* stream, int* n_kernels);
+int launch_attend(const AttendParams& p, void* stream, int* n_kernels);
+int launch_combine(const AttendParams& p, void* stream, int* n_kernels);
 
 }  // namespace kvp
