@@ -252,6 +252,8 @@ def main():
     ap.add_argument("--config", default="long_context", choices=["long_context", "decode_batch"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-steps", type=int, default=3)
+    ap.add_argument("--requests", type=int, default=0, help="override the request count (profiling cases)")
+    ap.add_argument("--context", type=int, default=0, help="override the long-context length (profiling cases)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -261,6 +263,12 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     w = workload(args.config)
+    if args.requests or args.context:
+        w["n_requests"] = args.requests or w["n_requests"]
+        L = args.context or w.get("length", 0)
+        w["lengths"] = [L] * w["n_requests"] if args.context else list(w["lengths"])[:w["n_requests"]]
+        w["length"] = L
+        args.no_cpu_baseline = True
 
     # the oracle baseline is spawned before the first CUDA call
     cpu = None
