@@ -17,6 +17,10 @@
 //         CTA; passes are separate launches.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <mutex>
+#include <new>
+
 #include "device_util.cuh"
 #include "kvpool_internal.h"
 
@@ -402,3 +406,115 @@ int launch_select(const AttendParams& p, void* stream, int* n_kernels) {
 }
 
 }  // namespace kvp
+
+// ===========================================================================
+// Top-k over a caller's score matrix with no allocation: the scratch (keys,
+// radix histograms, per-chunk counts, the selected list, an error word) is a
+// file-scope device array owned by this library.  The design pages have no
+// counterpart of this entry point; it exists for callers that can only hand
+// over an input and an output buffer.
+// ===========================================================================
+namespace kvp {
+namespace {
+
+constexpr size_t kStaticScratchBytes = 16u << 20;  // 16 MiB, held by every device that loads the library
+static __device__ __align__(256) uint8_t g_topk_scratch[kStaticScratchBytes];
+
+// device address of g_topk_scratch, looked up once per device
+constexpr int kMaxDevices = 64;
+static void* g_scratch_addr[kMaxDevices];
+static std::mutex g_scratch_mu;
+
+// scores -> orderable keys and the first radix histogram (top 11 bits)
+__global__ void __launch_bounds__(kSelThreads) static_keys_kernel(const __grid_constant__ AttendParams P,
+                                                                  const float* __restrict__ scores, int64_t ld) {
+  __shared__ uint32_t hist[kHistBins];
+  const int i = find_req(P, blockIdx.x, 1);
+  const AttendReq& R = P.reqs[i];
+  const int64_t k0 = (int64_t)(blockIdx.x - R.key_base) * kSelectKeysPerCta;
+  const int64_t k1 = min((int64_t)R.n_cand, k0 + kSelectKeysPerCta);
+  for (int b = threadIdx.x; b < kHistBins; b += blockDim.x) hist[b] = 0u;
+  __syncthreads();
+  uint32_t* keys = P.keys + (int64_t)i * P.key_stride;
+  for (int64_t e = k0 + threadIdx.x; e < k1; e += blockDim.x) {
+    const uint32_t key = score_key(scores[(int64_t)i * ld + e]);
+    keys[e] = key;
+    atomicAdd(&hist[key >> 21], 1u);
+  }
+  __syncthreads();
+  uint32_t* gh = P.hist + (int64_t)i * 3 * kHistBins;
+  for (int b = threadIdx.x; b < kHistBins; b += blockDim.x)
+    if (hist[b]) atomicAdd(&gh[b], hist[b]);
+}
+
+}  // namespace
+}  // namespace kvp
+
+extern "C" int kvpool_topk_static(const float* d_scores, int32_t n_rows, int32_t n_cols, int32_t top_k,
+                                  int32_t* d_topk_out, void* stream) {
+  using namespace kvp;
+  if (n_rows < 0 || n_cols < 0 || top_k < 0) return KVPOOL_ERR_INVALID_ARG;
+  if (n_rows == 0 || top_k == 0) return KVPOOL_OK;
+  if (!d_scores || !d_topk_out || n_rows > kMaxAttendReqs) return KVPOOL_ERR_INVALID_ARG;
+  // scratch plan: [error word | hist | counts | selected | keys], each 256-B aligned
+  const int64_t chunks = std::max<int64_t>(1, ((int64_t)n_cols + kSelectKeysPerCta - 1) / kSelectKeysPerCta);
+  auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
+  const int64_t off_hist = 256;
+  const int64_t off_counts = off_hist + up(4LL * n_rows * 3 * kHistBins);
+  const int64_t off_sel = off_counts + up(8LL * n_rows * chunks);
+  const int64_t off_keys = off_sel + up(4LL * n_rows * top_k);
+  const int64_t need = off_keys + up(4LL * n_rows * n_cols);
+  if (need > (int64_t)kStaticScratchBytes) return KVPOOL_ERR_INVALID_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVPOOL_ERR_CUDA;
+  uint8_t* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_topk_scratch) != cudaSuccess || !ptr) return KVPOOL_ERR_CUDA;
+      g_scratch_addr[dev] = ptr;
+    }
+    base = static_cast<uint8_t*>(g_scratch_addr[dev]);
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the error word and the histograms must start at zero; the rest is overwritten
+  if (cudaMemsetAsync(base, 0, (size_t)off_counts, s) != cudaSuccess) return KVPOOL_ERR_CUDA;
+
+  AttendParams* P = new (std::nothrow) AttendParams();
+  if (!P) return KVPOOL_ERR_INVALID_ARG;
+  P->pool.arena = base;
+  P->pool.err = 0;
+  P->topk_out = d_topk_out;
+  P->top_k = top_k;
+  P->n = n_rows;
+  P->row0 = 0;
+  P->keys = reinterpret_cast<uint32_t*>(base + off_keys);
+  P->key_stride = n_cols;
+  P->hist = reinterpret_cast<uint32_t*>(base + off_hist);
+  P->counts = reinterpret_cast<uint32_t*>(base + off_counts);
+  P->max_key_ctas = (int32_t)chunks;
+  P->sel = reinterpret_cast<int32_t*>(base + off_sel);
+  P->sel_stride = top_k;
+  for (int i = 0; i < n_rows; ++i) {
+    AttendReq& R = P->reqs[i];
+    R = AttendReq{};
+    R.n_cand = n_cols;
+    R.k = std::min(top_k, n_cols);
+    R.select_all = R.k == n_cols ? 1 : 0;
+    R.key_base = (int32_t)(i * chunks);
+  }
+  P->total_key_ctas = (int32_t)(n_rows * chunks);
+  int rc = 0;
+  bool radix = false;
+  for (int i = 0; i < n_rows; ++i) radix |= !P->reqs[i].select_all && P->reqs[i].k > 0;
+  if (radix) {
+    static_keys_kernel<<<P->total_key_ctas, kSelThreads, 0, s>>>(*P, d_scores, n_cols);
+    rc = (int)cudaGetLastError();
+  }
+  int nk = 0;
+  if (rc == 0) rc = launch_select(*P, stream, &nk);
+  delete P;
+  return rc == 0 ? KVPOOL_OK : KVPOOL_ERR_CUDA;
+}

@@ -26,7 +26,8 @@ KERNEL_NAMES = ["append", "score", "select", "attend", "combine"]
 EXPORTS = ["kvpool_required_bytes", "kvpool_create", "kvpool_destroy", "kvpool_alloc_request",
            "kvpool_free_request", "kvpool_share_prefix", "kvpool_append", "kvpool_decode_attend",
            "kvpool_request_info", "kvpool_block_refcount", "kvpool_free_block_count", "kvpool_get_layout",
-           "kvpool_check_device", "kvpool_profile_enable", "kvpool_profile_read", "kvpool_last_error"]
+           "kvpool_check_device", "kvpool_profile_enable", "kvpool_profile_read", "kvpool_last_error",
+           "kvpool_topk_static"]
 
 
 class KvpoolError(RuntimeError):
@@ -90,6 +91,7 @@ def lib():
         L.kvpool_check_device.argtypes = [vp, vp, C.POINTER(C.c_uint32)]
         L.kvpool_profile_enable.argtypes = [vp, C.c_int]
         L.kvpool_profile_read.argtypes = [vp, i32, C.POINTER(C.c_double), C.POINTER(i64), C.POINTER(i64)]
+        L.kvpool_topk_static.argtypes = [vp, i32, i32, i32, vp, vp]
         L.kvpool_last_error.restype = C.c_char_p
         L.kvpool_last_error.argtypes = [vp]
         _lib = L
@@ -139,6 +141,14 @@ class PoolConfig:
 def required_bytes(cfg: PoolConfig) -> int:
     c = cfg.to_c()
     return int(lib().kvpool_required_bytes(C.byref(c)))
+
+
+def topk_static(scores, top_k: int, out, stream=None) -> int:
+    """Top-k of each row of a [n_rows][n_cols] fp32 device tensor into
+    ``out`` ([n_rows][top_k] int32) using only the library's static device
+    scratch (no allocation); see kvpool_topk_static in include/kvpool.h."""
+    n_rows, n_cols = scores.shape
+    return lib().kvpool_topk_static(scores.data_ptr(), n_rows, n_cols, top_k, out.data_ptr(), _stream(stream))
 
 
 def _ptr(t) -> Optional[int]:

@@ -175,6 +175,28 @@ int kvpool_append(kvpool_t* pool, int32_t n, const int32_t* h_req_ids, const int
 int kvpool_decode_attend(kvpool_t* pool, int32_t layer, int32_t n, const int32_t* h_req_ids, const void* d_q,
                          const void* d_q_idx, int32_t top_k, float* d_out, int32_t* d_topk_out, void* stream);
 
+/* Top-k selection over a caller's score matrix that allocates nothing.  The
+ * design pages have no counterpart of this entry point: it is the indexer's
+ * selection step (same rule as decode_attend: k = min(top_k, n_cols) largest
+ * scores, ties to the lower index, -0 == +0, ascending indices padded with
+ * -1) offered on its own to callers that cannot allocate device memory --
+ * code that runs while a stream is being captured into a CUDA graph, or a
+ * plugin that only receives its input and output buffers from a host
+ * framework that owns every allocation.
+ * d_scores: [n_rows][n_cols] fp32 (finite) on the device; d_topk_out:
+ * [n_rows][top_k] int32.  Its scratch (sort keys, radix histograms, counts)
+ * is a file-scope 16 MiB device array in this library, present on every GPU
+ * that loads it until the process exits: n_rows <= 256 and
+ * 4*n_rows*n_cols + 4*n_rows*top_k + 24 KiB*n_rows (+ small) <= 16 MiB, else
+ * INVALID_ARG.  No cudaMalloc, cudaFree or allocating library routine is
+ * called.  The first call on a device looks up that device's address of the
+ * array (for the current device) and should come before any stream capture.
+ * Every call shares the array and clears what must start at zero; calls that
+ * overlap on the GPU (other streams, other host threads) race.  Errors:
+ * INVALID_ARG, CUDA. */
+int kvpool_topk_static(const float* d_scores, int32_t n_rows, int32_t n_cols, int32_t top_k, int32_t* d_topk_out,
+                       void* stream);
+
 /* ---- host-side queries (no device access) ---- */
 typedef struct kvpool_info {
   int64_t length;   /* tokens appended (or shared) so far */
