@@ -11,7 +11,7 @@
 // producer warp streams the split's entries through a ring of stages guarded
 // by mbarriers; consumer threads (8 dims of one head each) run an online
 // softmax in the log2 domain and write a partial (max, sum, output) per head.
-// The combine kernel merges the partials.  All waits are time-limited.
+// A merge kernel combines the partials.  All waits are time-limited.
 #include <cuda_runtime.h>
 
 #include "device_util.cuh"
@@ -127,8 +127,7 @@ __global__ void __launch_bounds__(kAttendThreadsMax) attend_kernel(const __grid_
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kStages;
-  int64_t* addr = reinterpret_cast<int64_t*>(smem + 64);
-  uint8_t* stage_mem = smem + 64 + kMaxSplitLen * 8;
+  uint8_t* stage_mem = smem + 64;
   const int64_t stage_bytes = (int64_t)e_stage * ES;
 
   if (tid == 0) {
@@ -138,38 +137,49 @@ __global__ void __launch_bounds__(kAttendThreadsMax) attend_kernel(const __grid_
     }
     mbar_fence_init();
   }
-  // zero this request's select histograms for the next call (they were
-  // consumed by the select passes that ran before this kernel)
+  // zero this request's select histogram for the next call (the select
+  // passes that read it ran before this kernel)
   if (split == 0 && P.layer.has_csa) {
-    uint32_t* gh = P.hist + (int64_t)i * 3 * kHistBins;
-    for (int b = tid; b < 3 * kHistBins; b += blockDim.x) gh[b] = 0u;
+    uint32_t* gh = P.hist + (int64_t)i * kHistBins;
+    for (int b = tid; b < kHistBins; b += blockDim.x) gh[b] = 0u;
   }
-  for (int v = tid; v < cnt; v += blockDim.x) addr[v] = source_offset(P, i, R, v0 + v);
   __syncthreads();
 
   const int n_st = (cnt + e_stage - 1) / e_stage;
   if (tid >= n_cons) {
-    // producer warp: one lane issues the bulk copies of each stage
-    if (tid == n_cons) {
-      int issued = 0;
-      bool ok = true;
-      for (int st = 0; st < n_st; ++st) {
-        const int s = st % kStages;
-        if (st >= kStages && !mbar_wait(&empty[s], ((st / kStages) - 1) & 1, pd)) {
-          ok = false;
-          break;
+    // producer warp: lanes compute source addresses 32 at a time, one batch
+    // ahead of the copies; lane 0 issues the bulk copies of each stage
+    const int lane = tid - n_cons;
+    if (lane >= 32) return;
+    int64_t cur = lane < cnt ? source_offset(P, i, R, v0 + lane) : 0;
+    int64_t nxt = 32 + lane < cnt ? source_offset(P, i, R, v0 + 32 + lane) : 0;
+    int batch = 0;
+    bool ok = true;
+    int issued = 0;
+    for (int st = 0; st < n_st; ++st) {
+      const int s = st % kStages;
+      if (lane == 0 && st >= kStages && !mbar_wait(&empty[s], ((st / kStages) - 1) & 1, pd)) ok = false;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      const int e0 = st * e_stage;
+      const int ne = min(e_stage, cnt - e0);
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(ne * ES));
+      uint8_t* dst = stage_mem + s * stage_bytes;
+      for (int e = 0; e < ne; ++e) {
+        const int x = e0 + e;
+        if ((x >> 5) != batch) {  // next batch of addresses; start the one after it
+          batch = x >> 5;
+          cur = nxt;
+          const int y = (batch + 1) * 32 + lane;
+          nxt = y < cnt ? source_offset(P, i, R, v0 + y) : 0;
         }
-        const int e0 = st * e_stage;
-        const int ne = min(e_stage, cnt - e0);
-        mbar_arrive_expect_tx(&full[s], (uint32_t)(ne * ES));
-        uint8_t* dst = stage_mem + s * stage_bytes;
-        for (int e = 0; e < ne; ++e) bulk_g2s(dst + e * ES, pd.arena + addr[e0 + e], (uint32_t)ES, &full[s]);
-        issued = st + 1;
+        const int64_t a = __shfl_sync(0xffffffffu, cur, x & 31);
+        if (lane == 0) bulk_g2s(dst + e * ES, pd.arena + a, (uint32_t)ES, &full[s]);
       }
-      if (!ok) {  // drain the copies still in flight before leaving
-        for (int st = max(0, issued - kStages); st < issued; ++st) mbar_wait(&full[st % kStages], (st / kStages) & 1, pd);
-      }
+      issued = st + 1;
     }
+    if (!ok && lane == 0)  // drain the copies still in flight before leaving
+      for (int st = max(0, issued - kStages); st < issued; ++st) mbar_wait(&full[st % kStages], (st / kStages) & 1, pd);
     return;
   }
 
@@ -247,33 +257,77 @@ __global__ void __launch_bounds__(kAttendThreadsMax) attend_kernel(const __grid_
     if ((tid & 31) == 0) mbar_arrive(&empty[s]);
   }
 
-  const int gsplit = blockIdx.x;
-  float* po = P.part_o + (int64_t)gsplit * HD + h * pd.head_dim + dd0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) po[j] = o[j];
+  float* po = P.part_o + (int64_t)blockIdx.x * HD + h * pd.head_dim + dd0;
+  reinterpret_cast<float4*>(po)[0] = make_float4(o[0], o[1], o[2], o[3]);
+  reinterpret_cast<float4*>(po)[1] = make_float4(o[4], o[5], o[6], o[7]);
   if (dd0 == 0) {
-    float* ml = P.part_ml + ((int64_t)gsplit * pd.heads + h) * 2;
+    float* ml = P.part_ml + ((int64_t)blockIdx.x * pd.heads + h) * 2;
     ml[0] = m_run;
     ml[1] = l_run;
   }
 }
 
-// grid (n requests, heads); head_dim threads
-__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ AttendParams P) {
-  const int i = blockIdx.x, h = blockIdx.y, j = threadIdx.x;
+// Merge of the split partials of one (request, head): o = sum_s 2^(m_s - M) o_s
+// / sum_s 2^(m_s - M) l_s.  Warp w takes splits w, w + 8, ...; lane l owns
+// dims [4l, 4l + 4).
+constexpr int kCombineWarps = 8;
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ AttendParams P) {
+  __shared__ float red_o[kCombineWarps][128];
+  __shared__ float red_l[kCombineWarps];
+  __shared__ float sM;
+  const int i = blockIdx.x, h = blockIdx.y;
   const AttendReq& R = P.reqs[i];
   const PoolDesc& pd = P.pool;
-  float M = -INFINITY;
-  for (int s = 0; s < R.n_split; ++s) M = fmaxf(M, P.part_ml[((int64_t)(R.split_base + s) * pd.heads + h) * 2]);
-  float den = 0.0f, num = 0.0f;
-  for (int s = 0; s < R.n_split; ++s) {
-    const int64_t gs = R.split_base + s;
-    const float* ml = P.part_ml + (gs * pd.heads + h) * 2;
-    const float w = exp2f(ml[0] - M);
-    den = fmaf(ml[1], w, den);
-    num = fmaf(P.part_o[gs * pd.HD + h * pd.head_dim + j], w, num);
+  const int d = pd.head_dim;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // M: max over the splits' running maxima of this head
+  float m = -INFINITY;
+  for (int s = threadIdx.x; s < R.n_split; s += blockDim.x)
+    m = fmaxf(m, P.part_ml[((int64_t)(R.split_base + s) * pd.heads + h) * 2]);
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) red_l[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = -INFINITY;
+    for (int w = 0; w < kCombineWarps; ++w) M = fmaxf(M, red_l[w]);
+    sM = M;
   }
-  P.out[((int64_t)(P.row0 + i) * pd.heads + h) * pd.head_dim + j] = num / den;
+  __syncthreads();
+  const float M = sM;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float l = 0.0f;
+  const bool on = 4 * lane < d;
+#pragma unroll 4
+  for (int s = warp; s < R.n_split; s += kCombineWarps) {
+    const int64_t gs = R.split_base + s;
+    const float2 ml = *reinterpret_cast<const float2*>(P.part_ml + (gs * pd.heads + h) * 2);
+    const float wgt = exp2f(ml.x - M);
+    l = fmaf(ml.y, wgt, l);
+    if (on) {
+      const float4 v = *reinterpret_cast<const float4*>(P.part_o + gs * pd.HD + h * d + 4 * lane);
+      acc.x = fmaf(v.x, wgt, acc.x);
+      acc.y = fmaf(v.y, wgt, acc.y);
+      acc.z = fmaf(v.z, wgt, acc.z);
+      acc.w = fmaf(v.w, wgt, acc.w);
+    }
+  }
+  __syncthreads();
+  if (on) {
+    red_o[warp][4 * lane] = acc.x;
+    red_o[warp][4 * lane + 1] = acc.y;
+    red_o[warp][4 * lane + 2] = acc.z;
+    red_o[warp][4 * lane + 3] = acc.w;
+  }
+  if (lane == 0) red_l[warp] = l;
+  __syncthreads();
+  if (threadIdx.x < d) {
+    float num = 0.0f, den = 0.0f;
+    for (int w = 0; w < kCombineWarps; ++w) {
+      num += red_o[w][threadIdx.x];
+      den += red_l[w];
+    }
+    P.out[((int64_t)(P.row0 + i) * pd.heads + h) * d + threadIdx.x] = num / den;
+  }
 }
 
 template <int IN, int CACHE>
@@ -310,7 +364,7 @@ int attend_stage_entries(const PoolDesc& pd) {
 }
 
 size_t attend_smem_bytes(const PoolDesc& pd) {
-  return 64 + (size_t)kMaxSplitLen * 8 + (size_t)kStages * attend_stage_entries(pd) * pd.entry_bytes;
+  return 64 + (size_t)kStages * attend_stage_entries(pd) * pd.entry_bytes;
 }
 
 int attend_max_split_len() { return kMaxSplitLen; }
@@ -336,8 +390,7 @@ int launch_attend(const AttendParams& p, void* stream, int* n_kernels) {
 int launch_combine(const AttendParams& p, void* stream, int* n_kernels) {
   if (p.n <= 0) return 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  dim3 grid(p.n, p.pool.heads);
-  combine_kernel<<<grid, p.pool.head_dim, 0, s>>>(p);
+  combine_kernel<<<dim3(p.n, p.pool.heads), kCombineWarps * 32, 0, s>>>(p);
   *n_kernels += 1;
   return (int)cudaGetLastError();
 }

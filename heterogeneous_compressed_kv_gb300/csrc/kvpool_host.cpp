@@ -34,7 +34,8 @@ using namespace kvp;
 namespace {
 
 constexpr int kMaxSplits = 4096;
-constexpr int kTargetSplits = 4 * 152;  // CTAs of the attention kernel per launch (2 per SM, 2 waves)
+constexpr int kTargetSplits = 2 * 152;  // CTAs of the attention kernel per launch (2 per SM, one wave)
+constexpr int kScoreCtas = 152;         // CTAs of the score kernel per launch (1 per SM, one wave)
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int value_bytes(int dtype) { return dtype == KVPOOL_F32 ? 4 : dtype == KVPOOL_BF16 ? 2 : 1; }
@@ -44,7 +45,7 @@ bool kind_has_hca(int k) { return k == KVPOOL_HCA || k == KVPOOL_CSA_HCA; }
 struct Layout {
   PoolDesc pd;
   LayerDesc layers[kMaxLayers];
-  int64_t hist, keys, counts, sel, part_o, part_ml;
+  int64_t hist, sync, thr, keys, cand, counts, sel, part_o, part_ml;
   int64_t key_stride;
   int32_t max_key_ctas, sel_stride, n_attend_rows;
   int64_t total;
@@ -153,10 +154,18 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
   L.key_stride = (int64_t)(c->max_blocks_per_request + 1) * CB;
   L.max_key_ctas = (int32_t)((L.key_stride + kSelectKeysPerCta - 1) / kSelectKeysPerCta);
   L.sel_stride = std::max(1, c->max_top_k);
+  if (L.max_key_ctas > kMaxKeyCtasPerReq) return "max_blocks_per_request too large for the top-k select";
+  // zero-initialised part: histograms and sync counters
   L.hist = cur;
-  cur = round_up(cur + 4LL * L.n_attend_rows * 3 * kHistBins, 256);
+  cur = round_up(cur + 4LL * L.n_attend_rows * kHistBins, 256);
+  L.sync = cur;
+  cur = round_up(cur + 16LL * L.n_attend_rows, 256);
+  L.thr = cur;
+  cur = round_up(cur + 8LL * L.n_attend_rows, 256);
   L.keys = cur;
   cur = round_up(cur + 4LL * L.n_attend_rows * L.key_stride, 256);
+  L.cand = cur;
+  cur = round_up(cur + 8LL * L.n_attend_rows * L.key_stride, 256);
   L.counts = cur;
   cur = round_up(cur + 8LL * L.n_attend_rows * L.max_key_ctas, 256);
   L.sel = cur;
@@ -332,7 +341,7 @@ int kvpool_create(const kvpool_config* cfg, void* d_arena, size_t arena_bytes, v
     }
     // error word and select histograms start at zero
     cudaError_t e = cudaMemsetAsync(p->arena + L.pd.err, 0, 256, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(p->arena + L.hist, 0, (size_t)(L.keys - L.hist), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p->arena + L.hist, 0, (size_t)(L.thr - L.hist), s);
     if (e != cudaSuccess) { int rc = p->cuda_fail(e, "arena init"); delete p; return rc; }
   }
   *out = p;
@@ -570,6 +579,9 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
     P.counts = reinterpret_cast<uint32_t*>(p->arena + p->lay.counts);
     P.max_key_ctas = p->lay.max_key_ctas;
     P.sel = reinterpret_cast<int32_t*>(p->arena + p->lay.sel);
+    P.cand = reinterpret_cast<uint2*>(p->arena + p->lay.cand);
+    P.sync = reinterpret_cast<uint32_t*>(p->arena + p->lay.sync);
+    P.thr = reinterpret_cast<uint32_t*>(p->arena + p->lay.thr);
     P.sel_stride = p->lay.sel_stride;
     P.part_o = reinterpret_cast<float*>(p->arena + p->lay.part_o);
     P.part_ml = reinterpret_cast<float*>(p->arena + p->lay.part_ml);
@@ -577,9 +589,16 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
     const int64_t fp8 = pd.cache_dtype == KVPOOL_FP8_E4M3 ? 1 : 0;
     const int64_t entry_algo = 2LL * pd.HD * pd.vs + 4 * fp8;
     const int64_t idx_algo = (int64_t)pd.XD * pd.vs + 2 * fp8;
-    int64_t total_src = 0;
+    int64_t total_src = 0, total_segs = 0;
     int score_ctas = 0, key_ctas = 0;
     int64_t score_bytes = 0, attend_bytes = 0, out_bytes = 0;
+    for (int i = 0; i < gn; ++i) {
+      const Request& q = p->reqs[h_req_ids[g0 + i]];
+      const int32_t n_cand = Ld.has_csa ? (int32_t)(q.length / p->cfg.m) : 0;
+      const int32_t k = std::min(top_k, n_cand);
+      if (k != n_cand && k > 0) total_segs += (n_cand + CB - 1) / CB;
+    }
+    P.segs_per_cta = (int32_t)std::min<int64_t>(4096, std::max<int64_t>(8, (total_segs + kScoreCtas - 1) / kScoreCtas));
     for (int i = 0; i < gn; ++i) {
       const Request& q = p->reqs[h_req_ids[g0 + i]];
       AttendReq& R = P.reqs[i];
@@ -595,11 +614,11 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
       R.score_base = score_ctas;
       const int nseg = (R.n_cand + CB - 1) / CB;
       if (!R.select_all && R.k > 0) {
-        score_ctas += (nseg + kScoreSegsPerCta - 1) / kScoreSegsPerCta;
+        score_ctas += (nseg + P.segs_per_cta - 1) / P.segs_per_cta;
         score_bytes += (int64_t)R.n_cand * idx_algo + (int64_t)nseg * 4 + (int64_t)pd.XD * pd.isz;
       }
       R.key_base = key_ctas;
-      // emit CTAs: one per 4096 candidates; at least one when topk_out needs its -1 padding
+      // select CTAs: one per 4096 candidates; at least one when topk_out needs its -1 padding
       if (Ld.has_csa || d_topk_out)
         key_ctas += std::max(1, (int)((R.n_cand + kSelectKeysPerCta - 1) / kSelectKeysPerCta));
       total_src += (int64_t)R.k + R.n_hca + R.w;

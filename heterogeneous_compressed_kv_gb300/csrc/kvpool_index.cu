@@ -15,6 +15,7 @@
 //         pass and an emit pass with ordered block scans then write the
 //         selected indices in ascending order.  No pass waits on another
 //         CTA; passes are separate launches.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -40,6 +41,8 @@ __device__ __forceinline__ int find_req(const AttendParams& P, int cta, int whic
   return lo;
 }
 
+// One 16-byte chunk of an indexer key folded into the score chain, in order;
+// q points at the chunk's query values in shared memory (16-byte aligned).
 template <int CACHE>
 struct IdxChunk;
 
@@ -47,10 +50,11 @@ template <>
 struct IdxChunk<KVPOOL_F32> {
   static constexpr int kVals = 4;
   __device__ static float chain(const uint4& c, const float* q, float acc) {
-    acc = __fmaf_rn(q[0], __uint_as_float(c.x), acc);
-    acc = __fmaf_rn(q[1], __uint_as_float(c.y), acc);
-    acc = __fmaf_rn(q[2], __uint_as_float(c.z), acc);
-    acc = __fmaf_rn(q[3], __uint_as_float(c.w), acc);
+    const float4 a = *reinterpret_cast<const float4*>(q);
+    acc = __fmaf_rn(a.x, __uint_as_float(c.x), acc);
+    acc = __fmaf_rn(a.y, __uint_as_float(c.y), acc);
+    acc = __fmaf_rn(a.z, __uint_as_float(c.z), acc);
+    acc = __fmaf_rn(a.w, __uint_as_float(c.w), acc);
     return acc;
   }
 };
@@ -58,11 +62,13 @@ template <>
 struct IdxChunk<KVPOOL_BF16> {
   static constexpr int kVals = 8;
   __device__ static float chain(const uint4& c, const float* q, float acc) {
+    const float4 a = *reinterpret_cast<const float4*>(q), b = *reinterpret_cast<const float4*>(q + 4);
+    const float qq[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      acc = __fmaf_rn(q[2 * i], bf16_bits_to_f32(w[i] & 0xFFFFu), acc);
-      acc = __fmaf_rn(q[2 * i + 1], bf16_bits_to_f32(w[i] >> 16), acc);
+      acc = __fmaf_rn(qq[2 * i], bf16_bits_to_f32(w[i] & 0xFFFFu), acc);
+      acc = __fmaf_rn(qq[2 * i + 1], bf16_bits_to_f32(w[i] >> 16), acc);
     }
     return acc;
   }
@@ -74,84 +80,252 @@ struct IdxChunk<KVPOOL_FP8_E4M3> {
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
+      const float4 qq = *reinterpret_cast<const float4*>(q + 4 * i);
       const float2 a = e4m3x2_to_f32x2((uint16_t)(w[i] & 0xFFFFu));
       const float2 b = e4m3x2_to_f32x2((uint16_t)(w[i] >> 16));
-      acc = __fmaf_rn(q[4 * i + 0], a.x, acc);
-      acc = __fmaf_rn(q[4 * i + 1], a.y, acc);
-      acc = __fmaf_rn(q[4 * i + 2], b.x, acc);
-      acc = __fmaf_rn(q[4 * i + 3], b.y, acc);
+      acc = __fmaf_rn(qq.x, a.x, acc);
+      acc = __fmaf_rn(qq.y, a.y, acc);
+      acc = __fmaf_rn(qq.z, b.x, acc);
+      acc = __fmaf_rn(qq.w, b.y, acc);
     }
     return acc;
   }
 };
 
-constexpr int kScoreThreads = 256;
-constexpr int kChunkBatch = 8;  // 16-byte chunks loaded together per lane
+// Fast chains: the same fixed-order fp32 chain with the products taken by the
+// mixed-precision FMA (f16 x f16 + f32 or bf16 x bf16 + f32; a product of two
+// f16 or two bf16 values is exact in fp32 and the FMA rounds once, so every
+// step equals fmaf on the widened operands).  qh holds the query as f16 (fp8
+// keys, which convert exactly to f16) or bf16 (bf16 keys) pairs.
+__device__ __forceinline__ float fma_f16(uint16_t a, uint16_t b, float c) {
+  float d;
+  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_bf16(uint16_t a, uint16_t b, float c) {
+  float d;
+  asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(two));
+  return h;
+}
+
+template <int CACHE>
+struct IdxChunkFast;
+template <>
+struct IdxChunkFast<KVPOOL_FP8_E4M3> {  // 16 keys per chunk, q as 16 f16
+  __device__ static float chain(const uint4& c, const uint32_t* qh, float acc) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    const uint4 qa = *reinterpret_cast<const uint4*>(qh), qb = *reinterpret_cast<const uint4*>(qh + 4);
+    const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t a = e4m3x2_to_f16x2((uint16_t)(w[i] & 0xFFFFu));
+      const uint32_t b = e4m3x2_to_f16x2((uint16_t)(w[i] >> 16));
+      acc = fma_f16((uint16_t)(a & 0xFFFFu), (uint16_t)(q[2 * i] & 0xFFFFu), acc);
+      acc = fma_f16((uint16_t)(a >> 16), (uint16_t)(q[2 * i] >> 16), acc);
+      acc = fma_f16((uint16_t)(b & 0xFFFFu), (uint16_t)(q[2 * i + 1] & 0xFFFFu), acc);
+      acc = fma_f16((uint16_t)(b >> 16), (uint16_t)(q[2 * i + 1] >> 16), acc);
+    }
+    return acc;
+  }
+};
+template <>
+struct IdxChunkFast<KVPOOL_BF16> {  // 8 keys per chunk, q as 8 bf16
+  __device__ static float chain(const uint4& c, const uint32_t* qh, float acc) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    const uint4 qa = *reinterpret_cast<const uint4*>(qh);
+    const uint32_t q[4] = {qa.x, qa.y, qa.z, qa.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc = fma_bf16((uint16_t)(w[i] & 0xFFFFu), (uint16_t)(q[i] & 0xFFFFu), acc);
+      acc = fma_bf16((uint16_t)(w[i] >> 16), (uint16_t)(q[i] >> 16), acc);
+    }
+    return acc;
+  }
+};
+template <>
+struct IdxChunkFast<KVPOOL_F32> {  // unused: fp32 keys take the fp32 chain
+  __device__ static float chain(const uint4&, const uint32_t*, float acc) { return acc; }
+};
+
+// ---------------------------------------------------------------------------
+// score kernel.  Every warp streams its own blocks: lane 0 issues a 1-D bulk
+// copy of a block's indexer section (keys + fp8 scales, contiguous) into one
+// of the warp's R shared-memory slots; the warp waits on that slot's
+// mbarrier, copies its keys into registers (lane e = entry e), refills the
+// slot with the warp's next-but-(R-1) block, and runs the chains.  Warp w of
+// a CTA takes the CTA's blocks w, w + W, w + 2W, ...; a slot's barrier is only
+// waited on by its own warp, in order, so every parity wait is exact.
+// ---------------------------------------------------------------------------
+constexpr int kScoreWarps = 8;
+constexpr int kScoreThreads = kScoreWarps * 32;
+constexpr int kScoreMaxRing = 3;                      // slots per warp
+constexpr int kScoreMaxSlots = kScoreWarps * kScoreMaxRing;
+constexpr int kScoreStageBudget = 200 * 1024;         // shared memory for slots (1 CTA per SM)
 
 template <int IN, int CACHE>
-__global__ void __launch_bounds__(kScoreThreads) score_kernel(const __grid_constant__ AttendParams P) {
-  extern __shared__ float q_sh[];  // [XD] fp32 indexer query
-  __shared__ uint32_t hist[kHistBins];
+__global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(const __grid_constant__ AttendParams P, int stage_bytes,
+                                                                 int ring, int stage_off) {
+  extern __shared__ __align__(128) uint8_t sm[];
   const PoolDesc& pd = P.pool;
   const LayerDesc& L = P.layer;
+  const int XD = pd.XD;
+  constexpr int CW = kScoreWarps;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm);
+  float* q_sh = reinterpret_cast<float*>(sm + 8 * kScoreMaxSlots);
+  uint16_t* qh_sh = reinterpret_cast<uint16_t*>(q_sh + XD);  // q as f16 (fp8 keys) or bf16 (bf16 keys)
+  uint32_t* hist = reinterpret_cast<uint32_t*>(qh_sh + XD);
+  uint8_t* slots = sm + stage_off;
+
   const int i = find_req(P, blockIdx.x, 0);
   const AttendReq& R = P.reqs[i];
   const int CB = pd.csa_per_block;
   const int nseg = (R.n_cand + CB - 1) / CB;
-  const int seg0 = (blockIdx.x - R.score_base) * kScoreSegsPerCta;
-  const int seg1 = min(nseg, seg0 + kScoreSegsPerCta);
+  const int seg_begin = (blockIdx.x - R.score_base) * P.segs_per_cta;
+  const int seg_end = min(nseg, seg_begin + P.segs_per_cta);
+  const int n_st = max(0, seg_end - seg_begin);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  for (int b = threadIdx.x; b < kHistBins; b += blockDim.x) hist[b] = 0u;
-  const int XD = pd.XD;
-  for (int v = threadIdx.x; v < XD; v += blockDim.x) {
-    const int64_t row = (int64_t)(P.row0 + i) * XD + v;
-    q_sh[v] = IN == KVPOOL_F32 ? reinterpret_cast<const float*>(P.q_idx)[row]
-                               : bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(P.q_idx)[row]);
+  if (tid == 0) {
+    for (int s = 0; s < CW * ring; ++s) mbar_init(&full[s], 1);
+    mbar_fence_init();
   }
-  __syncthreads();
+  for (int b = tid; b < kHistBins; b += blockDim.x) hist[b] = 0u;
+  // the fast chain needs the query exactly in the keys' 16-bit format
+  int exact = CACHE != KVPOOL_F32;
+  for (int v = tid; v < XD; v += blockDim.x) {
+    const int64_t row = (int64_t)(P.row0 + i) * XD + v;
+    const float qv = IN == KVPOOL_F32 ? reinterpret_cast<const float*>(P.q_idx)[row]
+                                      : bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(P.q_idx)[row]);
+    q_sh[v] = qv;
+    if (CACHE == KVPOOL_FP8_E4M3) {
+      const __half hq = __float2half_rn(qv);
+      qh_sh[v] = __half_as_ushort(hq);
+      exact &= __half2float(hq) == qv;
+    } else if (CACHE == KVPOOL_BF16) {
+      const uint16_t bq = f32_to_bf16_bits(qv);
+      qh_sh[v] = bq;
+      exact &= bf16_bits_to_f32(bq) == qv;
+    }
+  }
+  const bool fast = __syncthreads_and(exact) != 0;
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // this warp's blocks: st = warp + j * CW, j = 0 .. mine-1
+  const int mine = warp < n_st ? (n_st - 1 - warp) / CW + 1 : 0;
+  const int32_t* table = reinterpret_cast<const int32_t*>(pd.arena + pd.table) + (int64_t)R.slot * pd.max_bpr;
+  const int32_t staging = pd.staging_base + R.slot;
+  auto block_id = [&](int jj) -> int32_t {  // id of this warp's jj-th block (any lane)
+    const int seg = seg_begin + warp + jj * CW;
+    if (jj >= mine || seg >= R.n_sealed) return staging;
+    const int32_t bid = table[seg];
+    if (bid < 0 || bid >= pd.max_blocks) {
+      flag_error(pd, kErrBadBlock);
+      return staging;  // read something valid; the error word reports it
+    }
+    return bid;
+  };
+  // block ids 32 at a time, one batch ahead of their use (lane x holds block
+  // batch*32 + x); requests come in increasing order
+  int32_t id_cur = block_id(lane), id_nxt = block_id(32 + lane);
+  int id_batch = 0;
+  auto src_of = [&](int jj) -> const uint8_t* {  // all lanes call it
+    while ((jj >> 5) > id_batch) {
+      ++id_batch;
+      id_cur = id_nxt;
+      id_nxt = block_id((id_batch + 1) * 32 + lane);
+    }
+    const int32_t bid = __shfl_sync(0xffffffffu, id_cur, jj & 31);
+    return pd.arena + L.block_pool + (int64_t)bid * L.block_bytes + L.idx_off;
+  };
+  uint64_t* my_full = full + warp * ring;
+  uint8_t* my_slots = slots + (int64_t)warp * ring * stage_bytes;
+  for (int jj = 0; jj < mine && jj < ring; ++jj) {
+    const uint8_t* src = src_of(jj);
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&my_full[jj], (uint32_t)stage_bytes);
+      bulk_g2s(my_slots + (int64_t)jj * stage_bytes, src, (uint32_t)stage_bytes, &my_full[jj]);
+    }
+  }
+
   constexpr int V = IdxChunk<CACHE>::kVals;
   const int n_chunks = pd.idx_chunks;
-  const int32_t* table = reinterpret_cast<const int32_t*>(pd.arena + pd.table) + (int64_t)R.slot * pd.max_bpr;
+  const int key_bytes = CB * (int)pd.idx_entry_bytes;
   uint32_t* keys = P.keys + (int64_t)i * P.key_stride;
-
-  for (int seg = seg0 + warp; seg < seg1; seg += kScoreThreads / 32) {
-    int32_t bid = seg < R.n_sealed ? table[seg] : pd.staging_base + R.slot;
-    if (seg < R.n_sealed && (bid < 0 || bid >= pd.max_blocks)) {
-      if (lane == 0) flag_error(pd, kErrBadBlock);
-      continue;
-    }
-    const uint8_t* sec = pd.arena + L.block_pool + (int64_t)bid * L.block_bytes;
-    const uint8_t* kbase = sec + L.idx_off;
-    for (int e0 = 0; e0 < CB; e0 += 32) {
-      const int e = e0 + lane;
-      const int64_t E = (int64_t)seg * CB + e;
-      const bool valid = e < CB && E < R.n_cand;
-      float acc = 0.0f;
+  const uint32_t* qh = reinterpret_cast<const uint32_t*>(qh_sh);
+  int j = 0;
+  for (; j < mine; ++j) {
+    const int slot = j % ring;
+    if (!mbar_wait(&my_full[slot], (j / ring) & 1, pd)) break;
+    const uint8_t* stg = my_slots + (int64_t)slot * stage_bytes;
+    const int64_t E = (int64_t)(seg_begin + warp + j * CW) * CB + lane;
+    const bool valid = lane < CB && E < R.n_cand;
+    float acc = 0.0f;
+    float scale = 1.0f;
+    if (n_chunks <= 16) {
+      // the lane's key into registers, then the slot takes the next block
+      uint4 ch[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (c < n_chunks && valid) ch[c] = *reinterpret_cast<const uint4*>(stg + ((int64_t)c * CB + lane) * 16);
+      if (CACHE == KVPOOL_FP8_E4M3 && valid)
+        scale = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(stg + key_bytes + 2 * lane));
+      __syncwarp();
+      if (j + ring < mine) {
+        const uint8_t* src = src_of(j + ring);
+        if (lane == 0) {
+          fence_proxy_async();  // the warp's reads of the slot come before the copy that overwrites it
+          mbar_arrive_expect_tx(&my_full[slot], (uint32_t)stage_bytes);
+          bulk_g2s(my_slots + (int64_t)slot * stage_bytes, src, (uint32_t)stage_bytes, &my_full[slot]);
+        }
+      }
       if (valid) {
-        for (int c0 = 0; c0 < n_chunks; c0 += kChunkBatch) {
-          uint4 ch[kChunkBatch];
+        if (fast) {
 #pragma unroll
-          for (int b = 0; b < kChunkBatch; ++b)
-            if (c0 + b < n_chunks) ch[b] = ld_stream16(kbase + ((int64_t)(c0 + b) * CB + e) * 16);
+          for (int c = 0; c < 16; ++c)
+            if (c < n_chunks) acc = IdxChunkFast<CACHE>::chain(ch[c], qh + c * (V / 2), acc);
+        } else {
 #pragma unroll
-          for (int b = 0; b < kChunkBatch; ++b)
-            if (c0 + b < n_chunks) acc = IdxChunk<CACHE>::chain(ch[b], q_sh + (c0 + b) * V, acc);
+          for (int c = 0; c < 16; ++c)
+            if (c < n_chunks) acc = IdxChunk<CACHE>::chain(ch[c], q_sh + c * V, acc);
         }
-        if constexpr (CACHE == KVPOOL_FP8_E4M3) {
-          const uint16_t sb = *reinterpret_cast<const uint16_t*>(sec + L.idx_scale_off + 2 * e);
-          acc = __fmul_rn(acc, bf16_bits_to_f32(sb));
+      }
+    } else {
+      if (valid) {
+        for (int c = 0; c < n_chunks; ++c) {
+          const uint4 chk = *reinterpret_cast<const uint4*>(stg + ((int64_t)c * CB + lane) * 16);
+          acc = fast ? IdxChunkFast<CACHE>::chain(chk, qh + c * (V / 2), acc)
+                     : IdxChunk<CACHE>::chain(chk, q_sh + c * V, acc);
         }
-        const uint32_t key = score_key(acc);
-        keys[E] = key;
-        atomicAdd(&hist[key >> 21], 1u);
+        if (CACHE == KVPOOL_FP8_E4M3)
+          scale = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(stg + key_bytes + 2 * lane));
+      }
+      __syncwarp();
+      if (j + ring < mine) {
+        const uint8_t* src = src_of(j + ring);
+        if (lane == 0) {
+          fence_proxy_async();  // the warp's reads of the slot come before the copy that overwrites it
+          mbar_arrive_expect_tx(&my_full[slot], (uint32_t)stage_bytes);
+          bulk_g2s(my_slots + (int64_t)slot * stage_bytes, src, (uint32_t)stage_bytes, &my_full[slot]);
+        }
       }
     }
+    if (valid) {
+      if constexpr (CACHE == KVPOOL_FP8_E4M3) acc = __fmul_rn(acc, scale);
+      const uint32_t key = score_key(acc);
+      keys[E] = key;
+      atomicAdd(&hist[key >> 21], 1u);
+    }
+  }
+  if (j < mine && lane == 0) {  // a wait gave up: drain this warp's copies still in flight
+    for (int jj = j; jj < mine && jj < j + ring; ++jj) mbar_wait(&my_full[jj % ring], (jj / ring) & 1, pd);
   }
   __syncthreads();
-  uint32_t* gh = P.hist + (int64_t)i * 3 * kHistBins;
-  for (int b = threadIdx.x; b < kHistBins; b += blockDim.x)
+  uint32_t* gh = P.hist + (int64_t)i * kHistBins;
+  for (int b = tid; b < kHistBins; b += blockDim.x)
     if (hist[b]) atomicAdd(&gh[b], hist[b]);
 }
 
@@ -179,8 +353,8 @@ __device__ void find_digit(const uint32_t* h, int nbins, uint32_t k, uint32_t* s
     sh[t] += add;
     __syncthreads();
   }
-  const uint32_t incl = sh[t];          // keys in bins >= t*per
-  const uint32_t above = incl - own;    // keys in bins >= (t+1)*per
+  const uint32_t incl = sh[t];        // keys in bins >= t*per
+  const uint32_t above = incl - own;  // keys in bins >= (t+1)*per
   if (above < k && incl >= k) {
     uint32_t acc = above;
     for (int b = per - 1; b >= 0; --b) {
@@ -196,91 +370,103 @@ __device__ void find_digit(const uint32_t* h, int nbins, uint32_t k, uint32_t* s
   __syncthreads();
 }
 
-struct Thresh {
-  uint32_t T, need;
-};
-
-// Recompute the select state from the global histograms of request i.
-// level: how many radix levels are complete (1, 2 or 3).
-__device__ void select_state(const AttendParams& P, int i, int level, uint32_t* sh, uint32_t* out /*[4]*/) {
-  const AttendReq& R = P.reqs[i];
-  const uint32_t* gh = P.hist + (int64_t)i * 3 * kHistBins;
-  __shared__ uint32_t st[6];
-  if (threadIdx.x == 0) st[0] = st[1] = st[2] = st[3] = st[4] = st[5] = 0;
-  __syncthreads();
-  find_digit(gh, kHistBins, (uint32_t)R.k, sh, &st[0], &st[1]);
-  if (level >= 2) find_digit(gh + kHistBins, kHistBins, st[1], sh, &st[2], &st[3]);
-  if (level >= 3) find_digit(gh + 2 * kHistBins, 1024, st[3], sh, &st[4], &st[5]);
-  out[0] = st[0];
-  out[1] = st[2];
-  out[2] = st[4];
-  out[3] = level == 1 ? st[1] : level == 2 ? st[3] : st[5];
-  __syncthreads();
-}
-
-__global__ void __launch_bounds__(kSelThreads) select_hist_kernel(const __grid_constant__ AttendParams P, int level) {
+// Pass 1 of the select (one CTA per 4096 keys of a request): the first digit
+// d1 of the k-th largest key follows from the score histogram; keys above
+// bucket d1 are surely selected (counted per chunk), keys inside it become
+// candidates.  The last CTA of the request then finds the exact threshold T
+// among the candidates (two more radix digits) and how many keys equal to T
+// are taken, and completes the per-chunk counts.  No CTA waits on another:
+// the last one is found with an atomic counter after a fence.
+__global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __grid_constant__ AttendParams P) {
   __shared__ uint32_t sh[kSelThreads];
-  __shared__ uint32_t hist[kHistBins];
-  const int i = find_req(P, blockIdx.x, 1);
-  const AttendReq& R = P.reqs[i];
-  if (R.select_all || R.k == 0) return;
-  const int64_t k0 = (int64_t)(blockIdx.x - R.key_base) * kSelectKeysPerCta;
-  if (k0 >= R.n_cand) return;
-  const int64_t k1 = min((int64_t)R.n_cand, k0 + kSelectKeysPerCta);
-  uint32_t s[4];
-  select_state(P, i, level - 1, sh, s);
-  for (int b = threadIdx.x; b < kHistBins; b += blockDim.x) hist[b] = 0u;
-  __syncthreads();
-  const uint32_t* keys = P.keys + (int64_t)i * P.key_stride;
-  for (int64_t e = k0 + threadIdx.x; e < k1; e += blockDim.x) {
-    const uint32_t key = keys[e];
-    if (level == 2) {
-      if ((key >> 21) == s[0]) atomicAdd(&hist[(key >> 10) & 2047u], 1u);
-    } else {
-      if ((key >> 10) == ((s[0] << 11) | s[1])) atomicAdd(&hist[key & 1023u], 1u);
-    }
-  }
-  __syncthreads();
-  uint32_t* gh = P.hist + (int64_t)i * 3 * kHistBins + (level - 1) * kHistBins;
-  const int nb = level == 2 ? kHistBins : 1024;
-  for (int b = threadIdx.x; b < nb; b += blockDim.x)
-    if (hist[b]) atomicAdd(&gh[b], hist[b]);
-}
-
-__device__ __forceinline__ Thresh final_thresh(const AttendParams& P, int i, uint32_t* sh) {
-  uint32_t s[4];
-  select_state(P, i, 3, sh, s);
-  return Thresh{(s[0] << 21) | (s[1] << 10) | s[2], s[3]};
-}
-
-// counts[i][chunk] = (keys > T, keys == T) in the chunk
-__global__ void __launch_bounds__(kSelThreads) select_count_kernel(const __grid_constant__ AttendParams P) {
-  __shared__ uint32_t sh[kSelThreads];
-  __shared__ uint32_t red[2];
+  __shared__ uint32_t st[8];
+  __shared__ uint32_t h2[kHistBins];
+  __shared__ uint32_t cgt[kMaxKeyCtasPerReq], ceq[kMaxKeyCtasPerReq];
+  __shared__ int is_last;
   const int i = find_req(P, blockIdx.x, 1);
   const AttendReq& R = P.reqs[i];
   if (R.select_all || R.k == 0) return;
   const int chunk = blockIdx.x - R.key_base;
+  const int n_chunks = (R.n_cand + kSelectKeysPerCta - 1) / kSelectKeysPerCta;
   const int64_t k0 = (int64_t)chunk * kSelectKeysPerCta;
   if (k0 >= R.n_cand) return;
-  const int64_t k1 = min((int64_t)R.n_cand, k0 + kSelectKeysPerCta);
-  const Thresh th = final_thresh(P, i, sh);
-  if (threadIdx.x == 0) red[0] = red[1] = 0;
-  __syncthreads();
+  const int64_t kend = min((int64_t)R.n_cand, k0 + kSelectKeysPerCta);
+  uint32_t* sync = P.sync + (int64_t)i * 4;
+  uint2* cand = P.cand + (int64_t)i * P.key_stride;
   const uint32_t* keys = P.keys + (int64_t)i * P.key_stride;
-  uint32_t gt = 0, eq = 0;
-  for (int64_t e = k0 + threadIdx.x; e < k1; e += blockDim.x) {
-    const uint32_t key = keys[e];
-    gt += key > th.T;
-    eq += key == th.T;
+  const int tid = threadIdx.x, lane = tid & 31;
+
+  find_digit(P.hist + (int64_t)i * kHistBins, kHistBins, (uint32_t)R.k, sh, &st[0], &st[1]);
+  const uint32_t d1 = st[0], k1 = st[1];
+  uint32_t gt = 0;
+  for (int64_t base = k0; base < kend; base += kSelThreads) {
+    const int64_t e = base + tid;
+    const bool in = e < kend;
+    const uint32_t key = in ? keys[e] : 0u;
+    gt += (in && (key >> 21) > d1) ? 1u : 0u;
+    const bool is_c = in && (key >> 21) == d1;
+    const unsigned mask = __ballot_sync(0xffffffffu, is_c);
+    if (mask) {
+      const int leader = __ffs(mask) - 1;
+      uint32_t pos = 0;
+      if (lane == leader) pos = atomicAdd(&sync[0], (uint32_t)__popc(mask));
+      pos = __shfl_sync(0xffffffffu, pos, leader);
+      if (is_c) cand[pos + __popc(mask & ((1u << lane) - 1u))] = make_uint2(key, (uint32_t)e);
+    }
   }
-  atomicAdd(&red[0], gt);
-  atomicAdd(&red[1], eq);
+  // chunk total of surely-selected keys
+  for (int o = 16; o > 0; o >>= 1) gt += __shfl_xor_sync(0xffffffffu, gt, o);
+  if (tid == 0) st[2] = 0;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t* c = P.counts + ((int64_t)i * P.max_key_ctas + chunk) * 2;
-    c[0] = red[0];
-    c[1] = red[1];
+  if (lane == 0) atomicAdd(&st[2], gt);
+  __syncthreads();
+  uint32_t* cnt = P.counts + ((int64_t)i * P.max_key_ctas) * 2;
+  if (tid == 0) {
+    cnt[2 * chunk] = st[2];
+    cnt[2 * chunk + 1] = 0;
+    __threadfence();
+    is_last = atomicAdd(&sync[1], 1u) == (uint32_t)(n_chunks - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+
+  // ---- the last CTA: exact threshold among the candidates ----
+  const uint32_t n_c = __ldcg(&sync[0]);
+  for (int b = tid; b < kHistBins; b += kSelThreads) h2[b] = 0u;
+  __syncthreads();
+  for (uint32_t j = tid; j < n_c; j += kSelThreads) atomicAdd(&h2[(__ldcg(&cand[j]).x >> 10) & 2047u], 1u);
+  __syncthreads();
+  find_digit(h2, kHistBins, k1, sh, &st[3], &st[4]);
+  const uint32_t d2 = st[3], k2 = st[4];
+  for (int b = tid; b < kHistBins; b += kSelThreads) h2[b] = 0u;
+  __syncthreads();
+  const uint32_t pre = (d1 << 11) | d2;
+  for (uint32_t j = tid; j < n_c; j += kSelThreads) {
+    const uint32_t key = __ldcg(&cand[j]).x;
+    if ((key >> 10) == pre) atomicAdd(&h2[key & 1023u], 1u);
+  }
+  __syncthreads();
+  find_digit(h2, 1024, k2, sh, &st[5], &st[6]);
+  const uint32_t T = (pre << 10) | st[5], need = st[6];
+  for (int c = tid; c < n_chunks; c += kSelThreads) cgt[c] = ceq[c] = 0u;
+  __syncthreads();
+  for (uint32_t j = tid; j < n_c; j += kSelThreads) {
+    const uint2 ce = __ldcg(&cand[j]);
+    const int c = (int)(ce.y / kSelectKeysPerCta);
+    if (ce.x > T) atomicAdd(&cgt[c], 1u);
+    else if (ce.x == T) atomicAdd(&ceq[c], 1u);
+  }
+  __syncthreads();
+  for (int c = tid; c < n_chunks; c += kSelThreads) {
+    cnt[2 * c] = __ldcg(&cnt[2 * c]) + cgt[c];
+    cnt[2 * c + 1] = ceq[c];
+  }
+  if (tid == 0) {
+    P.thr[2 * i] = T;
+    P.thr[2 * i + 1] = need;
+    sync[0] = 0u;  // ready for the next call
+    sync[1] = 0u;
   }
 }
 
@@ -301,6 +487,8 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, ui
   return incl - v;
 }
 
+// Pass 2: every chunk writes its selected indices in ascending order at the
+// positions the per-chunk counts of the chunks before it give.
 __global__ void __launch_bounds__(kSelThreads) select_emit_kernel(const __grid_constant__ AttendParams P) {
   __shared__ uint32_t sh[kSelThreads];
   const int i = find_req(P, blockIdx.x, 1);
@@ -320,8 +508,7 @@ __global__ void __launch_bounds__(kSelThreads) select_emit_kernel(const __grid_c
     }
     return;
   }
-  const Thresh th = final_thresh(P, i, sh);
-  // totals of earlier chunks of this request
+  const uint32_t T = P.thr[2 * i], need = P.thr[2 * i + 1];
   uint32_t base_gt = 0, base_eq = 0;
   const uint32_t* cnt = P.counts + (int64_t)i * P.max_key_ctas * 2;
   for (int c = 0; c < chunk; ++c) {
@@ -329,34 +516,28 @@ __global__ void __launch_bounds__(kSelThreads) select_emit_kernel(const __grid_c
     base_eq += cnt[2 * c + 1];
   }
   const uint32_t* keys = P.keys + (int64_t)i * P.key_stride;
-  // each thread owns kItems consecutive keys of the chunk
   const int64_t my0 = k0 + (int64_t)threadIdx.x * kItems;
   uint32_t kk[kItems];
   uint32_t n_gt = 0, n_eq = 0;
 #pragma unroll
   for (int j = 0; j < kItems; ++j) {
-    kk[j] = (my0 + j < k1) ? keys[my0 + j] : 0u;
     const bool in = my0 + j < k1;
-    n_gt += in && kk[j] > th.T;
-    n_eq += in && kk[j] == th.T;
+    kk[j] = in ? keys[my0 + j] : 0u;
+    n_gt += in && kk[j] > T;
+    n_eq += in && kk[j] == T;
   }
   uint32_t tot;
   const uint32_t pre_gt = block_excl_scan(n_gt, sh, &tot);
   const uint32_t pre_eq = block_excl_scan(n_eq, sh, &tot);
-  uint32_t eq_rank = base_eq + pre_eq;  // equal keys before my first one
+  uint32_t eq_rank = base_eq + pre_eq;  // keys equal to T before my first one
   uint32_t gt_rank = base_gt + pre_gt;
 #pragma unroll
   for (int j = 0; j < kItems; ++j) {
     const int64_t e = my0 + j;
     if (e >= k1) break;
-    bool take = false;
-    if (kk[j] > th.T) {
-      take = true;
-    } else if (kk[j] == th.T) {
-      take = eq_rank < th.need;
-    }
+    const bool take = kk[j] > T || (kk[j] == T && eq_rank < need);
     if (take) {
-      const uint32_t pos = gt_rank + min(eq_rank, th.need);
+      const uint32_t pos = gt_rank + min(eq_rank, need);
       if (pos < (uint32_t)R.k) {
         sel[pos] = (int32_t)e;
         if (tko) tko[pos] = (int32_t)e;
@@ -364,25 +545,49 @@ __global__ void __launch_bounds__(kSelThreads) select_emit_kernel(const __grid_c
         flag_error(P.pool, kErrBadIndex);
       }
     }
-    if (kk[j] > th.T) ++gt_rank;
-    if (kk[j] == th.T) ++eq_rank;
+    if (kk[j] > T) ++gt_rank;
+    if (kk[j] == T) ++eq_rank;
   }
 }
 
 }  // namespace
 
+// Score CTAs of a launch, and the shared-memory plan of the score kernel.
+int score_stage_plan(const PoolDesc& pd, int* stage_bytes, int* ring, int* stage_off, size_t* smem) {
+  *stage_bytes = pd.csa_per_block * (int)pd.idx_entry_bytes +
+                 (pd.cache_dtype == KVPOOL_FP8_E4M3 ? (2 * pd.csa_per_block + 15) / 16 * 16 : 0);
+  *ring = std::max(1, std::min(kScoreMaxRing, kScoreStageBudget / (kScoreWarps * *stage_bytes)));
+  *stage_off = (8 * kScoreMaxSlots + 6 * pd.XD + 4 * kHistBins + 127) / 128 * 128;
+  *smem = (size_t)*stage_off + (size_t)kScoreWarps * *ring * *stage_bytes;
+  return 0;
+}
+
+template <int IN, int CACHE>
+static int launch_score_t(const AttendParams& p, cudaStream_t s) {
+  int sb, ns, so;
+  size_t smem;
+  score_stage_plan(p.pool, &sb, &ns, &so, &smem);
+  auto k = score_kernel<IN, CACHE>;
+  static size_t set = 0;
+  if (set < smem) {
+    cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    set = smem;
+  }
+  k<<<p.total_score_ctas, kScoreThreads, smem, s>>>(p, sb, ns, so);
+  return 0;
+}
+
 int launch_score(const AttendParams& p, void* stream, int* n_kernels) {
   if (p.total_score_ctas <= 0) return 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const size_t smem = sizeof(float) * p.pool.XD;
   const int key = p.pool.in_dtype * 3 + p.pool.cache_dtype;
   switch (key) {
-    case KVPOOL_F32 * 3 + KVPOOL_F32: score_kernel<KVPOOL_F32, KVPOOL_F32><<<p.total_score_ctas, kScoreThreads, smem, s>>>(p); break;
-    case KVPOOL_F32 * 3 + KVPOOL_BF16: score_kernel<KVPOOL_F32, KVPOOL_BF16><<<p.total_score_ctas, kScoreThreads, smem, s>>>(p); break;
-    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3: score_kernel<KVPOOL_F32, KVPOOL_FP8_E4M3><<<p.total_score_ctas, kScoreThreads, smem, s>>>(p); break;
-    case KVPOOL_BF16 * 3 + KVPOOL_F32: score_kernel<KVPOOL_BF16, KVPOOL_F32><<<p.total_score_ctas, kScoreThreads, smem, s>>>(p); break;
-    case KVPOOL_BF16 * 3 + KVPOOL_BF16: score_kernel<KVPOOL_BF16, KVPOOL_BF16><<<p.total_score_ctas, kScoreThreads, smem, s>>>(p); break;
-    case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3: score_kernel<KVPOOL_BF16, KVPOOL_FP8_E4M3><<<p.total_score_ctas, kScoreThreads, smem, s>>>(p); break;
+    case KVPOOL_F32 * 3 + KVPOOL_F32: launch_score_t<KVPOOL_F32, KVPOOL_F32>(p, s); break;
+    case KVPOOL_F32 * 3 + KVPOOL_BF16: launch_score_t<KVPOOL_F32, KVPOOL_BF16>(p, s); break;
+    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3: launch_score_t<KVPOOL_F32, KVPOOL_FP8_E4M3>(p, s); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_F32: launch_score_t<KVPOOL_BF16, KVPOOL_F32>(p, s); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_BF16: launch_score_t<KVPOOL_BF16, KVPOOL_BF16>(p, s); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3: launch_score_t<KVPOOL_BF16, KVPOOL_FP8_E4M3>(p, s); break;
     default: return (int)cudaErrorInvalidValue;
   }
   *n_kernels += 1;
@@ -395,10 +600,8 @@ int launch_select(const AttendParams& p, void* stream, int* n_kernels) {
   bool any_radix = false;
   for (int i = 0; i < p.n; ++i) any_radix |= (!p.reqs[i].select_all && p.reqs[i].k > 0);
   if (any_radix) {
-    select_hist_kernel<<<p.total_key_ctas, kSelThreads, 0, s>>>(p, 2);
-    select_hist_kernel<<<p.total_key_ctas, kSelThreads, 0, s>>>(p, 3);
-    select_count_kernel<<<p.total_key_ctas, kSelThreads, 0, s>>>(p);
-    *n_kernels += 3;
+    select_compact_kernel<<<p.total_key_ctas, kSelThreads, 0, s>>>(p);
+    *n_kernels += 1;
   }
   select_emit_kernel<<<p.total_key_ctas, kSelThreads, 0, s>>>(p);
   *n_kernels += 1;
@@ -442,7 +645,7 @@ __global__ void __launch_bounds__(kSelThreads) static_keys_kernel(const __grid_c
     atomicAdd(&hist[key >> 21], 1u);
   }
   __syncthreads();
-  uint32_t* gh = P.hist + (int64_t)i * 3 * kHistBins;
+  uint32_t* gh = P.hist + (int64_t)i * kHistBins;
   for (int b = threadIdx.x; b < kHistBins; b += blockDim.x)
     if (hist[b]) atomicAdd(&gh[b], hist[b]);
 }
@@ -456,14 +659,18 @@ extern "C" int kvpool_topk_static(const float* d_scores, int32_t n_rows, int32_t
   if (n_rows < 0 || n_cols < 0 || top_k < 0) return KVPOOL_ERR_INVALID_ARG;
   if (n_rows == 0 || top_k == 0) return KVPOOL_OK;
   if (!d_scores || !d_topk_out || n_rows > kMaxAttendReqs) return KVPOOL_ERR_INVALID_ARG;
-  // scratch plan: [error word | hist | counts | selected | keys], each 256-B aligned
+  // scratch plan: [error word | hist | sync | thresholds | counts | selected | keys | candidates]
   const int64_t chunks = std::max<int64_t>(1, ((int64_t)n_cols + kSelectKeysPerCta - 1) / kSelectKeysPerCta);
+  if (chunks > kMaxKeyCtasPerReq) return KVPOOL_ERR_INVALID_ARG;
   auto up = [](int64_t x) { return (x + 255) / 256 * 256; };
   const int64_t off_hist = 256;
-  const int64_t off_counts = off_hist + up(4LL * n_rows * 3 * kHistBins);
+  const int64_t off_sync = off_hist + up(4LL * n_rows * kHistBins);
+  const int64_t off_thr = off_sync + up(16LL * n_rows);
+  const int64_t off_counts = off_thr + up(8LL * n_rows);
   const int64_t off_sel = off_counts + up(8LL * n_rows * chunks);
   const int64_t off_keys = off_sel + up(4LL * n_rows * top_k);
-  const int64_t need = off_keys + up(4LL * n_rows * n_cols);
+  const int64_t off_cand = off_keys + up(4LL * n_rows * n_cols);
+  const int64_t need = off_cand + up(8LL * n_rows * n_cols);
   if (need > (int64_t)kStaticScratchBytes) return KVPOOL_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -479,8 +686,9 @@ extern "C" int kvpool_topk_static(const float* d_scores, int32_t n_rows, int32_t
     base = static_cast<uint8_t*>(g_scratch_addr[dev]);
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // the error word and the histograms must start at zero; the rest is overwritten
-  if (cudaMemsetAsync(base, 0, (size_t)off_counts, s) != cudaSuccess) return KVPOOL_ERR_CUDA;
+  // the error word, the histograms and the sync counters must start at zero;
+  // everything else is written before it is read
+  if (cudaMemsetAsync(base, 0, (size_t)off_thr, s) != cudaSuccess) return KVPOOL_ERR_CUDA;
 
   AttendParams* P = new (std::nothrow) AttendParams();
   if (!P) return KVPOOL_ERR_INVALID_ARG;
@@ -497,6 +705,9 @@ extern "C" int kvpool_topk_static(const float* d_scores, int32_t n_rows, int32_t
   P->max_key_ctas = (int32_t)chunks;
   P->sel = reinterpret_cast<int32_t*>(base + off_sel);
   P->sel_stride = top_k;
+  P->cand = reinterpret_cast<uint2*>(base + off_cand);
+  P->sync = reinterpret_cast<uint32_t*>(base + off_sync);
+  P->thr = reinterpret_cast<uint32_t*>(base + off_thr);
   for (int i = 0; i < n_rows; ++i) {
     AttendReq& R = P->reqs[i];
     R = AttendReq{};

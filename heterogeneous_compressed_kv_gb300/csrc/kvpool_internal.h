@@ -11,7 +11,7 @@ namespace kvp {
 
 constexpr int kMaxLayers = 16;
 constexpr int kHistBins = 2048;          // radix digit of the top-k select (11 bits)
-constexpr int kScoreSegsPerCta = 64;     // block segments scored by one CTA
+constexpr int kMaxKeyCtasPerReq = 256;   // select chunks per request (1M candidates)
 constexpr int kSelectKeysPerCta = 4096;  // keys handled by one select CTA
 constexpr int kMaxAppendUnits = 512;     // units per append launch
 constexpr int kMaxAttendReqs = 256;      // requests per attend-side launch
@@ -96,8 +96,8 @@ struct AttendReq {
   int32_t select_all; // k == N_c: every CSA entry is selected
   int32_t score_base; // first score CTA of this request
   int32_t key_base;   // first select CTA of this request
-  int32_t split_base; // first attention split of this request
-  int32_t n_split;
+  int32_t split_base; // first attention split of this request (in the partials)
+  int32_t n_split;    // splits of the whole source list
   int32_t split_len;  // virtual entries per split
 };
 
@@ -112,13 +112,18 @@ struct AttendParams {
   int32_t n;                 // requests in this launch
   int32_t row0;              // first row of q / out for this launch
   int32_t total_score_ctas, total_key_ctas, total_splits;
+  int32_t segs_per_cta;      // block segments scored by one score CTA
+  int32_t src_lo, src_hi;    // attention sources [lo, hi) of the virtual list this launch covers
   // scratch (device pointers)
-  uint32_t* keys;            // [kMaxAttendReqs][max_cand]
+  uint32_t* keys;            // [rows][key_stride] orderable score keys
   int64_t key_stride;        // max_cand
-  uint32_t* hist;            // [kMaxAttendReqs][3][kHistBins]
-  uint32_t* counts;          // [kMaxAttendReqs][max_key_ctas][2]
+  uint32_t* hist;            // [rows][kHistBins] first radix digit histogram
+  uint32_t* counts;          // [rows][max_key_ctas][2] (keys > T, keys == T) per select chunk
   int32_t max_key_ctas;
-  int32_t* sel;              // [kMaxAttendReqs][max_top_k]
+  uint2* cand;               // [rows][key_stride] (key, index) of the boundary bucket
+  uint32_t* sync;            // [rows][4]: candidates, select CTAs done, attention splits done, pad
+  uint32_t* thr;             // [rows][2] (T, keys == T taken)
+  int32_t* sel;              // [rows][sel_stride]
   int32_t sel_stride;
   float* part_o;             // [max_splits][HD]
   float* part_ml;            // [max_splits][H][2]

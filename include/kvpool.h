@@ -186,9 +186,9 @@ int kvpool_decode_attend(kvpool_t* pool, int32_t layer, int32_t n, const int32_t
  * d_scores: [n_rows][n_cols] fp32 (finite) on the device; d_topk_out:
  * [n_rows][top_k] int32.  Its scratch (sort keys, radix histograms, counts)
  * is a file-scope 16 MiB device array in this library, present on every GPU
- * that loads it until the process exits: n_rows <= 256 and
- * 4*n_rows*n_cols + 4*n_rows*top_k + 24 KiB*n_rows (+ small) <= 16 MiB, else
- * INVALID_ARG.  No cudaMalloc, cudaFree or allocating library routine is
+ * that loads it until the process exits: n_rows <= 256, n_cols <= 1,048,576 and
+ * 12*n_rows*n_cols + 4*n_rows*top_k + 8.5 KiB*n_rows (+ small) <= 16 MiB,
+ * else INVALID_ARG.  No cudaMalloc, cudaFree or allocating library routine is
  * called.  The first call on a device looks up that device's address of the
  * array (for the current device) and should come before any stream capture.
  * Every call shares the array and clears what must start at zero; calls that
