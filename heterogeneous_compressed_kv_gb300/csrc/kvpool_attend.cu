@@ -11,7 +11,11 @@
 // producer warp streams the split's entries through a ring of stages guarded
 // by mbarriers; consumer threads (8 dims of one head each) run an online
 // softmax in the log2 domain and write a partial (max, sum, output) per head.
+// Consumer thread = 16 dims of one head; q.k takes mixed-precision FMAs
+// (f16 or bf16 products, exact in fp32) when the query is exactly
+// representable; fp8 values are weighted by p * scale rounded to f16.
 // A merge kernel combines the partials.  All waits are time-limited.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "device_util.cuh"
@@ -20,57 +24,18 @@
 namespace kvp {
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kMaxSplitLen = 1024;
 
-__device__ __forceinline__ int find_split_req(const AttendParams& P, int cta) {
+__device__ __forceinline__ int find_split_req(const AttendParams& P, int cta, int part) {
   int lo = 0, hi = P.n - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (P.reqs[mid].split_base <= cta) lo = mid;
+    if ((part ? P.reqs[mid].cta_base1 : P.reqs[mid].cta_base0) <= cta) lo = mid;
     else hi = mid - 1;
   }
   return lo;
 }
-
-template <int CACHE>
-struct KV8;
-template <>
-struct KV8<KVPOOL_F32> {
-  __device__ static void load(const uint8_t* p, float* x) {
-    const uint4 a = *reinterpret_cast<const uint4*>(p), b = *reinterpret_cast<const uint4*>(p + 16);
-    x[0] = __uint_as_float(a.x); x[1] = __uint_as_float(a.y); x[2] = __uint_as_float(a.z); x[3] = __uint_as_float(a.w);
-    x[4] = __uint_as_float(b.x); x[5] = __uint_as_float(b.y); x[6] = __uint_as_float(b.z); x[7] = __uint_as_float(b.w);
-  }
-};
-template <>
-struct KV8<KVPOOL_BF16> {
-  __device__ static void load(const uint8_t* p, float* x) {
-    const uint4 a = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
-      x[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
-    }
-  }
-};
-template <>
-struct KV8<KVPOOL_FP8_E4M3> {
-  __device__ static void load(const uint8_t* p, float* x) {
-    const uint2 a = *reinterpret_cast<const uint2*>(p);
-    const uint32_t w[2] = {a.x, a.y};
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float2 lo = e4m3x2_to_f32x2((uint16_t)(w[i] & 0xFFFFu));
-      const float2 hi = e4m3x2_to_f32x2((uint16_t)(w[i] >> 16));
-      x[4 * i] = lo.x;
-      x[4 * i + 1] = lo.y;
-      x[4 * i + 2] = hi.x;
-      x[4 * i + 3] = hi.y;
-    }
-  }
-};
 
 // Byte offset (from the arena) of virtual source v of request R.
 __device__ __forceinline__ int64_t source_offset(const AttendParams& P, int i, const AttendReq& R, int v) {
@@ -107,23 +72,87 @@ __device__ __forceinline__ int64_t source_offset(const AttendParams& P, int i, c
   return ring + (pos % pd.n_win) * pd.entry_bytes;
 }
 
-// TPH: consumer threads per head (head_dim / 8)
+__device__ __forceinline__ float fma_f16(uint16_t a, uint16_t b, float c) {
+  float d;
+  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_bf16(uint16_t a, uint16_t b, float c) {
+  float d;
+  asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)two));
+  return h;
+}
+__device__ __forceinline__ float f16_to_f32(uint32_t h) { return __half2float(__ushort_as_half((uint16_t)h)); }
+
+// Sixteen consecutive cache values of one entry (K or V part of one head) in
+// shared memory: as f16 pairs (fp8), bf16 pairs, or fp32.
+template <int CACHE>
+struct Row16;
+template <>
+struct Row16<KVPOOL_FP8_E4M3> {  // 16 B -> 8 f16x2 words
+  __device__ static void load(const uint8_t* p, uint32_t* w) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p);
+    const uint32_t b[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[2 * i] = e4m3x2_to_f16x2(b[i] & 0xFFFFu);
+      w[2 * i + 1] = e4m3x2_to_f16x2(b[i] >> 16);
+    }
+  }
+};
+template <>
+struct Row16<KVPOOL_BF16> {  // 32 B -> 8 bf16x2 words
+  __device__ static void load(const uint8_t* p, uint32_t* w) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p), b = *reinterpret_cast<const uint4*>(p + 16);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  }
+};
+template <>
+struct Row16<KVPOOL_F32> {  // 64 B -> 16 fp32 bit patterns
+  __device__ static void load(const uint8_t* p, uint32_t* w) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 a = *reinterpret_cast<const uint4*>(p + 16 * i);
+      w[4 * i] = a.x; w[4 * i + 1] = a.y; w[4 * i + 2] = a.z; w[4 * i + 3] = a.w;
+    }
+  }
+};
+
+// value j (0..15) of a loaded row as fp32
+template <int CACHE>
+__device__ __forceinline__ float row_value(const uint32_t* w, int j) {
+  if constexpr (CACHE == KVPOOL_F32) return __uint_as_float(w[j]);
+  else if constexpr (CACHE == KVPOOL_BF16) return bf16_bits_to_f32((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
+  else return f16_to_f32((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
+}
+
+// TPH: consumer threads per head (head_dim / 16); each owns 16 dims
 template <int IN, int CACHE, int TPH>
-__global__ void __launch_bounds__(kAttendThreadsMax) attend_kernel(const __grid_constant__ AttendParams P, int e_stage) {
+__global__ void __launch_bounds__(kAttendThreadsMax) attend_kernel(const __grid_constant__ AttendParams P, int e_stage,
+                                                                   int part) {
   extern __shared__ __align__(128) uint8_t smem[];
   const PoolDesc& pd = P.pool;
   const int HD = pd.HD;
-  const int n_cons = HD / 8;  // consumer threads
+  const int n_act = HD / 16;                    // consumer threads with work
+  const int n_cons = (n_act + 31) / 32 * 32;    // whole consumer warps
   const int n_cons_warps = n_cons / 32;
   const int tid = threadIdx.x;
-  const int i = find_split_req(P, blockIdx.x);
+  const int i = find_split_req(P, blockIdx.x, part);
   const AttendReq& R = P.reqs[i];
-  const int split = blockIdx.x - R.split_base;
-  const int n_src = R.k + R.n_hca + R.w;
-  const int v0 = split * R.split_len;
-  const int v1 = min(n_src, v0 + R.split_len);
+  const int split = blockIdx.x - (part ? R.cta_base1 : R.cta_base0);
+  // part 0 covers virtual sources [k, k + n_hca + w), part 1 covers [0, k)
+  const int lo = part ? 0 : R.k, hi = part ? R.k : R.k + R.n_hca + R.w;
+  const int len = part ? R.split_len1 : R.split_len0;
+  const int v0 = lo + split * len;
+  const int v1 = min(hi, v0 + len);
   const int cnt = v1 - v0;
   const int64_t ES = pd.entry_bytes;
+  const int64_t pslot = R.part_base + (part ? R.n_split0 : 0) + split;  // partial slot
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kStages;
@@ -137,20 +166,44 @@ __global__ void __launch_bounds__(kAttendThreadsMax) attend_kernel(const __grid_
     }
     mbar_fence_init();
   }
-  // zero this request's select histogram for the next call (the select
-  // passes that read it ran before this kernel)
-  if (split == 0 && P.layer.has_csa) {
-    uint32_t* gh = P.hist + (int64_t)i * kHistBins;
-    for (int b = tid; b < kHistBins; b += blockDim.x) gh[b] = 0u;
+  // consumer: head h, dims [dd0, dd0 + 16); the query row of this thread
+  const bool act = tid < n_act;
+  const int h = act ? tid / TPH : 0;
+  const int dd0 = act ? (tid % TPH) * 16 : 0;
+  float qf[16];
+  uint32_t qw[8];  // the query as f16 pairs (fp8 cache) or bf16 pairs (bf16 cache)
+  int exact = 1;
+  if (tid < n_cons) {
+    const int64_t base = (int64_t)(P.row0 + i) * HD + h * pd.head_dim + dd0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      qf[j] = IN == KVPOOL_F32 ? reinterpret_cast<const float*>(P.q)[base + j]
+                               : bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(P.q)[base + j]);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint32_t lo16 = 0, hi16 = 0;
+      if constexpr (CACHE == KVPOOL_FP8_E4M3) {
+        const __half a = __float2half_rn(qf[2 * j]), b = __float2half_rn(qf[2 * j + 1]);
+        exact &= (__half2float(a) == qf[2 * j]) && (__half2float(b) == qf[2 * j + 1]);
+        lo16 = __half_as_ushort(a);
+        hi16 = __half_as_ushort(b);
+      } else if constexpr (CACHE == KVPOOL_BF16) {
+        lo16 = f32_to_bf16_bits(qf[2 * j]);
+        hi16 = f32_to_bf16_bits(qf[2 * j + 1]);
+        exact &= (bf16_bits_to_f32(lo16) == qf[2 * j]) && (bf16_bits_to_f32(hi16) == qf[2 * j + 1]);
+      } else {
+        exact = 0;
+      }
+      qw[j] = lo16 | (hi16 << 16);
+    }
   }
-  __syncthreads();
+  const bool fast = __syncthreads_and(tid < n_cons ? exact : 1) != 0;
 
   const int n_st = (cnt + e_stage - 1) / e_stage;
   if (tid >= n_cons) {
     // producer warp: lanes compute source addresses 32 at a time, one batch
     // ahead of the copies; lane 0 issues the bulk copies of each stage
     const int lane = tid - n_cons;
-    if (lane >= 32) return;
     int64_t cur = lane < cnt ? source_offset(P, i, R, v0 + lane) : 0;
     int64_t nxt = 32 + lane < cnt ? source_offset(P, i, R, v0 + 32 + lane) : 0;
     int batch = 0;
@@ -183,30 +236,11 @@ __global__ void __launch_bounds__(kAttendThreadsMax) attend_kernel(const __grid_
     return;
   }
 
-  // consumer: head h, dims [dd0, dd0 + 8)
-  const int h = tid / TPH;
-  const int dd0 = (tid % TPH) * 8;
-  const float qscale = 1.4426950408889634f * rsqrtf((float)pd.head_dim);  // log2(e) / sqrt(d)
-  float q[8];
-  {
-    const int64_t base = (int64_t)(P.row0 + i) * HD + h * pd.head_dim + dd0;
-    if constexpr (IN == KVPOOL_F32) {
-      const float* qp = reinterpret_cast<const float*>(P.q) + base;
+  // scores in the log2 domain: dot(q, k) * log2(e) / sqrt(d) (* fp8 K scale)
+  const float qscale = 1.4426950408889634f * rsqrtf((float)pd.head_dim);
+  float m_run = -INFINITY, l_run = 0.0f, o[16];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) q[j] = qp[j] * qscale;
-    } else {
-      const uint4 a = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(P.q) + base);
-      const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        q[2 * j] = bf16_bits_to_f32(w[j] & 0xFFFFu) * qscale;
-        q[2 * j + 1] = bf16_bits_to_f32(w[j] >> 16) * qscale;
-      }
-    }
-  }
-  float m_run = -INFINITY, l_run = 0.0f, o[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) o[j] = 0.0f;
+  for (int j = 0; j < 16; ++j) o[j] = 0.0f;
   const int koff = (h * pd.head_dim + dd0) * pd.vs;
   const int voff = HD * pd.vs + koff;
 
@@ -222,33 +256,59 @@ __global__ void __launch_bounds__(kAttendThreadsMax) attend_kernel(const __grid_
         sc[u] = -INFINITY;
         if (e0 + u < ne) {
           const uint8_t* ent = base + (e0 + u) * ES;
-          float kx[8];
-          KV8<CACHE>::load(ent + koff, kx);
+          uint32_t kw[16];
+          Row16<CACHE>::load(ent + koff, kw);
           float d = 0.0f;
+          if (CACHE == KVPOOL_FP8_E4M3 && fast) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) d = fmaf(q[j], kx[j], d);
+            for (int j = 0; j < 8; ++j) {
+              d = fma_f16((uint16_t)(kw[j] & 0xFFFFu), (uint16_t)(qw[j] & 0xFFFFu), d);
+              d = fma_f16((uint16_t)(kw[j] >> 16), (uint16_t)(qw[j] >> 16), d);
+            }
+          } else if (CACHE == KVPOOL_BF16 && fast) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              d = fma_bf16((uint16_t)(kw[j] & 0xFFFFu), (uint16_t)(qw[j] & 0xFFFFu), d);
+              d = fma_bf16((uint16_t)(kw[j] >> 16), (uint16_t)(qw[j] >> 16), d);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) d = fmaf(qf[j], row_value<CACHE>(kw, j), d);
+          }
 #pragma unroll
           for (int off = TPH / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-          if constexpr (CACHE == KVPOOL_FP8_E4M3) d *= bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(ent + 2 * HD));
-          sc[u] = d;
+          float f = qscale;
+          if constexpr (CACHE == KVPOOL_FP8_E4M3) f *= bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(ent + 2 * HD));
+          sc[u] = d * f;
         }
       }
       const float mx = fmaxf(fmaxf(m_run, fmaxf(sc[0], sc[1])), fmaxf(sc[2], sc[3]));
       const float corr = exp2f(m_run - mx);
       l_run *= corr;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) o[j] *= corr;
+      for (int j = 0; j < 16; ++j) o[j] *= corr;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (e0 + u < ne) {
           const uint8_t* ent = base + (e0 + u) * ES;
-          float p = exp2f(sc[u] - mx);
+          const float p = exp2f(sc[u] - mx);
           l_run += p;
-          if constexpr (CACHE == KVPOOL_FP8_E4M3) p *= bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(ent + 2 * HD + 2));
-          float vx[8];
-          KV8<CACHE>::load(ent + voff, vx);
+          uint32_t vw[16];
+          Row16<CACHE>::load(ent + voff, vw);
+          if constexpr (CACHE == KVPOOL_FP8_E4M3) {
+            // weight times the V scale, rounded to f16; products with the f16
+            // values are exact, accumulation fp32
+            const float ps = p * bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(ent + 2 * HD + 2));
+            const uint16_t ph = __half_as_ushort(__float2half_rn(ps));
 #pragma unroll
-          for (int j = 0; j < 8; ++j) o[j] = fmaf(p, vx[j], o[j]);
+            for (int j = 0; j < 8; ++j) {
+              o[2 * j] = fma_f16((uint16_t)(vw[j] & 0xFFFFu), ph, o[2 * j]);
+              o[2 * j + 1] = fma_f16((uint16_t)(vw[j] >> 16), ph, o[2 * j + 1]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) o[j] = fmaf(p, row_value<CACHE>(vw, j), o[j]);
+          }
         }
       }
       m_run = mx;
@@ -257,98 +317,101 @@ __global__ void __launch_bounds__(kAttendThreadsMax) attend_kernel(const __grid_
     if ((tid & 31) == 0) mbar_arrive(&empty[s]);
   }
 
-  float* po = P.part_o + (int64_t)blockIdx.x * HD + h * pd.head_dim + dd0;
-  reinterpret_cast<float4*>(po)[0] = make_float4(o[0], o[1], o[2], o[3]);
-  reinterpret_cast<float4*>(po)[1] = make_float4(o[4], o[5], o[6], o[7]);
-  if (dd0 == 0) {
-    float* ml = P.part_ml + ((int64_t)blockIdx.x * pd.heads + h) * 2;
-    ml[0] = m_run;
-    ml[1] = l_run;
+  if (act) {
+    float* po = P.part_o + pslot * HD + h * pd.head_dim + dd0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) reinterpret_cast<float4*>(po)[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+    if (dd0 == 0) {
+      float* ml = P.part_ml + (pslot * pd.heads + h) * 2;
+      ml[0] = m_run;
+      ml[1] = l_run;
+    }
   }
 }
 
 // Merge of the split partials of one (request, head): o = sum_s 2^(m_s - M) o_s
-// / sum_s 2^(m_s - M) l_s.  Warp w takes splits w, w + 8, ...; lane l owns
-// dims [4l, 4l + 4).
-constexpr int kCombineWarps = 8;
+// / sum_s 2^(m_s - M) l_s.  Warp w merges splits w, w + 32, ... with its own
+// running maximum (one round of loads in flight), lane l owns dims
+// [4l, 4l + 4); the 32 warp results are merged through shared memory.
+constexpr int kCombineWarps = 32;
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ AttendParams P) {
   __shared__ float red_o[kCombineWarps][128];
-  __shared__ float red_l[kCombineWarps];
-  __shared__ float sM;
+  __shared__ float red_m[kCombineWarps], red_l[kCombineWarps];
   const int i = blockIdx.x, h = blockIdx.y;
   const AttendReq& R = P.reqs[i];
   const PoolDesc& pd = P.pool;
   const int d = pd.head_dim;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // M: max over the splits' running maxima of this head
-  float m = -INFINITY;
-  for (int s = threadIdx.x; s < R.n_split; s += blockDim.x)
-    m = fmaxf(m, P.part_ml[((int64_t)(R.split_base + s) * pd.heads + h) * 2]);
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if (lane == 0) red_l[warp] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float M = -INFINITY;
-    for (int w = 0; w < kCombineWarps; ++w) M = fmaxf(M, red_l[w]);
-    sM = M;
+  const int n_split = R.n_split0 + R.n_split1;
+  // the select passes that read this request's histogram are done: clear it
+  // for the next call
+  if (h == 0 && P.layer.has_csa) {
+    uint32_t* gh = P.hist + (int64_t)i * kHistBins;
+    for (int b = threadIdx.x; b < kHistBins; b += blockDim.x) gh[b] = 0u;
   }
-  __syncthreads();
-  const float M = sM;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float l = 0.0f;
   const bool on = 4 * lane < d;
+  float m = -INFINITY, l = 0.0f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-  for (int s = warp; s < R.n_split; s += kCombineWarps) {
-    const int64_t gs = R.split_base + s;
+  for (int s = warp; s < n_split; s += kCombineWarps) {
+    const int64_t gs = R.part_base + s;
     const float2 ml = *reinterpret_cast<const float2*>(P.part_ml + (gs * pd.heads + h) * 2);
-    const float wgt = exp2f(ml.x - M);
-    l = fmaf(ml.y, wgt, l);
-    if (on) {
-      const float4 v = *reinterpret_cast<const float4*>(P.part_o + gs * pd.HD + h * d + 4 * lane);
-      acc.x = fmaf(v.x, wgt, acc.x);
-      acc.y = fmaf(v.y, wgt, acc.y);
-      acc.z = fmaf(v.z, wgt, acc.z);
-      acc.w = fmaf(v.w, wgt, acc.w);
-    }
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (on) v = *reinterpret_cast<const float4*>(P.part_o + gs * pd.HD + h * d + 4 * lane);
+    if (ml.x == -INFINITY) continue;  // an empty split
+    const float mn = fmaxf(m, ml.x);
+    const float a = exp2f(m - mn), b = exp2f(ml.x - mn);
+    l = l * a + ml.y * b;
+    acc.x = acc.x * a + v.x * b;
+    acc.y = acc.y * a + v.y * b;
+    acc.z = acc.z * a + v.z * b;
+    acc.w = acc.w * a + v.w * b;
+    m = mn;
   }
-  __syncthreads();
   if (on) {
     red_o[warp][4 * lane] = acc.x;
     red_o[warp][4 * lane + 1] = acc.y;
     red_o[warp][4 * lane + 2] = acc.z;
     red_o[warp][4 * lane + 3] = acc.w;
   }
-  if (lane == 0) red_l[warp] = l;
+  if (lane == 0) {
+    red_m[warp] = m;
+    red_l[warp] = l;
+  }
   __syncthreads();
   if (threadIdx.x < d) {
+    float M = -INFINITY;
+    for (int w = 0; w < kCombineWarps; ++w) M = fmaxf(M, red_m[w]);
     float num = 0.0f, den = 0.0f;
     for (int w = 0; w < kCombineWarps; ++w) {
-      num += red_o[w][threadIdx.x];
-      den += red_l[w];
+      if (red_m[w] == -INFINITY) continue;
+      const float wt = exp2f(red_m[w] - M);
+      num = fmaf(red_o[w][threadIdx.x], wt, num);
+      den = fmaf(red_l[w], wt, den);
     }
     P.out[((int64_t)(P.row0 + i) * pd.heads + h) * d + threadIdx.x] = num / den;
   }
 }
 
 template <int IN, int CACHE>
-int launch_attend_t(const AttendParams& p, cudaStream_t s, int e_stage, size_t smem) {
-  const int threads = p.pool.HD / 8 + 32;
+int launch_attend_t(const AttendParams& p, cudaStream_t s, int e_stage, size_t smem, int part, int ctas) {
+  const int threads = (p.pool.HD / 16 + 31) / 32 * 32 + 32;
   if (p.pool.head_dim == 128) {
-    auto k = attend_kernel<IN, CACHE, 16>;
-    static size_t set16 = 0;
-    if (set16 < smem) {
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      set16 = smem;
-    }
-    k<<<p.total_splits, threads, smem, s>>>(p, e_stage);
-  } else if (p.pool.head_dim == 64) {
     auto k = attend_kernel<IN, CACHE, 8>;
     static size_t set8 = 0;
     if (set8 < smem) {
       cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       set8 = smem;
     }
-    k<<<p.total_splits, threads, smem, s>>>(p, e_stage);
+    k<<<ctas, threads, smem, s>>>(p, e_stage, part);
+  } else if (p.pool.head_dim == 64) {
+    auto k = attend_kernel<IN, CACHE, 4>;
+    static size_t set4 = 0;
+    if (set4 < smem) {
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      set4 = smem;
+    }
+    k<<<ctas, threads, smem, s>>>(p, e_stage, part);
   } else {
     return (int)cudaErrorInvalidValue;
   }
@@ -357,10 +420,10 @@ int launch_attend_t(const AttendParams& p, cudaStream_t s, int e_stage, size_t s
 
 }  // namespace
 
-// entries per pipeline stage: about 32 KiB of entries, at most 16
+// entries per pipeline stage: about 16 KiB of entries, at most 8
 int attend_stage_entries(const PoolDesc& pd) {
-  int e = (int)(32768 / pd.entry_bytes);
-  return e < 1 ? 1 : (e > 16 ? 16 : e);
+  int e = (int)(16384 / pd.entry_bytes);
+  return e < 1 ? 1 : (e > 8 ? 8 : e);
 }
 
 size_t attend_smem_bytes(const PoolDesc& pd) {
@@ -369,20 +432,22 @@ size_t attend_smem_bytes(const PoolDesc& pd) {
 
 int attend_max_split_len() { return kMaxSplitLen; }
 
-int launch_attend(const AttendParams& p, void* stream, int* n_kernels) {
-  if (p.total_splits <= 0) return 0;
+int launch_attend(const AttendParams& p, int part, int ctas, void* stream, int* n_kernels) {
+  if (ctas <= 0) return 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int e_stage = attend_stage_entries(p.pool);
   const size_t smem = attend_smem_bytes(p.pool);
   *n_kernels += 1;
   const int key = p.pool.in_dtype * 3 + p.pool.cache_dtype;
   switch (key) {
-    case KVPOOL_F32 * 3 + KVPOOL_F32: return launch_attend_t<KVPOOL_F32, KVPOOL_F32>(p, s, e_stage, smem);
-    case KVPOOL_F32 * 3 + KVPOOL_BF16: return launch_attend_t<KVPOOL_F32, KVPOOL_BF16>(p, s, e_stage, smem);
-    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3: return launch_attend_t<KVPOOL_F32, KVPOOL_FP8_E4M3>(p, s, e_stage, smem);
-    case KVPOOL_BF16 * 3 + KVPOOL_F32: return launch_attend_t<KVPOOL_BF16, KVPOOL_F32>(p, s, e_stage, smem);
-    case KVPOOL_BF16 * 3 + KVPOOL_BF16: return launch_attend_t<KVPOOL_BF16, KVPOOL_BF16>(p, s, e_stage, smem);
-    case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3: return launch_attend_t<KVPOOL_BF16, KVPOOL_FP8_E4M3>(p, s, e_stage, smem);
+    case KVPOOL_F32 * 3 + KVPOOL_F32: return launch_attend_t<KVPOOL_F32, KVPOOL_F32>(p, s, e_stage, smem, part, ctas);
+    case KVPOOL_F32 * 3 + KVPOOL_BF16: return launch_attend_t<KVPOOL_F32, KVPOOL_BF16>(p, s, e_stage, smem, part, ctas);
+    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3:
+      return launch_attend_t<KVPOOL_F32, KVPOOL_FP8_E4M3>(p, s, e_stage, smem, part, ctas);
+    case KVPOOL_BF16 * 3 + KVPOOL_F32: return launch_attend_t<KVPOOL_BF16, KVPOOL_F32>(p, s, e_stage, smem, part, ctas);
+    case KVPOOL_BF16 * 3 + KVPOOL_BF16: return launch_attend_t<KVPOOL_BF16, KVPOOL_BF16>(p, s, e_stage, smem, part, ctas);
+    case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3:
+      return launch_attend_t<KVPOOL_BF16, KVPOOL_FP8_E4M3>(p, s, e_stage, smem, part, ctas);
     default: return (int)cudaErrorInvalidValue;
   }
 }

@@ -34,7 +34,7 @@ using namespace kvp;
 namespace {
 
 constexpr int kMaxSplits = 4096;
-constexpr int kTargetSplits = 2 * 152;  // CTAs of the attention kernel per launch (2 per SM, one wave)
+constexpr int kTargetSplits = 4 * 152;  // CTAs of the attention kernel per launch (4 per SM, one wave)
 constexpr int kScoreCtas = 152;         // CTAs of the score kernel per launch (1 per SM, one wave)
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -151,7 +151,7 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
   }
   // decode-attention scratch
   L.n_attend_rows = std::min(c->max_batch, kMaxAttendReqs);
-  L.key_stride = (int64_t)(c->max_blocks_per_request + 1) * CB;
+  L.key_stride = round_up((int64_t)(c->max_blocks_per_request + 1) * CB, 16);  // 16-byte aligned rows
   L.max_key_ctas = (int32_t)((L.key_stride + kSelectKeysPerCta - 1) / kSelectKeysPerCta);
   L.sel_stride = std::max(1, c->max_top_k);
   if (L.max_key_ctas > kMaxKeyCtasPerReq) return "max_blocks_per_request too large for the top-k select";
@@ -222,6 +222,10 @@ struct kvpool {
   std::set<int32_t> free_slots;
   std::vector<Request> reqs;
   std::string err;
+  // second stream for the attention part that needs no top-k, and the events
+  // that fork it from / join it back to the caller's stream
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   // profiling
   bool profiling = false;
   std::vector<ProfileSlot> prof;
@@ -343,6 +347,10 @@ int kvpool_create(const kvpool_config* cfg, void* d_arena, size_t arena_bytes, v
     cudaError_t e = cudaMemsetAsync(p->arena + L.pd.err, 0, 256, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(p->arena + L.hist, 0, (size_t)(L.thr - L.hist), s);
     if (e != cudaSuccess) { int rc = p->cuda_fail(e, "arena init"); delete p; return rc; }
+    e = cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming);
+    if (e != cudaSuccess) { int rc = p->cuda_fail(e, "side stream"); kvpool_destroy(p); return rc; }
   }
   *out = p;
   return KVPOOL_OK;
@@ -355,6 +363,9 @@ int kvpool_destroy(kvpool_t* p) {
     cudaEventDestroy(s.b);
   }
   for (auto e : p->event_pool) cudaEventDestroy(e);
+  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+  if (p->ev_join) cudaEventDestroy(p->ev_join);
+  if (p->side) cudaStreamDestroy(p->side);
   delete p;
   return KVPOOL_OK;
 }
@@ -626,34 +637,71 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
                       (int64_t)pd.HD * pd.isz;
     }
     out_bytes = (int64_t)gn * pd.HD * 4;
-    int64_t split_len = std::max<int64_t>(16, (total_src + kTargetSplits - 1) / kTargetSplits);
-    split_len = std::min<int64_t>(split_len, max_split_len);
-    int splits = 0;
+    // each part is split to fill the GPU by itself (they run at different times)
+    int64_t src0 = 0, src1 = 0;
+    for (int i = 0; i < gn; ++i) {
+      src0 += (int64_t)P.reqs[i].n_hca + P.reqs[i].w;
+      src1 += P.reqs[i].k;
+    }
+    // part 0 runs beside the select on the side stream: 3 CTAs per SM leave a
+    // slot per SM for the select and the CSA part
+    const int64_t target0 = (Ld.has_csa && src1 > 0) ? 3 * 152 : kTargetSplits;
+    int64_t len0 = std::min<int64_t>(max_split_len, std::max<int64_t>(16, (src0 + target0 - 1) / target0));
+    int64_t len1 = std::min<int64_t>(max_split_len, std::max<int64_t>(16, (src1 + kTargetSplits - 1) / kTargetSplits));
+    int ctas0 = 0, ctas1 = 0, parts = 0;
     for (int pass = 0; pass < 2; ++pass) {
-      splits = 0;
+      ctas0 = ctas1 = parts = 0;
       for (int i = 0; i < gn; ++i) {
         AttendReq& R = P.reqs[i];
-        const int64_t ns = (int64_t)R.k + R.n_hca + R.w;
-        R.split_len = (int32_t)split_len;
-        R.n_split = (int32_t)((ns + split_len - 1) / split_len);
-        R.split_base = splits;
-        splits += R.n_split;
+        R.split_len0 = (int32_t)len0;
+        R.split_len1 = (int32_t)len1;
+        R.n_split0 = (int32_t)(((int64_t)R.n_hca + R.w + len0 - 1) / len0);
+        R.n_split1 = (int32_t)(((int64_t)R.k + len1 - 1) / len1);
+        R.cta_base0 = ctas0;
+        R.cta_base1 = ctas1;
+        R.part_base = parts;
+        ctas0 += R.n_split0;
+        ctas1 += R.n_split1;
+        parts += R.n_split0 + R.n_split1;
       }
-      if (splits <= kMaxSplits) break;
-      split_len = max_split_len;
+      if (parts <= kMaxSplits) break;
+      len0 = len1 = max_split_len;
     }
-    if (splits > kMaxSplits) {
+    if (parts > kMaxSplits) {
       rc = -1;
       p->fail(KVPOOL_ERR_INVALID_ARG, "decode_attend: too many attention splits");
       break;
     }
     P.total_score_ctas = score_ctas;
     P.total_key_ctas = key_ctas;
-    P.total_splits = splits;
-    if (Ld.has_csa) rc = p->launch(KVPOOL_KERNEL_SCORE, score_bytes, stream, [&](int* nk) { return launch_score(P, stream, nk); });
+    P.total_ctas0 = ctas0;
+    P.total_ctas1 = ctas1;
+    int64_t bytes1 = 0;
+    for (int i = 0; i < gn; ++i) bytes1 += (int64_t)P.reqs[i].k * (entry_algo + 4);
+    const int64_t bytes0 = attend_bytes - bytes1;
+    // [HCA | window] attention needs no top-k: after the indexer scan (which
+    // wants every SM) it runs on the side stream, beside the latency-bound
+    // select passes; the [selected CSA] part follows the select
+    const bool fork = Ld.has_csa && ctas0 > 0 && ctas1 > 0;
+    void* s0 = fork ? (void*)p->side : stream;
+    if (rc == 0 && Ld.has_csa)
+      rc = p->launch(KVPOOL_KERNEL_SCORE, score_bytes, stream, [&](int* nk) { return launch_score(P, stream, nk); });
+    if (rc == 0 && fork) {
+      cudaError_t e = cudaEventRecord(p->ev_fork, (cudaStream_t)stream);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(p->side, p->ev_fork, 0);
+      if (e != cudaSuccess) rc = (int)e;
+    }
+    if (rc == 0)
+      rc = p->launch(KVPOOL_KERNEL_ATTEND, bytes0, s0, [&](int* nk) { return launch_attend(P, 0, ctas0, s0, nk); });
     if (rc == 0 && key_ctas > 0)
       rc = p->launch(KVPOOL_KERNEL_SELECT, 0, stream, [&](int* nk) { return launch_select(P, stream, nk); });
-    if (rc == 0) rc = p->launch(KVPOOL_KERNEL_ATTEND, attend_bytes, stream, [&](int* nk) { return launch_attend(P, stream, nk); });
+    if (rc == 0)
+      rc = p->launch(KVPOOL_KERNEL_ATTEND, bytes1, stream, [&](int* nk) { return launch_attend(P, 1, ctas1, stream, nk); });
+    if (fork) {
+      cudaError_t e = cudaEventRecord(p->ev_join, p->side);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent((cudaStream_t)stream, p->ev_join, 0);
+      if (e != cudaSuccess && rc == 0) rc = (int)e;
+    }
     if (rc == 0) rc = p->launch(KVPOOL_KERNEL_COMBINE, out_bytes, stream, [&](int* nk) { return launch_combine(P, stream, nk); });
   }
   delete ap;

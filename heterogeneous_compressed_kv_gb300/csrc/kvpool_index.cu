@@ -334,27 +334,31 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(const __grid_co
 // ---------------------------------------------------------------------------
 constexpr int kSelThreads = 256;
 constexpr int kItems = kSelectKeysPerCta / kSelThreads;  // 16 keys per thread
+constexpr uint32_t kCandCache = 4096;                    // boundary-bucket candidates kept in shared memory
 
-// Block-wide: the digit d (bin index) at which the count of keys in bins
-// above d is < k and the count in bins >= d is >= k, and k - (count above d).
+// Block-wide (kSelThreads threads): the digit d (bin index) at which the
+// count of keys in bins above d is < k and the count in bins >= d is >= k,
+// and k - (count above d).  Thread t owns bins [t*per, (t+1)*per); suffix
+// sums run over warp shuffles, then across the 8 warps.
 __device__ void find_digit(const uint32_t* h, int nbins, uint32_t k, uint32_t* sh, uint32_t* d_out,
                            uint32_t* k_out) {
-  // thread t owns bins [t*per, (t+1)*per), per = nbins / 256
   const int per = nbins / kSelThreads;
-  const int t = threadIdx.x;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   uint32_t own = 0;
   for (int b = 0; b < per; ++b) own += h[t * per + b];
-  // inclusive suffix sum over threads (high bins first) via shared memory
-  sh[t] = own;
-  __syncthreads();
-  for (int off = 1; off < kSelThreads; off <<= 1) {
-    const uint32_t add = (t + off < kSelThreads) ? sh[t + off] : 0u;
-    __syncthreads();
-    sh[t] += add;
-    __syncthreads();
+  // inclusive suffix sum within the warp (higher lanes own higher bins)
+  uint32_t suf = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += v;
   }
-  const uint32_t incl = sh[t];        // keys in bins >= t*per
-  const uint32_t above = incl - own;  // keys in bins >= (t+1)*per
+  if (lane == 0) sh[warp] = suf;  // warp total
+  __syncthreads();
+  uint32_t above_warps = 0;
+  for (int w = warp + 1; w < kSelThreads / 32; ++w) above_warps += sh[w];
+  const uint32_t incl = suf + above_warps;  // keys in bins >= t*per
+  const uint32_t above = incl - own;        // keys in bins >= (t+1)*per
   if (above < k && incl >= k) {
     uint32_t acc = above;
     for (int b = per - 1; b >= 0; --b) {
@@ -370,18 +374,60 @@ __device__ void find_digit(const uint32_t* h, int nbins, uint32_t k, uint32_t* s
   __syncthreads();
 }
 
+// exclusive block scan of one value per thread; returns the block total
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, uint32_t* total) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  uint32_t inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += u;
+  }
+  __syncthreads();
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  uint32_t before = 0, tot = 0;
+  for (int w = 0; w < kSelThreads / 32; ++w) {
+    if (w < warp) before += sh[w];
+    tot += sh[w];
+  }
+  *total = tot;
+  return before + inc - v;
+}
+
+// kItems consecutive keys of thread t (chunk-local), from global memory
+__device__ __forceinline__ int load_items(const uint32_t* keys, int64_t my0, int64_t kend, uint32_t* kk) {
+  const int n = (int)max((int64_t)0, min((int64_t)kItems, kend - my0));
+  if (n == kItems) {
+#pragma unroll
+    for (int q = 0; q < kItems / 4; ++q) {
+      const uint4 v = *reinterpret_cast<const uint4*>(keys + my0 + 4 * q);
+      kk[4 * q] = v.x;
+      kk[4 * q + 1] = v.y;
+      kk[4 * q + 2] = v.z;
+      kk[4 * q + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kItems; ++j) kk[j] = j < n ? keys[my0 + j] : 0u;
+  }
+  return n;
+}
+
 // Pass 1 of the select (one CTA per 4096 keys of a request): the first digit
 // d1 of the k-th largest key follows from the score histogram; keys above
 // bucket d1 are surely selected (counted per chunk), keys inside it become
 // candidates.  The last CTA of the request then finds the exact threshold T
-// among the candidates (two more radix digits) and how many keys equal to T
-// are taken, and completes the per-chunk counts.  No CTA waits on another:
-// the last one is found with an atomic counter after a fence.
+// among the candidates (two more radix digits), how many keys equal to T are
+// taken, and every chunk's exclusive prefix of (keys > T, keys == T).  No
+// CTA waits on another: the last one is found with an atomic counter after a
+// fence.
 __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __grid_constant__ AttendParams P) {
   __shared__ uint32_t sh[kSelThreads];
   __shared__ uint32_t st[8];
   __shared__ uint32_t h2[kHistBins];
   __shared__ uint32_t cgt[kMaxKeyCtasPerReq], ceq[kMaxKeyCtasPerReq];
+  __shared__ uint2 cs[kCandCache];
   __shared__ int is_last;
   const int i = find_req(P, blockIdx.x, 1);
   const AttendReq& R = P.reqs[i];
@@ -396,24 +442,32 @@ __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __gri
   const uint32_t* keys = P.keys + (int64_t)i * P.key_stride;
   const int tid = threadIdx.x, lane = tid & 31;
 
+  uint32_t kk[kItems];
+  const int64_t my0 = k0 + (int64_t)tid * kItems;
+  const int n_mine = load_items(keys, my0, kend, kk);
   find_digit(P.hist + (int64_t)i * kHistBins, kHistBins, (uint32_t)R.k, sh, &st[0], &st[1]);
   const uint32_t d1 = st[0], k1 = st[1];
-  uint32_t gt = 0;
-  for (int64_t base = k0; base < kend; base += kSelThreads) {
-    const int64_t e = base + tid;
-    const bool in = e < kend;
-    const uint32_t key = in ? keys[e] : 0u;
-    gt += (in && (key >> 21) > d1) ? 1u : 0u;
-    const bool is_c = in && (key >> 21) == d1;
-    const unsigned mask = __ballot_sync(0xffffffffu, is_c);
-    if (mask) {
-      const int leader = __ffs(mask) - 1;
-      uint32_t pos = 0;
-      if (lane == leader) pos = atomicAdd(&sync[0], (uint32_t)__popc(mask));
-      pos = __shfl_sync(0xffffffffu, pos, leader);
-      if (is_c) cand[pos + __popc(mask & ((1u << lane) - 1u))] = make_uint2(key, (uint32_t)e);
+  uint32_t gt = 0, nc = 0;
+#pragma unroll
+  for (int j = 0; j < kItems; ++j) {
+    if (j < n_mine) {
+      gt += (kk[j] >> 21) > d1 ? 1u : 0u;
+      nc += (kk[j] >> 21) == d1 ? 1u : 0u;
     }
   }
+  // candidates: one atomic per warp, then each thread writes its own in order
+  uint32_t inc = nc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += u;
+  }
+  uint32_t base = 0;
+  if (lane == 31 && inc) base = atomicAdd(&sync[0], inc);
+  base = __shfl_sync(0xffffffffu, base, 31) + inc - nc;
+#pragma unroll
+  for (int j = 0; j < kItems; ++j)
+    if (j < n_mine && (kk[j] >> 21) == d1) cand[base++] = make_uint2(kk[j], (uint32_t)(my0 + j));
   // chunk total of surely-selected keys
   for (int o = 16; o > 0; o >>= 1) gt += __shfl_xor_sync(0xffffffffu, gt, o);
   if (tid == 0) st[2] = 0;
@@ -433,9 +487,13 @@ __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __gri
 
   // ---- the last CTA: exact threshold among the candidates ----
   const uint32_t n_c = __ldcg(&sync[0]);
+  const bool cached = n_c <= kCandCache;  // usually a few thousand: keep them in shared memory
+  if (cached)
+    for (uint32_t j = tid; j < n_c; j += kSelThreads) cs[j] = __ldcg(&cand[j]);
   for (int b = tid; b < kHistBins; b += kSelThreads) h2[b] = 0u;
   __syncthreads();
-  for (uint32_t j = tid; j < n_c; j += kSelThreads) atomicAdd(&h2[(__ldcg(&cand[j]).x >> 10) & 2047u], 1u);
+  auto cand_at = [&](uint32_t j) -> uint2 { return cached ? cs[j] : __ldcg(&cand[j]); };
+  for (uint32_t j = tid; j < n_c; j += kSelThreads) atomicAdd(&h2[(cand_at(j).x >> 10) & 2047u], 1u);
   __syncthreads();
   find_digit(h2, kHistBins, k1, sh, &st[3], &st[4]);
   const uint32_t d2 = st[3], k2 = st[4];
@@ -443,7 +501,7 @@ __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __gri
   __syncthreads();
   const uint32_t pre = (d1 << 11) | d2;
   for (uint32_t j = tid; j < n_c; j += kSelThreads) {
-    const uint32_t key = __ldcg(&cand[j]).x;
+    const uint32_t key = cand_at(j).x;
     if ((key >> 10) == pre) atomicAdd(&h2[key & 1023u], 1u);
   }
   __syncthreads();
@@ -452,15 +510,21 @@ __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __gri
   for (int c = tid; c < n_chunks; c += kSelThreads) cgt[c] = ceq[c] = 0u;
   __syncthreads();
   for (uint32_t j = tid; j < n_c; j += kSelThreads) {
-    const uint2 ce = __ldcg(&cand[j]);
+    const uint2 ce = cand_at(j);
     const int c = (int)(ce.y / kSelectKeysPerCta);
     if (ce.x > T) atomicAdd(&cgt[c], 1u);
     else if (ce.x == T) atomicAdd(&ceq[c], 1u);
   }
   __syncthreads();
-  for (int c = tid; c < n_chunks; c += kSelThreads) {
-    cnt[2 * c] = __ldcg(&cnt[2 * c]) + cgt[c];
-    cnt[2 * c + 1] = ceq[c];
+  // per-chunk exclusive prefixes (n_chunks <= kMaxKeyCtasPerReq = kSelThreads)
+  const uint32_t g = tid < n_chunks ? __ldcg(&cnt[2 * tid]) + cgt[tid] : 0u;
+  const uint32_t e = tid < n_chunks ? ceq[tid] : 0u;
+  uint32_t tot;
+  const uint32_t pg = block_excl_scan(g, sh, &tot);
+  const uint32_t pe = block_excl_scan(e, sh, &tot);
+  if (tid < n_chunks) {
+    cnt[2 * tid] = pg;
+    cnt[2 * tid + 1] = pe;
   }
   if (tid == 0) {
     P.thr[2 * i] = T;
@@ -470,25 +534,8 @@ __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __gri
   }
 }
 
-// exclusive block scan of one value per thread; returns the block total
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, uint32_t* total) {
-  const int t = threadIdx.x;
-  sh[t] = v;
-  __syncthreads();
-  for (int off = 1; off < kSelThreads; off <<= 1) {
-    const uint32_t add = t >= off ? sh[t - off] : 0u;
-    __syncthreads();
-    sh[t] += add;
-    __syncthreads();
-  }
-  const uint32_t incl = sh[t];
-  *total = sh[kSelThreads - 1];
-  __syncthreads();
-  return incl - v;
-}
-
-// Pass 2: every chunk writes its selected indices in ascending order at the
-// positions the per-chunk counts of the chunks before it give.
+// Pass 2: every chunk writes its selected indices in ascending order, from the
+// exclusive prefixes the last compact CTA stored for it.
 __global__ void __launch_bounds__(kSelThreads) select_emit_kernel(const __grid_constant__ AttendParams P) {
   __shared__ uint32_t sh[kSelThreads];
   const int i = find_req(P, blockIdx.x, 1);
@@ -500,31 +547,26 @@ __global__ void __launch_bounds__(kSelThreads) select_emit_kernel(const __grid_c
   if (chunk == 0 && tko)
     for (int j = R.k + threadIdx.x; j < P.top_k; j += blockDim.x) tko[j] = -1;
   if (R.k == 0 || k0 >= R.n_cand) return;
-  const int64_t k1 = min((int64_t)R.n_cand, k0 + kSelectKeysPerCta);
+  const int64_t kend = min((int64_t)R.n_cand, k0 + kSelectKeysPerCta);
   if (R.select_all) {
-    for (int64_t e = k0 + threadIdx.x; e < k1; e += blockDim.x) {
+    for (int64_t e = k0 + threadIdx.x; e < kend; e += blockDim.x) {
       sel[e] = (int32_t)e;
       if (tko) tko[e] = (int32_t)e;
     }
     return;
   }
   const uint32_t T = P.thr[2 * i], need = P.thr[2 * i + 1];
-  uint32_t base_gt = 0, base_eq = 0;
   const uint32_t* cnt = P.counts + (int64_t)i * P.max_key_ctas * 2;
-  for (int c = 0; c < chunk; ++c) {
-    base_gt += cnt[2 * c];
-    base_eq += cnt[2 * c + 1];
-  }
+  const uint32_t base_gt = cnt[2 * chunk], base_eq = cnt[2 * chunk + 1];
   const uint32_t* keys = P.keys + (int64_t)i * P.key_stride;
   const int64_t my0 = k0 + (int64_t)threadIdx.x * kItems;
   uint32_t kk[kItems];
+  const int n_mine = load_items(keys, my0, kend, kk);
   uint32_t n_gt = 0, n_eq = 0;
 #pragma unroll
   for (int j = 0; j < kItems; ++j) {
-    const bool in = my0 + j < k1;
-    kk[j] = in ? keys[my0 + j] : 0u;
-    n_gt += in && kk[j] > T;
-    n_eq += in && kk[j] == T;
+    n_gt += j < n_mine && kk[j] > T;
+    n_eq += j < n_mine && kk[j] == T;
   }
   uint32_t tot;
   const uint32_t pre_gt = block_excl_scan(n_gt, sh, &tot);
@@ -533,8 +575,8 @@ __global__ void __launch_bounds__(kSelThreads) select_emit_kernel(const __grid_c
   uint32_t gt_rank = base_gt + pre_gt;
 #pragma unroll
   for (int j = 0; j < kItems; ++j) {
+    if (j >= n_mine) break;
     const int64_t e = my0 + j;
-    if (e >= k1) break;
     const bool take = kk[j] > T || (kk[j] == T && eq_rank < need);
     if (take) {
       const uint32_t pos = gt_rank + min(eq_rank, need);
@@ -668,9 +710,10 @@ extern "C" int kvpool_topk_static(const float* d_scores, int32_t n_rows, int32_t
   const int64_t off_thr = off_sync + up(16LL * n_rows);
   const int64_t off_counts = off_thr + up(8LL * n_rows);
   const int64_t off_sel = off_counts + up(8LL * n_rows * chunks);
+  const int64_t stride = ((int64_t)n_cols + 3) / 4 * 4;  // 16-byte aligned key rows
   const int64_t off_keys = off_sel + up(4LL * n_rows * top_k);
-  const int64_t off_cand = off_keys + up(4LL * n_rows * n_cols);
-  const int64_t need = off_cand + up(8LL * n_rows * n_cols);
+  const int64_t off_cand = off_keys + up(4LL * n_rows * stride);
+  const int64_t need = off_cand + up(8LL * n_rows * stride);
   if (need > (int64_t)kStaticScratchBytes) return KVPOOL_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -699,7 +742,7 @@ extern "C" int kvpool_topk_static(const float* d_scores, int32_t n_rows, int32_t
   P->n = n_rows;
   P->row0 = 0;
   P->keys = reinterpret_cast<uint32_t*>(base + off_keys);
-  P->key_stride = n_cols;
+  P->key_stride = stride;
   P->hist = reinterpret_cast<uint32_t*>(base + off_hist);
   P->counts = reinterpret_cast<uint32_t*>(base + off_counts);
   P->max_key_ctas = (int32_t)chunks;

@@ -15,7 +15,7 @@ constexpr int kMaxKeyCtasPerReq = 256;   // select chunks per request (1M candid
 constexpr int kSelectKeysPerCta = 4096;  // keys handled by one select CTA
 constexpr int kMaxAppendUnits = 512;     // units per append launch
 constexpr int kMaxAttendReqs = 256;      // requests per attend-side launch
-constexpr int kAttendThreadsMax = 544;   // 16 consumer warps + 1 producer warp
+constexpr int kAttendThreadsMax = 288;   // 8 consumer warps (16 dims each) + 1 producer warp
 
 // device error word flags
 enum : uint32_t {
@@ -96,9 +96,12 @@ struct AttendReq {
   int32_t select_all; // k == N_c: every CSA entry is selected
   int32_t score_base; // first score CTA of this request
   int32_t key_base;   // first select CTA of this request
-  int32_t split_base; // first attention split of this request (in the partials)
-  int32_t n_split;    // splits of the whole source list
-  int32_t split_len;  // virtual entries per split
+  // attention: part 0 = [HCA entries | window] (needs no top-k), part 1 =
+  // [selected CSA entries]; each part is split into chunks of its split_len
+  int32_t split_len0, split_len1;  // sources per split of each part
+  int32_t n_split0, n_split1;
+  int32_t cta_base0, cta_base1;  // first attention CTA of each part's launch
+  int32_t part_base;             // first partial slot; part 1 follows part 0
 };
 
 struct AttendParams {
@@ -111,7 +114,8 @@ struct AttendParams {
   int32_t top_k;
   int32_t n;                 // requests in this launch
   int32_t row0;              // first row of q / out for this launch
-  int32_t total_score_ctas, total_key_ctas, total_splits;
+  int32_t total_score_ctas, total_key_ctas;
+  int32_t total_ctas0, total_ctas1;  // attention CTAs of part 0 and part 1
   int32_t segs_per_cta;      // block segments scored by one score CTA
   int32_t src_lo, src_hi;    // attention sources [lo, hi) of the virtual list this launch covers
   // scratch (device pointers)
@@ -136,7 +140,7 @@ int launch_append(const AppendParams& p, int n_layers, void* stream, int* n_kern
 int launch_share(const ShareParams& p, int n_layers, void* stream, int* n_kernels);
 int launch_score(const AttendParams& p, void* stream, int* n_kernels);
 int launch_select(const AttendParams& p, void* stream, int* n_kernels);
-int launch_attend(const AttendParams& p, void* stream, int* n_kernels);
+int launch_attend(const AttendParams& p, int part, int ctas, void* stream, int* n_kernels);
 int launch_combine(const AttendParams& p, void* stream, int* n_kernels);
 
 }  // namespace kvp
