@@ -144,12 +144,12 @@ __device__ __forceinline__ void write_entry(uint8_t* entry, const PoolDesc& pd, 
   }
 }
 
-// Indexer entry: 8 values at xv0 of the [Ih][Id] key, stored chunk-major.
+// Indexer entry: 8 values at xv0 of the [Ih][Id] key, stored chunk-major in
+// the block's indexer part `base`.
 template <int CACHE>
-__device__ __forceinline__ void write_idx(uint8_t* sec, const PoolDesc& pd, const LayerDesc& L, int slot, int xv0,
-                                          const float* x, float s) {
+__device__ __forceinline__ void write_idx(uint8_t* base, const PoolDesc& pd, int slot, int xv0, const float* x,
+                                          float s) {
   const int CB = pd.csa_per_block;
-  uint8_t* base = sec + L.idx_off;
   if constexpr (CACHE == KVPOOL_FP8_E4M3) {
     const int c = xv0 / 16, within = xv0 % 16;
     store8<CACHE>(base + ((int64_t)c * CB + slot) * 16 + within, x, s);
@@ -224,7 +224,9 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   }
 
   const int32_t dst_block = u.block_id >= 0 ? u.block_id : pd.staging_base + u.slot;
-  uint8_t* blk = pd.arena + L.block_pool + (int64_t)dst_block * L.block_bytes;
+  uint8_t* blk_csa = pd.arena + L.csa_pool + (int64_t)dst_block * L.csa_stride;
+  uint8_t* blk_idx = pd.arena + L.idx_pool + (int64_t)dst_block * L.idx_stride;
+  uint8_t* blk_hca = pd.arena + L.hca_pool + (int64_t)dst_block * L.hca_stride;
   uint8_t* ring = pd.arena + L.ring + (int64_t)u.slot * L.ring_req_bytes;
   const int64_t seg_pos0 = (int64_t)u.seg * mp;
 
@@ -263,15 +265,15 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
         }
         if ((t + 1) % m == 0) {  // a CSA group completes: entry slot (t+1)/m - 1 of the block
           const int slot = (t + 1) / m - 1;
-          write_entry<CACHE>(blk + L.csa_off + (int64_t)slot * pd.entry_bytes, pd, v0, half, hv, acc_c, sh);
+          write_entry<CACHE>(blk_csa + (int64_t)slot * pd.entry_bytes, pd, v0, half, hv, acc_c, sh);
           float s = 1.0f;
           if constexpr (CACHE == KVPOOL_FP8_E4M3) {
             const float3 r = block_max3(0.f, 0.f, idx_thread ? amax8(acc_x) : 0.f, sh);
             const uint16_t sb = fp8_scale_bits(r.z);
             s = bf16_bits_to_f32(sb);
-            if (idx_thread && xv0 == 0) *reinterpret_cast<uint16_t*>(blk + L.idx_scale_off + 2 * slot) = sb;
+            if (idx_thread && xv0 == 0) *reinterpret_cast<uint16_t*>(blk_idx + L.idx_scale_off + 2 * slot) = sb;
           }
-          if (idx_thread) write_idx<CACHE>(blk, pd, L, slot, xv0, acc_x, s);
+          if (idx_thread) write_idx<CACHE>(blk_idx, pd, slot, xv0, acc_x, s);
 #pragma unroll
           for (int j = 0; j < kVpt; ++j) acc_c[j] = acc_x[j] = 0.0f;
         }
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
     if (u.block_id < 0) {
       if (tid == 0) flag_error(pd, kErrBadBlock);
     } else {
-      write_entry<CACHE>(blk + L.hca_off, pd, v0, half, hv, acc_h, sh);
+      write_entry<CACHE>(blk_hca, pd, v0, half, hv, acc_h, sh);
     }
   }
   if (L.has_hca && u.t1 < mp) {
@@ -306,23 +308,25 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   // Seal: CSA / indexer entries staged by earlier calls move into the block.
   if (u.block_id >= 0 && L.has_csa && u.t0 >= m) {
     const int n_copy = u.t0 / m;
-    const uint8_t* stg = pd.arena + L.block_pool + (int64_t)(pd.staging_base + u.slot) * L.block_bytes;
+    const int32_t sid = pd.staging_base + u.slot;
+    const uint8_t* stg_csa = pd.arena + L.csa_pool + (int64_t)sid * L.csa_stride;
+    const uint8_t* stg_idx = pd.arena + L.idx_pool + (int64_t)sid * L.idx_stride;
     const int64_t bytes = (int64_t)n_copy * pd.entry_bytes;  // CSA entries, multiple of 16
     const int64_t per = ((bytes / 16 + P.n_slices - 1) / P.n_slices) * 16;
     const int64_t b0 = per * slice, b1 = min(bytes, b0 + per);
     for (int64_t o = b0 + tid * 16; o < b1; o += (int64_t)blockDim.x * 16)
-      *reinterpret_cast<uint4*>(blk + L.csa_off + o) = *reinterpret_cast<const uint4*>(stg + L.csa_off + o);
+      *reinterpret_cast<uint4*>(blk_csa + o) = *reinterpret_cast<const uint4*>(stg_csa + o);
     if (slice == 0) {
       const int CB = pd.csa_per_block;
       for (int i = tid; i < pd.idx_chunks * n_copy; i += blockDim.x) {
         const int c = i / n_copy, e = i % n_copy;
-        const int64_t o = L.idx_off + ((int64_t)c * CB + e) * 16;
-        *reinterpret_cast<uint4*>(blk + o) = *reinterpret_cast<const uint4*>(stg + o);
+        const int64_t o = ((int64_t)c * CB + e) * 16;
+        *reinterpret_cast<uint4*>(blk_idx + o) = *reinterpret_cast<const uint4*>(stg_idx + o);
       }
       if (CACHE == KVPOOL_FP8_E4M3) {
         for (int e = tid; e < n_copy; e += blockDim.x)
-          *reinterpret_cast<uint16_t*>(blk + L.idx_scale_off + 2 * e) =
-              *reinterpret_cast<const uint16_t*>(stg + L.idx_scale_off + 2 * e);
+          *reinterpret_cast<uint16_t*>(blk_idx + L.idx_scale_off + 2 * e) =
+              *reinterpret_cast<const uint16_t*>(stg_idx + L.idx_scale_off + 2 * e);
       }
     }
   }

@@ -56,7 +56,7 @@ __device__ __forceinline__ int64_t source_offset(const AttendParams& P, int i, c
       flag_error(pd, kErrBadBlock);
       return ring;
     }
-    return L.block_pool + (int64_t)bid * L.block_bytes + L.csa_off + (int64_t)(e % CB) * pd.entry_bytes;
+    return L.csa_pool + (int64_t)bid * L.csa_stride + (int64_t)(e % CB) * pd.entry_bytes;
   }
   v -= R.k;
   if (v < R.n_hca) {
@@ -65,7 +65,7 @@ __device__ __forceinline__ int64_t source_offset(const AttendParams& P, int i, c
       flag_error(pd, kErrBadBlock);
       return ring;
     }
-    return L.block_pool + (int64_t)bid * L.block_bytes + L.hca_off;
+    return L.hca_pool + (int64_t)bid * L.hca_stride;
   }
   v -= R.n_hca;
   const int64_t pos = R.length - R.w + v;

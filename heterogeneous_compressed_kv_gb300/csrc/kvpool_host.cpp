@@ -123,25 +123,26 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
     cur = round_up(cur + 4LL * c->heads * c->m_prime, 256);
     d.alpha_idx = cur;
     cur = round_up(cur + 4LL * c->idx_heads * c->m, 256);
-    int64_t off = 0;
-    d.csa_off = d.idx_off = d.idx_scale_off = d.hca_off = -1;
+    const int64_t n_ids = (int64_t)c->max_blocks + c->max_requests;
+    d.csa_pool = d.idx_pool = d.hca_pool = d.idx_scale_off = -1;
+    d.csa_stride = d.idx_stride = d.hca_stride = 0;
     if (d.has_csa) {
-      d.csa_off = off;
-      off += CB * pd.entry_bytes;
-      d.idx_off = off;
-      off += CB * pd.idx_entry_bytes;
+      d.csa_stride = CB * pd.entry_bytes;
+      d.csa_pool = cur;
+      cur = round_up(cur + d.csa_stride * n_ids, 256);
+      d.idx_stride = CB * pd.idx_entry_bytes;
       if (c->cache_dtype == KVPOOL_FP8_E4M3) {
-        d.idx_scale_off = off;
-        off += round_up(2LL * CB, 16);
+        d.idx_scale_off = d.idx_stride;
+        d.idx_stride += round_up(2LL * CB, 16);
       }
+      d.idx_pool = cur;
+      cur = round_up(cur + d.idx_stride * n_ids, 256);
     }
     if (d.has_hca) {
-      d.hca_off = off;
-      off += pd.entry_bytes;
+      d.hca_stride = pd.entry_bytes;
+      d.hca_pool = cur;
+      cur = round_up(cur + d.hca_stride * n_ids, 256);
     }
-    d.block_bytes = round_up(off, 256);
-    d.block_pool = cur;
-    cur = round_up(cur + d.block_bytes * ((int64_t)c->max_blocks + c->max_requests), 256);
     d.ring_req_bytes = round_up((int64_t)c->n_win * pd.entry_bytes, 256);
     d.ring = cur;
     cur += d.ring_req_bytes * c->max_requests;
@@ -276,6 +277,8 @@ struct kvpool {
     }
     return rc;
   }
+  std::vector<float> timeline;  // (kind, start, end) since profiling was enabled
+  cudaEvent_t t0 = nullptr;     // first event of the timeline (kept out of the pool)
   void settle_profile() {
     for (auto& s : prof) {
       cudaEventSynchronize(s.b);
@@ -284,7 +287,14 @@ struct kvpool {
       prof_ms[s.kernel] += ms;
       prof_launches[s.kernel] += s.n_kernels;
       prof_bytes[s.kernel] += s.bytes;
-      event_pool.push_back(s.a);
+      if (!t0) t0 = s.a;
+      float a = 0.f, b = 0.f;
+      cudaEventElapsedTime(&a, t0, s.a);
+      cudaEventElapsedTime(&b, t0, s.b);
+      timeline.push_back((float)s.kernel);
+      timeline.push_back(a);
+      timeline.push_back(b);
+      if (s.a != t0) event_pool.push_back(s.a);
       event_pool.push_back(s.b);
     }
     prof.clear();
@@ -363,6 +373,7 @@ int kvpool_destroy(kvpool_t* p) {
     cudaEventDestroy(s.b);
   }
   for (auto e : p->event_pool) cudaEventDestroy(e);
+  if (p->t0) cudaEventDestroy(p->t0);
   if (p->ev_fork) cudaEventDestroy(p->ev_fork);
   if (p->ev_join) cudaEventDestroy(p->ev_join);
   if (p->side) cudaStreamDestroy(p->side);
@@ -748,12 +759,13 @@ int kvpool_get_layout(const kvpool_t* p, kvpool_layout* out, int32_t layer, kvpo
     const LayerDesc& d = L.layers[layer];
     lo->kind = d.kind;
     lo->pad = 0;
-    lo->block_pool_offset = d.block_pool;
-    lo->block_bytes = d.block_bytes;
-    lo->csa_offset = d.csa_off;
-    lo->idx_offset = d.idx_off;
+    lo->csa_offset = d.csa_pool;
+    lo->csa_block_bytes = d.csa_stride;
+    lo->idx_offset = d.idx_pool;
+    lo->idx_block_bytes = d.idx_stride;
     lo->idx_scale_offset = d.idx_scale_off;
-    lo->hca_offset = d.hca_off;
+    lo->hca_offset = d.hca_pool;
+    lo->hca_block_bytes = d.hca_stride;
     lo->ring_offset = d.ring;
     lo->ring_request_bytes = d.ring_req_bytes;
     lo->acc_offset = d.acc;
@@ -783,6 +795,11 @@ int kvpool_profile_enable(kvpool_t* p, int enable) {
   if (!p) return KVPOOL_ERR_INVALID_ARG;
   if (enable) {
     p->settle_profile();
+    p->timeline.clear();
+    if (p->t0) {
+      p->event_pool.push_back(p->t0);
+      p->t0 = nullptr;
+    }
     for (int k = 0; k < KVPOOL_KERNEL_COUNT; ++k) {
       p->prof_ms[k] = 0;
       p->prof_launches[k] = 0;
@@ -800,6 +817,14 @@ int kvpool_profile_read(kvpool_t* p, int32_t kernel, double* ms_total, int64_t* 
   if (launches) *launches = p->prof_launches[kernel];
   if (bytes) *bytes = p->prof_bytes[kernel];
   return KVPOOL_OK;
+}
+
+int kvpool_profile_timeline(kvpool_t* p, int32_t cap, float* h_out) {
+  if (!p || cap < 0 || (cap > 0 && !h_out)) return KVPOOL_ERR_INVALID_ARG;
+  p->settle_profile();
+  const int32_t n = (int32_t)std::min<size_t>((size_t)cap, p->timeline.size() / 3);
+  std::memcpy(h_out, p->timeline.data(), sizeof(float) * 3 * (size_t)n);
+  return n;
 }
 
 const char* kvpool_last_error(const kvpool_t* p) { return p ? p->err.c_str() : "NULL pool"; }

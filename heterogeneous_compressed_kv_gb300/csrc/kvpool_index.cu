@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(const __grid_co
       id_nxt = block_id((id_batch + 1) * 32 + lane);
     }
     const int32_t bid = __shfl_sync(0xffffffffu, id_cur, jj & 31);
-    return pd.arena + L.block_pool + (int64_t)bid * L.block_bytes + L.idx_off;
+    return pd.arena + L.idx_pool + (int64_t)bid * L.idx_stride;
   };
   uint64_t* my_full = full + warp * ring;
   uint8_t* my_slots = slots + (int64_t)warp * ring * stage_bytes;
@@ -596,6 +596,8 @@ __global__ void __launch_bounds__(kSelThreads) select_emit_kernel(const __grid_c
 
 // Score CTAs of a launch, and the shared-memory plan of the score kernel.
 int score_stage_plan(const PoolDesc& pd, int* stage_bytes, int* ring, int* stage_off, size_t* smem) {
+  // one block's indexer part: keys, then (fp8) scales; the same size as the
+  // indexer plane's stride
   *stage_bytes = pd.csa_per_block * (int)pd.idx_entry_bytes +
                  (pd.cache_dtype == KVPOOL_FP8_E4M3 ? (2 * pd.csa_per_block + 15) / 16 * 16 : 0);
   *ring = std::max(1, std::min(kScoreMaxRing, kScoreStageBudget / (kScoreWarps * *stage_bytes)));

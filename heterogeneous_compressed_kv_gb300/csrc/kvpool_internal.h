@@ -29,8 +29,12 @@ enum : uint32_t {
 struct LayerDesc {
   int32_t kind;
   int32_t has_csa, has_hca;
-  int64_t block_pool, block_bytes;
-  int64_t csa_off, idx_off, idx_scale_off, hca_off;
+  // one plane per part, indexed by block id (ids >= staging_base are the
+  // requests' private staging blocks): CSA entries, indexer keys (+ fp8
+  // scales at idx_scale_off inside a block's part), HCA entry
+  int64_t csa_pool, csa_stride;
+  int64_t idx_pool, idx_stride, idx_scale_off;
+  int64_t hca_pool, hca_stride;
   int64_t ring, ring_req_bytes;
   int64_t acc, acc_req_bytes;  // acc: CSA [2HD] f32, idx [XD] f32, HCA [2HD] f32
   int64_t alpha_csa, alpha_hca, alpha_idx;  // f32 [H][m], [H][m'], [Ih][m]

@@ -27,7 +27,7 @@ EXPORTS = ["kvpool_required_bytes", "kvpool_create", "kvpool_destroy", "kvpool_a
            "kvpool_free_request", "kvpool_share_prefix", "kvpool_append", "kvpool_decode_attend",
            "kvpool_request_info", "kvpool_block_refcount", "kvpool_free_block_count", "kvpool_get_layout",
            "kvpool_check_device", "kvpool_profile_enable", "kvpool_profile_read", "kvpool_last_error",
-           "kvpool_topk_static"]
+           "kvpool_topk_static", "kvpool_profile_timeline"]
 
 
 class KvpoolError(RuntimeError):
@@ -58,9 +58,9 @@ class _Layout(C.Structure):
 
 
 class _LayerLayout(C.Structure):
-    _fields_ = [("kind", C.c_int32), ("pad", C.c_int32), ("block_pool_offset", C.c_int64),
-                ("block_bytes", C.c_int64), ("csa_offset", C.c_int64), ("idx_offset", C.c_int64),
-                ("idx_scale_offset", C.c_int64), ("hca_offset", C.c_int64), ("ring_offset", C.c_int64),
+    _fields_ = [("kind", C.c_int32), ("pad", C.c_int32), ("csa_offset", C.c_int64), ("csa_block_bytes", C.c_int64),
+                ("idx_offset", C.c_int64), ("idx_block_bytes", C.c_int64), ("idx_scale_offset", C.c_int64),
+                ("hca_offset", C.c_int64), ("hca_block_bytes", C.c_int64), ("ring_offset", C.c_int64),
                 ("ring_request_bytes", C.c_int64), ("acc_offset", C.c_int64), ("acc_request_bytes", C.c_int64)]
 
 
@@ -92,6 +92,7 @@ def lib():
         L.kvpool_profile_enable.argtypes = [vp, C.c_int]
         L.kvpool_profile_read.argtypes = [vp, i32, C.POINTER(C.c_double), C.POINTER(i64), C.POINTER(i64)]
         L.kvpool_topk_static.argtypes = [vp, i32, i32, i32, vp, vp]
+        L.kvpool_profile_timeline.argtypes = [vp, i32, vp]
         L.kvpool_last_error.restype = C.c_char_p
         L.kvpool_last_error.argtypes = [vp]
         _lib = L
@@ -267,6 +268,14 @@ class Pool:
 
     def profile_enable(self, on: bool = True) -> None:
         self._check(self.L.kvpool_profile_enable(self.h, 1 if on else 0), "profile_enable")
+
+    def profile_timeline(self, cap: int = 4096):
+        """[(kernel name, start ms, end ms)] of the recorded launches."""
+        buf = np.zeros((cap, 3), np.float32)
+        n = self.L.kvpool_profile_timeline(self.h, cap, buf.ctypes.data_as(C.c_void_p))
+        if n < 0:
+            raise KvpoolError(n, "profile_timeline")
+        return [(KERNEL_NAMES[int(k)], float(a), float(b)) for k, a, b in buf[:n]]
 
     def profile_read(self, kernel: int):
         ms, n, b = C.c_double(), C.c_int64(), C.c_int64()

@@ -224,10 +224,14 @@ int kvpool_free_block_count(const kvpool_t* pool);
  *   + e) * 16 from idx_offset (chunk-major, so a warp reading chunk c of 32
  *   consecutive entries reads 512 contiguous bytes); fp8 scales [csa_per_block]
  *   bf16 at idx_scale_offset.
- * Block section of a layer: csa entries [csa_per_block], indexer keys and
- *   scales, HCA entry; absent parts have offset -1.  Section of block id b at
- *   block_pool_offset + b * block_bytes; ids staging_base + r (r a request
- *   slot) are request r's private staging sections (its open block).
+ * Block parts of a layer, each in its own plane indexed by block id b:
+ *   CSA entries [csa_per_block] at csa_offset + b * csa_block_bytes, indexer
+ *   keys (then fp8 scales at idx_scale_offset) at idx_offset + b *
+ *   idx_block_bytes, the HCA entry at hca_offset + b * hca_block_bytes;
+ *   absent parts have offset -1.  Ids staging_base + r (r a request slot)
+ *   are request r's private staging blocks (its open block).  A request's
+ *   blocks, allocated in order, make its indexer keys and HCA entries
+ *   contiguous runs.
  * Window of request r: ring_offset + r * ring_request_bytes, token at
  *   position p in slot p mod n_win.
  * Compressor accumulators of request r (fp32): acc_offset + r * acc_request_bytes:
@@ -236,8 +240,9 @@ int kvpool_free_block_count(const kvpool_t* pool);
 typedef struct kvpool_layer_layout {
   int32_t kind;
   int32_t pad;
-  int64_t block_pool_offset, block_bytes;
-  int64_t csa_offset, idx_offset, idx_scale_offset, hca_offset;
+  int64_t csa_offset, csa_block_bytes;
+  int64_t idx_offset, idx_block_bytes, idx_scale_offset;
+  int64_t hca_offset, hca_block_bytes;
   int64_t ring_offset, ring_request_bytes;
   int64_t acc_offset, acc_request_bytes;
 } kvpool_layer_layout;
@@ -276,6 +281,13 @@ int kvpool_profile_enable(kvpool_t* pool, int enable);
  * bytes those launches had to move (inputs read + outputs written, scratch
  * excluded). */
 int kvpool_profile_read(kvpool_t* pool, int32_t kernel, double* ms_total, int64_t* launches, int64_t* bytes);
+
+/* Synchronize and write, for up to cap launch records since profiling was
+ * enabled, (kernel kind, start ms, end ms) triples relative to the first
+ * recorded event (h_out: [cap][3] float), in launch order, across the
+ * caller's stream and the pool's side stream; returns the number of records
+ * or a negative error.  Reading it does not reset the totals. */
+int kvpool_profile_timeline(kvpool_t* pool, int32_t cap, float* h_out);
 
 /* Last error message of this pool (never NULL). */
 const char* kvpool_last_error(const kvpool_t* pool);

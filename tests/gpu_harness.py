@@ -108,27 +108,22 @@ class GpuCase:
             else np.zeros(2, np.uint16)
         return code, sc
 
-    def block_section(self, layer, bid):
-        d = self.pool.layout(layer)
-        return d["block_pool_offset"] + bid * d["block_bytes"], d
+    def _bid(self, d, slot, e, ids):
+        seg = e // d["csa_per_block"]
+        return int(ids[seg]) if seg < len(ids) else d["staging_base"] + slot
 
     def csa_entry(self, layer, slot, e, ids, host=None):
         d = self.pool.layout(layer)
         CB = d["csa_per_block"]
-        seg = e // CB
-        bid = int(ids[seg]) if seg < len(ids) else d["staging_base"] + slot
-        base = d["block_pool_offset"] + bid * d["block_bytes"]
-        return self.entry(base + d["csa_offset"] + (e % CB) * d["entry_bytes"], host)
+        base = d["csa_offset"] + self._bid(d, slot, e, ids) * d["csa_block_bytes"]
+        return self.entry(base + (e % CB) * d["entry_bytes"], host)
 
     def idx_entry(self, layer, slot, e, ids, host=None):
         d = self.pool.layout(layer)
         CB = d["csa_per_block"]
-        seg = e // CB
-        bid = int(ids[seg]) if seg < len(ids) else d["staging_base"] + slot
-        base = d["block_pool_offset"] + bid * d["block_bytes"]
+        base = d["idx_offset"] + self._bid(d, slot, e, ids) * d["idx_block_bytes"]
         n_chunks = d["idx_entry_bytes"] // 16
-        code = np.concatenate([self.bytes_at(base + d["idx_offset"] + (c * CB + e % CB) * 16, 16, host)
-                               for c in range(n_chunks)])
+        code = np.concatenate([self.bytes_at(base + (c * CB + e % CB) * 16, 16, host) for c in range(n_chunks)])
         sc = np.zeros(1, np.uint16)
         if self.vs == 1:
             sc = self.bytes_at(base + d["idx_scale_offset"] + 2 * (e % CB), 2, host).copy().view(np.uint16)
@@ -136,7 +131,7 @@ class GpuCase:
 
     def hca_entry(self, layer, bid, host=None):
         d = self.pool.layout(layer)
-        return self.entry(d["block_pool_offset"] + bid * d["block_bytes"] + d["hca_offset"], host)
+        return self.entry(d["hca_offset"] + bid * d["hca_block_bytes"], host)
 
     def window_token(self, layer, slot, pos, host=None):
         d = self.pool.layout(layer)

@@ -82,19 +82,26 @@ def test_layout_is_aligned_and_disjoint(cache):
     for l in range(4):
         d = p.layout(l)
         nb = cfg.max_blocks + cfg.max_requests
-        for key in ("block_pool_offset", "ring_offset", "acc_offset"):
+        kind = d["kind"]
+        for part in ("csa", "idx", "hca"):
+            present = d[f"{part}_offset"] >= 0
+            assert present == (kind in ((K.CSA, K.CSA_HCA) if part != "hca" else (K.HCA, K.CSA_HCA)))
+            if present:
+                assert d[f"{part}_offset"] % 256 == 0 and d[f"{part}_block_bytes"] % 16 == 0
+                spans.append((d[f"{part}_offset"], d[f"{part}_offset"] + nb * d[f"{part}_block_bytes"]))
+            else:
+                assert d[f"{part}_block_bytes"] == 0
+        if kind in (K.CSA, K.CSA_HCA):
+            assert d["csa_block_bytes"] == 32 * lo["entry_bytes"]
+            assert d["idx_block_bytes"] >= 32 * lo["idx_entry_bytes"]
+            assert (d["idx_scale_offset"] == 32 * lo["idx_entry_bytes"]) == (cache == K.FP8_E4M3)
+        if kind in (K.HCA, K.CSA_HCA):
+            assert d["hca_block_bytes"] == lo["entry_bytes"]
+        for key in ("ring_offset", "acc_offset"):
             assert d[key] % 256 == 0
-        assert d["block_bytes"] % 256 == 0 and d["ring_request_bytes"] % 256 == 0
-        spans.append((d["block_pool_offset"], d["block_pool_offset"] + nb * d["block_bytes"]))
+        assert d["ring_request_bytes"] % 256 == 0
         spans.append((d["ring_offset"], d["ring_offset"] + 8 * d["ring_request_bytes"]))
         spans.append((d["acc_offset"], d["acc_offset"] + 8 * d["acc_request_bytes"]))
-        kind = d["kind"]
-        assert (d["csa_offset"] >= 0) == (kind in (K.CSA, K.CSA_HCA))
-        assert (d["hca_offset"] >= 0) == (kind in (K.HCA, K.CSA_HCA))
-        for key in ("csa_offset", "idx_offset", "idx_scale_offset", "hca_offset"):
-            assert d[key] == -1 or d[key] % 16 == 0
-        if kind == K.SWA_ONLY:
-            assert d["block_bytes"] == 0
     spans = sorted(s for s in spans if s[1] > s[0])
     for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
         assert a1 <= b0
