@@ -254,6 +254,7 @@ def main():
     ap.add_argument("--cpu-steps", type=int, default=3)
     ap.add_argument("--requests", type=int, default=0, help="override the request count (profiling cases)")
     ap.add_argument("--context", type=int, default=0, help="override the long-context length (profiling cases)")
+    ap.add_argument("--timeline", type=int, default=0, help="print the launch timeline of this many extra steps")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
@@ -291,7 +292,7 @@ def main():
     B, K_, W_ = w["n_requests"], args.steps, args.warmup
     lengths = [int(x) for x in w["lengths"]]
     mp_ = w["m_prime"]
-    extra = 2 * (K_ + W_) + 2
+    extra = 3 * (K_ + W_) + args.timeline + 2
     mbpr = (max(lengths) + extra) // mp_ + 2
     g = gates(w)
     cfg = K.PoolConfig(m=w["m"], m_prime=mp_, n_win=w["n_win"], heads=w["heads"], head_dim=w["head_dim"],
@@ -355,16 +356,22 @@ def main():
         pool.append(slots, one, k[t], v[t], x[t], stream=sp)
         pool.decode_attend(0, slots, q[t], qi[t], top_k, out, None, stream=sp)
 
+    # warm-up, every kernel kind recorded: the dominant kernel is the one with
+    # the most algorithmic bytes
+    pool.profile_enable(True)
     for t in range(W_):
         step(t, sk, sv, sx, sq, sqi)
     torch.cuda.synchronize()
+    warm = {n: pool.profile_read(i) for i, n in enumerate(K.KERNEL_NAMES)}
+    dom = max(("score", "attend", "append"), key=lambda n: warm[n][2])
 
     def barrier():
         if world > 1:
             dist.barrier()
 
+    # timed region: events only around the dominant kernel's launches
     clocks = Clocks(local)
-    pool.profile_enable(True)
+    pool.profile_enable(True, kinds=[K.KERNEL_NAMES.index(dom)])
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
@@ -378,13 +385,37 @@ def main():
     clk = clocks.stop()
     barrier()
     ms = ev0.elapsed_time(ev1)
-    prof = {n: pool.profile_read(i) for i, n in enumerate(K.KERNEL_NAMES)}
-    pool.profile_enable(False)
+    d_ms, d_n, d_b = pool.profile_read(K.KERNEL_NAMES.index(dom))
     pool.check_device(sp)
     if world > 1:
         t = torch.tensor([ms], dtype=torch.float64)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
+
+    # per-kernel breakdown: a second pass over the same step inputs, every
+    # launch between events (the events themselves cost a little time)
+    KB = min(K_, 200)
+    pool.profile_enable(True)
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for t in range(W_, W_ + KB):
+        step(t, sk, sv, sx, sq, sqi)
+    b1.record(stream)
+    torch.cuda.synchronize()
+    breakdown_ms = b0.elapsed_time(b1)
+    prof = {n: pool.profile_read(i) for i, n in enumerate(K.KERNEL_NAMES)}
+    pool.profile_enable(False)
+    pool.check_device(sp)
+
+    if args.timeline:
+        pool.profile_enable(True)
+        for t in range(args.timeline):
+            step(W_ + t, sk, sv, sx, sq, sqi)
+        torch.cuda.synchronize()
+        tl = pool.profile_timeline()
+        pool.profile_enable(False)
+        for name, a, b in tl:
+            print(f"timeline {name:8s} {a * 1e3:9.1f} {b * 1e3:9.1f} {1e3 * (b - a):8.1f} us", file=sys.stderr)
 
     # ---- end to end: pinned host inputs in, result out, every step ----
     ek, ev_, ex, eq, eqi = step_inputs(W_ + K_, W_ + K_)
@@ -427,18 +458,15 @@ def main():
     tokens = B * K_ * world
     value = tokens / (ms / 1e3)
     e2e_value = tokens / (e2e_ms / 1e3)
-    step_bytes = sum(b for (_, _, b) in prof.values()) / K_
+    step_bytes = sum(b for (_, _, b) in prof.values()) / KB
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
-    # dominant kernel: the one with the most algorithmic bytes
-    dom = max(("score", "attend", "append"), key=lambda n: prof[n][2])
-    d_ms, d_n, d_b = prof[dom]
     src = {"score": "heterogeneous_compressed_kv_gb300/csrc/kvpool_index.cu",
            "attend": "heterogeneous_compressed_kv_gb300/csrc/kvpool_attend.cu",
            "append": "heterogeneous_compressed_kv_gb300/csrc/kvpool_append.cu"}[dom]
     launches_dom = d_n
     achieved = (d_b / launches_dom) / (d_ms / launches_dom / 1e3) / 1e9 if d_ms > 0 else None
-    launches = sum(n for (_, n, _) in prof.values())
+    launches = round(sum(n for (_, n, _) in prof.values()) * K_ / KB)
 
     if rank != 0:
         return
@@ -451,9 +479,11 @@ def main():
                 hbm_gbs=step_bytes / (ms / K_ / 1e3) / 1e9,
                 hbm_frac_of_8tbs=step_bytes / (ms / K_ / 1e3) / 1e9 / NOMINAL_HBM_GBS,
                 hbm_frac_of_measured=step_bytes / (ms / K_ / 1e3) / 1e9 / hbm_peak,
-                kernels={n: dict(ms_per_step=pm / K_, launches=pn, gb_per_step=pb / K_ / 1e9,
+                kernels={n: dict(ms_per_step=pm / KB, launches=pn, gb_per_step=pb / KB / 1e9,
                                  gbs=(pb / (pm / 1e3) / 1e9) if pm > 0 else None)
                          for n, (pm, pn, pb) in prof.items()},
+                kernels_pass=dict(steps=KB, ms_per_step=breakdown_ms / KB,
+                                  note="separate pass over the same inputs, every launch between CUDA events"),
                 roofline=dict(kernel=dom, bound="hbm", achieved=achieved, peak=hbm_peak, unit="GB/s",
                               frac=(achieved / hbm_peak) if achieved else None,
                               traffic=traffic_record(dom, src), peak_source=peak_kind,

@@ -5,16 +5,19 @@
 //
 // A request's sources are one virtual list [selected CSA entries | HCA
 // entries | window tokens]; every source is one contiguous entry of
-// entry_bytes ([K | V] codes, fp8 scales), so one 1-D bulk copy (TMA) moves
-// it into shared memory wherever it lives (a shared block, the request's
-// staging block or its window ring).  A CTA takes one split of the list: its
-// producer warp streams the split's entries through a ring of stages guarded
-// by mbarriers; consumer threads (8 dims of one head each) run an online
-// softmax in the log2 domain and write a partial (max, sum, output) per head.
-// Consumer thread = 16 dims of one head; q.k takes mixed-precision FMAs
-// (f16 or bf16 products, exact in fp32) when the query is exactly
-// representable; fp8 values are weighted by p * scale rounded to f16.
-// A merge kernel combines the partials.  All waits are time-limited.
+// entry_bytes ([K | V] codes, fp8 scales), so a 1-D bulk copy (TMA) moves it
+// into shared memory wherever it lives (a shared block, the request's
+// staging block or its window ring); entries that follow each other in
+// memory move in one copy.  A CTA takes one split of the list: its producer
+// warp streams the split's entries through a ring of stages guarded by
+// mbarriers (lane e copies entry e of a stage); consumer threads (16 dims of
+// one head each) run an online softmax in the log2 domain and write a
+// partial (max, sum, output) per head.  Scores: with an fp8 cache and a bf16
+// query, tensor-core MMAs on the e4m3 codes (the query split into two exact
+// e4m3 pieces); otherwise mixed-precision FMAs (f16 or bf16 products, exact
+// in fp32) when the query is exactly representable, plain fp32 FMAs if not.
+// fp8 values are weighted by p * scale rounded to f16.  A merge kernel
+// combines the partials.  All waits are time-limited.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -26,6 +29,7 @@ namespace {
 
 constexpr int kStages = 4;
 constexpr int kMaxSplitLen = 1024;
+constexpr int kUnroll = 4;  // entries per online-softmax update
 
 __device__ __forceinline__ int find_split_req(const AttendParams& P, int cta, int part) {
   int lo = 0, hi = P.n - 1;
@@ -72,76 +76,319 @@ __device__ __forceinline__ int64_t source_offset(const AttendParams& P, int i, c
   return ring + (pos % pd.n_win) * pd.entry_bytes;
 }
 
-__device__ __forceinline__ float fma_f16(uint16_t a, uint16_t b, float c) {
-  float d;
-  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
-  return d;
+// ---- shared-memory loads and number formats of the consumer loop ----------
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
 }
-__device__ __forceinline__ float fma_bf16(uint16_t a, uint16_t b, float c) {
-  float d;
-  asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
-  return d;
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
 }
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  uint32_t h;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)two));
-  return h;
+// four e4m3 codes -> two f16x2 words (exact)
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
-__device__ __forceinline__ float f16_to_f32(uint32_t h) { return __half2float(__ushort_as_half((uint16_t)h)); }
+// c0 += lo(a) * lo(b), c1 += hi(a) * hi(b): f16 (or bf16) operands, products
+// exact in fp32, fp32 accumulation
+__device__ __forceinline__ void fma_f16x2(uint32_t a, uint32_t b, float& c0, float& c1) {
+  asm("{.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %0;\n\tfma.rn.f32.f16 %1, ah, bh, %1;}"
+      : "+f"(c0), "+f"(c1)
+      : "r"(a), "r"(b));
+}
+__device__ __forceinline__ void fma_bf16x2(uint32_t a, uint32_t b, float& c0, float& c1) {
+  asm("{.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %1, ah, bh, %1;}"
+      : "+f"(c0), "+f"(c1)
+      : "r"(a), "r"(b));
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float f16lo_to_f32(uint32_t w) { return __half2float(__ushort_as_half((uint16_t)(w & 0xFFFFu))); }
+__device__ __forceinline__ float f16hi_to_f32(uint32_t w) { return __half2float(__ushort_as_half((uint16_t)(w >> 16))); }
 
-// Sixteen consecutive cache values of one entry (K or V part of one head) in
-// shared memory: as f16 pairs (fp8), bf16 pairs, or fp32.
-template <int CACHE>
-struct Row16;
-template <>
-struct Row16<KVPOOL_FP8_E4M3> {  // 16 B -> 8 f16x2 words
-  __device__ static void load(const uint8_t* p, uint32_t* w) {
-    const uint4 a = *reinterpret_cast<const uint4*>(p);
-    const uint32_t b[4] = {a.x, a.y, a.z, a.w};
+// Dot product of the query's 16 dims with 16 key values at shared address a.
+// FAST: the query is exact in the mixed-precision operand type (f16 for an
+// fp8 cache, bf16 for a bf16 cache) and qw holds it as pairs; otherwise qf.
+template <int CACHE, bool FAST>
+__device__ __forceinline__ float dot16(uint32_t a, const uint32_t* qw, const float* qf) {
+  float c0 = 0.0f, c1 = 0.0f;
+  if constexpr (CACHE == KVPOOL_FP8_E4M3) {
+    const uint4 r = lds128(a);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      w[2 * i] = e4m3x2_to_f16x2(b[i] & 0xFFFFu);
-      w[2 * i + 1] = e4m3x2_to_f16x2(b[i] >> 16);
+      uint32_t lo, hi;
+      e4m3x4_to_f16x4(w[i], lo, hi);
+      if constexpr (FAST) {
+        fma_f16x2(lo, qw[2 * i], c0, c1);
+        fma_f16x2(hi, qw[2 * i + 1], c0, c1);
+      } else {
+        c0 = fmaf(qf[4 * i], f16lo_to_f32(lo), c0);
+        c1 = fmaf(qf[4 * i + 1], f16hi_to_f32(lo), c1);
+        c0 = fmaf(qf[4 * i + 2], f16lo_to_f32(hi), c0);
+        c1 = fmaf(qf[4 * i + 3], f16hi_to_f32(hi), c1);
+      }
     }
-  }
-};
-template <>
-struct Row16<KVPOOL_BF16> {  // 32 B -> 8 bf16x2 words
-  __device__ static void load(const uint8_t* p, uint32_t* w) {
-    const uint4 a = *reinterpret_cast<const uint4*>(p), b = *reinterpret_cast<const uint4*>(p + 16);
-    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-  }
-};
-template <>
-struct Row16<KVPOOL_F32> {  // 64 B -> 16 fp32 bit patterns
-  __device__ static void load(const uint8_t* p, uint32_t* w) {
+  } else if constexpr (CACHE == KVPOOL_BF16) {
+    const uint4 r0 = lds128(a), r1 = lds128(a + 16);
+    const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if constexpr (FAST) {
+        fma_bf16x2(w[i], qw[i], c0, c1);
+      } else {
+        c0 = fmaf(qf[2 * i], bf16_bits_to_f32(w[i] & 0xFFFFu), c0);
+        c1 = fmaf(qf[2 * i + 1], __uint_as_float(w[i] & 0xFFFF0000u), c1);
+      }
+    }
+  } else {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 a = *reinterpret_cast<const uint4*>(p + 16 * i);
-      w[4 * i] = a.x; w[4 * i + 1] = a.y; w[4 * i + 2] = a.z; w[4 * i + 3] = a.w;
+      const uint4 r = lds128(a + 16 * i);
+      c0 = fmaf(qf[4 * i], __uint_as_float(r.x), c0);
+      c1 = fmaf(qf[4 * i + 1], __uint_as_float(r.y), c1);
+      c0 = fmaf(qf[4 * i + 2], __uint_as_float(r.z), c0);
+      c1 = fmaf(qf[4 * i + 3], __uint_as_float(r.w), c1);
     }
   }
-};
-
-// value j (0..15) of a loaded row as fp32
-template <int CACHE>
-__device__ __forceinline__ float row_value(const uint32_t* w, int j) {
-  if constexpr (CACHE == KVPOOL_F32) return __uint_as_float(w[j]);
-  else if constexpr (CACHE == KVPOOL_BF16) return bf16_bits_to_f32((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
-  else return f16_to_f32((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu));
+  return c0 + c1;
 }
 
-// TPH: consumer threads per head (head_dim / 16); each owns 16 dims
+// o[0..16) += weight * (16 values at shared address a).  fp8: the weight is
+// p times the entry's V scale rounded to f16, so its products with the f16
+// values are exact; bf16 / fp32: p in fp32.
+template <int CACHE>
+__device__ __forceinline__ void acc16(uint32_t a, float wgt, float* o) {
+  if constexpr (CACHE == KVPOOL_FP8_E4M3) {
+    const uint32_t h = __half_as_ushort(__float2half_rn(wgt));
+    const uint32_t h2 = h | (h << 16);
+    const uint4 r = lds128(a);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t lo, hi;
+      e4m3x4_to_f16x4(w[i], lo, hi);
+      fma_f16x2(lo, h2, o[4 * i], o[4 * i + 1]);
+      fma_f16x2(hi, h2, o[4 * i + 2], o[4 * i + 3]);
+    }
+  } else if constexpr (CACHE == KVPOOL_BF16) {
+    const uint4 r0 = lds128(a), r1 = lds128(a + 16);
+    const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      o[2 * i] = fmaf(wgt, bf16_bits_to_f32(w[i] & 0xFFFFu), o[2 * i]);
+      o[2 * i + 1] = fmaf(wgt, __uint_as_float(w[i] & 0xFFFF0000u), o[2 * i + 1]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 r = lds128(a + 16 * i);
+      o[4 * i] = fmaf(wgt, __uint_as_float(r.x), o[4 * i]);
+      o[4 * i + 1] = fmaf(wgt, __uint_as_float(r.y), o[4 * i + 1]);
+      o[4 * i + 2] = fmaf(wgt, __uint_as_float(r.z), o[4 * i + 2]);
+      o[4 * i + 3] = fmaf(wgt, __uint_as_float(r.w), o[4 * i + 3]);
+    }
+  }
+}
+
+// Online-softmax update over NU entries starting at shared address a0
+// (entries ES bytes apart): scores in the log2 domain, then the weighted V.
+template <int CACHE, bool FAST, int TPH, int NU>
+__device__ __forceinline__ void update(uint32_t a0, uint32_t ES, uint32_t koff, uint32_t voff, uint32_t soff,
+                                       float qscale, const uint32_t* qw, const float* qf, float& m_run,
+                                       float& l_run, float* o) {
+  float sc[NU], vsc[NU];
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    const uint32_t a = a0 + u * ES;
+    float d = dot16<CACHE, FAST>(a + koff, qw, qf);
+#pragma unroll
+    for (int off = TPH / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+    if constexpr (CACHE == KVPOOL_FP8_E4M3) {
+      const uint32_t s2 = lds32(a + soff);  // K scale (low half), V scale (high half)
+      sc[u] = d * (qscale * bf16_bits_to_f32(s2 & 0xFFFFu));
+      vsc[u] = __uint_as_float(s2 & 0xFFFF0000u);
+    } else {
+      sc[u] = d * qscale;
+      vsc[u] = 1.0f;
+    }
+  }
+  float mx = m_run;
+#pragma unroll
+  for (int u = 0; u < NU; ++u) mx = fmaxf(mx, sc[u]);
+  const float corr = ex2(m_run - mx);
+  l_run *= corr;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) o[j] *= corr;
+#pragma unroll
+  for (int u = 0; u < NU; ++u) {
+    const float p = ex2(sc[u] - mx);
+    l_run += p;
+    acc16<CACHE>(a0 + u * ES + voff, p * vsc[u], o);
+  }
+  m_run = mx;
+}
+
+// ---- tensor-core scores: fp8 cache, bf16 query, head_dim 128 --------------
+// q.k of 4 entries x 4 heads is one m16n8k32 e4m3 MMA per 32 dims: A rows are
+// (head, entry) key rows straight from the staged entries, B columns are
+// (head, piece) query pieces.  A head's bf16 query scaled by 2^s (largest
+// magnitude in [128, 256)) is the exact sum of two e4m3 numbers per element
+// (8 significant bits = 4 + 4) for elements down to 2^-2 after scaling;
+// smaller ones keep their bits above 2^-10 (an error below 2^-17 of the
+// head's largest element).  Products of e4m3 values are exact.
+
+// Query pieces of this warp's 4 heads as the B fragments of the 4 MMAs of a
+// 128-dim head (bq[4c + r]: chunk c of 64 dims), and the factor that undoes
+// the scaling (times log2(e) / sqrt(d)).  Lane L holds the 16 query values
+// of head L / 8, dims 16 (L % 8) ...; the MMA k index is permuted so that a
+// lane's A bytes of one row are 16 contiguous dims.
+__device__ __forceinline__ void q_pieces_fp8(const float* qf, int lane, float qscale, uint32_t* bq, float& fq) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(qf[j]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+  int sh = amax > 0.0f ? 7 - ((int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127) : 0;
+  sh = max(-126, min(126, sh));
+  const float up = __uint_as_float((uint32_t)(127 + sh) << 23);
+  fq = qscale * __uint_as_float((uint32_t)(127 - sh) << 23);
+  uint32_t p0[4], p1[4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float x0 = qf[2 * j] * up, x1 = qf[2 * j + 1] * up;
+    const uint16_t c1 = f32x2_to_e4m3x2(x0, x1);
+    const float2 v1 = e4m3x2_to_f32x2(c1);
+    const uint16_t c2 = f32x2_to_e4m3x2(x0 - v1.x, x1 - v1.y);
+    if (j & 1) {
+      p0[j >> 1] |= (uint32_t)c1 << 16;
+      p1[j >> 1] |= (uint32_t)c2 << 16;
+    } else {
+      p0[j >> 1] = c1;
+      p1[j >> 1] = c2;
+    }
+  }
+  // B lane (g, t), chunk c: piece g & 1 of head g >> 1, dims 64c + 16t + [0, 16)
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int src = 8 * (g >> 1) + 4 * c + t;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint32_t a = __shfl_sync(0xffffffffu, p0[r], src);
+      const uint32_t b = __shfl_sync(0xffffffffu, p1[r], src);
+      bq[4 * c + r] = (g & 1) ? b : a;
+    }
+  }
+}
+
+__device__ __forceinline__ void mma_e4m3(float* d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Online-softmax update over NU (<= 4) entries starting at shared address a0:
+// MMA scores (rows of entries past NU repeat the last one and are ignored),
+// then the weighted V on CUDA cores.  arow: this lane's A row offset in an
+// entry ((4 warp + g / 4) * 128 + 16 t).
+template <int NU>
+__device__ __forceinline__ void update_tc(uint32_t a0, uint32_t ES, uint32_t arow, uint32_t voff, uint32_t soff,
+                                          int lane, const uint32_t* bq, float fq, float& m_run, float& l_run,
+                                          float* o) {
+  const uint32_t ra = a0 + (uint32_t)min((lane >> 2) & 3, NU - 1) * ES + arow;  // row g
+  const uint32_t rb = ra + 256;                                                 // row g + 8: head + 2
+  float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const uint4 lo = lds128(ra + 64 * c), hi = lds128(rb + 64 * c);
+    mma_e4m3(d, lo.x, hi.x, lo.y, hi.y, bq[4 * c], bq[4 * c + 1]);
+    mma_e4m3(d, lo.z, hi.z, lo.w, hi.w, bq[4 * c + 2], bq[4 * c + 3]);
+  }
+  // lane (g, t) holds head t, entry g & 3 when t & 1 == g / 4 (both pieces summed)
+  const float u = (lane & 3) < 2 ? d[0] + d[1] : d[2] + d[3];
+  const int hh = lane >> 3;  // this lane's head in the V phase
+  float sc[NU], vsc[NU];
+#pragma unroll
+  for (int e = 0; e < NU; ++e) {
+    const float dot = __shfl_sync(0xffffffffu, u, 16 * (hh & 1) + 4 * e + hh);
+    const uint32_t s2 = lds32(a0 + e * ES + soff);  // K scale (low half), V scale (high half)
+    sc[e] = dot * (fq * bf16_bits_to_f32(s2 & 0xFFFFu));
+    vsc[e] = __uint_as_float(s2 & 0xFFFF0000u);
+  }
+  float mx = m_run;
+#pragma unroll
+  for (int e = 0; e < NU; ++e) mx = fmaxf(mx, sc[e]);
+  const float corr = ex2(m_run - mx);
+  l_run *= corr;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) o[j] *= corr;
+#pragma unroll
+  for (int e = 0; e < NU; ++e) {
+    const float p = ex2(sc[e] - mx);
+    l_run += p;
+    acc16<KVPOOL_FP8_E4M3>(a0 + e * ES + voff, p * vsc[e], o);
+  }
+  m_run = mx;
+}
+
+__device__ __forceinline__ void consume_stage_tc(uint32_t base, int ne, uint32_t ES, uint32_t arow, uint32_t voff,
+                                                 uint32_t soff, int lane, const uint32_t* bq, float fq, float& m_run,
+                                                 float& l_run, float* o) {
+  int e0 = 0;
+  for (; e0 + 4 <= ne; e0 += 4) update_tc<4>(base + e0 * ES, ES, arow, voff, soff, lane, bq, fq, m_run, l_run, o);
+  switch (ne - e0) {
+    case 3: update_tc<3>(base + e0 * ES, ES, arow, voff, soff, lane, bq, fq, m_run, l_run, o); break;
+    case 2: update_tc<2>(base + e0 * ES, ES, arow, voff, soff, lane, bq, fq, m_run, l_run, o); break;
+    case 1: update_tc<1>(base + e0 * ES, ES, arow, voff, soff, lane, bq, fq, m_run, l_run, o); break;
+    default: break;
+  }
+}
+
+// Online-softmax updates over the ne entries of one stage, kUnroll at a time.
+template <int CACHE, bool FAST, int TPH>
+__device__ __forceinline__ void consume_stage(uint32_t base, int ne, uint32_t ES, uint32_t koff, uint32_t voff,
+                                              uint32_t soff, float qscale, const uint32_t* qw, const float* qf,
+                                              float& m_run, float& l_run, float* o) {
+  int e0 = 0;
+  for (; e0 + kUnroll <= ne; e0 += kUnroll)
+    update<CACHE, FAST, TPH, kUnroll>(base + e0 * ES, ES, koff, voff, soff, qscale, qw, qf, m_run, l_run, o);
+  switch (ne - e0) {
+    case 3: update<CACHE, FAST, TPH, 3>(base + e0 * ES, ES, koff, voff, soff, qscale, qw, qf, m_run, l_run, o); break;
+    case 2: update<CACHE, FAST, TPH, 2>(base + e0 * ES, ES, koff, voff, soff, qscale, qw, qf, m_run, l_run, o); break;
+    case 1: update<CACHE, FAST, TPH, 1>(base + e0 * ES, ES, koff, voff, soff, qscale, qw, qf, m_run, l_run, o); break;
+    default: break;
+  }
+}
+
+// TPH: consumer threads per head (head_dim / 16); each owns 16 dims.  One
+// CTA per split: a producer warp streams the split's entries through a ring
+// of kStages stages (lane e copies entry e of a stage; entries that follow
+// each other in memory go in one copy); the consumer threads run the online
+// softmax and write the split's partial.
 template <int IN, int CACHE, int TPH>
-__global__ void __launch_bounds__(kAttendThreadsMax) attend_kernel(const __grid_constant__ AttendParams P, int e_stage,
-                                                                   int part) {
+__global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __grid_constant__ AttendParams P,
+                                                                      int e_stage, int part) {
   extern __shared__ __align__(128) uint8_t smem[];
   const PoolDesc& pd = P.pool;
   const int HD = pd.HD;
-  const int n_act = HD / 16;                    // consumer threads with work
-  const int n_cons = (n_act + 31) / 32 * 32;    // whole consumer warps
-  const int n_cons_warps = n_cons / 32;
+  const int n_act = HD / 16;                  // consumer threads with work
+  const int n_cons = (n_act + 31) / 32 * 32;  // whole consumer warps
   const int tid = threadIdx.x;
+  const uint32_t ES = (uint32_t)pd.entry_bytes;
+  const uint32_t stage_bytes = (uint32_t)e_stage * ES;
   const int i = find_split_req(P, blockIdx.x, part);
   const AttendReq& R = P.reqs[i];
   const int split = blockIdx.x - (part ? R.cta_base1 : R.cta_base0);
@@ -149,61 +396,24 @@ __global__ void __launch_bounds__(kAttendThreadsMax) attend_kernel(const __grid_
   const int lo = part ? 0 : R.k, hi = part ? R.k : R.k + R.n_hca + R.w;
   const int len = part ? R.split_len1 : R.split_len0;
   const int v0 = lo + split * len;
-  const int v1 = min(hi, v0 + len);
-  const int cnt = v1 - v0;
-  const int64_t ES = pd.entry_bytes;
-  const int64_t pslot = R.part_base + (part ? R.n_split0 : 0) + split;  // partial slot
+  const int cnt = min(hi, v0 + len) - v0;
+  const int n_st = (cnt + e_stage - 1) / e_stage;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kStages;
   uint8_t* stage_mem = smem + 64;
-  const int64_t stage_bytes = (int64_t)e_stage * ES;
-
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], n_cons_warps);
+      mbar_init(&empty[s], n_cons / 32);
     }
     mbar_fence_init();
   }
-  // consumer: head h, dims [dd0, dd0 + 16); the query row of this thread
-  const bool act = tid < n_act;
-  const int h = act ? tid / TPH : 0;
-  const int dd0 = act ? (tid % TPH) * 16 : 0;
-  float qf[16];
-  uint32_t qw[8];  // the query as f16 pairs (fp8 cache) or bf16 pairs (bf16 cache)
-  int exact = 1;
-  if (tid < n_cons) {
-    const int64_t base = (int64_t)(P.row0 + i) * HD + h * pd.head_dim + dd0;
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      qf[j] = IN == KVPOOL_F32 ? reinterpret_cast<const float*>(P.q)[base + j]
-                               : bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(P.q)[base + j]);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint32_t lo16 = 0, hi16 = 0;
-      if constexpr (CACHE == KVPOOL_FP8_E4M3) {
-        const __half a = __float2half_rn(qf[2 * j]), b = __float2half_rn(qf[2 * j + 1]);
-        exact &= (__half2float(a) == qf[2 * j]) && (__half2float(b) == qf[2 * j + 1]);
-        lo16 = __half_as_ushort(a);
-        hi16 = __half_as_ushort(b);
-      } else if constexpr (CACHE == KVPOOL_BF16) {
-        lo16 = f32_to_bf16_bits(qf[2 * j]);
-        hi16 = f32_to_bf16_bits(qf[2 * j + 1]);
-        exact &= (bf16_bits_to_f32(lo16) == qf[2 * j]) && (bf16_bits_to_f32(hi16) == qf[2 * j + 1]);
-      } else {
-        exact = 0;
-      }
-      qw[j] = lo16 | (hi16 << 16);
-    }
-  }
-  const bool fast = __syncthreads_and(tid < n_cons ? exact : 1) != 0;
+  __syncthreads();
 
-  const int n_st = (cnt + e_stage - 1) / e_stage;
   if (tid >= n_cons) {
-    // producer warp: lanes compute source addresses 32 at a time, one batch
-    // ahead of the copies; lane 0 issues the bulk copies of each stage
-    const int lane = tid - n_cons;
+    // ---- producer warp: source addresses 32 at a time, one batch ahead ----
+    const int lane = tid & 31;
     int64_t cur = lane < cnt ? source_offset(P, i, R, v0 + lane) : 0;
     int64_t nxt = 32 + lane < cnt ? source_offset(P, i, R, v0 + 32 + lane) : 0;
     int batch = 0;
@@ -216,111 +426,121 @@ __global__ void __launch_bounds__(kAttendThreadsMax) attend_kernel(const __grid_
       if (!ok) break;
       const int e0 = st * e_stage;
       const int ne = min(e_stage, cnt - e0);
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(ne * ES));
-      uint8_t* dst = stage_mem + s * stage_bytes;
-      for (int e = 0; e < ne; ++e) {
-        const int x = e0 + e;
-        if ((x >> 5) != batch) {  // next batch of addresses; start the one after it
-          batch = x >> 5;
-          cur = nxt;
-          const int y = (batch + 1) * 32 + lane;
-          nxt = y < cnt ? source_offset(P, i, R, v0 + y) : 0;
-        }
-        const int64_t a = __shfl_sync(0xffffffffu, cur, x & 31);
-        if (lane == 0) bulk_g2s(dst + e * ES, pd.arena + a, (uint32_t)ES, &full[s]);
+      if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)ne * ES);
+      __syncwarp();
+      const int x = e0 + lane;
+      const int64_t ac = __shfl_sync(0xffffffffu, cur, x & 31);
+      const int64_t an = __shfl_sync(0xffffffffu, nxt, x & 31);
+      const int64_t a = (x >> 5) == batch ? ac : an;
+      // lane e starts a copy unless entry e - 1 ends right where entry e begins
+      const int64_t prev = __shfl_up_sync(0xffffffffu, a, 1);
+      const bool start = lane < ne && (lane == 0 || a != prev + (int64_t)ES);
+      const uint32_t starts = __ballot_sync(0xffffffffu, start);
+      if (start) {
+        const uint32_t later = starts & ~((2u << lane) - 1u);
+        const int end = later ? __ffs(later) - 1 : ne;
+        bulk_g2s(stage_mem + (size_t)s * stage_bytes + (size_t)lane * ES, pd.arena + a, (uint32_t)(end - lane) * ES,
+                 &full[s]);
+      }
+      if (((e0 + ne) >> 5) != batch) {  // the next stage starts in the next batch
+        ++batch;
+        cur = nxt;
+        const int y = (batch + 1) * 32 + lane;
+        nxt = y < cnt ? source_offset(P, i, R, v0 + y) : 0;
       }
       issued = st + 1;
     }
     if (!ok && lane == 0)  // drain the copies still in flight before leaving
-      for (int st = max(0, issued - kStages); st < issued; ++st) mbar_wait(&full[st % kStages], (st / kStages) & 1, pd);
+      for (int t = max(0, issued - kStages); t < issued; ++t) mbar_wait(&full[t % kStages], (t / kStages) & 1, pd);
     return;
   }
 
+  // ---- consumers: head h, dims [dd0, dd0 + 16) ----
+  const int lane = tid & 31;
+  const bool act = tid < n_act;
+  const int h = act ? tid / TPH : 0;
+  const int dd0 = act ? (tid % TPH) * 16 : 0;
   // scores in the log2 domain: dot(q, k) * log2(e) / sqrt(d) (* fp8 K scale)
   const float qscale = 1.4426950408889634f * rsqrtf((float)pd.head_dim);
+  const uint32_t koff = (uint32_t)((h * pd.head_dim + dd0) * pd.vs);
+  const uint32_t voff = (uint32_t)(HD * pd.vs) + koff;
+  const uint32_t soff = (uint32_t)(2 * HD * pd.vs);
+  const uint32_t stage0 = smem_addr(stage_mem);
+  // the thread's 16 query values; the mixed-precision path needs them exact in
+  // its operand type (decided per warp: every lane or none)
+  float qf[16];
+  uint32_t qw[8];
+  int exact = 1;
+  const uint8_t* qrow =
+      reinterpret_cast<const uint8_t*>(P.q) + ((int64_t)(P.row0 + i) * HD + h * pd.head_dim + dd0) * pd.isz;
+  if constexpr (IN == KVPOOL_F32) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 r = *reinterpret_cast<const uint4*>(qrow + 16 * c);
+      qf[4 * c] = __uint_as_float(r.x);
+      qf[4 * c + 1] = __uint_as_float(r.y);
+      qf[4 * c + 2] = __uint_as_float(r.z);
+      qf[4 * c + 3] = __uint_as_float(r.w);
+    }
+  } else {
+    const uint4 r0 = *reinterpret_cast<const uint4*>(qrow), r1 = *reinterpret_cast<const uint4*>(qrow + 16);
+    const uint32_t wq[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      qf[2 * j] = bf16_bits_to_f32(wq[j] & 0xFFFFu);
+      qf[2 * j + 1] = __uint_as_float(wq[j] & 0xFFFF0000u);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t lo16 = 0, hi16 = 0;
+    if constexpr (CACHE == KVPOOL_FP8_E4M3) {
+      const __half a = __float2half_rn(qf[2 * j]), b = __float2half_rn(qf[2 * j + 1]);
+      exact &= (__half2float(a) == qf[2 * j]) && (__half2float(b) == qf[2 * j + 1]);
+      lo16 = __half_as_ushort(a);
+      hi16 = __half_as_ushort(b);
+    } else if constexpr (CACHE == KVPOOL_BF16) {
+      lo16 = f32_to_bf16_bits(qf[2 * j]);
+      hi16 = f32_to_bf16_bits(qf[2 * j + 1]);
+      exact &= (bf16_bits_to_f32(lo16) == qf[2 * j]) && (bf16_bits_to_f32(hi16) == qf[2 * j + 1]);
+    } else {
+      exact = 0;
+    }
+    qw[j] = lo16 | (hi16 << 16);
+  }
+  const bool fast = __all_sync(0xffffffffu, exact) != 0;
+  // tensor-core scores: fp8 cache, bf16 query, 128-dim heads in groups of 4
+  // (warp w: heads 4w .. 4w + 3)
+  constexpr bool kTC = CACHE == KVPOOL_FP8_E4M3 && IN == KVPOOL_BF16 && TPH == 8;
+  const bool tc = kTC && pd.heads % 4 == 0;
+  const uint32_t arow = (uint32_t)((4 * (tid >> 5) + (lane >> 4)) * 128 + 16 * (lane & 3));
+  uint32_t bq[8];
+  float fq = 0.0f;
+  if (tc) q_pieces_fp8(qf, lane, qscale, bq, fq);
+
   float m_run = -INFINITY, l_run = 0.0f, o[16];
 #pragma unroll
   for (int j = 0; j < 16; ++j) o[j] = 0.0f;
-  const int koff = (h * pd.head_dim + dd0) * pd.vs;
-  const int voff = HD * pd.vs + koff;
-
   for (int st = 0; st < n_st; ++st) {
     const int s = st % kStages;
     if (!mbar_wait(&full[s], (st / kStages) & 1, pd)) break;
-    const uint8_t* base = stage_mem + s * stage_bytes;
+    const uint32_t base = stage0 + (uint32_t)s * stage_bytes;
     const int ne = min(e_stage, cnt - st * e_stage);
-    for (int e0 = 0; e0 < ne; e0 += 4) {
-      float sc[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        sc[u] = -INFINITY;
-        if (e0 + u < ne) {
-          const uint8_t* ent = base + (e0 + u) * ES;
-          uint32_t kw[16];
-          Row16<CACHE>::load(ent + koff, kw);
-          float d = 0.0f;
-          if (CACHE == KVPOOL_FP8_E4M3 && fast) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              d = fma_f16((uint16_t)(kw[j] & 0xFFFFu), (uint16_t)(qw[j] & 0xFFFFu), d);
-              d = fma_f16((uint16_t)(kw[j] >> 16), (uint16_t)(qw[j] >> 16), d);
-            }
-          } else if (CACHE == KVPOOL_BF16 && fast) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              d = fma_bf16((uint16_t)(kw[j] & 0xFFFFu), (uint16_t)(qw[j] & 0xFFFFu), d);
-              d = fma_bf16((uint16_t)(kw[j] >> 16), (uint16_t)(qw[j] >> 16), d);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) d = fmaf(qf[j], row_value<CACHE>(kw, j), d);
-          }
-#pragma unroll
-          for (int off = TPH / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-          float f = qscale;
-          if constexpr (CACHE == KVPOOL_FP8_E4M3) f *= bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(ent + 2 * HD));
-          sc[u] = d * f;
-        }
-      }
-      const float mx = fmaxf(fmaxf(m_run, fmaxf(sc[0], sc[1])), fmaxf(sc[2], sc[3]));
-      const float corr = exp2f(m_run - mx);
-      l_run *= corr;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) o[j] *= corr;
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        if (e0 + u < ne) {
-          const uint8_t* ent = base + (e0 + u) * ES;
-          const float p = exp2f(sc[u] - mx);
-          l_run += p;
-          uint32_t vw[16];
-          Row16<CACHE>::load(ent + voff, vw);
-          if constexpr (CACHE == KVPOOL_FP8_E4M3) {
-            // weight times the V scale, rounded to f16; products with the f16
-            // values are exact, accumulation fp32
-            const float ps = p * bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(ent + 2 * HD + 2));
-            const uint16_t ph = __half_as_ushort(__float2half_rn(ps));
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              o[2 * j] = fma_f16((uint16_t)(vw[j] & 0xFFFFu), ph, o[2 * j]);
-              o[2 * j + 1] = fma_f16((uint16_t)(vw[j] >> 16), ph, o[2 * j + 1]);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) o[j] = fmaf(p, row_value<CACHE>(vw, j), o[j]);
-          }
-        }
-      }
-      m_run = mx;
-    }
+    if (tc)
+      consume_stage_tc(base, ne, ES, arow, voff, soff, lane, bq, fq, m_run, l_run, o);
+    else if (fast)
+      consume_stage<CACHE, true, TPH>(base, ne, ES, koff, voff, soff, qscale, qw, qf, m_run, l_run, o);
+    else
+      consume_stage<CACHE, false, TPH>(base, ne, ES, koff, voff, soff, qscale, qw, qf, m_run, l_run, o);
     __syncwarp();
-    if ((tid & 31) == 0) mbar_arrive(&empty[s]);
+    if (lane == 0) mbar_arrive(&empty[s]);
   }
-
   if (act) {
+    const int64_t pslot = R.part_base + (part ? R.n_split0 : 0) + split;
     float* po = P.part_o + pslot * HD + h * pd.head_dim + dd0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) reinterpret_cast<float4*>(po)[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+    for (int j = 0; j < 4; ++j)
+      reinterpret_cast<float4*>(po)[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
     if (dd0 == 0) {
       float* ml = P.part_ml + (pslot * pd.heads + h) * 2;
       ml[0] = m_run;
@@ -420,9 +640,9 @@ int launch_attend_t(const AttendParams& p, cudaStream_t s, int e_stage, size_t s
 
 }  // namespace
 
-// entries per pipeline stage: about 16 KiB of entries, at most 8
+// entries per pipeline stage: about 16 KiB, at most 8
 int attend_stage_entries(const PoolDesc& pd) {
-  int e = (int)(16384 / pd.entry_bytes);
+  const int e = (int)(16448 / pd.entry_bytes);
   return e < 1 ? 1 : (e > 8 ? 8 : e);
 }
 

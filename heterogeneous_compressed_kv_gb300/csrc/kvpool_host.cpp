@@ -24,8 +24,6 @@
 
 namespace kvp {
 int append_slices(const PoolDesc& pd);
-int attend_stage_entries(const PoolDesc& pd);
-size_t attend_smem_bytes(const PoolDesc& pd);
 int attend_max_split_len();
 }  // namespace kvp
 
@@ -34,7 +32,8 @@ using namespace kvp;
 namespace {
 
 constexpr int kMaxSplits = 4096;
-constexpr int kTargetSplits = 4 * 152;  // CTAs of the attention kernel per launch (4 per SM, one wave)
+constexpr int kAttendCtas = 3 * 152;  // attention CTAs of a part that has the GPU to itself (3 per SM)
+constexpr int kPart0Ctas = 2 * 152;   // CTAs of the [HCA | window] part beside the select (2 per SM)
 constexpr int kScoreCtas = 152;         // CTAs of the score kernel per launch (1 per SM, one wave)
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -228,7 +227,7 @@ struct kvpool {
   cudaStream_t side = nullptr;
   cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   // profiling
-  bool profiling = false;
+  int profiling = 0;  // mask of the kernel kinds whose launches are recorded
   std::vector<ProfileSlot> prof;
   std::vector<cudaEvent_t> event_pool;
   double prof_ms[KVPOOL_KERNEL_COUNT] = {};
@@ -261,7 +260,8 @@ struct kvpool {
   template <class F>
   int launch(int kernel, int64_t bytes, void* stream, F&& f) {
     ProfileSlot s{};
-    if (profiling) {
+    const bool rec = (profiling >> kernel) & 1;
+    if (rec) {
       s.a = take_event();
       s.b = take_event();
       s.kernel = kernel;
@@ -270,7 +270,7 @@ struct kvpool {
     }
     int nk = 0;
     const int rc = f(&nk);
-    if (profiling) {
+    if (rec) {
       cudaEventRecord(s.b, (cudaStream_t)stream);
       s.n_kernels = nk;
       prof.push_back(s);
@@ -648,31 +648,32 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
                       (int64_t)pd.HD * pd.isz;
     }
     out_bytes = (int64_t)gn * pd.HD * 4;
-    // each part is split to fill the GPU by itself (they run at different times)
+    // each part is cut into splits, one CTA each, sized to fill the GPU
     int64_t src0 = 0, src1 = 0;
     for (int i = 0; i < gn; ++i) {
       src0 += (int64_t)P.reqs[i].n_hca + P.reqs[i].w;
       src1 += P.reqs[i].k;
     }
-    // part 0 runs beside the select on the side stream: 3 CTAs per SM leave a
-    // slot per SM for the select and the CSA part
-    const int64_t target0 = (Ld.has_csa && src1 > 0) ? 3 * 152 : kTargetSplits;
+    // part 0 runs beside the select on the side stream when both parts have
+    // work: two CTAs per SM leave room for the select and part 1
+    const bool forked = Ld.has_csa && src1 > 0;
+    const int64_t target0 = forked ? kPart0Ctas : kAttendCtas;
     int64_t len0 = std::min<int64_t>(max_split_len, std::max<int64_t>(16, (src0 + target0 - 1) / target0));
-    int64_t len1 = std::min<int64_t>(max_split_len, std::max<int64_t>(16, (src1 + kTargetSplits - 1) / kTargetSplits));
-    int ctas0 = 0, ctas1 = 0, parts = 0;
+    int64_t len1 = std::min<int64_t>(max_split_len, std::max<int64_t>(16, (src1 + kAttendCtas - 1) / kAttendCtas));
+    int splits0 = 0, splits1 = 0, parts = 0;
     for (int pass = 0; pass < 2; ++pass) {
-      ctas0 = ctas1 = parts = 0;
+      splits0 = splits1 = parts = 0;
       for (int i = 0; i < gn; ++i) {
         AttendReq& R = P.reqs[i];
         R.split_len0 = (int32_t)len0;
         R.split_len1 = (int32_t)len1;
         R.n_split0 = (int32_t)(((int64_t)R.n_hca + R.w + len0 - 1) / len0);
         R.n_split1 = (int32_t)(((int64_t)R.k + len1 - 1) / len1);
-        R.cta_base0 = ctas0;
-        R.cta_base1 = ctas1;
+        R.cta_base0 = splits0;
+        R.cta_base1 = splits1;
         R.part_base = parts;
-        ctas0 += R.n_split0;
-        ctas1 += R.n_split1;
+        splits0 += R.n_split0;
+        splits1 += R.n_split1;
         parts += R.n_split0 + R.n_split1;
       }
       if (parts <= kMaxSplits) break;
@@ -683,6 +684,7 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
       p->fail(KVPOOL_ERR_INVALID_ARG, "decode_attend: too many attention splits");
       break;
     }
+    const int ctas0 = splits0, ctas1 = splits1;
     P.total_score_ctas = score_ctas;
     P.total_key_ctas = key_ctas;
     P.total_ctas0 = ctas0;
@@ -791,9 +793,9 @@ int kvpool_check_device(kvpool_t* p, void* stream, uint32_t* word_out) {
   return KVPOOL_OK;
 }
 
-int kvpool_profile_enable(kvpool_t* p, int enable) {
-  if (!p) return KVPOOL_ERR_INVALID_ARG;
-  if (enable) {
+int kvpool_profile_enable(kvpool_t* p, int kinds) {
+  if (!p || (kinds & ~KVPOOL_PROFILE_ALL)) return KVPOOL_ERR_INVALID_ARG;
+  if (kinds) {
     p->settle_profile();
     p->timeline.clear();
     if (p->t0) {
@@ -806,7 +808,7 @@ int kvpool_profile_enable(kvpool_t* p, int enable) {
       p->prof_bytes[k] = 0;
     }
   }
-  p->profiling = enable != 0 && p->device();
+  p->profiling = p->device() ? kinds : 0;
   return KVPOOL_OK;
 }
 

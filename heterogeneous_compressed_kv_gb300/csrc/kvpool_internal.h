@@ -104,7 +104,7 @@ struct AttendReq {
   // [selected CSA entries]; each part is split into chunks of its split_len
   int32_t split_len0, split_len1;  // sources per split of each part
   int32_t n_split0, n_split1;
-  int32_t cta_base0, cta_base1;  // first attention CTA of each part's launch
+  int32_t cta_base0, cta_base1;  // first attention CTA (split) of this request in each part's launch
   int32_t part_base;             // first partial slot; part 1 follows part 0
 };
 
@@ -119,7 +119,7 @@ struct AttendParams {
   int32_t n;                 // requests in this launch
   int32_t row0;              // first row of q / out for this launch
   int32_t total_score_ctas, total_key_ctas;
-  int32_t total_ctas0, total_ctas1;  // attention CTAs of part 0 and part 1
+  int32_t total_ctas0, total_ctas1;  // attention CTAs (= splits) of part 0 and part 1
   int32_t segs_per_cta;      // block segments scored by one score CTA
   int32_t src_lo, src_hi;    // attention sources [lo, hi) of the virtual list this launch covers
   // scratch (device pointers)
@@ -129,7 +129,7 @@ struct AttendParams {
   uint32_t* counts;          // [rows][max_key_ctas][2] (keys > T, keys == T) per select chunk
   int32_t max_key_ctas;
   uint2* cand;               // [rows][key_stride] (key, index) of the boundary bucket
-  uint32_t* sync;            // [rows][4]: candidates, select CTAs done, attention splits done, pad
+  uint32_t* sync;            // [rows][4]: candidates, select CTAs done, pad, pad
   uint32_t* thr;             // [rows][2] (T, keys == T taken)
   int32_t* sel;              // [rows][sel_stride]
   int32_t sel_stride;

@@ -266,8 +266,13 @@ class Pool:
             raise KvpoolError(rc, f"check_device: {self.last_error()} (flags {w.value:#x})")
         return w.value
 
-    def profile_enable(self, on: bool = True) -> None:
-        self._check(self.L.kvpool_profile_enable(self.h, 1 if on else 0), "profile_enable")
+    def profile_enable(self, on: bool = True, kinds=None) -> None:
+        """Record the launches of the given kernel kinds (indexes into
+        KERNEL_NAMES; all kinds when None), or stop recording."""
+        mask = 0
+        if on:
+            mask = (1 << len(KERNEL_NAMES)) - 1 if kinds is None else sum(1 << int(k) for k in set(kinds))
+        self._check(self.L.kvpool_profile_enable(self.h, mask), "profile_enable")
 
     def profile_timeline(self, cap: int = 4096):
         """[(kernel name, start ms, end ms)] of the recorded launches."""

@@ -274,8 +274,12 @@ enum {
   KVPOOL_KERNEL_COMBINE = 4, /* split-K merge */
   KVPOOL_KERNEL_COUNT = 5
 };
-/* Enable (1) or disable (0) event recording; enabling resets the totals. */
-int kvpool_profile_enable(kvpool_t* pool, int enable);
+#define KVPOOL_PROFILE_ALL ((1 << KVPOOL_KERNEL_COUNT) - 1)
+/* Record events around the launches of the kernel kinds whose bit is set in
+ * kinds (bit k = KVPOOL_KERNEL_k; KVPOOL_PROFILE_ALL for every kind); 0
+ * disables recording.  A non-zero mask resets the totals and the timeline.
+ * Each recorded launch adds two event records to its stream. */
+int kvpool_profile_enable(kvpool_t* pool, int kinds);
 /* Synchronize and report, for one kernel kind, the summed device time of its
  * launches since profiling was enabled, the launch count and the algorithmic
  * bytes those launches had to move (inputs read + outputs written, scratch
