@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "kvpool_internal.h"
 
 namespace kvp {
@@ -45,6 +47,39 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   uint32_t u = __float_as_uint(s);
   if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ---------------------------------------------------------------------------
+// programmatic dependent launch: every kernel of this library starts with
+// pdl_start(), which lets the next kernel in the stream be scheduled (it
+// still waits for this grid to finish before touching memory) and waits for
+// the previous kernel in the stream to finish and flush.  Every CTA calls it
+// before any early exit, so a grid never completes before its predecessor.
+// Without the launch attribute both instructions are no-ops.  The attribute
+// is set where an early start hides launch latency on the critical path
+// (append, indexer scores, merge); kernels that run beside other work (the
+// select passes, attention) launch without it: their early-started CTAs
+// would hold SM resources that work needs.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_start() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------------------

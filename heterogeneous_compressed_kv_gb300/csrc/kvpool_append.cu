@@ -169,6 +169,7 @@ constexpr int kTokGroup = 8;  // tokens whose loads are issued together
 
 template <int IN, int CACHE>
 __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ AppendParams P) {
+  pdl_start();
   __shared__ float sh[3 * 16];
   const PoolDesc& pd = P.pool;
   const AppendUnit u = P.units[blockIdx.x];
@@ -338,6 +339,7 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
 // the CTA (0, 0, 0) also copies the shared block ids into dst's table row.
 template <int IN, int CACHE>
 __global__ void __launch_bounds__(512) share_kernel(const __grid_constant__ ShareParams P) {
+  pdl_start();
   __shared__ float sh[3 * 16];
   const PoolDesc& pd = P.pool;
   const int tok = blockIdx.x, slice = blockIdx.y, layer = blockIdx.z;
@@ -383,13 +385,13 @@ int launch_append(const AppendParams& p, int n_layers, void* stream, int* n_kern
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int key = p.pool.in_dtype * 3 + p.pool.cache_dtype;
   switch (key) {
-    case KVPOOL_F32 * 3 + KVPOOL_F32: append_kernel<KVPOOL_F32, KVPOOL_F32><<<grid, threads, 0, s>>>(p); break;
-    case KVPOOL_F32 * 3 + KVPOOL_BF16: append_kernel<KVPOOL_F32, KVPOOL_BF16><<<grid, threads, 0, s>>>(p); break;
-    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3: append_kernel<KVPOOL_F32, KVPOOL_FP8_E4M3><<<grid, threads, 0, s>>>(p); break;
-    case KVPOOL_BF16 * 3 + KVPOOL_F32: append_kernel<KVPOOL_BF16, KVPOOL_F32><<<grid, threads, 0, s>>>(p); break;
-    case KVPOOL_BF16 * 3 + KVPOOL_BF16: append_kernel<KVPOOL_BF16, KVPOOL_BF16><<<grid, threads, 0, s>>>(p); break;
+    case KVPOOL_F32 * 3 + KVPOOL_F32: launch_kernel(true, append_kernel<KVPOOL_F32, KVPOOL_F32>, grid, dim3(threads), 0, s, p); break;
+    case KVPOOL_F32 * 3 + KVPOOL_BF16: launch_kernel(true, append_kernel<KVPOOL_F32, KVPOOL_BF16>, grid, dim3(threads), 0, s, p); break;
+    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3: launch_kernel(true, append_kernel<KVPOOL_F32, KVPOOL_FP8_E4M3>, grid, dim3(threads), 0, s, p); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_F32: launch_kernel(true, append_kernel<KVPOOL_BF16, KVPOOL_F32>, grid, dim3(threads), 0, s, p); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_BF16: launch_kernel(true, append_kernel<KVPOOL_BF16, KVPOOL_BF16>, grid, dim3(threads), 0, s, p); break;
     case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3:
-      append_kernel<KVPOOL_BF16, KVPOOL_FP8_E4M3><<<grid, threads, 0, s>>>(p);
+      launch_kernel(true, append_kernel<KVPOOL_BF16, KVPOOL_FP8_E4M3>, grid, dim3(threads), 0, s, p);
       break;
     default: return (int)cudaErrorInvalidValue;
   }
@@ -405,12 +407,12 @@ int launch_share(const ShareParams& p, int n_layers, void* stream, int* n_kernel
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int key = p.pool.in_dtype * 3 + p.pool.cache_dtype;
   switch (key) {
-    case KVPOOL_F32 * 3 + KVPOOL_F32: share_kernel<KVPOOL_F32, KVPOOL_F32><<<grid, threads, 0, s>>>(p); break;
-    case KVPOOL_F32 * 3 + KVPOOL_BF16: share_kernel<KVPOOL_F32, KVPOOL_BF16><<<grid, threads, 0, s>>>(p); break;
-    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3: share_kernel<KVPOOL_F32, KVPOOL_FP8_E4M3><<<grid, threads, 0, s>>>(p); break;
-    case KVPOOL_BF16 * 3 + KVPOOL_F32: share_kernel<KVPOOL_BF16, KVPOOL_F32><<<grid, threads, 0, s>>>(p); break;
-    case KVPOOL_BF16 * 3 + KVPOOL_BF16: share_kernel<KVPOOL_BF16, KVPOOL_BF16><<<grid, threads, 0, s>>>(p); break;
-    case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3: share_kernel<KVPOOL_BF16, KVPOOL_FP8_E4M3><<<grid, threads, 0, s>>>(p); break;
+    case KVPOOL_F32 * 3 + KVPOOL_F32: launch_kernel(true, share_kernel<KVPOOL_F32, KVPOOL_F32>, grid, dim3(threads), 0, s, p); break;
+    case KVPOOL_F32 * 3 + KVPOOL_BF16: launch_kernel(true, share_kernel<KVPOOL_F32, KVPOOL_BF16>, grid, dim3(threads), 0, s, p); break;
+    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3: launch_kernel(true, share_kernel<KVPOOL_F32, KVPOOL_FP8_E4M3>, grid, dim3(threads), 0, s, p); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_F32: launch_kernel(true, share_kernel<KVPOOL_BF16, KVPOOL_F32>, grid, dim3(threads), 0, s, p); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_BF16: launch_kernel(true, share_kernel<KVPOOL_BF16, KVPOOL_BF16>, grid, dim3(threads), 0, s, p); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3: launch_kernel(true, share_kernel<KVPOOL_BF16, KVPOOL_FP8_E4M3>, grid, dim3(threads), 0, s, p); break;
     default: return (int)cudaErrorInvalidValue;
   }
   *n_kernels += 1;

@@ -381,6 +381,7 @@ __device__ __forceinline__ void consume_stage(uint32_t base, int ne, uint32_t ES
 template <int IN, int CACHE, int TPH>
 __global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __grid_constant__ AttendParams P,
                                                                       int e_stage, int part) {
+  pdl_start();
   extern __shared__ __align__(128) uint8_t smem[];
   const PoolDesc& pd = P.pool;
   const int HD = pd.HD;
@@ -555,6 +556,7 @@ __global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __gr
 // [4l, 4l + 4); the 32 warp results are merged through shared memory.
 constexpr int kCombineWarps = 32;
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ AttendParams P) {
+  pdl_start();
   __shared__ float red_o[kCombineWarps][128];
   __shared__ float red_m[kCombineWarps], red_l[kCombineWarps];
   const int i = blockIdx.x, h = blockIdx.y;
@@ -623,7 +625,7 @@ int launch_attend_t(const AttendParams& p, cudaStream_t s, int e_stage, size_t s
       cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       set8 = smem;
     }
-    k<<<ctas, threads, smem, s>>>(p, e_stage, part);
+    launch_kernel(false, k, dim3(ctas), dim3(threads), smem, s, p, e_stage, part);
   } else if (p.pool.head_dim == 64) {
     auto k = attend_kernel<IN, CACHE, 4>;
     static size_t set4 = 0;
@@ -631,7 +633,7 @@ int launch_attend_t(const AttendParams& p, cudaStream_t s, int e_stage, size_t s
       cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       set4 = smem;
     }
-    k<<<ctas, threads, smem, s>>>(p, e_stage, part);
+    launch_kernel(false, k, dim3(ctas), dim3(threads), smem, s, p, e_stage, part);
   } else {
     return (int)cudaErrorInvalidValue;
   }
@@ -675,7 +677,7 @@ int launch_attend(const AttendParams& p, int part, int ctas, void* stream, int* 
 int launch_combine(const AttendParams& p, void* stream, int* n_kernels) {
   if (p.n <= 0) return 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  combine_kernel<<<dim3(p.n, p.pool.heads), kCombineWarps * 32, 0, s>>>(p);
+  launch_kernel(true, combine_kernel, dim3(p.n, p.pool.heads), dim3(kCombineWarps * 32), 0, s, p);
   *n_kernels += 1;
   return (int)cudaGetLastError();
 }

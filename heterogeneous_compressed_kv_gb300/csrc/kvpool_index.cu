@@ -170,6 +170,7 @@ constexpr int kScoreStageBudget = 200 * 1024;         // shared memory for slots
 template <int IN, int CACHE>
 __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(const __grid_constant__ AttendParams P, int stage_bytes,
                                                                  int ring, int stage_off) {
+  pdl_start();
   extern __shared__ __align__(128) uint8_t sm[];
   const PoolDesc& pd = P.pool;
   const LayerDesc& L = P.layer;
@@ -423,6 +424,7 @@ __device__ __forceinline__ int load_items(const uint32_t* keys, int64_t my0, int
 // CTA waits on another: the last one is found with an atomic counter after a
 // fence.
 __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __grid_constant__ AttendParams P) {
+  pdl_start();
   __shared__ uint32_t sh[kSelThreads];
   __shared__ uint32_t st[8];
   __shared__ uint32_t h2[kHistBins];
@@ -537,6 +539,7 @@ __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __gri
 // Pass 2: every chunk writes its selected indices in ascending order, from the
 // exclusive prefixes the last compact CTA stored for it.
 __global__ void __launch_bounds__(kSelThreads) select_emit_kernel(const __grid_constant__ AttendParams P) {
+  pdl_start();
   __shared__ uint32_t sh[kSelThreads];
   const int i = find_req(P, blockIdx.x, 1);
   const AttendReq& R = P.reqs[i];
@@ -617,7 +620,7 @@ static int launch_score_t(const AttendParams& p, cudaStream_t s) {
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     set = smem;
   }
-  k<<<p.total_score_ctas, kScoreThreads, smem, s>>>(p, sb, ns, so);
+  launch_kernel(true, k, dim3(p.total_score_ctas), dim3(kScoreThreads), smem, s, p, sb, ns, so);
   return 0;
 }
 
@@ -644,10 +647,10 @@ int launch_select(const AttendParams& p, void* stream, int* n_kernels) {
   bool any_radix = false;
   for (int i = 0; i < p.n; ++i) any_radix |= (!p.reqs[i].select_all && p.reqs[i].k > 0);
   if (any_radix) {
-    select_compact_kernel<<<p.total_key_ctas, kSelThreads, 0, s>>>(p);
+    launch_kernel(false, select_compact_kernel, dim3(p.total_key_ctas), dim3(kSelThreads), 0, s, p);
     *n_kernels += 1;
   }
-  select_emit_kernel<<<p.total_key_ctas, kSelThreads, 0, s>>>(p);
+  launch_kernel(false, select_emit_kernel, dim3(p.total_key_ctas), dim3(kSelThreads), 0, s, p);
   *n_kernels += 1;
   return (int)cudaGetLastError();
 }
@@ -675,6 +678,7 @@ static std::mutex g_scratch_mu;
 // scores -> orderable keys and the first radix histogram (top 11 bits)
 __global__ void __launch_bounds__(kSelThreads) static_keys_kernel(const __grid_constant__ AttendParams P,
                                                                   const float* __restrict__ scores, int64_t ld) {
+  pdl_start();
   __shared__ uint32_t hist[kHistBins];
   const int i = find_req(P, blockIdx.x, 1);
   const AttendReq& R = P.reqs[i];
@@ -766,7 +770,7 @@ extern "C" int kvpool_topk_static(const float* d_scores, int32_t n_rows, int32_t
   bool radix = false;
   for (int i = 0; i < n_rows; ++i) radix |= !P->reqs[i].select_all && P->reqs[i].k > 0;
   if (radix) {
-    static_keys_kernel<<<P->total_key_ctas, kSelThreads, 0, s>>>(*P, d_scores, n_cols);
+    launch_kernel(false, static_keys_kernel, dim3(P->total_key_ctas), dim3(kSelThreads), 0, s, *P, d_scores, (int64_t)n_cols);
     rc = (int)cudaGetLastError();
   }
   int nk = 0;
