@@ -16,7 +16,7 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 K, V, IDXK, Q, QIDX, GATE_CSA, GATE_HCA, GATE_IDX, LEN = 1, 2, 3, 4, 5, 6, 7, 8, 9
-OUT_F32, OUT_BF16 = 0, 1
+OUT_F32, OUT_BF16, OUT_BF16_F32 = 0, 1, 2  # the last one host only
 
 
 class Run(C.Structure):
@@ -49,10 +49,16 @@ def _runs_array(runs):
     return arr
 
 
-def fill_host(n_values: int, out_dtype: int, seed: int, runs) -> np.ndarray:
+def fill_host(n_values: int, out_dtype: int, seed: int, runs, out: np.ndarray | None = None) -> np.ndarray:
     """runs: list of (stream, index0, count, out_offset).  Returns float32 values
-    (out_dtype OUT_F32) or uint16 bfloat16 bits (OUT_BF16)."""
-    out = np.zeros(n_values, np.float32 if out_dtype == OUT_F32 else np.uint16)
+    (OUT_F32), uint16 bfloat16 bits (OUT_BF16) or float32 bfloat16 values
+    (OUT_BF16_F32); `out` (contiguous, n_values elements of that type) is
+    filled in place when given."""
+    dt = np.uint16 if out_dtype == OUT_BF16 else np.float32
+    if out is None:
+        out = np.zeros(n_values, dt)
+    elif out.dtype != dt or out.size != n_values or not out.flags.c_contiguous:
+        raise ValueError("fill_host: out must be a contiguous array of n_values elements of the output type")
     arr = _runs_array(runs)
     rc = lib().kvgen_fill_host(out.ctypes.data_as(C.c_void_p), out_dtype, seed, len(runs), arr)
     if rc != 0:

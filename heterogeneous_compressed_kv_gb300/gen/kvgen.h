@@ -57,7 +57,9 @@ enum {
   KVGEN_LEN = 9,      /* request lengths / churn draws                        */
 };
 
-enum { KVGEN_OUT_F32 = 0, KVGEN_OUT_BF16 = 1 };
+/* output formats: float; uint16 bfloat16 bits; (host only) float holding the
+ * bfloat16-rounded value */
+enum { KVGEN_OUT_F32 = 0, KVGEN_OUT_BF16 = 1, KVGEN_OUT_BF16_F32 = 2 };
 
 KVGEN_HD uint64_t kvgen_stream_id(uint64_t kind, uint64_t layer, uint64_t request) {
   return (kind << 56) | ((layer & 0xFFFFull) << 40) | (request & 0xFFFFFFFFFFull);
@@ -114,8 +116,9 @@ typedef struct kvgen_run {
 extern "C" {
 #endif
 
-/* Fill a host buffer.  out_dtype: KVGEN_OUT_F32 (float) or KVGEN_OUT_BF16
- * (uint16 bfloat16 bits).  Returns 0, or -1 on a bad argument. */
+/* Fill a host buffer.  out_dtype: KVGEN_OUT_F32 (float), KVGEN_OUT_BF16
+ * (uint16 bfloat16 bits) or KVGEN_OUT_BF16_F32 (float holding the bfloat16
+ * value).  Returns 0, or -1 on a bad argument. */
 int kvgen_fill_host(void* out, int out_dtype, uint64_t seed, int n_runs, const kvgen_run* runs);
 
 /* Fill a device buffer on `stream` (a cudaStream_t, NULL = legacy default).

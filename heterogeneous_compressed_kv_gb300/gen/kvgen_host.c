@@ -3,7 +3,7 @@
 
 int kvgen_fill_host(void* out, int out_dtype, uint64_t seed, int n_runs, const kvgen_run* runs) {
   if (!out || n_runs < 0 || (n_runs > 0 && !runs)) return -1;
-  if (out_dtype != KVGEN_OUT_F32 && out_dtype != KVGEN_OUT_BF16) return -1;
+  if (out_dtype != KVGEN_OUT_F32 && out_dtype != KVGEN_OUT_BF16 && out_dtype != KVGEN_OUT_BF16_F32) return -1;
   for (int r = 0; r < n_runs; ++r) {
     const kvgen_run* run = &runs[r];
     if (run->count < 0 || run->index0 < 0 || run->out_offset < 0) return -1;
@@ -11,10 +11,14 @@ int kvgen_fill_host(void* out, int out_dtype, uint64_t seed, int n_runs, const k
     if (out_dtype == KVGEN_OUT_F32) {
       float* o = (float*)out + run->out_offset;
       for (int64_t i = 0; i < run->count; ++i) o[i] = kvgen_normal(base, (uint64_t)(run->index0 + i));
-    } else {
+    } else if (out_dtype == KVGEN_OUT_BF16) {
       uint16_t* o = (uint16_t*)out + run->out_offset;
       for (int64_t i = 0; i < run->count; ++i)
         o[i] = kvgen_bf16_bits(kvgen_normal(base, (uint64_t)(run->index0 + i)));
+    } else {
+      uint32_t* o = (uint32_t*)out + run->out_offset;
+      for (int64_t i = 0; i < run->count; ++i)
+        o[i] = (uint32_t)kvgen_bf16_bits(kvgen_normal(base, (uint64_t)(run->index0 + i))) << 16;
     }
   }
   return 0;

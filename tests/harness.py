@@ -28,10 +28,9 @@ def make_oracle(cfg, max_requests, max_blocks, max_blocks_per_request, gate_over
                     gate_idx=g_idx)
 
 
-def _values(cfg, n_values, runs):
-    if cfg["in_dtype"] == W.F32:
-        return gen.fill_host(n_values, gen.OUT_F32, cfg["seed"], runs)
-    return gen.bf16_bits_to_f32(gen.fill_host(n_values, gen.OUT_BF16, cfg["seed"], runs))
+def _values(cfg, n_values, runs, out=None):
+    return gen.fill_host(n_values, gen.OUT_F32 if cfg["in_dtype"] == W.F32 else gen.OUT_BF16_F32, cfg["seed"], runs,
+                         out)
 
 
 def tokens(cfg, reqs, pos0s, counts):
@@ -41,13 +40,15 @@ def tokens(cfg, reqs, pos0s, counts):
     HD = cfg["heads"] * cfg["head_dim"]
     XD = cfg["idx_heads"] * cfg["idx_dim"]
     T = int(sum(counts))
-    ks, vs, xs = [], [], []
-    for l in range(cfg["n_layers"]):
-        ks.append(_values(cfg, T * HD, gen.token_runs(gen.K, l, reqs, pos0s, counts, HD)))
-        vs.append(_values(cfg, T * HD, gen.token_runs(gen.V, l, reqs, pos0s, counts, HD)))
-        xs.append(_values(cfg, T * XD, gen.token_runs(gen.IDXK, l, reqs, pos0s, counts, XD)))
     nl = cfg["n_layers"]
-    return (np.stack(ks).reshape(nl, T, HD), np.stack(vs).reshape(nl, T, HD), np.stack(xs).reshape(nl, T, XD))
+    k = np.empty((nl, T, HD), np.float32)
+    v = np.empty((nl, T, HD), np.float32)
+    x = np.empty((nl, T, XD), np.float32)
+    for l in range(nl):
+        _values(cfg, T * HD, gen.token_runs(gen.K, l, reqs, pos0s, counts, HD), k[l].reshape(-1))
+        _values(cfg, T * HD, gen.token_runs(gen.V, l, reqs, pos0s, counts, HD), v[l].reshape(-1))
+        _values(cfg, T * XD, gen.token_runs(gen.IDXK, l, reqs, pos0s, counts, XD), x[l].reshape(-1))
+    return k, v, x
 
 
 def queries(cfg, layer, reqs, step):

@@ -1,0 +1,188 @@
+"""Parity at the workloads' full sizes, in the launch configuration bench.py
+times.  Where the oracle can follow the whole run in seconds it does (decode
+batch, chunked prefill); at 1M-token context it checks sampled outputs it can
+compute one by one and properties that hold at any size (long context)."""
+import numpy as np
+import pytest
+import torch
+
+from heterogeneous_compressed_kv_gb300 import gen
+from heterogeneous_compressed_kv_gb300 import kvpool as K
+from heterogeneous_compressed_kv_gb300.gen import workloads as W
+from tests import harness as H
+from tests.gpu_harness import GpuCase, check_out, compare_request_state
+
+pytestmark = pytest.mark.gpu
+
+
+def _pair(w, max_requests, max_blocks, mbpr, max_batch, max_top_k):
+    o = H.make_oracle(w, max_requests, max_blocks, mbpr)
+    g = GpuCase(w, max_requests, max_blocks, mbpr, max_batch, max_top_k)
+    return o, g
+
+
+def _append(o, g, slots, wids, pos0s, counts):
+    k, v, x = H.tokens(g.w, wids, pos0s, counts)
+    assert o.append(slots, counts, k, v, x) == 0
+    assert g.append(slots, wids, pos0s, counts, check=False) == 0, g.pool.last_error()
+
+
+def _attend(o, g, slots, wids, step, top_k):
+    q, qi = H.queries(g.w, 0, wids, step)
+    rc, ref, tk_ref = o.decode_attend(0, slots, q, qi, top_k)
+    assert rc == 0
+    out, tk = g.attend(0, slots, wids, step, top_k)
+    assert g.pool.check_device() == 0
+    assert np.array_equal(tk.cpu().numpy(), tk_ref), f"top-k index sets differ at step {step}"
+    return check_out(out.cpu().numpy().reshape(ref.shape), ref, g.w["cache_dtype"])
+
+
+def test_decode_batch_full():
+    """32 requests with lengths U[1, 8192] (seed 1), bf16, top_k 512: prefill
+    in 2048-token chunks, then 100 decode steps of one token per request;
+    top-k sets and outputs compared every 10th step, the stored state of
+    every request (sampled entries) at the end."""
+    w = W.DECODE_BATCH
+    B = w["n_requests"]
+    lens = [int(x) for x in W.uniform_lengths(w["seed"], B, w["len_lo"], w["len_hi"])]
+    steps = w["decode_steps"]
+    mbpr = (max(lens) + steps) // w["m_prime"] + 2
+    max_blocks = sum((L + steps) // w["m_prime"] + 1 for L in lens)
+    o, g = _pair(w, B, max_blocks, mbpr, B, w["top_k"])
+    slots = [g.pool.alloc_request() for _ in range(B)]
+    assert [o.alloc_request()[1] for _ in range(B)] == slots
+    wids = list(range(B))
+    pos = [0] * B
+    while True:
+        cnt = [min(2048, L - p) for L, p in zip(lens, pos)]
+        if sum(cnt) == 0:
+            break
+        _append(o, g, slots, wids, pos, cnt)
+        pos = [p + c for p, c in zip(pos, cnt)]
+    for step in range(steps):
+        _append(o, g, slots, wids, pos, [1] * B)
+        pos = [p + 1 for p in pos]
+        if step % 10 == 0 or step == steps - 1:
+            _attend(o, g, slots, wids, step, w["top_k"])
+    rng = np.random.default_rng(0)
+    for s in slots:
+        compare_request_state(g, o, s, sample=24, rng=rng)
+
+
+def test_chunked_prefill_full():
+    """4 requests x 32768 tokens in 2048-token chunks; the first 16384 tokens
+    are request 0's, shared by requests 1-3 through refcounted blocks (their
+    windows recomputed by the caller); every request then appends its own
+    16384 tokens in 2048-token chunks, batched.  Tables, refcounts and every
+    stored entry bit-exact; then decode steps at top_k 512."""
+    w = W.CHUNKED_PREFILL
+    B, T, C, S = w["n_requests"], w["tokens"], w["chunk"], w["shared"]
+    mp = w["m_prime"]
+    mbpr = T // mp + 4
+    o, g = _pair(w, B, S // mp + B * ((T - S) // mp + 2), mbpr, B, w["top_k"])
+    slots = [g.pool.alloc_request() for _ in range(B)]
+    assert [o.alloc_request()[1] for _ in range(B)] == slots
+    for p0 in range(0, S, C):
+        _append(o, g, [slots[0]], [0], [p0], [C])
+    wlen = min(S, w["n_win"])
+    k, v, _ = H.tokens(w, [0], [S - wlen], [wlen])
+    gk, gv, _ = g.tokens([0], [S - wlen], [wlen])
+    for dst in slots[1:]:
+        assert o.share_prefix(dst, slots[0], S, k, v) == 0
+        g.pool.share_prefix(dst, slots[0], S, gk, gv)
+    for b in o.request_info(slots[0])[2]:
+        assert g.pool.block_refcount(int(b)) == o.block_refcount(int(b)) == B
+    wids = list(range(B))
+    for p0 in range(S, T, C):
+        _append(o, g, slots, wids, [p0] * B, [C] * B)
+    assert g.pool.free_block_count() == o.free_block_count()
+    for s in slots:
+        compare_request_state(g, o, s)
+    pos = [T] * B
+    for step in range(4):
+        _append(o, g, slots, wids, pos, [1] * B)
+        pos = [p + 1 for p in pos]
+        _attend(o, g, slots, wids, step, w["top_k"])
+
+
+def _spawn_pool():
+    import multiprocessing as mp
+    import os
+    return mp.get_context("spawn").Pool(max(1, min(16, os.cpu_count() or 1)))
+
+
+def test_long_context_full_sampled():
+    """8 requests x 1,048,576 tokens, fp8 cache, top_k 2048, in bench.py's
+    pool configuration and prefill order (2048-token chunks, every request per
+    call), then one decode step.  For one request the oracle recomputes, one
+    piece at a time in worker processes, all 262,144 indexer scores (top-k set
+    compared bit for bit), all 8,192 HCA entries, the selected CSA entries and
+    the window, and the attention output (fp8 tolerance); sampled CSA,
+    indexer and HCA entries and the window are compared byte for byte with
+    the arena; block tables follow the smallest-free policy."""
+    from tests import oracle_pool as OP
+    w = W.LONG_CONTEXT
+    B, Lc, C, mp_, top_k = w["n_requests"], w["length"], w["chunk"], w["m_prime"], w["top_k"]
+    extra = 8
+    g = GpuCase(w, B, B * ((Lc + extra) // mp_ + 1), (Lc + extra) // mp_ + 2, B, top_k)
+    o = OP._oracle(w)
+    slots = [g.pool.alloc_request() for _ in range(B)]
+    wids = list(range(B))
+    for p0 in range(0, Lc, C):
+        assert g.append(slots, wids, [p0] * B, [C] * B, check=False) == 0
+    assert g.append(slots, wids, [Lc] * B, [1] * B, check=False) == 0
+    out, tk = g.attend(0, slots, wids, 0, top_k)
+    assert g.pool.check_device() == 0
+    out, tk = out.cpu().numpy(), tk.cpu().numpy()
+    L = Lc + 1
+    n_csa, n_hca = L // w["m"], L // mp_
+    # block ids: chunk c seals 16 blocks per request, requests in batch order
+    per = C // mp_
+    for r, s in enumerate(slots):
+        rc, info, ids = g.pool.request_info(s)
+        assert info["length"] == L and info["n_csa"] == n_csa and info["n_hca"] == n_hca
+        expect = [c * B * per + r * per + j for c in range(Lc // C) for j in range(per)]
+        assert ids.tolist() == expect
+    r = 5
+    s, wid = slots[r], wids[r]
+    _, ids = g.pool.request_info(s)[1:]
+    q, qi = H.queries(w, 0, [wid], 0)
+    pool = _spawn_pool()
+    try:
+        n_w = pool._processes
+        cuts = np.linspace(0, n_csa, 4 * n_w + 1).astype(int)
+        parts = pool.starmap(OP.idx_scores, [(w, wid, qi[0], int(a), int(b)) for a, b in zip(cuts[:-1], cuts[1:])])
+        scores = np.concatenate(parts)
+        hcuts = np.linspace(0, n_hca, 4 * n_w + 1).astype(int)
+        hparts = pool.starmap(OP.kv_entries, [(w, wid, 2, list(range(int(a), int(b)))) for a, b in zip(hcuts[:-1], hcuts[1:])])
+    finally:
+        pool.close()
+        pool.join()
+    import oracle as O
+    sel = O.topk(scores, top_k)
+    assert np.array_equal(tk[r], sel), "top-k index set differs from the oracle's"
+    hca_codes = np.concatenate([p[0] for p in hparts])
+    hca_scales = np.concatenate([p[1] for p in hparts])
+    csa_codes, csa_scales = OP.kv_entries(w, wid, 1, sel.tolist())
+    win_codes, win_scales = OP.window_entries(w, wid, L - w["n_win"], w["n_win"])
+    codes = np.concatenate([csa_codes, hca_codes, win_codes])
+    scales = np.concatenate([csa_scales, hca_scales, win_scales])
+    rc, ref = o.attend_sources(codes, scales, q[0])
+    assert rc == 0
+    check_out(out[r].reshape(ref.shape), ref, w["cache_dtype"])
+    # stored bytes: sampled CSA / indexer / HCA entries and the whole window
+    rng = np.random.default_rng(1)
+    es = sorted(set(rng.integers(0, n_csa, 48).tolist()) | {0, n_csa - 1})
+    cc, csc = OP.kv_entries(w, wid, 1, es)
+    ie = OP.idx_entries(w, wid, es)
+    for j, e in enumerate(es):
+        c, sc = g.csa_entry(0, s, e, ids)
+        assert np.array_equal(c, cc[j]) and np.array_equal(sc, csc[j]), f"CSA entry {e}"
+        c, sc = g.idx_entry(0, s, e, ids)
+        assert np.array_equal(c, ie[j][0]) and sc[0] == ie[j][1][0], f"indexer entry {e}"
+    for t in sorted(set(rng.integers(0, n_hca, 16).tolist()) | {n_hca - 1}):
+        c, sc = g.hca_entry(0, int(ids[t]))
+        assert np.array_equal(c, hca_codes[t]) and np.array_equal(sc, hca_scales[t]), f"HCA entry {t}"
+    for t, pos in enumerate(range(L - w["n_win"], L)):
+        c, sc = g.window_token(0, s, pos)
+        assert np.array_equal(c, win_codes[t]) and np.array_equal(sc, win_scales[t]), f"window token {pos}"
