@@ -19,41 +19,42 @@ def _oracle(cfg):
     return _ORACLES[key]
 
 
-def _rows(cfg, kind, wid, pos0, count, width):
+def _rows(cfg, kind, wid, pos0, count, width, layer=0):
     out = np.empty(count * width, np.float32)
-    H._values(cfg, count * width, gen.token_runs(kind, 0, [wid], [pos0], [count], width), out)
+    H._values(cfg, count * width, gen.token_runs(kind, layer, [wid], [pos0], [count], width), out)
     return out.reshape(count, width)
 
 
-def idx_scores(cfg, wid, q_idx, e0, e1):
+def idx_scores(cfg, wid, q_idx, e0, e1, layer=0):
     """Indexer scores of CSA entries [e0, e1) of workload request `wid`."""
     o = _oracle(cfg)
     m, XD = cfg["m"], cfg["idx_heads"] * cfg["idx_dim"]
-    keys = _rows(cfg, gen.IDXK, wid, e0 * m, (e1 - e0) * m, XD)
+    keys = _rows(cfg, gen.IDXK, wid, e0 * m, (e1 - e0) * m, XD, layer)
     out = np.empty(e1 - e0, np.float32)
     for j in range(e1 - e0):
-        code, sc = o.compress_idx(0, keys[j * m:(j + 1) * m])
+        code, sc = o.compress_idx(layer, keys[j * m:(j + 1) * m])
         out[j] = o.score(code, sc, q_idx)
     return out
 
 
-def idx_entries(cfg, wid, es):
+def idx_entries(cfg, wid, es, layer=0):
     """Indexer entries (codes, scales) of the CSA entries `es`."""
     o = _oracle(cfg)
     m, XD = cfg["m"], cfg["idx_heads"] * cfg["idx_dim"]
     res = []
     for e in es:
-        code, sc = o.compress_idx(0, _rows(cfg, gen.IDXK, wid, e * m, m, XD))
+        code, sc = o.compress_idx(layer, _rows(cfg, gen.IDXK, wid, e * m, m, XD, layer))
         res.append((code, sc))
     return res
 
 
-def _kv_rows(cfg, wid, pos0, count):
+def _kv_rows(cfg, wid, pos0, count, layer=0):
     HD = cfg["heads"] * cfg["head_dim"]
-    return np.concatenate([_rows(cfg, gen.K, wid, pos0, count, HD), _rows(cfg, gen.V, wid, pos0, count, HD)], axis=1)
+    return np.concatenate([_rows(cfg, gen.K, wid, pos0, count, HD, layer),
+                           _rows(cfg, gen.V, wid, pos0, count, HD, layer)], axis=1)
 
 
-def kv_entries(cfg, wid, kind, groups):
+def kv_entries(cfg, wid, kind, groups, layer=0):
     """CSA (kind 1, groups of m tokens) or HCA (kind 2, groups of m' tokens)
     entries of `groups` -> (codes [n][esz], scales [n][2])."""
     o = _oracle(cfg)
@@ -61,16 +62,16 @@ def kv_entries(cfg, wid, kind, groups):
     codes = np.empty((len(groups), o.esz), np.uint8)
     scales = np.empty((len(groups), 2), np.uint16)
     for j, e in enumerate(groups):
-        codes[j], scales[j] = o.compress_kv(0, kind, _kv_rows(cfg, wid, e * g, g))
+        codes[j], scales[j] = o.compress_kv(layer, kind, _kv_rows(cfg, wid, e * g, g, layer))
     return codes, scales
 
 
-def window_entries(cfg, wid, pos0, count):
+def window_entries(cfg, wid, pos0, count, layer=0):
     """Window tokens [pos0, pos0 + count): K and V halves encoded with one
     scale each."""
     from oracle import encode
     HD = cfg["heads"] * cfg["head_dim"]
-    rows = _kv_rows(cfg, wid, pos0, count)
+    rows = _kv_rows(cfg, wid, pos0, count, layer)
     o = _oracle(cfg)
     codes = np.empty((count, o.esz), np.uint8)
     scales = np.empty((count, 2), np.uint16)

@@ -186,3 +186,146 @@ def test_long_context_full_sampled():
     for t, pos in enumerate(range(L - w["n_win"], L)):
         c, sc = g.window_token(0, s, pos)
         assert np.array_equal(c, win_codes[t]) and np.array_equal(sc, win_scales[t]), f"window token {pos}"
+
+
+def _mixed_schedule(w, steps):
+    """The serving schedule on the host: departures and arrivals (slot,
+    workload id, length) per step and the peak number of sealed blocks.
+    Lengths are lognormal (median 4096, capped); slots are taken lowest first;
+    step 0 has no churn."""
+    B, n_ch, mp_ = w["n_requests"], W.churn_count(w), w["m_prime"]
+    lens = [int(x) for x in W.lognormal_lengths(w["seed"], B, w["len_median"], w["len_sigma"], w["len_cap"])]
+    cur = {s: L for s, L in enumerate(lens)}
+    free, wid, plan, peak = [], B, [], 0
+    for step in range(steps):
+        gone, arrivals = [], []
+        if step > 0:
+            order = sorted(cur)
+            gone = [order[j] for j in W.churn_picks(w["seed"], step, len(order), n_ch)]
+            for s in gone:
+                del cur[s]
+            free = sorted(free + gone)
+            for L in W.lognormal_lengths(w["seed"], n_ch, w["len_median"], w["len_sigma"], w["len_cap"],
+                                         index0=B + (step - 1) * n_ch):
+                s = free.pop(0)
+                arrivals.append((s, wid, int(L)))
+                cur[s] = int(L)
+                wid += 1
+        for s in cur:
+            cur[s] += 1
+        plan.append((gone, arrivals))
+        peak = max(peak, sum(L // mp_ for L in cur.values()))
+    return lens, plan, peak
+
+
+def test_mixed_serving_full_sampled():
+    """256 requests, lognormal lengths (median 4096, capped at 131072), four
+    layers [SWA-only, CSA, HCA, CSA], window 4096, top_k 1024; from the second
+    step on, 10% of the requests finish and as many arrive (their prefill
+    appended in 2048-token chunks) before every live request decodes one token
+    and attends in every layer, for 200 steps.  Block tables are checked against
+    the smallest-free policy replayed on the host (ids reused after
+    departures); for three requests (the longest live one and the two last
+    arrivals) the oracle recomputes every layer's attention output of the
+    last step from the generator's tokens, with the CSA layers' top-k sets
+    compared bit for bit, and sampled stored CSA entries byte for byte."""
+    from tests import oracle_pool as OP
+    import oracle as O
+    w = W.MIXED_SERVING
+    steps, C, mp_, top_k, n_win = w["decode_steps"], w["chunk"], w["m_prime"], w["top_k"], w["n_win"]
+    lens, plan, peak = _mixed_schedule(w, steps)
+    B = w["n_requests"]
+    g = GpuCase(w, B, peak + 64, (w["len_cap"] + steps) // mp_ + 2, B, top_k)
+    assert [g.pool.alloc_request() for _ in range(B)] == list(range(B))
+    import heapq
+    live = {s: [s, 0] for s in range(B)}  # slot -> [workload id, length]
+    free_ids = list(range(peak + 64))  # a heap
+    table = {s: [] for s in live}
+
+    def append(slots, counts):
+        assert g.append(slots, [live[s][0] for s in slots], [live[s][1] for s in slots], counts, check=False) == 0
+        # replay: smallest free id at each seal, requests in batch order, then positions
+        for s, c in zip(slots, counts):
+            for _ in range((live[s][1] + c) // mp_ - live[s][1] // mp_):
+                table[s].append(heapq.heappop(free_ids))
+            live[s][1] += c
+
+    def prefill(slots, targets):
+        while True:
+            cnt = [min(C, t - live[s][1]) for s, t in zip(slots, targets)]
+            if sum(cnt) == 0:
+                return
+            append(slots, cnt)
+
+    prefill(list(range(B)), lens)
+    last = {}
+    for step, (gone, arrivals) in enumerate(plan):
+        for s in gone:
+            g.pool.free_request(s)
+            for b in table.pop(s):
+                heapq.heappush(free_ids, b)
+            del live[s]
+        for s, wid, _ in arrivals:
+            assert g.pool.alloc_request() == s
+            live[s] = [wid, 0]
+            table[s] = []
+        if arrivals:
+            prefill([a[0] for a in arrivals], [a[2] for a in arrivals])
+        slots = sorted(live)
+        append(slots, [1] * len(slots))
+        for layer in range(4):
+            out, tk = g.attend(layer, slots, [live[s][0] for s in slots], step, top_k)
+            if step == steps - 1:
+                last[layer] = (slots, out.cpu().numpy(), tk.cpu().numpy())
+        assert g.pool.check_device() == 0
+    for s in sorted(live):
+        rc, info, ids = g.pool.request_info(s)
+        assert info["length"] == live[s][1]
+        assert ids.tolist() == table[s], f"block table of slot {s}"
+    assert g.pool.free_block_count() == len(free_ids)
+    # the oracle's last step for three requests
+    slots = last[0][0]
+    first = max(slots, key=lambda s: live[s][1])
+    late = sorted((s for s in slots if s != first), key=lambda s: -live[s][0])[:2]
+    o = OP._oracle(w)
+    pool = _spawn_pool()
+    try:
+        n_w = pool._processes
+        for s in [first] + late:
+            wid_s, L = live[s]
+            i = slots.index(s)
+            for layer, kind in enumerate(w["layer_kinds"]):
+                q, qi = H.queries(w, layer, [wid_s], steps - 1)
+                wc, ws = OP.window_entries(w, wid_s, max(0, L - n_win), min(L, n_win), layer)
+                codes, scales = [wc], [ws]
+                if kind == W.CSA:
+                    n_csa = L // w["m"]
+                    cuts = np.linspace(0, n_csa, 2 * n_w + 1).astype(int)
+                    sc = np.concatenate(pool.starmap(OP.idx_scores, [(w, wid_s, qi[0], int(a), int(b), layer)
+                                                                     for a, b in zip(cuts[:-1], cuts[1:])]))
+                    sel = O.topk(sc, top_k)
+                    assert np.array_equal(last[layer][2][i], sel), f"top-k of slot {s}, layer {layer}"
+                    cc, cs = OP.kv_entries(w, wid_s, 1, sel[sel >= 0].tolist(), layer)
+                    codes.insert(0, cc)
+                    scales.insert(0, cs)
+                elif kind == W.HCA:
+                    cuts = np.linspace(0, L // mp_, 2 * n_w + 1).astype(int)
+                    hp = pool.starmap(OP.kv_entries, [(w, wid_s, 2, list(range(int(a), int(b))), layer)
+                                                      for a, b in zip(cuts[:-1], cuts[1:])])
+                    codes.insert(0, np.concatenate([p[0] for p in hp]))
+                    scales.insert(0, np.concatenate([p[1] for p in hp]))
+                rc, ref = o.attend_sources(np.concatenate(codes), np.concatenate(scales), q[0])
+                assert rc == 0
+                check_out(last[layer][1][i].reshape(ref.shape), ref, w["cache_dtype"])
+            # sampled stored CSA entries of the two CSA layers
+            _, ids = g.pool.request_info(s)[1:]
+            n_csa = L // w["m"]
+            es = sorted(set(np.random.default_rng(s).integers(0, n_csa, 8).tolist())) if n_csa else []
+            for layer in (1, 3):
+                cc, cs = OP.kv_entries(w, wid_s, 1, es, layer)
+                for j, e in enumerate(es):
+                    c, sc_ = g.csa_entry(layer, s, e, ids)
+                    assert np.array_equal(c, cc[j]) and np.array_equal(sc_, cs[j]), f"CSA entry {e}, layer {layer}"
+    finally:
+        pool.close()
+        pool.join()
