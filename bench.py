@@ -216,6 +216,31 @@ class Clocks:
         return dict(sm_mhz=statistics.median(sm), sm_max_mhz=mx, reasons=sorted(reasons), samples=len(sm))
 
 
+# ---------------------------------------------------------------------------
+# replicas: one pool per rank, no data-path collective
+# ---------------------------------------------------------------------------
+def rank_env():
+    """(world size, rank, local rank) from the torchrun environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def replica_wids(rank, n_requests):
+    """Workload ids of this rank's requests: every rank serves its own."""
+    return [rank * n_requests + i for i in range(n_requests)]
+
+
+def max_over_ranks(x, world):
+    """The largest value of x over the ranks (the timing of the slowest)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -260,9 +285,7 @@ def main():
         run_reference(args)
         return
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     w = workload(args.config)
     if args.requests or args.context:
         w["n_requests"] = args.requests or w["n_requests"]
@@ -303,7 +326,7 @@ def main():
     arena = torch.empty(K.required_bytes(cfg), dtype=torch.uint8, device=dev)
     pool = K.Pool(cfg, arena, stream)
     slots = [pool.alloc_request() for _ in range(B)]
-    wids = [rank * B + i for i in range(B)]
+    wids = replica_wids(rank, B)
     HD, XD = w["heads"] * w["head_dim"], w["idx_heads"] * w["idx_dim"]
     tdt = torch.float32 if w["in_dtype"] == 0 else torch.bfloat16
     gdt = gen.OUT_F32 if w["in_dtype"] == 0 else gen.OUT_BF16
@@ -387,10 +410,7 @@ def main():
     ms = ev0.elapsed_time(ev1)
     d_ms, d_n, d_b = pool.profile_read(K.KERNEL_NAMES.index(dom))
     pool.check_device(sp)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world)
 
     # per-kernel breakdown: a second pass over the same step inputs, every
     # launch between events (the events themselves cost a little time)
@@ -448,10 +468,7 @@ def main():
     torch.cuda.synchronize()
     barrier()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world)
     h2d = (hk[0].numel() + hv[0].numel() + hx[0].numel() + hq[0].numel() + hqi[0].numel()) * hk.element_size()
     d2h = hout[0].numel() * 4
 
