@@ -18,6 +18,8 @@
 // in fp32) when the query is exactly representable, plain fp32 FMAs if not.
 // fp8 values are weighted by p * scale rounded to f16.  A merge kernel
 // combines the partials.  All waits are time-limited.
+#include <algorithm>
+
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -551,9 +553,10 @@ __global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __gr
 }
 
 // Merge of the split partials of one (request, head): o = sum_s 2^(m_s - M) o_s
-// / sum_s 2^(m_s - M) l_s.  Warp w merges splits w, w + 32, ... with its own
-// running maximum (one round of loads in flight), lane l owns dims
-// [4l, 4l + 4); the 32 warp results are merged through shared memory.
+// / sum_s 2^(m_s - M) l_s.  Warp w of the CTA's nw warps merges splits w,
+// w + nw, ... with its own running maximum, lane l owns dims [4l, 4l + 4);
+// the warp results are merged through shared memory.  nw is sized to the
+// split count (about four splits per warp, at most kCombineWarps).
 constexpr int kCombineWarps = 32;
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ AttendParams P) {
   pdl_start();
@@ -574,8 +577,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
   const bool on = 4 * lane < d;
   float m = -INFINITY, l = 0.0f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int nw = blockDim.x >> 5;
 #pragma unroll 4
-  for (int s = warp; s < n_split; s += kCombineWarps) {
+  for (int s = warp; s < n_split; s += nw) {
     const int64_t gs = R.part_base + s;
     const float2 ml = *reinterpret_cast<const float2*>(P.part_ml + (gs * pd.heads + h) * 2);
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -603,9 +607,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
   __syncthreads();
   if (threadIdx.x < d) {
     float M = -INFINITY;
-    for (int w = 0; w < kCombineWarps; ++w) M = fmaxf(M, red_m[w]);
+    for (int w = 0; w < nw; ++w) M = fmaxf(M, red_m[w]);
     float num = 0.0f, den = 0.0f;
-    for (int w = 0; w < kCombineWarps; ++w) {
+    for (int w = 0; w < nw; ++w) {
       if (red_m[w] == -INFINITY) continue;
       const float wt = exp2f(red_m[w] - M);
       num = fmaf(red_o[w][threadIdx.x], wt, num);
@@ -677,7 +681,11 @@ int launch_attend(const AttendParams& p, int part, int ctas, void* stream, int* 
 int launch_combine(const AttendParams& p, void* stream, int* n_kernels) {
   if (p.n <= 0) return 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  launch_kernel(true, combine_kernel, dim3(p.n, p.pool.heads), dim3(kCombineWarps * 32), 0, s, p);
+  int max_split = 1;
+  for (int i = 0; i < p.n; ++i) max_split = std::max(max_split, p.reqs[i].n_split0 + p.reqs[i].n_split1);
+  // enough threads for the output row (head_dim), about four splits per warp
+  const int nw = std::min(kCombineWarps, std::max((p.pool.head_dim + 31) / 32, (max_split + 3) / 4));
+  launch_kernel(true, combine_kernel, dim3(p.n, p.pool.heads), dim3(nw * 32), 0, s, p);
   *n_kernels += 1;
   return (int)cudaGetLastError();
 }
