@@ -20,7 +20,7 @@ SRC = os.path.join(HERE, "kvoracle.c")
 HDR = os.path.join(HERE, "kvoracle.h")
 LIB = os.path.join(HERE, "libkvoracle.so")
 
-F32, BF16, FP8 = 0, 1, 2
+F32, BF16, FP8, FP4 = 0, 1, 2, 3  # FP4: indexer entries only
 SWA_ONLY, CSA, HCA, CSA_HCA = 0, 1, 2, 3
 OK, ERR_INVALID_ARG, ERR_OUT_OF_BLOCKS, ERR_OUT_OF_REQUESTS, ERR_BAD_REQUEST, ERR_NOT_SHAREABLE = 0, -1, -2, -3, -4, -5
 ERR_CAPACITY = -8
@@ -48,7 +48,7 @@ class _Config(C.Structure):
                 ("layer_kinds", C.POINTER(C.c_int32)),
                 ("max_requests", C.c_int32), ("max_blocks", C.c_int32), ("max_blocks_per_request", C.c_int32),
                 ("gate_csa", C.POINTER(C.c_float)), ("gate_hca", C.POINTER(C.c_float)),
-                ("gate_idx", C.POINTER(C.c_float))]
+                ("gate_idx", C.POINTER(C.c_float)), ("idx_fp4", C.c_int32)]
 
 
 class _Info(C.Structure):
@@ -70,6 +70,10 @@ def lib():
         L.kvo_e4m3_from_f32.argtypes = [C.c_float]
         L.kvo_f32_from_e4m3.restype = C.c_float
         L.kvo_f32_from_e4m3.argtypes = [C.c_uint8]
+        L.kvo_e2m1_from_f32.restype = C.c_uint8
+        L.kvo_e2m1_from_f32.argtypes = [C.c_float]
+        L.kvo_f32_from_e2m1.restype = C.c_float
+        L.kvo_f32_from_e2m1.argtypes = [C.c_uint8]
         L.kvo_softmax_f32.argtypes = [vp, C.c_int, vp]
         L.kvo_encode.argtypes = [C.c_int, vp, C.c_int, vp, vp]
         L.kvo_decode.restype = C.c_double
@@ -112,6 +116,11 @@ def value_bytes(dtype: int) -> int:
     return 4 if dtype == F32 else 2 if dtype == BF16 else 1
 
 
+def code_bytes(dtype: int, n: int) -> int:
+    """Bytes of n encoded values (FP4: two per byte)."""
+    return (n + 1) // 2 if dtype == FP4 else n * value_bytes(dtype)
+
+
 # ---- scalar codecs -----------------------------------------------------
 def bf16_from_f32(x: float) -> int:
     return lib().kvo_bf16_from_f32(float(x))
@@ -129,6 +138,14 @@ def f32_from_e4m3(c: int) -> float:
     return lib().kvo_f32_from_e4m3(int(c))
 
 
+def e2m1_from_f32(x: float) -> int:
+    return lib().kvo_e2m1_from_f32(float(x))
+
+
+def f32_from_e2m1(c: int) -> float:
+    return lib().kvo_f32_from_e2m1(int(c))
+
+
 def softmax_f32(logits) -> np.ndarray:
     g = _f32(logits)
     out = np.zeros_like(g)
@@ -139,7 +156,7 @@ def softmax_f32(logits) -> np.ndarray:
 def encode(dtype: int, x):
     """-> (codes uint8 array, scale uint16)"""
     x = _f32(x)
-    code = np.zeros(x.size * value_bytes(dtype), np.uint8)
+    code = np.zeros(code_bytes(dtype, x.size), np.uint8)
     scale = np.zeros(1, np.uint16)
     lib().kvo_encode(dtype, _p(x), x.size, _p(code), _p(scale))
     return code, int(scale[0])
@@ -164,7 +181,8 @@ class Oracle:
     the fp32 values of the input-dtype tensors."""
 
     def __init__(self, *, m, m_prime, n_win, heads, head_dim, idx_heads, idx_dim, in_dtype, cache_dtype,
-                 layer_kinds, max_requests, max_blocks, max_blocks_per_request, gate_csa, gate_hca, gate_idx):
+                 layer_kinds, max_requests, max_blocks, max_blocks_per_request, gate_csa, gate_hca, gate_idx,
+                 idx_fp4=0):
         self.L = lib()
         self.kinds = np.ascontiguousarray(layer_kinds, dtype=np.int32)
         n_layers = self.kinds.size
@@ -175,7 +193,7 @@ class Oracle:
         cfg = _Config(m, m_prime, n_win, heads, head_dim, idx_heads, idx_dim, in_dtype, cache_dtype, n_layers,
                       self.kinds.ctypes.data_as(C.POINTER(C.c_int32)), max_requests, max_blocks,
                       max_blocks_per_request, self.g_csa.ctypes.data_as(fp), self.g_hca.ctypes.data_as(fp),
-                      self.g_idx.ctypes.data_as(fp))
+                      self.g_idx.ctypes.data_as(fp), int(idx_fp4))
         h = C.c_void_p()
         rc = self.L.kvo_create(C.byref(cfg), C.byref(h))
         if rc != OK:
@@ -187,7 +205,8 @@ class Oracle:
         self.cache_dtype, self.in_dtype, self.n_layers = cache_dtype, in_dtype, n_layers
         self.vs = value_bytes(cache_dtype)
         self.esz = 2 * self.HD * self.vs
-        self.xsz = self.XD * self.vs
+        self.idx_dtype = FP4 if idx_fp4 else cache_dtype
+        self.xsz = code_bytes(self.idx_dtype, self.XD)
         self.CB = m_prime // m
 
     def __del__(self):

@@ -68,6 +68,29 @@ float kvo_f32_from_e4m3(uint8_t c) {
   return (float)((c & 0x80) ? -v : v);
 }
 
+/* e2m1 (OCP MX FP4): 1 sign, 2 exponent (bias 1), 1 mantissa bit; the
+ * magnitudes 0, 0.5 (subnormal), 1, 1.5, 2, 3, 4, 6; no infinities or NaN.
+ * The nearest magnitude wins, a tie goes to the even code (mantissa bit 0),
+ * anything at or beyond 6 saturates to 6; the sign bit is the sign of x. */
+static const float kE2m1[8] = {0.0f, 0.5f, 1.0f, 1.5f, 2.0f, 3.0f, 4.0f, 6.0f};
+
+uint8_t kvo_e2m1_from_f32(float x) {
+  const uint8_t sign = signbit(x) ? 8 : 0;
+  const float a = fabsf(x);
+  if (a >= 6.0f) return sign | 7;
+  int best = 0;
+  for (int c = 1; c < 8; ++c) {
+    const float d = fabsf(a - kE2m1[c]), db = fabsf(a - kE2m1[best]);
+    if (d < db || (d == db && (c & 1) == 0)) best = c;
+  }
+  return (uint8_t)(sign | best);
+}
+
+float kvo_f32_from_e2m1(uint8_t c) {
+  const float v = kE2m1[c & 7];
+  return (c & 8) ? -v : v;
+}
+
 void kvo_softmax_f32(const float* g, int n, float* alpha) {
   double mx = g[0];
   for (int i = 1; i < n; ++i)
@@ -84,6 +107,8 @@ void kvo_softmax_f32(const float* g, int n, float* alpha) {
 
 int kvo_value_bytes(int dtype) { return dtype == KVO_F32 ? 4 : dtype == KVO_BF16 ? 2 : 1; }
 
+int64_t kvo_code_bytes(int dtype, int64_t n) { return dtype == KVO_FP4 ? (n + 1) / 2 : n * kvo_value_bytes(dtype); }
+
 void kvo_encode(int dtype, const float* x, int n, uint8_t* code, uint16_t* scale) {
   if (dtype == KVO_F32) {
     memcpy(code, x, 4 * (size_t)n);
@@ -93,13 +118,19 @@ void kvo_encode(int dtype, const float* x, int n, uint8_t* code, uint16_t* scale
       memcpy(code + 2 * (size_t)i, &b, 2);
     }
   } else {
+    const float top = dtype == KVO_FP4 ? 6.0f : 448.0f;
     float amax = 0.0f;
     for (int i = 0; i < n; ++i)
       if (fabsf(x[i]) > amax) amax = fabsf(x[i]);
-    uint16_t sb = kvo_bf16_from_f32(amax / 448.0f);
+    uint16_t sb = kvo_bf16_from_f32(amax / top);
     if (sb == 0) sb = 0x3F80; /* 1.0 */
     float s = kvo_f32_from_bf16(sb);
-    for (int i = 0; i < n; ++i) code[i] = kvo_e4m3_from_f32(x[i] / s);
+    if (dtype == KVO_FP4) {
+      for (int i = 0; i < (n + 1) / 2; ++i) code[i] = 0;
+      for (int i = 0; i < n; ++i) code[i / 2] |= (uint8_t)(kvo_e2m1_from_f32(x[i] / s) << (4 * (i & 1)));
+    } else {
+      for (int i = 0; i < n; ++i) code[i] = kvo_e4m3_from_f32(x[i] / s);
+    }
     *scale = sb;
   }
 }
@@ -116,12 +147,13 @@ static float raw_value(int dtype, const uint8_t* code, int i) {
     memcpy(&b, code + 2 * (size_t)i, 2);
     return kvo_f32_from_bf16(b);
   }
+  if (dtype == KVO_FP4) return kvo_f32_from_e2m1((uint8_t)((code[i / 2] >> (4 * (i & 1))) & 15));
   return kvo_f32_from_e4m3(code[i]);
 }
 
 double kvo_decode(int dtype, const uint8_t* code, const uint16_t* scale, int i) {
   double v = raw_value(dtype, code, i);
-  if (dtype == KVO_FP8) v *= (double)kvo_f32_from_bf16(*scale);
+  if (dtype == KVO_FP8 || dtype == KVO_FP4) v *= (double)kvo_f32_from_bf16(*scale);
   return v;
 }
 
@@ -167,6 +199,7 @@ struct kvo {
   kvo_config c;
   int32_t* kinds;
   int HD, XD, CB, esz, xsz, vs;
+  int idx_dtype; /* indexer entries: the cache dtype, or KVO_FP4 */
   float* alpha_csa; /* [n_layers][H][m]  */
   float* alpha_hca; /* [n_layers][H][m'] */
   float* alpha_idx; /* [n_layers][Ih][m] */
@@ -205,6 +238,7 @@ int kvo_create(const kvo_config* cfg, kvo_t** out) {
   if (c->heads < 1 || c->head_dim < 1 || c->idx_heads < 1 || c->idx_dim < 1) return KVO_ERR_INVALID_ARG;
   if (c->in_dtype != KVO_F32 && c->in_dtype != KVO_BF16) return KVO_ERR_INVALID_ARG;
   if (c->cache_dtype < KVO_F32 || c->cache_dtype > KVO_FP8) return KVO_ERR_INVALID_ARG;
+  if (c->idx_fp4 != 0 && c->idx_fp4 != 1) return KVO_ERR_INVALID_ARG;
   if (c->n_layers < 1 || !c->layer_kinds) return KVO_ERR_INVALID_ARG;
   if (c->max_requests < 1 || c->max_blocks < 1 || c->max_blocks_per_request < 1) return KVO_ERR_INVALID_ARG;
   for (int l = 0; l < c->n_layers; ++l)
@@ -220,7 +254,8 @@ int kvo_create(const kvo_config* cfg, kvo_t** out) {
   o->CB = c->m_prime / c->m; /* CSA entries per block */
   o->vs = kvo_value_bytes(c->cache_dtype);
   o->esz = 2 * o->HD * o->vs;
-  o->xsz = o->XD * o->vs;
+  o->idx_dtype = c->idx_fp4 ? KVO_FP4 : c->cache_dtype;
+  o->xsz = (int)kvo_code_bytes(o->idx_dtype, o->XD);
 
   /* gates: alpha = softmax over the group's positions, per layer and head */
   o->alpha_csa = (float*)calloc((size_t)c->n_layers * c->heads * c->m, sizeof(float));
@@ -333,15 +368,15 @@ int kvo_compress_idx(const kvo_t* o, int layer, const float* keys, uint8_t* code
     acc[v] = a;
   }
   *scale = 0;
-  kvo_encode(o->c.cache_dtype, acc, XD, code, scale);
+  kvo_encode(o->idx_dtype, acc, XD, code, scale);
   free(acc);
   return KVO_OK;
 }
 
 float kvo_score(const kvo_t* o, const uint8_t* code, const uint16_t* scale, const float* q_idx) {
   float a = 0.0f;
-  for (int v = 0; v < o->XD; ++v) a = fmaf(q_idx[v], raw_value(o->c.cache_dtype, code, v), a);
-  if (o->c.cache_dtype == KVO_FP8) a = a * kvo_f32_from_bf16(*scale);
+  for (int v = 0; v < o->XD; ++v) a = fmaf(q_idx[v], raw_value(o->idx_dtype, code, v), a);
+  if (o->idx_dtype == KVO_FP8 || o->idx_dtype == KVO_FP4) a = a * kvo_f32_from_bf16(*scale);
   return a;
 }
 

@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-enum { KVO_F32 = 0, KVO_BF16 = 1, KVO_FP8 = 2 };
+enum { KVO_F32 = 0, KVO_BF16 = 1, KVO_FP8 = 2, KVO_FP4 = 3 /* indexer entries only */ };
 enum { KVO_SWA_ONLY = 0, KVO_CSA = 1, KVO_HCA = 2, KVO_CSA_HCA = 3 };
 enum {
   KVO_OK = 0,
@@ -79,6 +79,7 @@ typedef struct kvo_config {
   const float* gate_csa; /* logits [n_layers][heads][m]       */
   const float* gate_hca; /* logits [n_layers][heads][m_prime] */
   const float* gate_idx; /* logits [n_layers][idx_heads][m]   */
+  int32_t idx_fp4;       /* 1: indexer entries in FP4 (e2m1 + one bf16 scale), 0: in the cache dtype */
 } kvo_config;
 
 typedef struct kvo kvo_t;
@@ -88,12 +89,16 @@ uint16_t kvo_bf16_from_f32(float x);
 float kvo_f32_from_bf16(uint16_t b);
 uint8_t kvo_e4m3_from_f32(float x); /* round to nearest even, saturate to +-448 */
 float kvo_f32_from_e4m3(uint8_t c);
+uint8_t kvo_e2m1_from_f32(float x); /* 4-bit code: round to nearest even, saturate to +-6 */
+float kvo_f32_from_e2m1(uint8_t c);
 
 /* softmax of n logits, computed in double, rounded to fp32 */
 void kvo_softmax_f32(const float* logits, int n, float* alpha);
 
-/* Encode n fp32 values into the cache dtype: codes are 4/2/1 bytes per value
- * (f32 bits, bf16 bits, e4m3); fp8 writes one bf16 scale to *scale. */
+/* Encode n fp32 values: codes are 4/2/1 bytes per value (f32 bits, bf16
+ * bits, e4m3) or two e2m1 codes per byte (FP4, element 2j in the low
+ * nibble); fp8 and fp4 write one bf16 scale to *scale (amax / 448, amax / 6;
+ * 1 if that is 0). */
 void kvo_encode(int dtype, const float* x, int n, uint8_t* code, uint16_t* scale);
 /* Exact value of element i of an encoded vector (fp8 multiplies its scale). */
 double kvo_decode(int dtype, const uint8_t* code, const uint16_t* scale, int i);
@@ -149,6 +154,8 @@ int kvo_window_token(const kvo_t* o, int layer, int32_t req, int64_t pos, uint8_
 /* all indexer scores of a request: out[n_csa] */
 int kvo_request_scores(const kvo_t* o, int layer, int32_t req, const float* q_idx, float* out);
 int kvo_value_bytes(int dtype);
+/* bytes of n encoded values (FP4: two per byte) */
+int64_t kvo_code_bytes(int dtype, int64_t n);
 
 #ifdef __cplusplus
 }

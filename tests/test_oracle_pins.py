@@ -542,3 +542,78 @@ def test_swa_only_layer_is_sliding_window_attention():
     # the SWA-only layer never forms entries, but blocks still seal (one id spans all layers)
     _, info, ids = o.request_info(r)
     assert info["n_blocks"] == 3 and o.request_entry(0, r, 1, 0)[0] == O.ERR_INVALID_ARG
+
+
+# --------------------------------------------------------------------------
+# FP4 (e2m1) indexer entries
+# --------------------------------------------------------------------------
+def _e2m1_value(code):
+    """Value of a 4-bit e2m1 code from its bit layout: sign, 2 exponent bits
+    (bias 1), 1 mantissa bit; exponent 0 is subnormal (0.m x 2^0)."""
+    s, e, m = code >> 3, (code >> 1) & 3, code & 1
+    mag = m * 0.5 if e == 0 else (1 + m / 2) * 2.0 ** (e - 1)
+    return -mag if s else mag
+
+
+def test_e2m1_codes_decode_to_the_format_values():
+    assert [_e2m1_value(c) for c in range(8)] == [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    for c in range(16):
+        v = O.f32_from_e2m1(c)
+        assert v == _e2m1_value(c) and math.copysign(1, v) == (-1 if c & 8 else 1)
+
+
+def test_e2m1_rounds_to_nearest_even_and_saturates():
+    from fractions import Fraction
+    mags = [Fraction(_e2m1_value(c)) for c in range(8)]
+
+    def expect(x):
+        s = 8 if math.copysign(1, x) < 0 else 0
+        a = Fraction(abs(x))
+        if a >= 6:
+            return s | 7
+        d = [abs(a - v) for v in mags]
+        best = min(d)
+        ties = [c for c in range(8) if d[c] == best]
+        return s | (ties[0] if len(ties) == 1 else [c for c in ties if c & 1 == 0][0])
+
+    xs = [0.0, -0.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.0, 7.0, 1e9, -0.25, -5.0, -1e-30, 0.2499, 0.2501,
+          4.999, 5.001]
+    rng = np.random.default_rng(21)
+    xs += list(rng.uniform(-8, 8, 2000).astype(np.float32)) + list((rng.standard_normal(500) * 1e-3).astype(np.float32))
+    for x in xs:
+        x = float(np.float32(x))
+        assert O.e2m1_from_f32(x) == expect(x), x
+
+
+def test_fp4_entry_scale_packing_and_error_bound():
+    rng = np.random.default_rng(22)
+    for trial in range(20):
+        x = (rng.standard_normal(256) * 10.0 ** rng.uniform(-3, 3)).astype(np.float32)
+        code, sc = O.encode(O.FP4, x)
+        assert code.size == 128
+        amax = np.float32(np.max(np.abs(x)))
+        assert sc == torch.tensor(float(amax / np.float32(6.0)), dtype=torch.float32).to(torch.bfloat16).view(torch.int16).item() & 0xFFFF
+        s = float(torch.tensor([sc], dtype=torch.int16).view(torch.bfloat16).float().item())
+        for i in range(256):
+            nib = (int(code[i // 2]) >> (4 * (i & 1))) & 15
+            assert nib == O.e2m1_from_f32(float(np.float32(x[i] / np.float32(s))))
+        dec = O.decode(O.FP4, code, sc, 256)
+        assert np.all(np.abs(dec - x) <= 0.25 * np.maximum(np.abs(x), s) + 1e-30)
+    code, sc = O.encode(O.FP4, np.zeros(32, np.float32))
+    assert sc == 0x3F80 and not code.any()
+
+
+def test_fp4_indexer_score_is_the_fixed_chain_times_the_scale():
+    cfg = small_cfg(idx_heads=4, idx_dim=64, in_dtype=O.BF16, cache_dtype=O.FP8, idx_fp4=1)
+    o = oracle_for(cfg)
+    assert o.xsz == 128
+    rng = np.random.default_rng(23)
+    keys = rng.standard_normal((4, 256)).astype(np.float32)
+    code, sc = o.compress_idx(0, keys)
+    s = np.float32(torch.tensor([int(sc[0])], dtype=torch.int16).view(torch.bfloat16).float().item())
+    q = torch.tensor(rng.standard_normal(256), dtype=torch.bfloat16).float().numpy()
+    acc = np.float32(0.0)
+    for v in range(256):
+        val = np.float32(_e2m1_value((int(code[v // 2]) >> (4 * (v & 1))) & 15))
+        acc = np.float32(acc + np.float32(q[v] * val))  # the product of bf16 and e2m1 values is exact in fp32
+    assert o.score(code, sc, q) == np.float32(acc * s)
