@@ -38,18 +38,21 @@ NOMINAL_HBM_GBS = 8000.0
 # ---------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------
-def workload(name):
+def workload(name, idx_fp4=False):
+    """The workload recipe; idx_fp4 stores the indexer entries in FP4 (e2m1 +
+    one bf16 scale) instead of the cache dtype."""
     from heterogeneous_compressed_kv_gb300.gen import workloads as W
     if name == "long_context":
         w = dict(W.LONG_CONTEXT)
         w["lengths"] = [w["length"]] * w["n_requests"]
-        return w
-    if name == "decode_batch":
+    elif name == "decode_batch":
         w = dict(W.DECODE_BATCH)
         w["lengths"] = W.uniform_lengths(w["seed"], w["n_requests"], w["len_lo"], w["len_hi"]).tolist()
         w["chunk"] = 2048
-        return w
-    raise SystemExit(f"unknown config {name}")
+    else:
+        raise SystemExit(f"unknown config {name}")
+    w["idx_fp4"] = 1 if idx_fp4 else 0
+    return w
 
 
 def gates(w):
@@ -66,12 +69,12 @@ def gates(w):
 def _oracle_worker(args):
     """Prefill one workload request into the oracle (untimed), then time
     `steps` decode steps (append 1 token + decode_attend) of it."""
-    name, wid, steps, warm = args
+    name, idx_fp4, wid, steps, warm = args
     sys.path.insert(0, ROOT)
     import numpy as np
     import oracle as O
     from heterogeneous_compressed_kv_gb300 import gen
-    w = workload(name)
+    w = workload(name, idx_fp4)
     L0 = int(w["lengths"][wid])
     total = L0 + warm + steps + 1
     g = gates(w)
@@ -79,7 +82,7 @@ def _oracle_worker(args):
                  idx_heads=w["idx_heads"], idx_dim=w["idx_dim"], in_dtype=w["in_dtype"],
                  cache_dtype=w["cache_dtype"], layer_kinds=w["layer_kinds"], max_requests=1,
                  max_blocks=total // w["m_prime"] + 1, max_blocks_per_request=total // w["m_prime"] + 1,
-                 gate_csa=g[0], gate_hca=g[1], gate_idx=g[2])
+                 gate_csa=g[0], gate_hca=g[1], gate_idx=g[2], idx_fp4=w["idx_fp4"])
     _, r = o.alloc_request()
     HD, XD = w["heads"] * w["head_dim"], w["idx_heads"] * w["idx_dim"]
     dt = gen.OUT_F32 if w["in_dtype"] == 0 else gen.OUT_BF16
@@ -117,11 +120,11 @@ def _oracle_worker(args):
     return time.perf_counter() - t0, t_setup
 
 
-def start_oracle(name, n_workers, steps, warm):
+def start_oracle(name, n_workers, steps, warm, idx_fp4=False):
     """Spawned before any CUDA call: one oracle process per sampled request."""
     ctx = mp.get_context("spawn")
     pool = ctx.Pool(n_workers)
-    res = pool.map_async(_oracle_worker, [(name, i, steps, warm) for i in range(n_workers)])
+    res = pool.map_async(_oracle_worker, [(name, idx_fp4, i, steps, warm) for i in range(n_workers)])
     return pool, res
 
 
@@ -137,9 +140,9 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    w = workload(args.config)
+    w = workload(args.config, args.idx_fp4)
     n = oracle_workers(w)
-    pool, res = start_oracle(args.config, n, args.steps, args.warmup)
+    pool, res = start_oracle(args.config, n, args.steps, args.warmup, args.idx_fp4)
     out = res.get()
     pool.close()
     t = max(o[0] for o in out)
@@ -161,6 +164,8 @@ def config_block(w, args):
              indexer=f"{w['idx_heads']}x{w['idx_dim']}", m=w["m"], m_prime=w["m_prime"], n_win=w["n_win"],
              top_k=w["top_k"], in_dtype={0: "f32", 1: "bf16"}[w["in_dtype"]],
              cache_dtype={0: "f32", 1: "bf16", 2: "fp8_e4m3+bf16_scale"}[w["cache_dtype"]])
+    if w.get("idx_fp4"):
+        c["indexer_dtype"] = "fp4_e2m1+bf16_scale"
     if w["name"] == "long_context":
         c["context"] = w["length"]
     else:
@@ -280,13 +285,14 @@ def main():
     ap.add_argument("--requests", type=int, default=0, help="override the request count (profiling cases)")
     ap.add_argument("--context", type=int, default=0, help="override the long-context length (profiling cases)")
     ap.add_argument("--timeline", type=int, default=0, help="print the launch timeline of this many extra steps")
+    ap.add_argument("--idx-fp4", action="store_true", help="indexer entries in FP4 (e2m1 + one bf16 scale)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
         return
 
     world, rank, local = rank_env()
-    w = workload(args.config)
+    w = workload(args.config, args.idx_fp4)
     if args.requests or args.context:
         w["n_requests"] = args.requests or w["n_requests"]
         L = args.context or w.get("length", 0)
@@ -297,7 +303,7 @@ def main():
     # the oracle baseline is spawned before the first CUDA call
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = (oracle_workers(w),) + start_oracle(args.config, oracle_workers(w), args.cpu_steps, 1)
+        cpu = (oracle_workers(w),) + start_oracle(args.config, oracle_workers(w), args.cpu_steps, 1, args.idx_fp4)
 
     import numpy as np
     import torch
@@ -322,7 +328,8 @@ def main():
                        idx_heads=w["idx_heads"], idx_dim=w["idx_dim"], in_dtype=w["in_dtype"],
                        cache_dtype=w["cache_dtype"], layer_kinds=w["layer_kinds"], max_requests=B,
                        max_blocks=sum((L + extra) // mp_ + 1 for L in lengths), max_blocks_per_request=mbpr,
-                       max_batch=B, max_top_k=w["top_k"], gate_csa=g[0], gate_hca=g[1], gate_idx=g[2])
+                       max_batch=B, max_top_k=w["top_k"], gate_csa=g[0], gate_hca=g[1], gate_idx=g[2],
+                       idx_fp4=w["idx_fp4"])
     arena = torch.empty(K.required_bytes(cfg), dtype=torch.uint8, device=dev)
     pool = K.Pool(cfg, arena, stream)
     slots = [pool.alloc_request() for _ in range(B)]

@@ -3,7 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
-#include <cuda_fp8.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,18 +22,49 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
 
-// e4m3 code -> exact fp32 value (via the hardware f16x2 conversion; every
-// e4m3 value is exact in f16 and in f32)
-__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t two) {
-  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
-  __half2 hh;
-  hh = *reinterpret_cast<__half2*>(&h);
-  return __half22float2(hh);
+// The short-float conversions below are the sm_100-family PTX instructions
+// (round to nearest even, saturating to the largest finite value); the first
+// operand of a packed conversion goes to the high half.
+
+// two e4m3 codes (the low byte first) -> f16x2; exact
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(two));
+  return h;
 }
 
-// two fp32 -> two e4m3 codes (round to nearest even, saturate to +-448)
+// e4m3 code pair -> exact fp32 values (every e4m3 value is exact in f16 and f32)
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t two) {
+  const uint32_t h = e4m3x2_to_f16x2(two);
+  return make_float2(__half2float(__ushort_as_half((uint16_t)(h & 0xFFFFu))),
+                     __half2float(__ushort_as_half((uint16_t)(h >> 16))));
+}
+
+// two fp32 -> two e4m3 codes (a in the low byte), saturate to +-448
 __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float a, float b) {
-  return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// two fp32 -> two e2m1 codes in one byte (a in the low nibble), saturate to +-6
+__device__ __forceinline__ uint8_t f32x2_to_e2m1x2(float a, float b) {
+  uint16_t r;
+  asm("{.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tmov.b16 %0, {t, 0};}" : "=h"(r) : "f"(a), "f"(b));
+  return (uint8_t)r;
+}
+
+// one byte of two e2m1 codes -> f16x2 (the low nibble in the low half); exact
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint8_t two) {
+  uint32_t h;
+  asm("{.reg .b8 t, z;\n\tmov.b16 {t, z}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;}" : "=r"(h) : "h"((uint16_t)two));
+  return h;
+}
+
+// fp4 scale of a vector with absolute maximum amax: bf16(amax / 6), 1 if 0
+__device__ __forceinline__ uint16_t fp4_scale_bits(float amax) {
+  uint16_t s = f32_to_bf16_bits(__fdiv_rn(amax, 6.0f));
+  return s == 0 ? (uint16_t)0x3F80 : s;
 }
 
 // fp8 scale of a vector with absolute maximum amax: bf16(amax / 448), 1 if 0

@@ -165,6 +165,17 @@ __device__ __forceinline__ void write_idx(uint8_t* base, const PoolDesc& pd, int
   }
 }
 
+// FP4 indexer entry: 8 values at xv0 as 4 bytes of e2m1 pairs (element 2j in
+// the low nibble) inside chunk xv0 / 32 of the block's indexer part.
+__device__ __forceinline__ void write_idx_fp4(uint8_t* base, const PoolDesc& pd, int slot, int xv0, const float* x,
+                                              float s) {
+  uint32_t w = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w |= (uint32_t)f32x2_to_e2m1x2(__fdiv_rn(x[2 * i], s), __fdiv_rn(x[2 * i + 1], s)) << (8 * i);
+  *reinterpret_cast<uint32_t*>(base + ((int64_t)(xv0 / 32) * pd.csa_per_block + slot) * 16 + (xv0 % 32) / 2) = w;
+}
+
 constexpr int kTokGroup = 8;  // tokens whose loads are issued together
 
 template <int IN, int CACHE>
@@ -191,6 +202,8 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   const int hv = v0 - half * HD;
   const int h = hv / pd.head_dim;
   const bool idx_thread = L.has_csa && slice == 0 && tid * kVpt < XD;
+  const bool idx_fp4 = pd.idx_dtype == KVPOOL_FP4_E2M1;
+  const bool idx_scaled = idx_fp4 || pd.idx_dtype == KVPOOL_FP8_E4M3;
   const int xv0 = tid * kVpt;
   const int g = idx_thread ? xv0 / pd.idx_dim : 0;
 
@@ -268,13 +281,16 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
           const int slot = (t + 1) / m - 1;
           write_entry<CACHE>(blk_csa + (int64_t)slot * pd.entry_bytes, pd, v0, half, hv, acc_c, sh);
           float s = 1.0f;
-          if constexpr (CACHE == KVPOOL_FP8_E4M3) {
+          if (idx_scaled) {  // uniform over the CTA: block-wide amax of the indexer entry
             const float3 r = block_max3(0.f, 0.f, idx_thread ? amax8(acc_x) : 0.f, sh);
-            const uint16_t sb = fp8_scale_bits(r.z);
+            const uint16_t sb = idx_fp4 ? fp4_scale_bits(r.z) : fp8_scale_bits(r.z);
             s = bf16_bits_to_f32(sb);
             if (idx_thread && xv0 == 0) *reinterpret_cast<uint16_t*>(blk_idx + L.idx_scale_off + 2 * slot) = sb;
           }
-          if (idx_thread) write_idx<CACHE>(blk_idx, pd, slot, xv0, acc_x, s);
+          if (idx_thread) {
+            if (idx_fp4) write_idx_fp4(blk_idx, pd, slot, xv0, acc_x, s);
+            else write_idx<CACHE>(blk_idx, pd, slot, xv0, acc_x, s);
+          }
 #pragma unroll
           for (int j = 0; j < kVpt; ++j) acc_c[j] = acc_x[j] = 0.0f;
         }
@@ -324,7 +340,7 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
         const int64_t o = ((int64_t)c * CB + e) * 16;
         *reinterpret_cast<uint4*>(blk_idx + o) = *reinterpret_cast<const uint4*>(stg_idx + o);
       }
-      if (CACHE == KVPOOL_FP8_E4M3) {
+      if (idx_scaled) {
         for (int e = tid; e < n_copy; e += blockDim.x)
           *reinterpret_cast<uint16_t*>(blk_idx + L.idx_scale_off + 2 * e) =
               *reinterpret_cast<const uint16_t*>(stg_idx + L.idx_scale_off + 2 * e);

@@ -39,6 +39,12 @@ constexpr int kScoreCtas = 152;         // CTAs of the score kernel per launch (
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int value_bytes(int dtype) { return dtype == KVPOOL_F32 ? 4 : dtype == KVPOOL_BF16 ? 2 : 1; }
 bool kind_has_csa(int k) { return k == KVPOOL_CSA || k == KVPOOL_CSA_HCA; }
+
+// algorithmic bytes of one indexer entry: its codes and (fp8, fp4) its scale
+int64_t idx_algo_bytes(const PoolDesc& pd) {
+  const bool scaled = pd.idx_dtype == KVPOOL_FP8_E4M3 || pd.idx_dtype == KVPOOL_FP4_E2M1;
+  return pd.idx_entry_bytes + (scaled ? 2 : 0);
+}
 bool kind_has_hca(int k) { return k == KVPOOL_HCA || k == KVPOOL_CSA_HCA; }
 
 struct Layout {
@@ -70,6 +76,8 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
   const int HD = c->heads * c->head_dim, XD = c->idx_heads * c->idx_dim;
   if (HD % 256 != 0 || HD > 4096) return "heads * head_dim must be a multiple of 256, at most 4096";
   if (XD % 16 != 0 || XD > 8 * 256) return "idx_heads * idx_dim must be a multiple of 16, at most 2048";
+  if (c->idx_fp4 != 0 && c->idx_fp4 != 1) return "idx_fp4 must be 0 or 1";
+  if (c->idx_fp4 && XD % 32 != 0) return "FP4 indexer entries need idx_heads * idx_dim to be a multiple of 32";
   const int vs = value_bytes(c->cache_dtype);
   bool any_csa = false;
   for (int l = 0; l < c->n_layers; ++l) {
@@ -97,7 +105,8 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
   pd.vs = vs;
   pd.isz = value_bytes(c->in_dtype);
   pd.csa_per_block = c->m_prime / c->m;
-  pd.idx_entry_bytes = (int64_t)XD * vs;
+  pd.idx_dtype = c->idx_fp4 ? KVPOOL_FP4_E2M1 : c->cache_dtype;
+  pd.idx_entry_bytes = c->idx_fp4 ? (int64_t)XD / 2 : (int64_t)XD * vs;
   pd.idx_chunks = (int32_t)(pd.idx_entry_bytes / 16);
   pd.entry_bytes = 2LL * HD * vs + (c->cache_dtype == KVPOOL_FP8_E4M3 ? 16 : 0);
   pd.max_blocks = c->max_blocks;
@@ -130,7 +139,7 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
       d.csa_pool = cur;
       cur = round_up(cur + d.csa_stride * n_ids, 256);
       d.idx_stride = CB * pd.idx_entry_bytes;
-      if (c->cache_dtype == KVPOOL_FP8_E4M3) {
+      if (pd.idx_dtype == KVPOOL_FP8_E4M3 || pd.idx_dtype == KVPOOL_FP4_E2M1) {
         d.idx_scale_off = d.idx_stride;
         d.idx_stride += round_up(2LL * CB, 16);
       }
@@ -522,7 +531,7 @@ int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_
     // algorithmic bytes: inputs read + window tokens and new entries written
     const PoolDesc& pd = p->lay.pd;
     const int64_t fp8 = pd.cache_dtype == KVPOOL_FP8_E4M3 ? 1 : 0;
-    const int64_t entry_algo = 2LL * pd.HD * pd.vs + 4 * fp8, idx_algo = (int64_t)pd.XD * pd.vs + 2 * fp8;
+    const int64_t entry_algo = 2LL * pd.HD * pd.vs + 4 * fp8, idx_algo = idx_algo_bytes(pd);
     int64_t bytes = 0;
     for (int l = 0; l < p->cfg.n_layers; ++l) {
       const LayerDesc& d = p->lay.layers[l];
@@ -610,7 +619,7 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
     // algorithmic bytes: codes + scales actually needed (layout padding excluded)
     const int64_t fp8 = pd.cache_dtype == KVPOOL_FP8_E4M3 ? 1 : 0;
     const int64_t entry_algo = 2LL * pd.HD * pd.vs + 4 * fp8;
-    const int64_t idx_algo = (int64_t)pd.XD * pd.vs + 2 * fp8;
+    const int64_t idx_algo = idx_algo_bytes(pd);
     int64_t total_src = 0, total_segs = 0;
     int score_ctas = 0, key_ctas = 0;
     int64_t score_bytes = 0, attend_bytes = 0, out_bytes = 0;

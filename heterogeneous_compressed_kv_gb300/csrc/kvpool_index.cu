@@ -92,6 +92,25 @@ struct IdxChunk<KVPOOL_FP8_E4M3> {
   }
 };
 
+template <>
+struct IdxChunk<KVPOOL_FP4_E2M1> {  // 32 e2m1 values, element 2j in the low nibble of byte j
+  static constexpr int kVals = 32;
+  __device__ static float chain(const uint4& c, const float* q, float acc) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t h = e2m1x2_to_f16x2((uint8_t)(w[i] >> (8 * b)));
+        const int v = 8 * i + 2 * b;
+        acc = __fmaf_rn(q[v], __half2float(__ushort_as_half((uint16_t)(h & 0xFFFFu))), acc);
+        acc = __fmaf_rn(q[v + 1], __half2float(__ushort_as_half((uint16_t)(h >> 16))), acc);
+      }
+    }
+    return acc;
+  }
+};
+
 // Fast chains: the same fixed-order fp32 chain with the products taken by the
 // mixed-precision FMA (f16 x f16 + f32 or bf16 x bf16 + f32; a product of two
 // f16 or two bf16 values is exact in fp32 and the FMA rounds once, so every
@@ -106,11 +125,6 @@ __device__ __forceinline__ float fma_bf16(uint16_t a, uint16_t b, float c) {
   float d;
   asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
   return d;
-}
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
-  uint32_t h;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(two));
-  return h;
 }
 
 template <int CACHE>
@@ -148,6 +162,24 @@ struct IdxChunkFast<KVPOOL_BF16> {  // 8 keys per chunk, q as 8 bf16
   }
 };
 template <>
+struct IdxChunkFast<KVPOOL_FP4_E2M1> {  // 32 keys per chunk, q as 32 f16
+  __device__ static float chain(const uint4& c, const uint32_t* qh, float acc) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 qv = *reinterpret_cast<const uint4*>(qh + 4 * i);
+      const uint32_t q[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint32_t h = e2m1x2_to_f16x2((uint8_t)(w[i] >> (8 * b)));
+        acc = fma_f16((uint16_t)(h & 0xFFFFu), (uint16_t)(q[b] & 0xFFFFu), acc);
+        acc = fma_f16((uint16_t)(h >> 16), (uint16_t)(q[b] >> 16), acc);
+      }
+    }
+    return acc;
+  }
+};
+template <>
 struct IdxChunkFast<KVPOOL_F32> {  // unused: fp32 keys take the fp32 chain
   __device__ static float chain(const uint4&, const uint32_t*, float acc) { return acc; }
 };
@@ -161,21 +193,30 @@ struct IdxChunkFast<KVPOOL_F32> {  // unused: fp32 keys take the fp32 chain
 // a CTA takes the CTA's blocks w, w + W, w + 2W, ...; a slot's barrier is only
 // waited on by its own warp, in order, so every parity wait is exact.
 // ---------------------------------------------------------------------------
-constexpr int kScoreWarps = 8;
-constexpr int kScoreThreads = kScoreWarps * 32;
+// Warps per score CTA: more warps keep more fixed-order chains in flight; FP4
+// blocks are small enough for 16 warps with 3 slots each, the larger blocks
+// of the other types fit 8.
+template <int IDX>
+struct ScoreShape {
+  static constexpr int kWarps = IDX == KVPOOL_FP4_E2M1 ? 16 : 8;
+  static constexpr int kRegChunks = IDX == KVPOOL_FP4_E2M1 ? 8 : 16;  // key chunks held in registers
+};
+constexpr int kScoreMaxWarps = 16;
 constexpr int kScoreMaxRing = 3;                      // slots per warp
-constexpr int kScoreMaxSlots = kScoreWarps * kScoreMaxRing;
+constexpr int kScoreMaxSlots = kScoreMaxWarps * kScoreMaxRing;
 constexpr int kScoreStageBudget = 200 * 1024;         // shared memory for slots (1 CTA per SM)
+__host__ __device__ constexpr int score_warps(int idx_dtype) { return idx_dtype == KVPOOL_FP4_E2M1 ? 16 : 8; }
 
 template <int IN, int CACHE>
-__global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(const __grid_constant__ AttendParams P, int stage_bytes,
+__global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kernel(const __grid_constant__ AttendParams P, int stage_bytes,
                                                                  int ring, int stage_off) {
   pdl_start();
   extern __shared__ __align__(128) uint8_t sm[];
   const PoolDesc& pd = P.pool;
   const LayerDesc& L = P.layer;
   const int XD = pd.XD;
-  constexpr int CW = kScoreWarps;
+  constexpr int CW = ScoreShape<CACHE>::kWarps;
+  constexpr int KCH = ScoreShape<CACHE>::kRegChunks;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm);
   float* q_sh = reinterpret_cast<float*>(sm + 8 * kScoreMaxSlots);
   uint16_t* qh_sh = reinterpret_cast<uint16_t*>(q_sh + XD);  // q as f16 (fp8 keys) or bf16 (bf16 keys)
@@ -203,7 +244,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(const __grid_co
     const float qv = IN == KVPOOL_F32 ? reinterpret_cast<const float*>(P.q_idx)[row]
                                       : bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(P.q_idx)[row]);
     q_sh[v] = qv;
-    if (CACHE == KVPOOL_FP8_E4M3) {
+    if (CACHE == KVPOOL_FP8_E4M3 || CACHE == KVPOOL_FP4_E2M1) {
       const __half hq = __float2half_rn(qv);
       qh_sh[v] = __half_as_ushort(hq);
       exact &= __half2float(hq) == qv;
@@ -266,13 +307,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(const __grid_co
     const bool valid = lane < CB && E < R.n_cand;
     float acc = 0.0f;
     float scale = 1.0f;
-    if (n_chunks <= 16) {
+    if (n_chunks <= KCH) {
       // the lane's key into registers, then the slot takes the next block
-      uint4 ch[16];
+      uint4 ch[KCH];
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
+      for (int c = 0; c < KCH; ++c)
         if (c < n_chunks && valid) ch[c] = *reinterpret_cast<const uint4*>(stg + ((int64_t)c * CB + lane) * 16);
-      if (CACHE == KVPOOL_FP8_E4M3 && valid)
+      if ((CACHE == KVPOOL_FP8_E4M3 || CACHE == KVPOOL_FP4_E2M1) && valid)
         scale = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(stg + key_bytes + 2 * lane));
       __syncwarp();
       if (j + ring < mine) {
@@ -286,11 +327,11 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(const __grid_co
       if (valid) {
         if (fast) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
+          for (int c = 0; c < KCH; ++c)
             if (c < n_chunks) acc = IdxChunkFast<CACHE>::chain(ch[c], qh + c * (V / 2), acc);
         } else {
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
+          for (int c = 0; c < KCH; ++c)
             if (c < n_chunks) acc = IdxChunk<CACHE>::chain(ch[c], q_sh + c * V, acc);
         }
       }
@@ -301,7 +342,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(const __grid_co
           acc = fast ? IdxChunkFast<CACHE>::chain(chk, qh + c * (V / 2), acc)
                      : IdxChunk<CACHE>::chain(chk, q_sh + c * V, acc);
         }
-        if (CACHE == KVPOOL_FP8_E4M3)
+        if (CACHE == KVPOOL_FP8_E4M3 || CACHE == KVPOOL_FP4_E2M1)
           scale = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(stg + key_bytes + 2 * lane));
       }
       __syncwarp();
@@ -315,7 +356,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_kernel(const __grid_co
       }
     }
     if (valid) {
-      if constexpr (CACHE == KVPOOL_FP8_E4M3) acc = __fmul_rn(acc, scale);
+      if constexpr (CACHE == KVPOOL_FP8_E4M3 || CACHE == KVPOOL_FP4_E2M1) acc = __fmul_rn(acc, scale);
       const uint32_t key = score_key(acc);
       keys[E] = key;
       atomicAdd(&hist[key >> 21], 1u);
@@ -602,10 +643,13 @@ int score_stage_plan(const PoolDesc& pd, int* stage_bytes, int* ring, int* stage
   // one block's indexer part: keys, then (fp8) scales; the same size as the
   // indexer plane's stride
   *stage_bytes = pd.csa_per_block * (int)pd.idx_entry_bytes +
-                 (pd.cache_dtype == KVPOOL_FP8_E4M3 ? (2 * pd.csa_per_block + 15) / 16 * 16 : 0);
-  *ring = std::max(1, std::min(kScoreMaxRing, kScoreStageBudget / (kScoreWarps * *stage_bytes)));
+                 (pd.idx_dtype == KVPOOL_FP8_E4M3 || pd.idx_dtype == KVPOOL_FP4_E2M1
+                      ? (2 * pd.csa_per_block + 15) / 16 * 16
+                      : 0);
+  const int warps = score_warps(pd.idx_dtype);
+  *ring = std::max(1, std::min(kScoreMaxRing, kScoreStageBudget / (warps * *stage_bytes)));
   *stage_off = (8 * kScoreMaxSlots + 6 * pd.XD + 4 * kHistBins + 127) / 128 * 128;
-  *smem = (size_t)*stage_off + (size_t)kScoreWarps * *ring * *stage_bytes;
+  *smem = (size_t)*stage_off + (size_t)warps * *ring * *stage_bytes;
   return 0;
 }
 
@@ -620,21 +664,24 @@ static int launch_score_t(const AttendParams& p, cudaStream_t s) {
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     set = smem;
   }
-  launch_kernel(true, k, dim3(p.total_score_ctas), dim3(kScoreThreads), smem, s, p, sb, ns, so);
+  launch_kernel(true, k, dim3(p.total_score_ctas), dim3(ScoreShape<CACHE>::kWarps * 32), smem, s, p, sb, ns, so);
   return 0;
 }
 
 int launch_score(const AttendParams& p, void* stream, int* n_kernels) {
   if (p.total_score_ctas <= 0) return 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const int key = p.pool.in_dtype * 3 + p.pool.cache_dtype;
+  // the score kernel reads indexer entries only: it is specialised on their type
+  const int key = p.pool.in_dtype * 4 + p.pool.idx_dtype;
   switch (key) {
-    case KVPOOL_F32 * 3 + KVPOOL_F32: launch_score_t<KVPOOL_F32, KVPOOL_F32>(p, s); break;
-    case KVPOOL_F32 * 3 + KVPOOL_BF16: launch_score_t<KVPOOL_F32, KVPOOL_BF16>(p, s); break;
-    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3: launch_score_t<KVPOOL_F32, KVPOOL_FP8_E4M3>(p, s); break;
-    case KVPOOL_BF16 * 3 + KVPOOL_F32: launch_score_t<KVPOOL_BF16, KVPOOL_F32>(p, s); break;
-    case KVPOOL_BF16 * 3 + KVPOOL_BF16: launch_score_t<KVPOOL_BF16, KVPOOL_BF16>(p, s); break;
-    case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3: launch_score_t<KVPOOL_BF16, KVPOOL_FP8_E4M3>(p, s); break;
+    case KVPOOL_F32 * 4 + KVPOOL_F32: launch_score_t<KVPOOL_F32, KVPOOL_F32>(p, s); break;
+    case KVPOOL_F32 * 4 + KVPOOL_BF16: launch_score_t<KVPOOL_F32, KVPOOL_BF16>(p, s); break;
+    case KVPOOL_F32 * 4 + KVPOOL_FP8_E4M3: launch_score_t<KVPOOL_F32, KVPOOL_FP8_E4M3>(p, s); break;
+    case KVPOOL_F32 * 4 + KVPOOL_FP4_E2M1: launch_score_t<KVPOOL_F32, KVPOOL_FP4_E2M1>(p, s); break;
+    case KVPOOL_BF16 * 4 + KVPOOL_F32: launch_score_t<KVPOOL_BF16, KVPOOL_F32>(p, s); break;
+    case KVPOOL_BF16 * 4 + KVPOOL_BF16: launch_score_t<KVPOOL_BF16, KVPOOL_BF16>(p, s); break;
+    case KVPOOL_BF16 * 4 + KVPOOL_FP8_E4M3: launch_score_t<KVPOOL_BF16, KVPOOL_FP8_E4M3>(p, s); break;
+    case KVPOOL_BF16 * 4 + KVPOOL_FP4_E2M1: launch_score_t<KVPOOL_BF16, KVPOOL_FP4_E2M1>(p, s); break;
     default: return (int)cudaErrorInvalidValue;
   }
   *n_kernels += 1;

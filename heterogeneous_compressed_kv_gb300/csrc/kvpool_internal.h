@@ -46,6 +46,7 @@ struct PoolDesc {
   int32_t m, m_prime, n_win;
   int32_t heads, head_dim, idx_heads, idx_dim, HD, XD;
   int32_t in_dtype, cache_dtype, vs, isz;  // cache value bytes, input value bytes
+  int32_t idx_dtype;                       // indexer entries: cache_dtype or KVPOOL_FP4_E2M1
   int32_t csa_per_block, idx_chunks;       // idx_chunks: 16-B chunks per indexer key
   int64_t entry_bytes, idx_entry_bytes;
   int32_t max_blocks, max_requests, max_bpr, staging_base;

@@ -15,7 +15,7 @@ from typing import Optional, Sequence
 
 import numpy as np
 
-F32, BF16, FP8_E4M3 = 0, 1, 2
+F32, BF16, FP8_E4M3, FP4_E2M1 = 0, 1, 2, 3  # FP4: indexer entries only (PoolConfig.idx_fp4)
 SWA_ONLY, CSA, HCA, CSA_HCA = 0, 1, 2, 3
 FLAG_NO_DEVICE = 1
 OK, ERR_INVALID_ARG, ERR_OUT_OF_BLOCKS, ERR_OUT_OF_REQUESTS, ERR_BAD_REQUEST = 0, -1, -2, -3, -4
@@ -43,7 +43,7 @@ class _Config(C.Structure):
                 ("layer_kinds", C.POINTER(C.c_int32)), ("max_requests", C.c_int32), ("max_blocks", C.c_int32),
                 ("max_blocks_per_request", C.c_int32), ("max_batch", C.c_int32), ("max_top_k", C.c_int32),
                 ("gate_csa", C.POINTER(C.c_float)), ("gate_hca", C.POINTER(C.c_float)),
-                ("gate_idx", C.POINTER(C.c_float)), ("flags", C.c_uint32)]
+                ("gate_idx", C.POINTER(C.c_float)), ("flags", C.c_uint32), ("idx_fp4", C.c_int32)]
 
 
 class _Info(C.Structure):
@@ -124,6 +124,7 @@ class PoolConfig:
     gate_hca: np.ndarray  # [n_layers][heads][m_prime]
     gate_idx: np.ndarray  # [n_layers][idx_heads][m]
     flags: int = 0
+    idx_fp4: int = 0  # 1: indexer entries in FP4 (e2m1 + one bf16 scale)
     _keep: list = field(default_factory=list, repr=False)
 
     def to_c(self) -> _Config:
@@ -136,7 +137,7 @@ class PoolConfig:
                        self.in_dtype, self.cache_dtype, kinds.size, kinds.ctypes.data_as(C.POINTER(C.c_int32)),
                        self.max_requests, self.max_blocks, self.max_blocks_per_request, self.max_batch,
                        self.max_top_k, g[0].ctypes.data_as(fp), g[1].ctypes.data_as(fp), g[2].ctypes.data_as(fp),
-                       self.flags)
+                       self.flags, self.idx_fp4)
 
 
 def required_bytes(cfg: PoolConfig) -> int:

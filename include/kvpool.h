@@ -80,6 +80,8 @@ enum {
   KVPOOL_F32 = 0,
   KVPOOL_BF16 = 1,
   KVPOOL_FP8_E4M3 = 2, /* cache only: e4m3 codes + one bf16 scale per K half, V half, indexer entry */
+  KVPOOL_FP4_E2M1 = 3, /* indexer entries only (kvpool_config.idx_fp4): two e2m1 codes per byte (element
+                          2j in the low nibble) + one bf16 scale = bf16(amax / 6), 1 if that is 0 */
 };
 
 /* ---- layer kinds (Figure 12-1 lists SWA, CSA and HCA layers) ---- */
@@ -113,6 +115,9 @@ typedef struct kvpool_config {
   const float* gate_hca;          /* [n_layers][heads][m_prime] */
   const float* gate_idx;          /* [n_layers][idx_heads][m] */
   uint32_t flags;                 /* KVPOOL_FLAG_* */
+  int32_t idx_fp4;                /* 1: indexer entries in FP4 (KVPOOL_FP4_E2M1), 0: in cache_dtype.
+                                     FP4 needs idx_heads * idx_dim to be a multiple of 32.  ([P3] s2.2
+                                     gives the lightning indexer FP4 keys.) */
 } kvpool_config;
 
 typedef struct kvpool kvpool_t;

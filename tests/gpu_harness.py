@@ -39,7 +39,9 @@ class GpuCase:
                                 in_dtype=w["in_dtype"], cache_dtype=w["cache_dtype"], layer_kinds=w["layer_kinds"],
                                 max_requests=max_requests, max_blocks=max_blocks, max_blocks_per_request=mbpr,
                                 max_batch=max_batch, max_top_k=max_top_k, gate_csa=g[0], gate_hca=g[1],
-                                gate_idx=g[2])
+                                gate_idx=g[2], idx_fp4=w.get("idx_fp4", 0))
+        # indexer entries carry a bf16 scale when they are fp8 or fp4
+        self.idx_scaled = w["cache_dtype"] == K.FP8_E4M3 or bool(w.get("idx_fp4", 0))
         nbytes = K.required_bytes(self.cfg)
         assert nbytes > 0
         self.arena = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
@@ -125,7 +127,7 @@ class GpuCase:
         n_chunks = d["idx_entry_bytes"] // 16
         code = np.concatenate([self.bytes_at(base + (c * CB + e % CB) * 16, 16, host) for c in range(n_chunks)])
         sc = np.zeros(1, np.uint16)
-        if self.vs == 1:
+        if self.idx_scaled:
             sc = self.bytes_at(base + d["idx_scale_offset"] + 2 * (e % CB), 2, host).copy().view(np.uint16)
         return code, sc
 
@@ -164,8 +166,8 @@ def compare_request_state(case, oracle, slot, layers=None, sample=None, rng=None
             rc, c_ref, s_ref = oracle.request_entry(l, slot, 3, e)
             c, s = case.idx_entry(l, slot, e, ids2, host)
             assert np.array_equal(c, c_ref), f"indexer entry {e} of layer {l} differs"
-            if case.vs == 1:
-                assert s[0] == s_ref[0]
+            if case.idx_scaled:
+                assert s[0] == s_ref[0], f"indexer entry {e} scale differs"
         if kind in (K.HCA, K.CSA_HCA):
             ts = range(len(ids1))
             if sample is not None and len(ids1) > sample:

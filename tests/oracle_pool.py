@@ -13,7 +13,7 @@ _ORACLES = {}
 
 
 def _oracle(cfg):
-    key = (cfg["name"], cfg["seed"])
+    key = (cfg["name"], cfg["seed"], cfg.get("idx_fp4", 0))
     if key not in _ORACLES:
         _ORACLES[key] = H.make_oracle(cfg, 1, 1, 1)
     return _ORACLES[key]

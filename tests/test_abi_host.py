@@ -52,7 +52,8 @@ def base_workload(**kw):
 
 @pytest.mark.parametrize("bad", [dict(m=3), dict(m=5, m_prime=128), dict(n_win=100), dict(n_win=64),
                                  dict(head_dim=96), dict(cache_dtype=7), dict(in_dtype=2), dict(max_batch=0),
-                                 dict(heads=1), dict(idx_dim=3), dict(layer_kinds=[9])])
+                                 dict(heads=1), dict(idx_dim=3), dict(layer_kinds=[9]),
+                                 dict(idx_fp4=1, idx_dim=16), dict(idx_fp4=2)])
 def test_invalid_configs_are_refused(bad):
     w = base_workload()
     wk = {k: v for k, v in bad.items() if k in w}
@@ -64,6 +65,14 @@ def test_invalid_configs_are_refused(bad):
     assert K.required_bytes(cfg) == 0
     with pytest.raises(K.KvpoolError):
         K.Pool(cfg)
+
+
+def test_fp4_indexer_layout():
+    w = base_workload(cache_dtype=K.BF16, in_dtype=K.BF16, heads=16, head_dim=128, idx_heads=4, idx_dim=64)
+    p = K.Pool(cfg_of(w, idx_fp4=1))
+    lo, d = p.layout(), p.layout(0)
+    assert lo["idx_entry_bytes"] == 128
+    assert d["idx_scale_offset"] == 32 * 128 and d["idx_block_bytes"] == 32 * 128 + 64
 
 
 @pytest.mark.parametrize("cache", [K.F32, K.BF16, K.FP8_E4M3])

@@ -111,7 +111,8 @@ def _spawn_pool():
     return mp.get_context("spawn").Pool(max(1, min(16, os.cpu_count() or 1)))
 
 
-def test_long_context_full_sampled():
+@pytest.mark.parametrize("idx_fp4", [0, 1])
+def test_long_context_full_sampled(idx_fp4):
     """8 requests x 1,048,576 tokens, fp8 cache, top_k 2048, in bench.py's
     pool configuration and prefill order (2048-token chunks, every request per
     call), then one decode step.  For one request the oracle recomputes, one
@@ -119,9 +120,10 @@ def test_long_context_full_sampled():
     compared bit for bit), all 8,192 HCA entries, the selected CSA entries and
     the window, and the attention output (fp8 tolerance); sampled CSA,
     indexer and HCA entries and the window are compared byte for byte with
-    the arena; block tables follow the smallest-free policy."""
+    the arena; block tables follow the smallest-free policy.  Indexer entries
+    in fp8 (the workload) or FP4."""
     from tests import oracle_pool as OP
-    w = W.LONG_CONTEXT
+    w = dict(W.LONG_CONTEXT, idx_fp4=idx_fp4)
     B, Lc, C, mp_, top_k = w["n_requests"], w["length"], w["chunk"], w["m_prime"], w["top_k"]
     extra = 8
     g = GpuCase(w, B, B * ((Lc + extra) // mp_ + 1), (Lc + extra) // mp_ + 2, B, top_k)

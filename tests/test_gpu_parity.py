@@ -50,6 +50,20 @@ def test_generator_device_matches_host():
         assert np.array_equal(got.view(host.dtype), host)
 
 
+def test_tiny_fp32_inputs_with_fp4_indexer():
+    """fp32 inputs and cache with FP4 indexer entries: the query is not exact
+    in f16, so the scores take the plain fp32 chain."""
+    w = dict(W.TINY, idx_fp4=1, seed=31)
+    o, g = make_pair(w, 2, 8, 4, 2, 64)
+    r = g.pool.alloc_request()
+    assert o.alloc_request() == (0, r)
+    append_both(o, g, [r], [0], [0], [300])
+    compare_request_state(g, o, r)
+    for step in range(3):
+        append_both(o, g, [r], [0], [300 + step], [1])
+        attend_both(o, g, 0, [r], [0], step, w["top_k"])
+
+
 def test_tiny_prefix_130_then_8_decode_steps():
     """Tiny workload: 1 layer, 1 request, prefix L=130 in one append (one
     sealed block, 32 CSA + 1 HCA, 2-token tail), then 8 x (append 1, attend)
@@ -70,12 +84,13 @@ def test_tiny_prefix_130_then_8_decode_steps():
         attend_both(o, g, 0, [r], [0], step, 64)
 
 
-@pytest.mark.parametrize("cache", [K.BF16, K.FP8_E4M3])
-def test_batched_ragged_appends_and_decode(cache):
+@pytest.mark.parametrize("cache,idx_fp4", [(K.BF16, 0), (K.FP8_E4M3, 0), (K.FP8_E4M3, 1), (K.BF16, 1)])
+def test_batched_ragged_appends_and_decode(cache, idx_fp4):
     """Decode-batch shapes (16 heads x 128, indexer 4 x 64) with ragged,
     unaligned multi-request appends (blocks sealed mid-call, a call spanning
-    three segments with a partial start and end), then decode steps."""
-    w = dict(W.DECODE_BATCH, cache_dtype=cache, seed=21)
+    three segments with a partial start and end), then decode steps; the
+    indexer entries in the cache dtype or in FP4."""
+    w = dict(W.DECODE_BATCH, cache_dtype=cache, seed=21, idx_fp4=idx_fp4)
     o, g = make_pair(w, 6, 64, 16, 6, 128)
     slots = [g.pool.alloc_request() for _ in range(5)]
     assert [o.alloc_request()[1] for _ in range(5)] == slots
