@@ -116,19 +116,27 @@ struct IdxChunk<KVPOOL_FP4_E2M1> {  // 32 e2m1 values, element 2j in the low nib
 // f16 or two bf16 values is exact in fp32 and the FMA rounds once, so every
 // step equals fmaf on the widened operands).  qh holds the query as f16 (fp8
 // keys, which convert exactly to f16) or bf16 (bf16 keys) pairs.
-__device__ __forceinline__ float fma_f16(uint16_t a, uint16_t b, float c) {
-  float d;
-  asm("fma.rn.f32.f16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
-  return d;
-}
-__device__ __forceinline__ float fma_bf16(uint16_t a, uint16_t b, float c) {
-  float d;
-  asm("fma.rn.f32.bf16 %0, %1, %2, %3;" : "=f"(d) : "h"(a), "h"(b), "f"(c));
-  return d;
-}
-
 template <int CACHE>
 struct IdxChunkFast;
+
+// acc = fma(hi(a), hi(b), fma(lo(a), lo(b), acc)): two chain steps on the
+// halves of two f16 (or bf16) pairs, low half first; the halves are taken
+// apart inside one asm block so no extraction instructions are emitted
+__device__ __forceinline__ float chain2_f16(uint32_t a, uint32_t b, float acc) {
+  asm("{.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.f16 %0, al, bl, %0;\n\tfma.rn.f32.f16 %0, ah, bh, %0;}"
+      : "+f"(acc)
+      : "r"(a), "r"(b));
+  return acc;
+}
+__device__ __forceinline__ float chain2_bf16(uint32_t a, uint32_t b, float acc) {
+  asm("{.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %0;\n\tfma.rn.f32.bf16 %0, ah, bh, %0;}"
+      : "+f"(acc)
+      : "r"(a), "r"(b));
+  return acc;
+}
+
 template <>
 struct IdxChunkFast<KVPOOL_FP8_E4M3> {  // 16 keys per chunk, q as 16 f16
   __device__ static float chain(const uint4& c, const uint32_t* qh, float acc) {
@@ -137,12 +145,8 @@ struct IdxChunkFast<KVPOOL_FP8_E4M3> {  // 16 keys per chunk, q as 16 f16
     const uint32_t q[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t a = e4m3x2_to_f16x2((uint16_t)(w[i] & 0xFFFFu));
-      const uint32_t b = e4m3x2_to_f16x2((uint16_t)(w[i] >> 16));
-      acc = fma_f16((uint16_t)(a & 0xFFFFu), (uint16_t)(q[2 * i] & 0xFFFFu), acc);
-      acc = fma_f16((uint16_t)(a >> 16), (uint16_t)(q[2 * i] >> 16), acc);
-      acc = fma_f16((uint16_t)(b & 0xFFFFu), (uint16_t)(q[2 * i + 1] & 0xFFFFu), acc);
-      acc = fma_f16((uint16_t)(b >> 16), (uint16_t)(q[2 * i + 1] >> 16), acc);
+      acc = chain2_f16(e4m3x2_to_f16x2((uint16_t)(w[i] & 0xFFFFu)), q[2 * i], acc);
+      acc = chain2_f16(e4m3x2_to_f16x2((uint16_t)(w[i] >> 16)), q[2 * i + 1], acc);
     }
     return acc;
   }
@@ -154,10 +158,7 @@ struct IdxChunkFast<KVPOOL_BF16> {  // 8 keys per chunk, q as 8 bf16
     const uint4 qa = *reinterpret_cast<const uint4*>(qh);
     const uint32_t q[4] = {qa.x, qa.y, qa.z, qa.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc = fma_bf16((uint16_t)(w[i] & 0xFFFFu), (uint16_t)(q[i] & 0xFFFFu), acc);
-      acc = fma_bf16((uint16_t)(w[i] >> 16), (uint16_t)(q[i] >> 16), acc);
-    }
+    for (int i = 0; i < 4; ++i) acc = chain2_bf16(w[i], q[i], acc);
     return acc;
   }
 };
@@ -170,11 +171,7 @@ struct IdxChunkFast<KVPOOL_FP4_E2M1> {  // 32 keys per chunk, q as 32 f16
       const uint4 qv = *reinterpret_cast<const uint4*>(qh + 4 * i);
       const uint32_t q[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const uint32_t h = e2m1x2_to_f16x2((uint8_t)(w[i] >> (8 * b)));
-        acc = fma_f16((uint16_t)(h & 0xFFFFu), (uint16_t)(q[b] & 0xFFFFu), acc);
-        acc = fma_f16((uint16_t)(h >> 16), (uint16_t)(q[b] >> 16), acc);
-      }
+      for (int b = 0; b < 4; ++b) acc = chain2_f16(e2m1x2_to_f16x2((uint8_t)(w[i] >> (8 * b))), q[b], acc);
     }
     return acc;
   }
