@@ -24,6 +24,8 @@ F32, BF16, FP8, FP4 = 0, 1, 2, 3  # FP4: indexer entries only
 SWA_ONLY, CSA, HCA, CSA_HCA = 0, 1, 2, 3
 OK, ERR_INVALID_ARG, ERR_OUT_OF_BLOCKS, ERR_OUT_OF_REQUESTS, ERR_BAD_REQUEST, ERR_NOT_SHAREABLE = 0, -1, -2, -3, -4, -5
 ERR_CAPACITY = -8
+ERR_BAD_IMAGE = -9
+IMAGE_WINDOW = 1
 
 _lock = threading.Lock()
 _lib = None
@@ -100,6 +102,14 @@ def lib():
         L.kvo_window_token.argtypes = [vp, C.c_int, i32, i64, vp, vp]
         L.kvo_request_scores.argtypes = [vp, C.c_int, i32, vp, vp]
         L.kvo_value_bytes.argtypes = [C.c_int]
+        L.kvo_fnv1a64.restype = C.c_uint64
+        L.kvo_fnv1a64.argtypes = [vp, i64]
+        L.kvo_fingerprint.restype = C.c_uint64
+        L.kvo_fingerprint.argtypes = [vp]
+        L.kvo_image_bytes.restype = i64
+        L.kvo_image_bytes.argtypes = [vp, i64, C.c_uint32]
+        L.kvo_export_prefix.argtypes = [vp, i32, i64, C.c_uint32, vp, i64]
+        L.kvo_import_prefix.argtypes = [vp, i32, vp, i64, vp, vp]
         _lib = L
     return _lib
 
@@ -168,6 +178,11 @@ def decode(dtype: int, code, scale: int, n: int) -> np.ndarray:
     return np.array([lib().kvo_decode(dtype, _p(code), _p(sc), i) for i in range(n)])
 
 
+def fnv1a64(data: bytes) -> int:
+    b = np.frombuffer(bytes(data), np.uint8).copy()
+    return int(lib().kvo_fnv1a64(_p(b) if b.size else None, b.size))
+
+
 def topk(scores, top_k: int) -> np.ndarray:
     s = _f32(scores)
     out = np.zeros(max(top_k, 1), np.int32)
@@ -234,6 +249,27 @@ class Oracle:
         wk = None if win_k is None else _f32(win_k)
         wv = None if win_v is None else _f32(win_v)
         return self.L.kvo_share_prefix(self.h, dst, src, n_tokens, _p(wk), _p(wv))
+
+    # prefix images -------------------------------------------------------
+    def fingerprint(self) -> int:
+        return int(self.L.kvo_fingerprint(self.h))
+
+    def image_bytes(self, n_tokens, flags=0) -> int:
+        return int(self.L.kvo_image_bytes(self.h, n_tokens, flags))
+
+    def export_prefix(self, r, n_tokens, flags=0, cap=None):
+        """(rc, image as uint8 array)"""
+        n = self.image_bytes(n_tokens, flags)
+        cap = max(n, 0) if cap is None else cap
+        img = np.zeros(max(cap, 1), np.uint8)
+        rc = self.L.kvo_export_prefix(self.h, r, n_tokens, flags, _p(img), cap)
+        return rc, img[:max(n, 0)]
+
+    def import_prefix(self, dst, image, win_k=None, win_v=None):
+        img = np.ascontiguousarray(image, np.uint8)
+        wk = None if win_k is None else _f32(win_k)
+        wv = None if win_v is None else _f32(win_v)
+        return self.L.kvo_import_prefix(self.h, dst, _p(img), img.size, _p(wk), _p(wv))
 
     def decode_attend(self, layer, req_ids, q, q_idx, top_k):
         req = np.ascontiguousarray(req_ids, dtype=np.int32)

@@ -206,6 +206,7 @@ struct kvo {
   block* blocks;
   int n_free_blocks;
   int block_hint; /* no free id below this */
+  uint64_t fingerprint; /* of the config, for prefix images */
   request* reqs;
 };
 
@@ -227,6 +228,61 @@ static void sec_free(layer_sec* s) {
   free(s->idx_code);
   free(s->idx_scale);
   free(s->hca_code);
+}
+
+/* FNV-1a, 64-bit (Fowler, Noll, Vo): h = offset basis; for each byte
+ * h = (h xor byte) * prime, modulo 2^64 */
+uint64_t kvo_fnv1a64(const uint8_t* bytes, int64_t n) {
+  uint64_t h = 0xcbf29ce484222325ull;
+  for (int64_t i = 0; i < n; ++i) {
+    h ^= bytes[i];
+    h *= 0x100000001b3ull;
+  }
+  return h;
+}
+
+typedef struct hasher {
+  uint64_t h;
+} hasher;
+
+static void hash_bytes(hasher* x, const uint8_t* b, int n) {
+  for (int i = 0; i < n; ++i) {
+    x->h ^= b[i];
+    x->h *= 0x100000001b3ull;
+  }
+}
+
+static void hash_i32(hasher* x, int32_t v) {
+  uint32_t u = (uint32_t)v;
+  uint8_t b[4] = {(uint8_t)u, (uint8_t)(u >> 8), (uint8_t)(u >> 16), (uint8_t)(u >> 24)};
+  hash_bytes(x, b, 4);
+}
+
+static void hash_f32s(hasher* x, const float* f, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) {
+    uint32_t u;
+    memcpy(&u, &f[i], 4);
+    hash_i32(x, (int32_t)u);
+  }
+}
+
+/* the canonical config record of prefix images (see kvoracle.h) */
+static uint64_t config_fingerprint(const kvo_config* c) {
+  hasher x = {0xcbf29ce484222325ull};
+  const int32_t f[11] = {c->m,       c->m_prime,  c->n_win,       c->heads,   c->head_dim, c->idx_heads,
+                         c->idx_dim, c->in_dtype, c->cache_dtype, c->idx_fp4, c->n_layers};
+  for (int i = 0; i < 11; ++i) hash_i32(&x, f[i]);
+  for (int l = 0; l < c->n_layers; ++l) {
+    const int k = c->layer_kinds[l];
+    hash_i32(&x, k);
+    if (k == KVO_CSA || k == KVO_CSA_HCA) {
+      hash_f32s(&x, c->gate_csa + (size_t)l * c->heads * c->m, (int64_t)c->heads * c->m);
+      hash_f32s(&x, c->gate_idx + (size_t)l * c->idx_heads * c->m, (int64_t)c->idx_heads * c->m);
+    }
+    if (k == KVO_HCA || k == KVO_CSA_HCA)
+      hash_f32s(&x, c->gate_hca + (size_t)l * c->heads * c->m_prime, (int64_t)c->heads * c->m_prime);
+  }
+  return x.h;
 }
 
 int kvo_create(const kvo_config* cfg, kvo_t** out) {
@@ -291,6 +347,7 @@ int kvo_create(const kvo_config* cfg, kvo_t** out) {
   o->n_free_blocks = c->max_blocks;
   o->block_hint = 0;
   o->reqs = (request*)calloc((size_t)c->max_requests, sizeof(request));
+  o->fingerprint = config_fingerprint(c);
   *out = o;
   return KVO_OK;
 }
@@ -826,6 +883,217 @@ int kvo_request_scores(const kvo_t* o, int l, int32_t r, const float* q_idx, flo
     const uint16_t* sc;
     locate_entry(o, l, q, 3, e, &c, &sc);
     out[e] = kvo_score(o, c, sc, q_idx);
+  }
+  return KVO_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* prefix images ([P3] s3, s3.1; [P4])                                   */
+/* ------------------------------------------------------------------ */
+
+uint64_t kvo_fingerprint(const kvo_t* o) { return o ? o->fingerprint : 0; }
+
+static int64_t round16(int64_t x) { return (x + 15) / 16 * 16; }
+static int idx_has_scale(const kvo_t* o) { return o->idx_dtype == KVO_FP8 || o->idx_dtype == KVO_FP4; }
+/* bytes of one K/V entry record: codes, then fp8 scales and zero padding */
+static int64_t entry_rec(const kvo_t* o) { return o->esz + (o->c.cache_dtype == KVO_FP8 ? 16 : 0); }
+static int64_t idx_part(const kvo_t* o) {
+  return (int64_t)o->CB * o->xsz + (idx_has_scale(o) ? round16(2 * (int64_t)o->CB) : 0);
+}
+/* bytes of one block's parts summed over the layers */
+static int64_t block_rec(const kvo_t* o) {
+  int64_t b = 0;
+  for (int l = 0; l < o->c.n_layers; ++l) {
+    if (has_csa(o, l)) b += o->CB * entry_rec(o) + idx_part(o);
+    if (has_hca(o, l)) b += entry_rec(o);
+  }
+  return b;
+}
+
+static void put_u32(uint8_t* p, uint32_t v) {
+  for (int i = 0; i < 4; ++i) p[i] = (uint8_t)(v >> (8 * i));
+}
+static void put_u64(uint8_t* p, uint64_t v) {
+  for (int i = 0; i < 8; ++i) p[i] = (uint8_t)(v >> (8 * i));
+}
+static uint32_t get_u32(const uint8_t* p) {
+  uint32_t v = 0;
+  for (int i = 0; i < 4; ++i) v |= (uint32_t)p[i] << (8 * i);
+  return v;
+}
+static uint64_t get_u64(const uint8_t* p) {
+  uint64_t v = 0;
+  for (int i = 0; i < 8; ++i) v |= (uint64_t)p[i] << (8 * i);
+  return v;
+}
+
+static const uint32_t kImageMagic = 0x4950564Bu; /* "KVPI" */
+
+/* the chunk-by-chunk indexer layout needs whole 16-byte chunks per key */
+static int image_ok(const kvo_t* o) { return !any_csa(o) || o->xsz % 16 == 0; }
+
+int64_t kvo_image_bytes(const kvo_t* o, int64_t n_tokens, uint32_t flags) {
+  if (!o || !image_ok(o) || n_tokens <= 0 || n_tokens % o->c.m_prime != 0) return -1;
+  const int64_t nb = n_tokens / o->c.m_prime;
+  const int64_t w = (flags & KVO_IMAGE_WINDOW) ? (n_tokens < o->c.n_win ? n_tokens : o->c.n_win) : 0;
+  return 64 + nb * block_rec(o) + w * entry_rec(o) * o->c.n_layers;
+}
+
+/* one K/V entry record from codes + scales */
+static void entry_to_rec(const kvo_t* o, const uint8_t* code, const uint16_t* scale, uint8_t* rec) {
+  memcpy(rec, code, (size_t)o->esz);
+  if (o->c.cache_dtype == KVO_FP8) {
+    uint8_t* t = rec + o->esz;
+    memset(t, 0, 16);
+    t[0] = (uint8_t)scale[0];
+    t[1] = (uint8_t)(scale[0] >> 8);
+    t[2] = (uint8_t)scale[1];
+    t[3] = (uint8_t)(scale[1] >> 8);
+  }
+}
+
+static void rec_to_entry(const kvo_t* o, const uint8_t* rec, uint8_t* code, uint16_t* scale) {
+  memcpy(code, rec, (size_t)o->esz);
+  if (o->c.cache_dtype == KVO_FP8) {
+    const uint8_t* t = rec + o->esz;
+    scale[0] = (uint16_t)(t[0] | (t[1] << 8));
+    scale[1] = (uint16_t)(t[2] | (t[3] << 8));
+  } else {
+    scale[0] = scale[1] = 0;
+  }
+}
+
+/* a block's indexer part: keys chunk by chunk, then the scales */
+static void idx_to_part(const kvo_t* o, const layer_sec* s, uint8_t* part) {
+  memset(part, 0, (size_t)idx_part(o));
+  for (int e = 0; e < o->CB; ++e)
+    for (int j = 0; j < o->xsz; ++j)
+      part[((int64_t)(j / 16) * o->CB + e) * 16 + j % 16] = s->idx_code[(size_t)e * o->xsz + j];
+  if (idx_has_scale(o)) {
+    uint8_t* t = part + (int64_t)o->CB * o->xsz;
+    for (int e = 0; e < o->CB; ++e) {
+      t[2 * e] = (uint8_t)s->idx_scale[e];
+      t[2 * e + 1] = (uint8_t)(s->idx_scale[e] >> 8);
+    }
+  }
+}
+
+static void part_to_idx(const kvo_t* o, const uint8_t* part, layer_sec* s) {
+  for (int e = 0; e < o->CB; ++e)
+    for (int j = 0; j < o->xsz; ++j)
+      s->idx_code[(size_t)e * o->xsz + j] = part[((int64_t)(j / 16) * o->CB + e) * 16 + j % 16];
+  const uint8_t* t = part + (int64_t)o->CB * o->xsz;
+  for (int e = 0; e < o->CB; ++e) s->idx_scale[e] = idx_has_scale(o) ? (uint16_t)(t[2 * e] | (t[2 * e + 1] << 8)) : 0;
+}
+
+int kvo_export_prefix(const kvo_t* o, int32_t req, int64_t n_tokens, uint32_t flags, uint8_t* image, int64_t cap) {
+  if (!o || !image || (flags & ~KVO_IMAGE_WINDOW) || !image_ok(o)) return KVO_ERR_INVALID_ARG;
+  if (!req_ok(o, req)) return KVO_ERR_BAD_REQUEST;
+  const request* q = &o->reqs[req];
+  if (n_tokens <= 0 || n_tokens % o->c.m_prime != 0 || n_tokens / o->c.m_prime > q->n_sealed)
+    return KVO_ERR_NOT_SHAREABLE;
+  if ((flags & KVO_IMAGE_WINDOW) && n_tokens != q->L) return KVO_ERR_NOT_SHAREABLE;
+  const int64_t total = kvo_image_bytes(o, n_tokens, flags);
+  if (cap < total) return KVO_ERR_INVALID_ARG;
+  const int64_t nb = n_tokens / o->c.m_prime, E = entry_rec(o), X = idx_part(o);
+  const int64_t w = (flags & KVO_IMAGE_WINDOW) ? (n_tokens < o->c.n_win ? n_tokens : o->c.n_win) : 0;
+
+  memset(image, 0, 64);
+  put_u32(image, kImageMagic);
+  put_u32(image + 4, 1);
+  put_u64(image + 8, o->fingerprint);
+  put_u64(image + 16, (uint64_t)n_tokens);
+  put_u32(image + 24, (uint32_t)nb);
+  put_u32(image + 28, (uint32_t)w);
+  put_u64(image + 32, (uint64_t)(nb * block_rec(o)));
+  put_u64(image + 40, (uint64_t)(w * E * o->c.n_layers));
+  put_u64(image + 48, (uint64_t)total);
+
+  uint8_t* p = image + 64;
+  for (int l = 0; l < o->c.n_layers; ++l) {
+    if (has_csa(o, l)) {
+      for (int64_t b = 0; b < nb; ++b) {
+        const layer_sec* s = &o->blocks[q->table[b]].layers[l];
+        for (int e = 0; e < o->CB; ++e, p += E) entry_to_rec(o, s->csa_code + (size_t)e * o->esz, s->csa_scale + 2 * e, p);
+      }
+      for (int64_t b = 0; b < nb; ++b, p += X) idx_to_part(o, &o->blocks[q->table[b]].layers[l], p);
+    }
+    if (has_hca(o, l))
+      for (int64_t b = 0; b < nb; ++b, p += E) {
+        const layer_sec* s = &o->blocks[q->table[b]].layers[l];
+        entry_to_rec(o, s->hca_code, s->hca_scale, p);
+      }
+  }
+  for (int l = 0; l < o->c.n_layers && w > 0; ++l) {
+    const req_layer* rl = &q->layers[l];
+    for (int64_t pos = n_tokens - w; pos < n_tokens; ++pos, p += E) {
+      const int64_t slot = pos % o->c.n_win;
+      entry_to_rec(o, rl->win_code + (size_t)slot * o->esz, rl->win_scale + 2 * slot, p);
+    }
+  }
+  return KVO_OK;
+}
+
+int kvo_import_prefix(kvo_t* o, int32_t dst, const uint8_t* image, int64_t bytes, const float* win_k,
+                      const float* win_v) {
+  if (!o || !image || !image_ok(o)) return KVO_ERR_INVALID_ARG;
+  if (!req_ok(o, dst)) return KVO_ERR_BAD_REQUEST;
+  if (bytes < 64 || get_u32(image) != kImageMagic || get_u32(image + 4) != 1 || get_u64(image + 8) != o->fingerprint)
+    return KVO_ERR_BAD_IMAGE;
+  const int64_t n_tokens = (int64_t)get_u64(image + 16);
+  const int64_t nb = (int64_t)get_u32(image + 24), w = (int64_t)get_u32(image + 28);
+  const uint32_t flags = w > 0 ? KVO_IMAGE_WINDOW : 0;
+  const int64_t total = kvo_image_bytes(o, n_tokens, flags);
+  const int64_t w_full = n_tokens < o->c.n_win ? n_tokens : o->c.n_win;
+  if (total < 0 || nb != n_tokens / o->c.m_prime || (w != 0 && w != w_full) || bytes < total ||
+      get_u64(image + 48) != (uint64_t)total || get_u64(image + 32) != (uint64_t)(nb * block_rec(o)) ||
+      get_u64(image + 40) != (uint64_t)(w * entry_rec(o) * o->c.n_layers))
+    return KVO_ERR_BAD_IMAGE;
+  request* q = &o->reqs[dst];
+  if (q->L != 0) return KVO_ERR_NOT_SHAREABLE;
+  if (w == 0 && (!win_k || !win_v)) return KVO_ERR_INVALID_ARG;
+  if (nb > o->c.max_blocks_per_request) return KVO_ERR_CAPACITY;
+  if (nb > o->n_free_blocks) return KVO_ERR_OUT_OF_BLOCKS;
+
+  const int64_t E = entry_rec(o), X = idx_part(o);
+  for (int64_t b = 0; b < nb; ++b) q->table[b] = block_take(o);
+  q->n_sealed = (int)nb;
+  q->L = n_tokens;
+  const uint8_t* p = image + 64;
+  for (int l = 0; l < o->c.n_layers; ++l) {
+    req_layer* rl = &q->layers[l];
+    rl->tail_len = 0;
+    rl->tail_idx_len = 0;
+    if (has_csa(o, l)) {
+      for (int64_t b = 0; b < nb; ++b) {
+        layer_sec* s = &o->blocks[q->table[b]].layers[l];
+        for (int e = 0; e < o->CB; ++e, p += E) rec_to_entry(o, p, s->csa_code + (size_t)e * o->esz, s->csa_scale + 2 * e);
+      }
+      for (int64_t b = 0; b < nb; ++b, p += X) part_to_idx(o, p, &o->blocks[q->table[b]].layers[l]);
+    }
+    if (has_hca(o, l))
+      for (int64_t b = 0; b < nb; ++b, p += E) {
+        layer_sec* s = &o->blocks[q->table[b]].layers[l];
+        rec_to_entry(o, p, s->hca_code, s->hca_scale);
+      }
+  }
+  if (w > 0) {
+    for (int l = 0; l < o->c.n_layers; ++l) {
+      req_layer* rl = &q->layers[l];
+      for (int64_t pos = n_tokens - w; pos < n_tokens; ++pos, p += E) {
+        const int64_t slot = pos % o->c.n_win;
+        rec_to_entry(o, p, rl->win_code + (size_t)slot * o->esz, rl->win_scale + 2 * slot);
+      }
+    }
+  } else { /* Zero SWA: the caller's recomputed window goes through the cache encoding */
+    float* kv = (float*)malloc(sizeof(float) * 2 * (size_t)o->HD);
+    for (int l = 0; l < o->c.n_layers; ++l)
+      for (int64_t t = 0; t < w_full; ++t) {
+        memcpy(kv, win_k + ((size_t)l * w_full + t) * o->HD, sizeof(float) * (size_t)o->HD);
+        memcpy(kv + o->HD, win_v + ((size_t)l * w_full + t) * o->HD, sizeof(float) * (size_t)o->HD);
+        window_put(o, &q->layers[l], n_tokens - w_full + t, kv);
+      }
+    free(kv);
   }
   return KVO_OK;
 }

@@ -153,6 +153,52 @@ int kvo_request_entry(const kvo_t* o, int layer, int32_t req, int kind, int64_t 
 int kvo_window_token(const kvo_t* o, int layer, int32_t req, int64_t pos, uint8_t* code, uint16_t* scale);
 /* all indexer scores of a request: out[n_csa] */
 int kvo_request_scores(const kvo_t* o, int layer, int32_t req, const float* q_idx, float* out);
+/* ---- prefix images ([P3] s3 disk-resident KV cache: the compressed block
+ * cache serialized and brought back by an async copy, skipping the prefill;
+ * [P3] s3.1 and [P4] SWA policies: Full / Periodic checkpoint / Zero) ----
+ * An image holds the first n_tokens / m' sealed blocks of a request (n_tokens
+ * a multiple of m'), optionally followed by the SWA window at n_tokens (a
+ * checkpoint, taken when the request's length is n_tokens).  Byte layout,
+ * little-endian:
+ *   header (64 B): u32 magic "KVPI", u32 version 1, u64 fingerprint of the
+ *     pool's config, i64 n_tokens, i32 n_blocks, i32 w = window tokens in
+ *     the image (0 without a window), u64 bytes of the block section, u64
+ *     bytes of the window section, u64 total bytes, u64 zero;
+ *   block section: for each layer in order, for each part the layer has
+ *     (CSA entries, indexer keys, HCA entry), that part of the n_blocks
+ *     blocks in table order;
+ *   window section: for each layer, the w window tokens at positions
+ *     n_tokens - w .. n_tokens - 1.
+ *   A K/V entry (CSA, HCA, window token) is its codes (K half, V half), then
+ *   for fp8 the bf16 K and V scales and 12 zero bytes.  A block's indexer
+ *   part is its CB = m'/m keys 16-byte chunk by chunk (byte j of key e at
+ *   ((j / 16) * CB + e) * 16 + j % 16), then for fp8 / FP4 keys the CB bf16
+ *   scales, zero-padded to a multiple of 16 bytes.  Images need each
+ *   indexer key to be whole 16-byte chunks (when a layer has CSA); other
+ *   configs are refused (INVALID_ARG, image bytes -1).
+ * The fingerprint is FNV-1a (64-bit) over the little-endian int32 fields m,
+ * m', n_win, heads, head_dim, idx_heads, idx_dim, in_dtype, cache_dtype,
+ * idx_fp4, n_layers, then per layer its kind followed by the fp32 bits of
+ * its gate logits (CSA then indexer if the layer has CSA; HCA if it has HCA).
+ */
+#define KVO_IMAGE_WINDOW 1u
+#define KVO_ERR_BAD_IMAGE (-9)
+uint64_t kvo_fnv1a64(const uint8_t* bytes, int64_t n);
+uint64_t kvo_fingerprint(const kvo_t* o);
+/* bytes of the image of an n_tokens prefix (-1 if n_tokens is not a positive multiple of m') */
+int64_t kvo_image_bytes(const kvo_t* o, int64_t n_tokens, uint32_t flags);
+/* Write the image; with KVO_IMAGE_WINDOW, n_tokens must be the request's length.
+ * Errors: BAD_REQUEST, NOT_SHAREABLE (not whole sealed blocks, or the window
+ * asked for at another length), INVALID_ARG (capacity too small). */
+int kvo_export_prefix(const kvo_t* o, int32_t req, int64_t n_tokens, uint32_t flags, uint8_t* image, int64_t cap);
+/* Restore an image into the fresh request dst: new block ids (smallest free, in
+ * image order), length n_tokens, empty tails; the window from the image, else
+ * ([P4] Zero SWA) from win_k / win_v [n_layers][w][heads][head_dim] fp32
+ * values of the recomputed tokens (w = min(n_tokens, n_win)), which must then
+ * be given.  Errors: BAD_IMAGE (magic, version, fingerprint, sizes),
+ * NOT_SHAREABLE (dst not fresh), CAPACITY, OUT_OF_BLOCKS, INVALID_ARG. */
+int kvo_import_prefix(kvo_t* o, int32_t dst, const uint8_t* image, int64_t bytes, const float* win_k,
+                      const float* win_v);
 int kvo_value_bytes(int dtype);
 /* bytes of n encoded values (FP4: two per byte) */
 int64_t kvo_code_bytes(int dtype, int64_t n);
