@@ -271,6 +271,117 @@ def traffic_record(kernel, source):
 
 
 # ---------------------------------------------------------------------------
+# prefix images (the host-memory prefix store): export and restore bandwidth
+# ---------------------------------------------------------------------------
+def run_prefix_image(args):
+    """Export (HBM -> page-locked host memory) and restore (host -> HBM) of one
+    long-context request's sealed blocks and window as a prefix image, each
+    call between CUDA events on the launching stream.  The copy engines' rate
+    for the same bytes over the same link (pinned cudaMemcpyAsync) is measured
+    beside them as the roofline denominator; the image is far larger than L2."""
+    import torch
+    from heterogeneous_compressed_kv_gb300 import gen
+    from heterogeneous_compressed_kv_gb300 import kvpool as K
+
+    w = workload("long_context", args.idx_fp4)
+    L = args.context or w["length"]
+    mp_ = w["m_prime"]
+    L = L // mp_ * mp_
+    K_, W_ = args.steps, args.warmup
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    g = gates(w)
+    nb = L // mp_
+    cfg = K.PoolConfig(m=w["m"], m_prime=mp_, n_win=w["n_win"], heads=w["heads"], head_dim=w["head_dim"],
+                       idx_heads=w["idx_heads"], idx_dim=w["idx_dim"], in_dtype=w["in_dtype"],
+                       cache_dtype=w["cache_dtype"], layer_kinds=w["layer_kinds"], max_requests=2,
+                       max_blocks=2 * nb + 2, max_blocks_per_request=nb + 1, max_batch=2, max_top_k=w["top_k"],
+                       gate_csa=g[0], gate_hca=g[1], gate_idx=g[2], idx_fp4=w["idx_fp4"])
+    arena = torch.empty(K.required_bytes(cfg), dtype=torch.uint8, device=dev)
+    pool = K.Pool(cfg, arena, stream)
+    a = pool.alloc_request()
+    HD, XD = w["heads"] * w["head_dim"], w["idx_heads"] * w["idx_dim"]
+    tdt = torch.float32 if w["in_dtype"] == 0 else torch.bfloat16
+    gdt = gen.OUT_F32 if w["in_dtype"] == 0 else gen.OUT_BF16
+    chunk = w["chunk"]
+    kb = torch.empty((1, chunk, HD), dtype=tdt, device=dev)
+    vb, xb = torch.empty_like(kb), torch.empty((1, chunk, XD), dtype=tdt, device=dev)
+    pool.profile_enable(True, kinds=[K.KERNEL_APPEND])
+    for p0 in range(0, L, chunk):  # the prefill a restore replaces (its append kernels timed)
+        c = min(chunk, L - p0)
+        gen.fill_device(kb.data_ptr(), gdt, w["seed"], gen.token_runs(gen.K, 0, [0], [p0], [c], HD), sp)
+        gen.fill_device(vb.data_ptr(), gdt, w["seed"], gen.token_runs(gen.V, 0, [0], [p0], [c], HD), sp)
+        gen.fill_device(xb.data_ptr(), gdt, w["seed"], gen.token_runs(gen.IDXK, 0, [0], [p0], [c], XD), sp)
+        pool.append([a], [c], kb, vb, xb, stream=sp)
+    torch.cuda.synchronize()
+    prefill_ms, prefill_launches, _ = pool.profile_read(K.KERNEL_APPEND)
+    del kb, vb, xb
+    pool.check_device(sp)
+
+    n_bytes = pool.image_bytes(L, K.IMAGE_WINDOW)
+    img = torch.empty(n_bytes, dtype=torch.uint8, pin_memory=True)
+    dbuf = torch.empty(n_bytes, dtype=torch.uint8, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    t_exp, t_imp, t_h2d, t_d2h = [], [], [], []
+    clocks = Clocks(0)
+    pool.profile_enable(True, kinds=[K.KERNEL_IMAGE])
+    for it in range(W_ + K_):
+        if it == W_:
+            clocks.start()
+        ev[0].record(stream)
+        pool.export_prefix(a, L, K.IMAGE_WINDOW, out=img, stream=sp)
+        ev[1].record(stream)
+        torch.cuda.synchronize()  # the host reads the header when restoring
+        b = pool.alloc_request()
+        ev[2].record(stream)
+        pool.import_prefix(b, img, stream=sp)
+        ev[3].record(stream)
+        torch.cuda.synchronize()
+        if it >= W_:
+            t_exp.append(ev[0].elapsed_time(ev[1]))
+            t_imp.append(ev[2].elapsed_time(ev[3]))
+        info_a, info_b = pool.request_info(a)[0], pool.request_info(b)[0]
+        assert info_a == info_b, (info_a, info_b)
+        pool.free_request(b)
+    clk = clocks.stop()
+    img_ms, img_launches, _ = pool.profile_read(K.KERNEL_IMAGE)
+    pool.profile_enable(False)
+    pool.check_device(sp)
+    for it in range(W_ + K_):  # the copy engines on the same bytes and link
+        ev[0].record(stream)
+        dbuf.copy_(img, non_blocking=True)
+        ev[1].record(stream)
+        img.copy_(dbuf, non_blocking=True)
+        ev[2].record(stream)
+        torch.cuda.synchronize()
+        if it >= W_:
+            t_h2d.append(ev[0].elapsed_time(ev[1]))
+            t_d2h.append(ev[1].elapsed_time(ev[2]))
+
+    med = lambda x: float(sorted(x)[len(x) // 2])
+    gbs = lambda ms: n_bytes / (ms / 1e3) / 1e9
+    imp, exp_, h2d, d2h = med(t_imp), med(t_exp), med(t_h2d), med(t_d2h)
+    line = dict(metric="prefix image restore bandwidth (page-locked host -> HBM)", value=gbs(imp), unit="GB/s",
+                n_gpus=1, steps=K_, warmup=W_, ms_per_step=imp, higher_is_better=True, scaling="none",
+                vs_baseline=None, dtype="u8", data="synthetic (seeded counter generator; no dataset)",
+                config=dict(workload=f"long_context prefix image: 1 request x {L:,} tokens, "
+                                     f"{'FP4' if w['idx_fp4'] else 'fp8'} indexer keys, with the SWA window",
+                            image_bytes=n_bytes, blocks=nb,
+                            l2="image larger than L2"),
+                roofline=dict(kernel="image_copy", bound="host link", achieved=gbs(imp), peak=gbs(h2d), unit="GB/s",
+                              frac=h2d / imp, traffic=None,
+                              peak_source="copy engines: pinned host -> device cudaMemcpyAsync of the same bytes, "
+                                          "measured in this run"),
+                export=dict(ms=exp_, gbs=gbs(exp_), copy_engine_gbs=gbs(d2h), frac=d2h / exp_),
+                prefill=dict(ms=prefill_ms, launches=prefill_launches,
+                             note="append kernels of the same tokens (the work a restore skips; no model forward)"),
+                kernel_ms_per_call=img_ms / max(1, 2 * (W_ + K_)), gpu_launches=img_launches, clocks=clk)
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
 def main():
@@ -286,7 +397,12 @@ def main():
     ap.add_argument("--context", type=int, default=0, help="override the long-context length (profiling cases)")
     ap.add_argument("--timeline", type=int, default=0, help="print the launch timeline of this many extra steps")
     ap.add_argument("--idx-fp4", action="store_true", help="indexer entries in FP4 (e2m1 + one bf16 scale)")
+    ap.add_argument("--prefix-image", action="store_true",
+                    help="time prefix image export / restore of one long-context request instead of decode steps")
     args = ap.parse_args()
+    if args.prefix_image:
+        run_prefix_image(args)
+        return
     if args.impl == "reference":
         run_reference(args)
         return

@@ -352,7 +352,8 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
 }
 
 // share_prefix: blockIdx.x = window token, blockIdx.y = slice, blockIdx.z = layer;
-// the CTA (0, 0, 0) also copies the shared block ids into dst's table row.
+// the CTA (0, 0, 0) also copies the shared block ids into dst's table row
+// (src >= 0; a restored prefix image writes its own ids).
 template <int IN, int CACHE>
 __global__ void __launch_bounds__(512) share_kernel(const __grid_constant__ ShareParams P) {
   pdl_start();
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(512) share_kernel(const __grid_constant__ Shar
   const int v0 = (slice * blockDim.x + threadIdx.x) * kVpt;
   const int half = v0 >= HD ? 1 : 0;
   const int hv = v0 - half * HD;
-  if (blockIdx.x == 0 && slice == 0 && layer == 0) {
+  if (P.src >= 0 && blockIdx.x == 0 && slice == 0 && layer == 0) {
     int32_t* table = reinterpret_cast<int32_t*>(pd.arena + pd.table);
     for (int b = threadIdx.x; b < P.n_blocks; b += blockDim.x)
       table[(int64_t)P.dst * pd.max_bpr + b] = table[(int64_t)P.src * pd.max_bpr + b];

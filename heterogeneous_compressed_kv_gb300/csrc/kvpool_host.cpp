@@ -205,6 +205,51 @@ void softmax_rows(const float* g, int rows, int n, std::vector<float>* out) {
   }
 }
 
+// FNV-1a 64 (Fowler, Noll, Vo) over the prefix-image config record:
+// little-endian int32 m, m', n_win, heads, head_dim, idx_heads, idx_dim,
+// in_dtype, cache_dtype, idx_fp4, n_layers, then per layer its kind and the
+// fp32 bits of the gate logits it uses (CSA then indexer; HCA).  A gate array
+// that is NULL (a pool without device memory) adds nothing.
+struct Fnv1a {
+  uint64_t h = 0xcbf29ce484222325ull;
+  void u32(uint32_t v) {
+    for (int i = 0; i < 4; ++i) {
+      h ^= (v >> (8 * i)) & 0xFFu;
+      h *= 0x100000001b3ull;
+    }
+  }
+  void floats(const float* f, int64_t n) {
+    if (!f) return;
+    for (int64_t i = 0; i < n; ++i) {
+      uint32_t u;
+      std::memcpy(&u, f + i, 4);
+      u32(u);
+    }
+  }
+};
+
+uint64_t config_fingerprint(const kvpool_config* c) {
+  Fnv1a x;
+  const int32_t f[11] = {c->m,       c->m_prime,  c->n_win,       c->heads,   c->head_dim, c->idx_heads,
+                         c->idx_dim, c->in_dtype, c->cache_dtype, c->idx_fp4, c->n_layers};
+  for (int32_t v : f) x.u32((uint32_t)v);
+  for (int l = 0; l < c->n_layers; ++l) {
+    const int k = c->layer_kinds[l];
+    x.u32((uint32_t)k);
+    if (kind_has_csa(k)) {
+      x.floats(c->gate_csa ? c->gate_csa + (size_t)l * c->heads * c->m : nullptr, (int64_t)c->heads * c->m);
+      x.floats(c->gate_idx ? c->gate_idx + (size_t)l * c->idx_heads * c->m : nullptr, (int64_t)c->idx_heads * c->m);
+    }
+    if (kind_has_hca(k))
+      x.floats(c->gate_hca ? c->gate_hca + (size_t)l * c->heads * c->m_prime : nullptr,
+               (int64_t)c->heads * c->m_prime);
+  }
+  return x.h;
+}
+
+constexpr uint32_t kImageMagic = 0x4950564Bu;  // "KVPI"
+constexpr int64_t kImageHeader = 64;
+
 struct Request {
   bool active = false;
   int64_t length = 0;
@@ -224,6 +269,7 @@ struct kvpool {
   kvpool_config cfg{};
   std::vector<int32_t> kinds;
   uint32_t flags = 0;
+  uint64_t fingerprint = 0;  // of the config, for prefix images
   Layout lay{};
   uint8_t* arena = nullptr;
   std::vector<int32_t> refcount;
@@ -332,6 +378,7 @@ int kvpool_create(const kvpool_config* cfg, void* d_arena, size_t arena_bytes, v
   p->cfg = *cfg;
   p->kinds.assign(cfg->layer_kinds, cfg->layer_kinds + cfg->n_layers);
   p->cfg.layer_kinds = p->kinds.data();
+  p->fingerprint = config_fingerprint(&p->cfg);
   p->cfg.gate_csa = p->cfg.gate_hca = p->cfg.gate_idx = nullptr;
   p->flags = cfg->flags;
   p->lay = L;
@@ -453,6 +500,262 @@ int kvpool_share_prefix(kvpool_t* p, int32_t dst, int32_t src, int64_t n_tokens,
   }
   d.table.assign(s.table.begin(), s.table.begin() + nb);
   for (int32_t b : d.table) p->refcount[b] += 1;
+  d.length = n_tokens;
+  return KVPOOL_OK;
+}
+
+}  // extern "C"
+
+// ---- prefix images ----------------------------------------------------------
+namespace {
+
+bool image_layout_ok(const kvpool_t* p) {
+  for (int k : p->kinds)
+    if (kind_has_csa(k) && p->lay.pd.idx_entry_bytes % 16 != 0) return false;
+  return true;
+}
+
+int64_t image_window_tokens(const kvpool_t* p, int64_t n_tokens, uint32_t flags) {
+  return (flags & KVPOOL_IMAGE_WINDOW) ? std::min<int64_t>(n_tokens, p->cfg.n_win) : 0;
+}
+
+// bytes of one block's parts, summed over the layers
+int64_t image_block_bytes(const kvpool_t* p) {
+  int64_t b = 0;
+  for (int l = 0; l < p->cfg.n_layers; ++l) {
+    const LayerDesc& d = p->lay.layers[l];
+    if (d.has_csa) b += d.csa_stride + d.idx_stride;
+    if (d.has_hca) b += d.hca_stride;
+  }
+  return b;
+}
+
+void put_le(uint8_t* dst, uint64_t v, int n) {
+  for (int i = 0; i < n; ++i) dst[i] = (uint8_t)(v >> (8 * i));
+}
+uint64_t get_le(const uint8_t* src, int n) {
+  uint64_t v = 0;
+  for (int i = 0; i < n; ++i) v |= (uint64_t)src[i] << (8 * i);
+  return v;
+}
+
+// The copies of an image: per layer and part, one segment per run of
+// adjacent block ids; then the window ring pieces.  Offsets are the image's.
+void image_segments(const kvpool_t* p, const std::vector<int32_t>& ids, int32_t slot, int64_t n_tokens, int64_t w,
+                    std::vector<ImageSeg>* segs) {
+  const int64_t nb = (int64_t)ids.size();
+  const PoolDesc& pd = p->lay.pd;
+  int64_t img = kImageHeader;
+  auto add_part = [&](int64_t pool, int64_t stride, int32_t mask_valid) {
+    for (int64_t b = 0; b < nb;) {
+      int64_t e = b + 1;
+      while (e < nb && ids[e] == ids[e - 1] + 1) ++e;
+      ImageSeg g{};
+      g.dev = pool + (int64_t)ids[b] * stride;
+      g.img = img + b * stride;
+      g.bytes = (e - b) * stride;
+      g.mask_row = mask_valid > 0 ? (int32_t)stride : 0;
+      g.mask_valid = mask_valid;
+      segs->push_back(g);
+      b = e;
+    }
+    img += nb * stride;
+  };
+  const bool idx_scaled = pd.idx_dtype == KVPOOL_FP8_E4M3 || pd.idx_dtype == KVPOOL_FP4_E2M1;
+  for (int l = 0; l < p->cfg.n_layers; ++l) {
+    const LayerDesc& d = p->lay.layers[l];
+    if (d.has_csa) {
+      add_part(d.csa_pool, d.csa_stride, 0);
+      const int64_t valid = d.idx_scale_off + 2LL * pd.csa_per_block;
+      add_part(d.idx_pool, d.idx_stride, idx_scaled && valid < d.idx_stride ? (int32_t)valid : 0);
+    }
+    if (d.has_hca) add_part(d.hca_pool, d.hca_stride, 0);
+  }
+  for (int l = 0; l < p->cfg.n_layers && w > 0; ++l) {
+    const LayerDesc& d = p->lay.layers[l];
+    const int64_t ring = d.ring + (int64_t)slot * d.ring_req_bytes;
+    const int64_t s0 = (n_tokens - w) % pd.n_win;
+    const int64_t first = std::min<int64_t>(w, pd.n_win - s0);
+    segs->push_back(ImageSeg{ring + s0 * pd.entry_bytes, img, first * pd.entry_bytes, 0, 0});
+    if (w > first) segs->push_back(ImageSeg{ring, img + first * pd.entry_bytes, (w - first) * pd.entry_bytes, 0, 0});
+    img += w * pd.entry_bytes;
+  }
+}
+
+// Launch the copies in batches of kMaxImageSegs segments and kMaxImageRuns
+// table runs.
+int launch_image_copies(kvpool_t* p, uint8_t* d_image, bool to_image, int32_t dst, const std::vector<ImageSeg>& segs,
+                        const std::vector<ImageRun>& runs, int64_t bytes, void* stream) {
+  const size_t n_launch = std::max((segs.size() + kMaxImageSegs - 1) / kMaxImageSegs,
+                                   (runs.size() + kMaxImageRuns - 1) / kMaxImageRuns);
+  for (size_t i = 0; i < n_launch; ++i) {
+    ImageParams ip{};
+    ip.pool = p->lay.pd;
+    ip.image = d_image;
+    ip.to_image = to_image ? 1 : 0;
+    ip.dst = dst;
+    const size_t s0 = i * kMaxImageSegs, s1 = std::min(segs.size(), s0 + kMaxImageSegs);
+    ip.n_segs = s1 > s0 ? (int32_t)(s1 - s0) : 0;
+    int64_t pieces = 0;
+    for (int32_t k = 0; k < ip.n_segs; ++k) {
+      ip.segs[k] = segs[s0 + k];
+      ip.piece_base[k] = pieces;
+      pieces += (ip.segs[k].bytes + kImagePieceBytes - 1) / kImagePieceBytes;
+    }
+    ip.piece_base[ip.n_segs] = pieces;
+    ip.n_pieces = pieces;
+    const size_t r0 = i * kMaxImageRuns, r1 = std::min(runs.size(), r0 + kMaxImageRuns);
+    ip.n_runs = r1 > r0 ? (int32_t)(r1 - r0) : 0;
+    for (int32_t k = 0; k < ip.n_runs; ++k) ip.runs[k] = runs[r0 + k];
+    const int rc = p->launch(KVPOOL_KERNEL_IMAGE, i == 0 ? 2 * bytes : 0, stream,
+                             [&](int* nk) { return launch_image(ip, stream, nk); });
+    if (rc != 0) return rc;
+  }
+  return 0;
+}
+
+// Device alias of a page-locked, mapped host buffer, or nullptr (pageable
+// memory included, even where the GPU could reach it through the host's page
+// tables).
+uint8_t* host_alias(const void* h) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, h) != cudaSuccess) {
+    cudaGetLastError();  // clear the (non-sticky) error
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
+  return static_cast<uint8_t*>(a.devicePointer);
+}
+
+}  // namespace
+
+extern "C" {
+
+uint64_t kvpool_fingerprint(const kvpool_t* p) { return p ? p->fingerprint : 0; }
+
+int64_t kvpool_image_bytes(const kvpool_t* p, int64_t n_tokens, uint32_t flags) {
+  if (!p || !image_layout_ok(p) || (flags & ~KVPOOL_IMAGE_WINDOW) || n_tokens <= 0 || n_tokens % p->cfg.m_prime != 0)
+    return -1;
+  const int64_t nb = n_tokens / p->cfg.m_prime, w = image_window_tokens(p, n_tokens, flags);
+  return kImageHeader + nb * image_block_bytes(p) + w * p->lay.pd.entry_bytes * p->cfg.n_layers;
+}
+
+int kvpool_export_prefix(kvpool_t* p, int32_t req, int64_t n_tokens, uint32_t flags, void* h_image, int64_t capacity,
+                         void* stream) {
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  if (!h_image || (flags & ~KVPOOL_IMAGE_WINDOW) || !image_layout_ok(p))
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "export_prefix: bad arguments");
+  if (!p->req_ok(req)) return p->fail(KVPOOL_ERR_BAD_REQUEST, "export_prefix: bad request id");
+  const Request& q = p->reqs[req];
+  const int mp = p->cfg.m_prime;
+  if (n_tokens <= 0 || n_tokens % mp != 0 || n_tokens / mp > (int64_t)q.table.size())
+    return p->fail(KVPOOL_ERR_NOT_SHAREABLE, "export_prefix: prefix is not whole sealed blocks");
+  if ((flags & KVPOOL_IMAGE_WINDOW) && n_tokens != q.length)
+    return p->fail(KVPOOL_ERR_NOT_SHAREABLE, "export_prefix: the window exists only at the request's length");
+  const int64_t total = kvpool_image_bytes(p, n_tokens, flags);
+  if (capacity < total) return p->fail(KVPOOL_ERR_INVALID_ARG, "export_prefix: capacity too small");
+  if (reinterpret_cast<uintptr_t>(h_image) % 16 != 0)
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "export_prefix: image not 16-byte aligned");
+  uint8_t* d_image = nullptr;
+  if (p->device() && !(d_image = host_alias(h_image)))
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "export_prefix: image is not page-locked host memory");
+  const int64_t nb = n_tokens / mp, w = image_window_tokens(p, n_tokens, flags);
+  const int64_t block_sec = nb * image_block_bytes(p), win_sec = w * p->lay.pd.entry_bytes * p->cfg.n_layers;
+
+  uint8_t* h = static_cast<uint8_t*>(h_image);
+  std::memset(h, 0, kImageHeader);
+  put_le(h, kImageMagic, 4);
+  put_le(h + 4, 1, 4);
+  put_le(h + 8, p->fingerprint, 8);
+  put_le(h + 16, (uint64_t)n_tokens, 8);
+  put_le(h + 24, (uint64_t)nb, 4);
+  put_le(h + 28, (uint64_t)w, 4);
+  put_le(h + 32, (uint64_t)block_sec, 8);
+  put_le(h + 40, (uint64_t)win_sec, 8);
+  put_le(h + 48, (uint64_t)total, 8);
+  if (!p->device()) return KVPOOL_OK;  // bookkeeping-only pool: the header alone
+
+  std::vector<int32_t> ids(q.table.begin(), q.table.begin() + nb);
+  std::vector<ImageSeg> segs;
+  image_segments(p, ids, req, n_tokens, w, &segs);
+  const int rc = launch_image_copies(p, d_image, true, req, segs, {}, block_sec + win_sec, stream);
+  if (rc != 0) return p->cuda_fail((cudaError_t)rc, "export_prefix launch");
+  return KVPOOL_OK;
+}
+
+int kvpool_import_prefix(kvpool_t* p, int32_t dst, const void* h_image, int64_t bytes, const void* d_win_k,
+                         const void* d_win_v, void* stream) {
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  if (!h_image || !image_layout_ok(p)) return p->fail(KVPOOL_ERR_INVALID_ARG, "import_prefix: bad arguments");
+  if (!p->req_ok(dst)) return p->fail(KVPOOL_ERR_BAD_REQUEST, "import_prefix: bad request id");
+  const uint8_t* h = static_cast<const uint8_t*>(h_image);
+  if (bytes < kImageHeader || get_le(h, 4) != kImageMagic || get_le(h + 4, 4) != 1 ||
+      get_le(h + 8, 8) != p->fingerprint)
+    return p->fail(KVPOOL_ERR_BAD_IMAGE, "import_prefix: not an image of this pool's config");
+  const int mp = p->cfg.m_prime;
+  const int64_t n_tokens = (int64_t)get_le(h + 16, 8);
+  const int64_t nb = (int64_t)get_le(h + 24, 4), w = (int64_t)get_le(h + 28, 4);
+  const uint32_t flags = w > 0 ? KVPOOL_IMAGE_WINDOW : 0u;
+  const int64_t total = kvpool_image_bytes(p, n_tokens, flags);
+  if (total < 0 || nb != n_tokens / mp || (w != 0 && w != std::min<int64_t>(n_tokens, p->cfg.n_win)) ||
+      bytes < total || get_le(h + 48, 8) != (uint64_t)total ||
+      get_le(h + 32, 8) != (uint64_t)(nb * image_block_bytes(p)) ||
+      get_le(h + 40, 8) != (uint64_t)(w * p->lay.pd.entry_bytes * p->cfg.n_layers))
+    return p->fail(KVPOOL_ERR_BAD_IMAGE, "import_prefix: inconsistent sizes");
+  Request& d = p->reqs[dst];
+  if (d.length != 0) return p->fail(KVPOOL_ERR_NOT_SHAREABLE, "import_prefix: dst is not fresh");
+  const bool zero_swa = w == 0;
+  if (p->device() && zero_swa != (d_win_k && d_win_v))
+    return p->fail(KVPOOL_ERR_INVALID_ARG, zero_swa ? "import_prefix: the image has no window: give one"
+                                                    : "import_prefix: the image has a window: give NULL windows");
+  if (p->device() && zero_swa &&
+      ((reinterpret_cast<uintptr_t>(d_win_k) | reinterpret_cast<uintptr_t>(d_win_v)) % 16) != 0)
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "import_prefix: window not 16-byte aligned");
+  if (nb > p->cfg.max_blocks_per_request) return p->fail(KVPOOL_ERR_CAPACITY, "import_prefix: prefix too long");
+  if (nb > (int64_t)p->free_blocks.size()) return p->fail(KVPOOL_ERR_OUT_OF_BLOCKS, "import_prefix: out of blocks");
+  if (reinterpret_cast<uintptr_t>(h_image) % 16 != 0)
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "import_prefix: image not 16-byte aligned");
+  uint8_t* d_image = nullptr;
+  if (p->device() && !(d_image = host_alias(h_image)))
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "import_prefix: image is not page-locked host memory");
+
+  // the smallest free ids, in image order (not yet taken: a failed launch leaves the pool unchanged)
+  std::vector<int32_t> ids;
+  ids.reserve(nb);
+  auto it = p->free_blocks.begin();
+  for (int64_t b = 0; b < nb; ++b, ++it) ids.push_back(*it);
+  if (p->device()) {
+    std::vector<ImageSeg> segs;
+    image_segments(p, ids, dst, n_tokens, w, &segs);
+    std::vector<ImageRun> runs;
+    for (int64_t b = 0; b < nb;) {
+      int64_t e = b + 1;
+      while (e < nb && ids[e] == ids[e - 1] + 1) ++e;
+      runs.push_back(ImageRun{(int32_t)b, ids[b], (int32_t)(e - b)});
+      b = e;
+    }
+    const int64_t moved = nb * image_block_bytes(p) + w * p->lay.pd.entry_bytes * p->cfg.n_layers;
+    int rc = launch_image_copies(p, d_image, false, dst, segs, runs, moved, stream);
+    if (rc == 0 && zero_swa) {  // Zero SWA: the recomputed window through the cache encoding
+      ShareParams sp{};
+      sp.pool = p->lay.pd;
+      std::memcpy(sp.layers, p->lay.layers, sizeof(sp.layers));
+      sp.win_k = d_win_k;
+      sp.win_v = d_win_v;
+      sp.dst = dst;
+      sp.src = -1;
+      sp.n_blocks = 0;
+      sp.w = (int)std::min<int64_t>(n_tokens, p->cfg.n_win);
+      sp.n_tokens = n_tokens;
+      rc = p->launch(KVPOOL_KERNEL_IMAGE, 0, stream, [&](int* nk) { return launch_share(sp, p->cfg.n_layers, stream, nk); });
+    }
+    if (rc != 0) return p->cuda_fail((cudaError_t)rc, "import_prefix launch");
+  }
+  for (int32_t id : ids) {
+    p->free_blocks.erase(id);
+    p->refcount[id] = 1;
+  }
+  d.table = ids;
   d.length = n_tokens;
   return KVPOOL_OK;
 }

@@ -1,0 +1,94 @@
+// kvpool_image.cu -- prefix images: copies between the arena (block part
+// planes, window rings, the block table) and a page-locked host image read
+// or written over the host link ("Ch 12 Inference framework: heterogeneous KV
+// scheduling" s3: the compressed block cache restored by an async copy
+// instead of a prefill; "V4 disk prefix cache": the window stored or not per
+// SWA policy).
+#include "device_util.cuh"
+
+namespace kvp {
+namespace {
+
+constexpr int kImageThreads = 256;
+constexpr int kUnitsPerThread = kImagePieceBytes / 16 / kImageThreads;  // 4
+static_assert(kUnitsPerThread * 16 * kImageThreads == kImagePieceBytes, "piece = whole units per thread");
+
+// zero the bytes of a 16-byte unit from byte `from` on
+__device__ __forceinline__ uint4 zero_tail(uint4 v, int from) {
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int lo = 4 * i;
+    if (from <= lo) w[i] = 0u;
+    else if (from < lo + 4) w[i] &= (1u << (8 * (from - lo))) - 1u;
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Each CTA copies pieces of kImagePieceBytes (grid-stride); a piece lies in
+// one segment.  Every thread issues its loads of a piece before its stores,
+// so a CTA keeps 16 KB in flight over the link.
+__global__ void __launch_bounds__(kImageThreads) image_copy_kernel(const __grid_constant__ ImageParams P) {
+  pdl_start();
+  const PoolDesc& pd = P.pool;
+  const int tid = threadIdx.x;
+  if (!P.to_image) {  // the imported blocks' ids into dst's table row
+    int32_t* row = reinterpret_cast<int32_t*>(pd.arena + pd.table) + (int64_t)P.dst * pd.max_bpr;
+    for (int r = blockIdx.x; r < P.n_runs; r += gridDim.x) {
+      const ImageRun u = P.runs[r];
+      if (u.b0 < 0 || u.cnt < 0 || u.b0 + u.cnt > pd.max_bpr || u.id0 < 0 || u.id0 + u.cnt > pd.max_blocks) {
+        if (tid == 0) flag_error(pd, kErrBadBlock);
+        continue;
+      }
+      for (int i = tid; i < u.cnt; i += blockDim.x) row[u.b0 + i] = u.id0 + i;
+    }
+  }
+  for (int64_t piece = blockIdx.x; piece < P.n_pieces; piece += gridDim.x) {
+    int lo = 0, hi = P.n_segs - 1;  // the segment holding this piece
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (P.piece_base[mid] <= piece) lo = mid;
+      else hi = mid - 1;
+    }
+    const ImageSeg& S = P.segs[lo];
+    const int64_t off0 = (piece - P.piece_base[lo]) * kImagePieceBytes;
+    const int64_t n = min((int64_t)kImagePieceBytes, S.bytes - off0);
+    const uint8_t* src = P.to_image ? pd.arena + S.dev + off0 : P.image + S.img + off0;
+    uint8_t* dst = P.to_image ? P.image + S.img + off0 : pd.arena + S.dev + off0;
+    uint4 v[kUnitsPerThread];
+#pragma unroll
+    for (int k = 0; k < kUnitsPerThread; ++k) {
+      const int64_t u = (int64_t)(k * kImageThreads + tid) * 16;
+      if (u < n) v[k] = P.to_image ? ld_stream16(src + u) : *reinterpret_cast<const uint4*>(src + u);
+    }
+#pragma unroll
+    for (int k = 0; k < kUnitsPerThread; ++k) {
+      const int64_t u = (int64_t)(k * kImageThreads + tid) * 16;
+      if (u < n) {
+        uint4 x = v[k];
+        if (P.to_image && S.mask_row > 0) {
+          const int r = (int)((off0 + u) % S.mask_row);
+          if (r + 16 > S.mask_valid) x = zero_tail(x, S.mask_valid - r);
+        }
+        *reinterpret_cast<uint4*>(dst + u) = x;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+int launch_image(const ImageParams& p, void* stream, int* n_kernels) {
+  if (p.n_pieces <= 0 && p.n_runs <= 0) return 0;
+  if (p.n_segs < 0 || p.n_segs > kMaxImageSegs || p.n_runs < 0 || p.n_runs > kMaxImageRuns ||
+      (p.n_pieces > 0 && p.n_segs == 0))
+    return (int)cudaErrorInvalidValue;
+  const int64_t work = p.n_pieces > p.n_runs ? p.n_pieces : p.n_runs;
+  const int ctas = (int)(work < 152 * 8 ? work : 152 * 8);
+  launch_kernel(true, image_copy_kernel, dim3(ctas), dim3(kImageThreads), 0, reinterpret_cast<cudaStream_t>(stream),
+                p);
+  *n_kernels += 1;
+  return (int)cudaGetLastError();
+}
+
+}  // namespace kvp

@@ -79,7 +79,8 @@ struct AppendParams {
   AppendUnit units[kMaxAppendUnits];
 };
 
-// share_prefix: window fill of dst + table row copy
+// share_prefix: window fill of dst + table row copy (src < 0: window only,
+// for a prefix image restored without its window)
 struct ShareParams {
   PoolDesc pool;
   LayerDesc layers[kMaxLayers];
@@ -87,6 +88,37 @@ struct ShareParams {
   const void* win_v;
   int32_t dst, src, n_blocks, w;
   int64_t n_tokens;
+};
+
+// ---- prefix images ----------------------------------------------------------
+// One contiguous copy between the arena and a host image: a run of adjacent
+// block ids of one part plane, or a piece of a window ring.  On export, the
+// bytes of each mask_row-long row from mask_valid on are written as zeros
+// (the padding after the indexer scales); mask_row 0 means no mask.
+struct ImageSeg {
+  int64_t dev;    // arena byte offset
+  int64_t img;    // image byte offset
+  int64_t bytes;  // multiple of 16
+  int32_t mask_row, mask_valid;
+};
+// block ids of an import: table[dst][b0 + i] = id0 + i for i < cnt
+struct ImageRun {
+  int32_t b0, id0, cnt;
+};
+constexpr int kMaxImageSegs = 64;
+constexpr int kMaxImageRuns = 64;
+constexpr int kImagePieceBytes = 16384;  // bytes one CTA copies per step
+
+struct ImageParams {
+  PoolDesc pool;
+  uint8_t* image;      // device alias of the page-locked host image
+  int32_t to_image;    // 1: export (arena -> image), 0: import
+  int32_t dst;         // request slot whose table row the runs fill (import)
+  int32_t n_segs, n_runs;
+  int64_t n_pieces;    // pieces of kImagePieceBytes over all segments
+  int64_t piece_base[kMaxImageSegs + 1];  // first piece of each segment
+  ImageSeg segs[kMaxImageSegs];
+  ImageRun runs[kMaxImageRuns];
 };
 
 // ---- decode attention -----------------------------------------------------
@@ -143,6 +175,7 @@ struct AttendParams {
 // Each launcher adds the number of kernels it launched to *n_kernels.
 int launch_append(const AppendParams& p, int n_layers, void* stream, int* n_kernels);
 int launch_share(const ShareParams& p, int n_layers, void* stream, int* n_kernels);
+int launch_image(const ImageParams& p, void* stream, int* n_kernels);
 int launch_score(const AttendParams& p, void* stream, int* n_kernels);
 int launch_select(const AttendParams& p, void* stream, int* n_kernels);
 int launch_attend(const AttendParams& p, int part, int ctas, void* stream, int* n_kernels);

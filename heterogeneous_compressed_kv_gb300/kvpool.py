@@ -19,15 +19,17 @@ F32, BF16, FP8_E4M3, FP4_E2M1 = 0, 1, 2, 3  # FP4: indexer entries only (PoolCon
 SWA_ONLY, CSA, HCA, CSA_HCA = 0, 1, 2, 3
 FLAG_NO_DEVICE = 1
 OK, ERR_INVALID_ARG, ERR_OUT_OF_BLOCKS, ERR_OUT_OF_REQUESTS, ERR_BAD_REQUEST = 0, -1, -2, -3, -4
-ERR_NOT_SHAREABLE, ERR_CUDA, ERR_DEVICE_CHECK, ERR_CAPACITY = -5, -6, -7, -8
-KERNEL_APPEND, KERNEL_SCORE, KERNEL_SELECT, KERNEL_ATTEND, KERNEL_COMBINE = range(5)
-KERNEL_NAMES = ["append", "score", "select", "attend", "combine"]
+ERR_NOT_SHAREABLE, ERR_CUDA, ERR_DEVICE_CHECK, ERR_CAPACITY, ERR_BAD_IMAGE = -5, -6, -7, -8, -9
+KERNEL_APPEND, KERNEL_SCORE, KERNEL_SELECT, KERNEL_ATTEND, KERNEL_COMBINE, KERNEL_IMAGE = range(6)
+KERNEL_NAMES = ["append", "score", "select", "attend", "combine", "image"]
+IMAGE_WINDOW = 1  # prefix image flag: include the SWA window (a checkpoint)
 
 EXPORTS = ["kvpool_required_bytes", "kvpool_create", "kvpool_destroy", "kvpool_alloc_request",
            "kvpool_free_request", "kvpool_share_prefix", "kvpool_append", "kvpool_decode_attend",
            "kvpool_request_info", "kvpool_block_refcount", "kvpool_free_block_count", "kvpool_get_layout",
            "kvpool_check_device", "kvpool_profile_enable", "kvpool_profile_read", "kvpool_last_error",
-           "kvpool_topk_static", "kvpool_profile_timeline"]
+           "kvpool_topk_static", "kvpool_profile_timeline", "kvpool_fingerprint", "kvpool_image_bytes",
+           "kvpool_export_prefix", "kvpool_import_prefix"]
 
 
 class KvpoolError(RuntimeError):
@@ -93,6 +95,12 @@ def lib():
         L.kvpool_profile_read.argtypes = [vp, i32, C.POINTER(C.c_double), C.POINTER(i64), C.POINTER(i64)]
         L.kvpool_topk_static.argtypes = [vp, i32, i32, i32, vp, vp]
         L.kvpool_profile_timeline.argtypes = [vp, i32, vp]
+        L.kvpool_fingerprint.restype = C.c_uint64
+        L.kvpool_fingerprint.argtypes = [vp]
+        L.kvpool_image_bytes.restype = i64
+        L.kvpool_image_bytes.argtypes = [vp, i64, C.c_uint32]
+        L.kvpool_export_prefix.argtypes = [vp, i32, i64, C.c_uint32, vp, i64, vp]
+        L.kvpool_import_prefix.argtypes = [vp, i32, vp, i64, vp, vp, vp]
         L.kvpool_last_error.restype = C.c_char_p
         L.kvpool_last_error.argtypes = [vp]
         _lib = L
@@ -170,6 +178,13 @@ def _stream(stream) -> Optional[int]:
     return stream.cuda_stream
 
 
+def _host_buffer(x):
+    """(address, bytes) of a host buffer: a numpy array or a CPU torch tensor."""
+    if isinstance(x, np.ndarray):
+        return x.ctypes.data, x.nbytes
+    return x.data_ptr(), x.numel() * x.element_size()
+
+
 def _i32(a) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=np.int32)
 
@@ -220,6 +235,35 @@ class Pool:
     def share_prefix(self, dst, src, n_tokens, win_k, win_v, stream=None, check=True) -> int:
         rc = self.L.kvpool_share_prefix(self.h, dst, src, n_tokens, _ptr(win_k), _ptr(win_v), _stream(stream))
         return self._check(rc, "share_prefix") if check else rc
+
+    # ---- prefix images (sealed blocks in page-locked host memory) ----
+    def fingerprint(self) -> int:
+        return int(self.L.kvpool_fingerprint(self.h))
+
+    def image_bytes(self, n_tokens: int, flags: int = 0) -> int:
+        return int(self.L.kvpool_image_bytes(self.h, n_tokens, flags))
+
+    def export_prefix(self, req, n_tokens, flags=0, out=None, stream=None, check=True):
+        """Write the image of req's first n_tokens tokens into `out` (a
+        page-locked uint8 host tensor; allocated when None) and return it.  The
+        copy runs in stream order: the image is complete once the stream has
+        reached it."""
+        if out is None:
+            import torch
+            out = torch.empty(max(self.image_bytes(n_tokens, flags), 64), dtype=torch.uint8, pin_memory=True)
+        addr, nbytes = _host_buffer(out)
+        rc = self.L.kvpool_export_prefix(self.h, req, n_tokens, flags, addr, nbytes, _stream(stream))
+        if check:
+            self._check(rc, "export_prefix")
+            return out
+        return rc
+
+    def import_prefix(self, dst, image, win_k=None, win_v=None, stream=None, check=True) -> int:
+        """Restore an image (page-locked host memory) into the fresh request
+        dst; win_k / win_v: the recomputed window for an image without one."""
+        addr, nbytes = _host_buffer(image)
+        rc = self.L.kvpool_import_prefix(self.h, dst, addr, nbytes, _ptr(win_k), _ptr(win_v), _stream(stream))
+        return self._check(rc, "import_prefix") if check else rc
 
     def append(self, req_ids, n_new, k, v, idx_k, stream=None, check=True) -> int:
         req, nn = _i32(req_ids), _i32(n_new)

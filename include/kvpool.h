@@ -73,6 +73,7 @@ enum {
   KVPOOL_ERR_CUDA = -6,            /* a CUDA runtime call failed (see kvpool_last_error) */
   KVPOOL_ERR_DEVICE_CHECK = -7,    /* a kernel flagged a bounds or wait-limit violation */
   KVPOOL_ERR_CAPACITY = -8,        /* a request would exceed max_blocks_per_request */
+  KVPOOL_ERR_BAD_IMAGE = -9,       /* a prefix image is malformed or from another config */
 };
 
 /* ---- element types ---- */
@@ -153,6 +154,76 @@ int kvpool_free_request(kvpool_t* pool, int32_t req);
  * sealed blocks, or dst not fresh), CUDA. */
 int kvpool_share_prefix(kvpool_t* pool, int32_t dst, int32_t src, int64_t n_tokens, const void* d_win_k,
                         const void* d_win_v, void* stream);
+
+/* ---- prefix images: sealed blocks in host memory ----
+ * "Ch 12 Inference framework: heterogeneous KV scheduling" s3 (disk-resident
+ * KV: the compressed block cache is serialized, and a prefix hit brings it
+ * back with an async copy instead of a prefill) and s3.1, with "V4 disk
+ * prefix cache" (SWA policies: Full, Periodic checkpointing, Zero).  Here the
+ * store is page-locked host memory; the copies run as kernels that read and
+ * write it over the host link.
+ *
+ * An image holds the first n_tokens / m' sealed blocks of a request
+ * (n_tokens a positive multiple of m') and, with KVPOOL_IMAGE_WINDOW, the
+ * SWA window at length n_tokens, which the pool holds only while the
+ * request's length is n_tokens (a checkpoint; at a multiple p of m' this is
+ * Periodic checkpointing).  Without the window a restore takes the caller's
+ * recomputed window tokens (Zero SWA).  Byte layout, little-endian:
+ *   header, 64 B: u32 magic 0x4950564B ("KVPI"), u32 version 1, u64 config
+ *     fingerprint, i64 n_tokens, i32 n_blocks, i32 w (window tokens in the
+ *     image, 0 if none), u64 block-section bytes, u64 window-section bytes,
+ *     u64 total bytes, u64 0;
+ *   block section: for each layer in order, for each part the layer has (CSA
+ *     entries, indexer keys, HCA entry) the n_blocks blocks' part in table
+ *     order, each exactly as stored in the part's plane (kvpool_layer_layout:
+ *     csa/idx/hca_block_bytes), with the zero padding after the indexer
+ *     scales forced to zero;
+ *   window section: for each layer the tokens at positions n_tokens - w ..
+ *     n_tokens - 1, one entry_bytes record each (w = min(n_tokens, n_win)).
+ * The fingerprint is FNV-1a 64 over the little-endian int32 fields m, m',
+ * n_win, heads, head_dim, idx_heads, idx_dim, in_dtype, cache_dtype, idx_fp4,
+ * n_layers, then per layer its kind and the fp32 bits of the gate logits it
+ * uses (CSA then indexer if it has CSA, HCA if it has HCA).  Images need each
+ * indexer key to be whole 16-byte chunks (when a layer has CSA).
+ *
+ * The image buffer is caller-owned page-locked host memory (cudaHostAlloc,
+ * or cudaHostRegister'd with cudaHostRegisterMapped), 16-byte aligned. */
+#define KVPOOL_IMAGE_WINDOW 1u
+
+/* FNV-1a 64 of the pool's config record (see above). */
+uint64_t kvpool_fingerprint(const kvpool_t* pool);
+
+/* Bytes of the image of an n_tokens prefix with `flags`; -1 if n_tokens is
+ * not a positive multiple of m' or the config has no image layout. */
+int64_t kvpool_image_bytes(const kvpool_t* pool, int64_t n_tokens, uint32_t flags);
+
+/* Write the image of request req's first n_tokens tokens into h_image
+ * (capacity bytes).  The header is written by the host during the call; the
+ * blocks and window are copied by a kernel in stream order on `stream`, so
+ * the image is complete when the stream reaches that point.  Errors:
+ * BAD_REQUEST, NOT_SHAREABLE (n_tokens not a multiple of m', beyond req's
+ * sealed blocks, or the window asked for at a length other than req's),
+ * INVALID_ARG (unknown flag, capacity below kvpool_image_bytes, a buffer that
+ * is not page-locked host memory or not 16-byte aligned, no image layout),
+ * CUDA. */
+int kvpool_export_prefix(kvpool_t* pool, int32_t req, int64_t n_tokens, uint32_t flags, void* h_image,
+                         int64_t capacity, void* stream);
+
+/* Restore an image into the fresh request dst: its blocks get new ids (the
+ * smallest free ids, in image order, refcount 1), dst's table and length
+ * n_tokens are set, and its window comes from the image, or, for an image
+ * without one, from d_win_k / d_win_v ([n_layers][w][heads][head_dim] in
+ * in_dtype, w = min(n_tokens, n_win), 16-byte aligned device memory: the
+ * recomputed K/V of positions n_tokens - w .. n_tokens - 1, as for
+ * kvpool_share_prefix); give NULL windows with an image that has one.  The
+ * host reads the header during the call (the image must be complete by
+ * then); a kernel copies the rest in stream order.  Errors: BAD_IMAGE
+ * (magic, version, fingerprint or sizes wrong, bytes too small),
+ * NOT_SHAREABLE (dst not fresh), CAPACITY, OUT_OF_BLOCKS, INVALID_ARG
+ * (windows missing or given when the image has one, buffer not page-locked
+ * or aligned), BAD_REQUEST, CUDA; an error leaves the pool unchanged. */
+int kvpool_import_prefix(kvpool_t* pool, int32_t dst, const void* h_image, int64_t bytes, const void* d_win_k,
+                         const void* d_win_v, void* stream);
 
 /* Append new tokens ([P1] s3, s4): for request h_req_ids[i], h_n_new[i]
  * tokens.  d_k, d_v: [n_layers][T][heads][head_dim], d_idx_k:
@@ -277,7 +348,8 @@ enum {
   KVPOOL_KERNEL_SELECT = 2,  /* top-k radix select passes and emit */
   KVPOOL_KERNEL_ATTEND = 3,  /* split-K attention over the three sources */
   KVPOOL_KERNEL_COMBINE = 4, /* split-K merge */
-  KVPOOL_KERNEL_COUNT = 5
+  KVPOOL_KERNEL_IMAGE = 5,   /* prefix image copies (export / import) */
+  KVPOOL_KERNEL_COUNT = 6
 };
 #define KVPOOL_PROFILE_ALL ((1 << KVPOOL_KERNEL_COUNT) - 1)
 /* Record events around the launches of the kernel kinds whose bit is set in

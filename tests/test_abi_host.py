@@ -166,6 +166,20 @@ def test_host_bookkeeping_matches_oracle_under_random_traffic():
             rc1 = o.share_prefix(int(dst), int(src), n_tok, win, win)
             rc2 = p.share_prefix(int(dst), int(src), n_tok, None, None, stream=0, check=False)
             assert rc1 == rc2
+        elif op < 5 and len(live) >= 2:  # a prefix image of src restored into dst
+            src, dst = (int(x) for x in rng.choice(live, 2, replace=False))
+            n_tok = int(rng.integers(0, 4)) * 16
+            flags = int(rng.integers(0, 2))
+            rc1, img = o.export_prefix(src, n_tok, flags, cap=1 << 22)
+            hdr = np.zeros(1 << 22, np.uint8)
+            rc2 = p.export_prefix(src, n_tok, flags, out=hdr, stream=0, check=False)
+            assert rc1 == rc2
+            if rc1 == 0:
+                assert hdr[:64].tobytes() == img[:64].tobytes()  # the library's header is the oracle's
+                win = np.zeros((1, min(n_tok, 32), HD), np.float32)
+                rc1 = o.import_prefix(dst, img, win, win)
+                rc2 = p.import_prefix(dst, img, stream=0, check=False)
+                assert rc1 == rc2
         elif live:
             k = int(rng.integers(1, min(4, len(live)) + 1))
             reqs = [int(x) for x in rng.choice(live, k, replace=False)]
@@ -206,3 +220,68 @@ def test_error_codes_match_oracle():
         assert o.free_request(r_) == p.L.kvpool_free_request(p.h, r_)
     assert o.free_request(1) == p.L.kvpool_free_request(p.h, 1) == K.ERR_BAD_REQUEST
     same_state(o, p, range(3))
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(cache_dtype=K.BF16, in_dtype=K.BF16),
+                                dict(cache_dtype=K.FP8_E4M3, in_dtype=K.BF16, idx_dim=32),
+                                dict(cache_dtype=K.FP8_E4M3, in_dtype=K.BF16, idx_fp4=1, idx_dim=32),
+                                dict(n_layers=3, layer_kinds=[K.SWA_ONLY, K.CSA, K.HCA], n_win=256)])
+def test_image_header_and_sizes_match_oracle(kw):
+    """The library's config fingerprint, image sizes and image header equal
+    the oracle's (both written from the documented layout, independently)."""
+    fp4 = kw.pop("idx_fp4", 0)
+    w = base_workload(**kw)
+    w["idx_fp4"] = fp4
+    o = H.make_oracle(w, 4, 16, 8)
+    p = K.Pool(cfg_of(w, max_requests=4, max_blocks=16, max_blocks_per_request=8, idx_fp4=fp4))
+    assert p.fingerprint() == o.fingerprint()
+    for n in (0, 64, 128, 384, 1024):
+        for f in (0, K.IMAGE_WINDOW):
+            assert p.image_bytes(n, f) == o.image_bytes(n, f)
+    r = p.alloc_request()
+    assert o.alloc_request()[1] == r
+    k, v, x = H.tokens(w, [r], [0], [300])
+    assert o.append([r], [300], k, v, x) == 0
+    p.append([r], [300], None, None, None, stream=0)
+    for n, f in ((256, 0), (128, 0)):
+        rc, img = o.export_prefix(r, n, f)
+        hdr = np.zeros(img.size, np.uint8)
+        p.export_prefix(r, n, f, out=hdr, stream=0)
+        assert hdr[:64].tobytes() == img[:64].tobytes()
+    for n, f, code in ((256, K.IMAGE_WINDOW, K.ERR_NOT_SHAREABLE), (320, 0, K.ERR_NOT_SHAREABLE),
+                       (100, 0, K.ERR_NOT_SHAREABLE), (128, 2, K.ERR_INVALID_ARG)):
+        hdr = np.zeros(1 << 20, np.uint8)
+        assert p.export_prefix(r, n, f, out=hdr, stream=0, check=False) == code
+    small = np.zeros(64, np.uint8)
+    assert p.export_prefix(r, 128, 0, out=small, stream=0, check=False) == K.ERR_INVALID_ARG  # capacity
+
+
+def test_image_import_refusals_match_oracle():
+    w = base_workload(m_prime=16, n_win=16, heads=4, head_dim=64, idx_dim=16)
+    o, p = both(w, max_requests=4, max_blocks=6, mbpr=3)
+    r = [p.alloc_request() for _ in range(4)]
+    assert [o.alloc_request()[1] for _ in range(4)] == r
+    z = lambda T: np.zeros((1, T, 256), np.float32)
+    zi = lambda T: np.zeros((1, T, 16), np.float32)
+    assert o.append([0], [48], z(48), z(48), zi(48)) == 0
+    p.append([0], [48], None, None, None, stream=0)
+    rc, img = o.export_prefix(0, 48, K.IMAGE_WINDOW)
+    win = z(16)
+    for bad_at in (0, 4, 8, 16, 24, 48):  # magic, version, fingerprint, n_tokens, n_blocks, total
+        bad = img.copy()
+        bad[bad_at] ^= 1
+        assert o.import_prefix(1, bad, win, win) == p.import_prefix(1, bad, stream=0, check=False) == \
+            K.ERR_BAD_IMAGE
+    assert o.import_prefix(1, img[:-16], win, win) == p.import_prefix(1, img[:-16], stream=0, check=False) == \
+        K.ERR_BAD_IMAGE
+    assert o.import_prefix(0, img, win, win) == p.import_prefix(0, img, stream=0, check=False) == \
+        K.ERR_NOT_SHAREABLE
+    assert o.import_prefix(1, img, win, win) == p.import_prefix(1, img, stream=0, check=False) == 0
+    same_state(o, p, range(4))
+    assert o.import_prefix(2, img, win, win) == p.import_prefix(2, img, stream=0, check=False) == \
+        K.ERR_OUT_OF_BLOCKS
+    same_state(o, p, range(4))
+    o2, p2 = both(w, max_requests=2, max_blocks=6, mbpr=2)
+    assert o2.alloc_request()[1] == p2.alloc_request()
+    assert o2.import_prefix(0, img, win, win) == p2.import_prefix(0, img, stream=0, check=False) == \
+        K.ERR_CAPACITY
