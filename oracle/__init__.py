@@ -50,7 +50,8 @@ class _Config(C.Structure):
                 ("layer_kinds", C.POINTER(C.c_int32)),
                 ("max_requests", C.c_int32), ("max_blocks", C.c_int32), ("max_blocks_per_request", C.c_int32),
                 ("gate_csa", C.POINTER(C.c_float)), ("gate_hca", C.POINTER(C.c_float)),
-                ("gate_idx", C.POINTER(C.c_float)), ("idx_fp4", C.c_int32)]
+                ("gate_idx", C.POINTER(C.c_float)), ("idx_fp4", C.c_int32), ("csa_hot_slots", C.c_int32),
+                ("csa_host_slots", C.c_int32)]
 
 
 class _Info(C.Structure):
@@ -110,6 +111,12 @@ def lib():
         L.kvo_image_bytes.argtypes = [vp, i64, C.c_uint32]
         L.kvo_export_prefix.argtypes = [vp, i32, i64, C.c_uint32, vp, i64]
         L.kvo_import_prefix.argtypes = [vp, i32, vp, i64, vp, vp]
+        L.kvo_block_location.argtypes = [vp, i32, C.POINTER(i32), C.POINTER(C.c_uint32)]
+        L.kvo_epoch.restype = C.c_uint32
+        L.kvo_epoch.argtypes = [vp]
+        L.kvo_inactive_blocks.argtypes = [vp, C.c_uint32, vp, i32]
+        L.kvo_offload.argtypes = [vp, C.c_int, vp]
+        L.kvo_fetch.argtypes = [vp, C.c_int, vp]
         _lib = L
     return _lib
 
@@ -197,7 +204,7 @@ class Oracle:
 
     def __init__(self, *, m, m_prime, n_win, heads, head_dim, idx_heads, idx_dim, in_dtype, cache_dtype,
                  layer_kinds, max_requests, max_blocks, max_blocks_per_request, gate_csa, gate_hca, gate_idx,
-                 idx_fp4=0):
+                 idx_fp4=0, csa_hot_slots=0, csa_host_slots=0):
         self.L = lib()
         self.kinds = np.ascontiguousarray(layer_kinds, dtype=np.int32)
         n_layers = self.kinds.size
@@ -208,7 +215,7 @@ class Oracle:
         cfg = _Config(m, m_prime, n_win, heads, head_dim, idx_heads, idx_dim, in_dtype, cache_dtype, n_layers,
                       self.kinds.ctypes.data_as(C.POINTER(C.c_int32)), max_requests, max_blocks,
                       max_blocks_per_request, self.g_csa.ctypes.data_as(fp), self.g_hca.ctypes.data_as(fp),
-                      self.g_idx.ctypes.data_as(fp), int(idx_fp4))
+                      self.g_idx.ctypes.data_as(fp), int(idx_fp4), int(csa_hot_slots), int(csa_host_slots))
         h = C.c_void_p()
         rc = self.L.kvo_create(C.byref(cfg), C.byref(h))
         if rc != OK:
@@ -270,6 +277,29 @@ class Oracle:
         wk = None if win_k is None else _f32(win_k)
         wv = None if win_v is None else _f32(win_v)
         return self.L.kvo_import_prefix(self.h, dst, _p(img), img.size, _p(wk), _p(wv))
+
+    # HiSparse placement ------------------------------------------------------
+    def block_location(self, b):
+        """(rc, loc, last_used): loc >= 0 hot slot, < 0 host slot -1-loc."""
+        loc, lu = C.c_int32(), C.c_uint32()
+        rc = self.L.kvo_block_location(self.h, b, C.byref(loc), C.byref(lu))
+        return rc, loc.value, lu.value
+
+    def epoch(self) -> int:
+        return int(self.L.kvo_epoch(self.h))
+
+    def inactive_blocks(self, idle, cap=1 << 16):
+        ids = np.zeros(max(cap, 1), np.int32)
+        n = self.L.kvo_inactive_blocks(self.h, idle, _p(ids), cap)
+        return ids[:min(n, cap)].copy() if n >= 0 else n
+
+    def offload(self, ids):
+        a = np.ascontiguousarray(ids, np.int32)
+        return self.L.kvo_offload(self.h, a.size, _p(a))
+
+    def fetch(self, ids):
+        a = np.ascontiguousarray(ids, np.int32)
+        return self.L.kvo_fetch(self.h, a.size, _p(a))
 
     def decode_attend(self, layer, req_ids, q, q_idx, top_k):
         req = np.ascontiguousarray(req_ids, dtype=np.int32)

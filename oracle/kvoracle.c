@@ -172,7 +172,9 @@ typedef struct layer_sec { /* one layer's share of a Classical block (or of a re
 
 typedef struct block {
   int refcount;
-  layer_sec* layers; /* allocated on first use, kept */
+  layer_sec* layers;  /* allocated on first use, kept */
+  int32_t loc;        /* HiSparse: >= 0 hot slot, < 0 host slot -1-loc */
+  uint32_t last_used; /* epoch of the last selection of one of its CSA entries */
 } block;
 
 typedef struct req_layer {
@@ -207,6 +209,11 @@ struct kvo {
   int n_free_blocks;
   int block_hint; /* no free id below this */
   uint64_t fingerprint; /* of the config, for prefix images */
+  int hisparse;         /* HiSparse placement on */
+  uint8_t* hot_used;    /* [csa_hot_slots] */
+  uint8_t* host_used;   /* [csa_host_slots] */
+  int hot_free, host_free;
+  uint32_t epoch;       /* decode_attend calls so far */
   request* reqs;
 };
 
@@ -348,12 +355,23 @@ int kvo_create(const kvo_config* cfg, kvo_t** out) {
   o->block_hint = 0;
   o->reqs = (request*)calloc((size_t)c->max_requests, sizeof(request));
   o->fingerprint = config_fingerprint(c);
+  o->hisparse = c->csa_hot_slots > 0;
+  if (c->csa_hot_slots < 0 || c->csa_host_slots < 0 || (!o->hisparse && c->csa_host_slots > 0)) {
+    kvo_destroy(o);
+    return KVO_ERR_INVALID_ARG;
+  }
+  o->hot_used = (uint8_t*)calloc((size_t)c->csa_hot_slots + 1, 1);
+  o->host_used = (uint8_t*)calloc((size_t)c->csa_host_slots + 1, 1);
+  o->hot_free = c->csa_hot_slots;
+  o->host_free = c->csa_host_slots;
   *out = o;
   return KVO_OK;
 }
 
 void kvo_destroy(kvo_t* o) {
   if (!o) return;
+  free(o->hot_used);
+  free(o->host_used);
   if (o->blocks) {
     for (int b = 0; b < o->c.max_blocks; ++b) {
       if (!o->blocks[b].layers) continue;
@@ -562,11 +580,51 @@ static int32_t block_take(kvo_t* o) { /* smallest free id */
   return -1; /* callers check n_free_blocks first */
 }
 
+/* HiSparse slots: smallest free; without HiSparse a block's CSA entries stay
+ * with the block (location = its id) */
+static int32_t hot_take(kvo_t* o) {
+  for (int32_t i = 0; i < o->c.csa_hot_slots; ++i)
+    if (!o->hot_used[i]) {
+      o->hot_used[i] = 1;
+      o->hot_free -= 1;
+      return i;
+    }
+  return -1; /* callers check hot_free first */
+}
+
+static int32_t host_take(kvo_t* o) {
+  for (int32_t i = 0; i < o->c.csa_host_slots; ++i)
+    if (!o->host_used[i]) {
+      o->host_used[i] = 1;
+      o->host_free -= 1;
+      return i;
+    }
+  return -1;
+}
+
+static void loc_release(kvo_t* o, int32_t loc) {
+  if (!o->hisparse) return;
+  if (loc >= 0) {
+    o->hot_used[loc] = 0;
+    o->hot_free += 1;
+  } else {
+    o->host_used[-1 - loc] = 0;
+    o->host_free += 1;
+  }
+}
+
+/* a block id just taken (sealed or restored): its CSA entries go to a hot slot */
+static void place_new_block(kvo_t* o, int32_t b) {
+  o->blocks[b].loc = o->hisparse ? hot_take(o) : b;
+  o->blocks[b].last_used = o->epoch;
+}
+
 static void block_release(kvo_t* o, int32_t b) {
   o->blocks[b].refcount -= 1;
   if (o->blocks[b].refcount == 0) {
     o->n_free_blocks += 1;
     if (b < o->block_hint) o->block_hint = b;
+    loc_release(o, o->blocks[b].loc);
   }
 }
 
@@ -625,6 +683,7 @@ static void token_into_layer(kvo_t* o, request* q, int l, const float* kv, const
  * the smallest free id and move the staged entries in ([P1] s2.2, [P3] s2.2) */
 static void seal_block(kvo_t* o, request* q) {
   int32_t id = block_take(o);
+  place_new_block(o, id);
   block* b = &o->blocks[id];
   for (int l = 0; l < o->c.n_layers; ++l) {
     req_layer* rl = &q->layers[l];
@@ -667,7 +726,7 @@ int kvo_append(kvo_t* o, int n, const int32_t* req_ids, const int32_t* n_new, co
     seals += L1 / o->c.m_prime - L0 / o->c.m_prime;
   }
   if (T > 0 && (!k || !v || (any_csa(o) && !idx_k))) return KVO_ERR_INVALID_ARG;
-  if (seals > o->n_free_blocks) return KVO_ERR_OUT_OF_BLOCKS;
+  if (seals > o->n_free_blocks || (o->hisparse && seals > o->hot_free)) return KVO_ERR_OUT_OF_BLOCKS;
 
   int HD = o->HD, XD = o->XD;
   float* kv = (float*)malloc(sizeof(float) * 2 * (size_t)HD);
@@ -747,6 +806,7 @@ int kvo_decode_attend(kvo_t* o, int layer, int n, const int32_t* req_ids, const 
     if (o->reqs[req_ids[i]].L == 0) return KVO_ERR_INVALID_ARG;
   }
   int HD = o->HD, XD = o->XD;
+  o->epoch += 1; /* this call's epoch */
   for (int i = 0; i < n; ++i) {
     const request* r = &o->reqs[req_ids[i]];
     int64_t N_c = has_csa(o, layer) ? r->L / o->c.m : 0;
@@ -769,6 +829,10 @@ int kvo_decode_attend(kvo_t* o, int layer, int n, const int32_t* req_ids, const 
     }
     if (topk)
       for (int j = 0; j < top_k; ++j) topk[(size_t)i * top_k + j] = sel[j];
+    for (int64_t j = 0; j < kk; ++j) { /* activity: the blocks of the selected sealed entries */
+      const int64_t seg = sel[j] / o->CB;
+      if (seg < r->n_sealed) o->blocks[r->table[seg]].last_used = o->epoch;
+    }
     /* sources: [selected CSA entries | every HCA entry | the window] */
     int64_t n_src = kk + N_h + w;
     uint8_t* codes = (uint8_t*)malloc((size_t)n_src * o->esz);
@@ -1053,10 +1117,13 @@ int kvo_import_prefix(kvo_t* o, int32_t dst, const uint8_t* image, int64_t bytes
   if (q->L != 0) return KVO_ERR_NOT_SHAREABLE;
   if (w == 0 && (!win_k || !win_v)) return KVO_ERR_INVALID_ARG;
   if (nb > o->c.max_blocks_per_request) return KVO_ERR_CAPACITY;
-  if (nb > o->n_free_blocks) return KVO_ERR_OUT_OF_BLOCKS;
+  if (nb > o->n_free_blocks || (o->hisparse && nb > o->hot_free)) return KVO_ERR_OUT_OF_BLOCKS;
 
   const int64_t E = entry_rec(o), X = idx_part(o);
-  for (int64_t b = 0; b < nb; ++b) q->table[b] = block_take(o);
+  for (int64_t b = 0; b < nb; ++b) {
+    q->table[b] = block_take(o);
+    place_new_block(o, q->table[b]);
+  }
   q->n_sealed = (int)nb;
   q->L = n_tokens;
   const uint8_t* p = image + 64;
@@ -1094,6 +1161,69 @@ int kvo_import_prefix(kvo_t* o, int32_t dst, const uint8_t* image, int64_t bytes
         window_put(o, &q->layers[l], n_tokens - w_full + t, kv);
       }
     free(kv);
+  }
+  return KVO_OK;
+}
+
+/* ------------------------------------------------------------------ */
+/* HiSparse placement                                                   */
+/* ------------------------------------------------------------------ */
+
+int kvo_block_location(const kvo_t* o, int32_t b, int32_t* loc, uint32_t* last_used) {
+  if (!o || b < 0 || b >= o->c.max_blocks || o->blocks[b].refcount == 0) return KVO_ERR_INVALID_ARG;
+  if (loc) *loc = o->blocks[b].loc;
+  if (last_used) *last_used = o->blocks[b].last_used;
+  return KVO_OK;
+}
+
+uint32_t kvo_epoch(const kvo_t* o) { return o ? o->epoch : 0; }
+
+int kvo_inactive_blocks(const kvo_t* o, uint32_t idle, int32_t* ids, int32_t cap) {
+  if (!o || cap < 0 || (cap > 0 && !ids)) return KVO_ERR_INVALID_ARG;
+  int n = 0;
+  for (int32_t b = 0; b < o->c.max_blocks; ++b) {
+    const block* x = &o->blocks[b];
+    if (x->refcount == 0 || x->loc < 0 || o->epoch - x->last_used < idle) continue;
+    if (n < cap) ids[n] = b;
+    ++n;
+  }
+  return n;
+}
+
+/* a list of distinct live block ids, all resident (want_hot) or all offloaded */
+static int ids_ok(const kvo_t* o, int n, const int32_t* ids, int want_hot) {
+  if (!o->hisparse || n < 0 || (n > 0 && !ids)) return 0;
+  for (int i = 0; i < n; ++i) {
+    const int32_t b = ids[i];
+    if (b < 0 || b >= o->c.max_blocks || o->blocks[b].refcount == 0) return 0;
+    if ((o->blocks[b].loc >= 0) != want_hot) return 0;
+    for (int j = 0; j < i; ++j)
+      if (ids[j] == b) return 0;
+  }
+  return 1;
+}
+
+int kvo_offload(kvo_t* o, int n, const int32_t* ids) {
+  if (!o || !ids_ok(o, n, ids, 1)) return KVO_ERR_INVALID_ARG;
+  if (n > o->host_free) return KVO_ERR_OUT_OF_BLOCKS;
+  for (int i = 0; i < n; ++i) {
+    block* x = &o->blocks[ids[i]];
+    const int32_t h = host_take(o);
+    loc_release(o, x->loc);
+    x->loc = -1 - h;
+  }
+  return KVO_OK;
+}
+
+int kvo_fetch(kvo_t* o, int n, const int32_t* ids) {
+  if (!o || !ids_ok(o, n, ids, 0)) return KVO_ERR_INVALID_ARG;
+  if (n > o->hot_free) return KVO_ERR_OUT_OF_BLOCKS;
+  for (int i = 0; i < n; ++i) {
+    block* x = &o->blocks[ids[i]];
+    const int32_t h = hot_take(o);
+    loc_release(o, x->loc);
+    x->loc = h;
+    x->last_used = o->epoch;
   }
   return KVO_OK;
 }

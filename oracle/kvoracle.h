@@ -80,6 +80,10 @@ typedef struct kvo_config {
   const float* gate_hca; /* logits [n_layers][heads][m_prime] */
   const float* gate_idx; /* logits [n_layers][idx_heads][m]   */
   int32_t idx_fp4;       /* 1: indexer entries in FP4 (e2m1 + one bf16 scale), 0: in the cache dtype */
+  /* HiSparse placement of sealed blocks' CSA entries: GPU-resident ("hot")
+   * slots and host slots; csa_hot_slots 0 = no HiSparse (every block's CSA
+   * entries stay where the block is) */
+  int32_t csa_hot_slots, csa_host_slots;
 } kvo_config;
 
 typedef struct kvo kvo_t;
@@ -199,6 +203,29 @@ int kvo_export_prefix(const kvo_t* o, int32_t req, int64_t n_tokens, uint32_t fl
  * NOT_SHAREABLE (dst not fresh), CAPACITY, OUT_OF_BLOCKS, INVALID_ARG. */
 int kvo_import_prefix(kvo_t* o, int32_t dst, const uint8_t* image, int64_t bytes, const float* win_k,
                       const float* win_v);
+/* ---- HiSparse: offload of inactive CSA entries ("V4 KV Layout" ESS /
+ * HiSparse table: inactive C4 entries of the Classical pool move off the GPU;
+ * "Why does V4 split pools?" s1, s3.2: only full, immutable blocks are
+ * moved).  Reading: a sealed block's CSA entries (every layer's) live in a
+ * hot slot or a host slot, taken smallest-free when the block seals (or is
+ * restored or fetched) and when it is offloaded; indexer keys and the HCA
+ * entry never move.  Activity: every decode_attend call advances the epoch
+ * by one; a call on a CSA layer stamps each block holding a selected entry
+ * with that epoch (a sealing, restore or fetch stamps the current epoch).  A
+ * block is inactive after `idle` epochs without a stamp.  Placement never
+ * changes a value. ---- */
+/* loc: >= 0 hot slot, < 0 host slot -1-loc; INVALID_ARG for a free block */
+int kvo_block_location(const kvo_t* o, int32_t block_id, int32_t* loc, uint32_t* last_used);
+uint32_t kvo_epoch(const kvo_t* o);
+/* resident sealed blocks with epoch - last_used >= idle, ascending; returns the count (<= cap written) */
+int kvo_inactive_blocks(const kvo_t* o, uint32_t idle, int32_t* ids, int32_t cap);
+/* Move the CSA entries of resident blocks to host slots (in the given order).
+ * Errors: INVALID_ARG (HiSparse off, a free, offloaded or repeated id),
+ * OUT_OF_BLOCKS (too few host slots); an error changes nothing. */
+int kvo_offload(kvo_t* o, int n, const int32_t* ids);
+/* Bring offloaded blocks back to hot slots.  Errors: INVALID_ARG (not
+ * offloaded, repeated), OUT_OF_BLOCKS (too few hot slots). */
+int kvo_fetch(kvo_t* o, int n, const int32_t* ids);
 int kvo_value_bytes(int dtype);
 /* bytes of n encoded values (FP4: two per byte) */
 int64_t kvo_code_bytes(int dtype, int64_t n);

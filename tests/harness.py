@@ -25,7 +25,8 @@ def make_oracle(cfg, max_requests, max_blocks, max_blocks_per_request, gate_over
                     in_dtype=cfg["in_dtype"], cache_dtype=cfg["cache_dtype"], layer_kinds=cfg["layer_kinds"],
                     max_requests=max_requests, max_blocks=max_blocks,
                     max_blocks_per_request=max_blocks_per_request, gate_csa=g_csa, gate_hca=g_hca,
-                    gate_idx=g_idx, idx_fp4=cfg.get("idx_fp4", 0))
+                    gate_idx=g_idx, idx_fp4=cfg.get("idx_fp4", 0), csa_hot_slots=cfg.get("csa_hot_slots", 0),
+                    csa_host_slots=cfg.get("csa_host_slots", 0))
 
 
 def _values(cfg, n_values, runs, out=None):
