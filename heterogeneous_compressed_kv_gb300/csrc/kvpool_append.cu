@@ -192,7 +192,8 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   constexpr int isz = InTraits<IN>::kBytes;
 
   if (u.slot < 0 || u.slot >= pd.max_requests || u.seg < 0 || u.seg >= pd.max_bpr + 1 ||
-      u.block_id >= pd.max_blocks || u.t0 < 0 || u.t1 > mp || u.t0 > u.t1) {
+      u.block_id >= pd.max_blocks || u.t0 < 0 || u.t1 > mp || u.t0 > u.t1 ||
+      (u.block_id >= 0 && (u.csa_slot < 0 || u.csa_slot >= pd.csa_staging_base))) {
     if (tid == 0) flag_error(pd, kErrBadIndex);
     return;
   }
@@ -238,7 +239,9 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   }
 
   const int32_t dst_block = u.block_id >= 0 ? u.block_id : pd.staging_base + u.slot;
-  uint8_t* blk_csa = pd.arena + L.csa_pool + (int64_t)dst_block * L.csa_stride;
+  // CSA entries go to the block's CSA slot (its id without HiSparse)
+  const int32_t csa_slot = u.block_id >= 0 ? u.csa_slot : pd.csa_staging_base + u.slot;
+  uint8_t* blk_csa = pd.arena + L.csa_pool + (int64_t)csa_slot * L.csa_stride;
   uint8_t* blk_idx = pd.arena + L.idx_pool + (int64_t)dst_block * L.idx_stride;
   uint8_t* blk_hca = pd.arena + L.hca_pool + (int64_t)dst_block * L.hca_stride;
   uint8_t* ring = pd.arena + L.ring + (int64_t)u.slot * L.ring_req_bytes;
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   if (u.block_id >= 0 && L.has_csa && u.t0 >= m) {
     const int n_copy = u.t0 / m;
     const int32_t sid = pd.staging_base + u.slot;
-    const uint8_t* stg_csa = pd.arena + L.csa_pool + (int64_t)sid * L.csa_stride;
+    const uint8_t* stg_csa = pd.arena + L.csa_pool + (int64_t)(pd.csa_staging_base + u.slot) * L.csa_stride;
     const uint8_t* stg_idx = pd.arena + L.idx_pool + (int64_t)sid * L.idx_stride;
     const int64_t bytes = (int64_t)n_copy * pd.entry_bytes;  // CSA entries, multiple of 16
     const int64_t per = ((bytes / 16 + P.n_slices - 1) / P.n_slices) * 16;
@@ -347,8 +350,13 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
       }
     }
   }
-  if (u.block_id >= 0 && slice == 0 && layer == 0 && tid == 0)
+  if (u.block_id >= 0 && slice == 0 && layer == 0 && tid == 0) {
     reinterpret_cast<int32_t*>(pd.arena + pd.table)[(int64_t)u.slot * pd.max_bpr + u.seg] = u.block_id;
+    if (pd.hisparse) {  // the new block's CSA location and activity stamp
+      reinterpret_cast<int32_t*>(pd.arena + pd.csa_loc)[u.block_id] = u.csa_slot;
+      reinterpret_cast<uint32_t*>(pd.arena + pd.last_used)[u.block_id] = P.epoch;
+    }
+  }
 }
 
 // share_prefix: blockIdx.x = window token, blockIdx.y = slice, blockIdx.z = layer;

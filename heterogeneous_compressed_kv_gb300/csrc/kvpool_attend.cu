@@ -43,12 +43,16 @@ __device__ __forceinline__ int find_split_req(const AttendParams& P, int cta, in
   return lo;
 }
 
-// Byte offset (from the arena) of virtual source v of request R.
-__device__ __forceinline__ int64_t source_offset(const AttendParams& P, int i, const AttendReq& R, int v) {
+// Device address of virtual source v of request R: an entry in the arena,
+// or (HiSparse) an offloaded CSA entry in its host slot, through the host
+// pool's device alias.  Reading a sealed block's CSA entry stamps the block
+// with this call's epoch (HiSparse activity).
+template <bool HS>
+__device__ __forceinline__ uint64_t source_addr(const AttendParams& P, int i, const AttendReq& R, int v) {
   const PoolDesc& pd = P.pool;
   const LayerDesc& L = P.layer;
   const int32_t* table = reinterpret_cast<const int32_t*>(pd.arena + pd.table) + (int64_t)R.slot * pd.max_bpr;
-  const int64_t ring = L.ring + (int64_t)R.slot * L.ring_req_bytes;
+  const uint64_t ring = reinterpret_cast<uint64_t>(pd.arena + L.ring + (int64_t)R.slot * L.ring_req_bytes);
   if (v < R.k) {
     const int32_t e = P.sel[(int64_t)i * P.sel_stride + v];
     if (e < 0 || e >= R.n_cand) {
@@ -57,12 +61,33 @@ __device__ __forceinline__ int64_t source_offset(const AttendParams& P, int i, c
     }
     const int CB = pd.csa_per_block;
     const int seg = e / CB;
-    const int32_t bid = seg < R.n_sealed ? table[seg] : pd.staging_base + R.slot;
-    if (seg < R.n_sealed && (bid < 0 || bid >= pd.max_blocks)) {
+    const int64_t in_block = (int64_t)(e % CB) * pd.entry_bytes;
+    if (seg >= R.n_sealed)  // the request's open block
+      return reinterpret_cast<uint64_t>(pd.arena + L.csa_pool +
+                                        (int64_t)(pd.csa_staging_base + R.slot) * L.csa_stride + in_block);
+    const int32_t bid = table[seg];
+    if (bid < 0 || bid >= pd.max_blocks) {
       flag_error(pd, kErrBadBlock);
       return ring;
     }
-    return L.csa_pool + (int64_t)bid * L.csa_stride + (int64_t)(e % CB) * pd.entry_bytes;
+    int32_t loc = bid;
+    if constexpr (HS) {
+      loc = reinterpret_cast<const int32_t*>(pd.arena + pd.csa_loc)[bid];
+      reinterpret_cast<uint32_t*>(pd.arena + pd.last_used)[bid] = P.epoch;
+      if (loc < 0) {
+        const int64_t h = -1 - (int64_t)loc;
+        if (!pd.host_pool || (h + 1) * pd.host_slot_bytes > pd.host_pool_bytes) {
+          flag_error(pd, kErrBadBlock);
+          return ring;
+        }
+        return reinterpret_cast<uint64_t>(pd.host_pool + h * pd.host_slot_bytes + L.csa_host_off + in_block);
+      }
+      if (loc >= pd.csa_staging_base) {
+        flag_error(pd, kErrBadBlock);
+        return ring;
+      }
+    }
+    return reinterpret_cast<uint64_t>(pd.arena + L.csa_pool + (int64_t)loc * L.csa_stride + in_block);
   }
   v -= R.k;
   if (v < R.n_hca) {
@@ -71,11 +96,11 @@ __device__ __forceinline__ int64_t source_offset(const AttendParams& P, int i, c
       flag_error(pd, kErrBadBlock);
       return ring;
     }
-    return L.hca_pool + (int64_t)bid * L.hca_stride;
+    return reinterpret_cast<uint64_t>(pd.arena + L.hca_pool + (int64_t)bid * L.hca_stride);
   }
   v -= R.n_hca;
   const int64_t pos = R.length - R.w + v;
-  return ring + (pos % pd.n_win) * pd.entry_bytes;
+  return ring + (uint64_t)((pos % pd.n_win) * pd.entry_bytes);
 }
 
 // ---- shared-memory loads and number formats of the consumer loop ----------
@@ -380,7 +405,7 @@ __device__ __forceinline__ void consume_stage(uint32_t base, int ne, uint32_t ES
 // of kStages stages (lane e copies entry e of a stage; entries that follow
 // each other in memory go in one copy); the consumer threads run the online
 // softmax and write the split's partial.
-template <int IN, int CACHE, int TPH>
+template <int IN, int CACHE, int TPH, bool HS>
 __global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __grid_constant__ AttendParams P,
                                                                       int e_stage, int part) {
   pdl_start();
@@ -417,8 +442,9 @@ __global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __gr
   if (tid >= n_cons) {
     // ---- producer warp: source addresses 32 at a time, one batch ahead ----
     const int lane = tid & 31;
-    int64_t cur = lane < cnt ? source_offset(P, i, R, v0 + lane) : 0;
-    int64_t nxt = 32 + lane < cnt ? source_offset(P, i, R, v0 + 32 + lane) : 0;
+    const uint64_t hbase = reinterpret_cast<uint64_t>(pd.host_pool), hbytes = (uint64_t)pd.host_pool_bytes;
+    uint64_t cur = lane < cnt ? source_addr<HS>(P, i, R, v0 + lane) : 0;
+    uint64_t nxt = 32 + lane < cnt ? source_addr<HS>(P, i, R, v0 + 32 + lane) : 0;
     int batch = 0;
     bool ok = true;
     int issued = 0;
@@ -429,27 +455,62 @@ __global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __gr
       if (!ok) break;
       const int e0 = st * e_stage;
       const int ne = min(e_stage, cnt - e0);
-      if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)ne * ES);
-      __syncwarp();
+      if constexpr (!HS) {
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)ne * ES);
+        __syncwarp();
+      }
       const int x = e0 + lane;
-      const int64_t ac = __shfl_sync(0xffffffffu, cur, x & 31);
-      const int64_t an = __shfl_sync(0xffffffffu, nxt, x & 31);
-      const int64_t a = (x >> 5) == batch ? ac : an;
+      const uint64_t ac = __shfl_sync(0xffffffffu, cur, x & 31);
+      const uint64_t an = __shfl_sync(0xffffffffu, nxt, x & 31);
+      const uint64_t a = (x >> 5) == batch ? ac : an;
+      // offloaded entries (HiSparse): the warp loads them from host memory
+      // into the stage before the stage's arrival releases it
+      const bool hst = HS && lane < ne && a - hbase < hbytes;
+      const uint32_t hmask = HS ? __ballot_sync(0xffffffffu, hst) : 0u;
+      if (HS && hmask) {
+        constexpr int kLd = 8;
+        const int units = (int)(ES / 16);
+        for (uint32_t mk = hmask; mk; mk &= mk - 1) {
+          const int j = __ffs(mk) - 1;
+          const uint4* src = reinterpret_cast<const uint4*>(__shfl_sync(0xffffffffu, a, j));
+          uint4* dst = reinterpret_cast<uint4*>(stage_mem + (size_t)s * stage_bytes + (size_t)j * ES);
+          for (int u0 = 0; u0 < units; u0 += 32 * kLd) {
+            uint4 t[kLd];
+#pragma unroll
+            for (int k = 0; k < kLd; ++k) {
+              const int u = u0 + k * 32 + lane;
+              if (u < units) t[k] = src[u];
+            }
+#pragma unroll
+            for (int k = 0; k < kLd; ++k) {
+              const int u = u0 + k * 32 + lane;
+              if (u < units) dst[u] = t[k];
+            }
+          }
+        }
+        fence_proxy_async();  // before later bulk copies into this stage
+        __syncwarp();
+      }
+      if constexpr (HS) {
+        if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(ne - __popc(hmask)) * ES);
+        __syncwarp();
+      }
       // lane e starts a copy unless entry e - 1 ends right where entry e begins
-      const int64_t prev = __shfl_up_sync(0xffffffffu, a, 1);
-      const bool start = lane < ne && (lane == 0 || a != prev + (int64_t)ES);
+      const uint64_t prev = __shfl_up_sync(0xffffffffu, a, 1);
+      const bool prev_host = lane > 0 && ((hmask >> (lane - 1)) & 1u);
+      const bool start = lane < ne && !hst && (lane == 0 || prev_host || a != prev + (uint64_t)ES);
       const uint32_t starts = __ballot_sync(0xffffffffu, start);
       if (start) {
-        const uint32_t later = starts & ~((2u << lane) - 1u);
+        const uint32_t later = (starts | hmask) & ~((2u << lane) - 1u);
         const int end = later ? __ffs(later) - 1 : ne;
-        bulk_g2s(stage_mem + (size_t)s * stage_bytes + (size_t)lane * ES, pd.arena + a, (uint32_t)(end - lane) * ES,
-                 &full[s]);
+        bulk_g2s(stage_mem + (size_t)s * stage_bytes + (size_t)lane * ES, reinterpret_cast<const void*>(a),
+                 (uint32_t)(end - lane) * ES, &full[s]);
       }
       if (((e0 + ne) >> 5) != batch) {  // the next stage starts in the next batch
         ++batch;
         cur = nxt;
         const int y = (batch + 1) * 32 + lane;
-        nxt = y < cnt ? source_offset(P, i, R, v0 + y) : 0;
+        nxt = y < cnt ? source_addr<HS>(P, i, R, v0 + y) : 0;
       }
       issued = st + 1;
     }
@@ -622,22 +683,21 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
 template <int IN, int CACHE>
 int launch_attend_t(const AttendParams& p, cudaStream_t s, int e_stage, size_t smem, int part, int ctas) {
   const int threads = (p.pool.HD / 16 + 31) / 32 * 32 + 32;
+  auto go = [&](auto k, size_t* set) {
+    if (*set < smem) {
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      *set = smem;
+    }
+    launch_kernel(false, k, dim3(ctas), dim3(threads), smem, s, p, e_stage, part);
+  };
+  static size_t set[4] = {0, 0, 0, 0};
+  const bool hs = p.pool.hisparse != 0;
   if (p.pool.head_dim == 128) {
-    auto k = attend_kernel<IN, CACHE, 8>;
-    static size_t set8 = 0;
-    if (set8 < smem) {
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      set8 = smem;
-    }
-    launch_kernel(false, k, dim3(ctas), dim3(threads), smem, s, p, e_stage, part);
+    if (hs) go(attend_kernel<IN, CACHE, 8, true>, &set[0]);
+    else go(attend_kernel<IN, CACHE, 8, false>, &set[1]);
   } else if (p.pool.head_dim == 64) {
-    auto k = attend_kernel<IN, CACHE, 4>;
-    static size_t set4 = 0;
-    if (set4 < smem) {
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      set4 = smem;
-    }
-    launch_kernel(false, k, dim3(ctas), dim3(threads), smem, s, p, e_stage, part);
+    if (hs) go(attend_kernel<IN, CACHE, 4, true>, &set[2]);
+    else go(attend_kernel<IN, CACHE, 4, false>, &set[3]);
   } else {
     return (int)cudaErrorInvalidValue;
   }

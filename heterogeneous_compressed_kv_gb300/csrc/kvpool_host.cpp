@@ -78,6 +78,9 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
   if (XD % 16 != 0 || XD > 8 * 256) return "idx_heads * idx_dim must be a multiple of 16, at most 2048";
   if (c->idx_fp4 != 0 && c->idx_fp4 != 1) return "idx_fp4 must be 0 or 1";
   if (c->idx_fp4 && XD % 32 != 0) return "FP4 indexer entries need idx_heads * idx_dim to be a multiple of 32";
+  if (c->csa_hot_slots < 0 || c->csa_host_slots < 0 || c->csa_hot_slots > c->max_blocks ||
+      (c->csa_hot_slots == 0 && c->csa_host_slots > 0))
+    return "HiSparse slots: 0 <= csa_hot_slots <= max_blocks, host slots only with hot slots";
   const int vs = value_bytes(c->cache_dtype);
   bool any_csa = false;
   for (int l = 0; l < c->n_layers; ++l) {
@@ -113,12 +116,19 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
   pd.max_requests = c->max_requests;
   pd.max_bpr = c->max_blocks_per_request;
   pd.staging_base = c->max_blocks;
+  pd.hisparse = c->csa_hot_slots > 0 ? 1 : 0;
+  pd.csa_staging_base = pd.hisparse ? c->csa_hot_slots : c->max_blocks;
 
   int64_t cur = 0;
   pd.err = cur;
   cur += 256;
   pd.table = cur;
   cur = round_up(cur + 4LL * c->max_requests * c->max_blocks_per_request, 256);
+  pd.csa_loc = cur;
+  cur = round_up(cur + 4LL * c->max_blocks, 256);
+  pd.last_used = cur;
+  cur = round_up(cur + 4LL * c->max_blocks, 256);
+  pd.host_slot_bytes = 0;
   const int CB = pd.csa_per_block;
   for (int l = 0; l < c->n_layers; ++l) {
     LayerDesc& d = L.layers[l];
@@ -132,12 +142,17 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
     d.alpha_idx = cur;
     cur = round_up(cur + 4LL * c->idx_heads * c->m, 256);
     const int64_t n_ids = (int64_t)c->max_blocks + c->max_requests;
-    d.csa_pool = d.idx_pool = d.hca_pool = d.idx_scale_off = -1;
+    const int64_t n_csa_slots = (int64_t)pd.csa_staging_base + c->max_requests;
+    d.csa_pool = d.idx_pool = d.hca_pool = d.idx_scale_off = d.csa_host_off = -1;
     d.csa_stride = d.idx_stride = d.hca_stride = 0;
     if (d.has_csa) {
       d.csa_stride = CB * pd.entry_bytes;
       d.csa_pool = cur;
-      cur = round_up(cur + d.csa_stride * n_ids, 256);
+      cur = round_up(cur + d.csa_stride * n_csa_slots, 256);
+      if (pd.hisparse) {
+        d.csa_host_off = pd.host_slot_bytes;
+        pd.host_slot_bytes += d.csa_stride;
+      }
       d.idx_stride = CB * pd.idx_entry_bytes;
       if (pd.idx_dtype == KVPOOL_FP8_E4M3 || pd.idx_dtype == KVPOOL_FP4_E2M1) {
         d.idx_scale_off = d.idx_stride;
@@ -276,6 +291,13 @@ struct kvpool {
   std::set<int32_t> free_blocks;
   std::set<int32_t> free_slots;
   std::vector<Request> reqs;
+  // HiSparse: where each live block's CSA entries are (>= 0 GPU slot, < 0
+  // host slot -1-loc; the id without HiSparse), the free slots, the epoch
+  std::vector<int32_t> loc;
+  std::set<int32_t> hot_free, host_free;
+  uint32_t epoch = 0;
+  uint8_t* host_pool = nullptr;  // device alias of the caller's host slots
+  int64_t host_pool_bytes = 0;
   std::string err;
   // second stream for the attention part that needs no top-k, and the events
   // that fork it from / join it back to the caller's stream
@@ -299,6 +321,24 @@ struct kvpool {
     return KVPOOL_ERR_CUDA;
   }
   bool req_ok(int32_t r) const { return r >= 0 && r < cfg.max_requests && reqs[r].active; }
+  bool hisparse() const { return lay.pd.hisparse != 0; }
+  // location of a block id just taken (sealed or restored): a GPU slot
+  int32_t take_hot(int32_t id) {
+    if (!hisparse()) return id;
+    const int32_t h = *hot_free.begin();
+    hot_free.erase(hot_free.begin());
+    return h;
+  }
+  void release_loc(int32_t l) {
+    if (!hisparse()) return;
+    if (l >= 0) hot_free.insert(l);
+    else host_free.insert(-1 - l);
+  }
+  // the device address of the CSA part of layer d of a block at location l
+  uint64_t csa_addr(const LayerDesc& d, int32_t l) const {
+    if (l >= 0) return reinterpret_cast<uint64_t>(arena + d.csa_pool + (int64_t)l * d.csa_stride);
+    return reinterpret_cast<uint64_t>(host_pool + (int64_t)(-1 - l) * lay.pd.host_slot_bytes + d.csa_host_off);
+  }
 
   // ---- profiling helpers ----
   cudaEvent_t take_event() {
@@ -385,6 +425,9 @@ int kvpool_create(const kvpool_config* cfg, void* d_arena, size_t arena_bytes, v
   p->arena = static_cast<uint8_t*>(d_arena);
   p->lay.pd.arena = p->arena;
   p->refcount.assign(cfg->max_blocks, 0);
+  p->loc.assign(cfg->max_blocks, 0);
+  for (int32_t h = 0; h < cfg->csa_hot_slots; ++h) p->hot_free.insert(p->hot_free.end(), h);
+  for (int32_t h = 0; h < cfg->csa_host_slots; ++h) p->host_free.insert(p->host_free.end(), h);
   for (int32_t b = 0; b < cfg->max_blocks; ++b) p->free_blocks.insert(p->free_blocks.end(), b);
   for (int32_t r = 0; r < cfg->max_requests; ++r) p->free_slots.insert(p->free_slots.end(), r);
   p->reqs.resize(cfg->max_requests);
@@ -451,7 +494,10 @@ int kvpool_alloc_request(kvpool_t* p, int32_t* req_out) {
 }
 
 static void release_block(kvpool_t* p, int32_t b) {
-  if (--p->refcount[b] == 0) p->free_blocks.insert(b);
+  if (--p->refcount[b] == 0) {
+    p->free_blocks.insert(b);
+    p->release_loc(p->loc[b]);
+  }
 }
 
 int kvpool_free_request(kvpool_t* p, int32_t r) {
@@ -506,7 +552,7 @@ int kvpool_share_prefix(kvpool_t* p, int32_t dst, int32_t src, int64_t n_tokens,
 
 }  // extern "C"
 
-// ---- prefix images ----------------------------------------------------------
+// ---- block copies: prefix images, HiSparse offload and fetch -----------------
 namespace {
 
 bool image_layout_ok(const kvpool_t* p) {
@@ -539,61 +585,83 @@ uint64_t get_le(const uint8_t* src, int n) {
   return v;
 }
 
-// The copies of an image: per layer and part, one segment per run of
-// adjacent block ids; then the window ring pieces.  Offsets are the image's.
-void image_segments(const kvpool_t* p, const std::vector<int32_t>& ids, int32_t slot, int64_t n_tokens, int64_t w,
-                    std::vector<ImageSeg>* segs) {
+// Append a copy, merged into the previous one when both ends continue it.
+void add_copy(std::vector<ImageSeg>* segs, uint64_t src, uint64_t dst, int64_t bytes, bool src_host, int32_t mask_row = 0,
+              int32_t mask_valid = 0) {
+  if (!segs->empty()) {
+    ImageSeg& g = segs->back();
+    if (g.src + (uint64_t)g.bytes == src && g.dst + (uint64_t)g.bytes == dst && g.mask_row == mask_row &&
+        g.mask_valid == mask_valid && (g.src_host != 0) == src_host) {
+      g.bytes += bytes;
+      return;
+    }
+  }
+  segs->push_back(ImageSeg{src, dst, bytes, mask_row, mask_valid, src_host ? 1 : 0, 0});
+}
+
+// Append the bookkeeping writes for block ids[i] at locs[i] (table index
+// b0 + i when b0 >= 0), merged into runs of consecutive ids and locations.
+void add_runs(std::vector<ImageRun>* runs, const std::vector<int32_t>& ids, const std::vector<int32_t>& locs, int32_t b0,
+              bool write_loc, bool stamp) {
+  for (size_t i = 0; i < ids.size();) {
+    size_t e = i + 1;
+    const int dir = write_loc && e < ids.size() && locs[e] == locs[i] - 1 ? -1 : 1;
+    while (e < ids.size() && ids[e] == ids[e - 1] + 1 && (!write_loc || locs[e] == locs[e - 1] + dir)) ++e;
+    runs->push_back(ImageRun{b0 >= 0 ? b0 + (int32_t)i : -1, ids[i], (int32_t)(e - i), locs[i],
+                             (int16_t)(write_loc ? dir : 0), (int16_t)(stamp ? 1 : 0)});
+    i = e;
+  }
+}
+
+// The copies between the pool and an image: per layer and part, the blocks
+// (ids, CSA entries at locs) in table order, then the window ring pieces.
+// to_image: pool -> image, else image -> pool.
+void image_segments(const kvpool_t* p, const std::vector<int32_t>& ids, const std::vector<int32_t>& locs, int32_t slot,
+                    int64_t n_tokens, int64_t w, uint64_t image, bool to_image, std::vector<ImageSeg>* segs) {
   const int64_t nb = (int64_t)ids.size();
   const PoolDesc& pd = p->lay.pd;
-  int64_t img = kImageHeader;
-  auto add_part = [&](int64_t pool, int64_t stride, int32_t mask_valid) {
-    for (int64_t b = 0; b < nb;) {
-      int64_t e = b + 1;
-      while (e < nb && ids[e] == ids[e - 1] + 1) ++e;
-      ImageSeg g{};
-      g.dev = pool + (int64_t)ids[b] * stride;
-      g.img = img + b * stride;
-      g.bytes = (e - b) * stride;
-      g.mask_row = mask_valid > 0 ? (int32_t)stride : 0;
-      g.mask_valid = mask_valid;
-      segs->push_back(g);
-      b = e;
-    }
-    img += nb * stride;
+  const uint64_t arena = reinterpret_cast<uint64_t>(p->arena);
+  uint64_t img = image + kImageHeader;
+  auto add = [&](uint64_t pool_addr, bool pool_host, int64_t bytes, int32_t mask_row, int32_t mask_valid) {
+    if (to_image) add_copy(segs, pool_addr, img, bytes, pool_host, mask_row, mask_valid);
+    else add_copy(segs, img, pool_addr, bytes, true);
+    img += bytes;
   };
   const bool idx_scaled = pd.idx_dtype == KVPOOL_FP8_E4M3 || pd.idx_dtype == KVPOOL_FP4_E2M1;
   for (int l = 0; l < p->cfg.n_layers; ++l) {
     const LayerDesc& d = p->lay.layers[l];
     if (d.has_csa) {
-      add_part(d.csa_pool, d.csa_stride, 0);
+      for (int64_t b = 0; b < nb; ++b) add(p->csa_addr(d, locs[b]), locs[b] < 0, d.csa_stride, 0, 0);
       const int64_t valid = d.idx_scale_off + 2LL * pd.csa_per_block;
-      add_part(d.idx_pool, d.idx_stride, idx_scaled && valid < d.idx_stride ? (int32_t)valid : 0);
+      const int32_t mvalid = idx_scaled && valid < d.idx_stride ? (int32_t)valid : 0;
+      for (int64_t b = 0; b < nb; ++b)
+        add(arena + d.idx_pool + (uint64_t)ids[b] * d.idx_stride, false, d.idx_stride, mvalid ? (int32_t)d.idx_stride : 0,
+            mvalid);
     }
-    if (d.has_hca) add_part(d.hca_pool, d.hca_stride, 0);
+    if (d.has_hca)
+      for (int64_t b = 0; b < nb; ++b) add(arena + d.hca_pool + (uint64_t)ids[b] * d.hca_stride, false, d.hca_stride, 0, 0);
   }
   for (int l = 0; l < p->cfg.n_layers && w > 0; ++l) {
     const LayerDesc& d = p->lay.layers[l];
-    const int64_t ring = d.ring + (int64_t)slot * d.ring_req_bytes;
+    const uint64_t ring = arena + d.ring + (uint64_t)slot * d.ring_req_bytes;
     const int64_t s0 = (n_tokens - w) % pd.n_win;
     const int64_t first = std::min<int64_t>(w, pd.n_win - s0);
-    segs->push_back(ImageSeg{ring + s0 * pd.entry_bytes, img, first * pd.entry_bytes, 0, 0});
-    if (w > first) segs->push_back(ImageSeg{ring, img + first * pd.entry_bytes, (w - first) * pd.entry_bytes, 0, 0});
-    img += w * pd.entry_bytes;
+    add(ring + (uint64_t)s0 * pd.entry_bytes, false, first * pd.entry_bytes, 0, 0);
+    if (w > first) add(ring, false, (w - first) * pd.entry_bytes, 0, 0);
   }
 }
 
-// Launch the copies in batches of kMaxImageSegs segments and kMaxImageRuns
-// table runs.
-int launch_image_copies(kvpool_t* p, uint8_t* d_image, bool to_image, int32_t dst, const std::vector<ImageSeg>& segs,
-                        const std::vector<ImageRun>& runs, int64_t bytes, void* stream) {
+// Launch the copies in batches of kMaxImageSegs copies and kMaxImageRuns
+// bookkeeping runs.
+int launch_block_copies(kvpool_t* p, int32_t dst, const std::vector<ImageSeg>& segs, const std::vector<ImageRun>& runs,
+                        int64_t bytes, void* stream) {
   const size_t n_launch = std::max((segs.size() + kMaxImageSegs - 1) / kMaxImageSegs,
                                    (runs.size() + kMaxImageRuns - 1) / kMaxImageRuns);
   for (size_t i = 0; i < n_launch; ++i) {
     ImageParams ip{};
     ip.pool = p->lay.pd;
-    ip.image = d_image;
-    ip.to_image = to_image ? 1 : 0;
     ip.dst = dst;
+    ip.epoch = p->epoch;
     const size_t s0 = i * kMaxImageSegs, s1 = std::min(segs.size(), s0 + kMaxImageSegs);
     ip.n_segs = s1 > s0 ? (int32_t)(s1 - s0) : 0;
     int64_t pieces = 0;
@@ -625,6 +693,33 @@ uint8_t* host_alias(const void* h) {
   }
   if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
   return static_cast<uint8_t*>(a.devicePointer);
+}
+
+// distinct live block ids, all resident (want_hot) or all offloaded
+bool hisparse_ids_ok(const kvpool_t* p, int32_t n, const int32_t* ids, bool want_hot) {
+  if (!p->hisparse() || n < 0 || (n > 0 && !ids)) return false;
+  std::set<int32_t> seen;
+  for (int32_t i = 0; i < n; ++i) {
+    const int32_t b = ids[i];
+    if (b < 0 || b >= p->cfg.max_blocks || p->refcount[b] == 0) return false;
+    if ((p->loc[b] >= 0) != want_hot || !seen.insert(b).second) return false;
+  }
+  return true;
+}
+
+// Move blocks' CSA entries to new locations (host slots or GPU slots).
+int move_blocks(kvpool_t* p, int32_t n, const int32_t* ids, const std::vector<int32_t>& to, bool stamp, void* stream) {
+  if (!p->device() || n == 0) return 0;
+  std::vector<ImageSeg> segs;
+  for (int l = 0; l < p->cfg.n_layers; ++l) {
+    const LayerDesc& d = p->lay.layers[l];
+    if (!d.has_csa) continue;
+    for (int32_t i = 0; i < n; ++i)
+      add_copy(&segs, p->csa_addr(d, p->loc[ids[i]]), p->csa_addr(d, to[i]), d.csa_stride, p->loc[ids[i]] < 0);
+  }
+  std::vector<ImageRun> runs;
+  add_runs(&runs, std::vector<int32_t>(ids, ids + n), to, -1, true, stamp);
+  return launch_block_copies(p, 0, segs, runs, (int64_t)n * p->lay.pd.host_slot_bytes, stream);
 }
 
 }  // namespace
@@ -675,10 +770,11 @@ int kvpool_export_prefix(kvpool_t* p, int32_t req, int64_t n_tokens, uint32_t fl
   put_le(h + 48, (uint64_t)total, 8);
   if (!p->device()) return KVPOOL_OK;  // bookkeeping-only pool: the header alone
 
-  std::vector<int32_t> ids(q.table.begin(), q.table.begin() + nb);
+  std::vector<int32_t> ids(q.table.begin(), q.table.begin() + nb), locs(nb);
+  for (int64_t b = 0; b < nb; ++b) locs[b] = p->loc[ids[b]];
   std::vector<ImageSeg> segs;
-  image_segments(p, ids, req, n_tokens, w, &segs);
-  const int rc = launch_image_copies(p, d_image, true, req, segs, {}, block_sec + win_sec, stream);
+  image_segments(p, ids, locs, req, n_tokens, w, reinterpret_cast<uint64_t>(d_image), true, &segs);
+  const int rc = launch_block_copies(p, req, segs, {}, block_sec + win_sec, stream);
   if (rc != 0) return p->cuda_fail((cudaError_t)rc, "export_prefix launch");
   return KVPOOL_OK;
 }
@@ -712,30 +808,30 @@ int kvpool_import_prefix(kvpool_t* p, int32_t dst, const void* h_image, int64_t 
       ((reinterpret_cast<uintptr_t>(d_win_k) | reinterpret_cast<uintptr_t>(d_win_v)) % 16) != 0)
     return p->fail(KVPOOL_ERR_INVALID_ARG, "import_prefix: window not 16-byte aligned");
   if (nb > p->cfg.max_blocks_per_request) return p->fail(KVPOOL_ERR_CAPACITY, "import_prefix: prefix too long");
-  if (nb > (int64_t)p->free_blocks.size()) return p->fail(KVPOOL_ERR_OUT_OF_BLOCKS, "import_prefix: out of blocks");
+  if (nb > (int64_t)p->free_blocks.size() || (p->hisparse() && nb > (int64_t)p->hot_free.size()))
+    return p->fail(KVPOOL_ERR_OUT_OF_BLOCKS, "import_prefix: out of blocks");
   if (reinterpret_cast<uintptr_t>(h_image) % 16 != 0)
     return p->fail(KVPOOL_ERR_INVALID_ARG, "import_prefix: image not 16-byte aligned");
   uint8_t* d_image = nullptr;
   if (p->device() && !(d_image = host_alias(h_image)))
     return p->fail(KVPOOL_ERR_INVALID_ARG, "import_prefix: image is not page-locked host memory");
 
-  // the smallest free ids, in image order (not yet taken: a failed launch leaves the pool unchanged)
-  std::vector<int32_t> ids;
-  ids.reserve(nb);
+  // the smallest free ids (and GPU slots), in image order; taken only once
+  // the launches succeeded, so an error leaves the pool unchanged
+  std::vector<int32_t> ids, locs;
   auto it = p->free_blocks.begin();
-  for (int64_t b = 0; b < nb; ++b, ++it) ids.push_back(*it);
+  auto ht = p->hot_free.begin();
+  for (int64_t b = 0; b < nb; ++b, ++it) {
+    ids.push_back(*it);
+    locs.push_back(p->hisparse() ? *ht++ : *it);
+  }
   if (p->device()) {
     std::vector<ImageSeg> segs;
-    image_segments(p, ids, dst, n_tokens, w, &segs);
+    image_segments(p, ids, locs, dst, n_tokens, w, reinterpret_cast<uint64_t>(d_image), false, &segs);
     std::vector<ImageRun> runs;
-    for (int64_t b = 0; b < nb;) {
-      int64_t e = b + 1;
-      while (e < nb && ids[e] == ids[e - 1] + 1) ++e;
-      runs.push_back(ImageRun{(int32_t)b, ids[b], (int32_t)(e - b)});
-      b = e;
-    }
+    add_runs(&runs, ids, locs, 0, p->hisparse(), p->hisparse());
     const int64_t moved = nb * image_block_bytes(p) + w * p->lay.pd.entry_bytes * p->cfg.n_layers;
-    int rc = launch_image_copies(p, d_image, false, dst, segs, runs, moved, stream);
+    int rc = launch_block_copies(p, dst, segs, runs, moved, stream);
     if (rc == 0 && zero_swa) {  // Zero SWA: the recomputed window through the cache encoding
       ShareParams sp{};
       sp.pool = p->lay.pd;
@@ -751,13 +847,124 @@ int kvpool_import_prefix(kvpool_t* p, int32_t dst, const void* h_image, int64_t 
     }
     if (rc != 0) return p->cuda_fail((cudaError_t)rc, "import_prefix launch");
   }
-  for (int32_t id : ids) {
-    p->free_blocks.erase(id);
-    p->refcount[id] = 1;
+  for (int64_t b = 0; b < nb; ++b) {
+    p->free_blocks.erase(ids[b]);
+    if (p->hisparse()) p->hot_free.erase(locs[b]);
+    p->refcount[ids[b]] = 1;
+    p->loc[ids[b]] = locs[b];
   }
   d.table = ids;
   d.length = n_tokens;
   return KVPOOL_OK;
+}
+
+// ---- HiSparse ----
+int64_t kvpool_host_slot_bytes(const kvpool_t* p) { return p ? p->lay.pd.host_slot_bytes : -1; }
+
+int kvpool_set_host_pool(kvpool_t* p, void* h_pool, int64_t bytes) {
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  if (!p->hisparse()) return p->fail(KVPOOL_ERR_INVALID_ARG, "set_host_pool: HiSparse is off");
+  if (!h_pool || bytes < (int64_t)p->cfg.csa_host_slots * p->lay.pd.host_slot_bytes ||
+      reinterpret_cast<uintptr_t>(h_pool) % 16 != 0)
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "set_host_pool: too small or not 16-byte aligned");
+  if ((int32_t)p->host_free.size() != p->cfg.csa_host_slots)
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "set_host_pool: blocks are offloaded to the current pool");
+  uint8_t* d = nullptr;
+  if (p->device() && !(d = host_alias(h_pool)))
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "set_host_pool: not page-locked host memory");
+  p->host_pool = d;
+  p->host_pool_bytes = bytes;
+  p->lay.pd.host_pool = d;
+  p->lay.pd.host_pool_bytes = bytes;
+  return KVPOOL_OK;
+}
+
+int kvpool_offload(kvpool_t* p, int32_t n, const int32_t* h_ids, void* stream) {
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  if (!hisparse_ids_ok(p, n, h_ids, true)) return p->fail(KVPOOL_ERR_INVALID_ARG, "offload: bad block ids");
+  if (p->device() && !p->host_pool) return p->fail(KVPOOL_ERR_INVALID_ARG, "offload: no host pool");
+  if (n > (int32_t)p->host_free.size()) return p->fail(KVPOOL_ERR_OUT_OF_BLOCKS, "offload: out of host slots");
+  std::vector<int32_t> to;
+  auto it = p->host_free.begin();
+  for (int32_t i = 0; i < n; ++i, ++it) to.push_back(-1 - *it);
+  const int rc = move_blocks(p, n, h_ids, to, false, stream);
+  if (rc != 0) return p->cuda_fail((cudaError_t)rc, "offload launch");
+  for (int32_t i = 0; i < n; ++i) {
+    p->host_free.erase(-1 - to[i]);
+    p->release_loc(p->loc[h_ids[i]]);
+    p->loc[h_ids[i]] = to[i];
+  }
+  return KVPOOL_OK;
+}
+
+int kvpool_fetch(kvpool_t* p, int32_t n, const int32_t* h_ids, void* stream) {
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  if (!hisparse_ids_ok(p, n, h_ids, false)) return p->fail(KVPOOL_ERR_INVALID_ARG, "fetch: bad block ids");
+  if (n > (int32_t)p->hot_free.size()) return p->fail(KVPOOL_ERR_OUT_OF_BLOCKS, "fetch: out of GPU slots");
+  std::vector<int32_t> to;
+  auto it = p->hot_free.begin();
+  for (int32_t i = 0; i < n; ++i, ++it) to.push_back(*it);
+  const int rc = move_blocks(p, n, h_ids, to, true, stream);
+  if (rc != 0) return p->cuda_fail((cudaError_t)rc, "fetch launch");
+  for (int32_t i = 0; i < n; ++i) {
+    p->hot_free.erase(to[i]);
+    p->release_loc(p->loc[h_ids[i]]);
+    p->loc[h_ids[i]] = to[i];
+  }
+  return KVPOOL_OK;
+}
+
+int kvpool_block_location(const kvpool_t* p, int32_t b, int32_t* loc) {
+  if (!p || !loc || b < 0 || b >= p->cfg.max_blocks || p->refcount[b] == 0) return KVPOOL_ERR_INVALID_ARG;
+  *loc = p->loc[b];
+  return KVPOOL_OK;
+}
+
+uint32_t kvpool_epoch(const kvpool_t* p) { return p ? p->epoch : 0; }
+
+}  // extern "C"
+
+namespace {
+// every block's activity stamp, read back after synchronizing the stream
+int read_activity(kvpool_t* p, std::vector<uint32_t>* out, void* stream) {
+  out->assign(p->cfg.max_blocks, 0);
+  cudaError_t e = cudaMemcpyAsync(out->data(), p->arena + p->lay.pd.last_used, 4ull * p->cfg.max_blocks,
+                                  cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  return (int)e;
+}
+}  // namespace
+
+extern "C" {
+
+int kvpool_block_activity(kvpool_t* p, int32_t n, const int32_t* h_ids, uint32_t* h_last_used, void* stream) {
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  if (!p->hisparse() || !p->device() || n < 0 || (n > 0 && (!h_ids || !h_last_used)))
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "block_activity: bad arguments");
+  for (int32_t i = 0; i < n; ++i)
+    if (h_ids[i] < 0 || h_ids[i] >= p->cfg.max_blocks || p->refcount[h_ids[i]] == 0)
+      return p->fail(KVPOOL_ERR_INVALID_ARG, "block_activity: a free block");
+  std::vector<uint32_t> a;
+  const int rc = read_activity(p, &a, stream);
+  if (rc != 0) return p->cuda_fail((cudaError_t)rc, "block_activity");
+  for (int32_t i = 0; i < n; ++i) h_last_used[i] = a[h_ids[i]];
+  return KVPOOL_OK;
+}
+
+int32_t kvpool_inactive_blocks(kvpool_t* p, uint32_t idle, int32_t* h_ids, int32_t cap, void* stream) {
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  if (!p->hisparse() || !p->device() || cap < 0 || (cap > 0 && !h_ids))
+    return p->fail(KVPOOL_ERR_INVALID_ARG, "inactive_blocks: bad arguments");
+  std::vector<uint32_t> a;
+  const int rc = read_activity(p, &a, stream);
+  if (rc != 0) return p->cuda_fail((cudaError_t)rc, "inactive_blocks");
+  int32_t n = 0;
+  for (int32_t b = 0; b < p->cfg.max_blocks; ++b) {
+    if (p->refcount[b] == 0 || p->loc[b] < 0 || p->epoch - a[b] < idle) continue;
+    if (n < cap) h_ids[n] = b;
+    ++n;
+  }
+  return n;
 }
 
 int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_t* h_n_new, const void* d_k,
@@ -784,16 +991,19 @@ int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_
   if (p->device() && ((reinterpret_cast<uintptr_t>(d_k) | reinterpret_cast<uintptr_t>(d_v) |
                        reinterpret_cast<uintptr_t>(d_idx_k)) % 16) != 0)
     return p->fail(KVPOOL_ERR_INVALID_ARG, "append: inputs must be 16-byte aligned");
-  if (seals > (int64_t)p->free_blocks.size()) return p->fail(KVPOOL_ERR_OUT_OF_BLOCKS, "append: out of blocks");
+  if (seals > (int64_t)p->free_blocks.size() || (p->hisparse() && seals > (int64_t)p->hot_free.size()))
+    return p->fail(KVPOOL_ERR_OUT_OF_BLOCKS, "append: out of blocks");
 
-  // reserve block ids: smallest free, requests in batch order, then positions
-  std::vector<std::vector<int32_t>> new_ids(n);
+  // reserve block ids: smallest free, requests in batch order, then positions;
+  // with HiSparse each also takes the smallest free GPU slot for its CSA entries
+  std::vector<std::vector<int32_t>> new_ids(n), new_locs(n);
   for (int i = 0; i < n; ++i) {
     const int64_t L0 = p->reqs[h_req_ids[i]].length, L1 = L0 + h_n_new[i];
     for (int64_t s = L0 / mp; s < L1 / mp; ++s) {
       const int32_t id = *p->free_blocks.begin();
       p->free_blocks.erase(p->free_blocks.begin());
       new_ids[i].push_back(id);
+      new_locs[i].push_back(p->take_hot(id));
     }
   }
 
@@ -819,6 +1029,7 @@ int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_
         u.ring_from = (int16_t)(std::min<int64_t>(std::max(ring_from_abs, a), b) - s * mp);
         u.in_row = (int32_t)(row + (a - L0));
         u.block_id = (s < L1 / mp) ? new_ids[i][(size_t)(s - L0 / mp)] : -1;
+        u.csa_slot = (s < L1 / mp) ? new_locs[i][(size_t)(s - L0 / mp)] : -1;
         (split && s == s_first ? phase1 : phase2).push_back(u);
       }
       row += h_n_new[i];
@@ -831,6 +1042,7 @@ int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_
     ap->idx_k = d_idx_k;
     ap->rows = T;
     ap->n_slices = append_slices(p->lay.pd);
+    ap->epoch = p->epoch;
     // algorithmic bytes: inputs read + window tokens and new entries written
     const PoolDesc& pd = p->lay.pd;
     const int64_t fp8 = pd.cache_dtype == KVPOOL_FP8_E4M3 ? 1 : 0;
@@ -859,12 +1071,16 @@ int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_
   if (rc != 0) {  // undo the reservation: nothing changes on error
     for (auto& v : new_ids)
       for (int32_t id : v) p->free_blocks.insert(id);
+    for (auto& v : new_locs)
+      for (int32_t l : v) p->release_loc(l);
     return p->cuda_fail((cudaError_t)rc, "append launch");
   }
   for (int i = 0; i < n; ++i) {
     Request& q = p->reqs[h_req_ids[i]];
-    for (int32_t id : new_ids[i]) {
+    for (size_t j = 0; j < new_ids[i].size(); ++j) {
+      const int32_t id = new_ids[i][j];
       p->refcount[id] = 1;
+      p->loc[id] = new_locs[i][j];
       q.table.push_back(id);
     }
     q.length += h_n_new[i];
@@ -895,11 +1111,13 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
   const int max_split_len = attend_max_split_len();
   AttendParams* ap = new AttendParams();
   int rc = 0;
+  p->epoch += 1;  // this call's epoch (HiSparse activity)
   for (int g0 = 0; g0 < n && rc == 0; g0 += kMaxAttendReqs) {
     const int gn = std::min(kMaxAttendReqs, n - g0);
     AttendParams& P = *ap;
     P.pool = pd;
     P.layer = Ld;
+    P.epoch = p->epoch;
     P.q = d_q;
     P.q_idx = d_q_idx;
     P.out = d_out;
@@ -1030,6 +1248,7 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
     if (rc == 0) rc = p->launch(KVPOOL_KERNEL_COMBINE, out_bytes, stream, [&](int* nk) { return launch_combine(P, stream, nk); });
   }
   delete ap;
+  if (rc != 0) p->epoch -= 1;
   if (rc == -1) return KVPOOL_ERR_INVALID_ARG;
   if (rc != 0) return p->cuda_fail((cudaError_t)rc, "decode_attend launch");
   return KVPOOL_OK;
@@ -1068,6 +1287,11 @@ int kvpool_get_layout(const kvpool_t* p, kvpool_layout* out, int32_t layer, kvpo
   out->table_offset = L.pd.table;
   out->error_offset = L.pd.err;
   out->total_bytes = L.total;
+  out->csa_staging_base = L.pd.csa_staging_base;
+  out->csa_hot_slots = p->cfg.csa_hot_slots;
+  out->host_slot_bytes = L.pd.host_slot_bytes;
+  out->csa_loc_offset = L.pd.csa_loc;
+  out->activity_offset = L.pd.last_used;
   if (lo) {
     if (layer < 0 || layer >= p->cfg.n_layers) return KVPOOL_ERR_INVALID_ARG;
     const LayerDesc& d = L.layers[layer];
@@ -1084,6 +1308,7 @@ int kvpool_get_layout(const kvpool_t* p, kvpool_layout* out, int32_t layer, kvpo
     lo->ring_request_bytes = d.ring_req_bytes;
     lo->acc_offset = d.acc;
     lo->acc_request_bytes = d.acc_req_bytes;
+    lo->csa_host_offset = d.csa_host_off;
   }
   return KVPOOL_OK;
 }

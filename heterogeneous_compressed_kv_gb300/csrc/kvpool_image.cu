@@ -1,9 +1,11 @@
-// kvpool_image.cu -- prefix images: copies between the arena (block part
-// planes, window rings, the block table) and a page-locked host image read
-// or written over the host link ("Ch 12 Inference framework: heterogeneous KV
+// kvpool_image.cu -- block copies between the arena (block part planes,
+// window rings) and page-locked host memory read or written over the host
+// link: prefix images ("Ch 12 Inference framework: heterogeneous KV
 // scheduling" s3: the compressed block cache restored by an async copy
 // instead of a prefill; "V4 disk prefix cache": the window stored or not per
-// SWA policy).
+// SWA policy) and HiSparse offload / fetch of CSA entries ("V4 KV Layout"
+// ESS / HiSparse table), with the moved blocks' table, location and activity
+// writes.
 #include "device_util.cuh"
 
 namespace kvp {
@@ -32,15 +34,20 @@ __global__ void __launch_bounds__(kImageThreads) image_copy_kernel(const __grid_
   pdl_start();
   const PoolDesc& pd = P.pool;
   const int tid = threadIdx.x;
-  if (!P.to_image) {  // the imported blocks' ids into dst's table row
-    int32_t* row = reinterpret_cast<int32_t*>(pd.arena + pd.table) + (int64_t)P.dst * pd.max_bpr;
-    for (int r = blockIdx.x; r < P.n_runs; r += gridDim.x) {
-      const ImageRun u = P.runs[r];
-      if (u.b0 < 0 || u.cnt < 0 || u.b0 + u.cnt > pd.max_bpr || u.id0 < 0 || u.id0 + u.cnt > pd.max_blocks) {
-        if (tid == 0) flag_error(pd, kErrBadBlock);
-        continue;
-      }
-      for (int i = tid; i < u.cnt; i += blockDim.x) row[u.b0 + i] = u.id0 + i;
+  // bookkeeping of the moved blocks: table row, locations, activity stamps
+  int32_t* row = reinterpret_cast<int32_t*>(pd.arena + pd.table) + (int64_t)P.dst * pd.max_bpr;
+  int32_t* loc = reinterpret_cast<int32_t*>(pd.arena + pd.csa_loc);
+  uint32_t* stamp = reinterpret_cast<uint32_t*>(pd.arena + pd.last_used);
+  for (int r = blockIdx.x; r < P.n_runs; r += gridDim.x) {
+    const ImageRun u = P.runs[r];
+    if (u.cnt < 0 || u.id0 < 0 || u.id0 + u.cnt > pd.max_blocks || (u.b0 >= 0 && u.b0 + u.cnt > pd.max_bpr)) {
+      if (tid == 0) flag_error(pd, kErrBadBlock);
+      continue;
+    }
+    for (int i = tid; i < u.cnt; i += blockDim.x) {
+      if (u.b0 >= 0) row[u.b0 + i] = u.id0 + i;
+      if (u.loc_dir != 0) loc[u.id0 + i] = u.loc0 + i * u.loc_dir;
+      if (u.stamp) stamp[u.id0 + i] = P.epoch;
     }
   }
   for (int64_t piece = blockIdx.x; piece < P.n_pieces; piece += gridDim.x) {
@@ -53,20 +60,20 @@ __global__ void __launch_bounds__(kImageThreads) image_copy_kernel(const __grid_
     const ImageSeg& S = P.segs[lo];
     const int64_t off0 = (piece - P.piece_base[lo]) * kImagePieceBytes;
     const int64_t n = min((int64_t)kImagePieceBytes, S.bytes - off0);
-    const uint8_t* src = P.to_image ? pd.arena + S.dev + off0 : P.image + S.img + off0;
-    uint8_t* dst = P.to_image ? P.image + S.img + off0 : pd.arena + S.dev + off0;
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(S.src) + off0;
+    uint8_t* dst = reinterpret_cast<uint8_t*>(S.dst) + off0;
     uint4 v[kUnitsPerThread];
 #pragma unroll
     for (int k = 0; k < kUnitsPerThread; ++k) {
       const int64_t u = (int64_t)(k * kImageThreads + tid) * 16;
-      if (u < n) v[k] = P.to_image ? ld_stream16(src + u) : *reinterpret_cast<const uint4*>(src + u);
+      if (u < n) v[k] = S.src_host ? *reinterpret_cast<const uint4*>(src + u) : ld_stream16(src + u);
     }
 #pragma unroll
     for (int k = 0; k < kUnitsPerThread; ++k) {
       const int64_t u = (int64_t)(k * kImageThreads + tid) * 16;
       if (u < n) {
         uint4 x = v[k];
-        if (P.to_image && S.mask_row > 0) {
+        if (S.mask_row > 0) {
           const int r = (int)((off0 + u) % S.mask_row);
           if (r + 16 > S.mask_valid) x = zero_tail(x, S.mask_valid - r);
         }

@@ -38,6 +38,7 @@ struct LayerDesc {
   int64_t ring, ring_req_bytes;
   int64_t acc, acc_req_bytes;  // acc: CSA [2HD] f32, idx [XD] f32, HCA [2HD] f32
   int64_t alpha_csa, alpha_hca, alpha_idx;  // f32 [H][m], [H][m'], [Ih][m]
+  int64_t csa_host_off;  // HiSparse: this layer's CSA entries inside a host slot
 };
 
 // Everything a kernel needs to know about the pool (passed by value).
@@ -52,6 +53,13 @@ struct PoolDesc {
   int32_t max_blocks, max_requests, max_bpr, staging_base;
   int64_t table;  // int32 [max_requests][max_bpr]
   int64_t err;    // uint32
+  // HiSparse: CSA entries of a sealed block at its location (csa_loc[id]:
+  // >= 0 a CSA plane slot, < 0 host slot -1-loc); without it the location is
+  // the id.  Staging CSA slots start at csa_staging_base.
+  int32_t hisparse, csa_staging_base;
+  int64_t csa_loc, last_used;  // int32 / uint32 [max_blocks]
+  uint8_t* host_pool;          // device alias of the host slots (or null)
+  int64_t host_slot_bytes, host_pool_bytes;
 };
 
 // ---- append ---------------------------------------------------------------
@@ -65,6 +73,7 @@ struct AppendUnit {
   int16_t pad;
   int32_t in_row;    // input row of the token at t0
   int32_t block_id;  // id the segment seals into in this call, or -1
+  int32_t csa_slot;  // CSA plane slot of that block (its id without HiSparse)
 };
 
 struct AppendParams {
@@ -76,6 +85,7 @@ struct AppendParams {
   int64_t rows;  // T: rows per layer in the inputs
   int32_t n_units;
   int32_t n_slices;  // CTAs that split one unit's 2*H*d values
+  uint32_t epoch;    // HiSparse activity stamp of the blocks sealed here
   AppendUnit units[kMaxAppendUnits];
 };
 
@@ -90,20 +100,24 @@ struct ShareParams {
   int64_t n_tokens;
 };
 
-// ---- prefix images ----------------------------------------------------------
-// One contiguous copy between the arena and a host image: a run of adjacent
-// block ids of one part plane, or a piece of a window ring.  On export, the
-// bytes of each mask_row-long row from mask_valid on are written as zeros
-// (the padding after the indexer scales); mask_row 0 means no mask.
+// ---- block copies: prefix images, HiSparse offload and fetch ------------------
+// One contiguous copy: a run of adjacent block parts, a piece of a window
+// ring, between the arena, a host image and the host slots.  The bytes of
+// each mask_row-long row from mask_valid on are written as zeros (the
+// padding after the indexer scales, on export); mask_row 0 means no mask.
 struct ImageSeg {
-  int64_t dev;    // arena byte offset
-  int64_t img;    // image byte offset
-  int64_t bytes;  // multiple of 16
+  uint64_t src, dst;  // device addresses (a host buffer's device alias)
+  int64_t bytes;      // multiple of 16
   int32_t mask_row, mask_valid;
+  int32_t src_host;   // the source is host memory
+  int32_t pad;
 };
-// block ids of an import: table[dst][b0 + i] = id0 + i for i < cnt
+// bookkeeping writes for blocks id0 + i, i < cnt: table[dst][b0 + i] = id0 + i
+// (b0 >= 0), csa_loc[id0 + i] = loc0 + i * loc_dir (loc_dir != 0), and
+// last_used[id0 + i] = epoch (stamp)
 struct ImageRun {
-  int32_t b0, id0, cnt;
+  int32_t b0, id0, cnt, loc0;
+  int16_t loc_dir, stamp;
 };
 constexpr int kMaxImageSegs = 64;
 constexpr int kMaxImageRuns = 64;
@@ -111,9 +125,8 @@ constexpr int kImagePieceBytes = 16384;  // bytes one CTA copies per step
 
 struct ImageParams {
   PoolDesc pool;
-  uint8_t* image;      // device alias of the page-locked host image
-  int32_t to_image;    // 1: export (arena -> image), 0: import
-  int32_t dst;         // request slot whose table row the runs fill (import)
+  int32_t dst;         // request slot whose table row the runs fill
+  uint32_t epoch;      // activity stamp of the runs' blocks
   int32_t n_segs, n_runs;
   int64_t n_pieces;    // pieces of kImagePieceBytes over all segments
   int64_t piece_base[kMaxImageSegs + 1];  // first piece of each segment
@@ -149,6 +162,7 @@ struct AttendParams {
   float* out;
   int32_t* topk_out;
   int32_t top_k;
+  uint32_t epoch;            // HiSparse activity stamp of this call
   int32_t n;                 // requests in this launch
   int32_t row0;              // first row of q / out for this launch
   int32_t total_score_ctas, total_key_ctas;

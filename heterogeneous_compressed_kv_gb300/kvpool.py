@@ -29,7 +29,9 @@ EXPORTS = ["kvpool_required_bytes", "kvpool_create", "kvpool_destroy", "kvpool_a
            "kvpool_request_info", "kvpool_block_refcount", "kvpool_free_block_count", "kvpool_get_layout",
            "kvpool_check_device", "kvpool_profile_enable", "kvpool_profile_read", "kvpool_last_error",
            "kvpool_topk_static", "kvpool_profile_timeline", "kvpool_fingerprint", "kvpool_image_bytes",
-           "kvpool_export_prefix", "kvpool_import_prefix"]
+           "kvpool_export_prefix", "kvpool_import_prefix", "kvpool_host_slot_bytes", "kvpool_set_host_pool",
+           "kvpool_offload", "kvpool_fetch", "kvpool_block_location", "kvpool_epoch", "kvpool_block_activity",
+           "kvpool_inactive_blocks"]
 
 
 class KvpoolError(RuntimeError):
@@ -45,7 +47,8 @@ class _Config(C.Structure):
                 ("layer_kinds", C.POINTER(C.c_int32)), ("max_requests", C.c_int32), ("max_blocks", C.c_int32),
                 ("max_blocks_per_request", C.c_int32), ("max_batch", C.c_int32), ("max_top_k", C.c_int32),
                 ("gate_csa", C.POINTER(C.c_float)), ("gate_hca", C.POINTER(C.c_float)),
-                ("gate_idx", C.POINTER(C.c_float)), ("flags", C.c_uint32), ("idx_fp4", C.c_int32)]
+                ("gate_idx", C.POINTER(C.c_float)), ("flags", C.c_uint32), ("idx_fp4", C.c_int32),
+                ("csa_hot_slots", C.c_int32), ("csa_host_slots", C.c_int32)]
 
 
 class _Info(C.Structure):
@@ -56,14 +59,16 @@ class _Info(C.Structure):
 class _Layout(C.Structure):
     _fields_ = [("entry_bytes", C.c_int64), ("idx_entry_bytes", C.c_int64), ("csa_per_block", C.c_int32),
                 ("staging_base", C.c_int32), ("table_offset", C.c_int64), ("error_offset", C.c_int64),
-                ("total_bytes", C.c_int64)]
+                ("total_bytes", C.c_int64), ("csa_staging_base", C.c_int32), ("csa_hot_slots", C.c_int32),
+                ("host_slot_bytes", C.c_int64), ("csa_loc_offset", C.c_int64), ("activity_offset", C.c_int64)]
 
 
 class _LayerLayout(C.Structure):
     _fields_ = [("kind", C.c_int32), ("pad", C.c_int32), ("csa_offset", C.c_int64), ("csa_block_bytes", C.c_int64),
                 ("idx_offset", C.c_int64), ("idx_block_bytes", C.c_int64), ("idx_scale_offset", C.c_int64),
                 ("hca_offset", C.c_int64), ("hca_block_bytes", C.c_int64), ("ring_offset", C.c_int64),
-                ("ring_request_bytes", C.c_int64), ("acc_offset", C.c_int64), ("acc_request_bytes", C.c_int64)]
+                ("ring_request_bytes", C.c_int64), ("acc_offset", C.c_int64), ("acc_request_bytes", C.c_int64),
+                ("csa_host_offset", C.c_int64)]
 
 
 _lib = None
@@ -101,6 +106,17 @@ def lib():
         L.kvpool_image_bytes.argtypes = [vp, i64, C.c_uint32]
         L.kvpool_export_prefix.argtypes = [vp, i32, i64, C.c_uint32, vp, i64, vp]
         L.kvpool_import_prefix.argtypes = [vp, i32, vp, i64, vp, vp, vp]
+        L.kvpool_host_slot_bytes.restype = i64
+        L.kvpool_host_slot_bytes.argtypes = [vp]
+        L.kvpool_set_host_pool.argtypes = [vp, vp, i64]
+        L.kvpool_offload.argtypes = [vp, i32, vp, vp]
+        L.kvpool_fetch.argtypes = [vp, i32, vp, vp]
+        L.kvpool_block_location.argtypes = [vp, i32, C.POINTER(i32)]
+        L.kvpool_epoch.restype = C.c_uint32
+        L.kvpool_epoch.argtypes = [vp]
+        L.kvpool_block_activity.argtypes = [vp, i32, vp, vp, vp]
+        L.kvpool_inactive_blocks.restype = i32
+        L.kvpool_inactive_blocks.argtypes = [vp, C.c_uint32, vp, i32, vp]
         L.kvpool_last_error.restype = C.c_char_p
         L.kvpool_last_error.argtypes = [vp]
         _lib = L
@@ -133,6 +149,8 @@ class PoolConfig:
     gate_idx: np.ndarray  # [n_layers][idx_heads][m]
     flags: int = 0
     idx_fp4: int = 0  # 1: indexer entries in FP4 (e2m1 + one bf16 scale)
+    csa_hot_slots: int = 0  # HiSparse: GPU slots for sealed blocks' CSA entries (0 = off)
+    csa_host_slots: int = 0  # HiSparse: host slots for offloaded CSA entries
     _keep: list = field(default_factory=list, repr=False)
 
     def to_c(self) -> _Config:
@@ -145,7 +163,7 @@ class PoolConfig:
                        self.in_dtype, self.cache_dtype, kinds.size, kinds.ctypes.data_as(C.POINTER(C.c_int32)),
                        self.max_requests, self.max_blocks, self.max_blocks_per_request, self.max_batch,
                        self.max_top_k, g[0].ctypes.data_as(fp), g[1].ctypes.data_as(fp), g[2].ctypes.data_as(fp),
-                       self.flags, self.idx_fp4)
+                       self.flags, self.idx_fp4, self.csa_hot_slots, self.csa_host_slots)
 
 
 def required_bytes(cfg: PoolConfig) -> int:
@@ -264,6 +282,59 @@ class Pool:
         addr, nbytes = _host_buffer(image)
         rc = self.L.kvpool_import_prefix(self.h, dst, addr, nbytes, _ptr(win_k), _ptr(win_v), _stream(stream))
         return self._check(rc, "import_prefix") if check else rc
+
+    # ---- HiSparse: inactive CSA entries off the GPU ----
+    def host_slot_bytes(self) -> int:
+        return int(self.L.kvpool_host_slot_bytes(self.h))
+
+    def set_host_pool(self, pool=None, check=True):
+        """Give the pool its host slots (a page-locked uint8 host tensor; one is
+        allocated when None) and return it; the caller keeps it alive."""
+        if pool is None:
+            import torch
+            pool = torch.empty(max(self.cfg.csa_host_slots * self.host_slot_bytes(), 16), dtype=torch.uint8,
+                               pin_memory=True)
+        addr, nbytes = _host_buffer(pool)
+        rc = self.L.kvpool_set_host_pool(self.h, addr, nbytes)
+        if check:
+            self._check(rc, "set_host_pool")
+            self._host_pool = pool
+            return pool
+        return rc
+
+    def offload(self, block_ids, stream=None, check=True) -> int:
+        ids = _i32(block_ids)
+        rc = self.L.kvpool_offload(self.h, ids.size, ids.ctypes.data_as(C.c_void_p), _stream(stream))
+        return self._check(rc, "offload") if check else rc
+
+    def fetch(self, block_ids, stream=None, check=True) -> int:
+        ids = _i32(block_ids)
+        rc = self.L.kvpool_fetch(self.h, ids.size, ids.ctypes.data_as(C.c_void_p), _stream(stream))
+        return self._check(rc, "fetch") if check else rc
+
+    def block_location(self, block_id: int):
+        """(rc, loc): loc >= 0 a GPU slot, < 0 host slot -1 - loc."""
+        loc = C.c_int32()
+        rc = self.L.kvpool_block_location(self.h, block_id, C.byref(loc))
+        return rc, loc.value
+
+    def epoch(self) -> int:
+        return int(self.L.kvpool_epoch(self.h))
+
+    def block_activity(self, block_ids, stream=None) -> np.ndarray:
+        ids = _i32(block_ids)
+        out = np.zeros(max(ids.size, 1), np.uint32)
+        rc = self.L.kvpool_block_activity(self.h, ids.size, ids.ctypes.data_as(C.c_void_p),
+                                          out.ctypes.data_as(C.c_void_p), _stream(stream))
+        self._check(rc, "block_activity")
+        return out[:ids.size]
+
+    def inactive_blocks(self, idle: int, cap: int = 1 << 20, stream=None) -> np.ndarray:
+        ids = np.zeros(max(cap, 1), np.int32)
+        n = self.L.kvpool_inactive_blocks(self.h, idle, ids.ctypes.data_as(C.c_void_p), cap, _stream(stream))
+        if n < 0:
+            self._check(n, "inactive_blocks")
+        return ids[:min(n, cap)].copy()
 
     def append(self, req_ids, n_new, k, v, idx_k, stream=None, check=True) -> int:
         req, nn = _i32(req_ids), _i32(n_new)

@@ -119,6 +119,9 @@ typedef struct kvpool_config {
   int32_t idx_fp4;                /* 1: indexer entries in FP4 (KVPOOL_FP4_E2M1), 0: in cache_dtype.
                                      FP4 needs idx_heads * idx_dim to be a multiple of 32.  ([P3] s2.2
                                      gives the lightning indexer FP4 keys.) */
+  int32_t csa_hot_slots;          /* HiSparse: GPU slots for sealed blocks' CSA entries (0 = off: a
+                                     block's CSA entries stay with the block id; else <= max_blocks) */
+  int32_t csa_host_slots;         /* HiSparse: host slots for offloaded blocks' CSA entries (0 if off) */
 } kvpool_config;
 
 typedef struct kvpool kvpool_t;
@@ -225,6 +228,64 @@ int kvpool_export_prefix(kvpool_t* pool, int32_t req, int64_t n_tokens, uint32_t
 int kvpool_import_prefix(kvpool_t* pool, int32_t dst, const void* h_image, int64_t bytes, const void* d_win_k,
                          const void* d_win_v, void* stream);
 
+/* ---- HiSparse: inactive CSA entries off the GPU ----
+ * "V4 KV Layout: Classical + State dual pool" (ESS / HiSparse table: HiSparse
+ * moves inactive C4 entries of the Classical pool off the GPU, on top of the
+ * layout) and "Why does V4 split pools? ..." s1 / s3.2 (only full, immutable
+ * blocks move; the SWA window stays resident).  With csa_hot_slots > 0 a
+ * sealed block's CSA entries (every layer's) live in one of csa_hot_slots
+ * GPU slots or, once offloaded, in one of csa_host_slots slots of a
+ * caller-owned page-locked host pool; its indexer keys and HCA entry never
+ * move (the indexer scans every key, and every HCA entry is read, each step).
+ * Slots are taken smallest-free when a block seals, is restored or fetched
+ * (hot) and when it is offloaded (host); they return when the block is freed.
+ * Attention reads a selected entry of an offloaded block straight from host
+ * memory.  Activity: every kvpool_decode_attend call advances the pool's
+ * epoch by one; a call on a CSA layer stamps each block holding a selected
+ * entry with that epoch, and sealing, restoring or fetching a block stamps the
+ * current epoch.  A block is inactive after `idle` epochs without a stamp.
+ * Placement never changes a value: outputs are bit-identical whether or not
+ * blocks are offloaded.  All of this is in stream order on `stream`. */
+
+/* Bytes of one host slot: the CSA entries of one block over all CSA layers. */
+int64_t kvpool_host_slot_bytes(const kvpool_t* pool);
+
+/* Give the pool its host slots: h_pool page-locked (mapped) host memory of at
+ * least csa_host_slots * kvpool_host_slot_bytes bytes, 16-byte aligned,
+ * owned by the caller and kept until kvpool_destroy.  Needed before the first
+ * offload.  Errors: INVALID_ARG (HiSparse off, too small, not page-locked or
+ * aligned, already set while blocks are offloaded). */
+int kvpool_set_host_pool(kvpool_t* pool, void* h_pool, int64_t bytes);
+
+/* Move the CSA entries of the resident sealed blocks h_ids[0..n) to host
+ * slots (taken in the given order), freeing their GPU slots.  Errors:
+ * INVALID_ARG (HiSparse off, no host pool, an id that is free, offloaded or
+ * repeated), OUT_OF_BLOCKS (too few free host slots), CUDA; an error changes
+ * nothing. */
+int kvpool_offload(kvpool_t* pool, int32_t n, const int32_t* h_ids, void* stream);
+
+/* Bring offloaded blocks back to GPU slots (and stamp them).  Errors:
+ * INVALID_ARG (an id that is free, resident or repeated), OUT_OF_BLOCKS (too
+ * few free GPU slots), CUDA. */
+int kvpool_fetch(kvpool_t* pool, int32_t n, const int32_t* h_ids, void* stream);
+
+/* Where block id's CSA entries are (host bookkeeping, no synchronization):
+ * *loc >= 0 a GPU slot, < 0 host slot -1 - *loc (without HiSparse *loc is
+ * the id).  Errors: INVALID_ARG (a free block). */
+int kvpool_block_location(const kvpool_t* pool, int32_t block_id, int32_t* loc);
+
+/* Decode calls so far (the current epoch). */
+uint32_t kvpool_epoch(const kvpool_t* pool);
+
+/* Synchronize `stream` and write the activity stamps of blocks h_ids[0..n)
+ * to h_last_used.  Errors: INVALID_ARG (HiSparse off, a free block), CUDA. */
+int kvpool_block_activity(kvpool_t* pool, int32_t n, const int32_t* h_ids, uint32_t* h_last_used, void* stream);
+
+/* Synchronize `stream` and list the resident sealed blocks with epoch -
+ * stamp >= idle, ascending ids, up to cap of them into h_ids; returns how
+ * many there are (negative: an error: INVALID_ARG with HiSparse off, CUDA). */
+int32_t kvpool_inactive_blocks(kvpool_t* pool, uint32_t idle, int32_t* h_ids, int32_t cap, void* stream);
+
 /* Append new tokens ([P1] s3, s4): for request h_req_ids[i], h_n_new[i]
  * tokens.  d_k, d_v: [n_layers][T][heads][head_dim], d_idx_k:
  * [n_layers][T][idx_heads][idx_dim] (may be NULL when no layer has CSA), all
@@ -300,14 +361,19 @@ int kvpool_free_block_count(const kvpool_t* pool);
  *   + e) * 16 from idx_offset (chunk-major, so a warp reading chunk c of 32
  *   consecutive entries reads 512 contiguous bytes); fp8 scales [csa_per_block]
  *   bf16 at idx_scale_offset.
- * Block parts of a layer, each in its own plane indexed by block id b:
- *   CSA entries [csa_per_block] at csa_offset + b * csa_block_bytes, indexer
- *   keys (then fp8 scales at idx_scale_offset) at idx_offset + b *
- *   idx_block_bytes, the HCA entry at hca_offset + b * hca_block_bytes;
- *   absent parts have offset -1.  Ids staging_base + r (r a request slot)
- *   are request r's private staging blocks (its open block).  A request's
- *   blocks, allocated in order, make its indexer keys and HCA entries
- *   contiguous runs.
+ * Block parts of a layer, each in its own plane: CSA entries [csa_per_block]
+ *   at csa_offset + s * csa_block_bytes where s is the block's location (its
+ *   id without HiSparse, its GPU slot with it; an offloaded block's CSA
+ *   entries are at its host slot * host_slot_bytes + csa_host_offset in the
+ *   host pool), indexer keys (then fp8 / FP4 scales at idx_scale_offset) at
+ *   idx_offset + b * idx_block_bytes, the HCA entry at hca_offset + b *
+ *   hca_block_bytes, b the block id; absent parts have offset -1.  Ids
+ *   staging_base + r (r a request slot) are request r's private staging
+ *   blocks (its open block); its CSA staging slot is csa_staging_base + r.
+ *   A request's blocks, allocated in order, make its indexer keys and HCA
+ *   entries contiguous runs.
+ * HiSparse: int32 locations [max_blocks] at csa_loc_offset and uint32
+ *   activity stamps [max_blocks] at activity_offset.
  * Window of request r: ring_offset + r * ring_request_bytes, token at
  *   position p in slot p mod n_win.
  * Compressor accumulators of request r (fp32): acc_offset + r * acc_request_bytes:
@@ -321,6 +387,7 @@ typedef struct kvpool_layer_layout {
   int64_t hca_offset, hca_block_bytes;
   int64_t ring_offset, ring_request_bytes;
   int64_t acc_offset, acc_request_bytes;
+  int64_t csa_host_offset; /* this layer's CSA entries inside a host slot (-1 without CSA) */
 } kvpool_layer_layout;
 
 typedef struct kvpool_layout {
@@ -331,6 +398,10 @@ typedef struct kvpool_layout {
   int64_t table_offset;
   int64_t error_offset;    /* uint32 device error word */
   int64_t total_bytes;
+  int32_t csa_staging_base; /* CSA plane slot of request 0's staging block */
+  int32_t csa_hot_slots;    /* 0 without HiSparse */
+  int64_t host_slot_bytes;  /* 0 without HiSparse */
+  int64_t csa_loc_offset, activity_offset;
 } kvpool_layout;
 
 /* Layout of the pool and (if layer_out != NULL) of one layer. */

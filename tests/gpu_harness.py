@@ -39,13 +39,15 @@ class GpuCase:
                                 in_dtype=w["in_dtype"], cache_dtype=w["cache_dtype"], layer_kinds=w["layer_kinds"],
                                 max_requests=max_requests, max_blocks=max_blocks, max_blocks_per_request=mbpr,
                                 max_batch=max_batch, max_top_k=max_top_k, gate_csa=g[0], gate_hca=g[1],
-                                gate_idx=g[2], idx_fp4=w.get("idx_fp4", 0))
+                                gate_idx=g[2], idx_fp4=w.get("idx_fp4", 0), csa_hot_slots=w.get("csa_hot_slots", 0),
+                                csa_host_slots=w.get("csa_host_slots", 0))
         # indexer entries carry a bf16 scale when they are fp8 or fp4
         self.idx_scaled = w["cache_dtype"] == K.FP8_E4M3 or bool(w.get("idx_fp4", 0))
         nbytes = K.required_bytes(self.cfg)
         assert nbytes > 0
         self.arena = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
         self.pool = K.Pool(self.cfg, self.arena)
+        self.host_pool = self.pool.set_host_pool() if self.cfg.csa_host_slots > 0 else None
         self.nl = len(w["layer_kinds"])
         self.HD = w["heads"] * w["head_dim"]
         self.XD = w["idx_heads"] * w["idx_dim"]
@@ -115,10 +117,22 @@ class GpuCase:
         return int(ids[seg]) if seg < len(ids) else d["staging_base"] + slot
 
     def csa_entry(self, layer, slot, e, ids, host=None):
+        """A CSA entry where the block's location puts it: the staging slot, a
+        GPU slot, or (offloaded) a slot of the host pool."""
         d = self.pool.layout(layer)
         CB = d["csa_per_block"]
-        base = d["csa_offset"] + self._bid(d, slot, e, ids) * d["csa_block_bytes"]
-        return self.entry(base + (e % CB) * d["entry_bytes"], host)
+        seg = e // CB
+        if seg >= len(ids):
+            s_ = d["csa_staging_base"] + slot
+        else:
+            rc, s_ = self.pool.block_location(int(ids[seg]))
+            assert rc == 0
+        if s_ < 0:
+            torch.cuda.synchronize()
+            raw = self.host_pool.numpy()
+            off = (-1 - s_) * d["host_slot_bytes"] + d["csa_host_offset"] + (e % CB) * d["entry_bytes"]
+            return self.entry(off, raw)
+        return self.entry(d["csa_offset"] + s_ * d["csa_block_bytes"] + (e % CB) * d["entry_bytes"], host)
 
     def idx_entry(self, layer, slot, e, ids, host=None):
         d = self.pool.layout(layer)

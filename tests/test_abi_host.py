@@ -285,3 +285,79 @@ def test_image_import_refusals_match_oracle():
     assert o2.alloc_request()[1] == p2.alloc_request()
     assert o2.import_prefix(0, img, win, win) == p2.import_prefix(0, img, stream=0, check=False) == \
         K.ERR_CAPACITY
+
+
+def test_hisparse_bookkeeping_matches_oracle_under_random_traffic():
+    """GPU and host slots of sealed blocks (smallest free at seal, restore,
+    offload and fetch; returned when a block is freed) and every refusal
+    equal the oracle's."""
+    w = base_workload(heads=4, head_dim=64, idx_heads=1, idx_dim=16, m_prime=16, n_win=32)
+    w.update(csa_hot_slots=14, csa_host_slots=12)
+    o = H.make_oracle(w, 6, 24, 8)
+    p = K.Pool(cfg_of(w, max_requests=6, max_blocks=24, max_blocks_per_request=8, max_batch=6, csa_hot_slots=14,
+                      csa_host_slots=12))
+    rng = np.random.default_rng(21)
+    live = []
+    HD = 256
+    for step in range(400):
+        op = rng.integers(0, 12)
+        if op < 2:
+            rc1, r1 = o.alloc_request()
+            try:
+                rc2, r2 = 0, p.alloc_request()
+            except K.KvpoolError as e:
+                rc2, r2 = e.code, None
+            assert rc1 == rc2
+            if rc1 == 0:
+                assert r1 == r2
+                live.append(r1)
+        elif op < 3 and live:
+            r = live.pop(rng.integers(0, len(live)))
+            assert o.free_request(r) == 0
+            p.free_request(r)
+        elif op < 4 and len(live) >= 2:
+            src, dst = (int(x) for x in rng.choice(live, 2, replace=False))
+            n_tok = int(rng.integers(0, 4)) * 16
+            rc1, img = o.export_prefix(src, n_tok, 0, cap=1 << 22)
+            if rc1 == 0:
+                win = np.zeros((1, min(n_tok, 32), HD), np.float32)
+                assert o.import_prefix(dst, img, win, win) == p.import_prefix(dst, img, stream=0, check=False)
+        elif op < 6:  # offload or fetch some live blocks (sometimes refused)
+            ids = [b for b in range(24) if o.block_location(b)[0] == 0]
+            if ids:
+                pick = [int(x) for x in rng.choice(ids, min(len(ids), int(rng.integers(1, 5))), replace=False)]
+                if rng.random() < 0.1:
+                    pick.append(pick[0])  # repeated -> refused by both
+                if op == 4:
+                    assert o.offload(pick) == p.offload(pick, stream=0, check=False)
+                else:
+                    assert o.fetch(pick) == p.fetch(pick, stream=0, check=False)
+        elif live:
+            k = int(rng.integers(1, min(3, len(live)) + 1))
+            reqs = [int(x) for x in rng.choice(live, k, replace=False)]
+            counts = [int(x) for x in rng.integers(0, 40, len(reqs))]
+            T = sum(counts)
+            z = np.zeros((1, T, HD), np.float32)
+            assert o.append(reqs, counts, z, z, np.zeros((1, T, 16), np.float32)) == \
+                p.append(reqs, counts, None, None, None, stream=0, check=False)
+        for b in range(24):
+            rc1, l1, _ = o.block_location(b)
+            rc2, l2 = p.block_location(b)
+            assert rc1 == rc2 and (rc1 != 0 or l1 == l2), (step, b, rc1, rc2, l1, l2)
+        assert o.free_block_count() == p.free_block_count()
+
+
+def test_hisparse_refusals():
+    w = base_workload(m_prime=16, n_win=16, heads=4, head_dim=64, idx_dim=16)
+    for hot, host in ((-1, 0), (0, 4), (25, 0)):
+        cfg = cfg_of(w, max_blocks=24, csa_hot_slots=hot, csa_host_slots=host)
+        assert K.required_bytes(cfg) == 0
+    p = K.Pool(cfg_of(w, max_blocks=24))
+    assert p.offload([0], stream=0, check=False) == K.ERR_INVALID_ARG  # HiSparse off
+    assert p.set_host_pool(np.zeros(64, np.uint8), check=False) == K.ERR_INVALID_ARG
+    p = K.Pool(cfg_of(w, max_blocks=24, csa_hot_slots=8, csa_host_slots=4))
+    lay = p.layout(0)
+    assert p.host_slot_bytes() == lay["csa_block_bytes"] == 4 * 2048  # 4 CSA entries of 2 x 256 fp32
+    assert lay["csa_staging_base"] == 8 and lay["csa_hot_slots"] == 8
+    assert lay["host_slot_bytes"] == lay["csa_block_bytes"] and lay["csa_host_offset"] == 0
+    assert p.set_host_pool(np.zeros(16, np.uint8), check=False) == K.ERR_INVALID_ARG  # too small
