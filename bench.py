@@ -166,6 +166,8 @@ def config_block(w, args):
              cache_dtype={0: "f32", 1: "bf16", 2: "fp8_e4m3+bf16_scale"}[w["cache_dtype"]])
     if w.get("idx_fp4"):
         c["indexer_dtype"] = "fp4_e2m1+bf16_scale"
+    if getattr(args, "hisparse", 0) > 0:
+        c["hisparse_offloaded"] = args.hisparse
     if w["name"] == "long_context":
         c["context"] = w["length"]
     else:
@@ -342,7 +344,7 @@ def run_prefix_image(args):
         if it >= W_:
             t_exp.append(ev[0].elapsed_time(ev[1]))
             t_imp.append(ev[2].elapsed_time(ev[3]))
-        info_a, info_b = pool.request_info(a)[0], pool.request_info(b)[0]
+        info_a, info_b = pool.request_info(a)[1], pool.request_info(b)[1]
         assert info_a == info_b, (info_a, info_b)
         pool.free_request(b)
     clk = clocks.stop()
@@ -397,6 +399,8 @@ def main():
     ap.add_argument("--context", type=int, default=0, help="override the long-context length (profiling cases)")
     ap.add_argument("--timeline", type=int, default=0, help="print the launch timeline of this many extra steps")
     ap.add_argument("--idx-fp4", action="store_true", help="indexer entries in FP4 (e2m1 + one bf16 scale)")
+    ap.add_argument("--hisparse", type=float, default=0.0,
+                    help="HiSparse: offload this fraction of the sealed blocks' CSA entries to host memory first")
     ap.add_argument("--prefix-image", action="store_true",
                     help="time prefix image export / restore of one long-context request instead of decode steps")
     args = ap.parse_args()
@@ -446,8 +450,13 @@ def main():
                        max_blocks=sum((L + extra) // mp_ + 1 for L in lengths), max_blocks_per_request=mbpr,
                        max_batch=B, max_top_k=w["top_k"], gate_csa=g[0], gate_hca=g[1], gate_idx=g[2],
                        idx_fp4=w["idx_fp4"])
+    n_sealed = sum(L // mp_ for L in lengths)
+    if args.hisparse > 0:  # every block gets a GPU slot; a fraction moves to host slots after the prefill
+        cfg.csa_hot_slots = cfg.max_blocks
+        cfg.csa_host_slots = n_sealed
     arena = torch.empty(K.required_bytes(cfg), dtype=torch.uint8, device=dev)
     pool = K.Pool(cfg, arena, stream)
+    host_slots = pool.set_host_pool() if args.hisparse > 0 else None
     slots = [pool.alloc_request() for _ in range(B)]
     wids = replica_wids(rank, B)
     HD, XD = w["heads"] * w["head_dim"], w["idx_heads"] * w["idx_dim"]
@@ -474,6 +483,26 @@ def main():
     torch.cuda.synchronize()
     pool.check_device(sp)
     t_setup = time.perf_counter() - t_setup
+
+    # ---- HiSparse: offload an evenly spread fraction of every request's sealed blocks ----
+    hisparse = None
+    if args.hisparse > 0:
+        off = []
+        for s_ in slots:
+            ids = pool.request_info(s_)[2]
+            nb = len(ids)
+            off += [int(ids[j]) for j in range(nb) if int((j + 1) * args.hisparse) != int(j * args.hisparse)]
+        o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        o0.record(stream)
+        pool.offload(off, stream=sp)
+        o1.record(stream)
+        torch.cuda.synchronize()
+        pool.check_device(sp)
+        mv = len(off) * pool.host_slot_bytes()
+        hisparse = dict(fraction=args.hisparse, offloaded_blocks=len(off), sealed_blocks=n_sealed,
+                        offload_ms=o0.elapsed_time(o1), offload_gbs=mv / (o0.elapsed_time(o1) / 1e3) / 1e9,
+                        hbm_freed_gb=mv / 1e9,
+                        host_entry_bytes_per_step=round(args.hisparse * B * w["top_k"] * (2 * HD + 4)))
 
     # ---- step inputs, resident in HBM before timing ----
     S = 2 * (W_ + K_)  # device-timed steps then the end-to-end steps
@@ -630,6 +659,7 @@ def main():
                               peak_source=peak_kind,
                               bytes_per_launch=d_b / launches_dom, ms_per_launch=d_ms / launches_dom),
                 e2e=dict(value=e2e_value, unit="tokens/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
+                **({"hisparse": hisparse} if hisparse else {}),
                 gpu_launches=launches, setup_s=t_setup, clocks=clk)
     if cpu is not None:
         n_w, cpool, cres = cpu
