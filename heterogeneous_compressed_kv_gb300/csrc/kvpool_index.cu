@@ -460,8 +460,10 @@ __device__ __forceinline__ int load_items(const uint32_t* keys, int64_t my0, int
 // among the candidates (two more radix digits), how many keys equal to T are
 // taken, and every chunk's exclusive prefix of (keys > T, keys == T).  No
 // CTA waits on another: the last one is found with an atomic counter after a
-// fence.
-__global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __grid_constant__ AttendParams P) {
+// fence.  fused: every request of the launch has one chunk, so its only CTA
+// also writes the ordered selection (pass 2 is not launched).
+__global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __grid_constant__ AttendParams P,
+                                                                     int fused) {
   pdl_start();
   __shared__ uint32_t sh[kSelThreads];
   __shared__ uint32_t st[8];
@@ -471,6 +473,17 @@ __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __gri
   __shared__ int is_last;
   const int i = find_req(P, blockIdx.x, 1);
   const AttendReq& R = P.reqs[i];
+  int32_t* sel = P.sel + (int64_t)i * P.sel_stride;
+  int32_t* tko = P.topk_out ? P.topk_out + (int64_t)(P.row0 + i) * P.top_k : nullptr;
+  if (fused) {  // what pass 2 does for the requests that need no radix select
+    if (tko)
+      for (int j = R.k + threadIdx.x; j < P.top_k; j += blockDim.x) tko[j] = -1;
+    if (R.select_all)
+      for (int e = threadIdx.x; e < R.k; e += blockDim.x) {
+        sel[e] = e;
+        if (tko) tko[e] = e;
+      }
+  }
   if (R.select_all || R.k == 0) return;
   const int chunk = blockIdx.x - R.key_base;
   const int n_chunks = (R.n_cand + kSelectKeysPerCta - 1) / kSelectKeysPerCta;
@@ -571,6 +584,33 @@ __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __gri
     P.thr[2 * i + 1] = need;
     sync[0] = 0u;  // ready for the next call
     sync[1] = 0u;
+  }
+  if (!fused) return;
+  // the only chunk: the keys are still in registers; write the selection in
+  // ascending index order (keys above T, then the first `need` equal to T)
+  uint32_t n_gt = 0, n_eq = 0;
+#pragma unroll
+  for (int j = 0; j < kItems; ++j) {
+    n_gt += j < n_mine && kk[j] > T;
+    n_eq += j < n_mine && kk[j] == T;
+  }
+  uint32_t gt_rank = block_excl_scan(n_gt, sh, &tot);
+  uint32_t eq_rank = block_excl_scan(n_eq, sh, &tot);
+#pragma unroll
+  for (int j = 0; j < kItems; ++j) {
+    if (j >= n_mine) break;
+    const int64_t e = my0 + j;
+    if (kk[j] > T || (kk[j] == T && eq_rank < need)) {
+      const uint32_t pos = gt_rank + min(eq_rank, need);
+      if (pos < (uint32_t)R.k) {
+        sel[pos] = (int32_t)e;
+        if (tko) tko[pos] = (int32_t)e;
+      } else {
+        flag_error(P.pool, kErrBadIndex);
+      }
+    }
+    if (kk[j] > T) ++gt_rank;
+    if (kk[j] == T) ++eq_rank;
   }
 }
 
@@ -690,12 +730,16 @@ int launch_select(const AttendParams& p, void* stream, int* n_kernels) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   bool any_radix = false;
   for (int i = 0; i < p.n; ++i) any_radix |= (!p.reqs[i].select_all && p.reqs[i].k > 0);
-  if (any_radix) {
-    launch_kernel(false, select_compact_kernel, dim3(p.total_key_ctas), dim3(kSelThreads), 0, s, p);
+  // one chunk per request (at most kSelectKeysPerCta candidates each): one pass does it all
+  const int fused = p.total_key_ctas == p.n ? 1 : 0;
+  if (any_radix || fused) {
+    launch_kernel(false, select_compact_kernel, dim3(p.total_key_ctas), dim3(kSelThreads), 0, s, p, fused);
     *n_kernels += 1;
   }
-  launch_kernel(false, select_emit_kernel, dim3(p.total_key_ctas), dim3(kSelThreads), 0, s, p);
-  *n_kernels += 1;
+  if (!fused) {
+    launch_kernel(false, select_emit_kernel, dim3(p.total_key_ctas), dim3(kSelThreads), 0, s, p);
+    *n_kernels += 1;
+  }
   return (int)cudaGetLastError();
 }
 

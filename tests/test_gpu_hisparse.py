@@ -81,13 +81,37 @@ def test_offloaded_blocks_give_bit_identical_outputs(name):
     assert any(o.block_location(b)[1] < 0 for b in range(32) if o.block_location(b)[0] == 0)
     for s_ in slots:
         compare_request_state(g, o, s_)
-    # images of requests with offloaded blocks: the oracle's bytes
+    # images of requests with offloaded blocks: the oracle's bytes; restored
+    # into the HiSparse pool they take GPU slots and stamps like the oracle's
     n = (L[0] // mp) * mp
-    if n > 0:
-        rc, ref_img = o.export_prefix(slots[0], n, 0)
-        img = g.pool.export_prefix(slots[0], n, 0)
-        torch.cuda.synchronize()
-        assert np.array_equal(img.numpy()[:ref_img.size], ref_img)
+    assert n > 0
+    rc, ref_img = o.export_prefix(slots[0], n, 0)
+    img = g.pool.export_prefix(slots[0], n, 0)
+    torch.cuda.synchronize()
+    assert np.array_equal(img.numpy()[:ref_img.size], ref_img)
+    for s_ in slots[1:]:
+        assert o.free_request(s_) == 0
+        g.pool.free_request(s_)
+    r = g.pool.alloc_request()
+    assert o.alloc_request()[1] == r
+    wl = min(n, w["n_win"])
+    k, v, _ = H.tokens(w, [slots[0]], [n - wl], [wl])
+    gk, gv, _ = g.tokens([slots[0]], [n - wl], [wl])
+    assert o.import_prefix(r, ref_img, k, v) == 0
+    g.pool.import_prefix(r, img, gk, gv)
+    torch.cuda.synchronize()
+    assert g.pool.check_device() == 0
+    locations_match(o, g, 32)
+    ids = o.request_info(r)[2].tolist()
+    assert g.pool.block_activity(ids).tolist() == [o.block_location(b)[2] for b in ids]
+    compare_request_state(g, o, r)
+    for layer in range(g.nl):
+        q, qi = H.queries(w, layer, [slots[0], slots[0]], 99)  # both rows: the source's query
+        rc, out_ref, tk_ref = o.decode_attend(layer, [slots[0], r], q, qi, 256)
+        out_g, tk_g = g.attend(layer, [slots[0], r], [slots[0], slots[0]], 99, 256)
+        assert g.pool.check_device() == 0
+        assert np.array_equal(tk_g.cpu().numpy(), tk_ref)
+        check_out(out_g.cpu().numpy().reshape(out_ref.shape), out_ref, w["cache_dtype"])
 
 
 def test_host_slot_bytes_span_every_csa_layer():
