@@ -636,24 +636,33 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
     for (int b = threadIdx.x; b < kHistBins; b += blockDim.x) gh[b] = 0u;
   }
   const bool on = 4 * lane < d;
-  float m = -INFINITY, l = 0.0f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const int nw = blockDim.x >> 5;
+  // the largest split maximum first, so that every split's weight is
+  // independent of the others and its loads can all be in flight at once
+  float mloc = -INFINITY;
+  for (int s = threadIdx.x; s < n_split; s += blockDim.x)
+    mloc = fmaxf(mloc, P.part_ml[((R.part_base + s) * pd.heads + h) * 2]);
+  mloc = warp_max(mloc);
+  if (lane == 0) red_m[warp] = mloc;
+  __syncthreads();
+  float M = -INFINITY;
+  for (int w = 0; w < nw; ++w) M = fmaxf(M, red_m[w]);
+  float l = 0.0f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
 #pragma unroll 4
-  for (int s = warp; s < n_split; s += nw) {
-    const int64_t gs = R.part_base + s;
-    const float2 ml = *reinterpret_cast<const float2*>(P.part_ml + (gs * pd.heads + h) * 2);
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (on) v = *reinterpret_cast<const float4*>(P.part_o + gs * pd.HD + h * d + 4 * lane);
-    if (ml.x == -INFINITY) continue;  // an empty split
-    const float mn = fmaxf(m, ml.x);
-    const float a = exp2f(m - mn), b = exp2f(ml.x - mn);
-    l = l * a + ml.y * b;
-    acc.x = acc.x * a + v.x * b;
-    acc.y = acc.y * a + v.y * b;
-    acc.z = acc.z * a + v.z * b;
-    acc.w = acc.w * a + v.w * b;
-    m = mn;
+    for (int s = warp; s < n_split; s += nw) {
+      const int64_t gs = R.part_base + s;
+      const float2 ml = *reinterpret_cast<const float2*>(P.part_ml + (gs * pd.heads + h) * 2);
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (on) v = *reinterpret_cast<const float4*>(P.part_o + gs * pd.HD + h * d + 4 * lane);
+      const float b = ml.x == -INFINITY ? 0.0f : exp2f(ml.x - M);  // an empty split weighs nothing
+      l = fmaf(ml.y, b, l);
+      acc.x = fmaf(v.x, b, acc.x);
+      acc.y = fmaf(v.y, b, acc.y);
+      acc.z = fmaf(v.z, b, acc.z);
+      acc.w = fmaf(v.w, b, acc.w);
+    }
   }
   if (on) {
     red_o[warp][4 * lane] = acc.x;
@@ -661,20 +670,13 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
     red_o[warp][4 * lane + 2] = acc.z;
     red_o[warp][4 * lane + 3] = acc.w;
   }
-  if (lane == 0) {
-    red_m[warp] = m;
-    red_l[warp] = l;
-  }
+  if (lane == 0) red_l[warp] = l;
   __syncthreads();
   if (threadIdx.x < d) {
-    float M = -INFINITY;
-    for (int w = 0; w < nw; ++w) M = fmaxf(M, red_m[w]);
     float num = 0.0f, den = 0.0f;
     for (int w = 0; w < nw; ++w) {
-      if (red_m[w] == -INFINITY) continue;
-      const float wt = exp2f(red_m[w] - M);
-      num = fmaf(red_o[w][threadIdx.x], wt, num);
-      den = fmaf(red_l[w], wt, den);
+      num += red_o[w][threadIdx.x];
+      den += red_l[w];
     }
     P.out[((int64_t)(P.row0 + i) * pd.heads + h) * d + threadIdx.x] = num / den;
   }
