@@ -2,6 +2,8 @@
 times.  Where the oracle can follow the whole run in seconds it does (decode
 batch, chunked prefill); at 1M-token context it checks sampled outputs it can
 compute one by one and properties that hold at any size (long context)."""
+import struct
+
 import numpy as np
 import pytest
 import torch
@@ -188,6 +190,45 @@ def test_long_context_full_sampled(idx_fp4):
     for t, pos in enumerate(range(L - w["n_win"], L)):
         c, sc = g.window_token(0, s, pos)
         assert np.array_equal(c, win_codes[t]) and np.array_equal(sc, win_scales[t]), f"window token {pos}"
+    if idx_fp4:
+        return
+    # the request's 1,048,576-token prefix as an image (Zero SWA): sampled
+    # entries where the image layout puts them; then restored in its place,
+    # grown by the same token and decoded again: the same bits as before
+    n = (L // mp_) * mp_
+    nb = n // mp_
+    img = g.pool.export_prefix(s, n, 0)
+    torch.cuda.synchronize()
+    raw = img.numpy()
+    magic, ver, fp, n_tok, nbh, wh = struct.unpack("<IIQqii", raw[:32].tobytes())
+    assert (magic, ver, fp, n_tok, nbh, wh) == (0x4950564B, 1, o.fingerprint(), n, nb, 0)
+    lay = g.pool.layout(0)
+    E, CBk, X = lay["entry_bytes"], lay["csa_per_block"], lay["idx_block_bytes"]
+    HDb = 2 * w["heads"] * w["head_dim"]
+    for j, e in enumerate(es):
+        b, t = divmod(e, CBk)
+        if b >= nb:
+            continue
+        off = 64 + (b * CBk + t) * E
+        assert np.array_equal(raw[off:off + HDb], cc[j]), f"image CSA entry {e}"
+        assert raw[off + HDb:off + HDb + 4].tobytes() == csc[j].astype("<u2").tobytes()
+        part = raw[64 + nb * CBk * E + b * X:64 + nb * CBk * E + (b + 1) * X]
+        key = bytes(part[(k // 16 * CBk + t) * 16 + k % 16] for k in range(lay["idx_entry_bytes"]))
+        assert key == ie[j][0].tobytes(), f"image indexer entry {e}"
+    for t in sorted(set(rng.integers(0, nb, 16).tolist()) | {nb - 1}):
+        off = 64 + nb * (CBk * E + X) + t * E
+        assert np.array_equal(raw[off:off + HDb], hca_codes[t]), f"image HCA entry {t}"
+    before = g.attend(0, slots, wids, 1, top_k)
+    g.pool.free_request(s)
+    assert g.pool.alloc_request() == s
+    wl = w["n_win"]
+    gk, gv, _ = g.tokens([wid], [n - wl], [wl])
+    g.pool.import_prefix(s, img, gk, gv)
+    assert g.pool.request_info(s)[2].tolist() == ids[:nb].tolist()  # its own ids back: the smallest free
+    assert g.append([s], [wid], [Lc], [1], check=False) == 0
+    after = g.attend(0, slots, wids, 1, top_k)
+    assert g.pool.check_device() == 0
+    assert torch.equal(before[0], after[0]) and torch.equal(before[1], after[1]), "restored request differs"
 
 
 def _mixed_schedule(w, steps):
