@@ -693,7 +693,8 @@ int launch_attend_t(const AttendParams& p, cudaStream_t s, int e_stage, size_t s
     launch_kernel(false, k, dim3(ctas), dim3(threads), smem, s, p, e_stage, part);
   };
   static size_t set[4] = {0, 0, 0, 0};
-  const bool hs = p.pool.hisparse != 0;
+  // only part 1 (selected CSA entries) can meet an offloaded entry
+  const bool hs = p.pool.hisparse != 0 && part == 1;
   if (p.pool.head_dim == 128) {
     if (hs) go(attend_kernel<IN, CACHE, 8, true>, &set[0]);
     else go(attend_kernel<IN, CACHE, 8, false>, &set[1]);
