@@ -1190,6 +1190,21 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
     const int64_t target0 = forked ? kPart0Ctas : kAttendCtas;
     int64_t len0 = std::min<int64_t>(max_split_len, std::max<int64_t>(16, (src0 + target0 - 1) / target0));
     int64_t len1 = std::min<int64_t>(max_split_len, std::max<int64_t>(16, (src1 + kAttendCtas - 1) / kAttendCtas));
+    // every request rounds its split count up: lengthen the splits until the
+    // CTAs fit one wave (a few CTAs past it would double the part's time)
+    auto fit = [&](int64_t len, int64_t cap, bool part1) {
+      for (; len < max_split_len; ++len) {
+        int64_t ctas = 0;
+        for (int i = 0; i < gn; ++i) {
+          const int64_t src = part1 ? P.reqs[i].k : (int64_t)P.reqs[i].n_hca + P.reqs[i].w;
+          ctas += (src + len - 1) / len;
+        }
+        if (ctas <= cap) break;
+      }
+      return len;
+    };
+    len0 = fit(len0, target0, false);
+    len1 = fit(len1, kAttendCtas, true);
     int splits0 = 0, splits1 = 0, parts = 0;
     for (int pass = 0; pass < 2; ++pass) {
       splits0 = splits1 = parts = 0;
