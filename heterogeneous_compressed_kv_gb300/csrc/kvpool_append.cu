@@ -198,6 +198,36 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
     return;
   }
 
+  // Seal copy CTAs (slices n_slices ..): the CSA / indexer entries that
+  // earlier calls staged move into the sealing block, spread over
+  // copy_slices CTAs of the unit (this call's own entries go to the block
+  // directly).
+  if (slice >= P.n_slices) {
+    if (u.block_id < 0 || !L.has_csa || u.t0 < m) return;
+    const int cs = slice - P.n_slices, ncs = P.copy_slices;
+    const int n_copy = u.t0 / m;
+    const int CB = pd.csa_per_block;
+    const int32_t sid = pd.staging_base + u.slot;
+    const uint8_t* stg_csa = pd.arena + L.csa_pool + (int64_t)(pd.csa_staging_base + u.slot) * L.csa_stride;
+    uint8_t* dst_csa = pd.arena + L.csa_pool + (int64_t)u.csa_slot * L.csa_stride;
+    const uint8_t* stg_idx = pd.arena + L.idx_pool + (int64_t)sid * L.idx_stride;
+    uint8_t* dst_idx = pd.arena + L.idx_pool + (int64_t)u.block_id * L.idx_stride;
+    const int64_t units = (int64_t)n_copy * pd.entry_bytes / 16;  // CSA entries, 16-byte units
+    for (int64_t o = (int64_t)cs * blockDim.x + tid; o < units; o += (int64_t)ncs * blockDim.x)
+      reinterpret_cast<uint4*>(dst_csa)[o] = reinterpret_cast<const uint4*>(stg_csa)[o];
+    for (int64_t k = (int64_t)cs * blockDim.x + tid; k < (int64_t)pd.idx_chunks * n_copy; k += (int64_t)ncs * blockDim.x) {
+      const int c = (int)(k / n_copy), e = (int)(k % n_copy);
+      const int64_t o = ((int64_t)c * CB + e) * 16;
+      *reinterpret_cast<uint4*>(dst_idx + o) = *reinterpret_cast<const uint4*>(stg_idx + o);
+    }
+    const bool scaled = pd.idx_dtype == KVPOOL_FP8_E4M3 || pd.idx_dtype == KVPOOL_FP4_E2M1;
+    if (scaled && cs == 0)
+      for (int e = tid; e < n_copy; e += blockDim.x)
+        *reinterpret_cast<uint16_t*>(dst_idx + L.idx_scale_off + 2 * e) =
+            *reinterpret_cast<const uint16_t*>(stg_idx + L.idx_scale_off + 2 * e);
+    return;
+  }
+
   const int v0 = (slice * blockDim.x + tid) * kVpt;  // my values in [K | V]
   const int half = v0 >= HD ? 1 : 0;
   const int hv = v0 - half * HD;
@@ -325,31 +355,6 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
     }
   }
 
-  // Seal: CSA / indexer entries staged by earlier calls move into the block.
-  if (u.block_id >= 0 && L.has_csa && u.t0 >= m) {
-    const int n_copy = u.t0 / m;
-    const int32_t sid = pd.staging_base + u.slot;
-    const uint8_t* stg_csa = pd.arena + L.csa_pool + (int64_t)(pd.csa_staging_base + u.slot) * L.csa_stride;
-    const uint8_t* stg_idx = pd.arena + L.idx_pool + (int64_t)sid * L.idx_stride;
-    const int64_t bytes = (int64_t)n_copy * pd.entry_bytes;  // CSA entries, multiple of 16
-    const int64_t per = ((bytes / 16 + P.n_slices - 1) / P.n_slices) * 16;
-    const int64_t b0 = per * slice, b1 = min(bytes, b0 + per);
-    for (int64_t o = b0 + tid * 16; o < b1; o += (int64_t)blockDim.x * 16)
-      *reinterpret_cast<uint4*>(blk_csa + o) = *reinterpret_cast<const uint4*>(stg_csa + o);
-    if (slice == 0) {
-      const int CB = pd.csa_per_block;
-      for (int i = tid; i < pd.idx_chunks * n_copy; i += blockDim.x) {
-        const int c = i / n_copy, e = i % n_copy;
-        const int64_t o = ((int64_t)c * CB + e) * 16;
-        *reinterpret_cast<uint4*>(blk_idx + o) = *reinterpret_cast<const uint4*>(stg_idx + o);
-      }
-      if (idx_scaled) {
-        for (int e = tid; e < n_copy; e += blockDim.x)
-          *reinterpret_cast<uint16_t*>(blk_idx + L.idx_scale_off + 2 * e) =
-              *reinterpret_cast<const uint16_t*>(stg_idx + L.idx_scale_off + 2 * e);
-      }
-    }
-  }
   if (u.block_id >= 0 && slice == 0 && layer == 0 && tid == 0) {
     reinterpret_cast<int32_t*>(pd.arena + pd.table)[(int64_t)u.slot * pd.max_bpr + u.seg] = u.block_id;
     if (pd.hisparse) {  // the new block's CSA location and activity stamp
@@ -406,7 +411,8 @@ int launch_append(const AppendParams& p, int n_layers, void* stream, int* n_kern
   if (p.n_units <= 0) return 0;
   if (p.n_slices != append_slices(p.pool)) return (int)cudaErrorInvalidValue;
   const int threads = append_threads(p.pool, p.n_slices);
-  dim3 grid(p.n_units, p.n_slices, n_layers);
+  if (p.copy_slices < 0) return (int)cudaErrorInvalidValue;
+  dim3 grid(p.n_units, p.n_slices + p.copy_slices, n_layers);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int key = p.pool.in_dtype * 3 + p.pool.cache_dtype;
   switch (key) {

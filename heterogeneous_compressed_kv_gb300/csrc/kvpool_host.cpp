@@ -35,6 +35,7 @@ constexpr int kMaxSplits = 4096;
 constexpr int kAttendCtas = 3 * 152;  // attention CTAs of a part that has the GPU to itself (3 per SM)
 constexpr int kPart0Ctas = 2 * 152;   // CTAs of the [HCA | window] part beside the select (2 per SM)
 constexpr int kScoreCtas = 152;         // CTAs of the score kernel per launch (1 per SM, one wave)
+constexpr int kSealCopySlices = 8;      // CTAs per sealing unit that copy its staged entries
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int value_bytes(int dtype) { return dtype == KVPOOL_F32 ? 4 : dtype == KVPOOL_BF16 ? 2 : 1; }
@@ -1062,6 +1063,11 @@ int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_
       for (size_t o = 0; o < list->size() && rc == 0; o += kMaxAppendUnits) {
         ap->n_units = (int32_t)std::min<size_t>(kMaxAppendUnits, list->size() - o);
         std::memcpy(ap->units, list->data() + o, sizeof(AppendUnit) * ap->n_units);
+        // a unit that seals a block with entries staged by earlier calls gets
+        // copy CTAs for them
+        ap->copy_slices = 0;
+        for (int32_t k = 0; k < ap->n_units; ++k)
+          if (any_csa && ap->units[k].block_id >= 0 && ap->units[k].t0 >= p->cfg.m) ap->copy_slices = kSealCopySlices;
         rc = p->launch(KVPOOL_KERNEL_APPEND, bytes, stream, [&](int* nk) { return launch_append(*ap, p->cfg.n_layers, stream, nk); });
         bytes = 0;
       }

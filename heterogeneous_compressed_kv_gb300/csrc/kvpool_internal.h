@@ -85,6 +85,7 @@ struct AppendParams {
   int64_t rows;  // T: rows per layer in the inputs
   int32_t n_units;
   int32_t n_slices;  // CTAs that split one unit's 2*H*d values
+  int32_t copy_slices;  // further CTAs per unit that copy a sealing block's staged entries (0: none seal)
   uint32_t epoch;    // HiSparse activity stamp of the blocks sealed here
   AppendUnit units[kMaxAppendUnits];
 };
