@@ -257,8 +257,8 @@ def measured_peaks():
 
 
 def traffic_record(kernel, source):
-    """DRAM bytes per launch of `kernel` from a committed ncu summary, only if
-    the kernel source is unchanged since the capture."""
+    """DRAM bytes per launch of `kernel` ("workload/kernel") from a committed
+    ncu summary, only if the kernel source is unchanged since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -655,7 +655,8 @@ def main():
                                   note="separate pass over the same inputs, every launch between CUDA events"),
                 roofline=dict(kernel=dom, bound="hbm", achieved=achieved, peak=hbm_peak, unit="GB/s",
                               frac=(achieved / hbm_peak) if achieved else None,
-                              traffic=traffic_record(dom + ("_fp4" if dom == "score" and w["idx_fp4"] else ""), src),
+                              traffic=traffic_record(f"{w['name']}/{dom}" + ("_fp4" if dom == "score" and w["idx_fp4"] else ""),
+                                                     src),
                               peak_source=peak_kind,
                               bytes_per_launch=d_b / launches_dom, ms_per_launch=d_ms / launches_dom),
                 e2e=dict(value=e2e_value, unit="tokens/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
