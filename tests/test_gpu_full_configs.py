@@ -261,7 +261,8 @@ def _mixed_schedule(w, steps):
     return lens, plan, peak
 
 
-def test_mixed_serving_full_sampled():
+@pytest.mark.parametrize("hisparse", [False, True], ids=["resident", "hisparse"])
+def test_mixed_serving_full_sampled(hisparse):
     """256 requests, lognormal lengths (median 4096, capped at 131072), four
     layers [SWA-only, CSA, HCA, CSA], window 4096, top_k 1024; from the second
     step on, 10% of the requests finish and as many arrive (their prefill
@@ -271,14 +272,19 @@ def test_mixed_serving_full_sampled():
     departures); for three requests (the longest live one and the two last
     arrivals) the oracle recomputes every layer's attention output of the
     last step from the generator's tokens, with the CSA layers' top-k sets
-    compared bit for bit, and sampled stored CSA entries byte for byte."""
+    compared bit for bit, and sampled stored CSA entries byte for byte.
+    With HiSparse, every tenth step the blocks idle for 3 or more decode
+    calls move their CSA entries to host slots (up to 2,048 of them) and a
+    few come back: the same checks hold, the attention reading offloaded
+    entries from host memory."""
     from tests import oracle_pool as OP
     import oracle as O
     w = W.MIXED_SERVING
     steps, C, mp_, top_k, n_win = w["decode_steps"], w["chunk"], w["m_prime"], w["top_k"], w["n_win"]
     lens, plan, peak = _mixed_schedule(w, steps)
     B = w["n_requests"]
-    g = GpuCase(w, B, peak + 64, (w["len_cap"] + steps) // mp_ + 2, B, top_k)
+    gw = dict(w, csa_hot_slots=peak + 64, csa_host_slots=2048) if hisparse else w
+    g = GpuCase(gw, B, peak + 64, (w["len_cap"] + steps) // mp_ + 2, B, top_k)
     assert [g.pool.alloc_request() for _ in range(B)] == list(range(B))
     import heapq
     live = {s: [s, 0] for s in range(B)}  # slot -> [workload id, length]
@@ -302,6 +308,7 @@ def test_mixed_serving_full_sampled():
 
     prefill(list(range(B)), lens)
     last = {}
+    moved = 0
     for step, (gone, arrivals) in enumerate(plan):
         for s in gone:
             g.pool.free_request(s)
@@ -321,11 +328,20 @@ def test_mixed_serving_full_sampled():
             if step == steps - 1:
                 last[layer] = (slots, out.cpu().numpy(), tk.cpu().numpy())
         assert g.pool.check_device() == 0
+        if hisparse and step % 10 == 5:
+            room = 2048 - sum(1 for ids in table.values() for b in ids if g.pool.block_location(b)[1] < 0)
+            idle = g.pool.inactive_blocks(3).tolist()[:room]
+            g.pool.offload(idle)
+            moved += len(idle)
+            back = [b for ids in table.values() for b in ids if g.pool.block_location(b)[1] < 0][:8]
+            g.pool.fetch(back)
+            assert g.pool.check_device() == 0
     for s in sorted(live):
         rc, info, ids = g.pool.request_info(s)
         assert info["length"] == live[s][1]
         assert ids.tolist() == table[s], f"block table of slot {s}"
     assert g.pool.free_block_count() == len(free_ids)
+    assert moved > 0 or not hisparse
     # the oracle's last step for three requests
     slots = last[0][0]
     first = max(slots, key=lambda s: live[s][1])
