@@ -176,7 +176,15 @@ __device__ __forceinline__ void write_idx_fp4(uint8_t* base, const PoolDesc& pd,
   *reinterpret_cast<uint32_t*>(base + ((int64_t)(xv0 / 32) * pd.csa_per_block + slot) * 16 + (xv0 % 32) / 2) = w;
 }
 
-constexpr int kTokGroup = 8;  // tokens whose loads are issued together
+constexpr int kTokGroup = 8;
+__device__ __forceinline__ void ld8f(const float* p, float* x) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0], b = reinterpret_cast<const float4*>(p)[1];
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void st8f(float* p, const float* x) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+}  // tokens whose loads are issued together
 
 template <int IN, int CACHE>
 __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ AppendParams P) {
@@ -257,14 +265,14 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   for (int j = 0; j < kVpt; ++j) acc_c[j] = acc_h[j] = acc_x[j] = 0.0f;
   if (L.has_hca && u.t0 > 0) {
 #pragma unroll
-    for (int j = 0; j < kVpt; ++j) acc_h[j] = acc_h_ptr[j];
+    ld8f(acc_h_ptr, acc_h);
   }
   if (L.has_csa && (u.t0 % m) != 0) {
 #pragma unroll
-    for (int j = 0; j < kVpt; ++j) acc_c[j] = acc_c_ptr[j];
+    ld8f(acc_c_ptr, acc_c);
     if (idx_thread) {
 #pragma unroll
-      for (int j = 0; j < kVpt; ++j) acc_x[j] = acc_x_ptr[j];
+      ld8f(acc_x_ptr, acc_x);
     }
   }
 
@@ -344,14 +352,14 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   }
   if (L.has_hca && u.t1 < mp) {
 #pragma unroll
-    for (int j = 0; j < kVpt; ++j) acc_h_ptr[j] = acc_h[j];
+    st8f(acc_h_ptr, acc_h);
   }
   if (L.has_csa && (u.t1 % m) != 0) {
 #pragma unroll
-    for (int j = 0; j < kVpt; ++j) acc_c_ptr[j] = acc_c[j];
+    st8f(acc_c_ptr, acc_c);
     if (idx_thread) {
 #pragma unroll
-      for (int j = 0; j < kVpt; ++j) acc_x_ptr[j] = acc_x[j];
+      st8f(acc_x_ptr, acc_x);
     }
   }
 
