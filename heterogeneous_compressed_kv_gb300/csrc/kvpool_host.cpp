@@ -1334,6 +1334,14 @@ int kvpool_get_layout(const kvpool_t* p, kvpool_layout* out, int32_t layer, kvpo
   return KVPOOL_OK;
 }
 
+int kvpool_wait_selftest(kvpool_t* p, void* stream) {
+  if (!p) return KVPOOL_ERR_INVALID_ARG;
+  if (!p->device()) return p->fail(KVPOOL_ERR_INVALID_ARG, "wait_selftest: pool has no device");
+  const int rc = launch_wait_selftest(p->lay.pd, stream);
+  if (rc != 0) return p->cuda_fail((cudaError_t)rc, "wait_selftest launch");
+  return KVPOOL_OK;
+}
+
 int kvpool_check_device(kvpool_t* p, void* stream, uint32_t* word_out) {
   if (!p) return KVPOOL_ERR_INVALID_ARG;
   if (!p->device()) {

@@ -83,7 +83,22 @@ __global__ void __launch_bounds__(kImageThreads) image_copy_kernel(const __grid_
   }
 }
 
+// One thread waits on a barrier that expects an arrival nothing makes: the
+// bounded wait gives up after its limit and sets the wait flag.
+__global__ void wait_selftest_kernel(const PoolDesc pd) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  mbar_fence_init();
+  mbar_wait(&bar, 0, pd);
+}
+
 }  // namespace
+
+int launch_wait_selftest(const PoolDesc& pd, void* stream) {
+  wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(pd);
+  return (int)cudaGetLastError();
+}
 
 int launch_image(const ImageParams& p, void* stream, int* n_kernels) {
   if (p.n_pieces <= 0 && p.n_runs <= 0) return 0;

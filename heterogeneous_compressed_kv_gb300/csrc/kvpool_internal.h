@@ -191,6 +191,7 @@ struct AttendParams {
 int launch_append(const AppendParams& p, int n_layers, void* stream, int* n_kernels);
 int launch_share(const ShareParams& p, int n_layers, void* stream, int* n_kernels);
 int launch_image(const ImageParams& p, void* stream, int* n_kernels);
+int launch_wait_selftest(const PoolDesc& pd, void* stream);
 int launch_score(const AttendParams& p, void* stream, int* n_kernels);
 int launch_select(const AttendParams& p, void* stream, int* n_kernels);
 int launch_attend(const AttendParams& p, int part, int ctas, void* stream, int* n_kernels);

@@ -31,7 +31,7 @@ EXPORTS = ["kvpool_required_bytes", "kvpool_create", "kvpool_destroy", "kvpool_a
            "kvpool_topk_static", "kvpool_profile_timeline", "kvpool_fingerprint", "kvpool_image_bytes",
            "kvpool_export_prefix", "kvpool_import_prefix", "kvpool_host_slot_bytes", "kvpool_set_host_pool",
            "kvpool_offload", "kvpool_fetch", "kvpool_block_location", "kvpool_epoch", "kvpool_block_activity",
-           "kvpool_inactive_blocks"]
+           "kvpool_inactive_blocks", "kvpool_wait_selftest"]
 
 
 class KvpoolError(RuntimeError):
@@ -117,6 +117,7 @@ def lib():
         L.kvpool_block_activity.argtypes = [vp, i32, vp, vp, vp]
         L.kvpool_inactive_blocks.restype = i32
         L.kvpool_inactive_blocks.argtypes = [vp, C.c_uint32, vp, i32, vp]
+        L.kvpool_wait_selftest.argtypes = [vp, vp]
         L.kvpool_last_error.restype = C.c_char_p
         L.kvpool_last_error.argtypes = [vp]
         _lib = L
@@ -374,6 +375,10 @@ class Pool:
         if layer is not None:
             d.update({f: getattr(ll, f) for f, _ in _LayerLayout._fields_})
         return d
+
+    def wait_selftest(self, stream=None) -> None:
+        """A kernel whose barrier wait runs out (see kvpool_wait_selftest)."""
+        self._check(self.L.kvpool_wait_selftest(self.h, _stream(stream)), "wait_selftest")
 
     def check_device(self, stream=None) -> int:
         w = C.c_uint32()

@@ -412,6 +412,14 @@ int kvpool_get_layout(const kvpool_t* pool, kvpool_layout* out, int32_t layer, k
  * gets the flags), or CUDA. */
 int kvpool_check_device(kvpool_t* pool, void* stream, uint32_t* word_out);
 
+/* Self-test of the bounded waits (the failure detection of the kernels):
+ * one CTA waits, in stream order, on a barrier that nothing completes; after
+ * the wait limit (1 s) it sets the wait flag in the device error word and
+ * returns, leaving the context usable.  kvpool_check_device then reports
+ * DEVICE_CHECK with flag 1.  No memory other than the error word is touched.
+ * Errors: INVALID_ARG (a pool without device memory), CUDA. */
+int kvpool_wait_selftest(kvpool_t* pool, void* stream);
+
 /* ---- profiling: CUDA events around each launch, on the launch stream ---- */
 enum {
   KVPOOL_KERNEL_APPEND = 0,  /* fused append / compress / seal */

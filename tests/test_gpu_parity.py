@@ -210,3 +210,25 @@ def test_mixed_layer_kinds_with_churn():
     for s_ in sorted(live):
         if live[s_][1] > 0:
             compare_request_state(g, o, s_)
+
+
+def test_bounded_wait_is_reported_and_the_pool_stays_usable():
+    """Failure detection without a fault: a kernel waits on a barrier that
+    nothing completes; its wait gives up after the 1 s limit and sets the
+    wait flag, which kvpool_check_device reports; the context, the pool and
+    the error word are usable afterwards."""
+    import time
+    w = dict(W.DECODE_BATCH, seed=26)
+    o, g = make_pair(w, 2, 8, 4, 2, 64)
+    r = g.pool.alloc_request()
+    assert o.alloc_request()[1] == r
+    append_both(o, g, [r], [0], [0], [200])
+    t0 = time.time()
+    g.pool.wait_selftest()
+    with pytest.raises(K.KvpoolError) as e:
+        g.pool.check_device()
+    assert e.value.code == K.ERR_DEVICE_CHECK and "flags 0x1" in str(e.value)
+    assert time.time() - t0 >= 0.9
+    assert g.pool.check_device() == 0  # read and cleared
+    append_both(o, g, [r], [r], [200], [1])
+    attend_both(o, g, 0, [r], [r], 0, 64)
