@@ -30,6 +30,9 @@ namespace kvp {
 namespace {
 
 constexpr int kStages = 4;
+// the stages' full and empty barriers sit in front of the staged entries
+constexpr int kBarBytes = 64;
+static_assert(2 * kStages * (int)sizeof(uint64_t) <= kBarBytes, "the barriers must fit in front of the stages");
 constexpr int kMaxSplitLen = 1024;
 constexpr int kUnroll = 4;  // entries per online-softmax update
 
@@ -429,7 +432,7 @@ __global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __gr
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + kStages;
-  uint8_t* stage_mem = smem + 64;
+  uint8_t* stage_mem = smem + kBarBytes;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -716,7 +719,7 @@ int attend_stage_entries(const PoolDesc& pd) {
 }
 
 size_t attend_smem_bytes(const PoolDesc& pd) {
-  return 64 + (size_t)kStages * attend_stage_entries(pd) * pd.entry_bytes;
+  return kBarBytes + (size_t)kStages * attend_stage_entries(pd) * pd.entry_bytes;
 }
 
 int attend_max_split_len() { return kMaxSplitLen; }
