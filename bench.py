@@ -524,12 +524,12 @@ def main():
 
     sk, sv, sx, sq, sqi = step_inputs(0, W_ + K_)
     out = torch.empty((B, HD), dtype=torch.float32, device=dev)
-    one = [1] * B
     top_k = w["top_k"]
+    slot_ids, one = np.asarray(slots, np.int32), np.ones(B, np.int32)  # converted once, not every call
 
     def step(t, k, v, x, q, qi):
-        pool.append(slots, one, k[t], v[t], x[t], stream=sp)
-        pool.decode_attend(0, slots, q[t], qi[t], top_k, out, None, stream=sp)
+        pool.append(slot_ids, one, k[t], v[t], x[t], stream=sp)
+        pool.decode_attend(0, slot_ids, q[t], qi[t], top_k, out, None, stream=sp)
 
     # warm-up, every kernel kind recorded: the dominant kernel is the one with
     # the most algorithmic bytes
@@ -563,6 +563,15 @@ def main():
     d_ms, d_n, d_b = pool.profile_read(K.KERNEL_NAMES.index(dom))
     pool.check_device(sp)
     ms = max_over_ranks(ms, world)
+
+    # host cost of a step: the enqueue time of a short burst (short enough not
+    # to fill the launch queue, so the host never waits for the GPU)
+    nb = min(K_, 16)
+    h0 = time.perf_counter()
+    for t in range(W_, W_ + nb):
+        step(t, sk, sv, sx, sq, sqi)
+    host_us = (time.perf_counter() - h0) / nb * 1e6
+    torch.cuda.synchronize()
 
     # per-kernel breakdown: a second pass over the same step inputs, every
     # launch between events (the events themselves cost a little time)
@@ -664,7 +673,7 @@ def main():
                               bytes_per_launch=d_b / launches_dom, ms_per_launch=d_ms / launches_dom),
                 e2e=dict(value=e2e_value, unit="tokens/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
                 **({"hisparse": hisparse} if hisparse else {}),
-                gpu_launches=launches, setup_s=t_setup, clocks=clk)
+                gpu_launches=launches, setup_s=t_setup, clocks=clk, host_enqueue_us_per_step=host_us)
     if cpu is not None:
         n_w, cpool, cres = cpu
         try:

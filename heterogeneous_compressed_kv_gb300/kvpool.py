@@ -205,6 +205,8 @@ def _host_buffer(x):
 
 
 def _i32(a) -> np.ndarray:
+    if type(a) is np.ndarray and a.dtype == np.int32 and a.flags.c_contiguous:
+        return a
     return np.ascontiguousarray(a, dtype=np.int32)
 
 
@@ -305,12 +307,12 @@ class Pool:
 
     def offload(self, block_ids, stream=None, check=True) -> int:
         ids = _i32(block_ids)
-        rc = self.L.kvpool_offload(self.h, ids.size, ids.ctypes.data_as(C.c_void_p), _stream(stream))
+        rc = self.L.kvpool_offload(self.h, ids.size, ids.ctypes.data, _stream(stream))
         return self._check(rc, "offload") if check else rc
 
     def fetch(self, block_ids, stream=None, check=True) -> int:
         ids = _i32(block_ids)
-        rc = self.L.kvpool_fetch(self.h, ids.size, ids.ctypes.data_as(C.c_void_p), _stream(stream))
+        rc = self.L.kvpool_fetch(self.h, ids.size, ids.ctypes.data, _stream(stream))
         return self._check(rc, "fetch") if check else rc
 
     def block_location(self, block_id: int):
@@ -325,27 +327,27 @@ class Pool:
     def block_activity(self, block_ids, stream=None) -> np.ndarray:
         ids = _i32(block_ids)
         out = np.zeros(max(ids.size, 1), np.uint32)
-        rc = self.L.kvpool_block_activity(self.h, ids.size, ids.ctypes.data_as(C.c_void_p),
-                                          out.ctypes.data_as(C.c_void_p), _stream(stream))
+        rc = self.L.kvpool_block_activity(self.h, ids.size, ids.ctypes.data,
+                                          out.ctypes.data, _stream(stream))
         self._check(rc, "block_activity")
         return out[:ids.size]
 
     def inactive_blocks(self, idle: int, cap: int = 1 << 20, stream=None) -> np.ndarray:
         ids = np.zeros(max(cap, 1), np.int32)
-        n = self.L.kvpool_inactive_blocks(self.h, idle, ids.ctypes.data_as(C.c_void_p), cap, _stream(stream))
+        n = self.L.kvpool_inactive_blocks(self.h, idle, ids.ctypes.data, cap, _stream(stream))
         if n < 0:
             self._check(n, "inactive_blocks")
         return ids[:min(n, cap)].copy()
 
     def append(self, req_ids, n_new, k, v, idx_k, stream=None, check=True) -> int:
         req, nn = _i32(req_ids), _i32(n_new)
-        rc = self.L.kvpool_append(self.h, req.size, req.ctypes.data_as(C.c_void_p), nn.ctypes.data_as(C.c_void_p),
+        rc = self.L.kvpool_append(self.h, req.size, req.ctypes.data, nn.ctypes.data,
                                   _ptr(k), _ptr(v), _ptr(idx_k), _stream(stream))
         return self._check(rc, "append") if check else rc
 
     def decode_attend(self, layer, req_ids, q, q_idx, top_k, out, topk_out=None, stream=None, check=True) -> int:
         req = _i32(req_ids)
-        rc = self.L.kvpool_decode_attend(self.h, layer, req.size, req.ctypes.data_as(C.c_void_p), _ptr(q),
+        rc = self.L.kvpool_decode_attend(self.h, layer, req.size, req.ctypes.data, _ptr(q),
                                          _ptr(q_idx), top_k, _ptr(out), _ptr(topk_out), _stream(stream))
         return self._check(rc, "decode_attend") if check else rc
 
@@ -353,7 +355,7 @@ class Pool:
     def request_info(self, req: int, cap: int = 1 << 16):
         info = _Info()
         ids = np.zeros(max(cap, 1), np.int32)
-        rc = self.L.kvpool_request_info(self.h, req, C.byref(info), ids.ctypes.data_as(C.c_void_p), cap)
+        rc = self.L.kvpool_request_info(self.h, req, C.byref(info), ids.ctypes.data, cap)
         if rc != OK:
             return rc, None, None
         d = {f: getattr(info, f) for f, _ in _Info._fields_}
@@ -398,7 +400,7 @@ class Pool:
     def profile_timeline(self, cap: int = 4096):
         """[(kernel name, start ms, end ms)] of the recorded launches."""
         buf = np.zeros((cap, 3), np.float32)
-        n = self.L.kvpool_profile_timeline(self.h, cap, buf.ctypes.data_as(C.c_void_p))
+        n = self.L.kvpool_profile_timeline(self.h, cap, buf.ctypes.data)
         if n < 0:
             raise KvpoolError(n, "profile_timeline")
         return [(KERNEL_NAMES[int(k)], float(a), float(b)) for k, a, b in buf[:n]]
