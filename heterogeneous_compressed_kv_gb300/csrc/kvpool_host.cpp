@@ -48,6 +48,24 @@ int64_t idx_algo_bytes(const PoolDesc& pd) {
 }
 bool kind_has_hca(int k) { return k == KVPOOL_HCA || k == KVPOOL_CSA_HCA; }
 
+// The smallest run length in [lo, hi] for which the CTAs sum_i ceil(work_i /
+// len) fit `cap` (one wave); lo when no length does (more pieces of work than
+// CTAs) .  The count falls as the length grows, so a bisection finds it.
+int64_t fit_one_wave(const std::vector<int64_t>& work, int64_t lo, int64_t hi, int64_t cap) {
+  auto ctas = [&](int64_t len) {
+    int64_t c = 0;
+    for (int64_t w : work) c += (w + len - 1) / len;
+    return c;
+  };
+  if (lo >= hi || ctas(lo) <= cap || ctas(hi) > cap) return lo;
+  while (hi - lo > 1) {  // ctas(lo) > cap >= ctas(hi)
+    const int64_t mid = lo + (hi - lo) / 2;
+    if (ctas(mid) <= cap) hi = mid;
+    else lo = mid;
+  }
+  return hi;
+}
+
 struct Layout {
   PoolDesc pd;
   LayerDesc layers[kMaxLayers];
@@ -1150,13 +1168,20 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
     int64_t total_src = 0, total_segs = 0;
     int score_ctas = 0, key_ctas = 0;
     int64_t score_bytes = 0, attend_bytes = 0, out_bytes = 0;
+    std::vector<int64_t> req_segs;  // segments each request has scored
     for (int i = 0; i < gn; ++i) {
       const Request& q = p->reqs[h_req_ids[g0 + i]];
       const int32_t n_cand = Ld.has_csa ? (int32_t)(q.length / p->cfg.m) : 0;
       const int32_t k = std::min(top_k, n_cand);
-      if (k != n_cand && k > 0) total_segs += (n_cand + CB - 1) / CB;
+      if (k != n_cand && k > 0) {
+        total_segs += (n_cand + CB - 1) / CB;
+        req_segs.push_back((n_cand + CB - 1) / CB);
+      }
     }
-    P.segs_per_cta = (int32_t)std::min<int64_t>(4096, std::max<int64_t>(8, (total_segs + kScoreCtas - 1) / kScoreCtas));
+    // a score CTA takes a run of one request's segments; every request rounds
+    // its CTA count up, so lengthen the runs until the CTAs fit one wave
+    const int64_t spc0 = std::min<int64_t>(4096, std::max<int64_t>(8, (total_segs + kScoreCtas - 1) / kScoreCtas));
+    P.segs_per_cta = (int32_t)fit_one_wave(req_segs, spc0, 4096, kScoreCtas);
     for (int i = 0; i < gn; ++i) {
       const Request& q = p->reqs[h_req_ids[g0 + i]];
       AttendReq& R = P.reqs[i];
@@ -1198,19 +1223,13 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
     int64_t len1 = std::min<int64_t>(max_split_len, std::max<int64_t>(16, (src1 + kAttendCtas - 1) / kAttendCtas));
     // every request rounds its split count up: lengthen the splits until the
     // CTAs fit one wave (a few CTAs past it would double the part's time)
-    auto fit = [&](int64_t len, int64_t cap, bool part1) {
-      for (; len < max_split_len; ++len) {
-        int64_t ctas = 0;
-        for (int i = 0; i < gn; ++i) {
-          const int64_t src = part1 ? P.reqs[i].k : (int64_t)P.reqs[i].n_hca + P.reqs[i].w;
-          ctas += (src + len - 1) / len;
-        }
-        if (ctas <= cap) break;
-      }
-      return len;
-    };
-    len0 = fit(len0, target0, false);
-    len1 = fit(len1, kAttendCtas, true);
+    std::vector<int64_t> src_0(gn), src_1(gn);
+    for (int i = 0; i < gn; ++i) {
+      src_0[i] = (int64_t)P.reqs[i].n_hca + P.reqs[i].w;
+      src_1[i] = P.reqs[i].k;
+    }
+    len0 = fit_one_wave(src_0, len0, max_split_len, target0);
+    len1 = fit_one_wave(src_1, len1, max_split_len, kAttendCtas);
     int splits0 = 0, splits1 = 0, parts = 0;
     for (int pass = 0; pass < 2; ++pass) {
       splits0 = splits1 = parts = 0;
