@@ -460,10 +460,8 @@ __device__ __forceinline__ int load_items(const uint32_t* keys, int64_t my0, int
 // among the candidates (two more radix digits), how many keys equal to T are
 // taken, and every chunk's exclusive prefix of (keys > T, keys == T).  No
 // CTA waits on another: the last one is found with an atomic counter after a
-// fence.  fused: every request of the launch has one chunk, so its only CTA
-// also writes the ordered selection (pass 2 is not launched).
-__global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __grid_constant__ AttendParams P,
-                                                                     int fused) {
+// fence.
+__global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __grid_constant__ AttendParams P) {
   pdl_start();
   __shared__ uint32_t sh[kSelThreads];
   __shared__ uint32_t st[8];
@@ -473,17 +471,6 @@ __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __gri
   __shared__ int is_last;
   const int i = find_req(P, blockIdx.x, 1);
   const AttendReq& R = P.reqs[i];
-  int32_t* sel = P.sel + (int64_t)i * P.sel_stride;
-  int32_t* tko = P.topk_out ? P.topk_out + (int64_t)(P.row0 + i) * P.top_k : nullptr;
-  if (fused) {  // what pass 2 does for the requests that need no radix select
-    if (tko)
-      for (int j = R.k + threadIdx.x; j < P.top_k; j += blockDim.x) tko[j] = -1;
-    if (R.select_all)
-      for (int e = threadIdx.x; e < R.k; e += blockDim.x) {
-        sel[e] = e;
-        if (tko) tko[e] = e;
-      }
-  }
   if (R.select_all || R.k == 0) return;
   const int chunk = blockIdx.x - R.key_base;
   const int n_chunks = (R.n_cand + kSelectKeysPerCta - 1) / kSelectKeysPerCta;
@@ -585,15 +572,68 @@ __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __gri
     sync[0] = 0u;  // ready for the next call
     sync[1] = 0u;
   }
-  if (!fused) return;
-  // the only chunk: the keys are still in registers; write the selection in
-  // ascending index order (keys above T, then the first `need` equal to T)
+}
+
+// The whole select for a launch whose requests have at most
+// kSelectKeysPerCta candidates each: one CTA per request keeps the keys in
+// registers and takes the three radix digits of the k-th largest key from
+// shared-memory histograms (the first from the score histogram), then writes
+// the selection in ascending index order: keys above the threshold T and the
+// first `need` keys equal to it.
+__global__ void __launch_bounds__(kSelThreads) select_small_kernel(const __grid_constant__ AttendParams P) {
+  pdl_start();
+  __shared__ uint32_t sh[kSelThreads];
+  __shared__ uint32_t st[8];
+  __shared__ uint32_t h2[kHistBins];
+  const int i = blockIdx.x;
+  const AttendReq& R = P.reqs[i];
+  int32_t* sel = P.sel + (int64_t)i * P.sel_stride;
+  int32_t* tko = P.topk_out ? P.topk_out + (int64_t)(P.row0 + i) * P.top_k : nullptr;
+  if (tko)
+    for (int j = R.k + threadIdx.x; j < P.top_k; j += blockDim.x) tko[j] = -1;
+  if (R.k == 0) return;
+  if (R.select_all || R.n_cand > kSelectKeysPerCta) {  // (the host only sends requests that fit)
+    for (int e = threadIdx.x; e < R.k; e += blockDim.x) {
+      sel[e] = e;
+      if (tko) tko[e] = e;
+    }
+    if (!R.select_all && threadIdx.x == 0) flag_error(P.pool, kErrBadShape);
+    return;
+  }
+  const int tid = threadIdx.x;
+  const uint32_t* keys = P.keys + (int64_t)i * P.key_stride;
+  uint32_t kk[kItems];
+  const int64_t my0 = (int64_t)tid * kItems;
+  const int n_mine = load_items(keys, my0, R.n_cand, kk);
+  // first digit: from the score histogram
+  find_digit(P.hist + (int64_t)i * kHistBins, kHistBins, (uint32_t)R.k, sh, &st[0], &st[1]);
+  const uint32_t d1 = st[0], k1 = st[1];
+  // second digit: the next 11 bits of the keys in bucket d1
+  for (int b = tid; b < kHistBins; b += kSelThreads) h2[b] = 0u;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kItems; ++j)
+    if (j < n_mine && (kk[j] >> 21) == d1) atomicAdd(&h2[(kk[j] >> 10) & 2047u], 1u);
+  __syncthreads();
+  find_digit(h2, kHistBins, k1, sh, &st[2], &st[3]);
+  const uint32_t d2 = st[2], k2 = st[3];
+  const uint32_t pre = (d1 << 11) | d2;
+  // third digit: the low 10 bits of the keys with that prefix
+  for (int b = tid; b < 1024; b += kSelThreads) h2[b] = 0u;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < kItems; ++j)
+    if (j < n_mine && (kk[j] >> 10) == pre) atomicAdd(&h2[kk[j] & 1023u], 1u);
+  __syncthreads();
+  find_digit(h2, 1024, k2, sh, &st[4], &st[5]);
+  const uint32_t T = (pre << 10) | st[4], need = st[5];
   uint32_t n_gt = 0, n_eq = 0;
 #pragma unroll
   for (int j = 0; j < kItems; ++j) {
     n_gt += j < n_mine && kk[j] > T;
     n_eq += j < n_mine && kk[j] == T;
   }
+  uint32_t tot;
   uint32_t gt_rank = block_excl_scan(n_gt, sh, &tot);
   uint32_t eq_rank = block_excl_scan(n_eq, sh, &tot);
 #pragma unroll
@@ -728,18 +768,21 @@ int launch_score(const AttendParams& p, void* stream, int* n_kernels) {
 int launch_select(const AttendParams& p, void* stream, int* n_kernels) {
   if (p.total_key_ctas <= 0) return 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // one select CTA per request (at most kSelectKeysPerCta candidates each):
+  // the whole select in one pass
+  if (p.total_key_ctas == p.n) {
+    launch_kernel(false, select_small_kernel, dim3(p.n), dim3(kSelThreads), 0, s, p);
+    *n_kernels += 1;
+    return (int)cudaGetLastError();
+  }
   bool any_radix = false;
   for (int i = 0; i < p.n; ++i) any_radix |= (!p.reqs[i].select_all && p.reqs[i].k > 0);
-  // one chunk per request (at most kSelectKeysPerCta candidates each): one pass does it all
-  const int fused = p.total_key_ctas == p.n ? 1 : 0;
-  if (any_radix || fused) {
-    launch_kernel(false, select_compact_kernel, dim3(p.total_key_ctas), dim3(kSelThreads), 0, s, p, fused);
+  if (any_radix) {
+    launch_kernel(false, select_compact_kernel, dim3(p.total_key_ctas), dim3(kSelThreads), 0, s, p);
     *n_kernels += 1;
   }
-  if (!fused) {
-    launch_kernel(false, select_emit_kernel, dim3(p.total_key_ctas), dim3(kSelThreads), 0, s, p);
-    *n_kernels += 1;
-  }
+  launch_kernel(false, select_emit_kernel, dim3(p.total_key_ctas), dim3(kSelThreads), 0, s, p);
+  *n_kernels += 1;
   return (int)cudaGetLastError();
 }
 
