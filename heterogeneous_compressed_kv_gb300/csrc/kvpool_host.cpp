@@ -1277,7 +1277,7 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
     if (rc == 0)
       rc = p->launch(KVPOOL_KERNEL_ATTEND, bytes0, s0, [&](int* nk) { return launch_attend(P, 0, ctas0, s0, nk); });
     if (rc == 0 && key_ctas > 0)
-      rc = p->launch(KVPOOL_KERNEL_SELECT, 0, stream, [&](int* nk) { return launch_select(P, stream, nk); });
+      rc = p->launch(KVPOOL_KERNEL_SELECT, 0, stream, [&](int* nk) { return launch_select(P, stream, nk, !fork); });
     if (rc == 0)
       rc = p->launch(KVPOOL_KERNEL_ATTEND, bytes1, stream, [&](int* nk) { return launch_attend(P, 1, ctas1, stream, nk); });
     if (fork) {

@@ -16,6 +16,7 @@
 //         selected indices in ascending order.  No pass waits on another
 //         CTA; passes are separate launches.
 #include <cuda_fp16.h>
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -24,6 +25,8 @@
 
 #include "device_util.cuh"
 #include "kvpool_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace kvp {
 namespace {
@@ -375,13 +378,14 @@ constexpr int kSelThreads = 256;
 constexpr int kItems = kSelectKeysPerCta / kSelThreads;  // 16 keys per thread
 constexpr uint32_t kCandCache = 4096;                    // boundary-bucket candidates kept in shared memory
 
-// Block-wide (kSelThreads threads): the digit d (bin index) at which the
+// Block-wide (NT threads): the digit d (bin index) at which the
 // count of keys in bins above d is < k and the count in bins >= d is >= k,
 // and k - (count above d).  Thread t owns bins [t*per, (t+1)*per); suffix
 // sums run over warp shuffles, then across the 8 warps.
+template <int NT = kSelThreads>
 __device__ void find_digit(const uint32_t* h, int nbins, uint32_t k, uint32_t* sh, uint32_t* d_out,
                            uint32_t* k_out) {
-  const int per = nbins / kSelThreads;
+  const int per = nbins / NT;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   uint32_t own = 0;
   for (int b = 0; b < per; ++b) own += h[t * per + b];
@@ -395,7 +399,7 @@ __device__ void find_digit(const uint32_t* h, int nbins, uint32_t k, uint32_t* s
   if (lane == 0) sh[warp] = suf;  // warp total
   __syncthreads();
   uint32_t above_warps = 0;
-  for (int w = warp + 1; w < kSelThreads / 32; ++w) above_warps += sh[w];
+  for (int w = warp + 1; w < NT / 32; ++w) above_warps += sh[w];
   const uint32_t incl = suf + above_warps;  // keys in bins >= t*per
   const uint32_t above = incl - own;        // keys in bins >= (t+1)*per
   if (above < k && incl >= k) {
@@ -414,6 +418,7 @@ __device__ void find_digit(const uint32_t* h, int nbins, uint32_t k, uint32_t* s
 }
 
 // exclusive block scan of one value per thread; returns the block total
+template <int NT = kSelThreads>
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, uint32_t* total) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   uint32_t inc = v;
@@ -426,7 +431,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* sh, ui
   if (lane == 31) sh[warp] = inc;
   __syncthreads();
   uint32_t before = 0, tot = 0;
-  for (int w = 0; w < kSelThreads / 32; ++w) {
+  for (int w = 0; w < NT / 32; ++w) {
     if (w < warp) before += sh[w];
     tot += sh[w];
   }
@@ -654,6 +659,245 @@ __global__ void __launch_bounds__(kSelThreads) select_small_kernel(const __grid_
   }
 }
 
+// ---------------------------------------------------------------------------
+// Cluster select: one thread-block cluster of C CTAs (16, or 8 where a
+// 16-CTA cluster cannot be resident) per request.  CTA r of the cluster
+// holds keys [r*chunk, (r+1)*chunk) of its request in shared memory.  The
+// first radix digit d1 of the k-th largest key comes from the score
+// histogram; one pass over the keys lists those in buckets >= d1 (fewer than
+// k above d1, plus the boundary bucket) and histograms the boundary bucket's
+// next digit; the other two digits come from histograms summed across the
+// cluster through distributed shared memory, and the listed keys alone give
+// the counts and, in ascending index order, the selection, placed by the
+// cluster-wide exclusive prefix of (keys > T, keys == T).  One launch, no
+// global atomics, no CTA waiting on a counter.
+// Every exit before the first cluster barrier depends on the request only, so
+// either all CTAs of a cluster reach each barrier or none does.
+// ---------------------------------------------------------------------------
+constexpr int kSelCThreads = 512;
+constexpr int kSelClusterMax = 16;
+
+// Sum of the cluster's local histograms h (nb bins, nb a multiple of the
+// cluster size) into hred of every CTA: CTA r first sums the slice
+// [r*nb/C, (r+1)*nb/C) over the cluster into hpart, then every CTA gathers
+// the C slices.  Called by every thread of every CTA of the cluster.
+__device__ void cluster_hist_sum(cg::cluster_group& cl, uint32_t* h, uint32_t* hpart, uint32_t* hred, int nb) {
+  const int C = (int)cl.num_blocks();
+  const int r = (int)cl.block_rank();
+  const int per = nb / C;
+  cl.sync();  // every local histogram is complete
+  for (int t = threadIdx.x; t < per; t += blockDim.x) {
+    uint32_t v = 0;
+#pragma unroll 4
+    for (int c = 0; c < C; ++c) v += cl.map_shared_rank(h, c)[r * per + t];
+    hpart[t] = v;
+  }
+  cl.sync();  // every slice is summed, and no CTA reads a peer's h any more
+  for (int b = threadIdx.x; b < nb; b += blockDim.x) hred[b] = cl.map_shared_rank(hpart, b / per)[b % per];
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(kSelCThreads) select_cluster_kernel(const __grid_constant__ AttendParams P,
+                                                                      int cap_keys) {
+  pdl_start();
+  extern __shared__ __align__(16) uint32_t ks[];  // this CTA's keys [cap_keys], then 16-bit list slots [cap_keys]
+  __shared__ __align__(16) uint32_t h[kHistBins];
+  __shared__ __align__(16) uint32_t hred[kHistBins];
+  __shared__ uint32_t hpart[kHistBins / 8];
+  __shared__ uint32_t sh[32];
+  __shared__ uint32_t st[8];
+  __shared__ uint32_t wgt[kSelCThreads / 32], weq[kSelCThreads / 32];
+  __shared__ uint32_t tot[2];
+  cg::cluster_group cl = cg::this_cluster();
+  const int C = (int)cl.num_blocks();
+  const int r = (int)cl.block_rank();
+  const int i = (int)(blockIdx.x / C);
+  const AttendReq& R = P.reqs[i];
+  int32_t* sel = P.sel + (int64_t)i * P.sel_stride;
+  int32_t* tko = P.topk_out ? P.topk_out + (int64_t)(P.row0 + i) * P.top_k : nullptr;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gtid = r * kSelCThreads + tid, gstride = C * kSelCThreads;
+  if (tko)
+    for (int j = R.k + gtid; j < P.top_k; j += gstride) tko[j] = -1;
+  if (R.k == 0) return;
+  const int64_t chunk = (((int64_t)R.n_cand + C - 1) / C + 3) & ~(int64_t)3;  // a multiple of 4 keys
+  if (R.select_all || chunk > cap_keys) {  // (the host sends only requests that fit)
+    for (int e = gtid; e < R.k; e += gstride) {
+      sel[e] = e;
+      if (tko) tko[e] = e;
+    }
+    if (!R.select_all && gtid == 0) flag_error(P.pool, kErrBadShape);
+    return;
+  }
+  const int64_t c0 = (int64_t)r * chunk;
+  const int nk = (int)max((int64_t)0, min((int64_t)R.n_cand, c0 + chunk) - c0);
+  // keys and the score histogram -> shared memory, eight 16-byte loads in
+  // flight per thread (c0 is a multiple of 4; key rows are 16-byte aligned)
+  const uint4* keys4 = reinterpret_cast<const uint4*>(P.keys + (int64_t)i * P.key_stride + c0);
+  const uint4* hist4 = reinterpret_cast<const uint4*>(P.hist + (int64_t)i * kHistBins);
+  uint4* ks4 = reinterpret_cast<uint4*>(ks);
+  const int n4 = nk >> 2;
+  constexpr int kHist4 = kHistBins / 4;
+  {
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int q = j * kSelCThreads + tid;
+      if (q < kHist4) v[j] = hist4[q];
+      else if (q - kHist4 < n4) v[j] = keys4[q - kHist4];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int q = j * kSelCThreads + tid;
+      if (q < kHist4) reinterpret_cast<uint4*>(hred)[q] = v[j];
+      else if (q - kHist4 < n4) ks4[q - kHist4] = v[j];
+    }
+  }
+  for (int q0 = 8 * kSelCThreads - kHist4; q0 < n4; q0 += 8 * kSelCThreads) {
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int q = q0 + j * kSelCThreads + tid;
+      if (q < n4) v[j] = keys4[q];
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int q = q0 + j * kSelCThreads + tid;
+      if (q < n4) ks4[q] = v[j];
+    }
+  }
+  for (int e = (n4 << 2) + tid; e < nk; e += kSelCThreads) ks[e] = P.keys[(int64_t)i * P.key_stride + c0 + e];
+  for (int b = tid; b < kHistBins; b += kSelCThreads) h[b] = 0u;
+  __syncthreads();
+  // first digit: from the score histogram (the same in every CTA)
+  find_digit<kSelCThreads>(hred, kHistBins, (uint32_t)R.k, sh, &st[0], &st[1]);
+  const uint32_t d1 = st[0], k1 = st[1];
+  // one pass over the keys: each warp owns a run of consecutive keys and
+  // lists, in index order, the local indices of its keys in buckets >= d1
+  // (fewer than k of them lie above d1: the list is short); the keys in
+  // bucket d1 also count into the histogram of their next 11 bits
+  constexpr int kWarps = kSelCThreads / 32;
+  const int seg = ((nk + kWarps - 1) / kWarps + 127) & ~127;
+  const int w0 = min(nk, warp * seg), w1 = min(nk, w0 + seg);
+  uint16_t* lst = reinterpret_cast<uint16_t*>(ks + cap_keys) + w0;
+  uint32_t n_list = 0;
+  for (int e0 = w0; e0 < w1; e0 += 128) {
+    const int e = e0 + lane * 4;
+    uint32_t kv[4];
+    if (e + 3 < w1) {
+      const uint4 v = ks4[e >> 2];
+      kv[0] = v.x;
+      kv[1] = v.y;
+      kv[2] = v.z;
+      kv[3] = v.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) kv[j] = e + j < w1 ? ks[e + j] : 0u;
+    }
+    bool fl[4];
+    uint32_t c = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const bool valid = e + j < w1;
+      const uint32_t b = kv[j] >> 21;
+      if (valid && b == d1) atomicAdd(&h[(kv[j] >> 10) & 2047u], 1u);
+      fl[j] = valid && b >= d1;
+      c += fl[j] ? 1u : 0u;
+    }
+    uint32_t inc = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += u;
+    }
+    uint32_t pos = n_list + inc - c;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (fl[j]) lst[pos++] = (uint16_t)(e + j);
+    n_list += __shfl_sync(0xffffffffu, inc, 31);
+  }
+  cluster_hist_sum(cl, h, hpart, hred, kHistBins);
+  find_digit<kSelCThreads>(hred, kHistBins, k1, sh, &st[2], &st[3]);
+  const uint32_t pre = (d1 << 11) | st[2], k2 = st[3];
+  // third digit: the low 10 bits of the listed keys with that prefix
+  for (int b = tid; b < 1024; b += kSelCThreads) h[b] = 0u;
+  __syncthreads();
+  for (uint32_t t = lane; t < n_list; t += 32) {
+    const uint32_t key = ks[lst[t]];
+    if ((key >> 10) == pre) atomicAdd(&h[key & 1023u], 1u);
+  }
+  cluster_hist_sum(cl, h, hpart, hred, 1024);
+  find_digit<kSelCThreads>(hred, 1024, k2, sh, &st[4], &st[5]);
+  const uint32_t T = (pre << 10) | st[4], need = st[5];
+  // each warp's counts of (> T, == T): all of them are on its list
+  uint32_t n_gt = 0, n_eq = 0;
+  for (uint32_t t = lane; t < n_list; t += 32) {
+    const uint32_t key = ks[lst[t]];
+    n_gt += key > T ? 1u : 0u;
+    n_eq += key == T ? 1u : 0u;
+  }
+  n_gt = __reduce_add_sync(0xffffffffu, n_gt);
+  n_eq = __reduce_add_sync(0xffffffffu, n_eq);
+  if (lane == 0) {
+    wgt[warp] = n_gt;
+    weq[warp] = n_eq;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t a = 0, b = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      a += wgt[w];
+      b += weq[w];
+    }
+    tot[0] = a;
+    tot[1] = b;
+  }
+  cl.sync();  // every CTA's totals are visible to the cluster
+  if (warp == 0) {  // this CTA's exclusive prefix over the lower ranks
+    uint32_t a = 0, b = 0;
+    if (lane < r) {
+      const uint32_t* t = cl.map_shared_rank(tot, lane);
+      a = t[0];
+      b = t[1];
+    }
+    a = __reduce_add_sync(0xffffffffu, a);
+    b = __reduce_add_sync(0xffffffffu, b);
+    if (lane == 0) {
+      st[6] = a;
+      st[7] = b;
+    }
+  }
+  __syncthreads();
+  uint32_t gt_rank = st[6], eq_rank = st[7];
+  for (int w = 0; w < warp; ++w) {
+    gt_rank += wgt[w];
+    eq_rank += weq[w];
+  }
+  // ordered emission over the list: a selected key's position is the number
+  // of keys > T before it plus min(keys == T before it, need)
+  const uint32_t lt = (1u << lane) - 1u;
+  for (uint32_t t0 = 0; t0 < n_list; t0 += 32) {
+    const uint32_t t = t0 + lane;
+    const uint32_t e = t < n_list ? lst[t] : 0u;
+    const uint32_t key = t < n_list ? ks[e] : 0u;
+    const bool g = t < n_list && key > T, q = t < n_list && key == T;
+    const uint32_t gm = __ballot_sync(0xffffffffu, g), qm = __ballot_sync(0xffffffffu, q);
+    const uint32_t eqb = eq_rank + __popc(qm & lt);
+    if (g || (q && eqb < need)) {
+      const uint32_t pos = gt_rank + __popc(gm & lt) + min(eqb, need);
+      if (pos < (uint32_t)R.k) {
+        sel[pos] = (int32_t)(c0 + e);
+        if (tko) tko[pos] = (int32_t)(c0 + e);
+      } else {
+        flag_error(P.pool, kErrBadIndex);
+      }
+    }
+    gt_rank += __popc(gm);
+    eq_rank += __popc(qm);
+  }
+  cl.sync();  // no CTA leaves while a peer may still read its totals
+}
+
 // Pass 2: every chunk writes its selected indices in ascending order, from the
 // exclusive prefixes the last compact CTA stored for it.
 __global__ void __launch_bounds__(kSelThreads) select_emit_kernel(const __grid_constant__ AttendParams P) {
@@ -765,7 +1009,61 @@ int launch_score(const AttendParams& p, void* stream, int* n_kernels) {
   return (int)cudaGetLastError();
 }
 
-int launch_select(const AttendParams& p, void* stream, int* n_kernels) {
+namespace {
+
+// Cluster size and shared-memory key capacity of the cluster select on the
+// current device: 16 CTAs per cluster where a 16-CTA cluster with the largest
+// key buffer can be resident, else 8, else none (the two-pass select runs).
+struct ClusterShape {
+  int ctas = 0;
+  int cap_keys = 0;
+};
+constexpr int kClusterKeyBytes = 180 * 1024;  // 6 bytes per key: the key and a list slot
+constexpr int kShapeDevices = 64;
+
+ClusterShape cluster_shape() {
+  static std::mutex mu;
+  static bool done[kShapeDevices];
+  static ClusterShape shape[kShapeDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kShapeDevices) return {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev]) {
+    done[dev] = true;
+    ClusterShape c;
+    if (cudaFuncSetAttribute(select_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kClusterKeyBytes) ==
+            cudaSuccess &&
+        cudaFuncSetAttribute(select_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess) {
+      for (int n : {kSelClusterMax, 8}) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(n);
+        cfg.blockDim = dim3(kSelCThreads);
+        cfg.dynamicSmemBytes = kClusterKeyBytes;
+        cudaLaunchAttribute a[1];
+        a[0].id = cudaLaunchAttributeClusterDimension;
+        a[0].val.clusterDim.x = n;
+        a[0].val.clusterDim.y = 1;
+        a[0].val.clusterDim.z = 1;
+        cfg.attrs = a;
+        cfg.numAttrs = 1;
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, select_cluster_kernel, &cfg) == cudaSuccess && active > 0) {
+          c.ctas = n;
+          c.cap_keys = std::min(kClusterKeyBytes / 6, 65535);  // list slots hold 16-bit indices
+          break;
+        }
+      }
+    }
+    (void)cudaGetLastError();  // a refused attribute or query leaves the two-pass select
+    shape[dev] = c;
+  }
+  return shape[dev];
+}
+
+}  // namespace
+
+int launch_select(const AttendParams& p, void* stream, int* n_kernels, bool alone) {
   if (p.total_key_ctas <= 0) return 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // one select CTA per request (at most kSelectKeysPerCta candidates each):
@@ -775,8 +1073,34 @@ int launch_select(const AttendParams& p, void* stream, int* n_kernels) {
     *n_kernels += 1;
     return (int)cudaGetLastError();
   }
-  bool any_radix = false;
-  for (int i = 0; i < p.n; ++i) any_radix |= (!p.reqs[i].select_all && p.reqs[i].k > 0);
+  // requests of more than one cluster's worth of 4096-key chunks, when the
+  // select has the GPU to itself: one cluster per request, its keys in the
+  // CTAs' shared memory
+  int64_t max_cand = 0;
+  for (int i = 0; i < p.n; ++i)
+    if (!p.reqs[i].select_all && p.reqs[i].k > 0) max_cand = std::max<int64_t>(max_cand, p.reqs[i].n_cand);
+  const ClusterShape cs = alone ? cluster_shape() : ClusterShape{};
+  if (cs.ctas > 0 && max_cand > (int64_t)cs.ctas * kSelectKeysPerCta) {
+    const int64_t chunk = ((max_cand + cs.ctas - 1) / cs.ctas + 3) & ~(int64_t)3;
+    if (chunk <= cs.cap_keys) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(p.n * cs.ctas));
+      cfg.blockDim = dim3(kSelCThreads);
+      cfg.dynamicSmemBytes = (size_t)chunk * 6;
+      cfg.stream = s;
+      cudaLaunchAttribute a[1];
+      a[0].id = cudaLaunchAttributeClusterDimension;
+      a[0].val.clusterDim.x = (unsigned)cs.ctas;
+      a[0].val.clusterDim.y = 1;
+      a[0].val.clusterDim.z = 1;
+      cfg.attrs = a;
+      cfg.numAttrs = 1;
+      cudaLaunchKernelEx(&cfg, select_cluster_kernel, p, (int)chunk);
+      *n_kernels += 1;
+      return (int)cudaGetLastError();
+    }
+  }
+  bool any_radix = max_cand > 0;
   if (any_radix) {
     launch_kernel(false, select_compact_kernel, dim3(p.total_key_ctas), dim3(kSelThreads), 0, s, p);
     *n_kernels += 1;
@@ -905,7 +1229,7 @@ extern "C" int kvpool_topk_static(const float* d_scores, int32_t n_rows, int32_t
     rc = (int)cudaGetLastError();
   }
   int nk = 0;
-  if (rc == 0) rc = launch_select(*P, stream, &nk);
+  if (rc == 0) rc = launch_select(*P, stream, &nk, true);
   delete P;
   return rc == 0 ? KVPOOL_OK : KVPOOL_ERR_CUDA;
 }

@@ -193,7 +193,10 @@ int launch_share(const ShareParams& p, int n_layers, void* stream, int* n_kernel
 int launch_image(const ImageParams& p, void* stream, int* n_kernels);
 int launch_wait_selftest(const PoolDesc& pd, void* stream);
 int launch_score(const AttendParams& p, void* stream, int* n_kernels);
-int launch_select(const AttendParams& p, void* stream, int* n_kernels);
+// alone: nothing else runs on the GPU beside the select, so it may take one
+// thread-block cluster per large request (a cluster waits for 16 SMs with room
+// at once, which attention CTAs running beside it would hold)
+int launch_select(const AttendParams& p, void* stream, int* n_kernels, bool alone);
 int launch_attend(const AttendParams& p, int part, int ctas, void* stream, int* n_kernels);
 int launch_combine(const AttendParams& p, void* stream, int* n_kernels);
 

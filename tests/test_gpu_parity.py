@@ -176,6 +176,45 @@ def test_equal_scores_select_lowest_indices():
     check_out(out.cpu().numpy().reshape(ref.shape), ref, w["cache_dtype"])
 
 
+def test_select_paths_in_one_launch():
+    """One decode launch whose requests take different select shapes: 67,500
+    candidates (17 chunks of 4096 keys), 5,000 (2 chunks), 75 (a chunk with
+    a ragged tail), 0 (k = 0, padding only); top-k sets bit-exact,
+    outputs within fp32 tolerance; then the same with every indexer score
+    equal (q_idx = 0: the k lowest indices), which puts all 67,500 keys on
+    the threshold."""
+    w = dict(W.TINY, seed=26)
+    lens = [270003, 20001, 300, 2]
+    mp_ = w["m_prime"]
+    o, g = make_pair(w, 4, sum(L // mp_ + 1 for L in lens) + 4, lens[0] // mp_ + 4, 4, 4096)
+    slots = [g.pool.alloc_request() for _ in lens]
+    assert [o.alloc_request()[1] for _ in lens] == slots
+    pos = [0] * len(lens)
+    while True:
+        cnt = [min(16384, L - p) for L, p in zip(lens, pos)]
+        if sum(cnt) == 0:
+            break
+        live = [j for j, c in enumerate(cnt) if c > 0]
+        append_both(o, g, [slots[j] for j in live], live, [pos[j] for j in live], [cnt[j] for j in live])
+        pos = [p + c for p, c in zip(pos, cnt)]
+    wids = list(range(len(lens)))
+    for step, top_k in enumerate((64, 2048, 4096)):
+        attend_both(o, g, 0, slots, wids, step, top_k)
+    attend_both(o, g, 0, [slots[0], slots[3]], [0, 3], 7, 300)
+    q, _ = H.queries(w, 0, [0], 0)
+    qi = np.zeros((1, g.XD), np.float32)
+    rc, ref, tk_ref = o.decode_attend(0, [slots[0]], q, qi, 1000)
+    assert tk_ref[0].tolist() == list(range(1000))
+    gq, _ = g.queries(0, [0], 0)
+    gqi = torch.zeros((1, g.XD), dtype=g.tdtype, device="cuda")
+    out = torch.empty((1, g.HD), dtype=torch.float32, device="cuda")
+    tk = torch.empty((1, 1000), dtype=torch.int32, device="cuda")
+    g.pool.decode_attend(0, [slots[0]], gq, gqi, 1000, out, tk)
+    assert g.pool.check_device() == 0
+    assert tk.cpu().numpy()[0].tolist() == list(range(1000))
+    check_out(out.cpu().numpy().reshape(ref.shape), ref, w["cache_dtype"])
+
+
 def test_mixed_layer_kinds_with_churn():
     """Mixed-serving shapes at reduced scale: layers [SWA-only, CSA, HCA,
     CSA], window 512, requests finishing and arriving between steps."""

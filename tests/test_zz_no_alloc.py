@@ -53,3 +53,57 @@ def test_static_topk_refuses_oversized_and_pads():
     out = torch.zeros((1, 3), dtype=torch.int32, device="cuda")
     assert K.topk_static(s, 3, out) == 0
     assert out.cpu().tolist() == [[0, 1, 3]]  # 3, 3, then the first of the equal zeros
+
+
+def _scores(kind, rows, n, seed):
+    rng = np.random.default_rng(seed)
+    if kind == "normal":
+        return rng.standard_normal((rows, n)).astype(np.float32)
+    if kind == "ties":  # few distinct values: the k-th largest is shared by thousands of keys
+        return rng.integers(-3, 7, (rows, n)).astype(np.float32)
+    if kind == "signed_zeros":  # +0 and -0 are one value; the order among them is the index order
+        s = rng.choice(np.array([0.0, -0.0, 1.5, -2.0], np.float32), (rows, n))
+        return s.astype(np.float32)
+    if kind == "equal":
+        return np.full((rows, n), 0.25, np.float32)
+    if kind == "narrow":  # positive values in one octave: most keys share the top radix digits
+        return (1.0 + rng.random((rows, n))).astype(np.float32)
+    raise ValueError(kind)
+
+
+# candidate counts on both sides of the select paths' limits: one CTA per row
+# (<= 4096), 4096-key chunks with a last-CTA threshold (up to 16 chunks), one
+# thread-block cluster per row with its keys in shared memory (beyond), each
+# with a ragged last chunk
+@pytest.mark.parametrize("n, top_k, kind", [
+    (4096, 512, "normal"),
+    (4097, 512, "ties"),
+    (40000, 2048, "narrow"),
+    (65536, 2048, "normal"),
+    (65537, 2048, "ties"),
+    (65537, 1, "normal"),
+    (100003, 2048, "signed_zeros"),
+    (100003, 777, "equal"),
+    (262145, 2048, "narrow"),
+    (262145, 2048, "ties"),
+    (300001, 300001, "normal"),
+    (300001, 300000, "ties"),
+])
+def test_static_topk_matches_the_oracle_across_select_paths(n, top_k, kind):
+    """Every row's selection equals the oracle's top-k (largest scores,
+    the lowest indices first among equal ones, ascending order, -1 padding)
+    bit for bit, on two calls in a row."""
+    import oracle as O
+    rows = 4 if n <= 100003 else 2
+    s = _scores(kind, rows, n, seed=n + top_k)
+    d = torch.from_numpy(s).cuda()
+    ref = np.stack([O.topk(s[r], top_k) for r in range(rows)])
+    for call in range(2):
+        got = torch.full((rows, top_k), -7, dtype=torch.int32, device="cuda")
+        assert K.topk_static(d, top_k, got) == 0
+        torch.cuda.synchronize()
+        g = got.cpu().numpy()
+        for r in range(rows):
+            if not np.array_equal(g[r], ref[r]):
+                bad = np.nonzero(g[r] != ref[r])[0]
+                pytest.fail(f"call {call} row {r}: {bad.size} positions differ, first {bad[:6].tolist()}")
