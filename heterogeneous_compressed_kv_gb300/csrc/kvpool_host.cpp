@@ -32,8 +32,13 @@ using namespace kvp;
 namespace {
 
 constexpr int kMaxSplits = 4096;
-constexpr int kAttendCtas = 3 * 152;  // attention CTAs of a part that has the GPU to itself (3 per SM)
-constexpr int kPart0Ctas = 2 * 152;   // CTAs of the [HCA | window] part beside the select (2 per SM)
+// attention CTAs of a part that has the GPU to itself: 3 per SM, of which 2
+// are resident at a time (registers); 1.5 waves of shorter splits measured a
+// little faster than one wave of longer ones (long context 178.8 vs 180.6 us)
+constexpr int kAttendCtas = 3 * 152;
+// CTAs of the [HCA | window] part beside the select: 2 per SM, one wave
+// (228 or 152 CTAs left room for the select but the step took 190 / 213 us)
+constexpr int kPart0Ctas = 2 * 152;
 constexpr int kScoreCtas = 152;         // CTAs of the score kernel per launch (1 per SM, one wave)
 constexpr int kSealCopySlices = 8;      // CTAs per sealing unit that copy its staged entries
 
