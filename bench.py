@@ -667,8 +667,10 @@ def main():
                                   note="separate pass over the same inputs, every launch between CUDA events"),
                 roofline=dict(kernel=dom, bound="hbm", achieved=achieved, peak=hbm_peak, unit="GB/s",
                               frac=(achieved / hbm_peak) if achieved else None,
-                              traffic=traffic_record(f"{w['name']}/{dom}" + ("_fp4" if dom == "score" and w["idx_fp4"] else ""),
-                                                     src),
+                              # the records hold full-size launches: none for a resized workload
+                              traffic=None if (args.requests or args.context) else
+                              traffic_record(f"{w['name']}/{dom}" + ("_fp4" if dom == "score" and w["idx_fp4"] else ""),
+                                             src),
                               peak_source=peak_kind,
                               bytes_per_launch=d_b / launches_dom, ms_per_launch=d_ms / launches_dom),
                 e2e=dict(value=e2e_value, unit="tokens/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
