@@ -326,8 +326,12 @@ int kvpool_decode_attend(kvpool_t* pool, int32_t layer, int32_t n, const int32_t
  * that loads it until the process exits: n_rows <= 256, n_cols <= 1,048,576 and
  * 12*n_rows*n_cols + 4*n_rows*top_k + 8.5 KiB*n_rows (+ small) <= 16 MiB,
  * else INVALID_ARG.  No cudaMalloc, cudaFree or allocating library routine is
- * called.  The first call on a device looks up that device's address of the
- * array (for the current device) and should come before any stream capture.
+ * called.  Rows of more than 65,536 columns are selected by one 16-CTA
+ * thread-block cluster each (8 where 16 cannot be resident), which runs only
+ * where nothing else occupies the GPU's SMs; smaller rows by 4096-column
+ * chunks or one CTA per row.  The first call on a device looks up that
+ * device's address of the array and the cluster shape (for the current
+ * device) and should come before any stream capture.
  * Every call shares the array and clears what must start at zero; calls that
  * overlap on the GPU (other streams, other host threads) race.  Errors:
  * INVALID_ARG, CUDA. */
