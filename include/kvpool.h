@@ -327,9 +327,9 @@ int kvpool_decode_attend(kvpool_t* pool, int32_t layer, int32_t n, const int32_t
  * 12*n_rows*n_cols + 4*n_rows*top_k + 8.5 KiB*n_rows (+ small) <= 16 MiB,
  * else INVALID_ARG.  No cudaMalloc, cudaFree or allocating library routine is
  * called.  Rows of more than 65,536 columns are selected by one 16-CTA
- * thread-block cluster each (8 where 16 cannot be resident), which runs only
- * where nothing else occupies the GPU's SMs; smaller rows by 4096-column
- * chunks or one CTA per row.  The first call on a device looks up that
+ * thread-block cluster each (8 where 16 cannot be resident; a cluster starts
+ * only when that many SMs have room at once, so work running beside the call
+ * delays it); smaller rows by 4096-column chunks or one CTA per row.  The first call on a device looks up that
  * device's address of the array and the cluster shape (for the current
  * device) and should come before any stream capture.
  * Every call shares the array and clears what must start at zero; calls that
