@@ -88,9 +88,10 @@ __device__ __forceinline__ uint32_t score_key(float s) {
 // before any early exit, so a grid never completes before its predecessor.
 // Without the launch attribute both instructions are no-ops.  The attribute
 // is set where an early start hides launch latency on the critical path
-// (append, indexer scores, merge); kernels that run beside other work (the
-// select passes, attention) launch without it: their early-started CTAs
-// would hold SM resources that work needs.
+// (append, indexer scores, the one-CTA select, the [selected CSA] attention
+// part, merge); the two-pass select and the [HCA | window] part launch
+// without it: their early-started CTAs held SM resources that the work
+// beside them needed (measured slower).
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_start() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

@@ -1069,7 +1069,7 @@ int launch_select(const AttendParams& p, void* stream, int* n_kernels, bool alon
   // one select CTA per request (at most kSelectKeysPerCta candidates each):
   // the whole select in one pass
   if (p.total_key_ctas == p.n) {
-    launch_kernel(false, select_small_kernel, dim3(p.n), dim3(kSelThreads), 0, s, p);
+    launch_kernel(true, select_small_kernel, dim3(p.n), dim3(kSelThreads), 0, s, p);
     *n_kernels += 1;
     return (int)cudaGetLastError();
   }
