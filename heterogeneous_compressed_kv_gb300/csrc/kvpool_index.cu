@@ -1161,7 +1161,7 @@ extern "C" int kvpool_topk_static(const float* d_scores, int32_t n_rows, int32_t
   using namespace kvp;
   if (n_rows < 0 || n_cols < 0 || top_k < 0) return KVPOOL_ERR_INVALID_ARG;
   if (n_rows == 0 || top_k == 0) return KVPOOL_OK;
-  if (!d_scores || !d_topk_out || n_rows > kMaxAttendReqs) return KVPOOL_ERR_INVALID_ARG;
+  if ((!d_scores && n_cols > 0) || !d_topk_out || n_rows > kMaxAttendReqs) return KVPOOL_ERR_INVALID_ARG;
   // scratch plan: [error word | hist | sync | thresholds | counts | selected | keys | candidates]
   const int64_t chunks = std::max<int64_t>(1, ((int64_t)n_cols + kSelectKeysPerCta - 1) / kSelectKeysPerCta);
   if (chunks > kMaxKeyCtasPerReq) return KVPOOL_ERR_INVALID_ARG;

@@ -320,8 +320,8 @@ int kvpool_decode_attend(kvpool_t* pool, int32_t layer, int32_t n, const int32_t
  * code that runs while a stream is being captured into a CUDA graph, or a
  * plugin that only receives its input and output buffers from a host
  * framework that owns every allocation.
- * d_scores: [n_rows][n_cols] fp32 (finite) on the device; d_topk_out:
- * [n_rows][top_k] int32.  Its scratch (sort keys, radix histograms, counts)
+ * d_scores: [n_rows][n_cols] fp32 (finite) on the device (may be NULL when
+ * n_cols is 0: every row is then all -1); d_topk_out: [n_rows][top_k] int32.  Its scratch (sort keys, radix histograms, counts)
  * is a file-scope 16 MiB device array in this library, present on every GPU
  * that loads it until the process exits: n_rows <= 256, n_cols <= 1,048,576 and
  * 12*n_rows*n_cols + 4*n_rows*top_k + 8.5 KiB*n_rows (+ small) <= 16 MiB,

@@ -88,13 +88,18 @@ def _scores(kind, rows, n, seed):
     (262145, 2048, "ties"),
     (300001, 300001, "normal"),
     (300001, 300000, "ties"),
+    (491520, 2048, "narrow"),     # the largest rows a cluster takes (30,720 keys per CTA)
+    (491521, 2048, "narrow"),     # one more: 4096-key chunks
+    (1048576, 2048, "normal"),    # the largest row: 256 chunks
+    (1, 5, "normal"),             # fewer columns than top_k: all of them, then -1
+    (0, 3, "normal"),             # no columns: -1 only
 ])
 def test_static_topk_matches_the_oracle_across_select_paths(n, top_k, kind):
     """Every row's selection equals the oracle's top-k (largest scores,
     the lowest indices first among equal ones, ascending order, -1 padding)
     bit for bit, on two calls in a row."""
     import oracle as O
-    rows = 4 if n <= 100003 else 2
+    rows = 4 if n <= 100003 else (2 if n <= 300001 else 1)
     s = _scores(kind, rows, n, seed=n + top_k)
     d = torch.from_numpy(s).cuda()
     ref = np.stack([O.topk(s[r], top_k) for r in range(rows)])
