@@ -642,7 +642,7 @@ def main():
     step_bytes = sum(b for (_, _, b) in prof.values()) / KB
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
-    src = {"score": "heterogeneous_compressed_kv_gb300/csrc/kvpool_index.cu",
+    src = {"score": "heterogeneous_compressed_kv_gb300/csrc/kvpool_score.cu",
            "attend": "heterogeneous_compressed_kv_gb300/csrc/kvpool_attend.cu",
            "append": "heterogeneous_compressed_kv_gb300/csrc/kvpool_append.cu"}[dom]
     launches_dom = d_n

@@ -37,7 +37,7 @@ def nvcc() -> str:
 LIBS = {
     "kvpool": {
         "out": os.path.join(PKG, "libkvpool.so"),
-        "sources": ["csrc/kvpool_host.cpp", "csrc/kvpool_append.cu", "csrc/kvpool_index.cu",
+        "sources": ["csrc/kvpool_host.cpp", "csrc/kvpool_append.cu", "csrc/kvpool_score.cu", "csrc/kvpool_select.cu",
                     "csrc/kvpool_attend.cu", "csrc/kvpool_image.cu"],
         "headers": ["csrc/kvpool_internal.h", "csrc/device_util.cuh", "../include/kvpool.h"],
     },

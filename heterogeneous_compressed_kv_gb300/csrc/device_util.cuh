@@ -115,6 +115,21 @@ inline cudaError_t launch_kernel(bool pdl, void (*kernel)(KArgs...), dim3 grid, 
 }
 
 // ---------------------------------------------------------------------------
+// request of a CTA: requests are ordered by their first CTA index (score
+// CTAs: which 0, select CTAs: which 1); the last request whose base <= cta
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int find_req(const AttendParams& P, int cta, int which) {
+  int lo = 0, hi = P.n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    const int base = which == 0 ? P.reqs[mid].score_base : P.reqs[mid].key_base;
+    if (base <= cta) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------------------
 // error word
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void flag_error(const PoolDesc& p, uint32_t f) {
