@@ -51,7 +51,7 @@ class _Config(C.Structure):
                 ("max_requests", C.c_int32), ("max_blocks", C.c_int32), ("max_blocks_per_request", C.c_int32),
                 ("gate_csa", C.POINTER(C.c_float)), ("gate_hca", C.POINTER(C.c_float)),
                 ("gate_idx", C.POINTER(C.c_float)), ("idx_fp4", C.c_int32), ("csa_hot_slots", C.c_int32),
-                ("csa_host_slots", C.c_int32)]
+                ("csa_host_slots", C.c_int32), ("idx_per_token", C.c_int32)]
 
 
 class _Info(C.Structure):
@@ -85,6 +85,8 @@ def lib():
         L.kvo_compress_idx.argtypes = [vp, C.c_int, vp, vp, vp]
         L.kvo_score.restype = C.c_float
         L.kvo_score.argtypes = [vp, vp, vp, vp]
+        L.kvo_score_tokens.restype = C.c_float
+        L.kvo_score_tokens.argtypes = [vp, C.c_int, vp, vp, vp]
         L.kvo_topk.argtypes = [vp, i64, C.c_int, vp]
         L.kvo_attend_sources.argtypes = [vp, i64, vp, vp, vp, vp]
         L.kvo_create.argtypes = [C.POINTER(_Config), C.POINTER(vp)]
@@ -204,7 +206,7 @@ class Oracle:
 
     def __init__(self, *, m, m_prime, n_win, heads, head_dim, idx_heads, idx_dim, in_dtype, cache_dtype,
                  layer_kinds, max_requests, max_blocks, max_blocks_per_request, gate_csa, gate_hca, gate_idx,
-                 idx_fp4=0, csa_hot_slots=0, csa_host_slots=0):
+                 idx_fp4=0, csa_hot_slots=0, csa_host_slots=0, idx_per_token=0):
         self.L = lib()
         self.kinds = np.ascontiguousarray(layer_kinds, dtype=np.int32)
         n_layers = self.kinds.size
@@ -215,7 +217,8 @@ class Oracle:
         cfg = _Config(m, m_prime, n_win, heads, head_dim, idx_heads, idx_dim, in_dtype, cache_dtype, n_layers,
                       self.kinds.ctypes.data_as(C.POINTER(C.c_int32)), max_requests, max_blocks,
                       max_blocks_per_request, self.g_csa.ctypes.data_as(fp), self.g_hca.ctypes.data_as(fp),
-                      self.g_idx.ctypes.data_as(fp), int(idx_fp4), int(csa_hot_slots), int(csa_host_slots))
+                      self.g_idx.ctypes.data_as(fp), int(idx_fp4), int(csa_hot_slots), int(csa_host_slots),
+                      int(idx_per_token))
         h = C.c_void_p()
         rc = self.L.kvo_create(C.byref(cfg), C.byref(h))
         if rc != OK:
@@ -332,6 +335,13 @@ class Oracle:
         code = np.ascontiguousarray(code, np.uint8)
         sc = np.ascontiguousarray(np.atleast_1d(scale), np.uint16)
         return self.L.kvo_score(self.h, _p(code), _p(sc), _p(_f32(q_idx)))
+
+    def score_tokens(self, layer, codes, scales, q_idx):
+        """Score of one CSA entry from its m tokens' encoded keys (per-token
+        indexer keys): codes [m][xsz] uint8, scales [m] uint16."""
+        codes = np.ascontiguousarray(codes, np.uint8)
+        sc = np.ascontiguousarray(np.atleast_1d(scales), np.uint16)
+        return self.L.kvo_score_tokens(self.h, layer, _p(codes), _p(sc), _p(_f32(q_idx)))
 
     def attend_sources(self, codes, scales, q):
         codes = np.ascontiguousarray(codes, np.uint8)

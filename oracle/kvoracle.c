@@ -201,6 +201,7 @@ struct kvo {
   kvo_config c;
   int32_t* kinds;
   int HD, XD, CB, esz, xsz, vs;
+  int XB; /* indexer keys per block section: CB (one per CSA entry) or m' (one per token) */
   int idx_dtype; /* indexer entries: the cache dtype, or KVO_FP4 */
   float* alpha_csa; /* [n_layers][H][m]  */
   float* alpha_hca; /* [n_layers][H][m'] */
@@ -223,8 +224,8 @@ static int has_hca(const kvo_t* o, int l) { return o->kinds[l] == KVO_HCA || o->
 static void sec_alloc(const kvo_t* o, layer_sec* s) {
   s->csa_code = (uint8_t*)calloc((size_t)o->CB, (size_t)o->esz);
   s->csa_scale = (uint16_t*)calloc((size_t)o->CB * 2, 2);
-  s->idx_code = (uint8_t*)calloc((size_t)o->CB, (size_t)o->xsz);
-  s->idx_scale = (uint16_t*)calloc((size_t)o->CB, 2);
+  s->idx_code = (uint8_t*)calloc((size_t)o->XB, (size_t)o->xsz);
+  s->idx_scale = (uint16_t*)calloc((size_t)o->XB, 2);
   s->hca_code = (uint8_t*)calloc(1, (size_t)o->esz);
   s->hca_scale[0] = s->hca_scale[1] = 0;
 }
@@ -277,7 +278,8 @@ static void hash_f32s(hasher* x, const float* f, int64_t n) {
 static uint64_t config_fingerprint(const kvo_config* c) {
   hasher x = {0xcbf29ce484222325ull};
   const int32_t f[11] = {c->m,       c->m_prime,  c->n_win,       c->heads,   c->head_dim, c->idx_heads,
-                         c->idx_dim, c->in_dtype, c->cache_dtype, c->idx_fp4, c->n_layers};
+                         c->idx_dim, c->in_dtype, c->cache_dtype, c->idx_fp4 | (c->idx_per_token << 1),
+                         c->n_layers};
   for (int i = 0; i < 11; ++i) hash_i32(&x, f[i]);
   for (int l = 0; l < c->n_layers; ++l) {
     const int k = c->layer_kinds[l];
@@ -302,6 +304,7 @@ int kvo_create(const kvo_config* cfg, kvo_t** out) {
   if (c->in_dtype != KVO_F32 && c->in_dtype != KVO_BF16) return KVO_ERR_INVALID_ARG;
   if (c->cache_dtype < KVO_F32 || c->cache_dtype > KVO_FP8) return KVO_ERR_INVALID_ARG;
   if (c->idx_fp4 != 0 && c->idx_fp4 != 1) return KVO_ERR_INVALID_ARG;
+  if (c->idx_per_token != 0 && c->idx_per_token != 1) return KVO_ERR_INVALID_ARG;
   if (c->n_layers < 1 || !c->layer_kinds) return KVO_ERR_INVALID_ARG;
   if (c->max_requests < 1 || c->max_blocks < 1 || c->max_blocks_per_request < 1) return KVO_ERR_INVALID_ARG;
   for (int l = 0; l < c->n_layers; ++l)
@@ -315,6 +318,7 @@ int kvo_create(const kvo_config* cfg, kvo_t** out) {
   o->HD = c->heads * c->head_dim;
   o->XD = c->idx_heads * c->idx_dim;
   o->CB = c->m_prime / c->m; /* CSA entries per block */
+  o->XB = c->idx_per_token ? c->m_prime : o->CB;
   o->vs = kvo_value_bytes(c->cache_dtype);
   o->esz = 2 * o->HD * o->vs;
   o->idx_dtype = c->idx_fp4 ? KVO_FP4 : c->cache_dtype;
@@ -453,6 +457,25 @@ float kvo_score(const kvo_t* o, const uint8_t* code, const uint16_t* scale, cons
   for (int v = 0; v < o->XD; ++v) a = fmaf(q_idx[v], raw_value(o->idx_dtype, code, v), a);
   if (o->idx_dtype == KVO_FP8 || o->idx_dtype == KVO_FP4) a = a * kvo_f32_from_bf16(*scale);
   return a;
+}
+
+float kvo_score_tokens(const kvo_t* o, int layer, const uint8_t* codes, const uint16_t* scales, const float* q_idx) {
+  const int m = o->c.m, Ih = o->c.idx_heads, Id = o->c.idx_dim;
+  const float* alpha = o->alpha_idx + (size_t)layer * Ih * m;
+  const int scaled = o->idx_dtype == KVO_FP8 || o->idx_dtype == KVO_FP4;
+  float s = 0.0f;
+  for (int i = 0; i < m; ++i) {
+    const uint8_t* code = codes + (size_t)i * o->xsz;
+    float p = 0.0f;
+    for (int j = 0; j < Ih; ++j) {
+      float d = 0.0f;
+      for (int v = j * Id; v < (j + 1) * Id; ++v) d = fmaf(q_idx[v], (float)raw_value(o->idx_dtype, code, v), d);
+      if (scaled) d = d * kvo_f32_from_bf16(scales[i]);
+      p = fmaf(alpha[(size_t)j * m + i], d, p);
+    }
+    s = i == 0 ? p : s + p;
+  }
+  return s;
 }
 
 typedef struct cand {
@@ -662,14 +685,20 @@ static void token_into_layer(kvo_t* o, request* q, int l, const float* kv, const
     rl->tail_len += 1;
   }
   if (has_csa(o, l)) {
-    memcpy(rl->tail_idx + (size_t)rl->tail_idx_len * o->XD, idx, sizeof(float) * (size_t)o->XD);
-    rl->tail_idx_len += 1;
+    if (o->c.idx_per_token) { /* the token's own indexer key, at its place in the block */
+      int slot = (int)(pos % o->c.m_prime);
+      kvo_encode(o->idx_dtype, idx, o->XD, rl->stage.idx_code + (size_t)slot * o->xsz, rl->stage.idx_scale + slot);
+    } else {
+      memcpy(rl->tail_idx + (size_t)rl->tail_idx_len * o->XD, idx, sizeof(float) * (size_t)o->XD);
+      rl->tail_idx_len += 1;
+    }
     if ((pos + 1) % o->c.m == 0) { /* a CSA group of m tokens is complete */
       int64_t g = (pos + 1) / o->c.m - 1;
       int slot = (int)(g % o->CB);
       const float* group = rl->tail_kv + (size_t)(rl->tail_len - o->c.m) * HD2;
       kvo_compress_kv(o, l, 1, group, rl->stage.csa_code + (size_t)slot * o->esz, rl->stage.csa_scale + 2 * slot);
-      kvo_compress_idx(o, l, rl->tail_idx, rl->stage.idx_code + (size_t)slot * o->xsz, rl->stage.idx_scale + slot);
+      if (!o->c.idx_per_token)
+        kvo_compress_idx(o, l, rl->tail_idx, rl->stage.idx_code + (size_t)slot * o->xsz, rl->stage.idx_scale + slot);
       rl->tail_idx_len = 0;
     }
   }
@@ -691,8 +720,8 @@ static void seal_block(kvo_t* o, request* q) {
     if (has_csa(o, l)) {
       memcpy(dst->csa_code, rl->stage.csa_code, (size_t)o->CB * o->esz);
       memcpy(dst->csa_scale, rl->stage.csa_scale, (size_t)o->CB * 2 * 2);
-      memcpy(dst->idx_code, rl->stage.idx_code, (size_t)o->CB * o->xsz);
-      memcpy(dst->idx_scale, rl->stage.idx_scale, (size_t)o->CB * 2);
+      memcpy(dst->idx_code, rl->stage.idx_code, (size_t)o->XB * o->xsz);
+      memcpy(dst->idx_scale, rl->stage.idx_scale, (size_t)o->XB * 2);
     }
     if (has_hca(o, l)) {
       memcpy(dst->hca_code, rl->hca_new, (size_t)o->esz);
@@ -791,10 +820,16 @@ static void locate_entry(const kvo_t* o, int l, const request* q, int kind, int6
   if (kind == 1) {
     *code = sec->csa_code + (size_t)slot * o->esz;
     *scale = sec->csa_scale + 2 * slot;
-  } else {
-    *code = sec->idx_code + (size_t)slot * o->xsz;
-    *scale = sec->idx_scale + slot;
+  } else { /* per-token keys: the entry's first token; its m tokens follow */
+    const int ks = o->c.idx_per_token ? slot * o->c.m : slot;
+    *code = sec->idx_code + (size_t)ks * o->xsz;
+    *scale = sec->idx_scale + ks;
   }
+}
+
+/* indexer score of a CSA entry located by locate_entry (kind 3) */
+static float entry_score(const kvo_t* o, int l, const uint8_t* code, const uint16_t* scale, const float* q_idx) {
+  return o->c.idx_per_token ? kvo_score_tokens(o, l, code, scale, q_idx) : kvo_score(o, code, scale, q_idx);
 }
 
 int kvo_decode_attend(kvo_t* o, int layer, int n, const int32_t* req_ids, const float* q, const float* q_idx,
@@ -820,7 +855,7 @@ int kvo_decode_attend(kvo_t* o, int layer, int n, const int32_t* req_ids, const 
         const uint8_t* c;
         const uint16_t* sc;
         locate_entry(o, layer, r, 3, e, &c, &sc);
-        s[e] = kvo_score(o, c, sc, q_idx + (size_t)i * XD);
+        s[e] = entry_score(o, layer, c, sc, q_idx + (size_t)i * XD);
       }
       kvo_topk(s, N_c, top_k, sel);
       free(s);
@@ -900,7 +935,7 @@ int kvo_block_entry(const kvo_t* o, int l, int32_t b, int kind, int slot, uint8_
   } else if (kind == 2 && has_hca(o, l) && slot == 0) {
     memcpy(code, sec->hca_code, (size_t)o->esz);
     memcpy(scale, sec->hca_scale, 4);
-  } else if (kind == 3 && has_csa(o, l) && slot >= 0 && slot < o->CB) {
+  } else if (kind == 3 && has_csa(o, l) && slot >= 0 && slot < o->XB) {
     memcpy(code, sec->idx_code + (size_t)slot * o->xsz, (size_t)o->xsz);
     scale[0] = sec->idx_scale[slot];
   } else {
@@ -913,6 +948,15 @@ int kvo_request_entry(const kvo_t* o, int l, int32_t r, int kind, int64_t e, uin
   if (!o || l < 0 || l >= o->c.n_layers || (kind != 1 && kind != 3) || !has_csa(o, l)) return KVO_ERR_INVALID_ARG;
   if (!req_ok(o, r)) return KVO_ERR_BAD_REQUEST;
   const request* q = &o->reqs[r];
+  if (kind == 3 && o->c.idx_per_token) { /* per-token keys: e is a token position */
+    if (e < 0 || e >= q->L) return KVO_ERR_INVALID_ARG;
+    const int64_t seg = e / o->c.m_prime;
+    const int slot = (int)(e % o->c.m_prime);
+    const layer_sec* sec = seg < q->n_sealed ? &o->blocks[q->table[seg]].layers[l] : &q->layers[l].stage;
+    memcpy(code, sec->idx_code + (size_t)slot * o->xsz, (size_t)o->xsz);
+    scale[0] = sec->idx_scale[slot];
+    return KVO_OK;
+  }
   if (e < 0 || e >= q->L / o->c.m) return KVO_ERR_INVALID_ARG;
   const uint8_t* c;
   const uint16_t* sc;
@@ -946,7 +990,7 @@ int kvo_request_scores(const kvo_t* o, int l, int32_t r, const float* q_idx, flo
     const uint8_t* c;
     const uint16_t* sc;
     locate_entry(o, l, q, 3, e, &c, &sc);
-    out[e] = kvo_score(o, c, sc, q_idx);
+    out[e] = entry_score(o, l, c, sc, q_idx);
   }
   return KVO_OK;
 }
@@ -961,9 +1005,12 @@ static int64_t round16(int64_t x) { return (x + 15) / 16 * 16; }
 static int idx_has_scale(const kvo_t* o) { return o->idx_dtype == KVO_FP8 || o->idx_dtype == KVO_FP4; }
 /* bytes of one K/V entry record: codes, then fp8 scales and zero padding */
 static int64_t entry_rec(const kvo_t* o) { return o->esz + (o->c.cache_dtype == KVO_FP8 ? 16 : 0); }
-static int64_t idx_part(const kvo_t* o) {
+/* one run of CB indexer keys: codes chunk-major, then fp8 / FP4 scales padded
+ * to 16 bytes; a block holds XB / CB runs (one, or m with per-token keys) */
+static int64_t idx_run(const kvo_t* o) {
   return (int64_t)o->CB * o->xsz + (idx_has_scale(o) ? round16(2 * (int64_t)o->CB) : 0);
 }
+static int64_t idx_part(const kvo_t* o) { return (int64_t)(o->XB / o->CB) * idx_run(o); }
 /* bytes of one block's parts summed over the layers */
 static int64_t block_rec(const kvo_t* o) {
   int64_t b = 0;
@@ -1030,24 +1077,31 @@ static void rec_to_entry(const kvo_t* o, const uint8_t* rec, uint8_t* code, uint
 /* a block's indexer part: keys chunk by chunk, then the scales */
 static void idx_to_part(const kvo_t* o, const layer_sec* s, uint8_t* part) {
   memset(part, 0, (size_t)idx_part(o));
-  for (int e = 0; e < o->CB; ++e)
-    for (int j = 0; j < o->xsz; ++j)
-      part[((int64_t)(j / 16) * o->CB + e) * 16 + j % 16] = s->idx_code[(size_t)e * o->xsz + j];
-  if (idx_has_scale(o)) {
-    uint8_t* t = part + (int64_t)o->CB * o->xsz;
-    for (int e = 0; e < o->CB; ++e) {
-      t[2 * e] = (uint8_t)s->idx_scale[e];
-      t[2 * e + 1] = (uint8_t)(s->idx_scale[e] >> 8);
+  for (int q = 0; q < o->XB / o->CB; ++q) {
+    uint8_t* run = part + q * idx_run(o);
+    for (int e = 0; e < o->CB; ++e)
+      for (int j = 0; j < o->xsz; ++j)
+        run[((int64_t)(j / 16) * o->CB + e) * 16 + j % 16] = s->idx_code[(size_t)(q * o->CB + e) * o->xsz + j];
+    if (idx_has_scale(o)) {
+      uint8_t* t = run + (int64_t)o->CB * o->xsz;
+      for (int e = 0; e < o->CB; ++e) {
+        t[2 * e] = (uint8_t)s->idx_scale[q * o->CB + e];
+        t[2 * e + 1] = (uint8_t)(s->idx_scale[q * o->CB + e] >> 8);
+      }
     }
   }
 }
 
 static void part_to_idx(const kvo_t* o, const uint8_t* part, layer_sec* s) {
-  for (int e = 0; e < o->CB; ++e)
-    for (int j = 0; j < o->xsz; ++j)
-      s->idx_code[(size_t)e * o->xsz + j] = part[((int64_t)(j / 16) * o->CB + e) * 16 + j % 16];
-  const uint8_t* t = part + (int64_t)o->CB * o->xsz;
-  for (int e = 0; e < o->CB; ++e) s->idx_scale[e] = idx_has_scale(o) ? (uint16_t)(t[2 * e] | (t[2 * e + 1] << 8)) : 0;
+  for (int q = 0; q < o->XB / o->CB; ++q) {
+    const uint8_t* run = part + q * idx_run(o);
+    for (int e = 0; e < o->CB; ++e)
+      for (int j = 0; j < o->xsz; ++j)
+        s->idx_code[(size_t)(q * o->CB + e) * o->xsz + j] = run[((int64_t)(j / 16) * o->CB + e) * 16 + j % 16];
+    const uint8_t* t = run + (int64_t)o->CB * o->xsz;
+    for (int e = 0; e < o->CB; ++e)
+      s->idx_scale[q * o->CB + e] = idx_has_scale(o) ? (uint16_t)(t[2 * e] | (t[2 * e + 1] << 8)) : 0;
+  }
 }
 
 int kvo_export_prefix(const kvo_t* o, int32_t req, int64_t n_tokens, uint32_t flags, uint8_t* image, int64_t cap) {

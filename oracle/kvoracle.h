@@ -84,6 +84,10 @@ typedef struct kvo_config {
    * slots and host slots; csa_hot_slots 0 = no HiSparse (every block's CSA
    * entries stay where the block is) */
   int32_t csa_hot_slots, csa_host_slots;
+  /* 1: the indexer keeps one key per token (m' per block) instead of one per
+   * CSA entry; an entry's score combines its m tokens' scores with the
+   * entry's indexer gates (kvo_score_tokens) */
+  int32_t idx_per_token;
 } kvo_config;
 
 typedef struct kvo kvo_t;
@@ -117,6 +121,13 @@ int kvo_compress_kv(const kvo_t* o, int layer, int kind, const float* tokens, ui
 int kvo_compress_idx(const kvo_t* o, int layer, const float* keys, uint8_t* code, uint16_t* scale);
 /* indexer score of one encoded indexer entry */
 float kvo_score(const kvo_t* o, const uint8_t* code, const uint16_t* scale, const float* q_idx);
+/* indexer score of a CSA entry from its m tokens' encoded keys (per-token
+ * indexer keys; codes [m][Ih*Id*vsize] and scales [m] contiguous), gates of
+ * `layer`: token i's head-j dot D = fmaf chain over idx_dim from +0 (times
+ * the token's scale for fp8 / FP4), p_i = fmaf chain over heads of
+ * alpha_idx[j][i] * D, score = ((p_0 + p_1) + p_2) + ... in token order.
+ * By linearity this is the per-entry score of the uncompressed keys. */
+float kvo_score_tokens(const kvo_t* o, int layer, const uint8_t* codes, const uint16_t* scales, const float* q_idx);
 /* top-k over n scores: writes k = min(top_k, n) ascending indices, then -1 up to top_k */
 int kvo_topk(const float* scores, int64_t n, int top_k, int32_t* out);
 /* attention of q ([heads][head_dim]) over n_src encoded entries laid out
@@ -175,14 +186,15 @@ int kvo_request_scores(const kvo_t* o, int layer, int32_t req, const float* q_id
  *     n_tokens - w .. n_tokens - 1.
  *   A K/V entry (CSA, HCA, window token) is its codes (K half, V half), then
  *   for fp8 the bf16 K and V scales and 12 zero bytes.  A block's indexer
- *   part is its CB = m'/m keys 16-byte chunk by chunk (byte j of key e at
- *   ((j / 16) * CB + e) * 16 + j % 16), then for fp8 / FP4 keys the CB bf16
- *   scales, zero-padded to a multiple of 16 bytes.  Images need each
+ *   part is one run per CB = m'/m keys (one run, or m runs with per-token
+ *   keys, tokens in order): the run's keys 16-byte chunk by chunk (byte j
+ *   of key e at ((j / 16) * CB + e) * 16 + j % 16), then for fp8 / FP4 keys
+ *   the CB bf16 scales, zero-padded to a multiple of 16 bytes.  Images need each
  *   indexer key to be whole 16-byte chunks (when a layer has CSA); other
  *   configs are refused (INVALID_ARG, image bytes -1).
  * The fingerprint is FNV-1a (64-bit) over the little-endian int32 fields m,
  * m', n_win, heads, head_dim, idx_heads, idx_dim, in_dtype, cache_dtype,
- * idx_fp4, n_layers, then per layer its kind followed by the fp32 bits of
+ * idx_fp4 + 2 * idx_per_token, n_layers, then per layer its kind followed by the fp32 bits of
  * its gate logits (CSA then indexer if the layer has CSA; HCA if it has HCA).
  */
 #define KVO_IMAGE_WINDOW 1u

@@ -26,7 +26,7 @@ def make_oracle(cfg, max_requests, max_blocks, max_blocks_per_request, gate_over
                     max_requests=max_requests, max_blocks=max_blocks,
                     max_blocks_per_request=max_blocks_per_request, gate_csa=g_csa, gate_hca=g_hca,
                     gate_idx=g_idx, idx_fp4=cfg.get("idx_fp4", 0), csa_hot_slots=cfg.get("csa_hot_slots", 0),
-                    csa_host_slots=cfg.get("csa_host_slots", 0))
+                    csa_host_slots=cfg.get("csa_host_slots", 0), idx_per_token=cfg.get("idx_per_token", 0))
 
 
 def _values(cfg, n_values, runs, out=None):
