@@ -186,7 +186,9 @@ __device__ __forceinline__ void st8f(float* p, const float* x) {
   reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
 }  // tokens whose loads are issued together
 
-template <int IN, int CACHE>
+// PT: per-token indexer keys (the pool's idx_per_token), a separate
+// instantiation so the per-entry path keeps its registers
+template <int IN, int CACHE, bool PT>
 __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ AppendParams P) {
   pdl_start();
   __shared__ float sh[3 * 16];
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   // copy_slices CTAs of the unit (this call's own entries go to the block
   // directly).
   if (slice >= P.n_slices) {
-    if (u.block_id < 0 || !L.has_csa || u.t0 < m) return;
+    if (u.block_id < 0 || !L.has_csa || u.t0 < (PT ? 1 : m)) return;
     const int cs = slice - P.n_slices, ncs = P.copy_slices;
     const int n_copy = u.t0 / m;
     const int CB = pd.csa_per_block;
@@ -223,16 +225,20 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
     const int64_t units = (int64_t)n_copy * pd.entry_bytes / 16;  // CSA entries, 16-byte units
     for (int64_t o = (int64_t)cs * blockDim.x + tid; o < units; o += (int64_t)ncs * blockDim.x)
       reinterpret_cast<uint4*>(dst_csa)[o] = reinterpret_cast<const uint4*>(stg_csa)[o];
-    for (int64_t k = (int64_t)cs * blockDim.x + tid; k < (int64_t)pd.idx_chunks * n_copy; k += (int64_t)ncs * blockDim.x) {
-      const int c = (int)(k / n_copy), e = (int)(k % n_copy);
-      const int64_t o = ((int64_t)c * CB + e) * 16;
+    // indexer keys: of the staged entries, or with per-token keys of the
+    // staged tokens (key e in run e / CB, slot e % CB)
+    const int n_keys = PT ? u.t0 : n_copy;
+    for (int64_t k = (int64_t)cs * blockDim.x + tid; k < (int64_t)pd.idx_chunks * n_keys; k += (int64_t)ncs * blockDim.x) {
+      const int c = (int)(k / n_keys), e = (int)(k % n_keys);
+      const int64_t o = (int64_t)(e / CB) * L.idx_run + ((int64_t)c * CB + e % CB) * 16;
       *reinterpret_cast<uint4*>(dst_idx + o) = *reinterpret_cast<const uint4*>(stg_idx + o);
     }
     const bool scaled = pd.idx_dtype == KVPOOL_FP8_E4M3 || pd.idx_dtype == KVPOOL_FP4_E2M1;
     if (scaled && cs == 0)
-      for (int e = tid; e < n_copy; e += blockDim.x)
-        *reinterpret_cast<uint16_t*>(dst_idx + L.idx_scale_off + 2 * e) =
-            *reinterpret_cast<const uint16_t*>(stg_idx + L.idx_scale_off + 2 * e);
+      for (int e = tid; e < n_keys; e += blockDim.x) {
+        const int64_t o = (int64_t)(e / CB) * L.idx_run + L.idx_scale_off + 2 * (e % CB);
+        *reinterpret_cast<uint16_t*>(dst_idx + o) = *reinterpret_cast<const uint16_t*>(stg_idx + o);
+      }
     return;
   }
 
@@ -311,7 +317,29 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
         const float a = a_csa[t % m];
 #pragma unroll
         for (int j = 0; j < kVpt; ++j) acc_c[j] = __fmaf_rn(a, x[j], acc_c[j]);
-        if (idx_thread) {
+        if constexpr (PT) {
+          // the token's own indexer key, at key t % CB of run t / CB; the
+          // indexer threads are the first XD / 8 lanes of warp 0
+          if (slice == 0 && tid < 32) {
+            float y[kVpt];
+            if (idx_thread) InTraits<IN>::unpack(yr[gi], y);
+            float s = 1.0f;
+            uint8_t* run = blk_idx + (int64_t)(t / pd.csa_per_block) * L.idx_run;
+            const int key = t % pd.csa_per_block;
+            if (idx_scaled) {
+              float a = idx_thread ? amax8(y) : 0.0f;
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+              const uint16_t sb = idx_fp4 ? fp4_scale_bits(a) : fp8_scale_bits(a);
+              s = bf16_bits_to_f32(sb);
+              if (idx_thread && xv0 == 0) *reinterpret_cast<uint16_t*>(run + L.idx_scale_off + 2 * key) = sb;
+            }
+            if (idx_thread) {
+              if (idx_fp4) write_idx_fp4(run, pd, key, xv0, y, s);
+              else write_idx<CACHE>(run, pd, key, xv0, y, s);
+            }
+          }
+        } else if (idx_thread) {
           float y[kVpt];
           InTraits<IN>::unpack(yr[gi], y);
           const float b = a_idx[t % m];
@@ -322,13 +350,13 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
           const int slot = (t + 1) / m - 1;
           write_entry<CACHE>(blk_csa + (int64_t)slot * pd.entry_bytes, pd, v0, half, hv, acc_c, sh);
           float s = 1.0f;
-          if (idx_scaled) {  // uniform over the CTA: block-wide amax of the indexer entry
+          if (idx_scaled && !PT) {  // uniform over the CTA: block-wide amax of the indexer entry
             const float3 r = block_max3(0.f, 0.f, idx_thread ? amax8(acc_x) : 0.f, sh);
             const uint16_t sb = idx_fp4 ? fp4_scale_bits(r.z) : fp8_scale_bits(r.z);
             s = bf16_bits_to_f32(sb);
             if (idx_thread && xv0 == 0) *reinterpret_cast<uint16_t*>(blk_idx + L.idx_scale_off + 2 * slot) = sb;
           }
-          if (idx_thread) {
+          if (idx_thread && !PT) {
             if (idx_fp4) write_idx_fp4(blk_idx, pd, slot, xv0, acc_x, s);
             else write_idx<CACHE>(blk_idx, pd, slot, xv0, acc_x, s);
           }
@@ -423,14 +451,27 @@ int launch_append(const AppendParams& p, int n_layers, void* stream, int* n_kern
   dim3 grid(p.n_units, p.n_slices + p.copy_slices, n_layers);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const int key = p.pool.in_dtype * 3 + p.pool.cache_dtype;
+  auto go = [&](auto entry_kernel, auto token_kernel) {
+    launch_kernel(true, p.pool.idx_per_token ? token_kernel : entry_kernel, grid, dim3(threads), 0, s, p);
+  };
   switch (key) {
-    case KVPOOL_F32 * 3 + KVPOOL_F32: launch_kernel(true, append_kernel<KVPOOL_F32, KVPOOL_F32>, grid, dim3(threads), 0, s, p); break;
-    case KVPOOL_F32 * 3 + KVPOOL_BF16: launch_kernel(true, append_kernel<KVPOOL_F32, KVPOOL_BF16>, grid, dim3(threads), 0, s, p); break;
-    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3: launch_kernel(true, append_kernel<KVPOOL_F32, KVPOOL_FP8_E4M3>, grid, dim3(threads), 0, s, p); break;
-    case KVPOOL_BF16 * 3 + KVPOOL_F32: launch_kernel(true, append_kernel<KVPOOL_BF16, KVPOOL_F32>, grid, dim3(threads), 0, s, p); break;
-    case KVPOOL_BF16 * 3 + KVPOOL_BF16: launch_kernel(true, append_kernel<KVPOOL_BF16, KVPOOL_BF16>, grid, dim3(threads), 0, s, p); break;
+    case KVPOOL_F32 * 3 + KVPOOL_F32:
+      go(append_kernel<KVPOOL_F32, KVPOOL_F32, false>, append_kernel<KVPOOL_F32, KVPOOL_F32, true>);
+      break;
+    case KVPOOL_F32 * 3 + KVPOOL_BF16:
+      go(append_kernel<KVPOOL_F32, KVPOOL_BF16, false>, append_kernel<KVPOOL_F32, KVPOOL_BF16, true>);
+      break;
+    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3:
+      go(append_kernel<KVPOOL_F32, KVPOOL_FP8_E4M3, false>, append_kernel<KVPOOL_F32, KVPOOL_FP8_E4M3, true>);
+      break;
+    case KVPOOL_BF16 * 3 + KVPOOL_F32:
+      go(append_kernel<KVPOOL_BF16, KVPOOL_F32, false>, append_kernel<KVPOOL_BF16, KVPOOL_F32, true>);
+      break;
+    case KVPOOL_BF16 * 3 + KVPOOL_BF16:
+      go(append_kernel<KVPOOL_BF16, KVPOOL_BF16, false>, append_kernel<KVPOOL_BF16, KVPOOL_BF16, true>);
+      break;
     case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3:
-      launch_kernel(true, append_kernel<KVPOOL_BF16, KVPOOL_FP8_E4M3>, grid, dim3(threads), 0, s, p);
+      go(append_kernel<KVPOOL_BF16, KVPOOL_FP8_E4M3, false>, append_kernel<KVPOOL_BF16, KVPOOL_FP8_E4M3, true>);
       break;
     default: return (int)cudaErrorInvalidValue;
   }

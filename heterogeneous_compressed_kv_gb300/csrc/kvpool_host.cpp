@@ -102,6 +102,11 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
   if (XD % 16 != 0 || XD > 8 * 256) return "idx_heads * idx_dim must be a multiple of 16, at most 2048";
   if (c->idx_fp4 != 0 && c->idx_fp4 != 1) return "idx_fp4 must be 0 or 1";
   if (c->idx_fp4 && XD % 32 != 0) return "FP4 indexer entries need idx_heads * idx_dim to be a multiple of 32";
+  if (c->idx_per_token != 0 && c->idx_per_token != 1) return "idx_per_token must be 0 or 1";
+  if (c->idx_per_token && XD > 256) return "per-token indexer keys need idx_heads * idx_dim <= 256";
+  if (c->idx_per_token && c->idx_heads * c->m > 64) return "per-token indexer keys need idx_heads * m <= 64";
+  if (c->idx_per_token && ((c->idx_fp4 ? c->idx_dim / 2 : c->idx_dim * value_bytes(c->cache_dtype)) % 16 != 0))
+    return "per-token indexer keys need each head's key to be whole 16-byte chunks";
   if (c->csa_hot_slots < 0 || c->csa_host_slots < 0 || c->csa_hot_slots > c->max_blocks ||
       (c->csa_hot_slots == 0 && c->csa_host_slots > 0))
     return "HiSparse slots: 0 <= csa_hot_slots <= max_blocks, host slots only with hot slots";
@@ -135,6 +140,8 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
   pd.idx_dtype = c->idx_fp4 ? KVPOOL_FP4_E2M1 : c->cache_dtype;
   pd.idx_entry_bytes = c->idx_fp4 ? (int64_t)XD / 2 : (int64_t)XD * vs;
   pd.idx_chunks = (int32_t)(pd.idx_entry_bytes / 16);
+  pd.idx_per_token = c->idx_per_token;
+  pd.idx_runs = c->idx_per_token ? c->m : 1;
   pd.entry_bytes = 2LL * HD * vs + (c->cache_dtype == KVPOOL_FP8_E4M3 ? 16 : 0);
   pd.max_blocks = c->max_blocks;
   pd.max_requests = c->max_requests;
@@ -168,7 +175,7 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
     const int64_t n_ids = (int64_t)c->max_blocks + c->max_requests;
     const int64_t n_csa_slots = (int64_t)pd.csa_staging_base + c->max_requests;
     d.csa_pool = d.idx_pool = d.hca_pool = d.idx_scale_off = d.csa_host_off = -1;
-    d.csa_stride = d.idx_stride = d.hca_stride = 0;
+    d.csa_stride = d.idx_stride = d.hca_stride = d.idx_run = 0;
     if (d.has_csa) {
       d.csa_stride = CB * pd.entry_bytes;
       d.csa_pool = cur;
@@ -177,11 +184,12 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
         d.csa_host_off = pd.host_slot_bytes;
         pd.host_slot_bytes += d.csa_stride;
       }
-      d.idx_stride = CB * pd.idx_entry_bytes;
+      d.idx_run = CB * pd.idx_entry_bytes;
       if (pd.idx_dtype == KVPOOL_FP8_E4M3 || pd.idx_dtype == KVPOOL_FP4_E2M1) {
-        d.idx_scale_off = d.idx_stride;
-        d.idx_stride += round_up(2LL * CB, 16);
+        d.idx_scale_off = d.idx_run;
+        d.idx_run += round_up(2LL * CB, 16);
       }
+      d.idx_stride = d.idx_run * pd.idx_runs;
       d.idx_pool = cur;
       cur = round_up(cur + d.idx_stride * n_ids, 256);
     }
@@ -246,7 +254,7 @@ void softmax_rows(const float* g, int rows, int n, std::vector<float>* out) {
 
 // FNV-1a 64 (Fowler, Noll, Vo) over the prefix-image config record:
 // little-endian int32 m, m', n_win, heads, head_dim, idx_heads, idx_dim,
-// in_dtype, cache_dtype, idx_fp4, n_layers, then per layer its kind and the
+// in_dtype, cache_dtype, idx_fp4 + 2 * idx_per_token, n_layers, then per layer its kind and the
 // fp32 bits of the gate logits it uses (CSA then indexer; HCA).  A gate array
 // that is NULL (a pool without device memory) adds nothing.
 struct Fnv1a {
@@ -270,7 +278,8 @@ struct Fnv1a {
 uint64_t config_fingerprint(const kvpool_config* c) {
   Fnv1a x;
   const int32_t f[11] = {c->m,       c->m_prime,  c->n_win,       c->heads,   c->head_dim, c->idx_heads,
-                         c->idx_dim, c->in_dtype, c->cache_dtype, c->idx_fp4, c->n_layers};
+                         c->idx_dim, c->in_dtype, c->cache_dtype, c->idx_fp4 | (c->idx_per_token << 1),
+                         c->n_layers};
   for (int32_t v : f) x.u32((uint32_t)v);
   for (int l = 0; l < c->n_layers; ++l) {
     const int k = c->layer_kinds[l];
@@ -656,10 +665,11 @@ void image_segments(const kvpool_t* p, const std::vector<int32_t>& ids, const st
     const LayerDesc& d = p->lay.layers[l];
     if (d.has_csa) {
       for (int64_t b = 0; b < nb; ++b) add(p->csa_addr(d, locs[b]), locs[b] < 0, d.csa_stride, 0, 0);
+      // the padding after each run's scales is written as zeros
       const int64_t valid = d.idx_scale_off + 2LL * pd.csa_per_block;
-      const int32_t mvalid = idx_scaled && valid < d.idx_stride ? (int32_t)valid : 0;
+      const int32_t mvalid = idx_scaled && valid < d.idx_run ? (int32_t)valid : 0;
       for (int64_t b = 0; b < nb; ++b)
-        add(arena + d.idx_pool + (uint64_t)ids[b] * d.idx_stride, false, d.idx_stride, mvalid ? (int32_t)d.idx_stride : 0,
+        add(arena + d.idx_pool + (uint64_t)ids[b] * d.idx_stride, false, d.idx_stride, mvalid ? (int32_t)d.idx_run : 0,
             mvalid);
     }
     if (d.has_hca)
@@ -1090,7 +1100,8 @@ int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_
         // copy CTAs for them
         ap->copy_slices = 0;
         for (int32_t k = 0; k < ap->n_units; ++k)
-          if (any_csa && ap->units[k].block_id >= 0 && ap->units[k].t0 >= p->cfg.m) ap->copy_slices = kSealCopySlices;
+          if (any_csa && ap->units[k].block_id >= 0 && ap->units[k].t0 >= (p->cfg.idx_per_token ? 1 : p->cfg.m))
+            ap->copy_slices = kSealCopySlices;  // staged entries (or per-token keys) move into the block
         rc = p->launch(KVPOOL_KERNEL_APPEND, bytes, stream, [&](int* nk) { return launch_append(*ap, p->cfg.n_layers, stream, nk); });
         bytes = 0;
       }
@@ -1137,6 +1148,7 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
 
   const PoolDesc& pd = p->lay.pd;
   const int CB = pd.csa_per_block;
+  const int EPS = pd.idx_per_token ? CB / p->cfg.m : CB;  // CSA entries per score segment (a block, or a run of tokens)
   const int max_split_len = attend_max_split_len();
   AttendParams* ap = new AttendParams();
   int rc = 0;
@@ -1179,8 +1191,8 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
       const int32_t n_cand = Ld.has_csa ? (int32_t)(q.length / p->cfg.m) : 0;
       const int32_t k = std::min(top_k, n_cand);
       if (k != n_cand && k > 0) {
-        total_segs += (n_cand + CB - 1) / CB;
-        req_segs.push_back((n_cand + CB - 1) / CB);
+        total_segs += (n_cand + EPS - 1) / EPS;
+        req_segs.push_back((n_cand + EPS - 1) / EPS);
       }
     }
     // a score CTA takes a run of one request's segments; every request rounds
@@ -1200,10 +1212,10 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
       R.n_hca = Ld.has_hca ? (int32_t)(q.length / p->cfg.m_prime) : 0;
       R.w = (int32_t)std::min<int64_t>(q.length, p->cfg.n_win);
       R.score_base = score_ctas;
-      const int nseg = (R.n_cand + CB - 1) / CB;
+      const int nseg = (R.n_cand + EPS - 1) / EPS;
       if (!R.select_all && R.k > 0) {
         score_ctas += (nseg + P.segs_per_cta - 1) / P.segs_per_cta;
-        score_bytes += (int64_t)R.n_cand * idx_algo + (int64_t)nseg * 4 + (int64_t)pd.XD * pd.isz;
+        score_bytes += (int64_t)R.n_cand * pd.idx_runs * idx_algo + (int64_t)nseg * 4 + (int64_t)pd.XD * pd.isz;
       }
       R.key_base = key_ctas;
       // select CTAs: one per 4096 candidates; at least one when topk_out needs its -1 padding

@@ -34,6 +34,7 @@ struct LayerDesc {
   // scales at idx_scale_off inside a block's part), HCA entry
   int64_t csa_pool, csa_stride;
   int64_t idx_pool, idx_stride, idx_scale_off;
+  int64_t idx_run;  // bytes of one run of csa_per_block keys (+ scales); a block part holds idx_runs runs
   int64_t hca_pool, hca_stride;
   int64_t ring, ring_req_bytes;
   int64_t acc, acc_req_bytes;  // acc: CSA [2HD] f32, idx [XD] f32, HCA [2HD] f32
@@ -49,6 +50,7 @@ struct PoolDesc {
   int32_t in_dtype, cache_dtype, vs, isz;  // cache value bytes, input value bytes
   int32_t idx_dtype;                       // indexer entries: cache_dtype or KVPOOL_FP4_E2M1
   int32_t csa_per_block, idx_chunks;       // idx_chunks: 16-B chunks per indexer key
+  int32_t idx_per_token, idx_runs;         // per-token keys: m runs of csa_per_block keys per block, else 1 run
   int64_t entry_bytes, idx_entry_bytes;
   int32_t max_blocks, max_requests, max_bpr, staging_base;
   int64_t table;  // int32 [max_requests][max_bpr]

@@ -182,10 +182,16 @@ struct ScoreShape {
 constexpr int kScoreMaxWarps = 16;
 constexpr int kScoreMaxRing = 3;                      // slots per warp
 constexpr int kScoreMaxSlots = kScoreMaxWarps * kScoreMaxRing;
+constexpr int kScoreMaxGates = 64;  // per-token keys: idx_heads * m gates in shared memory
 constexpr int kScoreStageBudget = 140 * 1024;         // shared memory for slots: two per warp measured as fast as three
 __host__ __device__ constexpr int score_warps(int idx_dtype) { return idx_dtype == KVPOOL_FP4_E2M1 ? 16 : 8; }
 
-template <int IN, int CACHE>
+// PT: per-token indexer keys.  A segment is then one run of csa_per_block
+// tokens (csa_per_block / m entries) instead of one block; lane t scores
+// token t: each head's fp32 chain times the token's scale, an fp32 FMA chain
+// over the heads with the entry's gates alpha_idx[j][t % m], and the entry's
+// first lane adds its m tokens in order.
+template <int IN, int CACHE, bool PT>
 __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kernel(const __grid_constant__ AttendParams P, int stage_bytes,
                                                                  int ring, int stage_off) {
   pdl_start();
@@ -204,7 +210,14 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
   const int i = find_req(P, blockIdx.x, 0);
   const AttendReq& R = P.reqs[i];
   const int CB = pd.csa_per_block;
-  const int nseg = (R.n_cand + CB - 1) / CB;
+  const int m = pd.m;
+  const int EPS = PT ? CB / m : CB;  // entries per segment
+  const int nseg = (R.n_cand + EPS - 1) / EPS;
+  __shared__ float a_sh[kScoreMaxGates];  // per-token keys: the indexer gates [Ih][m]
+  if (PT) {
+    const float* ag = reinterpret_cast<const float*>(pd.arena + L.alpha_idx);
+    for (int v = threadIdx.x; v < pd.idx_heads * m && v < kScoreMaxGates; v += blockDim.x) a_sh[v] = ag[v];
+  }
   const int seg_begin = (blockIdx.x - R.score_base) * P.segs_per_cta;
   const int seg_end = min(nseg, seg_begin + P.segs_per_cta);
   const int n_st = max(0, seg_end - seg_begin);
@@ -240,8 +253,9 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
   const int32_t staging = pd.staging_base + R.slot;
   auto block_id = [&](int jj) -> int32_t {  // id of this warp's jj-th block (any lane)
     const int seg = seg_begin + warp + jj * CW;
-    if (jj >= mine || seg >= R.n_sealed) return staging;
-    const int32_t bid = table[seg];
+    const int blk = PT ? seg / m : seg;
+    if (jj >= mine || blk >= R.n_sealed) return staging;
+    const int32_t bid = table[blk];
     if (bid < 0 || bid >= pd.max_blocks) {
       flag_error(pd, kErrBadBlock);
       return staging;  // read something valid; the error word reports it
@@ -259,7 +273,8 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
       id_nxt = block_id((id_batch + 1) * 32 + lane);
     }
     const int32_t bid = __shfl_sync(0xffffffffu, id_cur, jj & 31);
-    return pd.arena + L.idx_pool + (int64_t)bid * L.idx_stride;
+    const int run = PT ? (seg_begin + warp + jj * CW) % m : 0;
+    return pd.arena + L.idx_pool + (int64_t)bid * L.idx_stride + (int64_t)run * L.idx_run;
   };
   uint64_t* my_full = full + warp * ring;
   uint8_t* my_slots = slots + (int64_t)warp * ring * stage_bytes;
@@ -279,10 +294,15 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
   int j = 0;
   for (; j < mine; ++j) {
     const int slot = j % ring;
-    if (!mbar_wait(&my_full[slot], (j / ring) & 1, pd)) break;
+    bool got = mbar_wait(&my_full[slot], (j / ring) & 1, pd);
+    if (PT) got = __all_sync(0xffffffffu, got);  // the lanes exchange scores below
+    if (!got) break;
     const uint8_t* stg = my_slots + (int64_t)slot * stage_bytes;
-    const int64_t E = (int64_t)(seg_begin + warp + j * CW) * CB + lane;
+    const int64_t T = (int64_t)(seg_begin + warp + j * CW) * CB + lane;  // entry, or token (PT)
+    const int64_t E = PT ? T / m : T;
     const bool valid = lane < CB && E < R.n_cand;
+    const int cph = n_chunks / pd.idx_heads;  // chunks per indexer head
+    const int ti = lane % m;                  // the token's place in its entry (PT)
     float acc = 0.0f;
     float scale = 1.0f;
     if (n_chunks <= KCH) {
@@ -302,7 +322,21 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
           bulk_g2s(my_slots + (int64_t)slot * stage_bytes, src, (uint32_t)stage_bytes, &my_full[slot]);
         }
       }
-      if (valid) {
+      if (valid && PT) {  // per head: chain, times the token's scale, into the gate chain
+        float d = 0.0f;
+#pragma unroll
+        for (int c = 0; c < KCH; ++c) {
+          if (c < n_chunks) {
+            d = fast ? IdxChunkFast<CACHE>::chain(ch[c], qh + c * (V / 2), d)
+                     : IdxChunk<CACHE>::chain(ch[c], q_sh + c * V, d);
+            if ((c + 1) % cph == 0) {
+              if constexpr (CACHE == KVPOOL_FP8_E4M3 || CACHE == KVPOOL_FP4_E2M1) d = __fmul_rn(d, scale);
+              acc = __fmaf_rn(a_sh[(c / cph) * m + ti], d, acc);
+              d = 0.0f;
+            }
+          }
+        }
+      } else if (valid) {
         if (fast) {
 #pragma unroll
           for (int c = 0; c < KCH; ++c)
@@ -315,13 +349,23 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
       }
     } else {
       if (valid) {
-        for (int c = 0; c < n_chunks; ++c) {
-          const uint4 chk = *reinterpret_cast<const uint4*>(stg + ((int64_t)c * CB + lane) * 16);
-          acc = fast ? IdxChunkFast<CACHE>::chain(chk, qh + c * (V / 2), acc)
-                     : IdxChunk<CACHE>::chain(chk, q_sh + c * V, acc);
-        }
         if (CACHE == KVPOOL_FP8_E4M3 || CACHE == KVPOOL_FP4_E2M1)
           scale = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(stg + key_bytes + 2 * lane));
+        float d = 0.0f;
+        for (int c = 0; c < n_chunks; ++c) {
+          const uint4 chk = *reinterpret_cast<const uint4*>(stg + ((int64_t)c * CB + lane) * 16);
+          if (PT) {
+            d = fast ? IdxChunkFast<CACHE>::chain(chk, qh + c * (V / 2), d) : IdxChunk<CACHE>::chain(chk, q_sh + c * V, d);
+            if ((c + 1) % cph == 0) {
+              if constexpr (CACHE == KVPOOL_FP8_E4M3 || CACHE == KVPOOL_FP4_E2M1) d = __fmul_rn(d, scale);
+              acc = __fmaf_rn(a_sh[(c / cph) * m + ti], d, acc);
+              d = 0.0f;
+            }
+          } else {
+            acc = fast ? IdxChunkFast<CACHE>::chain(chk, qh + c * (V / 2), acc)
+                       : IdxChunk<CACHE>::chain(chk, q_sh + c * V, acc);
+          }
+        }
       }
       __syncwarp();
       if (j + ring < mine) {
@@ -333,7 +377,15 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
         }
       }
     }
-    if (valid) {
+    if constexpr (PT) {  // the entry's first lane adds its m tokens in order
+      float sum = acc;
+      for (int k = 1; k < m; ++k) sum += __shfl_sync(0xffffffffu, acc, (lane + k) & 31);
+      if (valid && ti == 0) {
+        const uint32_t key = score_key(sum);
+        keys[E] = key;
+        atomicAdd(&hist[key >> 21], 1u);
+      }
+    } else if (valid) {
       if constexpr (CACHE == KVPOOL_FP8_E4M3 || CACHE == KVPOOL_FP4_E2M1) acc = __fmul_rn(acc, scale);
       const uint32_t key = score_key(acc);
       keys[E] = key;
@@ -366,12 +418,12 @@ int score_stage_plan(const PoolDesc& pd, int* stage_bytes, int* ring, int* stage
   return 0;
 }
 
-template <int IN, int CACHE>
+template <int IN, int CACHE, bool PT>
 static int launch_score_t(const AttendParams& p, cudaStream_t s) {
   int sb, ns, so;
   size_t smem;
   score_stage_plan(p.pool, &sb, &ns, &so, &smem);
-  auto k = score_kernel<IN, CACHE>;
+  auto k = score_kernel<IN, CACHE, PT>;
   static size_t set = 0;
   if (set < smem) {
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -386,15 +438,30 @@ int launch_score(const AttendParams& p, void* stream, int* n_kernels) {
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the score kernel reads indexer entries only: it is specialised on their type
   const int key = p.pool.in_dtype * 4 + p.pool.idx_dtype;
+  if (p.pool.idx_per_token) {  // per-token keys
+    switch (key) {
+      case KVPOOL_F32 * 4 + KVPOOL_F32: launch_score_t<KVPOOL_F32, KVPOOL_F32, true>(p, s); break;
+      case KVPOOL_F32 * 4 + KVPOOL_BF16: launch_score_t<KVPOOL_F32, KVPOOL_BF16, true>(p, s); break;
+      case KVPOOL_F32 * 4 + KVPOOL_FP8_E4M3: launch_score_t<KVPOOL_F32, KVPOOL_FP8_E4M3, true>(p, s); break;
+      case KVPOOL_F32 * 4 + KVPOOL_FP4_E2M1: launch_score_t<KVPOOL_F32, KVPOOL_FP4_E2M1, true>(p, s); break;
+      case KVPOOL_BF16 * 4 + KVPOOL_F32: launch_score_t<KVPOOL_BF16, KVPOOL_F32, true>(p, s); break;
+      case KVPOOL_BF16 * 4 + KVPOOL_BF16: launch_score_t<KVPOOL_BF16, KVPOOL_BF16, true>(p, s); break;
+      case KVPOOL_BF16 * 4 + KVPOOL_FP8_E4M3: launch_score_t<KVPOOL_BF16, KVPOOL_FP8_E4M3, true>(p, s); break;
+      case KVPOOL_BF16 * 4 + KVPOOL_FP4_E2M1: launch_score_t<KVPOOL_BF16, KVPOOL_FP4_E2M1, true>(p, s); break;
+      default: return (int)cudaErrorInvalidValue;
+    }
+    *n_kernels += 1;
+    return (int)cudaGetLastError();
+  }
   switch (key) {
-    case KVPOOL_F32 * 4 + KVPOOL_F32: launch_score_t<KVPOOL_F32, KVPOOL_F32>(p, s); break;
-    case KVPOOL_F32 * 4 + KVPOOL_BF16: launch_score_t<KVPOOL_F32, KVPOOL_BF16>(p, s); break;
-    case KVPOOL_F32 * 4 + KVPOOL_FP8_E4M3: launch_score_t<KVPOOL_F32, KVPOOL_FP8_E4M3>(p, s); break;
-    case KVPOOL_F32 * 4 + KVPOOL_FP4_E2M1: launch_score_t<KVPOOL_F32, KVPOOL_FP4_E2M1>(p, s); break;
-    case KVPOOL_BF16 * 4 + KVPOOL_F32: launch_score_t<KVPOOL_BF16, KVPOOL_F32>(p, s); break;
-    case KVPOOL_BF16 * 4 + KVPOOL_BF16: launch_score_t<KVPOOL_BF16, KVPOOL_BF16>(p, s); break;
-    case KVPOOL_BF16 * 4 + KVPOOL_FP8_E4M3: launch_score_t<KVPOOL_BF16, KVPOOL_FP8_E4M3>(p, s); break;
-    case KVPOOL_BF16 * 4 + KVPOOL_FP4_E2M1: launch_score_t<KVPOOL_BF16, KVPOOL_FP4_E2M1>(p, s); break;
+    case KVPOOL_F32 * 4 + KVPOOL_F32: launch_score_t<KVPOOL_F32, KVPOOL_F32, false>(p, s); break;
+    case KVPOOL_F32 * 4 + KVPOOL_BF16: launch_score_t<KVPOOL_F32, KVPOOL_BF16, false>(p, s); break;
+    case KVPOOL_F32 * 4 + KVPOOL_FP8_E4M3: launch_score_t<KVPOOL_F32, KVPOOL_FP8_E4M3, false>(p, s); break;
+    case KVPOOL_F32 * 4 + KVPOOL_FP4_E2M1: launch_score_t<KVPOOL_F32, KVPOOL_FP4_E2M1, false>(p, s); break;
+    case KVPOOL_BF16 * 4 + KVPOOL_F32: launch_score_t<KVPOOL_BF16, KVPOOL_F32, false>(p, s); break;
+    case KVPOOL_BF16 * 4 + KVPOOL_BF16: launch_score_t<KVPOOL_BF16, KVPOOL_BF16, false>(p, s); break;
+    case KVPOOL_BF16 * 4 + KVPOOL_FP8_E4M3: launch_score_t<KVPOOL_BF16, KVPOOL_FP8_E4M3, false>(p, s); break;
+    case KVPOOL_BF16 * 4 + KVPOOL_FP4_E2M1: launch_score_t<KVPOOL_BF16, KVPOOL_FP4_E2M1, false>(p, s); break;
     default: return (int)cudaErrorInvalidValue;
   }
   *n_kernels += 1;

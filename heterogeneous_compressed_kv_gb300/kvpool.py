@@ -48,7 +48,7 @@ class _Config(C.Structure):
                 ("max_blocks_per_request", C.c_int32), ("max_batch", C.c_int32), ("max_top_k", C.c_int32),
                 ("gate_csa", C.POINTER(C.c_float)), ("gate_hca", C.POINTER(C.c_float)),
                 ("gate_idx", C.POINTER(C.c_float)), ("flags", C.c_uint32), ("idx_fp4", C.c_int32),
-                ("csa_hot_slots", C.c_int32), ("csa_host_slots", C.c_int32)]
+                ("csa_hot_slots", C.c_int32), ("csa_host_slots", C.c_int32), ("idx_per_token", C.c_int32)]
 
 
 class _Info(C.Structure):
@@ -152,6 +152,7 @@ class PoolConfig:
     idx_fp4: int = 0  # 1: indexer entries in FP4 (e2m1 + one bf16 scale)
     csa_hot_slots: int = 0  # HiSparse: GPU slots for sealed blocks' CSA entries (0 = off)
     csa_host_slots: int = 0  # HiSparse: host slots for offloaded CSA entries
+    idx_per_token: int = 0  # 1: one indexer key per token (128 per block) instead of one per CSA entry
     _keep: list = field(default_factory=list, repr=False)
 
     def to_c(self) -> _Config:
@@ -164,7 +165,7 @@ class PoolConfig:
                        self.in_dtype, self.cache_dtype, kinds.size, kinds.ctypes.data_as(C.POINTER(C.c_int32)),
                        self.max_requests, self.max_blocks, self.max_blocks_per_request, self.max_batch,
                        self.max_top_k, g[0].ctypes.data_as(fp), g[1].ctypes.data_as(fp), g[2].ctypes.data_as(fp),
-                       self.flags, self.idx_fp4, self.csa_hot_slots, self.csa_host_slots)
+                       self.flags, self.idx_fp4, self.csa_hot_slots, self.csa_host_slots, self.idx_per_token)
 
 
 def required_bytes(cfg: PoolConfig) -> int:

@@ -122,6 +122,13 @@ typedef struct kvpool_config {
   int32_t csa_hot_slots;          /* HiSparse: GPU slots for sealed blocks' CSA entries (0 = off: a
                                      block's CSA entries stay with the block id; else <= max_blocks) */
   int32_t csa_host_slots;         /* HiSparse: host slots for offloaded blocks' CSA entries (0 if off) */
+  int32_t idx_per_token;          /* 1: the indexer keeps one key per token (m' per block, the
+                                     block figure's "128 indexer K") instead of one per CSA entry;
+                                     entry e's score is sum_i sum_j alpha_idx[j][i] * <q_j, key of
+                                     token m*e+i, head j> (fixed order: per token, each head's fp32
+                                     chain times the token's scale, an fp32 chain over heads with
+                                     the gates, then the m tokens added in order).  Needs
+                                     idx_heads * idx_dim <= 256. */
 } kvpool_config;
 
 typedef struct kvpool kvpool_t;
@@ -184,8 +191,8 @@ int kvpool_share_prefix(kvpool_t* pool, int32_t dst, int32_t src, int64_t n_toke
  *   window section: for each layer the tokens at positions n_tokens - w ..
  *     n_tokens - 1, one entry_bytes record each (w = min(n_tokens, n_win)).
  * The fingerprint is FNV-1a 64 over the little-endian int32 fields m, m',
- * n_win, heads, head_dim, idx_heads, idx_dim, in_dtype, cache_dtype, idx_fp4,
- * n_layers, then per layer its kind and the fp32 bits of the gate logits it
+ * n_win, heads, head_dim, idx_heads, idx_dim, in_dtype, cache_dtype, idx_fp4 +
+ * 2 * idx_per_token, n_layers, then per layer its kind and the fp32 bits of the gate logits it
  * uses (CSA then indexer if it has CSA, HCA if it has HCA).  Images need each
  * indexer key to be whole 16-byte chunks (when a layer has CSA).
  *
@@ -361,10 +368,12 @@ int kvpool_free_block_count(const kvpool_t* pool);
  * Entry (CSA entry, HCA entry, window token), entry_bytes long:
  *   K codes [heads][head_dim], V codes [heads][head_dim] in the cache dtype,
  *   then for fp8 a bf16 K scale, a bf16 V scale and 12 zero bytes.
- * Indexer keys of a block: 16-byte chunk c of entry e at (c * csa_per_block
- *   + e) * 16 from idx_offset (chunk-major, so a warp reading chunk c of 32
- *   consecutive entries reads 512 contiguous bytes); fp8 scales [csa_per_block]
- *   bf16 at idx_scale_offset.
+ * Indexer keys of a block: runs of csa_per_block keys (one run; with
+ *   idx_per_token, m runs of consecutive tokens, idx_block_bytes / m bytes
+ *   each): 16-byte chunk c of key e of a run at (c * csa_per_block + e) * 16
+ *   from the run's start (chunk-major, so a warp reading chunk c of 32
+ *   consecutive keys reads 512 contiguous bytes); fp8 / FP4 scales
+ *   [csa_per_block] bf16 at idx_scale_offset from the run's start.
  * Block parts of a layer, each in its own plane: CSA entries [csa_per_block]
  *   at csa_offset + s * csa_block_bytes where s is the block's location (its
  *   id without HiSparse, its GPU slot with it; an offloaded block's CSA

@@ -40,7 +40,7 @@ class GpuCase:
                                 max_requests=max_requests, max_blocks=max_blocks, max_blocks_per_request=mbpr,
                                 max_batch=max_batch, max_top_k=max_top_k, gate_csa=g[0], gate_hca=g[1],
                                 gate_idx=g[2], idx_fp4=w.get("idx_fp4", 0), csa_hot_slots=w.get("csa_hot_slots", 0),
-                                csa_host_slots=w.get("csa_host_slots", 0))
+                                csa_host_slots=w.get("csa_host_slots", 0), idx_per_token=w.get("idx_per_token", 0))
         # indexer entries carry a bf16 scale when they are fp8 or fp4
         self.idx_scaled = w["cache_dtype"] == K.FP8_E4M3 or bool(w.get("idx_fp4", 0))
         nbytes = K.required_bytes(self.cfg)
@@ -135,9 +135,17 @@ class GpuCase:
         return self.entry(d["csa_offset"] + s_ * d["csa_block_bytes"] + (e % CB) * d["entry_bytes"], host)
 
     def idx_entry(self, layer, slot, e, ids, host=None):
+        """Indexer key e: of CSA entry e, or with per-token keys of token e
+        (run e % m' // CB of its block, key e % CB of the run)."""
         d = self.pool.layout(layer)
         CB = d["csa_per_block"]
-        base = d["idx_offset"] + self._bid(d, slot, e, ids) * d["idx_block_bytes"]
+        if self.w.get("idx_per_token", 0):
+            mp, runs = self.w["m_prime"], self.w["m"]
+            seg = e // mp
+            bid = int(ids[seg]) if seg < len(ids) else d["staging_base"] + slot
+            base = d["idx_offset"] + bid * d["idx_block_bytes"] + (e % mp) // CB * (d["idx_block_bytes"] // runs)
+        else:
+            base = d["idx_offset"] + self._bid(d, slot, e, ids) * d["idx_block_bytes"]
         n_chunks = d["idx_entry_bytes"] // 16
         code = np.concatenate([self.bytes_at(base + (c * CB + e % CB) * 16, 16, host) for c in range(n_chunks)])
         sc = np.zeros(1, np.uint16)
@@ -177,11 +185,24 @@ def compare_request_state(case, oracle, slot, layers=None, sample=None, rng=None
             assert np.array_equal(c, c_ref), f"CSA entry {e} of layer {l} differs"
             if case.vs == 1:
                 assert np.array_equal(s, s_ref), f"CSA entry {e} scales differ"
+            if case.w.get("idx_per_token", 0):
+                continue
             rc, c_ref, s_ref = oracle.request_entry(l, slot, 3, e)
             c, s = case.idx_entry(l, slot, e, ids2, host)
             assert np.array_equal(c, c_ref), f"indexer entry {e} of layer {l} differs"
             if case.idx_scaled:
                 assert s[0] == s_ref[0], f"indexer entry {e} scale differs"
+        if n_csa and case.w.get("idx_per_token", 0):  # one key per token
+            ts = range(i1["length"])
+            if sample is not None and i1["length"] > 4 * sample:
+                ts = sorted(set(rng.integers(0, i1["length"], 4 * sample).tolist()) | {i1["length"] - 1, 0})
+            for t in ts:
+                rc, c_ref, s_ref = oracle.request_entry(l, slot, 3, t)
+                assert rc == 0
+                c, s = case.idx_entry(l, slot, t, ids2, host)
+                assert np.array_equal(c, c_ref), f"indexer key of token {t} of layer {l} differs"
+                if case.idx_scaled:
+                    assert s[0] == s_ref[0], f"indexer key of token {t} scale differs"
         if kind in (K.HCA, K.CSA_HCA):
             ts = range(len(ids1))
             if sample is not None and len(ids1) > sample:

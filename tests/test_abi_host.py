@@ -225,15 +225,25 @@ def test_error_codes_match_oracle():
 @pytest.mark.parametrize("kw", [dict(), dict(cache_dtype=K.BF16, in_dtype=K.BF16),
                                 dict(cache_dtype=K.FP8_E4M3, in_dtype=K.BF16, idx_dim=32),
                                 dict(cache_dtype=K.FP8_E4M3, in_dtype=K.BF16, idx_fp4=1, idx_dim=32),
-                                dict(n_layers=3, layer_kinds=[K.SWA_ONLY, K.CSA, K.HCA], n_win=256)])
+                                dict(n_layers=3, layer_kinds=[K.SWA_ONLY, K.CSA, K.HCA], n_win=256),
+                                dict(idx_per_token=1),
+                                dict(cache_dtype=K.FP8_E4M3, in_dtype=K.BF16, idx_dim=32, idx_per_token=1),
+                                dict(cache_dtype=K.FP8_E4M3, in_dtype=K.BF16, idx_fp4=1, idx_dim=32, idx_per_token=1)])
 def test_image_header_and_sizes_match_oracle(kw):
     """The library's config fingerprint, image sizes and image header equal
-    the oracle's (both written from the documented layout, independently)."""
+    the oracle's (both written from the documented layout, independently),
+    with per-entry and per-token indexer keys."""
     fp4 = kw.pop("idx_fp4", 0)
+    pt = kw.pop("idx_per_token", 0)
     w = base_workload(**kw)
     w["idx_fp4"] = fp4
+    w["idx_per_token"] = pt
     o = H.make_oracle(w, 4, 16, 8)
-    p = K.Pool(cfg_of(w, max_requests=4, max_blocks=16, max_blocks_per_request=8, idx_fp4=fp4))
+    p = K.Pool(cfg_of(w, max_requests=4, max_blocks=16, max_blocks_per_request=8, idx_fp4=fp4, idx_per_token=pt))
+    if pt:  # the block's indexer part is m runs of csa_per_block keys
+        d = p.layout(0)
+        run = d["csa_per_block"] * d["idx_entry_bytes"] + (64 if w["cache_dtype"] == K.FP8_E4M3 else 0)
+        assert d["idx_block_bytes"] == w["m"] * run
     assert p.fingerprint() == o.fingerprint()
     for n in (0, 64, 128, 384, 1024):
         for f in (0, K.IMAGE_WINDOW):
