@@ -38,9 +38,10 @@ NOMINAL_HBM_GBS = 8000.0
 # ---------------------------------------------------------------------------
 # workloads
 # ---------------------------------------------------------------------------
-def workload(name, idx_fp4=False):
+def workload(name, idx_fp4=False, idx_per_token=False):
     """The workload recipe; idx_fp4 stores the indexer entries in FP4 (e2m1 +
-    one bf16 scale) instead of the cache dtype."""
+    one bf16 scale) instead of the cache dtype; idx_per_token keeps one
+    indexer key per token instead of one per CSA entry."""
     from heterogeneous_compressed_kv_gb300.gen import workloads as W
     if name == "long_context":
         w = dict(W.LONG_CONTEXT)
@@ -52,6 +53,7 @@ def workload(name, idx_fp4=False):
     else:
         raise SystemExit(f"unknown config {name}")
     w["idx_fp4"] = 1 if idx_fp4 else 0
+    w["idx_per_token"] = 1 if idx_per_token else 0
     return w
 
 
@@ -69,12 +71,12 @@ def gates(w):
 def _oracle_worker(args):
     """Prefill one workload request into the oracle (untimed), then time
     `steps` decode steps (append 1 token + decode_attend) of it."""
-    name, idx_fp4, wid, steps, warm = args
+    name, idx_fp4, wid, steps, warm, idx_per_token = args
     sys.path.insert(0, ROOT)
     import numpy as np
     import oracle as O
     from heterogeneous_compressed_kv_gb300 import gen
-    w = workload(name, idx_fp4)
+    w = workload(name, idx_fp4, idx_per_token)
     L0 = int(w["lengths"][wid])
     total = L0 + warm + steps + 1
     g = gates(w)
@@ -82,7 +84,8 @@ def _oracle_worker(args):
                  idx_heads=w["idx_heads"], idx_dim=w["idx_dim"], in_dtype=w["in_dtype"],
                  cache_dtype=w["cache_dtype"], layer_kinds=w["layer_kinds"], max_requests=1,
                  max_blocks=total // w["m_prime"] + 1, max_blocks_per_request=total // w["m_prime"] + 1,
-                 gate_csa=g[0], gate_hca=g[1], gate_idx=g[2], idx_fp4=w["idx_fp4"])
+                 gate_csa=g[0], gate_hca=g[1], gate_idx=g[2], idx_fp4=w["idx_fp4"],
+                 idx_per_token=w["idx_per_token"])
     _, r = o.alloc_request()
     HD, XD = w["heads"] * w["head_dim"], w["idx_heads"] * w["idx_dim"]
     dt = gen.OUT_F32 if w["in_dtype"] == 0 else gen.OUT_BF16
@@ -120,11 +123,11 @@ def _oracle_worker(args):
     return time.perf_counter() - t0, t_setup
 
 
-def start_oracle(name, n_workers, steps, warm, idx_fp4=False):
+def start_oracle(name, n_workers, steps, warm, idx_fp4=False, idx_per_token=False):
     """Spawned before any CUDA call: one oracle process per sampled request."""
     ctx = mp.get_context("spawn")
     pool = ctx.Pool(n_workers)
-    res = pool.map_async(_oracle_worker, [(name, idx_fp4, i, steps, warm) for i in range(n_workers)])
+    res = pool.map_async(_oracle_worker, [(name, idx_fp4, i, steps, warm, idx_per_token) for i in range(n_workers)])
     return pool, res
 
 
@@ -140,9 +143,9 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    w = workload(args.config, args.idx_fp4)
+    w = workload(args.config, args.idx_fp4, args.idx_per_token)
     n = oracle_workers(w)
-    pool, res = start_oracle(args.config, n, args.steps, args.warmup, args.idx_fp4)
+    pool, res = start_oracle(args.config, n, args.steps, args.warmup, args.idx_fp4, args.idx_per_token)
     out = res.get()
     pool.close()
     t = max(o[0] for o in out)
@@ -166,6 +169,8 @@ def config_block(w, args):
              cache_dtype={0: "f32", 1: "bf16", 2: "fp8_e4m3+bf16_scale"}[w["cache_dtype"]])
     if w.get("idx_fp4"):
         c["indexer_dtype"] = "fp4_e2m1+bf16_scale"
+    if w.get("idx_per_token"):
+        c["indexer_keys"] = "one per token (128 per block)"
     if getattr(args, "hisparse", 0) > 0:
         c["hisparse_offloaded"] = args.hisparse
     if w["name"] == "long_context":
@@ -399,6 +404,7 @@ def main():
     ap.add_argument("--context", type=int, default=0, help="override the long-context length (profiling cases)")
     ap.add_argument("--timeline", type=int, default=0, help="print the launch timeline of this many extra steps")
     ap.add_argument("--idx-fp4", action="store_true", help="indexer entries in FP4 (e2m1 + one bf16 scale)")
+    ap.add_argument("--idx-per-token", action="store_true", help="one indexer key per token instead of per CSA entry")
     ap.add_argument("--hisparse", type=float, default=0.0,
                     help="HiSparse: offload this fraction of the sealed blocks' CSA entries to host memory first")
     ap.add_argument("--prefix-image", action="store_true",
@@ -412,7 +418,7 @@ def main():
         return
 
     world, rank, local = rank_env()
-    w = workload(args.config, args.idx_fp4)
+    w = workload(args.config, args.idx_fp4, args.idx_per_token)
     if args.requests or args.context:
         w["n_requests"] = args.requests or w["n_requests"]
         L = args.context or w.get("length", 0)
@@ -423,7 +429,8 @@ def main():
     # the oracle baseline is spawned before the first CUDA call
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = (oracle_workers(w),) + start_oracle(args.config, oracle_workers(w), args.cpu_steps, 1, args.idx_fp4)
+        cpu = (oracle_workers(w),) + start_oracle(args.config, oracle_workers(w), args.cpu_steps, 1, args.idx_fp4,
+                                                         args.idx_per_token)
 
     import numpy as np
     import torch
@@ -449,7 +456,7 @@ def main():
                        cache_dtype=w["cache_dtype"], layer_kinds=w["layer_kinds"], max_requests=B,
                        max_blocks=sum((L + extra) // mp_ + 1 for L in lengths), max_blocks_per_request=mbpr,
                        max_batch=B, max_top_k=w["top_k"], gate_csa=g[0], gate_hca=g[1], gate_idx=g[2],
-                       idx_fp4=w["idx_fp4"])
+                       idx_fp4=w["idx_fp4"], idx_per_token=w["idx_per_token"])
     n_sealed = sum(L // mp_ for L in lengths)
     if args.hisparse > 0:  # every block gets a GPU slot; a fraction moves to host slots after the prefill
         cfg.csa_hot_slots = cfg.max_blocks
@@ -669,7 +676,8 @@ def main():
                               frac=(achieved / hbm_peak) if achieved else None,
                               # the records hold full-size launches: none for a resized workload
                               traffic=None if (args.requests or args.context) else
-                              traffic_record(f"{w['name']}/{dom}" + ("_fp4" if dom == "score" and w["idx_fp4"] else ""),
+                              traffic_record(f"{w['name']}/{dom}" + ("_fp4" if dom == "score" and w["idx_fp4"] else "")
+                                             + ("_per_token" if dom == "score" and w["idx_per_token"] else ""),
                                              src),
                               peak_source=peak_kind,
                               bytes_per_launch=d_b / launches_dom, ms_per_launch=d_ms / launches_dom),

@@ -324,17 +324,31 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
       }
       if (valid && PT) {  // per head: chain, times the token's scale, into the gate chain
         float d = 0.0f;
-#pragma unroll
-        for (int c = 0; c < KCH; ++c) {
-          if (c < n_chunks) {
-            d = fast ? IdxChunkFast<CACHE>::chain(ch[c], qh + c * (V / 2), d)
-                     : IdxChunk<CACHE>::chain(ch[c], q_sh + c * V, d);
-            if ((c + 1) % cph == 0) {
-              if constexpr (CACHE == KVPOOL_FP8_E4M3 || CACHE == KVPOOL_FP4_E2M1) d = __fmul_rn(d, scale);
-              acc = __fmaf_rn(a_sh[(c / cph) * m + ti], d, acc);
-              d = 0.0f;
-            }
+        int left = cph;               // chunks left in the current head
+        const float* ga = a_sh + ti;  // the gate of the current head
+        auto head_done = [&]() {
+          if (--left == 0) {
+            if constexpr (CACHE == KVPOOL_FP8_E4M3 || CACHE == KVPOOL_FP4_E2M1) d = __fmul_rn(d, scale);
+            acc = __fmaf_rn(*ga, d, acc);
+            ga += m;
+            d = 0.0f;
+            left = cph;
           }
+        };
+        if (fast) {
+#pragma unroll
+          for (int c = 0; c < KCH; ++c)
+            if (c < n_chunks) {
+              d = IdxChunkFast<CACHE>::chain(ch[c], qh + c * (V / 2), d);
+              head_done();
+            }
+        } else {
+#pragma unroll
+          for (int c = 0; c < KCH; ++c)
+            if (c < n_chunks) {
+              d = IdxChunk<CACHE>::chain(ch[c], q_sh + c * V, d);
+              head_done();
+            }
         }
       } else if (valid) {
         if (fast) {
@@ -352,14 +366,18 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
         if (CACHE == KVPOOL_FP8_E4M3 || CACHE == KVPOOL_FP4_E2M1)
           scale = bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(stg + key_bytes + 2 * lane));
         float d = 0.0f;
+        int left = cph;
+        const float* ga = a_sh + ti;
         for (int c = 0; c < n_chunks; ++c) {
           const uint4 chk = *reinterpret_cast<const uint4*>(stg + ((int64_t)c * CB + lane) * 16);
           if (PT) {
             d = fast ? IdxChunkFast<CACHE>::chain(chk, qh + c * (V / 2), d) : IdxChunk<CACHE>::chain(chk, q_sh + c * V, d);
-            if ((c + 1) % cph == 0) {
+            if (--left == 0) {
               if constexpr (CACHE == KVPOOL_FP8_E4M3 || CACHE == KVPOOL_FP4_E2M1) d = __fmul_rn(d, scale);
-              acc = __fmaf_rn(a_sh[(c / cph) * m + ti], d, acc);
+              acc = __fmaf_rn(*ga, d, acc);
+              ga += m;
               d = 0.0f;
+              left = cph;
             }
           } else {
             acc = fast ? IdxChunkFast<CACHE>::chain(chk, qh + c * (V / 2), acc)
