@@ -6,6 +6,8 @@ from __future__ import annotations
 
 import numpy as np
 
+import oracle as O
+
 from heterogeneous_compressed_kv_gb300 import gen
 from tests import harness as H
 
@@ -13,7 +15,7 @@ _ORACLES = {}
 
 
 def _oracle(cfg):
-    key = (cfg["name"], cfg["seed"], cfg.get("idx_fp4", 0))
+    key = (cfg["name"], cfg["seed"], cfg.get("idx_fp4", 0), cfg.get("idx_per_token", 0))
     if key not in _ORACLES:
         _ORACLES[key] = H.make_oracle(cfg, 1, 1, 1)
     return _ORACLES[key]
@@ -31,10 +33,24 @@ def idx_scores(cfg, wid, q_idx, e0, e1, layer=0):
     m, XD = cfg["m"], cfg["idx_heads"] * cfg["idx_dim"]
     keys = _rows(cfg, gen.IDXK, wid, e0 * m, (e1 - e0) * m, XD, layer)
     out = np.empty(e1 - e0, np.float32)
+    if cfg.get("idx_per_token", 0):  # each token's key encoded alone; the entry mixes its m tokens
+        for j in range(e1 - e0):
+            enc = [O.encode(o.idx_dtype, keys[j * m + i]) for i in range(m)]
+            codes = np.concatenate([c for c, _ in enc])
+            scales = np.array([sc for _, sc in enc], np.uint16)
+            out[j] = o.score_tokens(layer, codes, scales, q_idx)
+        return out
     for j in range(e1 - e0):
         code, sc = o.compress_idx(layer, keys[j * m:(j + 1) * m])
         out[j] = o.score(code, sc, q_idx)
     return out
+
+
+def token_keys(cfg, wid, ts, layer=0):
+    """Per-token indexer keys (codes, scale) of tokens `ts`."""
+    o = _oracle(cfg)
+    XD = cfg["idx_heads"] * cfg["idx_dim"]
+    return [O.encode(o.idx_dtype, _rows(cfg, gen.IDXK, wid, t, 1, XD, layer)[0]) for t in ts]
 
 
 def idx_entries(cfg, wid, es, layer=0):

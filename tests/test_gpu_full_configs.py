@@ -113,8 +113,8 @@ def _spawn_pool():
     return mp.get_context("spawn").Pool(max(1, min(16, os.cpu_count() or 1)))
 
 
-@pytest.mark.parametrize("idx_fp4", [0, 1])
-def test_long_context_full_sampled(idx_fp4):
+@pytest.mark.parametrize("idx_fp4, per_token", [(0, 0), (1, 0), (0, 1)], ids=["fp8", "fp4", "fp8_per_token"])
+def test_long_context_full_sampled(idx_fp4, per_token):
     """8 requests x 1,048,576 tokens, fp8 cache, top_k 2048, in bench.py's
     pool configuration and prefill order (2048-token chunks, every request per
     call), then one decode step.  For one request the oracle recomputes, one
@@ -123,9 +123,9 @@ def test_long_context_full_sampled(idx_fp4):
     the window, and the attention output (fp8 tolerance); sampled CSA,
     indexer and HCA entries and the window are compared byte for byte with
     the arena; block tables follow the smallest-free policy.  Indexer entries
-    in fp8 (the workload) or FP4."""
+    in fp8 (the workload) or FP4, or one fp8 key per token."""
     from tests import oracle_pool as OP
-    w = dict(W.LONG_CONTEXT, idx_fp4=idx_fp4)
+    w = dict(W.LONG_CONTEXT, idx_fp4=idx_fp4, idx_per_token=per_token)
     B, Lc, C, mp_, top_k = w["n_requests"], w["length"], w["chunk"], w["m_prime"], w["top_k"]
     extra = 8
     g = GpuCase(w, B, B * ((Lc + extra) // mp_ + 1), (Lc + extra) // mp_ + 2, B, top_k)
@@ -178,19 +178,25 @@ def test_long_context_full_sampled(idx_fp4):
     rng = np.random.default_rng(1)
     es = sorted(set(rng.integers(0, n_csa, 48).tolist()) | {0, n_csa - 1})
     cc, csc = OP.kv_entries(w, wid, 1, es)
-    ie = OP.idx_entries(w, wid, es)
+    ie = None if per_token else OP.idx_entries(w, wid, es)
     for j, e in enumerate(es):
         c, sc = g.csa_entry(0, s, e, ids)
         assert np.array_equal(c, cc[j]) and np.array_equal(sc, csc[j]), f"CSA entry {e}"
-        c, sc = g.idx_entry(0, s, e, ids)
-        assert np.array_equal(c, ie[j][0]) and sc[0] == ie[j][1][0], f"indexer entry {e}"
+        if ie is not None:
+            c, sc = g.idx_entry(0, s, e, ids)
+            assert np.array_equal(c, ie[j][0]) and sc[0] == ie[j][1][0], f"indexer entry {e}"
+    if per_token:  # sampled tokens' own keys, including the staged tail
+        ts = sorted(set(rng.integers(0, L, 48).tolist()) | {0, L - 1})
+        for t, (kc, ks) in zip(ts, OP.token_keys(w, wid, ts)):
+            c, sc = g.idx_entry(0, s, t, ids)
+            assert np.array_equal(c, kc) and sc[0] == ks, f"indexer key of token {t}"
     for t in sorted(set(rng.integers(0, n_hca, 16).tolist()) | {n_hca - 1}):
         c, sc = g.hca_entry(0, int(ids[t]))
         assert np.array_equal(c, hca_codes[t]) and np.array_equal(sc, hca_scales[t]), f"HCA entry {t}"
     for t, pos in enumerate(range(L - w["n_win"], L)):
         c, sc = g.window_token(0, s, pos)
         assert np.array_equal(c, win_codes[t]) and np.array_equal(sc, win_scales[t]), f"window token {pos}"
-    if idx_fp4:
+    if idx_fp4 or per_token:
         return
     # the request's 1,048,576-token prefix as an image (Zero SWA): sampled
     # entries where the image layout puts them; then restored in its place,
