@@ -32,14 +32,15 @@ using namespace kvp;
 namespace {
 
 constexpr int kMaxSplits = 4096;
+// CTA targets per launch, in CTAs per SM (the SM count comes from the device):
 // attention CTAs of a part that has the GPU to itself: 3 per SM, of which 2
 // are resident at a time (registers); 1.5 waves of shorter splits measured a
 // little faster than one wave of longer ones (long context 178.8 vs 180.6 us)
-constexpr int kAttendCtas = 3 * 152;
+constexpr int kAttendCtasPerSm = 3;
 // CTAs of the [HCA | window] part beside the select: 2 per SM, one wave
-// (228 or 152 CTAs left room for the select but the step took 190 / 213 us)
-constexpr int kPart0Ctas = 2 * 152;
-constexpr int kScoreCtas = 152;         // CTAs of the score kernel per launch (1 per SM, one wave)
+// (1.5 or 1 per SM left room for the select but the step took 190 / 213 us)
+constexpr int kPart0CtasPerSm = 2;
+constexpr int kScoreCtasPerSm = 1;      // CTAs of the score kernel (1 per SM, one wave)
 constexpr int kSealCopySlices = 8;      // CTAs per sealing unit that copy its staged entries
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -320,6 +321,7 @@ struct kvpool {
   uint64_t fingerprint = 0;  // of the config, for prefix images
   Layout lay{};
   uint8_t* arena = nullptr;
+  int n_sms = 152;  // multiprocessors of the pool's device (queried at create)
   std::vector<int32_t> refcount;
   std::set<int32_t> free_blocks;
   std::set<int32_t> free_slots;
@@ -467,6 +469,12 @@ int kvpool_create(const kvpool_config* cfg, void* d_arena, size_t arena_bytes, v
 
   if (!no_dev) {
     cudaStream_t s = (cudaStream_t)stream;
+    // launch shapes are sized in CTAs per SM of the device the arena lives on
+    int dev = 0, sms = 0;
+    cudaError_t de = cudaGetDevice(&dev);
+    if (de == cudaSuccess) de = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (de != cudaSuccess || sms < 1) { int rc = p->cuda_fail(de != cudaSuccess ? de : cudaErrorInvalidDevice, "device query"); delete p; return rc; }
+    p->n_sms = sms;
     // gates: softmax on the host, one upload per layer and kind
     std::vector<float> a;
     for (int l = 0; l < cfg->n_layers; ++l) {
@@ -696,6 +704,7 @@ int launch_block_copies(kvpool_t* p, int32_t dst, const std::vector<ImageSeg>& s
     ip.pool = p->lay.pd;
     ip.dst = dst;
     ip.epoch = p->epoch;
+    ip.n_sms = p->n_sms;
     const size_t s0 = i * kMaxImageSegs, s1 = std::min(segs.size(), s0 + kMaxImageSegs);
     ip.n_segs = s1 > s0 ? (int32_t)(s1 - s0) : 0;
     int64_t pieces = 0;
@@ -1197,8 +1206,10 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
     }
     // a score CTA takes a run of one request's segments; every request rounds
     // its CTA count up, so lengthen the runs until the CTAs fit one wave
-    const int64_t spc0 = std::min<int64_t>(4096, std::max<int64_t>(8, (total_segs + kScoreCtas - 1) / kScoreCtas));
-    P.segs_per_cta = (int32_t)fit_one_wave(req_segs, spc0, 4096, kScoreCtas);
+    const int64_t score_target = (int64_t)kScoreCtasPerSm * p->n_sms;
+    const int64_t attend_target = (int64_t)kAttendCtasPerSm * p->n_sms;
+    const int64_t spc0 = std::min<int64_t>(4096, std::max<int64_t>(8, (total_segs + score_target - 1) / score_target));
+    P.segs_per_cta = (int32_t)fit_one_wave(req_segs, spc0, 4096, score_target);
     for (int i = 0; i < gn; ++i) {
       const Request& q = p->reqs[h_req_ids[g0 + i]];
       AttendReq& R = P.reqs[i];
@@ -1235,9 +1246,9 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
     // part 0 runs beside the select on the side stream when both parts have
     // work: two CTAs per SM leave room for the select and part 1
     const bool forked = Ld.has_csa && src1 > 0;
-    const int64_t target0 = forked ? kPart0Ctas : kAttendCtas;
+    const int64_t target0 = forked ? (int64_t)kPart0CtasPerSm * p->n_sms : attend_target;
     int64_t len0 = std::min<int64_t>(max_split_len, std::max<int64_t>(16, (src0 + target0 - 1) / target0));
-    int64_t len1 = std::min<int64_t>(max_split_len, std::max<int64_t>(16, (src1 + kAttendCtas - 1) / kAttendCtas));
+    int64_t len1 = std::min<int64_t>(max_split_len, std::max<int64_t>(16, (src1 + attend_target - 1) / attend_target));
     // every request rounds its split count up: lengthen the splits until the
     // CTAs fit one wave (a few CTAs past it would double the part's time)
     std::vector<int64_t> src_0(gn), src_1(gn);
@@ -1246,7 +1257,7 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
       src_1[i] = P.reqs[i].k;
     }
     len0 = fit_one_wave(src_0, len0, max_split_len, target0);
-    len1 = fit_one_wave(src_1, len1, max_split_len, kAttendCtas);
+    len1 = fit_one_wave(src_1, len1, max_split_len, attend_target);
     int splits0 = 0, splits1 = 0, parts = 0;
     for (int pass = 0; pass < 2; ++pass) {
       splits0 = splits1 = parts = 0;

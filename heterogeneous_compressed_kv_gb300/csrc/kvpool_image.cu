@@ -106,7 +106,8 @@ int launch_image(const ImageParams& p, void* stream, int* n_kernels) {
       (p.n_pieces > 0 && p.n_segs == 0))
     return (int)cudaErrorInvalidValue;
   const int64_t work = p.n_pieces > p.n_runs ? p.n_pieces : p.n_runs;
-  const int ctas = (int)(work < 152 * 8 ? work : 152 * 8);
+  const int64_t cap = (int64_t)kImageCtasPerSm * (p.n_sms > 0 ? p.n_sms : 1);  // at most 8 CTAs per SM
+  const int ctas = (int)(work < cap ? work : cap);
   launch_kernel(true, image_copy_kernel, dim3(ctas), dim3(kImageThreads), 0, reinterpret_cast<cudaStream_t>(stream),
                 p);
   *n_kernels += 1;

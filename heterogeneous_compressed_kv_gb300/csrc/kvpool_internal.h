@@ -125,11 +125,14 @@ struct ImageRun {
 constexpr int kMaxImageSegs = 64;
 constexpr int kMaxImageRuns = 64;
 constexpr int kImagePieceBytes = 16384;  // bytes one CTA copies per step
+constexpr int kImageCtasPerSm = 8;       // resident copy CTAs per SM (256 threads each)
 
 struct ImageParams {
   PoolDesc pool;
   int32_t dst;         // request slot whose table row the runs fill
   uint32_t epoch;      // activity stamp of the runs' blocks
+  int32_t n_sms;       // multiprocessors of the device (sizes the grid)
+  int32_t pad_;
   int32_t n_segs, n_runs;
   int64_t n_pieces;    // pieces of kImagePieceBytes over all segments
   int64_t piece_base[kMaxImageSegs + 1];  // first piece of each segment

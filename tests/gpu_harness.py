@@ -14,19 +14,31 @@ from tests import harness as H
 
 def tol(cache_dtype):
     """(max-abs, rel-L2) bound on the attention output: fp32 cache 1e-4 / 1e-5;
-    bf16 2e-2 / 5e-3; fp8 max-abs 6e-2 (rel-L2 not bounded separately)."""
-    return {K.F32: (1e-4, 1e-5), K.BF16: (2e-2, 5e-3), K.FP8_E4M3: (6e-2, None)}[cache_dtype]
+    bf16 2e-2 / 5e-3; fp8 6e-2 / 5e-3.
+
+    The fp8 max-abs bound alone cannot tell a right output from a wrong one at
+    long context: the output is a softmax average over ~10^4 sources, so its
+    entries are of order 1e-2 and an all-zero output is within 6e-2.  The
+    rel-L2 bound is the one with teeth there.  Both sides read the same
+    decoded codes; the GPU's own error sources are the query carried as two
+    e4m3 pieces (below 2^-17 of a head's largest element) and each weight
+    p * V-scale rounded to f16 (relative 2^-11 at most, about 2.8e-4 RMS, which
+    is the expected rel-L2 of the output), plus fp32 summation order.  5e-3 is
+    the bf16 bound: over ten times that expectation, and far below what a
+    missing source does (tests/test_parity_bounds.py)."""
+    return {K.F32: (1e-4, 1e-5), K.BF16: (2e-2, 5e-3), K.FP8_E4M3: (6e-2, 5e-3)}[cache_dtype]
 
 
 def check_out(gpu, ref, cache_dtype):
+    """Both bounds of tol(cache_dtype) on an attention output against the
+    oracle's; returns (max-abs error, rel-L2 error)."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     amax, rl2 = tol(cache_dtype)
     err = np.max(np.abs(gpu - ref))
     rel = np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-30)
     assert err <= amax, f"max-abs error {err} > {amax}"
-    if rl2 is not None:
-        assert rel <= rl2, f"rel-L2 error {rel} > {rl2}"
+    assert rel <= rl2, f"rel-L2 error {rel} > {rl2}"
     return err, rel
 
 
