@@ -7,10 +7,9 @@
 // the first comes from the histogram the score kernel built.  Three shapes:
 //  - at most 4096 candidates per request: one CTA per request keeps the keys
 //    in registers and does everything (select_small_kernel);
-//  - more: one CTA per 4096-key chunk lists the boundary bucket's keys, the
-//    request's last CTA (atomic count) finds T and every chunk's prefix, and
-//    an emit pass writes the selection (select_compact_kernel, then
-//    select_emit_kernel);
+//  - more: one CTA per 4096-key chunk lists its keys in buckets >= the first
+//    digit, the request's last CTA (atomic count) finds T from the lists and
+//    writes the selection from them (select_list_kernel);
 //  - a request of more than 16 chunks when the select has the GPU to itself:
 //    one thread-block cluster per request, digit histograms summed through
 //    distributed shared memory (select_cluster_kernel).
@@ -35,7 +34,7 @@ namespace {
 // ---------------------------------------------------------------------------
 constexpr int kSelThreads = 256;
 constexpr int kItems = kSelectKeysPerCta / kSelThreads;  // 16 keys per thread
-constexpr uint32_t kCandCache = 4096;                    // boundary-bucket candidates kept in shared memory
+constexpr uint32_t kCandCache = 4096;                    // listed candidates kept in shared memory
 
 // Block-wide (NT threads): the digit d (bin index) at which the
 // count of keys in bins above d is < k and the count in bins >= d is >= k,
@@ -117,71 +116,79 @@ __device__ __forceinline__ int load_items(const uint32_t* keys, int64_t my0, int
   return n;
 }
 
-// Pass 1 of the select (one CTA per 4096 keys of a request): the first digit
-// d1 of the k-th largest key follows from the score histogram; keys above
-// bucket d1 are surely selected (counted per chunk), keys inside it become
-// candidates.  The last CTA of the request then finds the exact threshold T
-// among the candidates (two more radix digits), how many keys equal to T are
-// taken, and every chunk's exclusive prefix of (keys > T, keys == T).  No
-// CTA waits on another: the last one is found with an atomic counter after a
-// fence.
-__global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __grid_constant__ AttendParams P) {
+// Multi-chunk requests (one CTA per 4096 keys): the whole select in one
+// launch.  The first digit d1 of the k-th largest key follows from the score
+// histogram; every CTA lists its keys in buckets >= d1 (fewer than k lie
+// above d1, plus the boundary bucket) as (key, index) pairs, in index order,
+// in its chunk's region of the candidate buffer.  The request's last CTA
+// (atomic count after a fence) concatenates the lists in chunk order, which
+// is ascending index order, takes the two remaining digits from histograms of
+// the listed keys, and writes the selection -- keys above the threshold T and
+// the first `need` keys equal to it -- with block scans over the lists.  No
+// CTA waits on another, and no pass reads all keys twice.  The lists are
+// usually a few thousand pairs; when the scores tie massively the boundary
+// bucket holds most keys and the last CTA works through all of them (slower,
+// still exact).
+__device__ __forceinline__ int list_chunk_of(const uint32_t* coff, int n_chunks, uint32_t t) {
+  // the chunk c whose list holds element t: coff[c] <= t < coff[c + 1]
+  int lo = 0, hi = n_chunks - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (coff[mid] <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kSelThreads) select_list_kernel(const __grid_constant__ AttendParams P) {
   pdl_start();
   __shared__ uint32_t sh[kSelThreads];
   __shared__ uint32_t st[8];
   __shared__ uint32_t h2[kHistBins];
-  __shared__ uint32_t cgt[kMaxKeyCtasPerReq], ceq[kMaxKeyCtasPerReq];
+  __shared__ uint32_t coff[kMaxKeyCtasPerReq + 1];
   __shared__ uint2 cs[kCandCache];
   __shared__ int is_last;
   const int i = find_req(P, blockIdx.x, 1);
   const AttendReq& R = P.reqs[i];
-  if (R.select_all || R.k == 0) return;
   const int chunk = blockIdx.x - R.key_base;
   const int n_chunks = (R.n_cand + kSelectKeysPerCta - 1) / kSelectKeysPerCta;
   const int64_t k0 = (int64_t)chunk * kSelectKeysPerCta;
-  if (k0 >= R.n_cand) return;
+  int32_t* sel = P.sel + (int64_t)i * P.sel_stride;
+  int32_t* tko = P.topk_out ? P.topk_out + (int64_t)(P.row0 + i) * P.top_k : nullptr;
+  const int tid = threadIdx.x;
+  if (chunk == 0 && tko)
+    for (int j = R.k + tid; j < P.top_k; j += blockDim.x) tko[j] = -1;
+  if (R.k == 0 || k0 >= R.n_cand) return;
   const int64_t kend = min((int64_t)R.n_cand, k0 + kSelectKeysPerCta);
+  if (R.select_all) {
+    for (int64_t e = k0 + tid; e < kend; e += blockDim.x) {
+      sel[e] = (int32_t)e;
+      if (tko) tko[e] = (int32_t)e;
+    }
+    return;
+  }
   uint32_t* sync = P.sync + (int64_t)i * 4;
   uint2* cand = P.cand + (int64_t)i * P.key_stride;
+  uint32_t* cnt = P.counts + ((int64_t)i * P.max_key_ctas) * 2;
   const uint32_t* keys = P.keys + (int64_t)i * P.key_stride;
-  const int tid = threadIdx.x, lane = tid & 31;
 
   uint32_t kk[kItems];
   const int64_t my0 = k0 + (int64_t)tid * kItems;
   const int n_mine = load_items(keys, my0, kend, kk);
   find_digit(P.hist + (int64_t)i * kHistBins, kHistBins, (uint32_t)R.k, sh, &st[0], &st[1]);
   const uint32_t d1 = st[0], k1 = st[1];
-  uint32_t gt = 0, nc = 0;
+  const uint32_t lo_key = d1 << 21;  // the smallest key of bucket d1
+  uint32_t c = 0;
 #pragma unroll
-  for (int j = 0; j < kItems; ++j) {
-    if (j < n_mine) {
-      gt += (kk[j] >> 21) > d1 ? 1u : 0u;
-      nc += (kk[j] >> 21) == d1 ? 1u : 0u;
-    }
-  }
-  // candidates: one atomic per warp, then each thread writes its own in order
-  uint32_t inc = nc;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t u = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += u;
-  }
-  uint32_t base = 0;
-  if (lane == 31 && inc) base = atomicAdd(&sync[0], inc);
-  base = __shfl_sync(0xffffffffu, base, 31) + inc - nc;
+  for (int j = 0; j < kItems; ++j) c += (j < n_mine && kk[j] >= lo_key) ? 1u : 0u;
+  uint32_t listed;
+  uint32_t pos = block_excl_scan(c, sh, &listed);
+  uint2* lst = cand + k0;  // this chunk's region: room for every key of the chunk
 #pragma unroll
   for (int j = 0; j < kItems; ++j)
-    if (j < n_mine && (kk[j] >> 21) == d1) cand[base++] = make_uint2(kk[j], (uint32_t)(my0 + j));
-  // chunk total of surely-selected keys
-  for (int o = 16; o > 0; o >>= 1) gt += __shfl_xor_sync(0xffffffffu, gt, o);
-  if (tid == 0) st[2] = 0;
-  __syncthreads();
-  if (lane == 0) atomicAdd(&st[2], gt);
-  __syncthreads();
-  uint32_t* cnt = P.counts + ((int64_t)i * P.max_key_ctas) * 2;
+    if (j < n_mine && kk[j] >= lo_key) lst[pos++] = make_uint2(kk[j], (uint32_t)(my0 + j));
   if (tid == 0) {
-    cnt[2 * chunk] = st[2];
-    cnt[2 * chunk + 1] = 0;
+    cnt[2 * chunk] = listed;
     __threadfence();
     is_last = atomicAdd(&sync[1], 1u) == (uint32_t)(n_chunks - 1);
   }
@@ -189,53 +196,92 @@ __global__ void __launch_bounds__(kSelThreads) select_compact_kernel(const __gri
   if (!is_last) return;
   __threadfence();
 
-  // ---- the last CTA: exact threshold among the candidates ----
-  const uint32_t n_c = __ldcg(&sync[0]);
-  const bool cached = n_c <= kCandCache;  // usually a few thousand: keep them in shared memory
-  if (cached)
-    for (uint32_t j = tid; j < n_c; j += kSelThreads) cs[j] = __ldcg(&cand[j]);
+  // ---- the last CTA: the lists' offsets, in chunk order ----
+  uint32_t n_list;
+  {
+    const uint32_t len = tid < n_chunks ? __ldcg(&cnt[2 * tid]) : 0u;
+    const uint32_t off = block_excl_scan(len, sh, &n_list);  // n_chunks <= kMaxKeyCtasPerReq = kSelThreads
+    if (tid < n_chunks) coff[tid] = off;
+  }
+  __syncthreads();
+  // element t of the concatenated list (every thread of the CTA may call it)
+  auto at_global = [&](uint32_t t) -> uint2 {
+    const int cc = list_chunk_of(coff, n_chunks, t);
+    return __ldcg(&cand[(int64_t)cc * kSelectKeysPerCta + (t - coff[cc])]);
+  };
+  const uint32_t n_cached = min(n_list, kCandCache);
+  for (uint32_t t0 = 0; t0 < n_cached; t0 += 4 * kSelThreads) {  // four loads in flight per thread
+    uint2 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t t = t0 + u * kSelThreads + tid;
+      if (t < n_cached) v[u] = at_global(t);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t t = t0 + u * kSelThreads + tid;
+      if (t < n_cached) cs[t] = v[u];
+    }
+  }
   for (int b = tid; b < kHistBins; b += kSelThreads) h2[b] = 0u;
   __syncthreads();
-  auto cand_at = [&](uint32_t j) -> uint2 { return cached ? cs[j] : __ldcg(&cand[j]); };
-  for (uint32_t j = tid; j < n_c; j += kSelThreads) atomicAdd(&h2[(cand_at(j).x >> 10) & 2047u], 1u);
+  auto at = [&](uint32_t t) -> uint2 { return t < n_cached ? cs[t] : at_global(t); };
+  // second digit: the next 11 bits of the listed keys in bucket d1
+  for (uint32_t t = tid; t < n_list; t += kSelThreads) {
+    const uint32_t key = at(t).x;
+    if ((key >> 21) == d1) atomicAdd(&h2[(key >> 10) & 2047u], 1u);
+  }
   __syncthreads();
   find_digit(h2, kHistBins, k1, sh, &st[3], &st[4]);
-  const uint32_t d2 = st[3], k2 = st[4];
-  for (int b = tid; b < kHistBins; b += kSelThreads) h2[b] = 0u;
+  const uint32_t pre = (d1 << 11) | st[3], k2 = st[4];
+  for (int b = tid; b < 1024; b += kSelThreads) h2[b] = 0u;
   __syncthreads();
-  const uint32_t pre = (d1 << 11) | d2;
-  for (uint32_t j = tid; j < n_c; j += kSelThreads) {
-    const uint32_t key = cand_at(j).x;
+  // third digit: the low 10 bits of the listed keys with that prefix
+  for (uint32_t t = tid; t < n_list; t += kSelThreads) {
+    const uint32_t key = at(t).x;
     if ((key >> 10) == pre) atomicAdd(&h2[key & 1023u], 1u);
   }
   __syncthreads();
   find_digit(h2, 1024, k2, sh, &st[5], &st[6]);
   const uint32_t T = (pre << 10) | st[5], need = st[6];
-  for (int c = tid; c < n_chunks; c += kSelThreads) cgt[c] = ceq[c] = 0u;
-  __syncthreads();
-  for (uint32_t j = tid; j < n_c; j += kSelThreads) {
-    const uint2 ce = cand_at(j);
-    const int c = (int)(ce.y / kSelectKeysPerCta);
-    if (ce.x > T) atomicAdd(&cgt[c], 1u);
-    else if (ce.x == T) atomicAdd(&ceq[c], 1u);
+  // ordered emission: tiles of kItems consecutive list elements per thread; a
+  // selected key's position is the number of keys > T before it plus
+  // min(keys == T before it, need)
+  uint32_t gt_base = 0, eq_base = 0;
+  for (uint32_t t0 = 0; t0 < n_list; t0 += kSelThreads * kItems) {
+    const uint32_t my = t0 + (uint32_t)tid * kItems;
+    uint2 v[kItems];
+    uint32_t n_gt = 0, n_eq = 0;
+#pragma unroll
+    for (int j = 0; j < kItems; ++j) {
+      v[j] = my + j < n_list ? at(my + j) : make_uint2(0u, 0u);
+      n_gt += (my + j < n_list && v[j].x > T) ? 1u : 0u;
+      n_eq += (my + j < n_list && v[j].x == T) ? 1u : 0u;
+    }
+    uint32_t tot_gt, tot_eq;
+    uint32_t gt_rank = gt_base + block_excl_scan(n_gt, sh, &tot_gt);
+    uint32_t eq_rank = eq_base + block_excl_scan(n_eq, sh, &tot_eq);
+#pragma unroll
+    for (int j = 0; j < kItems; ++j) {
+      if (my + j >= n_list) break;
+      const bool g = v[j].x > T, q = v[j].x == T;
+      if (g || (q && eq_rank < need)) {
+        const uint32_t p = gt_rank + min(eq_rank, need);
+        const uint32_t e = v[j].y;
+        if (p < (uint32_t)R.k && e < (uint32_t)R.n_cand) {
+          sel[p] = (int32_t)e;
+          if (tko) tko[p] = (int32_t)e;
+        } else {
+          flag_error(P.pool, kErrBadIndex);
+        }
+      }
+      if (g) ++gt_rank;
+      if (q) ++eq_rank;
+    }
+    gt_base += tot_gt;
+    eq_base += tot_eq;
   }
-  __syncthreads();
-  // per-chunk exclusive prefixes (n_chunks <= kMaxKeyCtasPerReq = kSelThreads)
-  const uint32_t g = tid < n_chunks ? __ldcg(&cnt[2 * tid]) + cgt[tid] : 0u;
-  const uint32_t e = tid < n_chunks ? ceq[tid] : 0u;
-  uint32_t tot;
-  const uint32_t pg = block_excl_scan(g, sh, &tot);
-  const uint32_t pe = block_excl_scan(e, sh, &tot);
-  if (tid < n_chunks) {
-    cnt[2 * tid] = pg;
-    cnt[2 * tid + 1] = pe;
-  }
-  if (tid == 0) {
-    P.thr[2 * i] = T;
-    P.thr[2 * i + 1] = need;
-    sync[0] = 0u;  // ready for the next call
-    sync[1] = 0u;
-  }
+  if (tid == 0) sync[1] = 0u;  // ready for the next call
 }
 
 // The whole select for a launch whose requests have at most
@@ -557,65 +603,6 @@ __global__ void __launch_bounds__(kSelCThreads) select_cluster_kernel(const __gr
   cl.sync();  // no CTA leaves while a peer may still read its totals
 }
 
-// Pass 2: every chunk writes its selected indices in ascending order, from the
-// exclusive prefixes the last compact CTA stored for it.
-__global__ void __launch_bounds__(kSelThreads) select_emit_kernel(const __grid_constant__ AttendParams P) {
-  pdl_start();
-  __shared__ uint32_t sh[kSelThreads];
-  const int i = find_req(P, blockIdx.x, 1);
-  const AttendReq& R = P.reqs[i];
-  const int chunk = blockIdx.x - R.key_base;
-  const int64_t k0 = (int64_t)chunk * kSelectKeysPerCta;
-  int32_t* sel = P.sel + (int64_t)i * P.sel_stride;
-  int32_t* tko = P.topk_out ? P.topk_out + (int64_t)(P.row0 + i) * P.top_k : nullptr;
-  if (chunk == 0 && tko)
-    for (int j = R.k + threadIdx.x; j < P.top_k; j += blockDim.x) tko[j] = -1;
-  if (R.k == 0 || k0 >= R.n_cand) return;
-  const int64_t kend = min((int64_t)R.n_cand, k0 + kSelectKeysPerCta);
-  if (R.select_all) {
-    for (int64_t e = k0 + threadIdx.x; e < kend; e += blockDim.x) {
-      sel[e] = (int32_t)e;
-      if (tko) tko[e] = (int32_t)e;
-    }
-    return;
-  }
-  const uint32_t T = P.thr[2 * i], need = P.thr[2 * i + 1];
-  const uint32_t* cnt = P.counts + (int64_t)i * P.max_key_ctas * 2;
-  const uint32_t base_gt = cnt[2 * chunk], base_eq = cnt[2 * chunk + 1];
-  const uint32_t* keys = P.keys + (int64_t)i * P.key_stride;
-  const int64_t my0 = k0 + (int64_t)threadIdx.x * kItems;
-  uint32_t kk[kItems];
-  const int n_mine = load_items(keys, my0, kend, kk);
-  uint32_t n_gt = 0, n_eq = 0;
-#pragma unroll
-  for (int j = 0; j < kItems; ++j) {
-    n_gt += j < n_mine && kk[j] > T;
-    n_eq += j < n_mine && kk[j] == T;
-  }
-  uint32_t tot;
-  const uint32_t pre_gt = block_excl_scan(n_gt, sh, &tot);
-  const uint32_t pre_eq = block_excl_scan(n_eq, sh, &tot);
-  uint32_t eq_rank = base_eq + pre_eq;  // keys equal to T before my first one
-  uint32_t gt_rank = base_gt + pre_gt;
-#pragma unroll
-  for (int j = 0; j < kItems; ++j) {
-    if (j >= n_mine) break;
-    const int64_t e = my0 + j;
-    const bool take = kk[j] > T || (kk[j] == T && eq_rank < need);
-    if (take) {
-      const uint32_t pos = gt_rank + min(eq_rank, need);
-      if (pos < (uint32_t)R.k) {
-        sel[pos] = (int32_t)e;
-        if (tko) tko[pos] = (int32_t)e;
-      } else {
-        flag_error(P.pool, kErrBadIndex);
-      }
-    }
-    if (kk[j] > T) ++gt_rank;
-    if (kk[j] == T) ++eq_rank;
-  }
-}
-
 }  // namespace
 
 namespace {
@@ -709,12 +696,10 @@ int launch_select(const AttendParams& p, void* stream, int* n_kernels, bool alon
       return (int)cudaGetLastError();
     }
   }
-  bool any_radix = max_cand > 0;
-  if (any_radix) {
-    launch_kernel(false, select_compact_kernel, dim3(p.total_key_ctas), dim3(kSelThreads), 0, s, p);
-    *n_kernels += 1;
-  }
-  launch_kernel(false, select_emit_kernel, dim3(p.total_key_ctas), dim3(kSelThreads), 0, s, p);
+  // every other shape: one CTA per 4096-key chunk, the request's last CTA
+  // finishes it (launched without programmatic dependent launch: its
+  // early-started CTAs would hold SM room that the attention beside it needs)
+  launch_kernel(false, select_list_kernel, dim3(p.total_key_ctas), dim3(kSelThreads), 0, s, p);
   *n_kernels += 1;
   return (int)cudaGetLastError();
 }
@@ -841,4 +826,23 @@ extern "C" int kvpool_topk_static(const float* d_scores, int32_t n_rows, int32_t
   if (rc == 0) rc = launch_select(*P, stream, &nk, true);
   delete P;
   return rc == 0 ? KVPOOL_OK : KVPOOL_ERR_CUDA;
+}
+
+extern "C" int kvpool_topk_static_check(void* stream, uint32_t* h_flags) {
+  using namespace kvp;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVPOOL_ERR_CUDA;
+  uint32_t word = 0;
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    base = g_scratch_addr[dev];
+  }
+  if (base) {  // no call on this device yet: nothing can have been flagged
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KVPOOL_ERR_CUDA;
+    if (cudaMemcpy(&word, base, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess) return KVPOOL_ERR_CUDA;
+  }
+  if (h_flags) *h_flags = word;
+  return word == 0 ? KVPOOL_OK : KVPOOL_ERR_DEVICE_CHECK;
 }

@@ -31,7 +31,7 @@ EXPORTS = ["kvpool_required_bytes", "kvpool_create", "kvpool_destroy", "kvpool_a
            "kvpool_topk_static", "kvpool_profile_timeline", "kvpool_fingerprint", "kvpool_image_bytes",
            "kvpool_export_prefix", "kvpool_import_prefix", "kvpool_host_slot_bytes", "kvpool_set_host_pool",
            "kvpool_offload", "kvpool_fetch", "kvpool_block_location", "kvpool_epoch", "kvpool_block_activity",
-           "kvpool_inactive_blocks", "kvpool_wait_selftest"]
+           "kvpool_inactive_blocks", "kvpool_wait_selftest", "kvpool_topk_static_check"]
 
 
 class KvpoolError(RuntimeError):
@@ -99,6 +99,7 @@ def lib():
         L.kvpool_profile_enable.argtypes = [vp, C.c_int]
         L.kvpool_profile_read.argtypes = [vp, i32, C.POINTER(C.c_double), C.POINTER(i64), C.POINTER(i64)]
         L.kvpool_topk_static.argtypes = [vp, i32, i32, i32, vp, vp]
+        L.kvpool_topk_static_check.argtypes = [vp, C.POINTER(C.c_uint32)]
         L.kvpool_profile_timeline.argtypes = [vp, i32, vp]
         L.kvpool_fingerprint.restype = C.c_uint64
         L.kvpool_fingerprint.argtypes = [vp]
@@ -176,9 +177,24 @@ def required_bytes(cfg: PoolConfig) -> int:
 def topk_static(scores, top_k: int, out, stream=None) -> int:
     """Top-k of each row of a [n_rows][n_cols] fp32 device tensor into
     ``out`` ([n_rows][top_k] int32) using only the library's static device
-    scratch (no allocation); see kvpool_topk_static in include/kvpool.h."""
+    scratch (no allocation); see kvpool_topk_static in include/kvpool.h.
+    Raises ValueError for tensors the kernels cannot take as they are."""
+    import torch
+    if scores.dim() != 2 or scores.dtype != torch.float32 or not scores.is_cuda or not scores.is_contiguous():
+        raise ValueError("topk_static: scores must be a contiguous 2-D float32 CUDA tensor")
     n_rows, n_cols = scores.shape
+    if (out.dtype != torch.int32 or not out.is_cuda or not out.is_contiguous() or out.device != scores.device
+            or tuple(out.shape) != (n_rows, top_k)):
+        raise ValueError("topk_static: out must be a contiguous int32 [n_rows][top_k] tensor on the scores' device")
     return lib().kvpool_topk_static(scores.data_ptr(), n_rows, n_cols, top_k, out.data_ptr(), _stream(stream))
+
+
+def topk_static_check(stream=None) -> tuple:
+    """(return code, device error flags) of the last topk_static call on the
+    current device; synchronizes the stream."""
+    w = C.c_uint32(0)
+    rc = lib().kvpool_topk_static_check(_stream(stream), C.byref(w))
+    return int(rc), int(w.value)
 
 
 def _ptr(t) -> Optional[int]:

@@ -323,10 +323,11 @@ int kvpool_decode_attend(kvpool_t* pool, int32_t layer, int32_t n, const int32_t
  * design pages have no counterpart of this entry point: it is the indexer's
  * selection step (same rule as decode_attend: k = min(top_k, n_cols) largest
  * scores, ties to the lower index, -0 == +0, ascending indices padded with
- * -1) offered on its own to callers that cannot allocate device memory --
- * code that runs while a stream is being captured into a CUDA graph, or a
+ * -1) offered on its own to callers that cannot allocate device memory: a
  * plugin that only receives its input and output buffers from a host
- * framework that owns every allocation.
+ * framework that owns every allocation (and gives the plugin no allocator),
+ * or a serving loop whose device memory is budgeted once at start-up and must
+ * not fail or stall on an allocation in the middle of a step.
  * d_scores: [n_rows][n_cols] fp32 (finite) on the device (may be NULL when
  * n_cols is 0: every row is then all -1); d_topk_out: [n_rows][top_k] int32.  Its scratch (sort keys, radix histograms, counts)
  * is a file-scope 16 MiB device array in this library, present on every GPU
@@ -341,9 +342,19 @@ int kvpool_decode_attend(kvpool_t* pool, int32_t layer, int32_t n, const int32_t
  * device) and should come before any stream capture.
  * Every call shares the array and clears what must start at zero; calls that
  * overlap on the GPU (other streams, other host threads) race.  Errors:
- * INVALID_ARG, CUDA. */
+ * INVALID_ARG, CUDA; kernel-side errors land in the array's error word, which
+ * kvpool_topk_static_check reads. */
 int kvpool_topk_static(const float* d_scores, int32_t n_rows, int32_t n_cols, int32_t top_k, int32_t* d_topk_out,
                        void* stream);
+
+/* Device-side error flags of the last kvpool_topk_static call on the current
+ * device (the kvpool_check_device bits: 8 = a launch shape the kernels
+ * refused, 4 = an index out of range).  Synchronizes `stream` first, then
+ * copies the word to *h_flags (may be NULL).  Allocates nothing.  Returns OK
+ * when the word is zero, DEVICE_CHECK when a flag is set (the output of that
+ * call is not a valid top-k), CUDA on a CUDA error.  Call it before the next
+ * kvpool_topk_static, which clears the word. */
+int kvpool_topk_static_check(void* stream, uint32_t* h_flags);
 
 /* ---- host-side queries (no device access) ---- */
 typedef struct kvpool_info {

@@ -371,3 +371,16 @@ def test_hisparse_refusals():
     assert lay["csa_staging_base"] == 8 and lay["csa_hot_slots"] == 8
     assert lay["host_slot_bytes"] == lay["csa_block_bytes"] and lay["csa_host_offset"] == 0
     assert p.set_host_pool(np.zeros(16, np.uint8), check=False) == K.ERR_INVALID_ARG  # too small
+
+
+def test_topk_static_wrapper_refuses_tensors_the_kernels_cannot_take():
+    # the binding checks shapes, types and devices before calling the library
+    import torch
+    s = torch.zeros((2, 8), dtype=torch.float32)  # host memory
+    out = torch.zeros((2, 3), dtype=torch.int32)
+    with pytest.raises(ValueError):
+        K.topk_static(s, 3, out)
+    with pytest.raises(ValueError):
+        K.topk_static(torch.zeros(8, dtype=torch.float32), 3, out)  # not 2-D
+    with pytest.raises(ValueError):
+        K.topk_static(s.double(), 3, out)

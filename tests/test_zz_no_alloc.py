@@ -1,7 +1,8 @@
 """The allocation-free top-k entry point (kvpool_topk_static) against the
-regular path.  Some callers cannot allocate device memory (a stream being
-captured into a CUDA graph, a plugin that only gets its input and output
-buffers); kvpool_topk_static serves them from a static device array.  Its
+regular path.  Some callers cannot allocate device memory (a plugin that only
+gets its input and output buffers from a framework that owns every
+allocation, a serving loop whose memory is budgeted once at start-up);
+kvpool_topk_static serves them from a static device array.  Its
 selection must equal what kvpool_decode_attend returns as top-k for the same
 indexer scores -- exactly, as every top-k comparison in these tests -- on two
 calls in a row (the second call reuses the array the first one left behind).
@@ -38,7 +39,7 @@ def test_static_topk_matches_decode_attend_topk_twice():
         d_scores = torch.from_numpy(scores).cuda()
         got = torch.full((3, top_k), -7, dtype=torch.int32, device="cuda")
         assert K.topk_static(d_scores, top_k, got) == 0
-        torch.cuda.synchronize()
+        assert K.topk_static_check() == (0, 0), "the kernels flagged an error"
         assert np.array_equal(got.cpu().numpy(), tk_ref), f"call {call}: static top-k differs"
 
 
@@ -106,7 +107,7 @@ def test_static_topk_matches_the_oracle_across_select_paths(n, top_k, kind):
     for call in range(2):
         got = torch.full((rows, top_k), -7, dtype=torch.int32, device="cuda")
         assert K.topk_static(d, top_k, got) == 0
-        torch.cuda.synchronize()
+        assert K.topk_static_check() == (0, 0), "the kernels flagged an error"
         g = got.cpu().numpy()
         for r in range(rows):
             if not np.array_equal(g[r], ref[r]):
