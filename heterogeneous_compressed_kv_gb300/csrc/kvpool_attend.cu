@@ -517,7 +517,10 @@ __global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __gr
       }
       issued = st + 1;
     }
-    if (!ok && lane == 0)  // drain the copies still in flight before leaving
+    // on every exit path, wait (time-limited) for this CTA's copies still in
+    // flight, so the CTA never ends while bulk copies land in its shared
+    // memory: a consumer whose wait ran out may already have left
+    if (lane == 0)
       for (int t = max(0, issued - kStages); t < issued; ++t) mbar_wait(&full[t % kStages], (t / kStages) & 1, pd);
     return;
   }

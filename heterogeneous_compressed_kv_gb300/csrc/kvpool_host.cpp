@@ -404,6 +404,9 @@ struct kvpool {
       cudaEventRecord(s.b, (cudaStream_t)stream);
       s.n_kernels = nk;
       prof.push_back(s);
+    } else if (profiling & KVPOOL_PROFILE_COUNT) {  // counted without events
+      prof_launches[kernel] += nk;
+      prof_bytes[kernel] += bytes;
     }
     return rc;
   }
@@ -1407,7 +1410,7 @@ int kvpool_check_device(kvpool_t* p, void* stream, uint32_t* word_out) {
 }
 
 int kvpool_profile_enable(kvpool_t* p, int kinds) {
-  if (!p || (kinds & ~KVPOOL_PROFILE_ALL)) return KVPOOL_ERR_INVALID_ARG;
+  if (!p || (kinds & ~(KVPOOL_PROFILE_ALL | KVPOOL_PROFILE_COUNT))) return KVPOOL_ERR_INVALID_ARG;
   if (kinds) {
     p->settle_profile();
     p->timeline.clear();

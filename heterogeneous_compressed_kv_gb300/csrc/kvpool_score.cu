@@ -171,12 +171,15 @@ struct IdxChunkFast<KVPOOL_F32> {  // unused: fp32 keys take the fp32 chain
 // a CTA takes the CTA's blocks w, w + W, w + 2W, ...; a slot's barrier is only
 // waited on by its own warp, in order, so every parity wait is exact.
 // ---------------------------------------------------------------------------
-// Warps per score CTA: more warps keep more fixed-order chains in flight; FP4
-// blocks are small enough for 16 warps with 3 slots each, the larger blocks
-// of the other types fit 8.
+// Warps per score CTA: more warps keep more fixed-order chains in flight (the
+// chain is latency-bound: one dependent FMA per key value).  FP4 blocks are
+// small enough for 16 warps with 2 slots each; fp8 blocks take 16 warps with
+// one slot each (a warp moves its block's keys into registers and refills the
+// slot before running its chains, so the copy of its next block is in flight
+// meanwhile: 16 copies per SM); the 16 KiB bf16 blocks fit 8 warps.
 template <int IDX>
 struct ScoreShape {
-  static constexpr int kWarps = IDX == KVPOOL_FP4_E2M1 ? 16 : 8;
+  static constexpr int kWarps = (IDX == KVPOOL_FP4_E2M1 || IDX == KVPOOL_FP8_E4M3) ? 16 : 8;
   static constexpr int kRegChunks = IDX == KVPOOL_FP4_E2M1 ? 8 : 16;  // key chunks held in registers
 };
 constexpr int kScoreMaxWarps = 16;
@@ -184,7 +187,9 @@ constexpr int kScoreMaxRing = 3;                      // slots per warp
 constexpr int kScoreMaxSlots = kScoreMaxWarps * kScoreMaxRing;
 constexpr int kScoreMaxGates = 64;  // per-token keys: idx_heads * m gates in shared memory
 constexpr int kScoreStageBudget = 140 * 1024;         // shared memory for slots: two per warp measured as fast as three
-__host__ __device__ constexpr int score_warps(int idx_dtype) { return idx_dtype == KVPOOL_FP4_E2M1 ? 16 : 8; }
+__host__ __device__ constexpr int score_warps(int idx_dtype) {
+  return (idx_dtype == KVPOOL_FP4_E2M1 || idx_dtype == KVPOOL_FP8_E4M3) ? 16 : 8;
+}
 
 // PT: per-token indexer keys.  A segment is then one run of csa_per_block
 // tokens (csa_per_block / m entries) instead of one block; lane t scores

@@ -70,6 +70,37 @@ def churn_count(cfg) -> int:
     return int(round(cfg["churn"] * cfg["n_requests"]))
 
 
+def mixed_schedule(cfg, steps: int):
+    """The mixed-serving schedule on the host: the initial lengths, and per
+    decode step the slots that finish, the arrivals (slot, workload id,
+    length) and the peak number of sealed blocks.  Lengths are lognormal
+    (median 4096, capped); arrivals take the lowest free slots; step 0 has no
+    churn; every active request grows by one token per step."""
+    B, n_ch, mp_ = cfg["n_requests"], churn_count(cfg), cfg["m_prime"]
+    lens = [int(x) for x in lognormal_lengths(cfg["seed"], B, cfg["len_median"], cfg["len_sigma"], cfg["len_cap"])]
+    cur = {s: L for s, L in enumerate(lens)}
+    free, wid, plan, peak = [], B, [], 0
+    for step in range(steps):
+        gone, arrivals = [], []
+        if step > 0:
+            order = sorted(cur)
+            gone = [order[j] for j in churn_picks(cfg["seed"], step, len(order), n_ch)]
+            for s in gone:
+                del cur[s]
+            free = sorted(free + gone)
+            for L in lognormal_lengths(cfg["seed"], n_ch, cfg["len_median"], cfg["len_sigma"], cfg["len_cap"],
+                                       index0=B + (step - 1) * n_ch):
+                s = free.pop(0)
+                arrivals.append((s, wid, int(L)))
+                cur[s] = int(L)
+                wid += 1
+        for s in cur:
+            cur[s] += 1
+        plan.append((gone, arrivals))
+        peak = max(peak, sum(L // mp_ for L in cur.values()))
+    return lens, plan, peak
+
+
 def blocks_needed(lengths, m_prime: int) -> int:
     return int(sum(int(L) // m_prime for L in lengths))
 

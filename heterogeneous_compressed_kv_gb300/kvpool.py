@@ -23,6 +23,7 @@ ERR_NOT_SHAREABLE, ERR_CUDA, ERR_DEVICE_CHECK, ERR_CAPACITY, ERR_BAD_IMAGE = -5,
 KERNEL_APPEND, KERNEL_SCORE, KERNEL_SELECT, KERNEL_ATTEND, KERNEL_COMBINE, KERNEL_IMAGE = range(6)
 KERNEL_NAMES = ["append", "score", "select", "attend", "combine", "image"]
 IMAGE_WINDOW = 1  # prefix image flag: include the SWA window (a checkpoint)
+PROFILE_COUNT = 1 << 16  # profiling flag: count launches and bytes without events
 
 EXPORTS = ["kvpool_required_bytes", "kvpool_create", "kvpool_destroy", "kvpool_alloc_request",
            "kvpool_free_request", "kvpool_share_prefix", "kvpool_append", "kvpool_decode_attend",
@@ -406,12 +407,16 @@ class Pool:
             raise KvpoolError(rc, f"check_device: {self.last_error()} (flags {w.value:#x})")
         return w.value
 
-    def profile_enable(self, on: bool = True, kinds=None) -> None:
+    def profile_enable(self, on: bool = True, kinds=None, count: bool = False) -> None:
         """Record the launches of the given kernel kinds (indexes into
-        KERNEL_NAMES; all kinds when None), or stop recording."""
+        KERNEL_NAMES; all kinds when None), or stop recording.  count: every
+        launch of every kind also adds its kernel count and algorithmic bytes
+        to the totals, with no events (kinds=[] counts without timing)."""
         mask = 0
         if on:
             mask = (1 << len(KERNEL_NAMES)) - 1 if kinds is None else sum(1 << int(k) for k in set(kinds))
+            if count:
+                mask |= PROFILE_COUNT
         self._check(self.L.kvpool_profile_enable(self.h, mask), "profile_enable")
 
     def profile_timeline(self, cap: int = 4096):

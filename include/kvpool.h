@@ -455,9 +455,14 @@ enum {
   KVPOOL_KERNEL_COUNT = 6
 };
 #define KVPOOL_PROFILE_ALL ((1 << KVPOOL_KERNEL_COUNT) - 1)
+/* With this bit in the mask every launch of every kind also adds its kernel
+ * count and algorithmic bytes to its kind's totals, with no events (its time
+ * is not measured): accounting that leaves the launches' timing untouched. */
+#define KVPOOL_PROFILE_COUNT (1 << 16)
 /* Record events around the launches of the kernel kinds whose bit is set in
- * kinds (bit k = KVPOOL_KERNEL_k; KVPOOL_PROFILE_ALL for every kind); 0
- * disables recording.  A non-zero mask resets the totals and the timeline.
+ * kinds (bit k = KVPOOL_KERNEL_k; KVPOOL_PROFILE_ALL for every kind), and with
+ * KVPOOL_PROFILE_COUNT count every launch; 0 disables recording.  A non-zero
+ * mask resets the totals and the timeline.
  * Each recorded launch adds two event records to its stream. */
 int kvpool_profile_enable(kvpool_t* pool, int kinds);
 /* Synchronize and report, for one kernel kind, the summed device time of its
