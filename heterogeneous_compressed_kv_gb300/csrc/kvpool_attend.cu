@@ -621,9 +621,11 @@ __global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __gr
 
 // Merge of the split partials of one (request, head): o = sum_s 2^(m_s - M) o_s
 // / sum_s 2^(m_s - M) l_s.  Warp w of the CTA's nw warps merges splits w,
-// w + nw, ... with its own running maximum, lane l owns dims [4l, 4l + 4);
-// the warp results are merged through shared memory.  nw is sized to the
-// split count (about four splits per warp, at most kCombineWarps).
+// w + nw, ... into its own running (max, sum, output) in one pass -- every
+// split's loads are independent of the running state, so they are all in
+// flight together -- lane l owning dims [4l, 4l + 4); the warps' states are
+// then merged through shared memory.  nw is sized to the split count (about
+// four splits per warp, at most kCombineWarps).
 constexpr int kCombineWarps = 32;
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __grid_constant__ AttendParams P) {
   pdl_start();
@@ -643,32 +645,24 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
   }
   const bool on = 4 * lane < d;
   const int nw = blockDim.x >> 5;
-  // the largest split maximum first, so that every split's weight is
-  // independent of the others and its loads can all be in flight at once
-  float mloc = -INFINITY;
-  for (int s = threadIdx.x; s < n_split; s += blockDim.x)
-    mloc = fmaxf(mloc, P.part_ml[((R.part_base + s) * pd.heads + h) * 2]);
-  mloc = warp_max(mloc);
-  if (lane == 0) red_m[warp] = mloc;
-  __syncthreads();
-  float M = -INFINITY;
-  for (int w = 0; w < nw; ++w) M = fmaxf(M, red_m[w]);
-  float l = 0.0f;
+  float m = -INFINITY, l = 0.0f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
 #pragma unroll 4
-    for (int s = warp; s < n_split; s += nw) {
-      const int64_t gs = R.part_base + s;
-      const float2 ml = *reinterpret_cast<const float2*>(P.part_ml + (gs * pd.heads + h) * 2);
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (on) v = *reinterpret_cast<const float4*>(P.part_o + gs * pd.HD + h * d + 4 * lane);
-      const float b = ml.x == -INFINITY ? 0.0f : exp2f(ml.x - M);  // an empty split weighs nothing
-      l = fmaf(ml.y, b, l);
-      acc.x = fmaf(v.x, b, acc.x);
-      acc.y = fmaf(v.y, b, acc.y);
-      acc.z = fmaf(v.z, b, acc.z);
-      acc.w = fmaf(v.w, b, acc.w);
-    }
+  for (int s = warp; s < n_split; s += nw) {
+    const int64_t gs = R.part_base + s;
+    const float2 ml = *reinterpret_cast<const float2*>(P.part_ml + (gs * pd.heads + h) * 2);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (on) v = *reinterpret_cast<const float4*>(P.part_o + gs * pd.HD + h * d + 4 * lane);
+    const bool empty = ml.x == -INFINITY;  // an empty split weighs nothing
+    const float mn = empty ? m : fmaxf(m, ml.x);
+    const float a = m == mn ? 1.0f : exp2f(m - mn);
+    const float b = empty ? 0.0f : exp2f(ml.x - mn);
+    l = fmaf(ml.y, b, l * a);
+    acc.x = fmaf(v.x, b, acc.x * a);
+    acc.y = fmaf(v.y, b, acc.y * a);
+    acc.z = fmaf(v.z, b, acc.z * a);
+    acc.w = fmaf(v.w, b, acc.w * a);
+    m = mn;
   }
   if (on) {
     red_o[warp][4 * lane] = acc.x;
@@ -676,13 +670,20 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const __gri
     red_o[warp][4 * lane + 2] = acc.z;
     red_o[warp][4 * lane + 3] = acc.w;
   }
-  if (lane == 0) red_l[warp] = l;
+  if (lane == 0) {
+    red_m[warp] = m;
+    red_l[warp] = l;
+  }
   __syncthreads();
   if (threadIdx.x < d) {
+    float M = -INFINITY;
+    for (int w = 0; w < nw; ++w) M = fmaxf(M, red_m[w]);
     float num = 0.0f, den = 0.0f;
     for (int w = 0; w < nw; ++w) {
-      num += red_o[w][threadIdx.x];
-      den += red_l[w];
+      if (red_m[w] == -INFINITY) continue;
+      const float f = exp2f(red_m[w] - M);
+      num = fmaf(red_o[w][threadIdx.x], f, num);
+      den = fmaf(red_l[w], f, den);
     }
     P.out[((int64_t)(P.row0 + i) * pd.heads + h) * d + threadIdx.x] = num / den;
   }
