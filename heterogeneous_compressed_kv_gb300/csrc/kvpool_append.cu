@@ -39,6 +39,9 @@ struct InTraits<KVPOOL_F32> {
     x[6] = __uint_as_float(r.b.z); x[7] = __uint_as_float(r.b.w);
   }
   __device__ static void load8(const uint8_t* p, float* x) { unpack(load(p), x); }
+  __device__ static void load8_shared(const uint8_t* p, float* x) {
+    unpack(Raw{*reinterpret_cast<const uint4*>(p), *reinterpret_cast<const uint4*>(p + 16)}, x);
+  }
 };
 template <>
 struct InTraits<KVPOOL_BF16> {
@@ -54,6 +57,7 @@ struct InTraits<KVPOOL_BF16> {
     }
   }
   __device__ static void load8(const uint8_t* p, float* x) { unpack(load(p), x); }
+  __device__ static void load8_shared(const uint8_t* p, float* x) { unpack(*reinterpret_cast<const uint4*>(p), x); }
 };
 
 // Store 8 fp32 values (already scaled for fp8) as cache codes at dst.
@@ -186,9 +190,107 @@ __device__ __forceinline__ void st8f(float* p, const float* x) {
   reinterpret_cast<float4*>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
 }  // tokens whose loads are issued together
 
+// ---------------------------------------------------------------------------
+// Staged token rows (long units, e.g. prefill chunks): the unit's input rows
+// -- this CTA's span of each K and V row and, for slice 0, each indexer row --
+// stream through a ring of kAppendStages shared-memory stages of
+// P.stage_tokens tokens, filled by 1-D bulk copies (one copy for all tokens of
+// a stage where the span is the whole row, else one per token, issued by the
+// lanes of warp 0).  token(t, x, y) then runs for every token in order with
+// the thread's values read from shared memory -- the same per-token work and
+// order as the direct loads, so every stored value is identical.  Returns
+// false (the same in every thread) if a wait ran out; the copies still in
+// flight are waited for (time-limited) first.
+// ---------------------------------------------------------------------------
+constexpr int kAppendStages = 4;
+constexpr int kAppendRingOffset = 128;  // the stages' barriers sit in front of the ring
+
+template <int IN, typename F>
+__device__ bool staged_tokens(const AppendParams& P, const AppendUnit& u, int layer, int slice, int HD, int XD,
+                              bool idx_thread, int half, int hv, int xv0, F&& token) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  constexpr int isz = InTraits<IN>::kBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring);
+  uint8_t* stages = ring + kAppendRingOffset;
+  const PoolDesc& pd = P.pool;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int cv0 = slice * blockDim.x * kVpt, cv1 = cv0 + blockDim.x * kVpt;  // this CTA's values of [K | V]
+  const int k_lo = min(cv0, HD), k_hi = min(cv1, HD);
+  const int v_lo = max(cv0, HD) - HD, v_hi = max(cv1, HD) - HD;
+  const int kb = (k_hi - k_lo) * isz, vb = (v_hi - v_lo) * isz;
+  const int xb = (slice == 0 && P.layers[layer].has_csa) ? XD * isz : 0;
+  const int TS = P.stage_tokens;
+  const int tok_bytes = kb + vb + xb;
+  const int64_t stage_bytes = (int64_t)TS * tok_bytes;
+  const int n_tok = u.t1 - u.t0;
+  const int n_st = (n_tok + TS - 1) / TS;
+  const int64_t row0 = (int64_t)layer * P.rows + u.in_row;
+  const uint8_t* kin = reinterpret_cast<const uint8_t*>(P.k) + row0 * HD * isz + (int64_t)k_lo * isz;
+  const uint8_t* vin = reinterpret_cast<const uint8_t*>(P.v) + row0 * HD * isz + (int64_t)v_lo * isz;
+  const uint8_t* xin = xb ? reinterpret_cast<const uint8_t*>(P.idx_k) + row0 * XD * isz : nullptr;
+  if (tid == 0) {
+    for (int s = 0; s < kAppendStages; ++s) mbar_init(&full[s], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  auto issue = [&](int st) {  // warp 0: stage st into slot st % kAppendStages
+    const int s = st % kAppendStages;
+    const int j0 = st * TS, nt = min(TS, n_tok - j0);
+    uint8_t* dst = stages + (int64_t)s * stage_bytes;
+    if (lane == 0) {
+      fence_proxy_async();  // the CTA's reads of the slot come before the copies that overwrite it
+      mbar_arrive_expect_tx(&full[s], (uint32_t)(nt * tok_bytes));
+    }
+    __syncwarp();
+    if (kb) {
+      if (kb == HD * isz) {
+        if (lane == 0) bulk_g2s(dst, kin + (int64_t)j0 * kb, (uint32_t)(nt * kb), &full[s]);
+      } else {
+        for (int j = lane; j < nt; j += 32) bulk_g2s(dst + j * kb, kin + (int64_t)(j0 + j) * HD * isz, kb, &full[s]);
+      }
+    }
+    if (vb) {
+      uint8_t* dv = dst + (int64_t)TS * kb;
+      if (vb == HD * isz) {
+        if (lane == 0) bulk_g2s(dv, vin + (int64_t)j0 * vb, (uint32_t)(nt * vb), &full[s]);
+      } else {
+        for (int j = lane; j < nt; j += 32) bulk_g2s(dv + j * vb, vin + (int64_t)(j0 + j) * HD * isz, vb, &full[s]);
+      }
+    }
+    if (xb && lane == 0) bulk_g2s(dst + (int64_t)TS * (kb + vb), xin + (int64_t)j0 * xb, (uint32_t)(nt * xb), &full[s]);
+  };
+  if (tid < 32)
+    for (int st = 0; st < n_st && st < kAppendStages; ++st) issue(st);
+  for (int st = 0; st < n_st; ++st) {
+    const int s = st % kAppendStages;
+    const bool got = mbar_wait(&full[s], (st / kAppendStages) & 1, pd);
+    if (__syncthreads_or(!got)) {  // drain the copies still in flight, then give up
+      if (tid == 0)
+        for (int k = st; k < n_st && k < st + kAppendStages; ++k)
+          mbar_wait(&full[k % kAppendStages], (k / kAppendStages) & 1, pd);
+      return false;
+    }
+    const uint8_t* src = stages + (int64_t)s * stage_bytes;
+    const int nt = min(TS, n_tok - st * TS);
+    for (int j = 0; j < nt; ++j) {
+      float x[kVpt], y[kVpt];
+      const uint8_t* px = half == 0 ? src + j * kb + (hv - k_lo) * isz
+                                    : src + (int64_t)TS * kb + j * vb + (hv - v_lo) * isz;
+      InTraits<IN>::load8_shared(px, x);
+      if (idx_thread) InTraits<IN>::load8_shared(src + (int64_t)TS * (kb + vb) + j * xb + xv0 * isz, y);
+      token(u.t0 + st * TS + j, x, y);
+    }
+    __syncthreads();  // every thread is done with slot s
+    if (tid < 32 && st + kAppendStages < n_st) issue(st + kAppendStages);
+  }
+  return true;
+}
+
 // PT: per-token indexer keys (the pool's idx_per_token), a separate
 // instantiation so the per-entry path keeps its registers
-template <int IN, int CACHE, bool PT>
+// STAGED: the unit's tokens arrive through staged_tokens (long units) instead
+// of direct loads of kTokGroup tokens at a time.
+template <int IN, int CACHE, bool PT, bool STAGED>
 __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ AppendParams P) {
   pdl_start();
   __shared__ float sh[3 * 16];
@@ -270,14 +372,11 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
 #pragma unroll
   for (int j = 0; j < kVpt; ++j) acc_c[j] = acc_h[j] = acc_x[j] = 0.0f;
   if (L.has_hca && u.t0 > 0) {
-#pragma unroll
     ld8f(acc_h_ptr, acc_h);
   }
   if (L.has_csa && (u.t0 % m) != 0) {
-#pragma unroll
     ld8f(acc_c_ptr, acc_c);
     if (idx_thread) {
-#pragma unroll
       ld8f(acc_x_ptr, acc_x);
     }
   }
@@ -291,85 +390,93 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   uint8_t* ring = pd.arena + L.ring + (int64_t)u.slot * L.ring_req_bytes;
   const int64_t seg_pos0 = (int64_t)u.seg * mp;
 
-  using Raw = typename InTraits<IN>::Raw;
-  for (int tb = u.t0; tb < u.t1; tb += kTokGroup) {
-    const int n = min(kTokGroup, u.t1 - tb);
-    Raw xr[kTokGroup], yr[kTokGroup];
+  // the per-token work (window, compressor chains, completed entries); x: this
+  // thread's kVpt input values of token t, y: its indexer values (idx threads)
+  auto token = [&](int t, const float* x, const float* y) {
+    if (L.has_hca) {
+      const float a = a_hca[t];
 #pragma unroll
-    for (int gi = 0; gi < kTokGroup; ++gi) {
-      if (gi < n) {
-        xr[gi] = InTraits<IN>::load(in_kv + (int64_t)(tb - u.t0 + gi) * HD * isz);
-        if (idx_thread) yr[gi] = InTraits<IN>::load(in_x + (int64_t)(tb - u.t0 + gi) * XD * isz);
-      }
+      for (int j = 0; j < kVpt; ++j) acc_h[j] = __fmaf_rn(a, x[j], acc_h[j]);
     }
+    if (L.has_csa) {
+      const float a = a_csa[t % m];
 #pragma unroll
-    for (int gi = 0; gi < kTokGroup; ++gi) {
-      if (gi >= n) break;
-      const int t = tb + gi;
-      float x[kVpt];
-      InTraits<IN>::unpack(xr[gi], x);
-      if (L.has_hca) {
-        const float a = a_hca[t];
-#pragma unroll
-        for (int j = 0; j < kVpt; ++j) acc_h[j] = __fmaf_rn(a, x[j], acc_h[j]);
-      }
-      if (L.has_csa) {
-        const float a = a_csa[t % m];
-#pragma unroll
-        for (int j = 0; j < kVpt; ++j) acc_c[j] = __fmaf_rn(a, x[j], acc_c[j]);
-        if constexpr (PT) {
-          // the token's own indexer key, at key t % CB of run t / CB; the
-          // indexer threads are the first XD / 8 lanes of warp 0
-          if (slice == 0 && tid < 32) {
-            float y[kVpt];
-            if (idx_thread) InTraits<IN>::unpack(yr[gi], y);
-            float s = 1.0f;
-            uint8_t* run = blk_idx + (int64_t)(t / pd.csa_per_block) * L.idx_run;
-            const int key = t % pd.csa_per_block;
-            if (idx_scaled) {
-              float a = idx_thread ? amax8(y) : 0.0f;
-#pragma unroll
-              for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-              const uint16_t sb = idx_fp4 ? fp4_scale_bits(a) : fp8_scale_bits(a);
-              s = bf16_bits_to_f32(sb);
-              if (idx_thread && xv0 == 0) *reinterpret_cast<uint16_t*>(run + L.idx_scale_off + 2 * key) = sb;
-            }
-            if (idx_thread) {
-              if (idx_fp4) write_idx_fp4(run, pd, key, xv0, y, s);
-              else write_idx<CACHE>(run, pd, key, xv0, y, s);
-            }
-          }
-        } else if (idx_thread) {
-          float y[kVpt];
-          InTraits<IN>::unpack(yr[gi], y);
-          const float b = a_idx[t % m];
-#pragma unroll
-          for (int j = 0; j < kVpt; ++j) acc_x[j] = __fmaf_rn(b, y[j], acc_x[j]);
-        }
-        if ((t + 1) % m == 0) {  // a CSA group completes: entry slot (t+1)/m - 1 of the block
-          const int slot = (t + 1) / m - 1;
-          write_entry<CACHE>(blk_csa + (int64_t)slot * pd.entry_bytes, pd, v0, half, hv, acc_c, sh);
+      for (int j = 0; j < kVpt; ++j) acc_c[j] = __fmaf_rn(a, x[j], acc_c[j]);
+      if constexpr (PT) {
+        // the token's own indexer key, at key t % CB of run t / CB; the
+        // indexer threads are the first XD / 8 lanes of warp 0
+        if (slice == 0 && tid < 32) {
           float s = 1.0f;
-          if (idx_scaled && !PT) {  // uniform over the CTA: block-wide amax of the indexer entry
-            const float3 r = block_max3(0.f, 0.f, idx_thread ? amax8(acc_x) : 0.f, sh);
-            const uint16_t sb = idx_fp4 ? fp4_scale_bits(r.z) : fp8_scale_bits(r.z);
-            s = bf16_bits_to_f32(sb);
-            if (idx_thread && xv0 == 0) *reinterpret_cast<uint16_t*>(blk_idx + L.idx_scale_off + 2 * slot) = sb;
-          }
-          if (idx_thread && !PT) {
-            if (idx_fp4) write_idx_fp4(blk_idx, pd, slot, xv0, acc_x, s);
-            else write_idx<CACHE>(blk_idx, pd, slot, xv0, acc_x, s);
-          }
+          uint8_t* run = blk_idx + (int64_t)(t / pd.csa_per_block) * L.idx_run;
+          const int key = t % pd.csa_per_block;
+          if (idx_scaled) {
+            float a = idx_thread ? amax8(y) : 0.0f;
 #pragma unroll
-          for (int j = 0; j < kVpt; ++j) acc_c[j] = acc_x[j] = 0.0f;
+            for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+            const uint16_t sb = idx_fp4 ? fp4_scale_bits(a) : fp8_scale_bits(a);
+            s = bf16_bits_to_f32(sb);
+            if (idx_thread && xv0 == 0) *reinterpret_cast<uint16_t*>(run + L.idx_scale_off + 2 * key) = sb;
+          }
+          if (idx_thread) {
+            if (idx_fp4) write_idx_fp4(run, pd, key, xv0, y, s);
+            else write_idx<CACHE>(run, pd, key, xv0, y, s);
+          }
         }
+      } else if (idx_thread) {
+        const float b = a_idx[t % m];
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) acc_x[j] = __fmaf_rn(b, y[j], acc_x[j]);
       }
-      if (t >= u.ring_from) {  // the token enters the SWA window
-        const int64_t pos = seg_pos0 + t;
-        write_entry<CACHE>(ring + (pos % pd.n_win) * pd.entry_bytes, pd, v0, half, hv, x, sh);
+      if ((t + 1) % m == 0) {  // a CSA group completes: entry slot (t+1)/m - 1 of the block
+        const int slot = (t + 1) / m - 1;
+        write_entry<CACHE>(blk_csa + (int64_t)slot * pd.entry_bytes, pd, v0, half, hv, acc_c, sh);
+        float s = 1.0f;
+        if (idx_scaled && !PT) {  // uniform over the CTA: block-wide amax of the indexer entry
+          const float3 r = block_max3(0.f, 0.f, idx_thread ? amax8(acc_x) : 0.f, sh);
+          const uint16_t sb = idx_fp4 ? fp4_scale_bits(r.z) : fp8_scale_bits(r.z);
+          s = bf16_bits_to_f32(sb);
+          if (idx_thread && xv0 == 0) *reinterpret_cast<uint16_t*>(blk_idx + L.idx_scale_off + 2 * slot) = sb;
+        }
+        if (idx_thread && !PT) {
+          if (idx_fp4) write_idx_fp4(blk_idx, pd, slot, xv0, acc_x, s);
+          else write_idx<CACHE>(blk_idx, pd, slot, xv0, acc_x, s);
+        }
+#pragma unroll
+        for (int j = 0; j < kVpt; ++j) acc_c[j] = acc_x[j] = 0.0f;
       }
     }
+    if (t >= u.ring_from) {  // the token enters the SWA window
+      const int64_t pos = seg_pos0 + t;
+      write_entry<CACHE>(ring + (pos % pd.n_win) * pd.entry_bytes, pd, v0, half, hv, x, sh);
+    }
+  };
+
+  bool ok = true;
+  if constexpr (!STAGED) {
+    using Raw = typename InTraits<IN>::Raw;
+    for (int tb = u.t0; tb < u.t1; tb += kTokGroup) {
+      const int n = min(kTokGroup, u.t1 - tb);
+      Raw xr[kTokGroup], yr[kTokGroup];
+#pragma unroll
+      for (int gi = 0; gi < kTokGroup; ++gi) {
+        if (gi < n) {
+          xr[gi] = InTraits<IN>::load(in_kv + (int64_t)(tb - u.t0 + gi) * HD * isz);
+          if (idx_thread) yr[gi] = InTraits<IN>::load(in_x + (int64_t)(tb - u.t0 + gi) * XD * isz);
+        }
+      }
+#pragma unroll
+      for (int gi = 0; gi < kTokGroup; ++gi) {
+        if (gi >= n) break;
+        float x[kVpt], y[kVpt];
+        InTraits<IN>::unpack(xr[gi], x);
+        if (idx_thread) InTraits<IN>::unpack(yr[gi], y);
+        token(tb + gi, x, y);
+      }
+    }
+  } else {
+    ok = staged_tokens<IN>(P, u, layer, slice, HD, XD, idx_thread, half, hv, xv0, token);
   }
+  if (!ok) return;  // a wait ran out: the error word says so, nothing more is written
 
   if (L.has_hca && u.t1 == mp) {  // the HCA group completes with the block
     if (u.block_id < 0) {
@@ -379,14 +486,11 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
     }
   }
   if (L.has_hca && u.t1 < mp) {
-#pragma unroll
     st8f(acc_h_ptr, acc_h);
   }
   if (L.has_csa && (u.t1 % m) != 0) {
-#pragma unroll
     st8f(acc_c_ptr, acc_c);
     if (idx_thread) {
-#pragma unroll
       st8f(acc_x_ptr, acc_x);
     }
   }
@@ -432,6 +536,8 @@ __global__ void __launch_bounds__(512) share_kernel(const __grid_constant__ Shar
 
 int append_threads(const PoolDesc& pd, int n_slices) { return 2 * pd.HD / kVpt / n_slices; }
 
+constexpr int kAppendStageBudget = 48 * 1024;  // bytes of one stage of the staged path
+
 }  // namespace
 
 // CTAs that split one unit's 2*H*d values (8 per thread): one CTA up to 256
@@ -443,40 +549,68 @@ int append_slices(const PoolDesc& pd) {
   return chunks / 256;
 }
 
+// Slices of the staged path: the same as the direct path, so a CTA's span of
+// a K or V row is the whole row (one bulk copy moves all tokens of a stage);
+// finer slices of 64 threads measured slower (1 KB copies, 4 warps per SM).
+int append_slices_staged(const PoolDesc& pd) { return append_slices(pd); }
+
+// Bytes one token takes in a stage (the widest slice: slice 0 also stages the
+// indexer row), tokens per stage, and the dynamic shared memory of the ring.
+static int append_token_bytes(const PoolDesc& pd, int n_slices) {
+  return (2 * pd.HD / n_slices) * pd.isz + pd.XD * pd.isz;
+}
+int append_stage_tokens(const PoolDesc& pd, int n_slices) {
+  const int tb = append_token_bytes(pd, n_slices);
+  int ts = 32;
+  while (ts > 1 && ts * tb > kAppendStageBudget) ts /= 2;
+  return ts;
+}
+static size_t append_staged_smem(const PoolDesc& pd, int n_slices, int ts) {
+  return (size_t)kAppendRingOffset + (size_t)kAppendStages * ts * append_token_bytes(pd, n_slices);
+}
+
 int launch_append(const AppendParams& p, int n_layers, void* stream, int* n_kernels) {
   if (p.n_units <= 0) return 0;
-  if (p.n_slices != append_slices(p.pool)) return (int)cudaErrorInvalidValue;
+  const int want = p.staged ? append_slices_staged(p.pool) : append_slices(p.pool);
+  if (p.n_slices != want) return (int)cudaErrorInvalidValue;
+  if (p.staged && (p.stage_tokens < 1 || p.stage_tokens > 32 || p.stage_tokens != append_stage_tokens(p.pool, p.n_slices)))
+    return (int)cudaErrorInvalidValue;
   const int threads = append_threads(p.pool, p.n_slices);
   if (p.copy_slices < 0) return (int)cudaErrorInvalidValue;
   dim3 grid(p.n_units, p.n_slices + p.copy_slices, n_layers);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t smem = p.staged ? append_staged_smem(p.pool, p.n_slices, p.stage_tokens) : 0;
   const int key = p.pool.in_dtype * 3 + p.pool.cache_dtype;
-  auto go = [&](auto entry_kernel, auto token_kernel) {
-    launch_kernel(true, p.pool.idx_per_token ? token_kernel : entry_kernel, grid, dim3(threads), 0, s, p);
+  // the four instantiations of one dtype pair: (per-entry | per-token keys) x (direct | staged)
+  auto go = [&](auto k_entry, auto k_token, auto k_entry_st, auto k_token_st) {
+    if (p.staged) {
+      // the ring needs more than the default dynamic shared memory; staged
+      // launches move whole prefill chunks, so the attribute is simply set
+      // before each one
+      auto k = p.pool.idx_per_token ? k_token_st : k_entry_st;
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      return launch_kernel(true, k, grid, dim3(threads), smem, s, p);
+    } else {
+      return launch_kernel(true, p.pool.idx_per_token ? k_token : k_entry, grid, dim3(threads), 0, s, p);
+    }
   };
+  cudaError_t e = cudaSuccess;
+#define KVP_APPEND_KERNELS(I, C) \
+  append_kernel<I, C, false, false>, append_kernel<I, C, true, false>, append_kernel<I, C, false, true>, \
+      append_kernel<I, C, true, true>
   switch (key) {
-    case KVPOOL_F32 * 3 + KVPOOL_F32:
-      go(append_kernel<KVPOOL_F32, KVPOOL_F32, false>, append_kernel<KVPOOL_F32, KVPOOL_F32, true>);
-      break;
-    case KVPOOL_F32 * 3 + KVPOOL_BF16:
-      go(append_kernel<KVPOOL_F32, KVPOOL_BF16, false>, append_kernel<KVPOOL_F32, KVPOOL_BF16, true>);
-      break;
-    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3:
-      go(append_kernel<KVPOOL_F32, KVPOOL_FP8_E4M3, false>, append_kernel<KVPOOL_F32, KVPOOL_FP8_E4M3, true>);
-      break;
-    case KVPOOL_BF16 * 3 + KVPOOL_F32:
-      go(append_kernel<KVPOOL_BF16, KVPOOL_F32, false>, append_kernel<KVPOOL_BF16, KVPOOL_F32, true>);
-      break;
-    case KVPOOL_BF16 * 3 + KVPOOL_BF16:
-      go(append_kernel<KVPOOL_BF16, KVPOOL_BF16, false>, append_kernel<KVPOOL_BF16, KVPOOL_BF16, true>);
-      break;
-    case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3:
-      go(append_kernel<KVPOOL_BF16, KVPOOL_FP8_E4M3, false>, append_kernel<KVPOOL_BF16, KVPOOL_FP8_E4M3, true>);
-      break;
+    case KVPOOL_F32 * 3 + KVPOOL_F32: e = go(KVP_APPEND_KERNELS(KVPOOL_F32, KVPOOL_F32)); break;
+    case KVPOOL_F32 * 3 + KVPOOL_BF16: e = go(KVP_APPEND_KERNELS(KVPOOL_F32, KVPOOL_BF16)); break;
+    case KVPOOL_F32 * 3 + KVPOOL_FP8_E4M3: e = go(KVP_APPEND_KERNELS(KVPOOL_F32, KVPOOL_FP8_E4M3)); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_F32: e = go(KVP_APPEND_KERNELS(KVPOOL_BF16, KVPOOL_F32)); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_BF16: e = go(KVP_APPEND_KERNELS(KVPOOL_BF16, KVPOOL_BF16)); break;
+    case KVPOOL_BF16 * 3 + KVPOOL_FP8_E4M3: e = go(KVP_APPEND_KERNELS(KVPOOL_BF16, KVPOOL_FP8_E4M3)); break;
     default: return (int)cudaErrorInvalidValue;
   }
+#undef KVP_APPEND_KERNELS
   *n_kernels += 1;
-  return (int)cudaGetLastError();
+  return (int)(e != cudaSuccess ? e : cudaGetLastError());
 }
 
 int launch_share(const ShareParams& p, int n_layers, void* stream, int* n_kernels) {

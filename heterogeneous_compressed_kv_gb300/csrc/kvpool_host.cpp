@@ -23,7 +23,6 @@
 #include "kvpool_internal.h"
 
 namespace kvp {
-int append_slices(const PoolDesc& pd);
 int attend_max_split_len();
 }  // namespace kvp
 
@@ -42,6 +41,8 @@ constexpr int kAttendCtasPerSm = 3;
 constexpr int kPart0CtasPerSm = 2;
 constexpr int kScoreCtasPerSm = 1;      // CTAs of the score kernel (1 per SM, one wave)
 constexpr int kSealCopySlices = 8;      // CTAs per sealing unit that copy its staged entries
+constexpr int kStagedMinTokens = 16;    // an append call with a unit this long ...
+constexpr int kStagedMaxCtasPerSm = 1;  // ... and at most this many CTAs per SM takes the staged path
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int value_bytes(int dtype) { return dtype == KVPOOL_F32 ? 4 : dtype == KVPOOL_BF16 ? 2 : 1; }
@@ -101,6 +102,7 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
   const int HD = c->heads * c->head_dim, XD = c->idx_heads * c->idx_dim;
   if (HD % 256 != 0 || HD > 4096) return "heads * head_dim must be a multiple of 256, at most 4096";
   if (XD % 16 != 0 || XD > 8 * 256) return "idx_heads * idx_dim must be a multiple of 16, at most 2048";
+  if (XD > 2 * HD) return "idx_heads * idx_dim must be at most 2 * heads * head_dim";
   if (c->idx_fp4 != 0 && c->idx_fp4 != 1) return "idx_fp4 must be 0 or 1";
   if (c->idx_fp4 && XD % 32 != 0) return "FP4 indexer entries need idx_heads * idx_dim to be a multiple of 32";
   if (c->idx_per_token != 0 && c->idx_per_token != 1) return "idx_per_token must be 0 or 1";
@@ -1087,7 +1089,17 @@ int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_
     ap->v = d_v;
     ap->idx_k = d_idx_k;
     ap->rows = T;
-    ap->n_slices = append_slices(p->lay.pd);
+    // units of many tokens (prefill chunks) in a launch too small to fill the
+    // GPU stream their rows through shared memory (several stages in flight per
+    // CTA); otherwise every thread loads its tokens directly, kTokGroup at a
+    // time (enough in flight once there are a few CTAs per SM)
+    int64_t longest = 0, ctas = 0;
+    for (const auto* list : {&phase1, &phase2})
+      for (const AppendUnit& u : *list) longest = std::max<int64_t>(longest, u.t1 - u.t0);
+    ctas = (int64_t)(phase1.size() + phase2.size()) * append_slices(p->lay.pd) * p->cfg.n_layers;
+    ap->staged = (longest >= kStagedMinTokens && ctas <= (int64_t)kStagedMaxCtasPerSm * p->n_sms) ? 1 : 0;
+    ap->n_slices = ap->staged ? append_slices_staged(p->lay.pd) : append_slices(p->lay.pd);
+    ap->stage_tokens = ap->staged ? append_stage_tokens(p->lay.pd, ap->n_slices) : 0;
     ap->epoch = p->epoch;
     // algorithmic bytes: inputs read + window tokens and new entries written
     const PoolDesc& pd = p->lay.pd;

@@ -89,6 +89,8 @@ struct AppendParams {
   int32_t n_slices;  // CTAs that split one unit's 2*H*d values
   int32_t copy_slices;  // further CTAs per unit that copy a sealing block's staged entries (0: none seal)
   uint32_t epoch;    // HiSparse activity stamp of the blocks sealed here
+  int32_t staged;        // tokens arrive through shared-memory stages (long units)
+  int32_t stage_tokens;  // tokens per stage of the staged path
   AppendUnit units[kMaxAppendUnits];
 };
 
@@ -194,6 +196,9 @@ struct AttendParams {
 // ---- launchers (implemented in the .cu files; return cudaError_t as int) --
 // Each launcher adds the number of kernels it launched to *n_kernels.
 int launch_append(const AppendParams& p, int n_layers, void* stream, int* n_kernels);
+int append_slices(const PoolDesc& pd);         // CTAs per unit, direct token loads
+int append_slices_staged(const PoolDesc& pd);  // CTAs per unit, staged token rows
+int append_stage_tokens(const PoolDesc& pd, int n_slices);
 int launch_share(const ShareParams& p, int n_layers, void* stream, int* n_kernels);
 int launch_image(const ImageParams& p, void* stream, int* n_kernels);
 int launch_wait_selftest(const PoolDesc& pd, void* stream);
