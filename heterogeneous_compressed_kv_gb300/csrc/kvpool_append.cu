@@ -390,16 +390,24 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   uint8_t* ring = pd.arena + L.ring + (int64_t)u.slot * L.ring_req_bytes;
   const int64_t seg_pos0 = (int64_t)u.seg * mp;
 
+  // The tokens come in order from u.t0, so the per-token positions are
+  // counters rather than divisions: tm = t % m, tq = t / m, and for per-token
+  // keys tk = t % CB, tr = t / CB.  The window is a whole number of blocks, so
+  // a segment's tokens never wrap the ring: slot = (segment start mod n_win) + t.
+  int tm = u.t0 % m, tq = u.t0 / m;
+  int tk = u.t0 % pd.csa_per_block, tr = u.t0 / pd.csa_per_block;
+  const int64_t ring_base = seg_pos0 % pd.n_win;
+
   // the per-token work (window, compressor chains, completed entries); x: this
   // thread's kVpt input values of token t, y: its indexer values (idx threads)
   auto token = [&](int t, const float* x, const float* y) {
     if (L.has_hca) {
-      const float a = a_hca[t];
+      const float a = __ldg(a_hca + t);
 #pragma unroll
       for (int j = 0; j < kVpt; ++j) acc_h[j] = __fmaf_rn(a, x[j], acc_h[j]);
     }
     if (L.has_csa) {
-      const float a = a_csa[t % m];
+      const float a = __ldg(a_csa + tm);
 #pragma unroll
       for (int j = 0; j < kVpt; ++j) acc_c[j] = __fmaf_rn(a, x[j], acc_c[j]);
       if constexpr (PT) {
@@ -407,8 +415,8 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
         // indexer threads are the first XD / 8 lanes of warp 0
         if (slice == 0 && tid < 32) {
           float s = 1.0f;
-          uint8_t* run = blk_idx + (int64_t)(t / pd.csa_per_block) * L.idx_run;
-          const int key = t % pd.csa_per_block;
+          uint8_t* run = blk_idx + (int64_t)tr * L.idx_run;
+          const int key = tk;
           if (idx_scaled) {
             float a = idx_thread ? amax8(y) : 0.0f;
 #pragma unroll
@@ -423,12 +431,12 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
           }
         }
       } else if (idx_thread) {
-        const float b = a_idx[t % m];
+        const float b = __ldg(a_idx + tm);
 #pragma unroll
         for (int j = 0; j < kVpt; ++j) acc_x[j] = __fmaf_rn(b, y[j], acc_x[j]);
       }
-      if ((t + 1) % m == 0) {  // a CSA group completes: entry slot (t+1)/m - 1 of the block
-        const int slot = (t + 1) / m - 1;
+      if (tm == m - 1) {  // a CSA group completes: entry slot (t+1)/m - 1 = t / m of the block
+        const int slot = tq;
         write_entry<CACHE>(blk_csa + (int64_t)slot * pd.entry_bytes, pd, v0, half, hv, acc_c, sh);
         float s = 1.0f;
         if (idx_scaled && !PT) {  // uniform over the CTA: block-wide amax of the indexer entry
@@ -445,9 +453,15 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
         for (int j = 0; j < kVpt; ++j) acc_c[j] = acc_x[j] = 0.0f;
       }
     }
-    if (t >= u.ring_from) {  // the token enters the SWA window
-      const int64_t pos = seg_pos0 + t;
-      write_entry<CACHE>(ring + (pos % pd.n_win) * pd.entry_bytes, pd, v0, half, hv, x, sh);
+    if (t >= u.ring_from)  // the token enters the SWA window
+      write_entry<CACHE>(ring + (ring_base + t) * pd.entry_bytes, pd, v0, half, hv, x, sh);
+    if (++tm == m) {
+      tm = 0;
+      ++tq;
+    }
+    if (++tk == pd.csa_per_block) {
+      tk = 0;
+      ++tr;
     }
   };
 
