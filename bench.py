@@ -167,6 +167,9 @@ def run_reference(args):
     if rank != 0:
         return
     w = workload(args.config, args.idx_fp4, args.idx_per_token)
+    if args.config in ("chunked_prefill", "mixed_serving"):
+        run_reference_protocol(args, w)
+        return
     n = oracle_workers(w)
     pool, res = start_oracle(args.config, n, args.steps, args.warmup, args.idx_fp4, args.idx_per_token)
     out = res.get()
@@ -181,6 +184,38 @@ def run_reference(args):
                 cpu_baseline=dict(value=value, unit="tokens/s", cores=n, kind="oracle",
                                   sample=f"{n} of {w['n_requests']} requests (one process each) at their full "
                                          f"context; setup (oracle prefill) {max(o[1] for o in out):.0f} s untimed"),
+                e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line))
+
+
+def run_reference_protocol(args, w):
+    """--impl reference for chunked prefill (the whole protocol per step, one
+    process; at most 3 timed steps, each ~1-2 s of oracle work) and mixed
+    serving (decode steps of all 4 layers for sampled requests, one process
+    each)."""
+    ctx = mp.get_context("spawn")
+    if args.config == "chunked_prefill":
+        steps = min(args.steps, 3)
+        with ctx.Pool(1) as pool:
+            t = pool.map(_c3_oracle_worker, [(steps, min(args.warmup, 1))])[0]
+        n, tokens = 1, (w["shared"] + w["n_requests"] * (w["tokens"] - w["shared"])) * steps
+        metric, sample = METRIC + " (chunked prefill: appended tokens/s)", \
+            f"{steps} runs of the whole protocol in one process; inputs drawn untimed"
+    else:
+        n = max(1, min(8, (os.cpu_count() or 2) - 1))
+        steps = min(args.steps, 3)
+        with ctx.Pool(n) as pool:
+            t = max(pool.map(_c5_oracle_worker, [(i, steps) for i in range(n)]))
+        tokens = n * steps
+        metric, sample = METRIC + " (mixed serving: decode tokens/s)", \
+            f"{n} of {w['n_requests']} requests at their initial lengths, {steps} decode steps of all 4 layers each, " \
+            f"one process per request; prefill untimed"
+    value = tokens / t
+    line = dict(impl="reference", metric=metric, value=value, unit="tokens/s", n_gpus=args.gpus, steps=steps,
+                warmup=args.warmup, ms_per_step=1e3 * t / steps, higher_is_better=True, scaling="weak",
+                vs_baseline=None, dtype="f64 attention / f32 compressor and scores", data="synthetic",
+                config=config_block(w, args),
+                cpu_baseline=dict(value=value, unit="tokens/s", cores=n, kind="oracle", sample=sample),
                 e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line))
 

@@ -271,3 +271,35 @@ def test_bounded_wait_is_reported_and_the_pool_stays_usable():
     assert g.pool.check_device() == 0  # read and cleared
     append_both(o, g, [r], [r], [200], [1])
     attend_both(o, g, 0, [r], [r], 0, 64)
+
+
+def test_profiling_events_and_count_only_agree():
+    """The two profiling modes account the same launches: two pools with the
+    same history run the same decode step, one recording events and one
+    counting without events; launch counts and algorithmic bytes agree for
+    every kernel kind, the count-only mode measures no time and records no
+    timeline, and the outputs are the same bits."""
+    w = dict(W.DECODE_BATCH, seed=27)
+    cases = [GpuCase(w, 3, 32, 8, 3, 128) for _ in range(2)]
+    totals, outs = [], []
+    for g, (kinds, count) in zip(cases, ((None, False), ([], True))):
+        slots = [g.pool.alloc_request() for _ in range(3)]
+        g.append(slots, slots, [0, 0, 0], [700, 300, 1100])
+        g.pool.profile_enable(True, kinds=kinds, count=count)
+        g.append(slots, slots, [700, 300, 1100], [1, 1, 1])
+        out, tk = g.attend(0, slots, slots, 0, 128)
+        assert g.pool.check_device() == 0
+        totals.append([g.pool.profile_read(k) for k in range(len(K.KERNEL_NAMES))])
+        if count:
+            assert g.pool.profile_timeline() == []
+        g.pool.profile_enable(False)
+        outs.append((out.cpu().numpy(), tk.cpu().numpy()))
+    ev, ct = totals
+    for k, name in enumerate(K.KERNEL_NAMES):
+        assert ev[k][1:] == ct[k][1:], (name, ev[k], ct[k])
+        assert ct[k][0] == 0.0, name
+    for name in ("append", "score", "select", "attend", "combine"):
+        e = ev[K.KERNEL_NAMES.index(name)]
+        assert e[0] > 0 and e[1] > 0 and e[2] > 0, (name, e)
+    assert np.array_equal(outs[0][1], outs[1][1])
+    assert np.array_equal(outs[0][0].view(np.uint8), outs[1][0].view(np.uint8))
