@@ -300,6 +300,8 @@ def test_profiling_events_and_count_only_agree():
         assert ct[k][0] == 0.0, name
     for name in ("append", "score", "select", "attend", "combine"):
         e = ev[K.KERNEL_NAMES.index(name)]
-        assert e[0] > 0 and e[1] > 0 and e[2] > 0, (name, e)
+        assert e[0] > 0 and e[1] > 0, (name, e)
+        # the select's keys are scratch that stays in L2: no algorithmic bytes
+        assert (e[2] == 0) == (name == "select"), (name, e)
     assert np.array_equal(outs[0][1], outs[1][1])
     assert np.array_equal(outs[0][0].view(np.uint8), outs[1][0].view(np.uint8))
