@@ -218,7 +218,7 @@ __device__ bool staged_tokens(const AppendParams& P, const AppendUnit& u, int la
   const int k_lo = min(cv0, HD), k_hi = min(cv1, HD);
   const int v_lo = max(cv0, HD) - HD, v_hi = max(cv1, HD) - HD;
   const int kb = (k_hi - k_lo) * isz, vb = (v_hi - v_lo) * isz;
-  const int xb = (slice == 0 && P.layers[layer].has_csa) ? XD * isz : 0;
+  const int xb = (slice == 0 && P.layers[layer].has_csa && u.role != kUnitHca) ? XD * isz : 0;
   const int TS = P.stage_tokens;
   const int tok_bytes = kb + vb + xb;
   const int64_t stage_bytes = (int64_t)TS * tok_bytes;
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   // copy_slices CTAs of the unit (this call's own entries go to the block
   // directly).
   if (slice >= P.n_slices) {
-    if (u.block_id < 0 || !L.has_csa || u.t0 < (PT ? 1 : m)) return;
+    if (u.role == kUnitCsa || u.block_id < 0 || !L.has_csa || u.t0 < (PT ? 1 : m)) return;
     const int cs = slice - P.n_slices, ncs = P.copy_slices;
     const int n_copy = u.t0 / m;
     const int CB = pd.csa_per_block;
@@ -348,7 +348,11 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   const int half = v0 >= HD ? 1 : 0;
   const int hv = v0 - half * HD;
   const int h = hv / pd.head_dim;
-  const bool idx_thread = L.has_csa && slice == 0 && tid * kVpt < XD;
+  // the parts of the unit this CTA does (one layer's kinds decide the rest)
+  const bool do_hca = L.has_hca && u.role != kUnitCsa;
+  const bool do_csa = L.has_csa && u.role != kUnitHca;
+  const bool do_win = u.role != kUnitHca;
+  const bool idx_thread = do_csa && slice == 0 && tid * kVpt < XD;
   const bool idx_fp4 = pd.idx_dtype == KVPOOL_FP4_E2M1;
   const bool idx_scaled = idx_fp4 || pd.idx_dtype == KVPOOL_FP8_E4M3;
   const int xv0 = tid * kVpt;
@@ -371,10 +375,10 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   float acc_c[kVpt], acc_h[kVpt], acc_x[kVpt];
 #pragma unroll
   for (int j = 0; j < kVpt; ++j) acc_c[j] = acc_h[j] = acc_x[j] = 0.0f;
-  if (L.has_hca && u.t0 > 0) {
+  if (do_hca && u.t0 > 0) {
     ld8f(acc_h_ptr, acc_h);
   }
-  if (L.has_csa && (u.t0 % m) != 0) {
+  if (do_csa && (u.t0 % m) != 0) {
     ld8f(acc_c_ptr, acc_c);
     if (idx_thread) {
       ld8f(acc_x_ptr, acc_x);
@@ -401,12 +405,12 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   // the per-token work (window, compressor chains, completed entries); x: this
   // thread's kVpt input values of token t, y: its indexer values (idx threads)
   auto token = [&](int t, const float* x, const float* y) {
-    if (L.has_hca) {
+    if (do_hca) {
       const float a = __ldg(a_hca + t);
 #pragma unroll
       for (int j = 0; j < kVpt; ++j) acc_h[j] = __fmaf_rn(a, x[j], acc_h[j]);
     }
-    if (L.has_csa) {
+    if (do_csa) {
       const float a = __ldg(a_csa + tm);
 #pragma unroll
       for (int j = 0; j < kVpt; ++j) acc_c[j] = __fmaf_rn(a, x[j], acc_c[j]);
@@ -453,7 +457,7 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
         for (int j = 0; j < kVpt; ++j) acc_c[j] = acc_x[j] = 0.0f;
       }
     }
-    if (t >= u.ring_from)  // the token enters the SWA window
+    if (do_win && t >= u.ring_from)  // the token enters the SWA window
       write_entry<CACHE>(ring + (ring_base + t) * pd.entry_bytes, pd, v0, half, hv, x, sh);
     if (++tm == m) {
       tm = 0;
@@ -492,17 +496,17 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   }
   if (!ok) return;  // a wait ran out: the error word says so, nothing more is written
 
-  if (L.has_hca && u.t1 == mp) {  // the HCA group completes with the block
+  if (do_hca && u.t1 == mp) {  // the HCA group completes with the block
     if (u.block_id < 0) {
       if (tid == 0) flag_error(pd, kErrBadBlock);
     } else {
       write_entry<CACHE>(blk_hca, pd, v0, half, hv, acc_h, sh);
     }
   }
-  if (L.has_hca && u.t1 < mp) {
+  if (do_hca && u.t1 < mp) {
     st8f(acc_h_ptr, acc_h);
   }
-  if (L.has_csa && (u.t1 % m) != 0) {
+  if (do_csa && (u.t1 % m) != 0) {
     st8f(acc_c_ptr, acc_c);
     if (idx_thread) {
       st8f(acc_x_ptr, acc_x);
@@ -587,7 +591,7 @@ int launch_append(const AppendParams& p, int n_layers, void* stream, int* n_kern
   if (p.n_units <= 0) return 0;
   const int want = p.staged ? append_slices_staged(p.pool) : append_slices(p.pool);
   if (p.n_slices != want) return (int)cudaErrorInvalidValue;
-  if (p.staged && (p.stage_tokens < 1 || p.stage_tokens > 32 || p.stage_tokens != append_stage_tokens(p.pool, p.n_slices)))
+  if (p.staged && (p.stage_tokens < 1 || p.stage_tokens != append_stage_tokens(p.pool, p.n_slices)))
     return (int)cudaErrorInvalidValue;
   const int threads = append_threads(p.pool, p.n_slices);
   if (p.copy_slices < 0) return (int)cudaErrorInvalidValue;

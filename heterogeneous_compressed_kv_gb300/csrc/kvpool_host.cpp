@@ -43,6 +43,8 @@ constexpr int kScoreCtasPerSm = 1;      // CTAs of the score kernel (1 per SM, o
 constexpr int kSealCopySlices = 8;      // CTAs per sealing unit that copy its staged entries
 constexpr int kStagedMinTokens = 16;    // an append call with a unit this long ...
 constexpr int kStagedMaxCtasPerSm = 1;  // ... and at most this many CTAs per SM takes the staged path
+constexpr int kSplitMinTokens = 64;     // a unit this long in a launch that leaves SMs idle ...
+constexpr int kMaxCsaParts = 4;         // ... spreads its CSA groups over up to this many CTAs
 
 int64_t round_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 int value_bytes(int dtype) { return dtype == KVPOOL_F32 ? 4 : dtype == KVPOOL_BF16 ? 2 : 1; }
@@ -1082,6 +1084,48 @@ int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_
       }
       row += h_n_new[i];
     }
+    // a launch of few long units (a prefill chunk of one request) would leave
+    // most SMs idle while each CTA walks its unit's tokens in order: such a
+    // unit becomes one CTA for its HCA chain over all its tokens and `parts`
+    // CTAs for its CSA / indexer groups and window tokens (ranges of whole CSA
+    // groups; only the first may start and only the last may end inside a
+    // group, so every State accumulator has one reader and one writer)
+    {
+      const int m = p->cfg.m;
+      const int64_t base = (int64_t)(phase1.size() + phase2.size()) * append_slices(p->lay.pd) * p->cfg.n_layers;
+      // (two CTAs per SM with half-size stages, or a split into the HCA chain
+      // and one CSA part, measured slower: the CTAs that share an SM take
+      // longer than the unsplit unit)
+      const int parts = base > 0 ? (int)std::min<int64_t>(kMaxCsaParts, p->n_sms / base - 1) : 0;
+      if (parts >= 2) {
+        for (auto* list : {&phase1, &phase2}) {
+          std::vector<AppendUnit> out;
+          for (const AppendUnit& u : *list) {
+            const int len = u.t1 - u.t0;
+            if (len < kSplitMinTokens || ((u.t0 % m) != 0 && (u.t1 % m) != 0)) {
+              out.push_back(u);
+              continue;
+            }
+            AppendUnit hu = u;
+            hu.role = kUnitHca;
+            out.push_back(hu);
+            int a = u.t0;
+            for (int k = 1; k <= parts && a < u.t1; ++k) {
+              const int b = k == parts ? (int)u.t1 : std::min<int>(u.t1, (u.t0 + (len * k + parts - 1) / parts + m - 1) / m * m);
+              if (b <= a) continue;
+              AppendUnit cu = u;
+              cu.role = kUnitCsa;
+              cu.t0 = (int16_t)a;
+              cu.t1 = (int16_t)b;
+              cu.in_row = u.in_row + (a - u.t0);
+              out.push_back(cu);
+              a = b;
+            }
+          }
+          *list = std::move(out);
+        }
+      }
+    }
     AppendParams* ap = new AppendParams();
     ap->pool = p->lay.pd;
     std::memcpy(ap->layers, p->lay.layers, sizeof(ap->layers));
@@ -1124,7 +1168,8 @@ int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_
         // copy CTAs for them
         ap->copy_slices = 0;
         for (int32_t k = 0; k < ap->n_units; ++k)
-          if (any_csa && ap->units[k].block_id >= 0 && ap->units[k].t0 >= (p->cfg.idx_per_token ? 1 : p->cfg.m))
+          if (any_csa && ap->units[k].role != kUnitCsa && ap->units[k].block_id >= 0 &&
+              ap->units[k].t0 >= (p->cfg.idx_per_token ? 1 : p->cfg.m))
             ap->copy_slices = kSealCopySlices;  // staged entries (or per-token keys) move into the block
         rc = p->launch(KVPOOL_KERNEL_APPEND, bytes, stream, [&](int* nk) { return launch_append(*ap, p->cfg.n_layers, stream, nk); });
         bytes = 0;

@@ -67,12 +67,18 @@ struct PoolDesc {
 // ---- append ---------------------------------------------------------------
 // One (request, block segment) touched by an append call: positions
 // seg*m' + t for t in [t0, t1).
+// A unit's work: all of it, or -- units of many tokens in a launch too small
+// to fill the GPU -- the HCA chain over all its tokens (plus the seal copies)
+// in one CTA and the CSA / indexer chains and window writes over a range of
+// whole CSA groups in each of several others.
+enum : int16_t { kUnitAll = 0, kUnitHca = 1, kUnitCsa = 2 };
+
 struct AppendUnit {
   int32_t slot;      // request slot
   int32_t seg;       // block index within the request
   int16_t t0, t1;    // token range inside the segment
   int16_t ring_from; // first t written to the window (t1 if none)
-  int16_t pad;
+  int16_t role;      // kUnitAll, or one part of a unit split over CTAs (kUnitHca / kUnitCsa)
   int32_t in_row;    // input row of the token at t0
   int32_t block_id;  // id the segment seals into in this call, or -1
   int32_t csa_slot;  // CSA plane slot of that block (its id without HiSparse)

@@ -84,6 +84,31 @@ def test_tiny_prefix_130_then_8_decode_steps():
         attend_both(o, g, 0, [r], [0], step, 64)
 
 
+@pytest.mark.parametrize("cache,idx_fp4,per_token", [(K.BF16, 0, 0), (K.FP8_E4M3, 0, 0), (K.FP8_E4M3, 1, 0),
+                                                    (K.BF16, 0, 1)])
+def test_long_units_split_over_ctas(cache, idx_fp4, per_token):
+    """Prefill chunks of one request, the launches too small to fill the
+    GPU: each long unit's HCA chain runs in one CTA and its CSA groups and
+    window tokens in several others.  130 tokens, then 2,000 (the first unit
+    starts inside a CSA group, the last ends inside one), then 2,048 more,
+    then decode steps; every stored entry, accumulator-derived entry and
+    window token bit-exact, attention within tolerance."""
+    w = dict(W.DECODE_BATCH, cache_dtype=cache, seed=28, idx_fp4=idx_fp4, idx_per_token=per_token)
+    o, g = make_pair(w, 2, 48, 40, 2, 256)
+    r = g.pool.alloc_request()
+    assert o.alloc_request()[1] == r
+    L = 0
+    for n in (130, 2000, 2048):
+        append_both(o, g, [r], [r], [L], [n])
+        L += n
+        compare_request_state(g, o, r)
+    for step in range(3):
+        append_both(o, g, [r], [r], [L], [1])
+        L += 1
+        attend_both(o, g, 0, [r], [r], step, 256)
+    compare_request_state(g, o, r)
+
+
 @pytest.mark.parametrize("cache,idx_fp4", [(K.BF16, 0), (K.FP8_E4M3, 0), (K.FP8_E4M3, 1), (K.BF16, 1)])
 def test_batched_ragged_appends_and_decode(cache, idx_fp4):
     """Decode-batch shapes (16 heads x 128, indexer 4 x 64) with ragged,
