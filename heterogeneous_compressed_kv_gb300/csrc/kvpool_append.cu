@@ -24,6 +24,13 @@ namespace {
 
 constexpr int kVpt = 8;  // consecutive values per thread
 
+// 16 bytes from a shared-memory address
+__device__ __forceinline__ uint4 lds16(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+
 template <int IN>
 struct InTraits;
 template <>
@@ -39,9 +46,7 @@ struct InTraits<KVPOOL_F32> {
     x[6] = __uint_as_float(r.b.z); x[7] = __uint_as_float(r.b.w);
   }
   __device__ static void load8(const uint8_t* p, float* x) { unpack(load(p), x); }
-  __device__ static void load8_shared(const uint8_t* p, float* x) {
-    unpack(Raw{*reinterpret_cast<const uint4*>(p), *reinterpret_cast<const uint4*>(p + 16)}, x);
-  }
+  __device__ static void load8_sa(uint32_t a, float* x) { unpack(Raw{lds16(a), lds16(a + 16)}, x); }
 };
 template <>
 struct InTraits<KVPOOL_BF16> {
@@ -57,7 +62,7 @@ struct InTraits<KVPOOL_BF16> {
     }
   }
   __device__ static void load8(const uint8_t* p, float* x) { unpack(load(p), x); }
-  __device__ static void load8_shared(const uint8_t* p, float* x) { unpack(*reinterpret_cast<const uint4*>(p), x); }
+  __device__ static void load8_sa(uint32_t a, float* x) { unpack(lds16(a), x); }
 };
 
 // Store 8 fp32 values (already scaled for fp8) as cache codes at dst.
@@ -73,10 +78,11 @@ __device__ __forceinline__ void store8<KVPOOL_F32>(uint8_t* dst, const float* x,
 }
 template <>
 __device__ __forceinline__ void store8<KVPOOL_BF16>(uint8_t* dst, const float* x, float) {
+  // two values per conversion (round to nearest even; the first operand goes
+  // to the high half)
   uint32_t w[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    w[i] = (uint32_t)f32_to_bf16_bits(x[2 * i]) | ((uint32_t)f32_to_bf16_bits(x[2 * i + 1]) << 16);
+  for (int i = 0; i < 4; ++i) asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w[i]) : "f"(x[2 * i + 1]), "f"(x[2 * i]));
   *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 template <>
@@ -259,6 +265,12 @@ __device__ bool staged_tokens(const AppendParams& P, const AppendUnit& u, int la
     }
     if (xb && lane == 0) bulk_g2s(dst + (int64_t)TS * (kb + vb), xin + (int64_t)j0 * xb, (uint32_t)(nt * xb), &full[s]);
   };
+  // the thread's values in a stage: shared-memory addresses of token 0 and
+  // the step from one token to the next
+  const uint32_t stage_sa = smem_addr(stages);
+  const uint32_t x_off = (uint32_t)(half == 0 ? (hv - k_lo) * isz : TS * kb + (hv - v_lo) * isz);
+  const uint32_t x_step = (uint32_t)(half == 0 ? kb : vb);
+  const uint32_t y_off = (uint32_t)(TS * (kb + vb) + xv0 * isz);
   if (tid < 32)
     for (int st = 0; st < n_st && st < kAppendStages; ++st) issue(st);
   for (int st = 0; st < n_st; ++st) {
@@ -270,15 +282,14 @@ __device__ bool staged_tokens(const AppendParams& P, const AppendUnit& u, int la
           mbar_wait(&full[k % kAppendStages], (k / kAppendStages) & 1, pd);
       return false;
     }
-    const uint8_t* src = stages + (int64_t)s * stage_bytes;
     const int nt = min(TS, n_tok - st * TS);
-    for (int j = 0; j < nt; ++j) {
+    uint32_t px = stage_sa + (uint32_t)(s * stage_bytes) + x_off, py = stage_sa + (uint32_t)(s * stage_bytes) + y_off;
+    int t = u.t0 + st * TS;
+    for (int j = 0; j < nt; ++j, px += x_step, py += (uint32_t)xb, ++t) {
       float x[kVpt], y[kVpt];
-      const uint8_t* px = half == 0 ? src + j * kb + (hv - k_lo) * isz
-                                    : src + (int64_t)TS * kb + j * vb + (hv - v_lo) * isz;
-      InTraits<IN>::load8_shared(px, x);
-      if (idx_thread) InTraits<IN>::load8_shared(src + (int64_t)TS * (kb + vb) + j * xb + xv0 * isz, y);
-      token(u.t0 + st * TS + j, x, y);
+      InTraits<IN>::load8_sa(px, x);
+      if (idx_thread) InTraits<IN>::load8_sa(py, y);
+      token(t, x, y);
     }
     __syncthreads();  // every thread is done with slot s
     if (tid < 32 && st + kAppendStages < n_st) issue(st + kAppendStages);
@@ -400,18 +411,23 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
   // a segment's tokens never wrap the ring: slot = (segment start mod n_win) + t.
   int tm = u.t0 % m, tq = u.t0 / m;
   int tk = u.t0 % pd.csa_per_block, tr = u.t0 / pd.csa_per_block;
+  // the gates of the current token: HCA by position, CSA / indexer by the
+  // position in the group (advanced with the counters)
+  const float* pa_h = a_hca + u.t0;
+  const float* pa_c = a_csa + tm;
+  const float* pa_x = a_idx + tm;
   const int64_t ring_base = seg_pos0 % pd.n_win;
 
   // the per-token work (window, compressor chains, completed entries); x: this
   // thread's kVpt input values of token t, y: its indexer values (idx threads)
   auto token = [&](int t, const float* x, const float* y) {
     if (do_hca) {
-      const float a = __ldg(a_hca + t);
+      const float a = __ldg(pa_h);
 #pragma unroll
       for (int j = 0; j < kVpt; ++j) acc_h[j] = __fmaf_rn(a, x[j], acc_h[j]);
     }
     if (do_csa) {
-      const float a = __ldg(a_csa + tm);
+      const float a = __ldg(pa_c);
 #pragma unroll
       for (int j = 0; j < kVpt; ++j) acc_c[j] = __fmaf_rn(a, x[j], acc_c[j]);
       if constexpr (PT) {
@@ -435,7 +451,7 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
           }
         }
       } else if (idx_thread) {
-        const float b = __ldg(a_idx + tm);
+        const float b = __ldg(pa_x);
 #pragma unroll
         for (int j = 0; j < kVpt; ++j) acc_x[j] = __fmaf_rn(b, y[j], acc_x[j]);
       }
@@ -459,13 +475,20 @@ __global__ void __launch_bounds__(512) append_kernel(const __grid_constant__ App
     }
     if (do_win && t >= u.ring_from)  // the token enters the SWA window
       write_entry<CACHE>(ring + (ring_base + t) * pd.entry_bytes, pd, v0, half, hv, x, sh);
+    ++pa_h;
+    ++pa_c;
+    ++pa_x;
     if (++tm == m) {
       tm = 0;
+      pa_c = a_csa;
+      pa_x = a_idx;
       ++tq;
     }
-    if (++tk == pd.csa_per_block) {
-      tk = 0;
-      ++tr;
+    if constexpr (PT) {
+      if (++tk == pd.csa_per_block) {
+        tk = 0;
+        ++tr;
+      }
     }
   };
 

@@ -228,30 +228,6 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
   const int n_st = max(0, seg_end - seg_begin);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  if (tid == 0) {
-    for (int s = 0; s < CW * ring; ++s) mbar_init(&full[s], 1);
-    mbar_fence_init();
-  }
-  for (int b = tid; b < kHistBins; b += blockDim.x) hist[b] = 0u;
-  // the fast chain needs the query exactly in the keys' 16-bit format
-  int exact = CACHE != KVPOOL_F32;
-  for (int v = tid; v < XD; v += blockDim.x) {
-    const int64_t row = (int64_t)(P.row0 + i) * XD + v;
-    const float qv = IN == KVPOOL_F32 ? reinterpret_cast<const float*>(P.q_idx)[row]
-                                      : bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(P.q_idx)[row]);
-    q_sh[v] = qv;
-    if (CACHE == KVPOOL_FP8_E4M3 || CACHE == KVPOOL_FP4_E2M1) {
-      const __half hq = __float2half_rn(qv);
-      qh_sh[v] = __half_as_ushort(hq);
-      exact &= __half2float(hq) == qv;
-    } else if (CACHE == KVPOOL_BF16) {
-      const uint16_t bq = f32_to_bf16_bits(qv);
-      qh_sh[v] = bq;
-      exact &= bf16_bits_to_f32(bq) == qv;
-    }
-  }
-  const bool fast = __syncthreads_and(exact) != 0;
-
   // this warp's blocks: st = warp + j * CW, j = 0 .. mine-1
   const int mine = warp < n_st ? (n_st - 1 - warp) / CW + 1 : 0;
   const int32_t* table = reinterpret_cast<const int32_t*>(pd.arena + pd.table) + (int64_t)R.slot * pd.max_bpr;
@@ -283,6 +259,14 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
   };
   uint64_t* my_full = full + warp * ring;
   uint8_t* my_slots = slots + (int64_t)warp * ring * stage_bytes;
+  // every warp initialises its own barriers and starts its first copies
+  // before the query is loaded (the copies need neither the query nor the
+  // other warps)
+  if (lane == 0) {
+    for (int s = 0; s < ring; ++s) mbar_init(&my_full[s], 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
   for (int jj = 0; jj < mine && jj < ring; ++jj) {
     const uint8_t* src = src_of(jj);
     if (lane == 0) {
@@ -290,6 +274,27 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
       bulk_g2s(my_slots + (int64_t)jj * stage_bytes, src, (uint32_t)stage_bytes, &my_full[jj]);
     }
   }
+
+  // the histogram and the query (its loads overlap the first copies)
+  for (int b = tid; b < kHistBins; b += blockDim.x) hist[b] = 0u;
+  // the fast chain needs the query exactly in the keys' 16-bit format
+  int exact = CACHE != KVPOOL_F32;
+  for (int v = tid; v < XD; v += blockDim.x) {
+    const int64_t row = (int64_t)(P.row0 + i) * XD + v;
+    const float qv = IN == KVPOOL_F32 ? reinterpret_cast<const float*>(P.q_idx)[row]
+                                      : bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(P.q_idx)[row]);
+    q_sh[v] = qv;
+    if (CACHE == KVPOOL_FP8_E4M3 || CACHE == KVPOOL_FP4_E2M1) {
+      const __half hq = __float2half_rn(qv);
+      qh_sh[v] = __half_as_ushort(hq);
+      exact &= __half2float(hq) == qv;
+    } else if (CACHE == KVPOOL_BF16) {
+      const uint16_t bq = f32_to_bf16_bits(qv);
+      qh_sh[v] = bq;
+      exact &= bf16_bits_to_f32(bq) == qv;
+    }
+  }
+  const bool fast = __syncthreads_and(exact) != 0;
 
   constexpr int V = IdxChunk<CACHE>::kVals;
   const int n_chunks = pd.idx_chunks;
