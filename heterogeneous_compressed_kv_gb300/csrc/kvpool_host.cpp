@@ -14,7 +14,9 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <memory>
 #include <new>
+#include <cstddef>
 #include <set>
 #include <string>
 #include <vector>
@@ -320,6 +322,10 @@ struct ProfileSlot {
 
 struct kvpool {
   kvpool_config cfg{};
+  // kernel parameter blocks, reused by every call (a call fills the header
+  // and the entries it launches with; nothing else is read)
+  std::unique_ptr<AppendParams> append_params;
+  std::unique_ptr<AttendParams> attend_params;
   std::vector<int32_t> kinds;
   uint32_t flags = 0;
   uint64_t fingerprint = 0;  // of the config, for prefix images
@@ -1126,7 +1132,9 @@ int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_
         }
       }
     }
-    AppendParams* ap = new AppendParams();
+    if (!p->append_params) p->append_params.reset(new AppendParams());
+    AppendParams* ap = p->append_params.get();
+    std::memset(static_cast<void*>(ap), 0, offsetof(AppendParams, units));
     ap->pool = p->lay.pd;
     std::memcpy(ap->layers, p->lay.layers, sizeof(ap->layers));
     ap->k = d_k;
@@ -1175,7 +1183,6 @@ int kvpool_append(kvpool_t* p, int32_t n, const int32_t* h_req_ids, const int32_
         bytes = 0;
       }
     }
-    delete ap;
   }
   if (rc != 0) {  // undo the reservation: nothing changes on error
     for (auto& v : new_ids)
@@ -1219,12 +1226,14 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
   const int CB = pd.csa_per_block;
   const int EPS = pd.idx_per_token ? CB / p->cfg.m : CB;  // CSA entries per score segment (a block, or a run of tokens)
   const int max_split_len = attend_max_split_len();
-  AttendParams* ap = new AttendParams();
+  if (!p->attend_params) p->attend_params.reset(new AttendParams());
+  AttendParams* ap = p->attend_params.get();
   int rc = 0;
   p->epoch += 1;  // this call's epoch (HiSparse activity)
   for (int g0 = 0; g0 < n && rc == 0; g0 += kMaxAttendReqs) {
     const int gn = std::min(kMaxAttendReqs, n - g0);
     AttendParams& P = *ap;
+    std::memset(static_cast<void*>(ap), 0, offsetof(AttendParams, reqs));
     P.pool = pd;
     P.layer = Ld;
     P.epoch = p->epoch;
@@ -1375,7 +1384,6 @@ int kvpool_decode_attend(kvpool_t* p, int32_t layer, int32_t n, const int32_t* h
     }
     if (rc == 0) rc = p->launch(KVPOOL_KERNEL_COMBINE, out_bytes, stream, [&](int* nk) { return launch_combine(P, stream, nk); });
   }
-  delete ap;
   if (rc != 0) p->epoch -= 1;
   if (rc == -1) return KVPOOL_ERR_INVALID_ARG;
   if (rc != 0) return p->cuda_fail((cudaError_t)rc, "decode_attend launch");
