@@ -1120,9 +1120,20 @@ def main():
     top_k = w["top_k"]
     slot_ids, one = np.asarray(slots, np.int32), np.ones(B, np.int32)  # converted once, not every call
 
+    # every step's input views made once, outside the timed loops (a tensor
+    # view costs about a microsecond of host time per input)
+    views = {}
+
     def step(t, k, v, x, q, qi):
-        pool.append(slot_ids, one, k[t], v[t], x[t], stream=sp)
-        pool.decode_attend(0, slot_ids, q[t], qi[t], top_k, out, None, stream=sp)
+        key = (id(k), t)
+        vw = views.get(key)
+        if vw is None:
+            vw = views[key] = (k[t], v[t], x[t], q[t], qi[t])
+        pool.append(slot_ids, one, vw[0], vw[1], vw[2], stream=sp)
+        pool.decode_attend(0, slot_ids, vw[3], vw[4], top_k, out, None, stream=sp)
+
+    for t in range(W_ + K_):
+        views[(id(sk), t)] = (sk[t], sv[t], sx[t], sq[t], sqi[t])
 
     # warm-up, every kernel kind recorded: the dominant kernel is the one with
     # the most algorithmic bytes
