@@ -109,6 +109,30 @@ def test_long_units_split_over_ctas(cache, idx_fp4, per_token):
     compare_request_state(g, o, r)
 
 
+@pytest.mark.parametrize("cache", [K.BF16, K.FP8_E4M3])
+def test_split_units_with_mixed_layer_kinds(cache):
+    """Split units across layers of every kind ([SWA-only, CSA, HCA, CSA],
+    window 512): one request's appends of 600 and 640 tokens are few units
+    for 4 layers x 2 slices, so each long unit runs as an HCA CTA and CSA
+    CTAs; in a layer without HCA the HCA CTA has nothing but the seal copies,
+    in one without CSA the CSA CTAs only write the window."""
+    w = dict(W.MIXED_SERVING, n_win=512, seed=29, cache_dtype=cache)
+    o, g = make_pair(w, 2, 40, 16, 2, 256)
+    r = g.pool.alloc_request()
+    assert o.alloc_request()[1] == r
+    L = 0
+    for n in (130, 600, 640):
+        append_both(o, g, [r], [r], [L], [n])
+        L += n
+        compare_request_state(g, o, r)
+    for step in range(2):
+        append_both(o, g, [r], [r], [L], [1])
+        L += 1
+        for layer in range(4):
+            attend_both(o, g, layer, [r], [r], step, 256)
+    compare_request_state(g, o, r)
+
+
 @pytest.mark.parametrize("cache,idx_fp4", [(K.BF16, 0), (K.FP8_E4M3, 0), (K.FP8_E4M3, 1), (K.BF16, 1)])
 def test_batched_ragged_appends_and_decode(cache, idx_fp4):
     """Decode-batch shapes (16 heads x 128, indexer 4 x 64) with ragged,
