@@ -239,6 +239,7 @@ __device__ bool staged_tokens(const AppendParams& P, const AppendUnit& u, int la
     mbar_fence_init();
   }
   __syncthreads();
+  const uint64_t l2pol = l2_evict_first_policy();  // the input rows are read once
   auto issue = [&](int st) {  // warp 0: stage st into slot st % kAppendStages
     const int s = st % kAppendStages;
     const int j0 = st * TS, nt = min(TS, n_tok - j0);
@@ -250,20 +251,20 @@ __device__ bool staged_tokens(const AppendParams& P, const AppendUnit& u, int la
     __syncwarp();
     if (kb) {
       if (kb == HD * isz) {
-        if (lane == 0) bulk_g2s(dst, kin + (int64_t)j0 * kb, (uint32_t)(nt * kb), &full[s]);
+        if (lane == 0) bulk_g2s_stream(dst, kin + (int64_t)j0 * kb, (uint32_t)(nt * kb), &full[s], l2pol);
       } else {
-        for (int j = lane; j < nt; j += 32) bulk_g2s(dst + j * kb, kin + (int64_t)(j0 + j) * HD * isz, kb, &full[s]);
+        for (int j = lane; j < nt; j += 32) bulk_g2s_stream(dst + j * kb, kin + (int64_t)(j0 + j) * HD * isz, kb, &full[s], l2pol);
       }
     }
     if (vb) {
       uint8_t* dv = dst + (int64_t)TS * kb;
       if (vb == HD * isz) {
-        if (lane == 0) bulk_g2s(dv, vin + (int64_t)j0 * vb, (uint32_t)(nt * vb), &full[s]);
+        if (lane == 0) bulk_g2s_stream(dv, vin + (int64_t)j0 * vb, (uint32_t)(nt * vb), &full[s], l2pol);
       } else {
-        for (int j = lane; j < nt; j += 32) bulk_g2s(dv + j * vb, vin + (int64_t)(j0 + j) * HD * isz, vb, &full[s]);
+        for (int j = lane; j < nt; j += 32) bulk_g2s_stream(dv + j * vb, vin + (int64_t)(j0 + j) * HD * isz, vb, &full[s], l2pol);
       }
     }
-    if (xb && lane == 0) bulk_g2s(dst + (int64_t)TS * (kb + vb), xin + (int64_t)j0 * xb, (uint32_t)(nt * xb), &full[s]);
+    if (xb && lane == 0) bulk_g2s_stream(dst + (int64_t)TS * (kb + vb), xin + (int64_t)j0 * xb, (uint32_t)(nt * xb), &full[s], l2pol);
   };
   // the thread's values in a stage: shared-memory addresses of token 0 and
   // the step from one token to the next

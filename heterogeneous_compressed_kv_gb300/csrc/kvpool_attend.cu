@@ -446,6 +446,7 @@ __global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __gr
     // ---- producer warp: source addresses 32 at a time, one batch ahead ----
     const int lane = tid & 31;
     const uint64_t hbase = reinterpret_cast<uint64_t>(pd.host_pool), hbytes = (uint64_t)pd.host_pool_bytes;
+    const uint64_t l2pol = l2_evict_first_policy();
     uint64_t cur = lane < cnt ? source_addr<HS>(P, i, R, v0 + lane) : 0;
     uint64_t nxt = 32 + lane < cnt ? source_addr<HS>(P, i, R, v0 + 32 + lane) : 0;
     int batch = 0;
@@ -506,8 +507,8 @@ __global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __gr
       if (start) {
         const uint32_t later = (starts | hmask) & ~((2u << lane) - 1u);
         const int end = later ? __ffs(later) - 1 : ne;
-        bulk_g2s(stage_mem + (size_t)s * stage_bytes + (size_t)lane * ES, reinterpret_cast<const void*>(a),
-                 (uint32_t)(end - lane) * ES, &full[s]);
+        bulk_g2s_stream(stage_mem + (size_t)s * stage_bytes + (size_t)lane * ES, reinterpret_cast<const void*>(a),
+                        (uint32_t)(end - lane) * ES, &full[s], l2pol);
       }
       if (((e0 + ne) >> 5) != batch) {  // the next stage starts in the next batch
         ++batch;

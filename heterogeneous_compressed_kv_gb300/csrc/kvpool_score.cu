@@ -257,6 +257,7 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
     const int run = PT ? (seg_begin + warp + jj * CW) % m : 0;
     return pd.arena + L.idx_pool + (int64_t)bid * L.idx_stride + (int64_t)run * L.idx_run;
   };
+  const uint64_t l2pol = l2_evict_first_policy();
   uint64_t* my_full = full + warp * ring;
   uint8_t* my_slots = slots + (int64_t)warp * ring * stage_bytes;
   // every warp initialises its own barriers and starts its first copies
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
     const uint8_t* src = src_of(jj);
     if (lane == 0) {
       mbar_arrive_expect_tx(&my_full[jj], (uint32_t)stage_bytes);
-      bulk_g2s(my_slots + (int64_t)jj * stage_bytes, src, (uint32_t)stage_bytes, &my_full[jj]);
+      bulk_g2s_stream(my_slots + (int64_t)jj * stage_bytes, src, (uint32_t)stage_bytes, &my_full[jj], l2pol);
     }
   }
 
@@ -329,7 +330,7 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
         if (lane == 0) {
           fence_proxy_async();  // the warp's reads of the slot come before the copy that overwrites it
           mbar_arrive_expect_tx(&my_full[slot], (uint32_t)stage_bytes);
-          bulk_g2s(my_slots + (int64_t)slot * stage_bytes, src, (uint32_t)stage_bytes, &my_full[slot]);
+          bulk_g2s_stream(my_slots + (int64_t)slot * stage_bytes, src, (uint32_t)stage_bytes, &my_full[slot], l2pol);
         }
       }
       if (valid && PT) {  // per head: chain, times the token's scale, into the gate chain
@@ -401,7 +402,7 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
         if (lane == 0) {
           fence_proxy_async();  // the warp's reads of the slot come before the copy that overwrites it
           mbar_arrive_expect_tx(&my_full[slot], (uint32_t)stage_bytes);
-          bulk_g2s(my_slots + (int64_t)slot * stage_bytes, src, (uint32_t)stage_bytes, &my_full[slot]);
+          bulk_g2s_stream(my_slots + (int64_t)slot * stage_bytes, src, (uint32_t)stage_bytes, &my_full[slot], l2pol);
         }
       }
     }
