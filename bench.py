@@ -91,10 +91,37 @@ def gates(w):
 # ---------------------------------------------------------------------------
 # CPU oracle leg (cpu_baseline and --impl reference); no CUDA in here
 # ---------------------------------------------------------------------------
+# The cpu_baseline processes are spawned before the first CUDA call but hold
+# until the GPU measurements are done (the gate), so that they do not compete
+# with the host thread that enqueues the GPU work.
+_GATE = None
+
+
+def _gate_init(gate):
+    global _GATE
+    _GATE = gate
+
+
+def _gate_wait():
+    if _GATE is not None:
+        _GATE.wait()
+
+
+def oracle_pool(n_workers, gated):
+    """A spawned pool of n_workers processes, and the gate that releases them
+    (already open when not gated)."""
+    ctx = mp.get_context("spawn")
+    gate = ctx.Event()
+    if not gated:
+        gate.set()
+    return ctx.Pool(n_workers, initializer=_gate_init, initargs=(gate,)), gate
+
+
 def _oracle_worker(args):
     """Prefill one workload request into the oracle (untimed), then time
     `steps` decode steps (append 1 token + decode_attend) of it."""
     name, idx_fp4, wid, steps, warm, idx_per_token = args
+    _gate_wait()
     sys.path.insert(0, ROOT)
     import numpy as np
     import oracle as O
@@ -146,12 +173,12 @@ def _oracle_worker(args):
     return time.perf_counter() - t0, t_setup
 
 
-def start_oracle(name, n_workers, steps, warm, idx_fp4=False, idx_per_token=False):
-    """Spawned before any CUDA call: one oracle process per sampled request."""
-    ctx = mp.get_context("spawn")
-    pool = ctx.Pool(n_workers)
+def start_oracle(name, n_workers, steps, warm, idx_fp4=False, idx_per_token=False, gated=False):
+    """Spawned before any CUDA call: one oracle process per sampled request
+    (held by the gate until it is opened when gated)."""
+    pool, gate = oracle_pool(n_workers, gated)
     res = pool.map_async(_oracle_worker, [(name, idx_fp4, i, steps, warm, idx_per_token) for i in range(n_workers)])
-    return pool, res
+    return pool, res, gate
 
 
 def oracle_workers(w):
@@ -171,7 +198,7 @@ def run_reference(args):
         run_reference_protocol(args, w)
         return
     n = oracle_workers(w)
-    pool, res = start_oracle(args.config, n, args.steps, args.warmup, args.idx_fp4, args.idx_per_token)
+    pool, res, _ = start_oracle(args.config, n, args.steps, args.warmup, args.idx_fp4, args.idx_per_token)
     out = res.get()
     pool.close()
     t = max(o[0] for o in out)
@@ -490,6 +517,7 @@ def _c3_oracle_worker(args):
     then `steps` timed runs of the protocol (each: 4 requests allocated, 16 +
     8 appends and 3 prefix shares, all freed)."""
     steps, warm = args
+    _gate_wait()
     sys.path.insert(0, ROOT)
     import numpy as np
     w = workload("chunked_prefill")
@@ -537,9 +565,8 @@ def run_chunked_prefill(args):
     K_, W_ = args.steps, args.warmup
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        ctx = mp.get_context("spawn")
-        cpool = ctx.Pool(1)
-        cpu = (cpool, cpool.map_async(_c3_oracle_worker, [(1, 0)]))
+        cpool, gate = oracle_pool(1, gated=True)
+        cpu = (cpool, cpool.map_async(_c3_oracle_worker, [(1, 0)]), gate)
 
     import torch
     import torch.distributed as dist
@@ -663,6 +690,8 @@ def run_chunked_prefill(args):
             break
     pool.check_device(sp)
     e2e_ms = statistics.median(e2e_windows)
+    if cpu is not None:  # the GPU measurements are done: release the oracle baseline
+        cpu[-1].set()
     if rank != 0:
         return
     peaks, peak_kind = measured_peaks()
@@ -693,7 +722,7 @@ def run_chunked_prefill(args):
                                    ms_per_step_max=max(windows) / K_),
                 gpu_launches=round(a_n / n_steps_timed * K_), clocks=clk)
     if cpu is not None:
-        cpool, cres = cpu
+        cpool, cres, _ = cpu
         try:
             t = cres.get(timeout=900)[0]
             line["cpu_baseline"] = dict(value=tokens_per_step / t, unit="tokens/s", cores=1, kind="oracle",
@@ -714,6 +743,7 @@ def _c5_oracle_worker(args):
     prefilled untimed, then `steps` timed decode steps (append one token on
     every layer, attention on each of the 4 layers)."""
     idx, steps = args
+    _gate_wait()
     sys.path.insert(0, ROOT)
     import numpy as np
     from heterogeneous_compressed_kv_gb300 import gen
@@ -761,9 +791,8 @@ def run_mixed_serving(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n_w = max(1, min(8, (os.cpu_count() or 2) - 1))
-        ctx = mp.get_context("spawn")
-        cpool = ctx.Pool(n_w)
-        cpu = (n_w, cpool, cpool.map_async(_c5_oracle_worker, [(i, args.cpu_steps) for i in range(n_w)]))
+        cpool, gate = oracle_pool(n_w, gated=True)
+        cpu = (n_w, cpool, cpool.map_async(_c5_oracle_worker, [(i, args.cpu_steps) for i in range(n_w)]), gate)
 
     import torch
     import torch.distributed as dist
@@ -912,6 +941,8 @@ def run_mixed_serving(args):
                 break
     pool.profile_enable(False)
     pool.check_device(sp)
+    if cpu is not None:  # the GPU measurements are done: release the oracle baseline
+        cpu[-1].set()
     if phase == "timed":
         clk = clocks.stop()
     if rank != 0:
@@ -947,7 +978,7 @@ def run_mixed_serving(args):
                 gpu_launches=round(sum(dec_launches) / len(dec_launches) * steps_each), setup_s=t_setup,
                 clocks=clk)
     if cpu is not None:
-        n_w, cpool, cres = cpu
+        n_w, cpool, cres, _ = cpu
         try:
             t = max(cres.get(timeout=900))
             line["cpu_baseline"] = dict(value=n_w * args.cpu_steps / t, unit="tokens/s", cores=n_w, kind="oracle",
@@ -1013,7 +1044,7 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = (oracle_workers(w),) + start_oracle(args.config, oracle_workers(w), args.cpu_steps, 1, args.idx_fp4,
-                                                         args.idx_per_token)
+                                                         args.idx_per_token, gated=True)
 
     import numpy as np
     import torch
@@ -1252,6 +1283,8 @@ def main():
         if sum(e2e_windows) >= 1e3 * MIN_TIMED_S / 2 or len(e2e_windows) >= max_windows:
             break
     e2e_ms = statistics.median(e2e_windows)
+    if cpu is not None:  # the GPU measurements are done: release the oracle baseline
+        cpu[-1].set()
     h2d = hin[0].numel() * hin.element_size()
     d2h = hout[0].numel() * 4
 
@@ -1300,7 +1333,7 @@ def main():
                                    ms_per_step_max=max(windows) / K_),
                 gpu_launches=launches, setup_s=t_setup, clocks=clk, host_enqueue_us_per_step=host_us)
     if cpu is not None:
-        n_w, cpool, cres = cpu
+        n_w, cpool, cres, _ = cpu
         try:
             res = cres.get(timeout=900)
             t = max(r[0] for r in res)
