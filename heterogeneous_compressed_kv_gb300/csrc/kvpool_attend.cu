@@ -107,6 +107,14 @@ __device__ __forceinline__ uint64_t source_addr(const AttendParams& P, int i, co
 }
 
 // ---- shared-memory loads and number formats of the consumer loop ----------
+// A bf16 consumer thread (TPH threads per head of TPH * 16 dims) owns dims
+// [8r, 8r + 8) and [TPH * 8 + 8r, TPH * 8 + 8r + 8) of its head, r = its rank
+// in the head: the second run starts TPH * 16 bytes after the first.  (16
+// contiguous dims per thread put neighbouring threads 32 bytes apart: two
+// shared-memory wavefronts per quarter-warp instead of one.)  Other caches
+// keep 16 contiguous dims per thread.
+template <int TPH>
+constexpr int kRun2Bytes = TPH * 16;
 __device__ __forceinline__ uint4 lds128(uint32_t a) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
@@ -148,7 +156,9 @@ __device__ __forceinline__ float f16hi_to_f32(uint32_t w) { return __half2float(
 // Dot product of the query's 16 dims with 16 key values at shared address a.
 // FAST: the query is exact in the mixed-precision operand type (f16 for an
 // fp8 cache, bf16 for a bf16 cache) and qw holds it as pairs; otherwise qf.
-template <int CACHE, bool FAST>
+// bf16: the thread's dims are two runs of 8, the second B2 bytes after the
+// first (so that neighbouring threads read neighbouring 16-byte words).
+template <int CACHE, bool FAST, int B2>
 __device__ __forceinline__ float dot16(uint32_t a, const uint32_t* qw, const float* qf) {
   float c0 = 0.0f, c1 = 0.0f;
   if constexpr (CACHE == KVPOOL_FP8_E4M3) {
@@ -169,7 +179,7 @@ __device__ __forceinline__ float dot16(uint32_t a, const uint32_t* qw, const flo
       }
     }
   } else if constexpr (CACHE == KVPOOL_BF16) {
-    const uint4 r0 = lds128(a), r1 = lds128(a + 16);
+    const uint4 r0 = lds128(a), r1 = lds128(a + B2);
     const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -193,10 +203,10 @@ __device__ __forceinline__ float dot16(uint32_t a, const uint32_t* qw, const flo
   return c0 + c1;
 }
 
-// o[0..16) += weight * (16 values at shared address a).  fp8: the weight is
-// p times the entry's V scale rounded to f16, so its products with the f16
-// values are exact; bf16 / fp32: p in fp32.
-template <int CACHE>
+// o[0..16) += weight * (16 values at shared address a; bf16: two runs of 8,
+// B2 bytes apart).  fp8: the weight is p times the entry's V scale rounded to
+// f16, so its products with the f16 values are exact; bf16 / fp32: p in fp32.
+template <int CACHE, int B2>
 __device__ __forceinline__ void acc16(uint32_t a, float wgt, float* o) {
   if constexpr (CACHE == KVPOOL_FP8_E4M3) {
     const uint32_t h = __half_as_ushort(__float2half_rn(wgt));
@@ -211,7 +221,7 @@ __device__ __forceinline__ void acc16(uint32_t a, float wgt, float* o) {
       fma_f16x2(hi, h2, o[4 * i + 2], o[4 * i + 3]);
     }
   } else if constexpr (CACHE == KVPOOL_BF16) {
-    const uint4 r0 = lds128(a), r1 = lds128(a + 16);
+    const uint4 r0 = lds128(a), r1 = lds128(a + B2);
     const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -240,7 +250,7 @@ __device__ __forceinline__ void update(uint32_t a0, uint32_t ES, uint32_t koff, 
 #pragma unroll
   for (int u = 0; u < NU; ++u) {
     const uint32_t a = a0 + u * ES;
-    float d = dot16<CACHE, FAST>(a + koff, qw, qf);
+    float d = dot16<CACHE, FAST, kRun2Bytes<TPH>>(a + koff, qw, qf);
 #pragma unroll
     for (int off = TPH / 2; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
     if constexpr (CACHE == KVPOOL_FP8_E4M3) {
@@ -263,7 +273,7 @@ __device__ __forceinline__ void update(uint32_t a0, uint32_t ES, uint32_t koff, 
   for (int u = 0; u < NU; ++u) {
     const float p = ex2(sc[u] - mx);
     l_run += p;
-    acc16<CACHE>(a0 + u * ES + voff, p * vsc[u], o);
+    acc16<CACHE, kRun2Bytes<TPH>>(a0 + u * ES + voff, p * vsc[u], o);
   }
   m_run = mx;
 }
@@ -369,7 +379,7 @@ __device__ __forceinline__ void update_tc(uint32_t a0, uint32_t ES, uint32_t aro
   for (int e = 0; e < NU; ++e) {
     const float p = ex2(sc[e] - mx);
     l_run += p;
-    acc16<KVPOOL_FP8_E4M3>(a0 + e * ES + voff, p * vsc[e], o);
+    acc16<KVPOOL_FP8_E4M3, 0>(a0 + e * ES + voff, p * vsc[e], o);
   }
   m_run = mx;
 }
@@ -526,14 +536,18 @@ __global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __gr
     return;
   }
 
-  // ---- consumers: head h, dims [dd0, dd0 + 16) ----
+  // ---- consumers: head h, dims [dA, dA + 8) and [dB, dB + 8) ----
+  // (bf16: two runs TPH * 8 dims apart; otherwise dB = dA + 8)
+  constexpr bool kRuns = CACHE == KVPOOL_BF16;
   const int lane = tid & 31;
   const bool act = tid < n_act;
   const int h = act ? tid / TPH : 0;
-  const int dd0 = act ? (tid % TPH) * 16 : 0;
+  const int rk = act ? tid % TPH : 0;
+  const int dA = kRuns ? 8 * rk : 16 * rk;
+  const int dB = kRuns ? TPH * 8 + 8 * rk : dA + 8;
   // scores in the log2 domain: dot(q, k) * log2(e) / sqrt(d) (* fp8 K scale)
   const float qscale = 1.4426950408889634f * rsqrtf((float)pd.head_dim);
-  const uint32_t koff = (uint32_t)((h * pd.head_dim + dd0) * pd.vs);
+  const uint32_t koff = (uint32_t)((h * pd.head_dim + dA) * pd.vs);
   const uint32_t voff = (uint32_t)(HD * pd.vs) + koff;
   const uint32_t soff = (uint32_t)(2 * HD * pd.vs);
   const uint32_t stage0 = smem_addr(stage_mem);
@@ -542,19 +556,20 @@ __global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __gr
   float qf[16];
   uint32_t qw[8];
   int exact = 1;
-  const uint8_t* qrow =
-      reinterpret_cast<const uint8_t*>(P.q) + ((int64_t)(P.row0 + i) * HD + h * pd.head_dim + dd0) * pd.isz;
+  const uint8_t* qrow = reinterpret_cast<const uint8_t*>(P.q) + ((int64_t)(P.row0 + i) * HD + h * pd.head_dim) * pd.isz;
+  const uint8_t* qa = qrow + dA * pd.isz;
+  const uint8_t* qb = qrow + dB * pd.isz;
   if constexpr (IN == KVPOOL_F32) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const uint4 r = *reinterpret_cast<const uint4*>(qrow + 16 * c);
+      const uint4 r = *reinterpret_cast<const uint4*>((c < 2 ? qa : qb) + 16 * (c & 1));
       qf[4 * c] = __uint_as_float(r.x);
       qf[4 * c + 1] = __uint_as_float(r.y);
       qf[4 * c + 2] = __uint_as_float(r.z);
       qf[4 * c + 3] = __uint_as_float(r.w);
     }
   } else {
-    const uint4 r0 = *reinterpret_cast<const uint4*>(qrow), r1 = *reinterpret_cast<const uint4*>(qrow + 16);
+    const uint4 r0 = *reinterpret_cast<const uint4*>(qa), r1 = *reinterpret_cast<const uint4*>(qb);
     const uint32_t wq[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -608,11 +623,12 @@ __global__ void __launch_bounds__(kAttendThreadsMax, 2) attend_kernel(const __gr
   }
   if (act) {
     const int64_t pslot = R.part_base + (part ? R.n_split0 : 0) + split;
-    float* po = P.part_o + pslot * HD + h * pd.head_dim + dd0;
+    float* po = P.part_o + pslot * HD + h * pd.head_dim;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      reinterpret_cast<float4*>(po)[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-    if (dd0 == 0) {
+      reinterpret_cast<float4*>(po + (j < 2 ? dA : dB))[j & 1] =
+          make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+    if (rk == 0) {
       float* ml = P.part_ml + (pslot * pd.heads + h) * 2;
       ml[0] = m_run;
       ml[1] = l_run;
