@@ -11,8 +11,16 @@ Prints one JSON line (rank 0).  With torchrun (N > 1) every rank serves its
 own 8 requests on its own GPU (weak scaling, no data-path collective; the
 process group only carries the timing barrier and the max over ranks).
 
-  python bench.py [--steps K] [--warmup W] [--config long_context|decode_batch]
+  python bench.py [--steps K] [--warmup W]
+                  [--config long_context|decode_batch|chunked_prefill|mixed_serving]
+                  [--idx-fp4 | --idx-per-token] [--hisparse F] [--prefix-image]
   python bench.py --impl reference   # the CPU oracle on the same workload
+
+The CPU oracle's bounded sample (cpu_baseline) runs in processes spawned
+before the first CUDA call that start working only once the GPU timing is
+done.  Decode workloads whose timed window would grow the mean context by
+more than 1% (the decode batch) rebuild their requests at the post-warm-up
+lengths, untimed, before every window.
 """
 from __future__ import annotations
 
