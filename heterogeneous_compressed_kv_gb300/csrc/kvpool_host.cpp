@@ -126,7 +126,6 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
     if (kind_has_csa(k) && (!c->gate_csa || !c->gate_idx)) return "gate_csa and gate_idx are required";
     if (kind_has_hca(k) && !c->gate_hca) return "gate_hca is required";
   }
-  (void)any_csa;
 
   Layout L{};
   PoolDesc& pd = L.pd;
@@ -238,6 +237,14 @@ std::string plan_layout(const kvpool_config* c, Layout* out) {
   L.part_ml = cur;
   cur = round_up(cur + 8LL * kMaxSplits * c->heads, 256);
   L.total = cur;
+  // the kernels' shared-memory plans must fit one CTA of an sm_100-family SM
+  if (any_csa) {
+    int sb = 0, ring = 0, so = 0, nw = 0;
+    size_t smem = 0;
+    score_stage_plan(pd, &sb, &ring, &so, &nw, &smem);
+    if (smem > kMaxDynSmem) return "indexer blocks too large for the score kernel's shared memory";
+  }
+  if (attend_smem_bytes(pd) > kMaxDynSmem) return "entries too large for the attention kernel's shared memory";
   *out = L;
   return "";
 }

@@ -10,6 +10,7 @@
 namespace kvp {
 
 constexpr int kMaxLayers = 16;
+constexpr size_t kMaxDynSmem = 232448;  // dynamic shared memory one CTA may opt into (227 KiB)
 constexpr int kHistBins = 2048;          // radix digit of the top-k select (11 bits)
 constexpr int kMaxKeyCtasPerReq = 256;   // select chunks per request (1M candidates)
 constexpr int kSelectKeysPerCta = 4096;  // keys handled by one select CTA
@@ -209,6 +210,10 @@ int launch_share(const ShareParams& p, int n_layers, void* stream, int* n_kernel
 int launch_image(const ImageParams& p, void* stream, int* n_kernels);
 int launch_wait_selftest(const PoolDesc& pd, void* stream);
 int launch_score(const AttendParams& p, void* stream, int* n_kernels);
+// the score kernel's shared-memory plan: one block's indexer bytes per slot,
+// slots per warp, the slots' offset, warps per CTA and the dynamic bytes
+int score_stage_plan(const PoolDesc& pd, int* stage_bytes, int* ring, int* stage_off, int* warps, size_t* smem);
+size_t attend_smem_bytes(const PoolDesc& pd);
 // alone: nothing else runs on the GPU beside the select, so it may take one
 // thread-block cluster per large request (a cluster waits for 16 SMs with room
 // at once, which attention CTAs running beside it would hold)

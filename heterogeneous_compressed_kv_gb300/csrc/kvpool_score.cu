@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
   const PoolDesc& pd = P.pool;
   const LayerDesc& L = P.layer;
   const int XD = pd.XD;
-  constexpr int CW = ScoreShape<CACHE>::kWarps;
+  const int CW = blockDim.x >> 5;  // warps (fewer than kWarps when a block's keys are large)
   constexpr int KCH = ScoreShape<CACHE>::kRegChunks;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm);
   float* q_sh = reinterpret_cast<float*>(sm + 8 * kScoreMaxSlots);
@@ -433,32 +433,34 @@ __global__ void __launch_bounds__(ScoreShape<CACHE>::kWarps * 32, 1) score_kerne
 }  // namespace
 
 // Score CTAs of a launch, and the shared-memory plan of the score kernel.
-int score_stage_plan(const PoolDesc& pd, int* stage_bytes, int* ring, int* stage_off, size_t* smem) {
+int score_stage_plan(const PoolDesc& pd, int* stage_bytes, int* ring, int* stage_off, int* warps, size_t* smem) {
   // one block's indexer part: keys, then (fp8) scales; the same size as the
   // indexer plane's stride
   *stage_bytes = pd.csa_per_block * (int)pd.idx_entry_bytes +
                  (pd.idx_dtype == KVPOOL_FP8_E4M3 || pd.idx_dtype == KVPOOL_FP4_E2M1
                       ? (2 * pd.csa_per_block + 15) / 16 * 16
                       : 0);
-  const int warps = score_warps(pd.idx_dtype);
-  *ring = std::max(1, std::min(kScoreMaxRing, kScoreStageBudget / (warps * *stage_bytes)));
+  // fewer warps when even one slot per warp would overrun the budget (large
+  // fp32 or bf16 indexer entries)
+  *warps = std::max(1, std::min(score_warps(pd.idx_dtype), kScoreStageBudget / *stage_bytes));
+  *ring = std::max(1, std::min(kScoreMaxRing, kScoreStageBudget / (*warps * *stage_bytes)));
   *stage_off = (8 * kScoreMaxSlots + 6 * pd.XD + 4 * kHistBins + 127) / 128 * 128;
-  *smem = (size_t)*stage_off + (size_t)warps * *ring * *stage_bytes;
+  *smem = (size_t)*stage_off + (size_t)*warps * *ring * *stage_bytes;
   return 0;
 }
 
 template <int IN, int CACHE, bool PT>
 static int launch_score_t(const AttendParams& p, cudaStream_t s) {
-  int sb, ns, so;
+  int sb, ns, so, nw;
   size_t smem;
-  score_stage_plan(p.pool, &sb, &ns, &so, &smem);
+  score_stage_plan(p.pool, &sb, &ns, &so, &nw, &smem);
   auto k = score_kernel<IN, CACHE, PT>;
   static size_t set = 0;
   if (set < smem) {
     cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     set = smem;
   }
-  launch_kernel(true, k, dim3(p.total_score_ctas), dim3(ScoreShape<CACHE>::kWarps * 32), smem, s, p, sb, ns, so);
+  launch_kernel(true, k, dim3(p.total_score_ctas), dim3(nw * 32), smem, s, p, sb, ns, so);
   return 0;
 }
 

@@ -67,6 +67,19 @@ def test_invalid_configs_are_refused(bad):
         K.Pool(cfg)
 
 
+def test_indexer_blocks_must_fit_the_score_kernels_shared_memory():
+    """One block's indexer keys are staged whole in shared memory: 32 fp32
+    entries of 32 x 64 values (256 KiB) cannot be, so the config is refused;
+    the same keys in bf16 (128 KiB) take one score warp and are accepted, as
+    are 4 x 64 fp32 keys (32 KiB per block, four warps)."""
+    big = dict(heads=16, head_dim=64, idx_heads=32, idx_dim=64)
+    assert K.required_bytes(cfg_of(base_workload(**big))) == 0
+    with pytest.raises(K.KvpoolError):
+        K.Pool(cfg_of(base_workload(**big)))
+    assert K.required_bytes(cfg_of(base_workload(cache_dtype=K.BF16, in_dtype=K.BF16, **big))) > 0
+    assert K.required_bytes(cfg_of(base_workload(heads=16, head_dim=128, idx_heads=4, idx_dim=64))) > 0
+
+
 def test_fp4_indexer_layout():
     w = base_workload(cache_dtype=K.BF16, in_dtype=K.BF16, heads=16, head_dim=128, idx_heads=4, idx_dim=64)
     p = K.Pool(cfg_of(w, idx_fp4=1))

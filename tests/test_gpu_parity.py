@@ -161,6 +161,29 @@ def test_batched_ragged_appends_and_decode(cache, idx_fp4):
         compare_request_state(g, o, s)
 
 
+@pytest.mark.parametrize("in_dtype,cache,heads,head_dim", [
+    (K.F32, K.BF16, 8, 64), (K.BF16, K.BF16, 8, 64), (K.F32, K.BF16, 16, 128),
+    (K.F32, K.FP8_E4M3, 8, 64), (K.BF16, K.FP8_E4M3, 8, 64), (K.F32, K.F32, 16, 128)])
+def test_attention_consumer_layouts(in_dtype, cache, heads, head_dim):
+    """Every mapping of the attention consumers' dims: bf16 caches take two
+    runs of 8 dims half a head apart, fp8 and fp32 caches 16 contiguous dims;
+    64- and 128-dim heads (4 and 8 threads per head); fp32 and bf16 inputs."""
+    w = dict(W.DECODE_BATCH, in_dtype=in_dtype, cache_dtype=cache, heads=heads, head_dim=head_dim, seed=33)
+    o, g = make_pair(w, 3, 32, 16, 3, 64)
+    slots = [g.pool.alloc_request() for _ in range(3)]
+    assert [o.alloc_request()[1] for _ in range(3)] == slots
+    L = [0] * 3
+    for counts in ([300, 77, 513], [200, 400, 3]):
+        append_both(o, g, slots, slots, L, counts)
+        L = [a + b for a, b in zip(L, counts)]
+    for step in range(2):
+        append_both(o, g, slots, slots, L, [1] * 3)
+        L = [a + 1 for a in L]
+        attend_both(o, g, 0, slots, slots, step, 64)
+    for sl in slots:
+        compare_request_state(g, o, sl)
+
+
 def test_prefix_sharing_with_recomputed_window():
     """Chunked-prefill shapes: request 0 appends 2048-token chunks; requests
     1 and 2 share its first 1024 tokens (8 sealed blocks) with the window
