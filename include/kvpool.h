@@ -139,9 +139,9 @@ size_t kvpool_required_bytes(const kvpool_config* cfg);
 /* Create a pool in the caller's device arena.  Validates cfg ([P1] s2.2:
  * m | m'; [P3] s2.2: the window is a whole number of blocks; heads * head_dim
  * a multiple of 256 up to 4096; idx_heads * idx_dim a multiple of 16 up to
- * 2048 and at most 2 * heads * head_dim; one block's indexer keys and four
- * entries' K/V small enough for the score and attention kernels to stage in
- * one CTA's 227 KiB of shared memory), computes the
+ * 2048 and at most 2 * heads * head_dim; one block's indexer keys (score
+ * kernel) and four stages of entries (attention kernel) small enough to stage
+ * in one CTA's 227 KiB of shared memory), computes the
  * gates' softmax on the host and uploads them, and clears the device error
  * word, in stream order on `stream`.  d_arena must stay allocated until
  * kvpool_destroy.  With KVPOOL_FLAG_NO_DEVICE, d_arena must be NULL and the
