@@ -54,11 +54,14 @@ __device__ __forceinline__ uint8_t f32x2_to_e2m1x2(float a, float b) {
   return (uint8_t)r;
 }
 
-// one byte of two e2m1 codes -> f16x2 (the low nibble in the low half); exact
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint8_t two) {
-  uint32_t h;
-  asm("{.reg .b8 t, z;\n\tmov.b16 {t, z}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;}" : "=r"(h) : "h"((uint16_t)two));
-  return h;
+// the four bytes of w (eight e2m1 codes, the low byte first) -> four f16x2
+// words; the bytes are taken apart inside one asm block
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t w, uint32_t* h) {
+  asm("{.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
 }
 
 // fp4 scale of a vector with absolute maximum amax: bf16(amax / 6), 1 if 0

@@ -80,9 +80,11 @@ struct IdxChunk<KVPOOL_FP4_E2M1> {  // 32 e2m1 values, element 2j in the low nib
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
+      uint32_t hw[4];
+      e2m1x8_to_f16x2x4(w[i], hw);
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const uint32_t h = e2m1x2_to_f16x2((uint8_t)(w[i] >> (8 * b)));
+        const uint32_t h = hw[b];
         const int v = 8 * i + 2 * b;
         acc = __fmaf_rn(q[v], __half2float(__ushort_as_half((uint16_t)(h & 0xFFFFu))), acc);
         acc = __fmaf_rn(q[v + 1], __half2float(__ushort_as_half((uint16_t)(h >> 16))), acc);
@@ -151,8 +153,10 @@ struct IdxChunkFast<KVPOOL_FP4_E2M1> {  // 32 keys per chunk, q as 32 f16
     for (int i = 0; i < 4; ++i) {
       const uint4 qv = *reinterpret_cast<const uint4*>(qh + 4 * i);
       const uint32_t q[4] = {qv.x, qv.y, qv.z, qv.w};
+      uint32_t h[4];
+      e2m1x8_to_f16x2x4(w[i], h);
 #pragma unroll
-      for (int b = 0; b < 4; ++b) acc = chain2_f16(e2m1x2_to_f16x2((uint8_t)(w[i] >> (8 * b))), q[b], acc);
+      for (int b = 0; b < 4; ++b) acc = chain2_f16(h[b], q[b], acc);
     }
     return acc;
   }
