@@ -343,7 +343,7 @@ int kvpool_decode_attend(kvpool_t* pool, int32_t layer, int32_t n, const int32_t
  * only when that many SMs have room at once, so work running beside the call
  * delays it); smaller rows by 4096-column chunks or one CTA per row.  The first call on a device looks up that
  * device's address of the array and the cluster shape (for the current
- * device) and should come before any stream capture.
+ * device).
  * Every call shares the array and clears what must start at zero; calls that
  * overlap on the GPU (other streams, other host threads) race.  Errors:
  * INVALID_ARG, CUDA; kernel-side errors land in the array's error word, which
