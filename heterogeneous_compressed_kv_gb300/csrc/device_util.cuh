@@ -1,5 +1,5 @@
 // device_util.cuh -- small device helpers for the kvpool kernels: number
-// formats, bounded mbarrier waits, 1-D bulk (TMA) copies, reductions.
+// formats, bounded mbarrier waits, 1-D bulk (TMA) copies and L2 hints, loads.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -226,16 +226,6 @@ __device__ __forceinline__ void bulk_g2s_stream(void* dst, const void* src, uint
       : "memory");
 }
 
-// 1-D bulk copy global -> shared, completing `bytes` of transaction on bar.
-// dst, src 16-byte aligned; bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // streaming loads
 // ---------------------------------------------------------------------------
@@ -250,28 +240,6 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 __device__ __forceinline__ uint4 ld_nc16(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-  return r;
-}
-
-// ---------------------------------------------------------------------------
-// reductions
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-// block-wide max over blockDim.x threads (multiple of 32); scratch >= 32 floats
-__device__ __forceinline__ float block_max(float v, float* scratch) {
-  v = warp_max(v);
-  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  __syncthreads();
-  if (l == 0) scratch[w] = v;
-  __syncthreads();
-  const int nw = blockDim.x >> 5;
-  float r = (l < nw) ? scratch[l] : 0.0f;
-  r = warp_max(r);
   return r;
 }
 
